@@ -1,0 +1,495 @@
+"""Benchmark of the HERALD hot path on one GB300 (or N independent replicas).
+
+One step = one block of one layer of the 32K Qwen2.5-7B-like workload
+(N=1, Hq=28, Hkv=4, d=128, ctx 32768, B=32, T=8, C=4096, K=1024, sink 64,
+local 256): herald_select (merged-query scan + top-C + stage-2 refine +
+top-K with sink/local) -> herald_gather into one of two pool buffers ->
+T x herald_denoise_attn -> herald_append_kv.  Metric: block tokens/s =
+N*B / (time per step).
+
+Timing: the step is captured once per cache copy into a CUDA graph and the
+graphs are replayed; the K cache and V cache are rotated over enough copies
+that the data touched between two uses of a copy exceeds L2 (cold-L2
+inputs).  A second, traced replay brackets every kernel with graph event
+nodes to time the dominant kernel for the roofline.  e2e: the same step
+through direct C-ABI calls with the step's inputs copied from pinned host
+buffers and its outputs read back, copies inside the timed region.
+`--impl reference`: the fp64 CPU oracle timed on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "block tokens/s (select + T sparse-attn steps) at 32K–128K; scan HBM GB/s"
+L2_BYTES = 129 * 2 ** 20
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clock, power and clock-event reasons of one GPU through
+    NVML (ctypes, the driver's library) every `period` seconds."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+    def __init__(self, torch_dev: int, period: float = 0.002):
+        self.period = period
+        self.samples: list[tuple[float, int, int, float]] = []
+        self.ok = False
+        self.max_mhz = None
+        self._stop = threading.Event()
+        try:
+            import torch
+            p = torch.cuda.get_device_properties(torch_dev)
+            bus = f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0".encode()
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if self.nv.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(self.h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = int(mx.value)
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _one(self):
+        clk, rs, pw = ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
+        self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk))
+        self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rs))
+        self.nv.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(pw))
+        self.samples.append((time.perf_counter(), int(clk.value), int(rs.value), pw.value / 1000.0))
+
+    def _run(self):
+        while not self._stop.is_set():
+            self._one()
+            time.sleep(self.period)
+
+    def start(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+
+    def stop(self):
+        if self.ok:
+            self._stop.set()
+            self.t.join()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [],
+                    "samples": 0, "source": "unavailable"}
+        win = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not win:  # region shorter than the period: nearest samples around it
+            win = sorted(self.samples, key=lambda s: abs(s[0] - 0.5 * (t0 + t1)))[:3]
+        reasons = set()
+        for s in win:
+            for bit, name in self.REASONS.items():
+                if s[2] & bit:
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median([s[1] for s in win])), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(win),
+                "power_w_max": max(s[3] for s in win), "source": "nvml"}
+
+
+# --------------------------------------------------------------------------- workload
+def workload():
+    from block_diffusion_sparse_gb300.workloads import QWEN_32K
+    return QWEN_32K
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_diffusion_sparse_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, src_hash: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if
+    the summary was taken on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        d = json.load(open(p))
+    except Exception:
+        return None
+    e = d.get("kernels", {}).get(kernel)
+    if not e or d.get("source_hash") != src_hash:
+        return None
+    return e.get("dram_bytes_per_launch_full_workload")
+
+
+class Bench:
+    def __init__(self, w, rank: int):
+        import torch
+        from block_diffusion_sparse_gb300 import herald as H
+        from block_diffusion_sparse_gb300 import synth
+        self.torch, self.H, self.w = torch, H, w
+        self.x = synth.make_layer(w)
+        x = self.x
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+        self.d = H.dims_of(w)
+        self.P = w.P
+        cache_bytes = 2 * x["k_cache"].nbytes
+        self.n_rot = max(2, int(np.ceil(2 * L2_BYTES / cache_bytes)) + 1)
+        k0, v0 = dev(x["k_cache"]), dev(x["v_cache"])
+        self.k = [k0] + [k0.clone() for _ in range(self.n_rot - 1)]
+        self.v = [v0] + [v0.clone() for _ in range(self.n_rot - 1)]
+        self.q_merge = dev(x["q_merge"])
+        self.q_steps = dev(x["q_steps"])
+        self.bk, self.bv = dev(x["block_k"]), dev(x["block_v"])
+        self.ctx = torch.from_numpy(x["ctx"]).cuda()
+        NG = (w.N, w.Hkv)
+        self.ws_bytes = H.herald_workspace_size(self.d, w.C, self.P)
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device="cuda")
+        self.idx = torch.zeros((*NG, self.P), dtype=torch.int32, device="cuda")
+        self.n_sel = torch.zeros(NG, dtype=torch.int32, device="cuda")
+        self.pool_k = [torch.zeros((*NG, self.P, w.d), dtype=torch.int16, device="cuda")
+                       for _ in range(2)]
+        self.pool_v = [torch.zeros_like(self.pool_k[0]) for _ in range(2)]
+        self.out = torch.zeros((w.T, w.N, w.B, w.Hq, w.d), dtype=torch.int16, device="cuda")
+
+    def step(self, r: int, stream=None, q_merge=None, q_steps=None, bk=None, bv=None):
+        """One block: select, gather, T attention steps, append."""
+        H, w = self.H, self.w
+        st = stream if stream is not None else self.torch.cuda.current_stream()
+        qm = self.q_merge if q_merge is None else q_merge
+        qs = self.q_steps if q_steps is None else q_steps
+        bk = self.bk if bk is None else bk
+        bv = self.bv if bv is None else bv
+        k, v = self.k[r], self.v[r]
+        pk, pv = self.pool_k[r % 2], self.pool_v[r % 2]
+        H.herald_select(self.d, qm, qs[0], k, self.ctx, w.C, w.K, w.S, w.W, self.P, self.idx,
+                        self.n_sel, self.ws, self.ws_bytes, st)
+        H.herald_gather(self.d, self.idx, self.n_sel, self.P, k, v, pk, pv, st)
+        for t in range(w.T):
+            H.herald_denoise_attn(self.d, qs[t], pk, pv, self.n_sel, self.P, bk[t], bv[t],
+                                  self.out[t], 0.0, self.ws, self.ws_bytes, st)
+        H.herald_append_kv(self.d, bk[w.T - 1], bv[w.T - 1], self.ctx, k, v, False, st)
+
+    def capture(self, traced: bool = False):
+        torch = self.torch
+        graphs, traces = [], []
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for r in range(self.n_rot):     # eager warm-up: kernel attributes, caches
+                self.step(r)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        for r in range(self.n_rot):
+            g = torch.cuda.CUDAGraph()
+            if traced:
+                tr = self.H.Trace(capacity=64, external=True)
+                with torch.cuda.graph(g):
+                    with tr:
+                        self.step(r)
+                traces.append(tr)
+            else:
+                with torch.cuda.graph(g):
+                    self.step(r)
+            graphs.append(g)
+        torch.cuda.synchronize()
+        return graphs, traces
+
+
+def algorithmic_work(w, n_sel: np.ndarray) -> dict:
+    """Algorithmic bytes / FLOPs per launch of each kernel (the design doc lists
+    the definitions)."""
+    NG = w.N * w.Hkv
+    R = w.R
+    ns = n_sel.astype(np.int64)
+    keys = ns + w.B
+    return {
+        "scan_kernel": {"bound": "hbm", "bytes": NG * w.L * w.d * 2},
+        "attn_kernel": {"bound": "hbm",
+                        "bytes": int(ns.sum()) * w.d * 2 * 2 + NG * w.B * w.d * 2 * 2
+                        + 2 * w.N * w.B * w.Hq * w.d * 2,
+                        "flops": int((4 * R * keys * w.d).sum())},
+        "gather_kernel": {"bound": "hbm", "bytes": int(ns.sum()) * w.d * 2 * 2 * 2},
+        "refine_pass1_kernel": {"bound": "tensor", "flops": 2 * R * w.C * w.d * NG},
+        "refine_pass2_kernel": {"bound": "tensor", "flops": 2 * R * w.C * w.d * NG},
+    }
+
+
+def peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
+            "fallback"
+
+
+# --------------------------------------------------------------------------- oracle
+def oracle_block(w, xf, T_sample=None):
+    """One block through the fp64 oracle: select, then T attention steps."""
+    import oracle
+    T = w.T if T_sample is None else T_sample
+    r = oracle.select(xf["q_merge"], xf["q_steps"][0], xf["k_cache"], xf["ctx"], w.C, w.K, w.S,
+                      w.W, w.P)
+    for t in range(T):
+        oracle.sparse_attn(xf["q_steps"][t], xf["k_cache"], xf["v_cache"], r["idx"], r["n_sel"],
+                           xf["block_k"][t], xf["block_v"][t])
+    return r
+
+
+def oracle_inputs(w):
+    from block_diffusion_sparse_gb300 import synth
+    x = synth.make_layer(w)
+    f = synth.bf16_to_f64
+    return {k: (f(v) if isinstance(v, np.ndarray) and v.dtype == np.uint16 else v)
+            for k, v in x.items()}
+
+
+def cpu_baseline(w, budget_s: float = 12.0) -> dict:
+    import oracle
+    xf = oracle_inputs(w)
+    oracle.num_threads()
+    t0 = time.perf_counter()
+    oracle_block(w, xf)                       # first block (also loads the library)
+    t_first = time.perf_counter() - t0
+    n = max(1, min(10, int(budget_s / max(t_first, 1e-3))))
+    t0 = time.perf_counter()
+    for _ in range(n):
+        oracle_block(w, xf)
+    dt = (time.perf_counter() - t0) / n
+    return {"value": w.N * w.B / dt, "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{n} full blocks of the same workload (select + gather + T={w.T} "
+                      f"attention steps), fp64 C + OpenMP, inputs resident in host RAM",
+            "s_per_block": dt}
+
+
+# --------------------------------------------------------------------------- arms
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    w = workload()
+    xf = oracle_inputs(w)
+    for _ in range(args.warmup):
+        oracle_block(w, xf)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_block(w, xf)
+    dt = (time.perf_counter() - t0) / args.steps
+    v = w.N * w.B / dt
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
+                       "ctx": w.L, "B": w.B, "T": w.T, "C": w.C, "K": w.K, "sink": w.S,
+                       "local": w.W},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": oracle.num_threads(),
+                             "kind": "oracle",
+                             "sample": "each step = one full block (select + gather + T "
+                                       "attention steps) of the workload"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+    w = workload()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    dev_idx = torch.cuda.current_device()
+    b = Bench(w, rank)
+    graphs, _ = b.capture(traced=False)
+    nrot = b.n_rot
+    clocks = ClockSampler(dev_idx)
+    clocks.start()
+    st = torch.cuda.current_stream()
+    for i in range(args.warmup):
+        graphs[i % nrot].replay()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    e0.record(st)
+    for i in range(args.steps):
+        graphs[(args.warmup + i) % nrot].replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    if dist:
+        dist.barrier()
+    clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    if dist:
+        tt = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    value = world * w.N * w.B / (ms * 1e-3)
+    err = b.H.herald_workspace_error(b.ws)
+
+    # traced replay: per-kernel durations (graph event nodes) for the roofline
+    tgraphs, traces = b.capture(traced=True)
+    per = {}
+    reps = max(3, min(args.steps, 50))
+    for i in range(reps):
+        r = i % nrot
+        tgraphs[r].replay()
+        torch.cuda.synchronize()
+        for name, dt in traces[r].durations_ms():
+            per.setdefault(name, []).append(dt)
+    launches_per_step = traces[0].count
+    tot = {k: float(np.sum(v)) / reps for k, v in per.items()}     # ms per step
+    avg = {k: float(np.mean(v)) for k, v in per.items()}           # ms per launch
+    ns = b.n_sel.cpu().numpy()
+    work = algorithmic_work(w, ns)
+    pk, pk_kind = peaks()
+    dominant = max(tot, key=tot.get)
+    src_hash = kernel_source_hash()
+
+    def roof(name):
+        wk = work.get(name)
+        if not wk:
+            return None
+        d_s = avg[name] * 1e-3
+        if wk["bound"] == "hbm":
+            ach = wk["bytes"] / d_s / 1e9
+            peak = pk["hbm_gbs"]
+            unit = "GB/s"
+        else:
+            ach = wk["flops"] / d_s / 1e12
+            peak = pk["bf16_tflops"]
+            unit = "TFLOP/s"
+        return {"bound": wk["bound"], "achieved": ach, "peak": peak, "unit": unit,
+                "frac": ach / peak, "traffic": ncu_traffic(name, src_hash),
+                "kernel": name, "launch_us": avg[name] * 1e3,
+                "algorithmic_bytes" if wk["bound"] == "hbm" else "algorithmic_flops":
+                    wk["bytes"] if wk["bound"] == "hbm" else wk["flops"],
+                "peak_source": f"{pk_kind} (MEASURED_PEAKS.json)" if pk_kind == "measured"
+                else "fallback"}
+
+    roofline = roof(dominant) or roof("attn_kernel")
+    scan = roof("scan_kernel")
+
+    # end to end through the C ABI with host buffers
+    e2e = run_e2e(b, args, dist)
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
+                       "ctx": w.L, "B": w.B, "T": w.T, "C": w.C, "K": w.K, "sink": w.S,
+                       "local": w.W, "parallelism": f"replicas x{world}",
+                       "l2": f"cold: K/V cache rotated over {nrot} copies "
+                             f"({nrot * 2 * b.x['k_cache'].nbytes / 2**20:.0f} MiB > L2)",
+                       "timing": "CUDA-graph replay of whole steps, CUDA events"},
+            "roofline": roofline,
+            "scan": {"achieved_gbs": scan["achieved"] if scan else None,
+                     "frac": scan["frac"] if scan else None,
+                     "launch_us": scan["launch_us"] if scan else None},
+            "kernels_ms_per_step": {k: round(v, 5) for k, v in sorted(tot.items(),
+                                                                      key=lambda kv: -kv[1])},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks.summary(t0, t1), "e2e": e2e,
+            "device_error_word": err, "source_hash": src_hash}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(b, args, dist):
+    """Step inputs from pinned host memory -> device, the step through the C
+    ABI (no graph), outputs back to pinned host memory; all inside the timed
+    region."""
+    torch = b.torch
+    w = b.w
+    hq_m = b.q_merge.cpu().pin_memory()
+    hq_s = b.q_steps.cpu().pin_memory()
+    hbk, hbv = b.bk.cpu().pin_memory(), b.bv.cpu().pin_memory()
+    o_out = torch.empty(b.out.shape, dtype=b.out.dtype).pin_memory()
+    o_idx = torch.empty(b.idx.shape, dtype=b.idx.dtype).pin_memory()
+    o_ns = torch.empty(b.n_sel.shape, dtype=b.n_sel.dtype).pin_memory()
+    dq_m, dq_s = torch.empty_like(b.q_merge), torch.empty_like(b.q_steps)
+    dbk, dbv = torch.empty_like(b.bk), torch.empty_like(b.bv)
+    h2d = sum(t.numel() * t.element_size() for t in (hq_m, hq_s, hbk, hbv))
+    d2h = sum(t.numel() * t.element_size() for t in (o_out, o_idx, o_ns))
+
+    def one(i):
+        dq_m.copy_(hq_m, non_blocking=True)
+        dq_s.copy_(hq_s, non_blocking=True)
+        dbk.copy_(hbk, non_blocking=True)
+        dbv.copy_(hbv, non_blocking=True)
+        b.step(i % b.n_rot, q_merge=dq_m, q_steps=dq_s, bk=dbk, bv=dbv)
+        o_out.copy_(b.out, non_blocking=True)
+        o_idx.copy_(b.idx, non_blocking=True)
+        o_ns.copy_(b.n_sel, non_blocking=True)
+
+    for i in range(args.warmup):
+        one(i)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for i in range(args.steps):
+        one(i)
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    if dist:
+        tt = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    world = dist.get_world_size() if dist else 1
+    return {"value": world * w.N * w.B / (ms * 1e-3), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": ms, "path": "direct C-ABI calls (no graph), pinned host buffers"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        if args.impl == "ours":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        tdist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+        dist = tdist
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, dist)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

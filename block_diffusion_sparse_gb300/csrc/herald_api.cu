@@ -1,0 +1,435 @@
+// herald_api.cu -- the extern "C" entry points of libherald.so: argument
+// validation, workspace carving, TMA descriptor encoding, and the kernel
+// launch sequence of each call.  No call allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <vector>
+
+#include "../../include/herald.h"
+#include "internal.cuh"
+
+using namespace herald;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+herald_status fail(herald_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+herald_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(HERALD_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+#define HERALD_TRY_CUDA(expr, where)          \
+  do {                                        \
+    cudaError_t e_ = (expr);                  \
+    if (e_ != cudaSuccess) return cuda_fail(e_, where); \
+  } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define HERALD_CHECK_PTR(p)                                                          \
+  do {                                                                               \
+    if ((p) == nullptr) return fail(HERALD_ERR_INVALID_ARG, "%s is NULL", #p);       \
+    if (!aligned16(p)) return fail(HERALD_ERR_INVALID_ARG, "%s is not 16-byte aligned", #p); \
+  } while (0)
+
+herald_status check_dims(const herald_dims& d) {
+  if (d.N < 1 || d.Hq < 1 || d.Hkv < 1 || d.B < 1 || d.L_max < 1)
+    return fail(HERALD_ERR_INVALID_ARG, "dims must be positive (N=%d Hq=%d Hkv=%d B=%d L_max=%d)",
+                d.N, d.Hq, d.Hkv, d.B, d.L_max);
+  if (d.Hq % d.Hkv != 0)
+    return fail(HERALD_ERR_UNSUPPORTED_SHAPE, "Hq=%d is not a multiple of Hkv=%d", d.Hq, d.Hkv);
+  const int G = d.Hq / d.Hkv;
+  if (G > 8) return fail(HERALD_ERR_UNSUPPORTED_SHAPE, "GQA group size %d > 8", G);
+  if (d.d != 64 && d.d != 128)
+    return fail(HERALD_ERR_UNSUPPORTED_SHAPE, "head dim %d not in {64, 128}", d.d);
+  if (d.B * G > 256)
+    return fail(HERALD_ERR_UNSUPPORTED_SHAPE, "B*G = %d > 256 query rows per KV head", d.B * G);
+  if ((long long)d.N * d.Hkv * d.L_max >= (1ll << 31))
+    return fail(HERALD_ERR_UNSUPPORTED_SHAPE, "N*Hkv*L_max too large");
+  if ((long long)d.N * d.B * d.Hq >= (1ll << 31))
+    return fail(HERALD_ERR_UNSUPPORTED_SHAPE, "N*B*Hq too large");
+  return HERALD_OK;
+}
+
+herald_status check_c(int C) {
+  if (C < 1 || C > kMaxC)
+    return fail(HERALD_ERR_UNSUPPORTED_SHAPE, "C=%d outside [1, %d]", C, kMaxC);
+  return HERALD_OK;
+}
+
+herald_status check_ws(const herald_dims& dm, int C, int P_max, void* ws, size_t ws_bytes,
+                       WsLayout* out) {
+  HERALD_CHECK_PTR(ws);
+  const WsLayout w = ws_layout(dm, C, P_max);
+  if (ws_bytes < w.total)
+    return fail(HERALD_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", ws_bytes,
+                w.total);
+  *out = w;
+  return HERALD_OK;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+// ---- device properties, cached per device
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// ---- TMA descriptor encoding through the driver entry point
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D view [N*Hkv*L_max rows][d] of the key cache; box 64 columns x 64 rows,
+// 128-byte swizzle (the scan's shared-memory layout).
+herald_status encode_kcache_map(const herald_dims& dm, const uint16_t* k_cache, CUtensorMap* map) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(HERALD_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  const cuuint64_t dims[2] = {cuuint64_t(dm.d), cuuint64_t(dm.N) * dm.Hkv * dm.L_max};
+  const cuuint64_t strides[1] = {cuuint64_t(dm.d) * 2};
+  const cuuint32_t box[2] = {64, cuuint32_t(kScanTileKeys)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(k_cache),
+                        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(HERALD_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+  return HERALD_OK;
+}
+
+// Device memory is streamed by TMA; mapped host (or managed) memory by
+// plain 16-byte copies.
+bool is_device_memory(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice;
+}
+
+herald_status run_stage1(const herald_dims& dm, const uint16_t* q_merge, const uint16_t* k_cache,
+                         const int32_t* ctx_len, int C, int32_t* cand, int32_t* n_cand, void* ws,
+                         const WsLayout& w, cudaStream_t st) {
+  const bool tma = is_device_memory(k_cache);
+  CUtensorMap map;
+  if (tma) {
+    herald_status s = encode_kcache_map(dm, k_cache, &map);
+    if (s != HERALD_OK) return s;
+  }
+  uint32_t* err = at<uint32_t>(ws, w.err);
+  float* qbar = at<float>(ws, w.qbar);
+  float* logits = at<float>(ws, w.logits);
+  float2* part1 = at<float2>(ws, w.part1);
+  float* s1 = at<float>(ws, w.s1);
+  uint32_t* hist = at<uint32_t>(ws, w.hist);
+  const int nsm = sm_count();
+  HERALD_TRY_CUDA(launch_merge_query(dm, q_merge, qbar, hist, st), "merge_query launch");
+  HERALD_TRY_CUDA(launch_scan(dm, tma ? &map : nullptr, k_cache, tma, qbar, ctx_len, logits, part1,
+                              w, err, nsm, st),
+                  "scan launch");
+  HERALD_TRY_CUDA(launch_s1_hist(dm, logits, part1, ctx_len, s1, hist, w, nsm, st),
+                  "s1_hist launch");
+  HERALD_TRY_CUDA(launch_topc(dm, s1, hist, ctx_len, C, cand, n_cand, w, st), "topc launch");
+  return HERALD_OK;
+}
+
+herald_status run_stage2(const herald_dims& dm, const uint16_t* q_block, const uint16_t* k_cache,
+                         const int32_t* ctx_len, const int32_t* cand, const int32_t* n_cand,
+                         int C, int K, int sink, int local, int P_max, int32_t* idx,
+                         int32_t* n_sel, void* ws, const WsLayout& w, cudaStream_t st) {
+  uint32_t* err = at<uint32_t>(ws, w.err);
+  HERALD_TRY_CUDA(launch_refine(dm, q_block, k_cache, cand, n_cand, C, at<float2>(ws, w.rpart),
+                                at<float>(ws, w.s2), w, err, st),
+                  "refine launch");
+  HERALD_TRY_CUDA(launch_topk_union(dm, ctx_len, cand, n_cand, at<float>(ws, w.s2), C, K, sink,
+                                    local, P_max, idx, n_sel, st),
+                  "topk_union launch");
+  return HERALD_OK;
+}
+
+herald_status check_budget(int C, int K, int sink, int local, int P_max) {
+  if (K < 0 || sink < 0 || local < 0)
+    return fail(HERALD_ERR_INVALID_ARG, "K=%d sink=%d local=%d must be >= 0", K, sink, local);
+  if (K > C) return fail(HERALD_ERR_INVALID_ARG, "K=%d > C=%d", K, C);
+  if ((long long)K + sink + local > P_max)
+    return fail(HERALD_ERR_INVALID_ARG, "P_max=%d < K+sink+local=%lld", P_max,
+                (long long)K + sink + local);
+  return HERALD_OK;
+}
+
+herald_status check_pmax(const herald_dims& dm, int P_max) {
+  if (P_max < 1) return fail(HERALD_ERR_INVALID_ARG, "P_max=%d must be >= 1", P_max);
+  if ((long long)dm.N * dm.Hkv * P_max >= (1ll << 31))
+    return fail(HERALD_ERR_UNSUPPORTED_SHAPE, "N*Hkv*P_max too large");
+  return HERALD_OK;
+}
+
+#define HERALD_RET_IF(x)              \
+  do {                                \
+    herald_status s_ = (x);           \
+    if (s_ != HERALD_OK) return s_;   \
+  } while (0)
+
+// ---- kernel tracing state (per host thread)
+struct TraceState {
+  cudaEvent_t* events = nullptr;
+  int capacity = 0;
+  int count = 0;
+  bool external = false;
+  bool in_kernel = false;
+  std::vector<const char*> names;
+};
+thread_local TraceState g_trace;
+
+}  // namespace
+
+namespace herald {
+
+void trace_before(cudaStream_t st, const char* name) {
+  TraceState& t = g_trace;
+  t.in_kernel = false;
+  if (!t.events || t.count >= t.capacity) return;
+  t.names[t.count] = name;
+  if (t.external)
+    cudaEventRecordWithFlags(t.events[2 * t.count], st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(t.events[2 * t.count], st);
+  t.in_kernel = true;
+}
+
+void trace_after(cudaStream_t st) {
+  TraceState& t = g_trace;
+  if (!t.in_kernel) return;
+  if (t.external)
+    cudaEventRecordWithFlags(t.events[2 * t.count + 1], st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(t.events[2 * t.count + 1], st);
+  t.in_kernel = false;
+  ++t.count;
+}
+
+}  // namespace herald
+
+extern "C" {
+
+herald_status herald_trace_begin(void** events, int capacity, int external) {
+  if (!events || capacity < 1) return fail(HERALD_ERR_INVALID_ARG, "trace needs >= 1 event pair");
+  g_trace.events = reinterpret_cast<cudaEvent_t*>(events);
+  g_trace.capacity = capacity;
+  g_trace.count = 0;
+  g_trace.external = external != 0;
+  g_trace.in_kernel = false;
+  g_trace.names.assign(size_t(capacity), nullptr);
+  return HERALD_OK;
+}
+
+int herald_trace_end(void) {
+  const int n = g_trace.count;
+  g_trace.events = nullptr;
+  return n;
+}
+
+const char* herald_trace_name(int i) {
+  if (i < 0 || i >= int(g_trace.names.size()) || !g_trace.names[size_t(i)]) return "";
+  return g_trace.names[size_t(i)];
+}
+
+size_t herald_workspace_size(herald_dims dims, int C, int P_max) {
+  if (check_dims(dims) != HERALD_OK || check_c(C) != HERALD_OK || P_max < 1) return 0;
+  return ws_layout(dims, C, P_max).total;
+}
+
+const char* herald_status_string(herald_status s) {
+  switch (s) {
+    case HERALD_OK: return "ok";
+    case HERALD_ERR_INVALID_ARG: return "invalid argument";
+    case HERALD_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case HERALD_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case HERALD_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+const char* herald_last_error(void) { return g_err; }
+
+herald_status herald_workspace_error(void* ws, void* stream, uint32_t* code) {
+  HERALD_CHECK_PTR(ws);
+  if (!code) return fail(HERALD_ERR_INVALID_ARG, "code is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  HERALD_TRY_CUDA(cudaStreamSynchronize(st), "stream synchronize");
+  uint32_t v = 0;
+  HERALD_TRY_CUDA(cudaMemcpy(&v, ws, sizeof v, cudaMemcpyDeviceToHost), "read error word");
+  *code = v;
+  if (v) HERALD_TRY_CUDA(cudaMemsetAsync(ws, 0, sizeof v, st), "clear error word");
+  return HERALD_OK;
+}
+
+herald_status herald_select_stage1(herald_dims dims, const uint16_t* q_merge,
+                                   const uint16_t* k_cache, const int32_t* ctx_len, int C,
+                                   int32_t* cand, int32_t* n_cand, void* ws, size_t ws_bytes,
+                                   void* stream) {
+  g_err[0] = 0;
+  HERALD_RET_IF(check_dims(dims));
+  HERALD_RET_IF(check_c(C));
+  HERALD_CHECK_PTR(q_merge);
+  HERALD_CHECK_PTR(k_cache);
+  HERALD_CHECK_PTR(ctx_len);
+  HERALD_CHECK_PTR(cand);
+  HERALD_CHECK_PTR(n_cand);
+  WsLayout w;
+  HERALD_RET_IF(check_ws(dims, C, 1, ws, ws_bytes, &w));
+  return run_stage1(dims, q_merge, k_cache, ctx_len, C, cand, n_cand, ws, w,
+                    static_cast<cudaStream_t>(stream));
+}
+
+herald_status herald_select_stage2(herald_dims dims, const uint16_t* q_block,
+                                   const uint16_t* k_cache, const int32_t* ctx_len,
+                                   const int32_t* cand, const int32_t* n_cand, int C, int K,
+                                   int sink, int local, int P_max, int32_t* idx, int32_t* n_sel,
+                                   void* ws, size_t ws_bytes, void* stream) {
+  g_err[0] = 0;
+  HERALD_RET_IF(check_dims(dims));
+  HERALD_RET_IF(check_c(C));
+  HERALD_RET_IF(check_pmax(dims, P_max));
+  HERALD_RET_IF(check_budget(C, K, sink, local, P_max));
+  HERALD_CHECK_PTR(q_block);
+  HERALD_CHECK_PTR(k_cache);
+  HERALD_CHECK_PTR(ctx_len);
+  HERALD_CHECK_PTR(cand);
+  HERALD_CHECK_PTR(n_cand);
+  HERALD_CHECK_PTR(idx);
+  HERALD_CHECK_PTR(n_sel);
+  WsLayout w;
+  HERALD_RET_IF(check_ws(dims, C, P_max, ws, ws_bytes, &w));
+  return run_stage2(dims, q_block, k_cache, ctx_len, cand, n_cand, C, K, sink, local, P_max, idx,
+                    n_sel, ws, w, static_cast<cudaStream_t>(stream));
+}
+
+herald_status herald_select(herald_dims dims, const uint16_t* q_merge, const uint16_t* q_block,
+                            const uint16_t* k_cache, const int32_t* ctx_len, int C, int K,
+                            int sink, int local, int P_max, int32_t* idx, int32_t* n_sel,
+                            void* ws, size_t ws_bytes, void* stream) {
+  g_err[0] = 0;
+  HERALD_RET_IF(check_dims(dims));
+  HERALD_RET_IF(check_c(C));
+  HERALD_RET_IF(check_pmax(dims, P_max));
+  HERALD_RET_IF(check_budget(C, K, sink, local, P_max));
+  HERALD_CHECK_PTR(q_merge);
+  HERALD_CHECK_PTR(q_block);
+  HERALD_CHECK_PTR(k_cache);
+  HERALD_CHECK_PTR(ctx_len);
+  HERALD_CHECK_PTR(idx);
+  HERALD_CHECK_PTR(n_sel);
+  WsLayout w;
+  HERALD_RET_IF(check_ws(dims, C, P_max, ws, ws_bytes, &w));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t* cand = at<int32_t>(ws, w.cand);
+  int32_t* n_cand = at<int32_t>(ws, w.n_cand);
+  HERALD_RET_IF(run_stage1(dims, q_merge, k_cache, ctx_len, C, cand, n_cand, ws, w, st));
+  return run_stage2(dims, q_block, k_cache, ctx_len, cand, n_cand, C, K, sink, local, P_max, idx,
+                    n_sel, ws, w, st);
+}
+
+herald_status herald_gather(herald_dims dims, const int32_t* idx, const int32_t* n_sel,
+                            int P_max, const uint16_t* k_cache, const uint16_t* v_cache,
+                            uint16_t* pool_k, uint16_t* pool_v, void* stream) {
+  g_err[0] = 0;
+  HERALD_RET_IF(check_dims(dims));
+  HERALD_RET_IF(check_pmax(dims, P_max));
+  HERALD_CHECK_PTR(idx);
+  HERALD_CHECK_PTR(n_sel);
+  HERALD_CHECK_PTR(k_cache);
+  HERALD_CHECK_PTR(v_cache);
+  HERALD_CHECK_PTR(pool_k);
+  HERALD_CHECK_PTR(pool_v);
+  HERALD_TRY_CUDA(launch_gather(dims, idx, n_sel, P_max, k_cache, v_cache, pool_k, pool_v,
+                                static_cast<cudaStream_t>(stream)),
+                  "gather launch");
+  return HERALD_OK;
+}
+
+herald_status herald_denoise_attn(herald_dims dims, const uint16_t* q, const uint16_t* pool_k,
+                                  const uint16_t* pool_v, const int32_t* n_sel, int P_max,
+                                  const uint16_t* block_k, const uint16_t* block_v,
+                                  uint16_t* out, float scale, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  g_err[0] = 0;
+  HERALD_RET_IF(check_dims(dims));
+  HERALD_RET_IF(check_pmax(dims, P_max));
+  HERALD_CHECK_PTR(q);
+  HERALD_CHECK_PTR(pool_k);
+  HERALD_CHECK_PTR(pool_v);
+  HERALD_CHECK_PTR(n_sel);
+  HERALD_CHECK_PTR(block_k);
+  HERALD_CHECK_PTR(block_v);
+  HERALD_CHECK_PTR(out);
+  if (!(scale >= 0.f) || isinf(scale)) return fail(HERALD_ERR_INVALID_ARG, "scale must be finite and >= 0");
+  WsLayout w;
+  HERALD_RET_IF(check_ws(dims, 1, P_max, ws, ws_bytes, &w));
+  if (scale == 0.f) scale = 1.0f / sqrtf(float(dims.d));
+  HERALD_TRY_CUDA(launch_attn(dims, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale,
+                              w, at<float>(ws, w.opart), at<float2>(ws, w.ml),
+                              at<uint32_t>(ws, w.err), static_cast<cudaStream_t>(stream)),
+                  "attention launch");
+  return HERALD_OK;
+}
+
+herald_status herald_append_kv(herald_dims dims, const uint16_t* block_k, const uint16_t* block_v,
+                               int32_t* ctx_len, uint16_t* k_cache, uint16_t* v_cache,
+                               int advance, void* stream) {
+  g_err[0] = 0;
+  HERALD_RET_IF(check_dims(dims));
+  HERALD_CHECK_PTR(block_k);
+  HERALD_CHECK_PTR(block_v);
+  HERALD_CHECK_PTR(ctx_len);
+  HERALD_CHECK_PTR(k_cache);
+  HERALD_CHECK_PTR(v_cache);
+  HERALD_TRY_CUDA(launch_append(dims, block_k, block_v, ctx_len, k_cache, v_cache, advance,
+                                static_cast<cudaStream_t>(stream)),
+                  "append launch");
+  return HERALD_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,112 @@
+// internal.cuh -- constants, workspace layout and kernel launchers shared by
+// the translation units of libherald.so.  Not part of the public ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/herald.h"
+
+namespace herald {
+
+// ---- stage-1 scan
+constexpr int kScanTileKeys = 64;   // keys per TMA tile (one warp iteration)
+constexpr int kScanWarps = 4;       // warps per CTA, each with its own ring
+constexpr int kScanStages = 3;      // TMA stages per warp
+// ---- stage-1 score histogram (bits [30:19] of a non-negative fp32)
+constexpr int kHistBins = 4096;
+constexpr int kHistShift = 19;
+// ---- tensor-core tiles
+constexpr int kTileM = 128;         // rows per UMMA tile (M)
+constexpr int kRefineChunk = 256;   // candidates per stage-2 pass-1 CTA (N)
+constexpr int kRefineRows2 = 128;   // candidates per stage-2 pass-2 CTA (M)
+constexpr int kAttnKeys = 128;      // keys per attention split
+constexpr int kMaxC = 16384;        // candidates held in shared memory by top-K
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// Byte offsets of every region inside a caller-provided workspace.
+struct WsLayout {
+  size_t err;        // uint32 device error word
+  size_t qbar;       // float [N][Hq][d]        merged queries, pre-scaled
+  size_t logits;     // float [N][Hq][L_pad]    stage-1 logits
+  size_t part1;      // float2 [N][Hq][tiles]   per-tile (max, sumexp)
+  size_t s1;         // float [N][Hkv][L_pad]   stage-1 scores
+  size_t hist;       // uint32 [N*Hkv][kHistBins]
+  size_t cand;       // int32 [N][Hkv][C]       (herald_select only)
+  size_t n_cand;     // int32 [N][Hkv]
+  size_t rpart;      // float2 [N][Hkv][R_pad][n_chunks]  refine row stats
+  size_t s2;         // float [N][Hkv][C]
+  size_t opart;      // float [N*Hkv][MT][S][128][d]      attention partials
+  size_t ml;         // float2 [N*Hkv][MT][S][128]
+  size_t total;
+  int L_pad, tiles_per_seg, R, MT, n_chunks, splits;
+};
+
+inline WsLayout ws_layout(const herald_dims& dm, int C, int P_max) {
+  WsLayout w{};
+  const size_t A = 256;
+  const int G = dm.Hq / dm.Hkv;
+  w.tiles_per_seg = cdiv(dm.L_max, kScanTileKeys);
+  w.L_pad = w.tiles_per_seg * kScanTileKeys;
+  w.R = dm.B * G;
+  w.MT = cdiv(w.R, kTileM);
+  w.n_chunks = cdiv(C, kRefineChunk);
+  w.splits = cdiv(P_max, kAttnKeys) + cdiv(dm.B, kAttnKeys);
+  const size_t NH = size_t(dm.N) * dm.Hq, NG = size_t(dm.N) * dm.Hkv;
+  size_t o = 0;
+  w.err = o;    o = align_up(o + 16, A);
+  w.qbar = o;   o = align_up(o + NH * dm.d * 4, A);
+  w.logits = o; o = align_up(o + NH * w.L_pad * 4, A);
+  w.part1 = o;  o = align_up(o + NH * w.tiles_per_seg * 8, A);
+  w.s1 = o;     o = align_up(o + NG * w.L_pad * 4, A);
+  w.hist = o;   o = align_up(o + NG * kHistBins * 4, A);
+  w.cand = o;   o = align_up(o + NG * C * 4, A);
+  w.n_cand = o; o = align_up(o + NG * 4, A);
+  w.rpart = o;  o = align_up(o + NG * size_t(w.MT) * kTileM * w.n_chunks * 8, A);
+  w.s2 = o;     o = align_up(o + NG * C * 4, A);
+  w.opart = o;  o = align_up(o + NG * w.MT * size_t(w.splits) * kTileM * dm.d * 4, A);
+  w.ml = o;     o = align_up(o + NG * w.MT * size_t(w.splits) * kTileM * 8, A);
+  w.total = o;
+  return w;
+}
+
+// ---- kernel tracing: when enabled on this host thread, every kernel launch
+// is bracketed by two caller-owned CUDA events recorded on its stream.
+void trace_before(cudaStream_t st, const char* name);
+void trace_after(cudaStream_t st);
+
+// ---- launchers (return the launch error; the caller maps it to a status)
+cudaError_t launch_merge_query(const herald_dims& dm, const uint16_t* q_merge, float* qbar,
+                               uint32_t* hist, cudaStream_t st);
+cudaError_t launch_scan(const herald_dims& dm, const CUtensorMap* kmap, const uint16_t* k_cache,
+                        bool use_tma, const float* qbar, const int32_t* ctx, float* logits,
+                        float2* part1, const WsLayout& w, uint32_t* err, int num_sms,
+                        cudaStream_t st);
+cudaError_t launch_s1_hist(const herald_dims& dm, const float* logits, const float2* part1,
+                           const int32_t* ctx, float* s1, uint32_t* hist, const WsLayout& w,
+                           int num_sms, cudaStream_t st);
+cudaError_t launch_topc(const herald_dims& dm, const float* s1, const uint32_t* hist,
+                        const int32_t* ctx, int C, int32_t* cand, int32_t* n_cand,
+                        const WsLayout& w, cudaStream_t st);
+cudaError_t launch_refine(const herald_dims& dm, const uint16_t* q_block, const uint16_t* k_cache,
+                          const int32_t* cand, const int32_t* n_cand, int C, float2* rpart,
+                          float* s2, const WsLayout& w, uint32_t* err, cudaStream_t st);
+cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const int32_t* cand,
+                              const int32_t* n_cand, const float* s2, int C, int K, int S, int W,
+                              int P_max, int32_t* idx, int32_t* n_sel, cudaStream_t st);
+cudaError_t launch_gather(const herald_dims& dm, const int32_t* idx, const int32_t* n_sel,
+                          int P_max, const uint16_t* k_cache, const uint16_t* v_cache,
+                          uint16_t* pool_k, uint16_t* pool_v, cudaStream_t st);
+cudaError_t launch_attn(const herald_dims& dm, const uint16_t* q, const uint16_t* pool_k,
+                        const uint16_t* pool_v, const int32_t* n_sel, int P_max,
+                        const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
+                        float scale, const WsLayout& w, float* opart, float2* ml, uint32_t* err,
+                        cudaStream_t st);
+cudaError_t launch_append(const herald_dims& dm, const uint16_t* block_k, const uint16_t* block_v,
+                          int32_t* ctx, uint16_t* k_cache, uint16_t* v_cache, int advance,
+                          cudaStream_t st);
+
+}  // namespace herald

@@ -1,0 +1,98 @@
+// move_kernels.cu -- data movement on the HERALD path:
+//   gather  the selected cache rows into one buffer of the double-buffered
+//           sparse KV pool (HERALD early abstract: the subset crosses the
+//           host link once per block and is reused for all T steps); the
+//           source may be HBM or mapped pinned host memory
+//   append  the decoded block's K/V rows at the end of the cache (HERALD v3
+//           abstract: the cache grows as blocks are decoded)
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace herald {
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// grid (ceil(P_max / rows_per_cta), N*Hkv), block 256; D/8 threads per row,
+// one 16-byte chunk each.
+template <int D>
+__global__ void __launch_bounds__(256)
+    gather_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ n_sel, int P_max,
+                  int L_max, const uint16_t* __restrict__ kc, const uint16_t* __restrict__ vc,
+                  uint16_t* __restrict__ pk, uint16_t* __restrict__ pv) {
+  constexpr int TPR = D / 8, RPC = 256 / TPR;
+  const int seg = blockIdx.y;
+  const int row = blockIdx.x * RPC + threadIdx.x / TPR, c = threadIdx.x % TPR;
+  if (row >= P_max) return;
+  const int ns = min(max(n_sel[seg], 0), P_max);
+  uint4 kv = make_uint4(0, 0, 0, 0), vv = kv;
+  if (row < ns) {
+    const int pos = idx[size_t(seg) * P_max + row];
+    if (pos >= 0 && pos < L_max) {
+      const size_t off = (size_t(seg) * L_max + pos) * D + c * 8;
+      kv = ld_nc_v4(kc + off);
+      vv = ld_nc_v4(vc + off);
+    }
+  }
+  const size_t dst = (size_t(seg) * P_max + row) * D + c * 8;
+  *reinterpret_cast<uint4*>(pk + dst) = kv;
+  *reinterpret_cast<uint4*>(pv + dst) = vv;
+}
+
+cudaError_t launch_gather(const herald_dims& dm, const int32_t* idx, const int32_t* n_sel,
+                          int P_max, const uint16_t* k_cache, const uint16_t* v_cache,
+                          uint16_t* pool_k, uint16_t* pool_v, cudaStream_t st) {
+  const int segs = dm.N * dm.Hkv;
+  trace_before(st, "gather_kernel");
+  if (dm.d == 128)
+    gather_kernel<128><<<dim3(cdiv(P_max, 16), segs), 256, 0, st>>>(idx, n_sel, P_max, dm.L_max,
+                                                                     k_cache, v_cache, pool_k,
+                                                                     pool_v);
+  else
+    gather_kernel<64><<<dim3(cdiv(P_max, 32), segs), 256, 0, st>>>(idx, n_sel, P_max, dm.L_max,
+                                                                    k_cache, v_cache, pool_k,
+                                                                    pool_v);
+  trace_after(st);
+  return cudaGetLastError();
+}
+
+// grid N, block 256: one CTA per sequence so that reading ctx_len[n] and
+// advancing it cannot race with another CTA.
+__global__ void __launch_bounds__(256)
+    append_kernel(const uint16_t* __restrict__ bk, const uint16_t* __restrict__ bv, int B,
+                  int Hkv, int d, int L_max, int32_t* __restrict__ ctx,
+                  uint16_t* __restrict__ kc, uint16_t* __restrict__ vc, int advance) {
+  __shared__ int L0;
+  const int n = blockIdx.x;
+  if (threadIdx.x == 0) L0 = min(max(ctx[n], 0), L_max);
+  __syncthreads();
+  const int cpr = d / 8;
+  for (int q = threadIdx.x; q < B * Hkv * cpr; q += blockDim.x) {
+    const int c = q % cpr, bg = q / cpr, g = bg % Hkv, b = bg / Hkv;
+    const int j = L0 + b;
+    if (j >= L_max) continue;
+    const size_t src = ((size_t(n) * B + b) * Hkv + g) * d + c * 8;
+    const size_t dst = ((size_t(n) * Hkv + g) * L_max + j) * d + c * 8;
+    *reinterpret_cast<uint4*>(kc + dst) = *reinterpret_cast<const uint4*>(bk + src);
+    *reinterpret_cast<uint4*>(vc + dst) = *reinterpret_cast<const uint4*>(bv + src);
+  }
+  __syncthreads();
+  if (advance && threadIdx.x == 0) ctx[n] = min(L0 + B, L_max);
+}
+
+cudaError_t launch_append(const herald_dims& dm, const uint16_t* block_k, const uint16_t* block_v,
+                          int32_t* ctx, uint16_t* k_cache, uint16_t* v_cache, int advance,
+                          cudaStream_t st) {
+  trace_before(st, "append_kernel");
+  append_kernel<<<dm.N, 256, 0, st>>>(block_k, block_v, dm.B, dm.Hkv, dm.d, dm.L_max, ctx,
+                                      k_cache, v_cache, advance);
+  trace_after(st);
+  return cudaGetLastError();
+}
+
+}  // namespace herald

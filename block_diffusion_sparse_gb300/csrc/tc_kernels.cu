@@ -1,0 +1,570 @@
+// tc_kernels.cu -- the dense contractions of the HERALD hot path on the 5th
+// generation tensor cores (tcgen05.mma, bf16 operands in 128B-swizzled
+// shared memory, fp32 accumulators in TMEM):
+//   refine_pass1  stage 2 (HERALD v3 abstract: the candidates are re-scored
+//                 with the block's real queries): S = Q_blk . K_cand^T per
+//                 (sequence, KV head), per-row (max, sumexp) over a chunk of
+//                 256 candidates
+//   refine_pass2  S^T = K_cand . Q_blk^T for 128 candidates x all B*G rows;
+//                 each thread owns one candidate and sums the row-softmax
+//                 probabilities over the rows -> s2 (column sum)
+//   attn          one 128-key split of sparse block attention (HERALD early
+//                 abstract: the selected subset is reused for every
+//                 denoising step; block keys are visible to every block
+//                 query): S = Q K^T, P = exp(S - rowmax), O = P V
+//   attn_combine  merges the splits by their (max, sum) into bf16 out
+#include <cuda_bf16.h>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace herald {
+
+constexpr int kTcThreads = 256;  // 8 warps: lane quadrant = warp % 4
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Copies `rows` rows of D bf16 (row r from src_of(r), or zeros when src_of
+// returns nullptr) into a K-major 128B-swizzled tile: D/64 column halves,
+// each [rows_alloc][128 bytes].  `any_src` is a valid global address used
+// as the (unread) source of zero-filled chunks.
+template <int D, typename SrcOf>
+__device__ __forceinline__ void load_rows_sw128(uint8_t* tile, int rows, int rows_alloc,
+                                                const uint16_t* any_src, SrcOf src_of) {
+  constexpr int CPR = D / 8;  // 16-byte chunks per row
+  for (int q = threadIdx.x; q < rows * CPR; q += blockDim.x) {
+    const int r = q / CPR, c = q - (q / CPR) * CPR;
+    const uint16_t* s = src_of(r);
+    cp_async_16(tile + (c >> 3) * (rows_alloc * 128) + sw128_off(r, c & 7),
+                s ? s + c * 8 : any_src, s ? 16u : 0u);
+  }
+}
+
+// TMEM allocation protocol: warp 0 allocates, everybody syncs.
+__device__ __forceinline__ void tmem_setup(uint32_t* slot, uint32_t ncols) {
+  __syncwarp();
+  if ((threadIdx.x >> 5) == 0) {
+    tmem_alloc(slot, ncols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+}
+__device__ __forceinline__ void tmem_teardown(uint32_t base, uint32_t ncols) {
+  tc_fence_before();
+  __syncthreads();
+  if ((threadIdx.x >> 5) == 0) {
+    tc_fence_after();
+    tmem_dealloc(base, ncols);
+  }
+}
+
+// ========================================================== refine_pass1
+template <int D>
+struct Ref1Cfg {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kQBytes = kHalves * kTileM * 128;
+  static constexpr int kKBytes = kHalves * kRefineChunk * 128;
+  static constexpr int kSmem = kQBytes + kKBytes + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads)
+    refine_pass1_kernel(const uint16_t* __restrict__ q_block, const uint16_t* __restrict__ kc,
+                        const int32_t* __restrict__ cand, const int32_t* __restrict__ n_cand,
+                        int B, int Hq, int Hkv, int L_max, int C, int R, int MT, int n_chunks,
+                        float scale, float2* __restrict__ rpart, uint32_t* err) {
+  using Cfg = Ref1Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_base;
+  __shared__ float2 red[2][kTileM];
+  uint8_t* Qs = align1024(smem_raw);
+  uint8_t* Ks = Qs + Cfg::kQBytes;
+  const int chunk = blockIdx.x, mt = blockIdx.y, seg = blockIdx.z;
+  const int n = seg / Hkv, g = seg - n * Hkv, G = Hq / Hkv;
+  const int nc = min(max(n_cand[seg], 0), C);
+  const int c0 = chunk * kRefineChunk;
+  if (c0 >= nc) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  tmem_setup(&tmem_base, 256);
+  const uint32_t tbase = tmem_base;
+
+  load_rows_sw128<D>(Qs, kTileM, kTileM, q_block, [&](int r) -> const uint16_t* {
+    const int row = mt * kTileM + r;
+    if (row >= R) return nullptr;
+    const int b = row / G, hl = row - (row / G) * G;
+    return q_block + ((size_t(n) * B + b) * Hq + g * G + hl) * D;
+  });
+  const int32_t* cd = cand + size_t(seg) * C;
+  load_rows_sw128<D>(Ks, kRefineChunk, kRefineChunk, kc, [&](int r) -> const uint16_t* {
+    const int ci = c0 + r;
+    if (ci >= nc) return nullptr;
+    return kc + (size_t(seg) * L_max + cd[ci]) * D;
+  });
+  cp_async_commit();
+  cp_async_wait_all();
+  fence_proxy_async_smem();
+  __syncthreads();
+  tc_fence_after();
+
+  if (threadIdx.x == 0) {
+    constexpr uint32_t idesc = make_idesc_bf16(kTileM, kRefineChunk, false, false);
+    const uint32_t qa = smem_u32(Qs), ka = smem_u32(Ks);
+#pragma unroll
+    for (int s = 0; s < D / 16; ++s) {
+      const uint32_t hv = s >> 2, koff = (s & 3) * 32;
+      const uint64_t a = make_sdesc_sw128(qa + hv * (kTileM * 128) + koff, 16, 1024);
+      const uint64_t b = make_sdesc_sw128(ka + hv * (kRefineChunk * 128) + koff, 16, 1024);
+      umma_bf16(tbase, a, b, idesc, s > 0 ? 1u : 0u);
+    }
+    umma_commit(&bar);
+  }
+  if (!mbar_wait(&bar, 0)) record_error(err, DEV_TIMEOUT_MMA);
+  tc_fence_after();
+  __syncwarp();
+
+  const int quad = warp & 3, ch = warp >> 2;
+  const int row = quad * 32 + lane;
+  const uint32_t taddr = tbase + (uint32_t(quad * 32) << 16) + uint32_t(ch * 128);
+  float m = -INFINITY;
+  float v[32];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    tmem_ld32(taddr + k * 32, v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (c0 + ch * 128 + k * 32 + i < nc) m = fmaxf(m, v[i] * scale);
+  }
+  float sum = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    tmem_ld32(taddr + k * 32, v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (c0 + ch * 128 + k * 32 + i < nc) sum += __expf(v[i] * scale - m);
+  }
+  red[ch][row] = make_float2(m, sum);
+  __syncthreads();
+  if (ch == 0) {
+    const float2 a = red[0][row], b = red[1][row];
+    const float M = fmaxf(a.x, b.x);
+    const float S = (a.x == -INFINITY ? 0.f : a.y * __expf(a.x - M)) +
+                    (b.x == -INFINITY ? 0.f : b.y * __expf(b.x - M));
+    const int grow = mt * kTileM + row;
+    if (grow < R) rpart[(size_t(seg) * MT * kTileM + grow) * n_chunks + chunk] = make_float2(M, S);
+  }
+  tmem_teardown(tbase, 256);
+}
+
+// ========================================================== refine_pass2
+template <int D>
+struct Ref2Cfg {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kKBytes = kHalves * kRefineRows2 * 128;
+  static constexpr int kQBytes = kHalves * 256 * 128;
+  static constexpr int kSmem = kKBytes + kQBytes + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads)
+    refine_pass2_kernel(const uint16_t* __restrict__ q_block, const uint16_t* __restrict__ kc,
+                        const int32_t* __restrict__ cand, const int32_t* __restrict__ n_cand,
+                        int B, int Hq, int Hkv, int L_max, int C, int R, int MT, int n_chunks,
+                        float scale, const float2* __restrict__ rpart, float* __restrict__ s2,
+                        uint32_t* err) {
+  using Cfg = Ref2Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_base;
+  __shared__ float lse[256];
+  __shared__ float red[2][kRefineRows2];
+  uint8_t* Ks = align1024(smem_raw);
+  uint8_t* Qs = Ks + Cfg::kKBytes;
+  const int seg = blockIdx.y, n = seg / Hkv, g = seg - n * Hkv, G = Hq / Hkv;
+  const int nc = min(max(n_cand[seg], 0), C);
+  const int c0 = blockIdx.x * kRefineRows2;
+  if (c0 >= nc) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Rp = (R + 15) & ~15;  // MMA N: multiple of 16
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  tmem_setup(&tmem_base, 256);
+  const uint32_t tbase = tmem_base;
+
+  const int32_t* cd = cand + size_t(seg) * C;
+  load_rows_sw128<D>(Ks, kRefineRows2, kRefineRows2, kc, [&](int r) -> const uint16_t* {
+    const int ci = c0 + r;
+    if (ci >= nc) return nullptr;
+    return kc + (size_t(seg) * L_max + cd[ci]) * D;
+  });
+  load_rows_sw128<D>(Qs, Rp, 256, q_block, [&](int r) -> const uint16_t* {
+    if (r >= R) return nullptr;
+    const int b = r / G, hl = r - (r / G) * G;
+    return q_block + ((size_t(n) * B + b) * Hq + g * G + hl) * D;
+  });
+  cp_async_commit();
+  // row log-sum-exp over all candidates from the pass-1 chunk partials
+  const int nch = (nc + kRefineChunk - 1) / kRefineChunk;
+  for (int r = threadIdx.x; r < R; r += kTcThreads) {
+    const float2* p = rpart + (size_t(seg) * MT * kTileM + r) * n_chunks;
+    float M = -INFINITY;
+    for (int k = 0; k < nch; ++k) M = fmaxf(M, p[k].x);
+    float S = 0.f;
+    for (int k = 0; k < nch; ++k) S += p[k].y * __expf(p[k].x - M);
+    lse[r] = M + __logf(S);
+  }
+  cp_async_wait_all();
+  fence_proxy_async_smem();
+  __syncthreads();
+  tc_fence_after();
+
+  if (threadIdx.x == 0) {
+    const uint32_t idesc = make_idesc_bf16(kRefineRows2, Rp, false, false);
+    const uint32_t ka = smem_u32(Ks), qa = smem_u32(Qs);
+#pragma unroll
+    for (int s = 0; s < D / 16; ++s) {
+      const uint32_t hv = s >> 2, koff = (s & 3) * 32;
+      const uint64_t a = make_sdesc_sw128(ka + hv * (kRefineRows2 * 128) + koff, 16, 1024);
+      const uint64_t b = make_sdesc_sw128(qa + hv * (256 * 128) + koff, 16, 1024);
+      umma_bf16(tbase, a, b, idesc, s > 0 ? 1u : 0u);
+    }
+    umma_commit(&bar);
+  }
+  if (!mbar_wait(&bar, 0)) record_error(err, DEV_TIMEOUT_MMA);
+  tc_fence_after();
+  __syncwarp();
+
+  const int quad = warp & 3, ch = warp >> 2;
+  const int row = quad * 32 + lane;
+  const uint32_t taddr = tbase + (uint32_t(quad * 32) << 16);
+  float acc = 0.f;
+  float v[32];
+  for (int k = 0; k < 4; ++k) {
+    const int col0 = ch * 128 + k * 32;
+    if (col0 >= R) break;  // uniform per warp
+    tmem_ld32(taddr + col0, v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (col0 + i < R) acc += __expf(v[i] * scale - lse[col0 + i]);
+  }
+  red[ch][row] = acc;
+  __syncthreads();
+  if (ch == 0 && c0 + row < nc) s2[size_t(seg) * C + c0 + row] = red[0][row] + red[1][row];
+  tmem_teardown(tbase, 256);
+}
+
+cudaError_t launch_refine(const herald_dims& dm, const uint16_t* q_block, const uint16_t* k_cache,
+                          const int32_t* cand, const int32_t* n_cand, int C, float2* rpart,
+                          float* s2, const WsLayout& w, uint32_t* err, cudaStream_t st) {
+  const float scale = 1.0f / sqrtf(float(dm.d));
+  const int segs = dm.N * dm.Hkv;
+  cudaError_t e;
+  if (dm.d == 128) {
+    static bool attr = false;
+    if (!attr) {
+      e = cudaFuncSetAttribute(refine_pass1_kernel<128>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, Ref1Cfg<128>::kSmem);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(refine_pass2_kernel<128>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, Ref2Cfg<128>::kSmem);
+      if (e != cudaSuccess) return e;
+      attr = true;
+    }
+    trace_before(st, "refine_pass1_kernel");
+    refine_pass1_kernel<128><<<dim3(w.n_chunks, w.MT, segs), kTcThreads, Ref1Cfg<128>::kSmem,
+                               st>>>(q_block, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv,
+                                     dm.L_max, C, w.R, w.MT, w.n_chunks, scale, rpart, err);
+    trace_after(st);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    trace_before(st, "refine_pass2_kernel");
+    refine_pass2_kernel<128><<<dim3(cdiv(C, kRefineRows2), segs), kTcThreads,
+                               Ref2Cfg<128>::kSmem, st>>>(q_block, k_cache, cand, n_cand, dm.B,
+                                                          dm.Hq, dm.Hkv, dm.L_max, C, w.R, w.MT,
+                                                          w.n_chunks, scale, rpart, s2, err);
+    trace_after(st);
+  } else {
+    static bool attr = false;
+    if (!attr) {
+      e = cudaFuncSetAttribute(refine_pass1_kernel<64>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, Ref1Cfg<64>::kSmem);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(refine_pass2_kernel<64>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, Ref2Cfg<64>::kSmem);
+      if (e != cudaSuccess) return e;
+      attr = true;
+    }
+    trace_before(st, "refine_pass1_kernel");
+    refine_pass1_kernel<64><<<dim3(w.n_chunks, w.MT, segs), kTcThreads, Ref1Cfg<64>::kSmem,
+                              st>>>(q_block, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv,
+                                    dm.L_max, C, w.R, w.MT, w.n_chunks, scale, rpart, err);
+    trace_after(st);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    trace_before(st, "refine_pass2_kernel");
+    refine_pass2_kernel<64><<<dim3(cdiv(C, kRefineRows2), segs), kTcThreads, Ref2Cfg<64>::kSmem,
+                              st>>>(q_block, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv,
+                                    dm.L_max, C, w.R, w.MT, w.n_chunks, scale, rpart, s2, err);
+    trace_after(st);
+  }
+  return cudaGetLastError();
+}
+
+// ================================================================== attn
+template <int D>
+struct AttnCfg {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kQBytes = kHalves * kTileM * 128;
+  static constexpr int kKBytes = kHalves * kAttnKeys * 128;
+  static constexpr int kVBytes = kHalves * kAttnKeys * 128;
+  static constexpr int kPBytes = 2 * kTileM * 128;  // 128 rows x 128 keys, 2 key halves
+  static constexpr int kSmem = kQBytes + kKBytes + kVBytes + kPBytes + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads)
+    attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ pool_k,
+                const uint16_t* __restrict__ pool_v, const int32_t* __restrict__ n_sel,
+                int P_max, const uint16_t* __restrict__ block_k,
+                const uint16_t* __restrict__ block_v, int B, int Hq, int Hkv, int R, int MT,
+                int S_max, float scale, float* __restrict__ opart, float2* __restrict__ ml,
+                uint32_t* err) {
+  using Cfg = AttnCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar[2];
+  __shared__ uint32_t tmem_base;
+  __shared__ float red_m[2][kTileM];
+  __shared__ float red_s[2][kTileM];
+  uint8_t* Qs = align1024(smem_raw);
+  uint8_t* Ks = Qs + Cfg::kQBytes;
+  uint8_t* Vs = Ks + Cfg::kKBytes;
+  uint8_t* Ps = Vs + Cfg::kVBytes;
+  const int split = blockIdx.x, mt = blockIdx.y, seg = blockIdx.z;
+  const int n = seg / Hkv, g = seg - n * Hkv, G = Hq / Hkv;
+  const int ns = min(max(n_sel[seg], 0), P_max);
+  const int n_pool = (ns + kAttnKeys - 1) / kAttnKeys;
+  const int n_blk = (B + kAttnKeys - 1) / kAttnKeys;
+  if (split >= n_pool + n_blk) return;
+  const bool from_pool = split < n_pool;
+  const int k0 = from_pool ? split * kAttnKeys : (split - n_pool) * kAttnKeys;
+  const int nkeys = from_pool ? min(kAttnKeys, ns - k0) : min(kAttnKeys, B - k0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_mbar_init();
+  }
+  tmem_setup(&tmem_base, 256);
+  const uint32_t tbase = tmem_base;
+
+  load_rows_sw128<D>(Qs, kTileM, kTileM, q, [&](int r) -> const uint16_t* {
+    const int row = mt * kTileM + r;
+    if (row >= R) return nullptr;
+    const int b = row / G, hl = row - (row / G) * G;
+    return q + ((size_t(n) * B + b) * Hq + g * G + hl) * D;
+  });
+  auto key_src = [&](const uint16_t* pool, const uint16_t* blk, int r) -> const uint16_t* {
+    if (r >= nkeys) return nullptr;
+    if (from_pool) return pool + (size_t(seg) * P_max + k0 + r) * D;
+    return blk + ((size_t(n) * B + k0 + r) * Hkv + g) * D;
+  };
+  load_rows_sw128<D>(Ks, kAttnKeys, kAttnKeys, block_k,
+                     [&](int r) { return key_src(pool_k, block_k, r); });
+  cp_async_commit();
+  load_rows_sw128<D>(Vs, kAttnKeys, kAttnKeys, block_v,
+                     [&](int r) { return key_src(pool_v, block_v, r); });
+  cp_async_commit();
+  asm volatile("cp.async.wait_group 1;" ::: "memory");  // Q and K landed
+  fence_proxy_async_smem();
+  __syncthreads();
+  tc_fence_after();
+
+  // S = Q K^T -> TMEM columns [0, 128)
+  if (threadIdx.x == 0) {
+    constexpr uint32_t idesc = make_idesc_bf16(kTileM, kAttnKeys, false, false);
+    const uint32_t qa = smem_u32(Qs), ka = smem_u32(Ks);
+#pragma unroll
+    for (int s = 0; s < D / 16; ++s) {
+      const uint32_t hv = s >> 2, koff = (s & 3) * 32;
+      const uint64_t a = make_sdesc_sw128(qa + hv * (kTileM * 128) + koff, 16, 1024);
+      const uint64_t b = make_sdesc_sw128(ka + hv * (kAttnKeys * 128) + koff, 16, 1024);
+      umma_bf16(tbase, a, b, idesc, s > 0 ? 1u : 0u);
+    }
+    umma_commit(&bar[0]);
+  }
+  if (!mbar_wait(&bar[0], 0)) record_error(err, DEV_TIMEOUT_MMA);
+  tc_fence_after();
+  __syncwarp();
+
+  const int quad = warp & 3, ch = warp >> 2;  // ch: key half [ch*64, ch*64+64)
+  const int row = quad * 32 + lane;
+  const uint32_t trow = tbase + (uint32_t(quad * 32) << 16);
+  float x[64];
+  {
+    float v[32];
+    tmem_ld32(trow + ch * 64, v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] = v[i];
+    tmem_ld32(trow + ch * 64 + 32, v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[32 + i] = v[i];
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 64; ++i) {
+    x[i] = (ch * 64 + i < nkeys) ? x[i] * scale : -INFINITY;
+    m = fmaxf(m, x[i]);
+  }
+  red_m[ch][row] = m;
+  __syncthreads();
+  m = fmaxf(red_m[0][row], red_m[1][row]);
+  float sum = 0.f;
+  uint8_t* prow = Ps + ch * (kTileM * 128);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    float p[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      p[e] = __expf(x[c * 8 + e] - m);
+      sum += p[e];
+    }
+    uint4 pk;
+    pk.x = pack_bf16(p[0], p[1]);
+    pk.y = pack_bf16(p[2], p[3]);
+    pk.z = pack_bf16(p[4], p[5]);
+    pk.w = pack_bf16(p[6], p[7]);
+    *reinterpret_cast<uint4*>(prow + sw128_off(row, c)) = pk;
+  }
+  red_s[ch][row] = sum;
+  asm volatile("cp.async.wait_group 0;" ::: "memory");  // V landed
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  // O = P V -> TMEM columns [128, 128 + D); V is the MN-major B operand
+  if (threadIdx.x == 0) {
+    constexpr uint32_t idesc = make_idesc_bf16(kTileM, D, false, true);
+    const uint32_t pa = smem_u32(Ps), va = smem_u32(Vs);
+#pragma unroll
+    for (int s = 0; s < kAttnKeys / 16; ++s) {
+      const uint32_t kh = s >> 2, koff = (s & 3) * 32;
+      const uint64_t a = make_sdesc_sw128(pa + kh * (kTileM * 128) + koff, 16, 1024);
+      const uint64_t b = make_sdesc_sw128(va + s * 2048, kAttnKeys * 128, 1024);
+      umma_bf16(tbase + 128, a, b, idesc, s > 0 ? 1u : 0u);
+    }
+    umma_commit(&bar[1]);
+  }
+  if (!mbar_wait(&bar[1], 0)) record_error(err, DEV_TIMEOUT_MMA);
+  tc_fence_after();
+  __syncwarp();
+
+  const size_t prow_idx = ((size_t(seg) * MT + mt) * S_max + split) * kTileM + row;
+  float* op = opart + prow_idx * D;
+#pragma unroll
+  for (int k = 0; k < D / 64; ++k) {
+    float v[32];
+    const int col = ch * (D / 2) + k * 32;
+    tmem_ld32(trow + 128 + col, v);
+#pragma unroll
+    for (int i = 0; i < 32; i += 4)
+      *reinterpret_cast<float4*>(op + col + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+  }
+  if (ch == 0) ml[prow_idx] = make_float2(m, red_s[0][row] + red_s[1][row]);
+  tmem_teardown(tbase, 256);
+}
+
+// =========================================================== attn_combine
+// One warp per output row (n, b, h); lane owns D/32 consecutive features.
+template <int D>
+__global__ void __launch_bounds__(256)
+    attn_combine_kernel(const float* __restrict__ opart, const float2* __restrict__ ml,
+                        const int32_t* __restrict__ n_sel, int P_max, int N, int B, int Hq,
+                        int Hkv, int MT, int S_max, uint16_t* __restrict__ out) {
+  constexpr int E = D / 32;
+  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (gw >= N * B * Hq) return;
+  const int n = gw / (B * Hq), b = (gw / Hq) % B, h = gw % Hq;
+  const int G = Hq / Hkv, g = h / G, r = b * G + (h - g * G);
+  const int mt = r / kTileM, i = r % kTileM, seg = n * Hkv + g;
+  const int ns = min(max(n_sel[seg], 0), P_max);
+  const int nsp = (ns + kAttnKeys - 1) / kAttnKeys + (B + kAttnKeys - 1) / kAttnKeys;
+  const size_t base = (size_t(seg) * MT + mt) * S_max;
+  float M = -INFINITY;
+  for (int s = 0; s < nsp; ++s) M = fmaxf(M, ml[(base + s) * kTileM + i].x);
+  float acc[E] = {};
+  float L = 0.f;
+  for (int s = 0; s < nsp; ++s) {
+    const float2 p = ml[(base + s) * kTileM + i];
+    const float w = __expf(p.x - M);
+    L += w * p.y;
+    const float* o = opart + ((base + s) * kTileM + i) * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] += w * o[e];
+  }
+  const float inv = 1.f / L;
+  uint16_t* dst = out + size_t(gw) * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; e += 2) {
+    const uint32_t pk = pack_bf16(acc[e] * inv, acc[e + 1] * inv);
+    *reinterpret_cast<uint32_t*>(dst + e) = pk;
+  }
+}
+
+cudaError_t launch_attn(const herald_dims& dm, const uint16_t* q, const uint16_t* pool_k,
+                        const uint16_t* pool_v, const int32_t* n_sel, int P_max,
+                        const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
+                        float scale, const WsLayout& w, float* opart, float2* ml, uint32_t* err,
+                        cudaStream_t st) {
+  const int segs = dm.N * dm.Hkv;
+  const int rows = dm.N * dm.B * dm.Hq;
+  cudaError_t e;
+  if (dm.d == 128) {
+    static bool attr = false;
+    if (!attr) {
+      e = cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               AttnCfg<128>::kSmem);
+      if (e != cudaSuccess) return e;
+      attr = true;
+    }
+    trace_before(st, "attn_kernel");
+    attn_kernel<128><<<dim3(w.splits, w.MT, segs), kTcThreads, AttnCfg<128>::kSmem, st>>>(
+        q, pool_k, pool_v, n_sel, P_max, block_k, block_v, dm.B, dm.Hq, dm.Hkv, w.R, w.MT,
+        w.splits, scale, opart, ml, err);
+    trace_after(st);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    trace_before(st, "attn_combine_kernel");
+    attn_combine_kernel<128><<<cdiv(rows, 8), 256, 0, st>>>(
+        opart, ml, n_sel, P_max, dm.N, dm.B, dm.Hq, dm.Hkv, w.MT, w.splits, out);
+    trace_after(st);
+  } else {
+    static bool attr = false;
+    if (!attr) {
+      e = cudaFuncSetAttribute(attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               AttnCfg<64>::kSmem);
+      if (e != cudaSuccess) return e;
+      attr = true;
+    }
+    trace_before(st, "attn_kernel");
+    attn_kernel<64><<<dim3(w.splits, w.MT, segs), kTcThreads, AttnCfg<64>::kSmem, st>>>(
+        q, pool_k, pool_v, n_sel, P_max, block_k, block_v, dm.B, dm.Hq, dm.Hkv, w.R, w.MT,
+        w.splits, scale, opart, ml, err);
+    trace_after(st);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    trace_before(st, "attn_combine_kernel");
+    attn_combine_kernel<64><<<cdiv(rows, 8), 256, 0, st>>>(
+        opart, ml, n_sel, P_max, dm.N, dm.B, dm.Hq, dm.Hkv, w.MT, w.splits, out);
+    trace_after(st);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace herald

@@ -1,0 +1,205 @@
+"""ctypes binding of libherald.so (include/herald.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  Tensors may be torch tensors (their data_ptr() is passed) or raw
+integer addresses; streams may be torch streams or raw cudaStream_t values.
+There is no CPU fallback: if the library is missing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libherald.so")
+
+HERALD_OK = 0
+STATUS = {0: "HERALD_OK", 1: "HERALD_ERR_INVALID_ARG", 2: "HERALD_ERR_UNSUPPORTED_SHAPE",
+          3: "HERALD_ERR_WORKSPACE_TOO_SMALL", 4: "HERALD_ERR_CUDA"}
+
+EXPORTS = ("herald_workspace_size", "herald_status_string", "herald_last_error",
+           "herald_workspace_error", "herald_select_stage1", "herald_select_stage2",
+           "herald_select", "herald_gather", "herald_denoise_attn", "herald_append_kv",
+           "herald_trace_begin", "herald_trace_end", "herald_trace_name")
+
+
+class HeraldError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        super().__init__(f"{STATUS.get(status, status)}: {detail}")
+        self.status = status
+
+
+class Dims(C.Structure):
+    _fields_ = [("N", C.c_int), ("Hq", C.c_int), ("Hkv", C.c_int), ("d", C.c_int),
+                ("B", C.c_int), ("L_max", C.c_int)]
+
+    def __repr__(self):
+        return (f"Dims(N={self.N}, Hq={self.Hq}, Hkv={self.Hkv}, d={self.d}, B={self.B}, "
+                f"L_max={self.L_max})")
+
+
+def dims(N, Hq, Hkv, d, B, L_max) -> Dims:
+    return Dims(int(N), int(Hq), int(Hkv), int(d), int(B), int(L_max))
+
+
+def dims_of(w) -> Dims:
+    """Dims of a workloads.Workload."""
+    return dims(w.N, w.Hq, w.Hkv, w.d, w.B, w.L_max)
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """Loads libherald.so (built by __graft_entry__.build() or build.py)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libherald.so not built ({LIB_PATH}); run "
+                "`python -m block_diffusion_sparse_gb300.build` first")
+        L = C.CDLL(LIB_PATH)
+        vp, i32, sz = C.c_void_p, C.c_int, C.c_size_t
+        L.herald_workspace_size.argtypes = [Dims, i32, i32]
+        L.herald_workspace_size.restype = sz
+        L.herald_status_string.argtypes = [i32]
+        L.herald_status_string.restype = C.c_char_p
+        L.herald_last_error.argtypes = []
+        L.herald_last_error.restype = C.c_char_p
+        L.herald_workspace_error.argtypes = [vp, vp, C.POINTER(C.c_uint32)]
+        L.herald_select_stage1.argtypes = [Dims, vp, vp, vp, i32, vp, vp, vp, sz, vp]
+        L.herald_select_stage2.argtypes = [Dims, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                           vp, vp, vp, sz, vp]
+        L.herald_select.argtypes = [Dims, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp,
+                                    sz, vp]
+        L.herald_gather.argtypes = [Dims, vp, vp, i32, vp, vp, vp, vp, vp]
+        L.herald_denoise_attn.argtypes = [Dims, vp, vp, vp, vp, i32, vp, vp, vp, C.c_float, vp,
+                                          sz, vp]
+        L.herald_append_kv.argtypes = [Dims, vp, vp, vp, vp, vp, i32, vp]
+        L.herald_trace_begin.argtypes = [C.POINTER(vp), i32, i32]
+        L.herald_trace_end.argtypes = []
+        L.herald_trace_name.argtypes = [i32]
+        L.herald_trace_name.restype = C.c_char_p
+        for name in EXPORTS:
+            if name not in ("herald_workspace_size", "herald_status_string",
+                            "herald_last_error", "herald_trace_name"):
+                getattr(L, name).restype = C.c_int
+        _lib = L
+    return _lib
+
+
+def _p(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    raise TypeError(f"expected a tensor or an address, got {type(x)}")
+
+
+def _s(stream):
+    if stream is None:
+        return None
+    if isinstance(stream, int):
+        return stream
+    if hasattr(stream, "cuda_stream"):
+        return stream.cuda_stream
+    raise TypeError(f"expected a stream, got {type(stream)}")
+
+
+def _nbytes(ws, ws_bytes):
+    if ws_bytes is not None:
+        return int(ws_bytes)
+    if hasattr(ws, "numel"):
+        return ws.numel() * ws.element_size()
+    raise ValueError("ws_bytes is required for a raw workspace address")
+
+
+def _check(status: int):
+    if status != HERALD_OK:
+        raise HeraldError(status, lib().herald_last_error().decode())
+
+
+def herald_workspace_size(d: Dims, C_: int, P_max: int) -> int:
+    return int(lib().herald_workspace_size(d, int(C_), int(P_max)))
+
+
+def herald_status_string(status: int) -> str:
+    return lib().herald_status_string(int(status)).decode()
+
+
+def herald_workspace_error(ws, stream=None) -> int:
+    code = C.c_uint32(0)
+    _check(lib().herald_workspace_error(_p(ws), _s(stream), C.byref(code)))
+    return int(code.value)
+
+
+def herald_select_stage1(d, q_merge, k_cache, ctx_len, C_, cand, n_cand, ws, ws_bytes=None,
+                         stream=None):
+    _check(lib().herald_select_stage1(d, _p(q_merge), _p(k_cache), _p(ctx_len), int(C_),
+                                      _p(cand), _p(n_cand), _p(ws), _nbytes(ws, ws_bytes),
+                                      _s(stream)))
+
+
+def herald_select_stage2(d, q_block, k_cache, ctx_len, cand, n_cand, C_, K, sink, local, P_max,
+                         idx, n_sel, ws, ws_bytes=None, stream=None):
+    _check(lib().herald_select_stage2(d, _p(q_block), _p(k_cache), _p(ctx_len), _p(cand),
+                                      _p(n_cand), int(C_), int(K), int(sink), int(local),
+                                      int(P_max), _p(idx), _p(n_sel), _p(ws),
+                                      _nbytes(ws, ws_bytes), _s(stream)))
+
+
+def herald_select(d, q_merge, q_block, k_cache, ctx_len, C_, K, sink, local, P_max, idx, n_sel,
+                  ws, ws_bytes=None, stream=None):
+    _check(lib().herald_select(d, _p(q_merge), _p(q_block), _p(k_cache), _p(ctx_len), int(C_),
+                               int(K), int(sink), int(local), int(P_max), _p(idx), _p(n_sel),
+                               _p(ws), _nbytes(ws, ws_bytes), _s(stream)))
+
+
+def herald_gather(d, idx, n_sel, P_max, k_cache, v_cache, pool_k, pool_v, stream=None):
+    _check(lib().herald_gather(d, _p(idx), _p(n_sel), int(P_max), _p(k_cache), _p(v_cache),
+                               _p(pool_k), _p(pool_v), _s(stream)))
+
+
+def herald_denoise_attn(d, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale=0.0,
+                        ws=None, ws_bytes=None, stream=None):
+    _check(lib().herald_denoise_attn(d, _p(q), _p(pool_k), _p(pool_v), _p(n_sel), int(P_max),
+                                     _p(block_k), _p(block_v), _p(out), float(scale), _p(ws),
+                                     _nbytes(ws, ws_bytes), _s(stream)))
+
+
+def herald_append_kv(d, block_k, block_v, ctx_len, k_cache, v_cache, advance=True,
+                     stream=None):
+    _check(lib().herald_append_kv(d, _p(block_k), _p(block_v), _p(ctx_len), _p(k_cache),
+                                  _p(v_cache), int(bool(advance)), _s(stream)))
+
+
+class Trace:
+    """Records a CUDA event pair around every kernel the library launches on
+    this thread (see herald_trace_begin).  `external=True` makes the events
+    graph nodes when the calls are stream-captured."""
+
+    def __init__(self, capacity: int = 256, external: bool = False):
+        import torch
+        self.capacity = capacity
+        self.external = external
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * capacity)]
+        self._arr = (C.c_void_p * (2 * capacity))(*[e.cuda_event for e in self.events])
+        self.count = 0
+        self.names: list[str] = []
+
+    def __enter__(self):
+        _check(lib().herald_trace_begin(self._arr, self.capacity, int(self.external)))
+        return self
+
+    def __exit__(self, *exc):
+        self.count = int(lib().herald_trace_end())
+        self.names = [lib().herald_trace_name(i).decode() for i in range(self.count)]
+        return False
+
+    def durations_ms(self) -> list[tuple[str, float]]:
+        """(kernel name, elapsed ms) per traced launch; call after the work
+        (or the graph replay that recorded the events) has synchronised."""
+        return [(self.names[i], self.events[2 * i].elapsed_time(self.events[2 * i + 1]))
+                for i in range(self.count)]

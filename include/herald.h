@@ -1,0 +1,177 @@
+/*
+ * herald.h -- C ABI of the HERALD hot path on one GPU (sm_103a).
+ *
+ * Method (web pages on the subject):
+ *   [V3]  "HERALD: High-Throughput Block Diffusion LLM Inference via CPU-GPU
+ *         Cooperative KV Cache Retrieval", arXiv 2606.21633 v3, abstract.
+ *   [EA]  HERALD early abstract (mlsift.com, "KV cache offloading" listing).
+ *   [SPD] SparDA summary (hyper.ai, arXiv 2606.04511), Method section.
+ *
+ * One block of a block-diffusion LLM layer is decoded as:
+ *   select (once per block)  ->  gather into a sparse pool  ->  T x attention.
+ * Selection has two stages [V3]: stage 1 scores one merged query per head
+ * (the mean of the B block queries) against the whole cache and keeps C
+ * candidates per KV head; stage 2 scores the block's real B*G queries of a
+ * GQA group against those candidates only and keeps K, to which sink and
+ * local positions are added.
+ *
+ * Conventions shared by every call:
+ *   - bf16 tensors are passed as uint16_t bit patterns; all tensors are dense
+ *     and row-major in the layouts given per argument.
+ *   - "device pointer" = memory the GPU can address: cudaMalloc memory, or
+ *     (where stated) mapped pinned host memory (cudaHostAlloc with
+ *     cudaHostAllocMapped, used through its device pointer).
+ *   - Every pointer must be 16-byte aligned.  The caller owns every buffer;
+ *     the library never allocates or frees device memory.
+ *   - All calls are asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream).  A call validates its arguments on the host
+ *     first and launches nothing if they are invalid.  Launch failures are
+ *     reported as HERALD_ERR_CUDA with the message in herald_last_error().
+ *     Faults inside kernels surface at the next synchronisation.
+ *   - Kernels that wait on their own asynchronous copies or tensor-core
+ *     work give up after about one second, record a code in the
+ *     workspace's error word and return; read it with
+ *     herald_workspace_error().
+ *   - GQA: query head h belongs to KV head h / G, G = Hq / Hkv.
+ *   - Scores use the scale 1/sqrt(d).  Ties in every top-m are broken
+ *     towards the lower cache position; index outputs are ascending.
+ *   - ctx_len values must lie in [0, L_max]; kernels clamp to that range.
+ *   - One workspace may not be shared by calls that can run concurrently.
+ */
+#ifndef HERALD_H
+#define HERALD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  HERALD_OK = 0,
+  HERALD_ERR_INVALID_ARG = 1,        /* null/misaligned pointer, bad count   */
+  HERALD_ERR_UNSUPPORTED_SHAPE = 2,  /* d, G, B*G, C outside supported set  */
+  HERALD_ERR_WORKSPACE_TOO_SMALL = 3,
+  HERALD_ERR_CUDA = 4                /* CUDA runtime/driver error            */
+} herald_status;
+
+/* Shapes of one attention layer.
+ *   N     sequences in the batch           (>= 1)
+ *   Hq    query heads                      (Hq % Hkv == 0, 1 <= G <= 8)
+ *   Hkv   KV heads                         (>= 1)
+ *   d     head dimension                   (64 or 128)
+ *   B     block size (queries per block)   (>= 1, B*G <= 256)
+ *   L_max cache rows per (sequence, KV head) (>= 1, N*Hkv*L_max < 2^31) */
+typedef struct {
+  int N, Hq, Hkv, d, B, L_max;
+} herald_dims;
+
+/* Bytes of workspace needed by herald_select*, herald_denoise_attn for these
+ * shapes, candidate count C and pool capacity P_max.  Returns 0 if the
+ * shapes are unsupported. */
+size_t herald_workspace_size(herald_dims dims, int C, int P_max);
+
+/* Static text for a status code. */
+const char *herald_status_string(herald_status s);
+
+/* Detail of the last error raised on this host thread ("" if none). */
+const char *herald_last_error(void);
+
+/* Synchronously reads and clears the device error word of a workspace
+ * (0 = no kernel gave up on a wait; 1 = a copy wait, 2 = a tensor-core wait
+ * ran out).  Synchronises `stream` first. */
+herald_status herald_workspace_error(void *ws, void *stream, uint32_t *code);
+
+/* Stage 1 of the selection [V3]: merged query + full-cache scan + top-C.
+ *   q_merge [N][B][Hq][d] bf16 device: the queries the merged query is
+ *           formed from (current or draft block; [EA] uses a draft block).
+ *   k_cache [N][Hkv][L_max][d] bf16: device memory or mapped pinned host.
+ *   ctx_len [N] int32 device: cached positions per sequence.
+ *   cand    [N][Hkv][C] int32 device out: the min(C, ctx) positions with
+ *           the largest stage-1 score s1[j] = sum over the group's heads of
+ *           softmax_j(qbar_h . k_j / sqrt(d)) ([SPD] S_tgt), ascending,
+ *           padded with -1.
+ *   n_cand  [N][Hkv] int32 device out: min(C, ctx). */
+herald_status herald_select_stage1(herald_dims dims, const uint16_t *q_merge,
+                                   const uint16_t *k_cache, const int32_t *ctx_len, int C,
+                                   int32_t *cand, int32_t *n_cand, void *ws, size_t ws_bytes,
+                                   void *stream);
+
+/* Stage 2 of the selection [V3] plus sink/local [SPD InfLLM-V2 decomposition].
+ *   q_block [N][B][Hq][d] bf16 device: the real queries of the block being
+ *           selected for.
+ *   cand, n_cand as written by herald_select_stage1 (C = its row length).
+ *   Score s2[c] = sum over the B*G rows of the group of softmax over the
+ *   candidates of q . k_cand / sqrt(d).  Keeps the min(K, n_cand) best, adds
+ *   positions [0, sink) and [ctx - local, ctx) clipped to [0, ctx), no
+ *   duplicates, ascending.
+ *   idx     [N][Hkv][P_max] int32 device out, -1 padded (P_max >= K+sink+local)
+ *   n_sel   [N][Hkv] int32 device out. */
+herald_status herald_select_stage2(herald_dims dims, const uint16_t *q_block,
+                                   const uint16_t *k_cache, const int32_t *ctx_len,
+                                   const int32_t *cand, const int32_t *n_cand, int C, int K,
+                                   int sink, int local, int P_max, int32_t *idx,
+                                   int32_t *n_sel, void *ws, size_t ws_bytes, void *stream);
+
+/* Both stages in order (candidates kept in the workspace).  Passing
+ * q_merge == q_block is the non-speculative case. */
+herald_status herald_select(herald_dims dims, const uint16_t *q_merge, const uint16_t *q_block,
+                            const uint16_t *k_cache, const int32_t *ctx_len, int C, int K,
+                            int sink, int local, int P_max, int32_t *idx, int32_t *n_sel,
+                            void *ws, size_t ws_bytes, void *stream);
+
+/* Gathers the selected rows into one buffer of the double-buffered sparse
+ * KV pool [EA]:  pool[n][g][s] = cache[n][g][idx[n][g][s]] for s < n_sel,
+ * zero rows for n_sel <= s < P_max.
+ *   k_cache, v_cache [N][Hkv][L_max][d] bf16, device or mapped pinned host.
+ *   pool_k, pool_v   [N][Hkv][P_max][d] bf16 device out. */
+herald_status herald_gather(herald_dims dims, const int32_t *idx, const int32_t *n_sel,
+                            int P_max, const uint16_t *k_cache, const uint16_t *v_cache,
+                            uint16_t *pool_k, uint16_t *pool_v, void *stream);
+
+/* One denoising step of sparse block attention over the pool [EA][V3]:
+ * every query (n, b, h) attends, without a mask, to the n_sel pool rows of
+ * KV head h/G followed by the B block keys of that head (bidirectional
+ * inside the block).
+ *   q        [N][B][Hq][d] bf16 device     block_k, block_v [N][B][Hkv][d]
+ *   pool_k/v [N][Hkv][P_max][d] bf16 device, as written by herald_gather
+ *   n_sel    [N][Hkv] int32 device
+ *   out      [N][B][Hq][d] bf16 device out
+ *   scale    softmax scale; 0 selects 1/sqrt(d). */
+herald_status herald_denoise_attn(herald_dims dims, const uint16_t *q, const uint16_t *pool_k,
+                                  const uint16_t *pool_v, const int32_t *n_sel, int P_max,
+                                  const uint16_t *block_k, const uint16_t *block_v,
+                                  uint16_t *out, float scale, void *ws, size_t ws_bytes,
+                                  void *stream);
+
+/* Appends a decoded block to the cache ([V3]: the cache grows with every
+ * decoded block):  cache[n][g][ctx_len[n] + b] = block[n][b][g] for b < B
+ * (rows at or past L_max are skipped), then, if advance != 0,
+ * ctx_len[n] = min(ctx_len[n] + B, L_max).
+ *   block_k, block_v [N][B][Hkv][d] bf16 device
+ *   k_cache, v_cache [N][Hkv][L_max][d] bf16, device or mapped pinned host
+ *   ctx_len [N] int32 device (read, and updated when advance != 0). */
+herald_status herald_append_kv(herald_dims dims, const uint16_t *block_k,
+                               const uint16_t *block_v, int32_t *ctx_len, uint16_t *k_cache,
+                               uint16_t *v_cache, int advance, void *stream);
+
+/* Kernel tracing, a profiling aid that is off by default.  While enabled on
+ * the calling host thread, every kernel the library launches is bracketed
+ * by two caller-created CUDA events (cudaEvent_t, timing enabled) recorded
+ * on the launch stream: launch i records events[2i] before and events[2i+1]
+ * after the kernel; launches past `capacity` are not traced.  With
+ * external != 0 the events are recorded with cudaEventRecordExternal, so a
+ * stream capture turns them into event-record nodes of the CUDA graph.
+ * herald_trace_end() stops tracing and returns the number of launches
+ * traced; herald_trace_name(i) gives the kernel name of launch i (valid
+ * until the next herald_trace_begin on this thread). */
+herald_status herald_trace_begin(void **events, int capacity, int external);
+int herald_trace_end(void);
+const char *herald_trace_name(int i);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HERALD_H */

@@ -1,0 +1,116 @@
+"""CPU-side checks of the C-ABI library: it loads, exports every symbol the
+header declares, and rejects invalid arguments on the host without touching
+a GPU (every failing call below returns before any CUDA call)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from block_diffusion_sparse_gb300 import herald as H
+from block_diffusion_sparse_gb300.workloads import ALL, QWEN_32K
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _built():
+    if not os.path.exists(H.LIB_PATH):
+        from block_diffusion_sparse_gb300 import build
+        build.build()
+    return H.lib()
+
+
+def _declared_symbols():
+    src = open(os.path.join(ROOT, "include", "herald.h")).read()
+    return sorted(set(re.findall(r"\b(herald_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declarations_are_all_exported():
+    lib = _built()
+    names = _declared_symbols()
+    assert set(names) == set(H.EXPORTS), names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_workspace_size_is_positive_and_monotone():
+    _built()
+    d = H.dims_of(QWEN_32K)
+    a = H.herald_workspace_size(d, 4096, 1344)
+    b = H.herald_workspace_size(d, 8192, 1344)
+    c = H.herald_workspace_size(d, 4096, 2688)
+    assert 0 < a < b and a < c
+    for w in ALL.values():
+        assert H.herald_workspace_size(H.dims_of(w), w.C, w.P) > 0
+
+
+@pytest.mark.parametrize("bad,status", [
+    (dict(d=96), 2),
+    (dict(Hq=30, Hkv=4), 2),
+    (dict(Hq=36, Hkv=4), 2),      # G = 9 > 8
+    (dict(B=64), 2),              # B*G = 448 > 256
+    (dict(N=0), 1),
+    (dict(L_max=0), 1),
+])
+def test_bad_dims_rejected(bad, status):
+    _built()
+    base = dict(N=1, Hq=28, Hkv=4, d=128, B=32, L_max=1024)
+    base.update(bad)
+    d = H.dims(**base)
+    assert H.herald_workspace_size(d, 256, 512) == 0
+    with pytest.raises(H.HeraldError) as e:
+        H.herald_select(d, 16, 16, 16, 16, 256, 128, 16, 64, 512, 16, 16, 16, ws_bytes=1 << 30)
+    assert e.value.status == status
+
+
+def test_argument_errors_rejected_before_launch():
+    _built()
+    d = H.dims(1, 4, 1, 64, 16, 2048)
+    ok = 1 << 12  # aligned fake address; never dereferenced on these paths
+    ws_need = H.herald_workspace_size(d, 256, 208)
+    cases = [
+        (dict(q_merge=0), 1),           # NULL pointer
+        (dict(q_block=ok + 8), 1),      # misaligned
+        (dict(K=300), 1),               # K > C
+        (dict(sink=-1), 1),
+        (dict(P_max=100), 1),           # P_max < K + sink + local
+        (dict(C=0), 2),
+        (dict(C=20000), 2),
+        (dict(ws_bytes=ws_need - 1), 3),
+    ]
+    for over, status in cases:
+        a = dict(q_merge=ok, q_block=ok, k_cache=ok, ctx=ok, C=256, K=128, sink=16, local=64,
+                 P_max=208, idx=ok, n_sel=ok, ws=ok, ws_bytes=ws_need)
+        a.update(over)
+        with pytest.raises(H.HeraldError) as e:
+            H.herald_select(d, a["q_merge"], a["q_block"], a["k_cache"], a["ctx"], a["C"], a["K"],
+                            a["sink"], a["local"], a["P_max"], a["idx"], a["n_sel"], a["ws"],
+                            a["ws_bytes"])
+        assert e.value.status == status, (over, e.value)
+        assert H.lib().herald_last_error().decode()
+
+
+def test_attention_and_gather_argument_errors():
+    _built()
+    d = H.dims(1, 4, 1, 64, 16, 2048)
+    ok = 1 << 12
+    ws = H.herald_workspace_size(d, 1, 208)
+    with pytest.raises(H.HeraldError) as e:
+        H.herald_denoise_attn(d, ok, ok, ok, ok, 208, ok, ok, 0, 0.0, ok, ws)
+    assert e.value.status == 1
+    with pytest.raises(H.HeraldError) as e:
+        H.herald_denoise_attn(d, ok, ok, ok, ok, 208, ok, ok, ok, -1.0, ok, ws)
+    assert e.value.status == 1
+    with pytest.raises(H.HeraldError) as e:
+        H.herald_gather(d, ok, ok, 0, ok, ok, ok, ok)
+    assert e.value.status == 1
+    with pytest.raises(H.HeraldError) as e:
+        H.herald_append_kv(d, ok, ok, ok, ok, ok + 4)
+    assert e.value.status == 1
+
+
+def test_status_strings():
+    _built()
+    for s in range(5):
+        assert H.herald_status_string(s)
+    assert H.herald_status_string(99) == "unknown status"

@@ -1,0 +1,365 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle, on
+the same seeded inputs.  Each stage is checked in isolation (stage 2 gets
+the oracle's candidates, attention gets the GPU's selected indices), so a
+tie-band swap upstream cannot cascade.  Index outputs: set-equal except
+entries within the tie band; gathers and appends: bit-exact; attention:
+max abs error <= 2e-2."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import oracle
+from block_diffusion_sparse_gb300 import herald as H
+from block_diffusion_sparse_gb300 import synth
+from block_diffusion_sparse_gb300.workloads import LLAMA_64K, QWEN_32K, TINY, Workload
+from helpers import ATTN_ATOL, BAND, assert_sets_within_band, bf16_dev_to_f64, dev, f64, segment
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    H.lib()
+
+
+def _case(name, **kw):
+    base = dict(N=1, Hq=4, Hkv=1, d=64, L=2048, B=16, T=2, C=256, K=128, S=16, W=64,
+                planted="points", n_planted=8, index=11, extra_rows=16)
+    base.update(kw)
+    return Workload(name, **base)
+
+
+CASES = [
+    TINY.scaled(T=2),
+    _case("g7-d128-ragged", Hq=14, Hkv=2, d=128, L=5000, B=32, C=512, K=200, S=8, W=40,
+          n_planted=20, index=12),
+    _case("g4-d128-n2", N=2, Hq=8, Hkv=2, d=128, L=3001, B=32, C=300, K=100, S=4, W=33,
+          n_planted=12, index=13),
+    _case("g1-b1", Hq=2, Hkv=2, d=64, L=700, B=1, C=130, K=64, S=0, W=0, n_planted=4, index=14),
+    _case("g8-b32-rows256", Hq=16, Hkv=2, d=128, L=1500, B=32, C=256, K=128, S=16, W=16,
+          n_planted=6, index=15),
+    _case("ctx-below-c", Hq=4, Hkv=1, d=128, L=100, B=8, C=256, K=64, S=16, W=16,
+          n_planted=2, index=16),
+]
+
+
+class Run:
+    """Uploads a workload and runs the CUDA path step by step."""
+
+    def __init__(self, w: Workload, x=None, ctx=None):
+        self.w, self.x = w, (x if x is not None else synth.make_layer(w))
+        if ctx is not None:
+            self.x["ctx"] = np.asarray(ctx, np.int32)
+        x = self.x
+        self.d = H.dims_of(w)
+        self.q_merge = dev(x["q_merge"])
+        self.q_steps = dev(x["q_steps"])
+        self.k = dev(x["k_cache"])
+        self.v = dev(x["v_cache"])
+        self.bk = dev(x["block_k"])
+        self.bv = dev(x["block_v"])
+        self.ctx = dev(x["ctx"])
+        self.P = w.P
+        self.ws_bytes = H.herald_workspace_size(self.d, w.C, self.P)
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device="cuda")
+        NG = (w.N, w.Hkv)
+        self.cand = torch.full((*NG, w.C), -7, dtype=torch.int32, device="cuda")
+        self.n_cand = torch.zeros(NG, dtype=torch.int32, device="cuda")
+        self.idx = torch.full((*NG, self.P), -7, dtype=torch.int32, device="cuda")
+        self.n_sel = torch.zeros(NG, dtype=torch.int32, device="cuda")
+        self.pool_k = torch.full((*NG, self.P, w.d), 99, dtype=torch.int16, device="cuda")
+        self.pool_v = torch.full((*NG, self.P, w.d), 99, dtype=torch.int16, device="cuda")
+        self.out = torch.zeros((w.N, w.B, w.Hq, w.d), dtype=torch.int16, device="cuda")
+
+    def stage1(self):
+        H.herald_select_stage1(self.d, self.q_merge, self.k, self.ctx, self.w.C, self.cand,
+                               self.n_cand, self.ws)
+
+    def stage2(self, cand=None, n_cand=None):
+        c = self.cand if cand is None else dev(np.asarray(cand, np.int32))
+        nc = self.n_cand if n_cand is None else dev(np.asarray(n_cand, np.int32))
+        w = self.w
+        H.herald_select_stage2(self.d, self.q_steps[0], self.k, self.ctx, c, nc, w.C, w.K, w.S,
+                               w.W, self.P, self.idx, self.n_sel, self.ws)
+
+    def select(self):
+        w = self.w
+        H.herald_select(self.d, self.q_merge, self.q_steps[0], self.k, self.ctx, w.C, w.K, w.S,
+                        w.W, self.P, self.idx, self.n_sel, self.ws)
+
+    def gather(self):
+        H.herald_gather(self.d, self.idx, self.n_sel, self.P, self.k, self.v, self.pool_k,
+                        self.pool_v)
+
+    def attn(self, t):
+        H.herald_denoise_attn(self.d, self.q_steps[t], self.pool_k, self.pool_v, self.n_sel,
+                              self.P, self.bk[t], self.bv[t], self.out, 0.0, self.ws)
+
+    def error_word(self):
+        return H.herald_workspace_error(self.ws)
+
+
+def _oracle_stage1(x):
+    qbar = oracle.merged_query(f64(x["q_merge"]))
+    _, _, s1 = oracle.stage1_scores(qbar, f64(x["k_cache"]), x["ctx"])
+    return s1
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_stage1_candidates(w):
+    r = Run(w)
+    r.stage1()
+    torch.cuda.synchronize()
+    assert r.error_word() == 0
+    s1 = _oracle_stage1(r.x)
+    cand_o, nc_o = oracle.topc(s1, r.x["ctx"], w.C)
+    cand, nc = r.cand.cpu().numpy(), r.n_cand.cpu().numpy()
+    np.testing.assert_array_equal(nc, nc_o)
+    for n in range(w.N):
+        for g in range(w.Hkv):
+            m = int(nc_o[n, g])
+            assert_sets_within_band(cand[n, g, :m], cand_o[n, g, :m], s1[n, g], m,
+                                    f"{w.name} stage1 n={n} g={g}")
+            assert (cand[n, g, m:] == -1).all()
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_stage2_from_oracle_candidates(w):
+    r = Run(w)
+    x = r.x
+    s1 = _oracle_stage1(x)
+    cand_o, nc_o = oracle.topc(s1, x["ctx"], w.C)
+    r.stage2(cand_o, nc_o)
+    torch.cuda.synchronize()
+    assert r.error_word() == 0
+    s2 = oracle.stage2_scores(f64(x["q_steps"][0]), f64(x["k_cache"]), cand_o, nc_o)
+    idx_o, ns_o = oracle.select_final(x["ctx"], w.L_max, cand_o, nc_o, s2, w.K, w.S, w.W, w.P)
+    idx, ns = r.idx.cpu().numpy(), r.n_sel.cpu().numpy()
+    for n in range(w.N):
+        for g in range(w.Hkv):
+            check_selection(idx[n, g], int(ns[n, g]), idx_o[n, g], int(ns_o[n, g]),
+                            cand_o[n, g], nc_o[n, g], s2[n, g], w, int(x["ctx"][n]),
+                            f"{w.name} n={n} g={g}")
+
+
+def check_selection(idx, ns, idx_o, ns_o, cand_o, nc_o, s2, w, L, what):
+    """Selected set vs the oracle's: ascending, sink and local present, -1
+    padding, and every differing position a candidate whose stage-2 score
+    lies within the tie band of the oracle's K-th score."""
+    got = idx[:ns].tolist()
+    assert got == sorted(set(got)), f"{what}: not ascending / duplicated"
+    sink_end = min(w.S, L)
+    local_begin = max(L - w.W, sink_end)
+    assert got[:sink_end] == list(range(sink_end)), what
+    assert got[len(got) - (L - local_begin):] == list(range(local_begin, L)), what
+    assert (idx[ns:] == -1).all(), what
+    m = int(nc_o)
+    Ke = min(w.K, m)
+    score = {int(cand_o[i]): float(s2[i]) for i in range(m)}
+    if Ke == 0:
+        assert ns == ns_o, what
+        return 0
+    thr = sorted(s2[:m], reverse=True)[Ke - 1]
+    diff = set(got) ^ set(idx_o[:ns_o].tolist())
+    bad = [j for j in diff if j not in score or score[j] <= 0 or thr <= 0
+           or abs(np.log(score[j]) - np.log(thr)) > BAND]
+    assert not bad, f"{what}: {len(bad)} selected positions outside the tie band: {bad[:5]}"
+    assert abs(ns - ns_o) <= len(diff), what
+    return len(diff)
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_gather_and_attention(w):
+    r = Run(w)
+    r.select()
+    r.gather()
+    torch.cuda.synchronize()
+    idx, ns = r.idx.cpu().numpy(), r.n_sel.cpu().numpy()
+    k, v = r.x["k_cache"], r.x["v_cache"]
+    pk = r.pool_k.cpu().numpy().view(np.uint16)
+    pv = r.pool_v.cpu().numpy().view(np.uint16)
+    for n in range(w.N):
+        for g in range(w.Hkv):
+            m = int(ns[n, g])
+            np.testing.assert_array_equal(pk[n, g, :m], k[n, g, idx[n, g, :m]])
+            np.testing.assert_array_equal(pv[n, g, :m], v[n, g, idx[n, g, :m]])
+            assert (pk[n, g, m:] == 0).all() and (pv[n, g, m:] == 0).all()
+    for t in range(w.T):
+        r.attn(t)
+        torch.cuda.synchronize()
+        out = bf16_dev_to_f64(r.out)
+        ref = oracle.sparse_attn(f64(r.x["q_steps"][t]), f64(k), f64(v), idx, ns,
+                                 f64(r.x["block_k"][t]), f64(r.x["block_v"][t]))
+        err = np.abs(out - ref).max()
+        assert err <= ATTN_ATOL, f"{w.name} step {t}: max abs err {err}"
+    assert r.error_word() == 0
+
+
+def test_dense_equals_sparse_when_budget_covers_context():
+    w = _case("dense", Hq=8, Hkv=2, d=128, L=600, B=16, C=600, K=600, S=0, W=0,
+              n_planted=3, index=17)
+    r = Run(w)
+    r.select()
+    r.gather()
+    r.attn(0)
+    torch.cuda.synchronize()
+    assert r.n_sel.cpu().numpy().tolist() == [[600, 600]]
+    assert (r.idx.cpu().numpy()[:, :, :600] == np.arange(600)).all()
+    x = r.x
+    dense = oracle.dense_attn(f64(x["q_steps"][0]), f64(x["k_cache"]), f64(x["v_cache"]),
+                              x["ctx"], f64(x["block_k"][0]), f64(x["block_v"][0]))
+    assert np.abs(bf16_dev_to_f64(r.out) - dense).max() <= ATTN_ATOL
+
+
+def test_empty_context_and_block_only_attention():
+    w = _case("empty", Hq=4, Hkv=1, d=64, L=512, B=16, C=64, K=32, S=4, W=4, index=18)
+    r = Run(w, ctx=[0])
+    r.select()
+    r.gather()
+    r.attn(0)
+    torch.cuda.synchronize()
+    assert r.n_sel.cpu().numpy().tolist() == [[0]]
+    assert (r.idx.cpu().numpy() == -1).all()
+    x = r.x
+    ref = oracle.dense_attn(f64(x["q_steps"][0]), f64(x["k_cache"]), f64(x["v_cache"]),
+                            x["ctx"], f64(x["block_k"][0]), f64(x["block_v"][0]))
+    assert np.abs(bf16_dev_to_f64(r.out) - ref).max() <= ATTN_ATOL
+
+
+def test_per_sequence_context_lengths():
+    w = _case("mixed-ctx", N=3, Hq=8, Hkv=2, d=128, L=2000, B=16, C=200, K=64, S=8, W=16,
+              n_planted=4, index=19)
+    r = Run(w, ctx=[2000, 777, 65])
+    r.select()
+    torch.cuda.synchronize()
+    x = r.x
+    s1 = _oracle_stage1(x)
+    cand_o, nc_o = oracle.topc(s1, x["ctx"], w.C)
+    s2 = oracle.stage2_scores(f64(x["q_steps"][0]), f64(x["k_cache"]), cand_o, nc_o)
+    idx_o, ns_o = oracle.select_final(x["ctx"], w.L_max, cand_o, nc_o, s2, w.K, w.S, w.W, w.P)
+    idx, ns = r.idx.cpu().numpy(), r.n_sel.cpu().numpy()
+    np.testing.assert_array_equal(ns, ns_o)
+    mism = (idx != idx_o).sum()
+    assert mism <= 2, f"{mism} index slots differ"
+
+
+def test_planted_heavy_hitters_selected_and_deterministic():
+    w = TINY
+    r = Run(w)
+    r.select()
+    torch.cuda.synchronize()
+    a = r.idx.clone()
+    r.select()
+    torch.cuda.synchronize()
+    assert torch.equal(a, r.idx)
+    sel = set(a.cpu().numpy()[0, 0, : int(r.n_sel[0, 0])].tolist())
+    assert set(int(p) for p in r.x["planted"][0]) <= sel
+    r.gather()
+    r.attn(0)
+    torch.cuda.synchronize()
+    o1 = r.out.clone()
+    r.attn(0)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, r.out)
+
+
+def test_append_matches_oracle_bit_exact():
+    w = _case("append", N=2, Hq=8, Hkv=2, d=128, L=300, B=16, C=64, K=32, S=4, W=4,
+              extra_rows=40, index=20)
+    r = Run(w, ctx=[300, 330])
+    H.herald_append_kv(r.d, r.bk[0], r.bv[0], r.ctx, r.k, r.v, advance=True)
+    torch.cuda.synchronize()
+    c2, k2, v2 = oracle.append(r.x["ctx"], f64(r.x["block_k"][0]), f64(r.x["block_v"][0]),
+                               f64(r.x["k_cache"]), f64(r.x["v_cache"]))
+    # the second sequence overflows L_max = 340: rows past it are skipped and
+    # the context is capped
+    assert r.ctx.cpu().numpy().tolist() == [316, 340]
+    kk = synth.bf16_to_f64(r.k.cpu().numpy().view(np.uint16))
+    vv = synth.bf16_to_f64(r.v.cpu().numpy().view(np.uint16))
+    np.testing.assert_array_equal(kk, k2)
+    np.testing.assert_array_equal(vv, v2)
+
+
+def test_host_resident_cache_matches_device_cache():
+    w = _case("host-kv", Hq=8, Hkv=2, d=128, L=4096, B=32, C=512, K=128, S=16, W=64,
+              n_planted=10, index=21)
+    r = Run(w)
+    r.select()
+    r.gather()
+    torch.cuda.synchronize()
+    idx_dev, ns_dev = r.idx.clone(), r.n_sel.clone()
+    pk_dev = r.pool_k.clone()
+    kh = torch.from_numpy(r.x["k_cache"].view(np.int16)).pin_memory()
+    vh = torch.from_numpy(r.x["v_cache"].view(np.int16)).pin_memory()
+    w_ = r.w
+    H.herald_select(r.d, r.q_merge, r.q_steps[0], kh, r.ctx, w_.C, w_.K, w_.S, w_.W, r.P, r.idx,
+                    r.n_sel, r.ws)
+    H.herald_gather(r.d, r.idx, r.n_sel, r.P, kh, vh, r.pool_k, r.pool_v)
+    torch.cuda.synchronize()
+    assert r.error_word() == 0
+    assert torch.equal(idx_dev, r.idx) and torch.equal(ns_dev, r.n_sel)
+    assert torch.equal(pk_dev, r.pool_k)
+
+
+@pytest.mark.parametrize("w", [QWEN_32K], ids=lambda w: w.name)
+def test_full_size_qwen_layer(w):
+    """The benchmarked workload at full size: every stage against the oracle."""
+    r = Run(w.scaled(T=2))
+    x = r.x
+    r.stage1()
+    torch.cuda.synchronize()
+    s1 = _oracle_stage1(x)
+    cand_o, nc_o = oracle.topc(s1, x["ctx"], w.C)
+    cand = r.cand.cpu().numpy()
+    for g in range(w.Hkv):
+        assert_sets_within_band(cand[0, g], cand_o[0, g], s1[0, g], w.C, f"stage1 g={g}")
+    planted = set(int(p) for p in x["planted"][0])
+    for g in range(w.Hkv):
+        assert planted <= set(cand[0, g].tolist())
+    r.stage2(cand_o, nc_o)
+    r.gather()
+    r.attn(1)
+    torch.cuda.synchronize()
+    assert r.error_word() == 0
+    idx, ns = r.idx.cpu().numpy(), r.n_sel.cpu().numpy()
+    s2 = oracle.stage2_scores(f64(x["q_steps"][0]), f64(x["k_cache"]), cand_o, nc_o)
+    idx_o, ns_o = oracle.select_final(x["ctx"], w.L_max, cand_o, nc_o, s2, w.K, w.S, w.W, w.P)
+    for g in range(w.Hkv):
+        check_selection(idx[0, g], int(ns[0, g]), idx_o[0, g], int(ns_o[0, g]), cand_o[0, g],
+                        nc_o[0, g], s2[0, g], w, w.L, f"qwen g={g}")
+        assert planted <= set(idx[0, g, : ns[0, g]].tolist())
+    out = bf16_dev_to_f64(r.out)
+    ref = oracle.sparse_attn(f64(x["q_steps"][1]), f64(x["k_cache"]), f64(x["v_cache"]), idx, ns,
+                             f64(x["block_k"][1]), f64(x["block_v"][1]))
+    assert np.abs(out - ref).max() <= ATTN_ATOL
+
+
+def test_full_size_llama_layer_sampled_segments():
+    """4 x 64K context, 8 KV heads: the GPU runs the whole batch; the oracle
+    checks two sampled (sequence, KV head) segments end to end."""
+    w = LLAMA_64K.scaled(T=1)
+    r = Run(w)
+    r.select()
+    r.gather()
+    r.attn(0)
+    torch.cuda.synchronize()
+    assert r.error_word() == 0
+    idx, ns = r.idx.cpu().numpy(), r.n_sel.cpu().numpy()
+    out = bf16_dev_to_f64(r.out)
+    for n, g in ((0, 0), (3, 7)):
+        xs = segment(r.x, w, n, g)
+        qbar = oracle.merged_query(f64(xs["q_merge"]))
+        _, _, s1 = oracle.stage1_scores(qbar, f64(xs["k_cache"]), xs["ctx"])
+        cand_o, nc_o = oracle.topc(s1, xs["ctx"], w.C)
+        planted = set(int(p) for p in r.x["planted"][n])
+        assert planted <= set(idx[n, g, : ns[n, g]].tolist())
+        ref = oracle.sparse_attn(f64(xs["q_steps"][0]), f64(xs["k_cache"]), f64(xs["v_cache"]),
+                                 idx[n:n + 1, g:g + 1], ns[n:n + 1, g:g + 1],
+                                 f64(xs["block_k"][0]), f64(xs["block_v"][0]))
+        hs = slice(g * w.G, (g + 1) * w.G)
+        assert np.abs(out[n:n + 1, :, hs] - ref).max() <= ATTN_ATOL
+        s2 = oracle.stage2_scores(f64(xs["q_steps"][0]), f64(xs["k_cache"]), cand_o, nc_o)
+        idx_o, ns_o = oracle.select_final(xs["ctx"], w.L_max, cand_o, nc_o, s2, w.K, w.S, w.W, w.P)
+        assert len(set(idx[n, g, : ns[n, g]].tolist()) ^ set(idx_o[0, 0, : ns_o[0, 0]].tolist())) <= 4
