@@ -405,20 +405,57 @@ __device__ void find_bin_from_top(const uint32_t* h, int nb, uint32_t need, uint
 }
 
 // ============================================================ topc_finish
-// One CTA of 1024 threads per (n, g).  Radix select of the C-th largest s1
-// in three digits (12 bits from the global histogram, then 11 and 8 bits
-// re-counted over the segment), then an ordered compaction that keeps every
-// s1 above the threshold and the lowest-position ties.
+// One CTA of 1024 threads per (n, g).  Radix select of the C-th largest s1:
+// the first 12-bit digit comes from the global histogram; the members of
+// that bin are collected into shared memory (bounded; a global two-digit
+// fallback handles overflow) and the remaining 19 bits are resolved there.
+// The ordered compaction then keeps every s1 above the threshold plus the
+// lowest-position ties, with one two-counter block scan.
 constexpr int kSelThreads = 1024;
+constexpr int kTieCap = 6144;
+
+// Block-wide exclusive scan of two counters at once (1024 threads).
+__device__ __forceinline__ void block_excl_scan2(uint32_t a, uint32_t b, uint32_t* wa,
+                                                 uint32_t* wb, uint32_t& ea, uint32_t& eb,
+                                                 uint32_t& ta, uint32_t& tb) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = a, y = b;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t xa = __shfl_up_sync(0xffffffffu, x, o);
+    const uint32_t yb = __shfl_up_sync(0xffffffffu, y, o);
+    if (lane >= o) { x += xa; y += yb; }
+  }
+  if (lane == 31) { wa[warp] = x; wb[warp] = y; }
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t u = wa[lane], v = wb[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t ua = __shfl_up_sync(0xffffffffu, u, o);
+      const uint32_t vb = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) { u += ua; v += vb; }
+    }
+    wa[lane] = u;
+    wb[lane] = v;
+  }
+  __syncthreads();
+  ea = (warp ? wa[warp - 1] : 0u) + x - a;
+  eb = (warp ? wb[warp - 1] : 0u) + y - b;
+  ta = wa[31];
+  tb = wb[31];
+  __syncthreads();
+}
 
 __global__ void __launch_bounds__(kSelThreads)
     topc_finish_kernel(const float* __restrict__ s1, const uint32_t* __restrict__ hist,
                        const int32_t* __restrict__ ctx, int Hkv, int L_max, int L_pad, int C,
                        int32_t* __restrict__ cand, int32_t* __restrict__ n_cand) {
   __shared__ uint32_t h[kHistBins];
-  __shared__ uint32_t wt[32];
+  __shared__ uint32_t tie_v[kTieCap];
+  __shared__ uint32_t wt[32], wt2[32];
   __shared__ int s_bin;
-  __shared__ uint32_t s_above;
+  __shared__ uint32_t s_above, s_cnt;
   const int seg = blockIdx.x, n = seg / Hkv;
   const int L = min(max(ctx[n], 0), L_max);
   const int Ce = min(C, L);
@@ -431,48 +468,80 @@ __global__ void __launch_bounds__(kSelThreads)
     return;
   }
   // digit 1: bits [30:19] from the global histogram
-  for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h[i] = hist[size_t(seg) * kHistBins + i];
+  for (int i = threadIdx.x; i < kHistBins; i += kSelThreads)
+    h[i] = hist[size_t(seg) * kHistBins + i];
+  if (threadIdx.x == 0) s_cnt = 0;
   __syncthreads();
   uint32_t need = uint32_t(Ce);
   find_bin_from_top<kSelThreads>(h, kHistBins, need, wt, &s_bin, &s_above);
-  uint32_t prefix = uint32_t(s_bin);
+  const uint32_t b1 = uint32_t(s_bin);
   need -= s_above;
+  // collect the low 19 bits of the members of bin b1
+  for (int j = threadIdx.x; j < L; j += kSelThreads) {
+    const uint32_t v = sv[j];
+    if ((v >> 19) == b1) {
+      const uint32_t slot = atomicAdd(&s_cnt, 1u);
+      if (slot < kTieCap) tie_v[slot] = v & 0x7FFFFu;
+    }
+  }
+  __syncthreads();
+  const uint32_t cnt = s_cnt;
+  const bool in_smem = cnt <= uint32_t(kTieCap);
   // digit 2: bits [18:8]
   for (int i = threadIdx.x; i < 2048; i += kSelThreads) h[i] = 0u;
   __syncthreads();
-  for (int j = threadIdx.x; j < L; j += kSelThreads) {
-    const uint32_t v = sv[j];
-    if ((v >> 19) == prefix) atomicAdd(&h[(v >> 8) & 2047u], 1u);
+  if (in_smem) {
+    for (uint32_t i = threadIdx.x; i < cnt; i += kSelThreads) atomicAdd(&h[tie_v[i] >> 8], 1u);
+  } else {
+    for (int j = threadIdx.x; j < L; j += kSelThreads) {
+      const uint32_t v = sv[j];
+      if ((v >> 19) == b1) atomicAdd(&h[(v >> 8) & 2047u], 1u);
+    }
   }
   __syncthreads();
   find_bin_from_top<kSelThreads>(h, 2048, need, wt, &s_bin, &s_above);
-  prefix = (prefix << 11) | uint32_t(s_bin);
+  const uint32_t b2 = uint32_t(s_bin);
   need -= s_above;
   // digit 3: bits [7:0]
   for (int i = threadIdx.x; i < 256; i += kSelThreads) h[i] = 0u;
   __syncthreads();
-  for (int j = threadIdx.x; j < L; j += kSelThreads) {
-    const uint32_t v = sv[j];
-    if ((v >> 8) == prefix) atomicAdd(&h[v & 255u], 1u);
+  if (in_smem) {
+    for (uint32_t i = threadIdx.x; i < cnt; i += kSelThreads) {
+      const uint32_t v = tie_v[i];
+      if ((v >> 8) == b2) atomicAdd(&h[v & 255u], 1u);
+    }
+  } else {
+    const uint32_t pre = (b1 << 11) | b2;
+    for (int j = threadIdx.x; j < L; j += kSelThreads) {
+      const uint32_t v = sv[j];
+      if ((v >> 8) == pre) atomicAdd(&h[v & 255u], 1u);
+    }
   }
   __syncthreads();
   find_bin_from_top<kSelThreads>(h, 256, need, wt, &s_bin, &s_above);
-  const uint32_t tau = (prefix << 8) | uint32_t(s_bin);
+  const uint32_t tau = (b1 << 19) | (b2 << 8) | uint32_t(s_bin);
   const uint32_t need_eq = need - s_above;  // ties at tau to keep, lowest position first
-  // ordered compaction
-  uint32_t base = 0, eq_base = 0;
-  for (int j0 = 0; j0 < L; j0 += kSelThreads) {
-    const int j = j0 + threadIdx.x;
-    const uint32_t v = j < L ? sv[j] : 0u;
-    const uint32_t is_eq = (j < L && v == tau) ? 1u : 0u;
-    uint32_t eq_tot;
-    const uint32_t eq_rank = eq_base + block_excl_scan<kSelThreads>(is_eq, wt, eq_tot);
-    const uint32_t sel = (j < L && (v > tau || (is_eq && eq_rank < need_eq))) ? 1u : 0u;
-    uint32_t sel_tot;
-    const uint32_t pos = base + block_excl_scan<kSelThreads>(sel, wt, sel_tot);
-    if (sel) out[pos] = j;
-    base += sel_tot;
-    eq_base += eq_tot;
+  // ordered compaction: thread t owns positions [t*E, (t+1)*E)
+  const int E = (L + kSelThreads - 1) / kSelThreads;
+  const int j0 = threadIdx.x * E, j1 = min(L, j0 + E);
+  uint32_t n_gt = 0, n_eq = 0;
+  for (int j = j0; j < j1; ++j) {
+    const uint32_t v = sv[j];
+    n_gt += v > tau;
+    n_eq += v == tau;
+  }
+  uint32_t gt_before, eq_before, gt_tot, eq_tot;
+  block_excl_scan2(n_gt, n_eq, wt, wt2, gt_before, eq_before, gt_tot, eq_tot);
+  for (int j = j0; j < j1; ++j) {
+    const uint32_t v = sv[j];
+    if (v > tau) {
+      const uint32_t pos = gt_before + min(eq_before, need_eq);
+      if (pos < uint32_t(Ce)) out[pos] = j;
+      ++gt_before;
+    } else if (v == tau) {
+      if (eq_before < need_eq && gt_before + eq_before < uint32_t(Ce)) out[gt_before + eq_before] = j;
+      ++eq_before;
+    }
   }
 }
 
@@ -546,15 +615,15 @@ __global__ void __launch_bounds__(kSelThreads)
     keep = keep && pos >= sink_end && pos < local_begin;
     uint32_t tot;
     const uint32_t at = base + block_excl_scan<kSelThreads>(keep ? 1u : 0u, wt, tot);
-    if (keep) out[sink_end + at] = pos;
+    if (keep && sink_end + int(at) < P_max) out[sink_end + at] = pos;
     base += tot;
     eq_base += eq_tot;
   }
   const int n_mid = int(base);
   for (int j = threadIdx.x; j < sink_end; j += kSelThreads) out[j] = j;
   for (int j = local_begin + threadIdx.x; j < L; j += kSelThreads)
-    out[sink_end + n_mid + (j - local_begin)] = j;
-  const int total = sink_end + n_mid + (L - local_begin);
+    if (sink_end + n_mid + (j - local_begin) < P_max) out[sink_end + n_mid + (j - local_begin)] = j;
+  const int total = min(P_max, sink_end + n_mid + (L - local_begin));
   for (int s = total + threadIdx.x; s < P_max; s += kSelThreads) out[s] = -1;
   if (threadIdx.x == 0) n_sel[seg] = total;
 }

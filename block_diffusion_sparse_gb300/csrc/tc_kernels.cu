@@ -14,6 +14,7 @@
 //                 query): S = Q K^T, P = exp(S - rowmax), O = P V
 //   attn_combine  merges the splits by their (max, sum) into bf16 out
 #include <cuda_bf16.h>
+#include <stdlib.h>
 
 #include "internal.cuh"
 #include "ptx.cuh"
@@ -482,6 +483,266 @@ __global__ void __launch_bounds__(kTcThreads)
   tmem_teardown(tbase, 256);
 }
 
+// ========================================================== attn_cluster
+// Split-KV attention whose splits are the kClusterCtas CTAs of one thread
+// block cluster per (sequence, KV head, 128-row tile).  CTA rank r owns key
+// tiles r and r + kClusterCtas (each 128 keys: pool rows, then the B block
+// rows).  Both tiles' scores share one row max, so the two P.V products
+// accumulate into one TMEM accumulator without rescaling.  The partial
+// (O, max, sum) of every CTA stays in its shared memory; after a cluster
+// barrier each CTA merges 128/kClusterCtas rows by reading its peers'
+// shared memory (distributed shared memory), and writes bf16 out.
+constexpr int kClusterCtas = 8;
+
+template <int D>
+struct AttnClCfg {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kTile = kHalves * 128 * 128;   // 128 rows x D bf16
+  static constexpr int kPT = kTile > 32768 ? kTile : 32768;  // K tile, later P (128 x 128)
+  static constexpr int kQ = 0;
+  static constexpr int kK0 = kTile, kK1 = kTile + kPT;
+  static constexpr int kV0 = kTile + 2 * kPT, kV1 = 2 * kTile + 2 * kPT;
+  static constexpr int kBytes = 3 * kTile + 2 * kPT;
+  static constexpr int kORow = D + 4;                  // fp32 row stride of the O partial
+  static constexpr int kSmem = kBytes + 1024;
+  static_assert(128 * kORow * 4 <= kTile + 2 * kPT, "O partial must fit over Q, P0, P1");
+};
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Full cluster barrier (hardware): release this CTA's shared-memory writes,
+// acquire the peers'.
+__device__ __forceinline__ void cluster_sync_all() {
+  __cluster_barrier_arrive();
+  __cluster_barrier_wait();
+}
+// Generic address of the same shared-memory object in CTA `rank` of the cluster.
+template <typename T>
+__device__ __forceinline__ const T* peer_ptr(const T* p, uint32_t rank) {
+  return static_cast<const T*>(__cluster_map_shared_rank(static_cast<const void*>(p), rank));
+}
+
+template <int D>
+__global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kTcThreads, 1)
+    attn_cluster_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ pool_k,
+                        const uint16_t* __restrict__ pool_v, const int32_t* __restrict__ n_sel,
+                        int P_max, const uint16_t* __restrict__ block_k,
+                        const uint16_t* __restrict__ block_v, int B, int Hq, int Hkv, int R,
+                        float scale, uint16_t* __restrict__ out, uint32_t* err) {
+  using Cfg = AttnClCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar[2];
+  __shared__ uint32_t tmem_base;
+  __shared__ float red_m[2][kTileM];
+  __shared__ float red_s[2][kTileM];
+  __shared__ float2 ml[kTileM];
+  uint8_t* base = align1024(smem_raw);
+  uint8_t* Qs = base + Cfg::kQ;
+  uint8_t* Ks[2] = {base + Cfg::kK0, base + Cfg::kK1};
+  uint8_t* Vs[2] = {base + Cfg::kV0, base + Cfg::kV1};
+  float* Os = reinterpret_cast<float*>(base);  // reuses Q, K0, K1 after the MMAs
+  const uint32_t rank = cluster_ctarank();
+  const int mt = blockIdx.y, seg = blockIdx.z;
+  const int n = seg / Hkv, g = seg - n * Hkv, G = Hq / Hkv;
+  const int ns = min(max(n_sel[seg], 0), P_max);
+  const int n_pool = (ns + kAttnKeys - 1) / kAttnKeys;
+  const int n_tiles = n_pool + (B + kAttnKeys - 1) / kAttnKeys;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // this CTA's tiles
+  int tiles[2], nk[2], nt = 0;
+  for (int k = 0; k < 2; ++k) {
+    const int t = int(rank) + k * kClusterCtas;
+    if (t < n_tiles) {
+      tiles[nt] = t;
+      nk[nt] = t < n_pool ? min(kAttnKeys, ns - t * kAttnKeys)
+                          : min(kAttnKeys, B - (t - n_pool) * kAttnKeys);
+      ++nt;
+    }
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_mbar_init();
+  }
+  tmem_setup(&tmem_base, 512);
+  const uint32_t tbase = tmem_base;
+  const int quad = warp & 3, ch = warp >> 2;
+  const int row = quad * 32 + lane;
+  const uint32_t trow = tbase + (uint32_t(quad * 32) << 16);
+  float m = -INFINITY, lsum = 0.f;
+
+  if (nt > 0) {
+    load_rows_sw128<D>(Qs, kTileM, kTileM, q, [&](int r) -> const uint16_t* {
+      const int rr = mt * kTileM + r;
+      if (rr >= R) return nullptr;
+      const int b = rr / G, hl = rr - (rr / G) * G;
+      return q + ((size_t(n) * B + b) * Hq + g * G + hl) * D;
+    });
+    for (int k = 0; k < nt; ++k) {
+      const int t = tiles[k], cnt = nk[k];
+      const bool pool_tile = t < n_pool;
+      const int k0 = pool_tile ? t * kAttnKeys : (t - n_pool) * kAttnKeys;
+      load_rows_sw128<D>(Ks[k], kAttnKeys, kAttnKeys, block_k, [&](int r) -> const uint16_t* {
+        if (r >= cnt) return nullptr;
+        return pool_tile ? pool_k + (size_t(seg) * P_max + k0 + r) * D
+                         : block_k + ((size_t(n) * B + k0 + r) * Hkv + g) * D;
+      });
+    }
+    cp_async_commit();
+    for (int k = 0; k < nt; ++k) {
+      const int t = tiles[k], cnt = nk[k];
+      const bool pool_tile = t < n_pool;
+      const int k0 = pool_tile ? t * kAttnKeys : (t - n_pool) * kAttnKeys;
+      load_rows_sw128<D>(Vs[k], kAttnKeys, kAttnKeys, block_v, [&](int r) -> const uint16_t* {
+        if (r >= cnt) return nullptr;
+        return pool_tile ? pool_v + (size_t(seg) * P_max + k0 + r) * D
+                         : block_v + ((size_t(n) * B + k0 + r) * Hkv + g) * D;
+      });
+    }
+    cp_async_commit();
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+    fence_proxy_async_smem();
+    __syncthreads();
+    tc_fence_after();
+    // S_k = Q K_k^T -> TMEM columns [128k, 128k + 128)
+    if (threadIdx.x == 0) {
+      constexpr uint32_t idesc = make_idesc_bf16(kTileM, kAttnKeys, false, false);
+      const uint32_t qa = smem_u32(Qs);
+      for (int k = 0; k < nt; ++k) {
+        const uint32_t ka = smem_u32(Ks[k]);
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s) {
+          const uint32_t hv = s >> 2, koff = (s & 3) * 32;
+          const uint64_t a = make_sdesc_sw128(qa + hv * (kTileM * 128) + koff, 16, 1024);
+          const uint64_t b = make_sdesc_sw128(ka + hv * (kAttnKeys * 128) + koff, 16, 1024);
+          umma_bf16(tbase + 128 * k, a, b, idesc, s > 0 ? 1u : 0u);
+        }
+      }
+      umma_commit(&bar[0]);
+    }
+    if (!mbar_wait(&bar[0], 0)) record_error(err, DEV_TIMEOUT_MMA);
+    tc_fence_after();
+    __syncwarp();
+    // scores of both tiles -> one row max
+    float x[2][64];
+    for (int k = 0; k < 2; ++k) {
+      if (k >= nt) break;
+      float v[32];
+      tmem_ld32(trow + 128 * k + ch * 64, v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[k][i] = v[i];
+      tmem_ld32(trow + 128 * k + ch * 64 + 32, v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[k][32 + i] = v[i];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        x[k][i] = (ch * 64 + i < nk[k]) ? x[k][i] * scale : -INFINITY;
+        m = fmaxf(m, x[k][i]);
+      }
+    }
+    red_m[ch][row] = m;
+    __syncthreads();
+    m = fmaxf(red_m[0][row], red_m[1][row]);
+    // P_k = exp(S_k - m) as bf16 over K_k's buffer (K-major A operand)
+    for (int k = 0; k < 2; ++k) {
+      if (k >= nt) break;
+      uint8_t* prow = Ks[k] + ch * (kTileM * 128);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        float p[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          p[e] = __expf(x[k][c * 8 + e] - m);
+          lsum += p[e];
+        }
+        uint4 pk;
+        pk.x = pack_bf16(p[0], p[1]);
+        pk.y = pack_bf16(p[2], p[3]);
+        pk.z = pack_bf16(p[4], p[5]);
+        pk.w = pack_bf16(p[6], p[7]);
+        *reinterpret_cast<uint4*>(prow + sw128_off(row, c)) = pk;
+      }
+    }
+    red_s[ch][row] = lsum;
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // O = sum_k P_k V_k -> TMEM columns [256, 256 + D)
+    if (threadIdx.x == 0) {
+      constexpr uint32_t idesc = make_idesc_bf16(kTileM, D, false, true);
+      for (int k = 0; k < nt; ++k) {
+        const uint32_t pa = smem_u32(Ks[k]), va = smem_u32(Vs[k]);
+#pragma unroll
+        for (int s = 0; s < kAttnKeys / 16; ++s) {
+          const uint32_t kh = s >> 2, koff = (s & 3) * 32;
+          const uint64_t a = make_sdesc_sw128(pa + kh * (kTileM * 128) + koff, 16, 1024);
+          const uint64_t b = make_sdesc_sw128(va + s * 2048, kAttnKeys * 128, 1024);
+          umma_bf16(tbase + 256, a, b, idesc, (k > 0 || s > 0) ? 1u : 0u);
+        }
+      }
+      umma_commit(&bar[1]);
+    }
+    if (!mbar_wait(&bar[1], 0)) record_error(err, DEV_TIMEOUT_MMA);
+    tc_fence_after();
+    __syncwarp();
+    // O partial -> shared memory (row-major fp32, padded rows)
+#pragma unroll
+    for (int k = 0; k < D / 64; ++k) {
+      float v[32];
+      const int col = ch * (D / 2) + k * 32;
+      tmem_ld32(trow + 256 + col, v);
+      float* orow = Os + row * Cfg::kORow + col;
+#pragma unroll
+      for (int i = 0; i < 32; i += 4)
+        *reinterpret_cast<float4*>(orow + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+    }
+    if (ch == 0) ml[row] = make_float2(m, red_s[0][row] + red_s[1][row]);
+  } else {
+    if (ch == 0) ml[row] = make_float2(-INFINITY, 0.f);
+  }
+  cluster_sync_all();
+  // merge: this CTA finalises rows [rank*RPC, (rank+1)*RPC)
+  constexpr int RPC = kTileM / kClusterCtas;   // 16 rows, 2 per warp
+  constexpr int E = D / 32;
+  for (int rr = warp; rr < RPC; rr += kTcThreads / 32) {
+    const int lr = int(rank) * RPC + rr;
+    const int grow = mt * kTileM + lr;
+    float M = -INFINITY;
+    float2 pm[kClusterCtas];
+#pragma unroll
+    for (int c = 0; c < kClusterCtas; ++c) {
+      pm[c] = *peer_ptr(&ml[lr], uint32_t(c));
+      M = fmaxf(M, pm[c].x);
+    }
+    float acc[E] = {};
+    float L = 0.f;
+#pragma unroll
+    for (int c = 0; c < kClusterCtas; ++c) {
+      if (pm[c].x == -INFINITY) continue;
+      const float wgt = __expf(pm[c].x - M);
+      L += wgt * pm[c].y;
+      const float* o = peer_ptr(Os + lr * Cfg::kORow + lane * E, uint32_t(c));
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] += wgt * o[e];
+    }
+    if (grow < R) {
+      const int b = grow / G, h = g * G + (grow - (grow / G) * G);
+      uint16_t* dst = out + ((size_t(n) * B + b) * Hq + h) * D + lane * E;
+      const float inv = 1.f / L;
+#pragma unroll
+      for (int e = 0; e < E; e += 2)
+        *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16(acc[e] * inv, acc[e + 1] * inv);
+    }
+  }
+  cluster_sync_all();  // peers may still be reading this CTA's partial
+  tmem_teardown(tbase, 512);
+}
+
 // =========================================================== attn_combine
 // One warp per output row (n, b, h); lane owns D/32 consecutive features.
 template <int D>
@@ -519,52 +780,68 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// The cluster kernel covers up to 2 * kClusterCtas key tiles (P_max + B up
+// to 2048 keys); larger pools use the split kernel plus a combine pass.
+// HERALD_ATTN_SPLIT=1 in the environment forces the split path (testing).
+static bool force_split() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("HERALD_ATTN_SPLIT");
+    v = (e && e[0] == '1') ? 1 : 0;
+  }
+  return v == 1;
+}
+
+template <int D>
+static cudaError_t launch_attn_t(const herald_dims& dm, const uint16_t* q, const uint16_t* pool_k,
+                                 const uint16_t* pool_v, const int32_t* n_sel, int P_max,
+                                 const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
+                                 float scale, const WsLayout& w, float* opart, float2* ml,
+                                 uint32_t* err, cudaStream_t st) {
+  const int segs = dm.N * dm.Hkv;
+  cudaError_t e;
+  static bool attr = false;
+  if (!attr) {
+    e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             AttnCfg<D>::kSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(attn_cluster_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             AttnClCfg<D>::kSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  if (w.splits <= 2 * kClusterCtas && !force_split()) {
+    trace_before(st, "attn_cluster_kernel");
+    attn_cluster_kernel<D><<<dim3(kClusterCtas, w.MT, segs), kTcThreads, AttnClCfg<D>::kSmem,
+                             st>>>(q, pool_k, pool_v, n_sel, P_max, block_k, block_v, dm.B, dm.Hq,
+                                   dm.Hkv, w.R, scale, out, err);
+    trace_after(st);
+    return cudaGetLastError();
+  }
+  trace_before(st, "attn_kernel");
+  attn_kernel<D><<<dim3(w.splits, w.MT, segs), kTcThreads, AttnCfg<D>::kSmem, st>>>(
+      q, pool_k, pool_v, n_sel, P_max, block_k, block_v, dm.B, dm.Hq, dm.Hkv, w.R, w.MT,
+      w.splits, scale, opart, ml, err);
+  trace_after(st);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int rows = dm.N * dm.B * dm.Hq;
+  trace_before(st, "attn_combine_kernel");
+  attn_combine_kernel<D><<<cdiv(rows, 8), 256, 0, st>>>(opart, ml, n_sel, P_max, dm.N, dm.B,
+                                                        dm.Hq, dm.Hkv, w.MT, w.splits, out);
+  trace_after(st);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attn(const herald_dims& dm, const uint16_t* q, const uint16_t* pool_k,
                         const uint16_t* pool_v, const int32_t* n_sel, int P_max,
                         const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
                         float scale, const WsLayout& w, float* opart, float2* ml, uint32_t* err,
                         cudaStream_t st) {
-  const int segs = dm.N * dm.Hkv;
-  const int rows = dm.N * dm.B * dm.Hq;
-  cudaError_t e;
-  if (dm.d == 128) {
-    static bool attr = false;
-    if (!attr) {
-      e = cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               AttnCfg<128>::kSmem);
-      if (e != cudaSuccess) return e;
-      attr = true;
-    }
-    trace_before(st, "attn_kernel");
-    attn_kernel<128><<<dim3(w.splits, w.MT, segs), kTcThreads, AttnCfg<128>::kSmem, st>>>(
-        q, pool_k, pool_v, n_sel, P_max, block_k, block_v, dm.B, dm.Hq, dm.Hkv, w.R, w.MT,
-        w.splits, scale, opart, ml, err);
-    trace_after(st);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    trace_before(st, "attn_combine_kernel");
-    attn_combine_kernel<128><<<cdiv(rows, 8), 256, 0, st>>>(
-        opart, ml, n_sel, P_max, dm.N, dm.B, dm.Hq, dm.Hkv, w.MT, w.splits, out);
-    trace_after(st);
-  } else {
-    static bool attr = false;
-    if (!attr) {
-      e = cudaFuncSetAttribute(attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               AttnCfg<64>::kSmem);
-      if (e != cudaSuccess) return e;
-      attr = true;
-    }
-    trace_before(st, "attn_kernel");
-    attn_kernel<64><<<dim3(w.splits, w.MT, segs), kTcThreads, AttnCfg<64>::kSmem, st>>>(
-        q, pool_k, pool_v, n_sel, P_max, block_k, block_v, dm.B, dm.Hq, dm.Hkv, w.R, w.MT,
-        w.splits, scale, opart, ml, err);
-    trace_after(st);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    trace_before(st, "attn_combine_kernel");
-    attn_combine_kernel<64><<<cdiv(rows, 8), 256, 0, st>>>(
-        opart, ml, n_sel, P_max, dm.N, dm.B, dm.Hq, dm.Hkv, w.MT, w.splits, out);
-    trace_after(st);
-  }
-  return cudaGetLastError();
+  if (dm.d == 128)
+    return launch_attn_t<128>(dm, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale,
+                              w, opart, ml, err, st);
+  return launch_attn_t<64>(dm, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale, w,
+                           opart, ml, err, st);
 }
 
 }  // namespace herald

@@ -185,6 +185,9 @@ class Trace:
         self.capacity = capacity
         self.external = external
         self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * capacity)]
+        for e in self.events:       # torch creates the CUDA event on first record
+            e.record()
+        torch.cuda.synchronize()
         self._arr = (C.c_void_p * (2 * capacity))(*[e.cuda_event for e in self.events])
         self.count = 0
         self.names: list[str] = []
