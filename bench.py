@@ -2,10 +2,12 @@
 
 One step = one block of one layer of the 32K Qwen2.5-7B-like workload
 (N=1, Hq=28, Hkv=4, d=128, ctx 32768, B=32, T=8, C=4096, K=1024, sink 64,
-local 256): herald_select (merged-query scan + top-C + stage-2 refine +
-top-K with sink/local) -> herald_gather into one of two pool buffers ->
-T x herald_denoise_attn -> herald_append_kv.  Metric: block tokens/s =
-N*B / (time per step).
+local 256) through the dual-stream block pipeline: stage 2 (refine + top-K
+with sink/local) -> gather into one of two pool buffers -> T x sparse
+block attention -> append, on the denoising stream, while stage 1
+(merged-query scan + top-C) for the next block runs on the selection
+stream.  Metric: block tokens/s = N*B / (time per step).  The same step
+without the overlap is reported as `serial`.
 
 Timing: the step is captured once per cache copy into a CUDA graph and the
 graphs are replayed; the K cache and V cache are rotated over enough copies
@@ -166,6 +168,7 @@ class Bench:
         self.P = w.P
         cache_bytes = 2 * x["k_cache"].nbytes
         self.n_rot = max(2, int(np.ceil(2 * L2_BYTES / cache_bytes)) + 1)
+        self.n_rot += self.n_rot % 2      # even: block parity = cache-copy parity
         k0, v0 = dev(x["k_cache"]), dev(x["v_cache"])
         self.k = [k0] + [k0.clone() for _ in range(self.n_rot - 1)]
         self.v = [v0] + [v0.clone() for _ in range(self.n_rot - 1)]
@@ -173,33 +176,35 @@ class Bench:
         self.q_steps = dev(x["q_steps"])
         self.bk, self.bv = dev(x["block_k"]), dev(x["block_v"])
         self.ctx = torch.from_numpy(x["ctx"]).cuda()
-        NG = (w.N, w.Hkv)
-        self.ws_bytes = H.herald_workspace_size(self.d, w.C, self.P)
-        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device="cuda")
-        self.idx = torch.zeros((*NG, self.P), dtype=torch.int32, device="cuda")
-        self.n_sel = torch.zeros(NG, dtype=torch.int32, device="cuda")
-        self.pool_k = [torch.zeros((*NG, self.P, w.d), dtype=torch.int16, device="cuda")
-                       for _ in range(2)]
-        self.pool_v = [torch.zeros_like(self.pool_k[0]) for _ in range(2)]
+        from block_diffusion_sparse_gb300.pipeline import BlockPipeline
+        self.pipe = BlockPipeline(self.d, w.C, w.K, w.S, w.W, self.P, w.T)
         self.out = torch.zeros((w.T, w.N, w.B, w.Hq, w.d), dtype=torch.int16, device="cuda")
+        self.overlap = True
+        # stage 1 of the first block (its own queries; no predecessor)
+        self.pipe.prime(self.q_merge, self.k[0], self.ctx, slot=0)
+        torch.cuda.synchronize()
 
-    def step(self, r: int, stream=None, q_merge=None, q_steps=None, bk=None, bv=None):
-        """One block: select, gather, T attention steps, append."""
-        H, w = self.H, self.w
-        st = stream if stream is not None else self.torch.cuda.current_stream()
-        qm = self.q_merge if q_merge is None else q_merge
+    @property
+    def idx(self):
+        return self.pipe.idx
+
+    @property
+    def n_sel(self):
+        return self.pipe.n_sel
+
+    @property
+    def ws(self):
+        return self.pipe.ws_den
+
+    def step(self, r: int, q_merge=None, q_steps=None, bk=None, bv=None):
+        """One block through the dual-stream pipeline (cache copy r; stage 1
+        of the next block scans copy r+1)."""
         qs = self.q_steps if q_steps is None else q_steps
         bk = self.bk if bk is None else bk
         bv = self.bv if bv is None else bv
-        k, v = self.k[r], self.v[r]
-        pk, pv = self.pool_k[r % 2], self.pool_v[r % 2]
-        H.herald_select(self.d, qm, qs[0], k, self.ctx, w.C, w.K, w.S, w.W, self.P, self.idx,
-                        self.n_sel, self.ws, self.ws_bytes, st)
-        H.herald_gather(self.d, self.idx, self.n_sel, self.P, k, v, pk, pv, st)
-        for t in range(w.T):
-            H.herald_denoise_attn(self.d, qs[t], pk, pv, self.n_sel, self.P, bk[t], bv[t],
-                                  self.out[t], 0.0, self.ws, self.ws_bytes, st)
-        H.herald_append_kv(self.d, bk[w.T - 1], bv[w.T - 1], self.ctx, k, v, False, st)
+        nxt = (r + 1) % self.n_rot
+        self.pipe.block(r, qs, bk, bv, self.k[r], self.v[r], self.ctx, self.out,
+                        next_k_cache=self.k[nxt], advance=False, overlap=self.overlap)
 
     def capture(self, traced: bool = False):
         torch = self.torch
@@ -237,12 +242,14 @@ def algorithmic_work(w, n_sel: np.ndarray) -> dict:
     R = w.R
     ns = n_sel.astype(np.int64)
     keys = ns + w.B
+    attn = {"bound": "hbm",
+            "bytes": int(ns.sum()) * w.d * 2 * 2 + NG * w.B * w.d * 2 * 2
+            + 2 * w.N * w.B * w.Hq * w.d * 2,
+            "flops": int((4 * R * keys * w.d).sum())}
     return {
         "scan_kernel": {"bound": "hbm", "bytes": NG * w.L * w.d * 2},
-        "attn_kernel": {"bound": "hbm",
-                        "bytes": int(ns.sum()) * w.d * 2 * 2 + NG * w.B * w.d * 2 * 2
-                        + 2 * w.N * w.B * w.Hq * w.d * 2,
-                        "flops": int((4 * R * keys * w.d).sum())},
+        "attn_kernel": attn,
+        "attn_cluster_kernel": attn,
         "gather_kernel": {"bound": "hbm", "bytes": int(ns.sum()) * w.d * 2 * 2 * 2},
         "refine_pass1_kernel": {"bound": "tensor", "flops": 2 * R * w.C * w.d * NG},
         "refine_pass2_kernel": {"bound": "tensor", "flops": 2 * R * w.C * w.d * NG},
@@ -359,6 +366,21 @@ def run_ours(args, rank, world, dist):
     value = job_value(ms, world, w.N * w.B)
     err = b.H.herald_workspace_error(b.ws)
 
+    # the same step without the selection/denoise overlap, for reference
+    b.overlap = False
+    sgraphs, _ = b.capture(traced=False)
+    for i in range(args.warmup):
+        sgraphs[i % nrot].replay()
+    torch.cuda.synchronize()
+    e0.record(st)
+    for i in range(args.steps):
+        sgraphs[(args.warmup + i) % nrot].replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    serial_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, "cuda")
+    b.overlap = True
+    del sgraphs
+
     # traced replay: per-kernel durations (graph event nodes) for the roofline
     try:
         tgraphs, traces = b.capture(traced=True)
@@ -409,7 +431,7 @@ def run_ours(args, rank, world, dist):
                 "peak_source": f"{pk_kind} (MEASURED_PEAKS.json)" if pk_kind == "measured"
                 else "fallback"}
 
-    roofline = roof(dominant) or roof("attn_kernel")
+    roofline = roof(dominant) or roof("attn_cluster_kernel") or roof("attn_kernel")
     scan = roof("scan_kernel")
 
     # end to end through the C ABI with host buffers
@@ -426,6 +448,8 @@ def run_ours(args, rank, world, dist):
                              f"({nrot * 2 * b.x['k_cache'].nbytes / 2**20:.0f} MiB > L2)",
                        "timing": "CUDA-graph replay of whole steps, CUDA events"},
             "roofline": roofline,
+            "serial": {"ms_per_step": serial_ms, "value": job_value(serial_ms, world, w.N * w.B),
+                       "what": "same step with stage 1 on the denoising stream (no overlap)"},
             "scan": {"achieved_gbs": scan["achieved"] if scan else None,
                      "frac": scan["frac"] if scan else None,
                      "launch_us": scan["launch_us"] if scan else None},

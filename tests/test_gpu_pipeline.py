@@ -1,0 +1,70 @@
+"""The dual-stream block pipeline over three consecutive blocks, with the
+cache growing by one block each time, against the oracle replaying the same
+schedule: stage 1 for block i+1 scans the cache before block i is appended,
+using block i's first-step queries as the merged query; stage 2, the union
+with sink/local and the attention use the cache after the append."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import oracle
+from block_diffusion_sparse_gb300 import herald as H
+from block_diffusion_sparse_gb300 import synth
+from block_diffusion_sparse_gb300.pipeline import BlockPipeline
+from block_diffusion_sparse_gb300.workloads import Workload
+from helpers import ATTN_ATOL, bf16_dev_to_f64, dev, f64
+
+
+@pytest.mark.parametrize("overlap", [True, False])
+def test_three_blocks_match_oracle_schedule(overlap):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    nb = 3
+    w = Workload("pipe", N=2, Hq=8, Hkv=2, d=128, L=3000, B=16, T=2, C=256, K=128, S=16, W=64,
+                 planted="points", n_planted=10, index=31, extra_rows=nb * 16)
+    x0 = synth.make_layer(w)
+    blocks = [synth.make_layer(w.scaled(L=64, extra_rows=0, n_planted=0), layer=i + 1)
+              for i in range(nb)]
+    d = H.dims_of(w)
+    k, v = dev(x0["k_cache"]), dev(x0["v_cache"])
+    ctx = dev(x0["ctx"])
+    pipe = BlockPipeline(d, w.C, w.K, w.S, w.W, w.P, w.T)
+    pipe.prime(dev(x0["q_merge"]), k, ctx)
+    got = []
+    for i, xb in enumerate(blocks):
+        out = torch.zeros((w.T, w.N, w.B, w.Hq, w.d), dtype=torch.int16, device="cuda")
+        pipe.block(i, dev(xb["q_steps"]), dev(xb["block_k"]), dev(xb["block_v"]), k, v, ctx,
+                   out, advance=True, overlap=overlap)
+        torch.cuda.synchronize()
+        got.append((pipe.idx.cpu().numpy().copy(), pipe.n_sel.cpu().numpy().copy(),
+                    bf16_dev_to_f64(out)))
+    assert H.herald_workspace_error(pipe.ws_den) == 0
+    assert H.herald_workspace_error(pipe.ws_sel) == 0
+    assert ctx.cpu().numpy().tolist() == [w.L + nb * w.B] * w.N
+
+    # oracle replay of the same schedule
+    kc, vc = f64(x0["k_cache"]), f64(x0["v_cache"])
+    cx = x0["ctx"].copy()
+    qbar = oracle.merged_query(f64(x0["q_merge"]))
+    cand, nc = oracle.topc(oracle.stage1_scores(qbar, kc, cx)[2], cx, w.C)
+    for i, xb in enumerate(blocks):
+        q0 = f64(xb["q_steps"][0])
+        s2 = oracle.stage2_scores(q0, kc, cand, nc)
+        idx_o, ns_o = oracle.select_final(cx, w.L_max, cand, nc, s2, w.K, w.S, w.W, w.P)
+        gi, gn, gout = got[i]
+        for n in range(w.N):
+            for g in range(w.Hkv):
+                a = set(gi[n, g, : gn[n, g]].tolist())
+                b = set(idx_o[n, g, : ns_o[n, g]].tolist())
+                assert len(a ^ b) <= 2, f"block {i} n={n} g={g}: {sorted(a ^ b)[:6]}"
+        for t in range(w.T):
+            ref = oracle.sparse_attn(f64(xb["q_steps"][t]), kc, vc, gi, gn,
+                                     f64(xb["block_k"][t]), f64(xb["block_v"][t]))
+            assert np.abs(gout[t] - ref).max() <= ATTN_ATOL
+        # stage 1 for the next block: before this block is appended
+        qbar = oracle.merged_query(q0)
+        cand, nc = oracle.topc(oracle.stage1_scores(qbar, kc, cx)[2], cx, w.C)
+        cx, kc, vc = oracle.append(cx, f64(xb["block_k"][w.T - 1]), f64(xb["block_v"][w.T - 1]),
+                                   kc, vc)
