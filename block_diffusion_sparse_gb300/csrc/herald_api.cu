@@ -121,17 +121,18 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D view [N*Hkv*L_max rows][d] of the key cache; box 64 columns x 64 rows,
-// 128-byte swizzle (the scan's shared-memory layout).
-herald_status encode_kcache_map(const herald_dims& dm, const uint16_t* k_cache, CUtensorMap* map) {
+// 2-D bf16 tensor map [rows][d] with a box of 64 columns x box_rows rows and
+// 128-byte swizzle (the UMMA K-major shared-memory layout).
+herald_status encode_rows_map(const void* base, uint64_t rows, int d, uint32_t box_rows,
+                              CUtensorMap* map) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(HERALD_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
-  const cuuint64_t dims[2] = {cuuint64_t(dm.d), cuuint64_t(dm.N) * dm.Hkv * dm.L_max};
-  const cuuint64_t strides[1] = {cuuint64_t(dm.d) * 2};
-  const cuuint32_t box[2] = {64, cuuint32_t(kScanTileKeys)};
+  const cuuint64_t dims[2] = {cuuint64_t(d), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(d) * 2};
+  const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(k_cache),
-                        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(HERALD_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
@@ -153,21 +154,25 @@ herald_status run_stage1(const herald_dims& dm, const uint16_t* q_merge, const u
                          const int32_t* ctx_len, int C, int32_t* cand, int32_t* n_cand, void* ws,
                          const WsLayout& w, cudaStream_t st) {
   const bool tma = is_device_memory(k_cache);
-  CUtensorMap map;
-  if (tma) {
-    herald_status s = encode_kcache_map(dm, k_cache, &map);
-    if (s != HERALD_OK) return s;
-  }
   uint32_t* err = at<uint32_t>(ws, w.err);
   float* qbar = at<float>(ws, w.qbar);
+  uint16_t* qhl = at<uint16_t>(ws, w.qhl);
+  CUtensorMap kmap, bmap;
+  if (tma) {
+    herald_status s = encode_rows_map(k_cache, uint64_t(dm.N) * dm.Hkv * dm.L_max, dm.d,
+                                      kTcScanKeys, &kmap);
+    if (s != HERALD_OK) return s;
+    s = encode_rows_map(qhl, uint64_t(dm.N) * dm.Hkv * kQhlRows, dm.d, kQhlRows, &bmap);
+    if (s != HERALD_OK) return s;
+  }
   float* logits = at<float>(ws, w.logits);
   float2* part1 = at<float2>(ws, w.part1);
   float* s1 = at<float>(ws, w.s1);
   uint32_t* hist = at<uint32_t>(ws, w.hist);
   const int nsm = sm_count();
-  HERALD_TRY_CUDA(launch_merge_query(dm, q_merge, qbar, hist, st), "merge_query launch");
-  HERALD_TRY_CUDA(launch_scan(dm, tma ? &map : nullptr, k_cache, tma, qbar, ctx_len, logits, part1,
-                              w, err, nsm, st),
+  HERALD_TRY_CUDA(launch_merge_query(dm, q_merge, qbar, qhl, hist, st), "merge_query launch");
+  HERALD_TRY_CUDA(launch_scan(dm, tma ? &kmap : nullptr, tma ? &bmap : nullptr, k_cache, qbar,
+                              ctx_len, logits, part1, w, err, nsm, st),
                   "scan launch");
   HERALD_TRY_CUDA(launch_s1_hist(dm, logits, part1, ctx_len, s1, hist, w, nsm, st),
                   "s1_hist launch");

@@ -11,9 +11,13 @@
 namespace herald {
 
 // ---- stage-1 scan
-constexpr int kScanTileKeys = 64;   // keys per TMA tile (one warp iteration)
+constexpr int kScanTileKeys = 64;   // CUDA-core scan (host-resident caches): keys per tile
 constexpr int kScanWarps = 4;       // warps per CTA, each with its own ring
-constexpr int kScanStages = 3;      // TMA stages per warp
+constexpr int kScanStages = 3;      // stages per warp
+constexpr int kTcScanKeys = 128;    // tensor-core scan: keys per tile (UMMA M)
+constexpr int kTcScanStages = 4;    // TMA ring depth of the tensor-core scan
+constexpr int kPartKeys = 32;       // keys per stage-1 (max, sumexp) partial
+constexpr int kQhlRows = 16;        // merged-query operand rows: 8 hi + 8 lo
 // ---- stage-1 score histogram (bits [30:19] of a non-negative fp32)
 constexpr int kHistBins = 4096;
 constexpr int kHistShift = 19;
@@ -31,8 +35,9 @@ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 struct WsLayout {
   size_t err;        // uint32 device error word
   size_t qbar;       // float [N][Hq][d]        merged queries, pre-scaled
+  size_t qhl;        // bf16 [N*Hkv][16][d]     merged queries as hi/lo bf16 rows
   size_t logits;     // float [N][Hq][L_pad]    stage-1 logits
-  size_t part1;      // float2 [N][Hq][tiles]   per-tile (max, sumexp)
+  size_t part1;      // float2 [N][Hq][parts]   per-32-key (max, sumexp)
   size_t s1;         // float [N][Hkv][L_pad]   stage-1 scores
   size_t hist;       // uint32 [N*Hkv][kHistBins]
   size_t cand;       // int32 [N][Hkv][C]       (herald_select only)
@@ -42,15 +47,17 @@ struct WsLayout {
   size_t opart;      // float [N*Hkv][MT][S][128][d]      attention partials
   size_t ml;         // float2 [N*Hkv][MT][S][128]
   size_t total;
-  int L_pad, tiles_per_seg, R, MT, n_chunks, splits;
+  int L_pad, tiles_per_seg, tiles128, parts, R, MT, n_chunks, splits;
 };
 
 inline WsLayout ws_layout(const herald_dims& dm, int C, int P_max) {
   WsLayout w{};
   const size_t A = 256;
   const int G = dm.Hq / dm.Hkv;
-  w.tiles_per_seg = cdiv(dm.L_max, kScanTileKeys);
-  w.L_pad = w.tiles_per_seg * kScanTileKeys;
+  w.L_pad = cdiv(dm.L_max, kTcScanKeys) * kTcScanKeys;
+  w.tiles_per_seg = w.L_pad / kScanTileKeys;
+  w.tiles128 = w.L_pad / kTcScanKeys;
+  w.parts = w.L_pad / kPartKeys;
   w.R = dm.B * G;
   w.MT = cdiv(w.R, kTileM);
   w.n_chunks = cdiv(C, kRefineChunk);
@@ -59,8 +66,9 @@ inline WsLayout ws_layout(const herald_dims& dm, int C, int P_max) {
   size_t o = 0;
   w.err = o;    o = align_up(o + 16, A);
   w.qbar = o;   o = align_up(o + NH * dm.d * 4, A);
+  w.qhl = o;    o = align_up(o + NG * kQhlRows * dm.d * 2, A);
   w.logits = o; o = align_up(o + NH * w.L_pad * 4, A);
-  w.part1 = o;  o = align_up(o + NH * w.tiles_per_seg * 8, A);
+  w.part1 = o;  o = align_up(o + NH * w.parts * 8, A);
   w.s1 = o;     o = align_up(o + NG * w.L_pad * 4, A);
   w.hist = o;   o = align_up(o + NG * kHistBins * 4, A);
   w.cand = o;   o = align_up(o + NG * C * 4, A);
@@ -80,11 +88,14 @@ void trace_after(cudaStream_t st);
 
 // ---- launchers (return the launch error; the caller maps it to a status)
 cudaError_t launch_merge_query(const herald_dims& dm, const uint16_t* q_merge, float* qbar,
-                               uint32_t* hist, cudaStream_t st);
-cudaError_t launch_scan(const herald_dims& dm, const CUtensorMap* kmap, const uint16_t* k_cache,
-                        bool use_tma, const float* qbar, const int32_t* ctx, float* logits,
-                        float2* part1, const WsLayout& w, uint32_t* err, int num_sms,
-                        cudaStream_t st);
+                               uint16_t* qhl, uint32_t* hist, cudaStream_t st);
+// kmap: the key cache as [N*Hkv*L_max][d], box 64 x 128 rows, 128B swizzle;
+// bmap: qhl as [N*Hkv*16][d], box 64 x 16 rows.  Without maps (host-resident
+// caches) the CUDA-core scan runs instead.
+cudaError_t launch_scan(const herald_dims& dm, const CUtensorMap* kmap, const CUtensorMap* bmap,
+                        const uint16_t* k_cache, const float* qbar, const int32_t* ctx,
+                        float* logits, float2* part1, const WsLayout& w, uint32_t* err,
+                        int num_sms, cudaStream_t st);
 cudaError_t launch_s1_hist(const herald_dims& dm, const float* logits, const float2* part1,
                            const int32_t* ctx, float* s1, uint32_t* hist, const WsLayout& w,
                            int num_sms, cudaStream_t st);

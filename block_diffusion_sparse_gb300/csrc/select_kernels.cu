@@ -18,39 +18,241 @@
 namespace herald {
 
 // ============================================================ merge_query
-// grid (N*Hq), block d.  Also zeroes the stage-1 histogram.
-__global__ void merge_query_kernel(const uint16_t* __restrict__ q, int B, int Hq, int d,
+// grid (N*Hq), block d.  qbar = mean over the B queries, pre-scaled by
+// 1/sqrt(d), in fp32 (for the CUDA-core scan) and as two bf16 rows hi =
+// bf16(qbar), lo = bf16(qbar - hi) (for the tensor-core scan: hi + lo keeps
+// ~16 mantissa bits).  Rows of absent heads (h >= G) are zero.  Also zeroes
+// the stage-1 histogram.
+__global__ void merge_query_kernel(const uint16_t* __restrict__ q, int B, int Hq, int Hkv, int d,
                                    float scale, float* __restrict__ qbar,
-                                   uint32_t* __restrict__ hist, int hist_words) {
+                                   uint16_t* __restrict__ qhl, uint32_t* __restrict__ hist,
+                                   int hist_words) {
   const int nh = blockIdx.x, n = nh / Hq, h = nh % Hq, e = threadIdx.x;
+  const int G = Hq / Hkv, g = h / G, hl = h - g * G;
   if (e < d) {
     float acc = 0.f;
-    for (int b = 0; b < B; ++b) {
-      const uint16_t u = q[((size_t(n) * B + b) * Hq + h) * d + e];
-      acc += __uint_as_float(uint32_t(u) << 16);
+    const uint16_t* src = q + (size_t(n) * B * Hq + h) * d + e;
+    int b = 0;
+    for (; b + 8 <= B; b += 8) {
+      uint16_t u[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) u[k] = src[size_t(b + k) * Hq * d];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc += __uint_as_float(uint32_t(u[k]) << 16);
     }
-    qbar[size_t(nh) * d + e] = acc / float(B) * scale;
+    for (; b < B; ++b) acc += __uint_as_float(uint32_t(src[size_t(b) * Hq * d]) << 16);
+    const float qv = acc / float(B) * scale;
+    qbar[size_t(nh) * d + e] = qv;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(qv);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(qv - __bfloat162float(hi));
+    uint16_t* rows = qhl + (size_t(n) * Hkv + g) * kQhlRows * d;
+    rows[size_t(hl) * d + e] = __bfloat16_as_ushort(hi);
+    rows[size_t(8 + hl) * d + e] = __bfloat16_as_ushort(lo);
+    if (hl == 0)
+      for (int r = G; r < 8; ++r) {
+        rows[size_t(r) * d + e] = 0;
+        rows[size_t(8 + r) * d + e] = 0;
+      }
   }
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < hist_words; i += gridDim.x * blockDim.x)
     hist[i] = 0u;
 }
 
 cudaError_t launch_merge_query(const herald_dims& dm, const uint16_t* q_merge, float* qbar,
-                               uint32_t* hist, cudaStream_t st) {
+                               uint16_t* qhl, uint32_t* hist, cudaStream_t st) {
   const float scale = 1.0f / sqrtf(float(dm.d));
   trace_before(st, "merge_query_kernel");
-  merge_query_kernel<<<dm.N * dm.Hq, dm.d, 0, st>>>(q_merge, dm.B, dm.Hq, dm.d, scale, qbar,
-                                                    hist, dm.N * dm.Hkv * kHistBins);
+  merge_query_kernel<<<dm.N * dm.Hq, dm.d, 0, st>>>(q_merge, dm.B, dm.Hq, dm.Hkv, dm.d, scale,
+                                                    qbar, qhl, hist,
+                                                    dm.N * dm.Hkv * kHistBins);
   trace_after(st);
   return cudaGetLastError();
 }
 
-// =================================================================== scan
-// Persistent: grid = #SMs.  Flattened tiles t = seg * tiles_per_seg + tile
-// (seg = n*Hkv + g) are split into contiguous per-CTA ranges; warp w of a CTA
-// takes tiles begin+w, begin+w+kScanWarps, ... through its own ring of
-// kScanStages shared-memory stages.  Each lane owns keys lane and lane+32 of
-// a 64-key tile; the two keys are the two halves of packed f32x2 FMAs.
+// Writes the (max, sumexp) of one 32-key group of logits (one per lane,
+// `valid` marks keys inside the context).
+__device__ __forceinline__ void write_part(float l, bool valid, float2* dst, int lane) {
+  const float m = warp_max(valid ? l : -INFINITY);
+  const float s = warp_sum(valid ? __expf(l - m) : 0.f);
+  if (lane == 0) *dst = make_float2(m, s);
+}
+
+// ======================================================== scan (tensor)
+// Stage-1 scan of a device-resident cache on the tensor cores.  The merged
+// queries of a KV group form a 16-row bf16 operand (8 hi rows + 8 lo rows);
+// a 128-key tile of the cache is the other operand, so one 128 x 16 x d UMMA
+// per tile yields every head's logit for 128 keys (hi + lo columns summed).
+// Persistent, warp-specialised: warp 4 streams key tiles through a
+// kTcScanStages-deep TMA ring, warp 5 issues the UMMAs into two TMEM
+// accumulators, warps 0-3 (one TMEM lane = one key each) write logits and
+// per-32-key (max, sumexp) partials while the next tile is multiplied.
+template <int D>
+struct TcScanCfg {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kHalfBytes = kTcScanKeys * 128;
+  static constexpr int kTileBytes = kHalves * kHalfBytes;
+  static constexpr int kBHalfBytes = kQhlRows * 128;
+  static constexpr int kBBytes = kHalves * kBHalfBytes;
+  static constexpr int kSmem = kTcScanStages * kTileBytes + 2048 + 1024;
+};
+constexpr int kTcScanThreads = 192;
+
+template <int D, int G>
+__global__ void __launch_bounds__(kTcScanThreads, 1)
+    scan_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap bmap, const int32_t* __restrict__ ctx,
+                   int Hkv, int L_max, int tiles_per_seg, int total_tiles, int L_pad, int parts,
+                   float* __restrict__ logits, float2* __restrict__ part1, uint32_t* err) {
+  using Cfg = TcScanCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full[kTcScanStages], empty[kTcScanStages];
+  __shared__ uint64_t tfull[2], tempty[2], bbar, mdone;
+  __shared__ uint32_t tmem_base;
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* Bs = ring + kTcScanStages * Cfg::kTileBytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Hq = Hkv * G;
+  const int t_begin = int((long long)blockIdx.x * total_tiles / gridDim.x);
+  const int t_end = int((long long)(blockIdx.x + 1) * total_tiles / gridDim.x);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTcScanStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(&bbar, 1);
+    mbar_init(&mdone, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_base, 32);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base;
+
+  // tile t covers keys [j0, j0 + 128) of segment seg = n*Hkv + g
+  auto tile = [&](int t, int& seg, int& j0, int& L) -> bool {
+    seg = t / tiles_per_seg;
+    j0 = (t - seg * tiles_per_seg) * kTcScanKeys;
+    L = min(max(ctx[seg / Hkv], 0), L_max);
+    return j0 < L;
+  };
+
+  if (warp == 4) {
+    if (lane == 0) {  // ---- TMA producer
+      tma_prefetch_desc(&kmap);
+      int i = 0;
+      for (int t = t_begin; t < t_end; ++t) {
+        int seg, j0, L;
+        if (!tile(t, seg, j0, L)) continue;
+        const int stage = i % kTcScanStages;
+        if (i >= kTcScanStages &&
+            !mbar_wait(&empty[stage], uint32_t((i / kTcScanStages) - 1) & 1u)) {
+          record_error(err, DEV_TIMEOUT_MMA);
+          break;
+        }
+        mbar_arrive_expect_tx(&full[stage], Cfg::kTileBytes);
+#pragma unroll
+        for (int hv = 0; hv < Cfg::kHalves; ++hv)
+          tma_load_2d(ring + stage * Cfg::kTileBytes + hv * Cfg::kHalfBytes, &kmap, &full[stage],
+                      hv * 64, seg * L_max + j0);
+        ++i;
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {  // ---- UMMA issuer
+      tma_prefetch_desc(&bmap);
+      constexpr uint32_t idesc = make_idesc_bf16(kTcScanKeys, kQhlRows, false, false);
+      int i = 0, cur_seg = -1;
+      uint32_t nb = 0, nd = 0;
+      bool ok = true;
+      for (int t = t_begin; t < t_end && ok; ++t) {
+        int seg, j0, L;
+        if (!tile(t, seg, j0, L)) continue;
+        if (seg != cur_seg) {  // new merged-query operand; earlier UMMAs must be done with Bs
+          if (i > 0) {
+            umma_commit(&mdone);
+            ok = mbar_wait(&mdone, nd & 1u);
+            ++nd;
+          }
+          mbar_arrive_expect_tx(&bbar, Cfg::kBBytes);
+#pragma unroll
+          for (int hv = 0; hv < Cfg::kHalves; ++hv)
+            tma_load_2d(Bs + hv * Cfg::kBHalfBytes, &bmap, &bbar, hv * 64, seg * kQhlRows);
+          ok = ok && mbar_wait(&bbar, nb & 1u);
+          ++nb;
+          cur_seg = seg;
+        }
+        const int stage = i % kTcScanStages, acc = i & 1;
+        ok = ok && mbar_wait(&full[stage], uint32_t(i / kTcScanStages) & 1u);
+        if (i >= 2) ok = ok && mbar_wait(&tempty[acc], uint32_t((i >> 1) - 1) & 1u);
+        if (!ok) {
+          record_error(err, DEV_TIMEOUT_TMA);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t ka = smem_u32(ring + stage * Cfg::kTileBytes), ba = smem_u32(Bs);
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s) {
+          const uint32_t hv = s >> 2, koff = (s & 3) * 32;
+          const uint64_t a = make_sdesc_sw128(ka + hv * Cfg::kHalfBytes + koff, 16, 1024);
+          const uint64_t b = make_sdesc_sw128(ba + hv * Cfg::kBHalfBytes + koff, 16, 1024);
+          umma_bf16(tbase + acc * kQhlRows, a, b, idesc, s > 0 ? 1u : 0u);
+        }
+        umma_commit(&empty[stage]);
+        umma_commit(&tfull[acc]);
+        ++i;
+      }
+    }
+  } else {  // ---- epilogue: warps 0-3, thread = key row of the tile
+    int i = 0;
+    for (int t = t_begin; t < t_end; ++t) {
+      int seg, j0, L;
+      if (!tile(t, seg, j0, L)) continue;
+      const int acc = i & 1;
+      if (!mbar_wait(&tfull[acc], uint32_t(i >> 1) & 1u)) {
+        record_error(err, DEV_TIMEOUT_MMA);
+        break;
+      }
+      tc_fence_after();
+      __syncwarp();
+      float v[16];
+      tmem_ld16(tbase + (uint32_t(warp * 32) << 16) + uint32_t(acc * kQhlRows), v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      const int n = seg / Hkv, g = seg - n * Hkv;
+      const int j = j0 + warp * 32 + lane;
+      const bool valid = j < L;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float l = v[h] + v[8 + h];
+        const size_t row = size_t(n) * Hq + g * G + h;
+        if (valid) logits[row * L_pad + j] = l;
+        write_part(l, valid, part1 + row * parts + (j0 / kPartKeys) + warp, lane);
+      }
+      ++i;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 32);
+  }
+}
+
+// ====================================================== scan (CUDA core)
+// Stage-1 scan of a cache in mapped host memory (read over the host link):
+// each warp streams 64-key tiles through its own cp.async ring; lane owns
+// keys lane and lane+32, the two halves of packed f32x2 FMAs.
 template <int D>
 struct ScanCfg {
   static constexpr int kHalves = D / 64;
@@ -59,15 +261,14 @@ struct ScanCfg {
   static constexpr int kSmem = kScanWarps * kScanStages * kTileBytes + 1024;
 };
 
-template <int D, int G, bool TMA>
+template <int D, int G>
 __global__ void __launch_bounds__(kScanWarps * 32, 1)
-    scan_kernel(const __grid_constant__ CUtensorMap kmap, const uint16_t* __restrict__ kc,
-                const float* __restrict__ qbar, const int32_t* __restrict__ ctx, int Hkv,
-                int L_max, int tiles_per_seg, int total_tiles, int L_pad,
-                float* __restrict__ logits, float2* __restrict__ part1, uint32_t* err) {
+    scan_cc_kernel(const uint16_t* __restrict__ kc, const float* __restrict__ qbar,
+                   const int32_t* __restrict__ ctx, int Hkv, int L_max, int tiles_per_seg,
+                   int total_tiles, int L_pad, int parts, float* __restrict__ logits,
+                   float2* __restrict__ part1) {
   using Cfg = ScanCfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bars[kScanWarps][kScanStages];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -76,78 +277,48 @@ __global__ void __launch_bounds__(kScanWarps * 32, 1)
   const int t_begin = int((long long)blockIdx.x * total_tiles / gridDim.x);
   const int t_end = int((long long)(blockIdx.x + 1) * total_tiles / gridDim.x);
 
-  if (TMA && lane == 0) {
-    tma_prefetch_desc(&kmap);
-    for (int s = 0; s < kScanStages; ++s) mbar_init(&bars[warp][s], 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
-
-  // Issues the load of this warp's i-th tile into `stage`; returns whether a
-  // load was issued (tiles past the context are skipped).
-  auto issue = [&](int i, int stage) -> bool {
+  // Issues the copies of this warp's i-th tile into `stage` (one commit
+  // group per tile, empty for tiles past the context).
+  auto issue = [&](int i, int stage) {
     const int t = t_begin + warp + i * kScanWarps;
-    bool ok = t < t_end;
-    int seg = 0, j0 = 0, L = 0;
-    if (ok) {
-      seg = t / tiles_per_seg;
-      j0 = (t - seg * tiles_per_seg) * kScanTileKeys;
-      L = min(max(ctx[seg / Hkv], 0), L_max);
-      ok = j0 < L;
-    }
-    uint8_t* dst = ring + stage * Cfg::kTileBytes;
-    if constexpr (TMA) {
-      if (ok && lane == 0) {
-        mbar_arrive_expect_tx(&bars[warp][stage], Cfg::kTileBytes);
-#pragma unroll
-        for (int hv = 0; hv < Cfg::kHalves; ++hv)
-          tma_load_2d(dst + hv * Cfg::kHalfBytes, &kmap, &bars[warp][stage], hv * 64,
-                      seg * L_max + j0);
-      }
-    } else {
-      if (ok) {
+    if (t < t_end) {
+      const int seg = t / tiles_per_seg;
+      const int j0 = (t - seg * tiles_per_seg) * kScanTileKeys;
+      const int L = min(max(ctx[seg / Hkv], 0), L_max);
+      if (j0 < L) {
+        uint8_t* dst = ring + stage * Cfg::kTileBytes;
         const uint16_t* base = kc + size_t(seg) * L_max * D;
-        // 64 rows x D/8 chunks of 16 bytes, spread over the 32 lanes
         for (int q = lane; q < kScanTileKeys * (D / 8); q += 32) {
           const int r = q / (D / 8), c = q % (D / 8);
           const int j = j0 + r;
           const bool v = j < L;
-          const uint16_t* src = base + size_t(v ? j : 0) * D + c * 8;
-          cp_async_16(dst + (c >> 3) * Cfg::kHalfBytes + sw128_off(r, c & 7), src, v ? 16u : 0u);
+          cp_async_16(dst + (c >> 3) * Cfg::kHalfBytes + sw128_off(r, c & 7),
+                      base + size_t(v ? j : 0) * D + c * 8, v ? 16u : 0u);
         }
       }
-      cp_async_commit();
     }
-    return ok;
+    cp_async_commit();
   };
 
-  uint32_t issued = 0, phase = 0;
 #pragma unroll
-  for (int s = 0; s < kScanStages; ++s) issued |= uint32_t(issue(s, s)) << s;
+  for (int s = 0; s < kScanStages; ++s) issue(s, s);
 
-  bool timed_out = false;
   for (int i = 0;; ++i) {
     const int t = t_begin + warp + i * kScanWarps;
     if (t >= t_end) break;
     const int stage = i % kScanStages;
-    const bool valid = (issued >> stage) & 1u;
     const int seg = t / tiles_per_seg;
     const int tl = t - seg * tiles_per_seg;
     const int n = seg / Hkv, g = seg - n * Hkv;
     const int j0 = tl * kScanTileKeys;
+    const int L = min(max(ctx[n], 0), L_max);
+    const bool valid = j0 < L;
     float2 acc[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) acc[h] = make_float2(0.f, 0.f);
+    asm volatile("cp.async.wait_group %0;" ::"n"(kScanStages - 1) : "memory");
+    __syncwarp();
     if (valid) {
-      if constexpr (TMA) {
-        if (!mbar_wait(&bars[warp][stage], (phase >> stage) & 1u)) {
-          timed_out = true;
-        }
-        phase ^= 1u << stage;
-      } else {
-        asm volatile("cp.async.wait_group %0;" ::"n"(kScanStages - 1) : "memory");
-        __syncwarp();
-      }
       const uint8_t* tile = ring + stage * Cfg::kTileBytes;
       const float* qb = qbar + (size_t(n) * Hq + g * G) * D;
 #pragma unroll 2
@@ -181,16 +352,9 @@ __global__ void __launch_bounds__(kScanWarps * 32, 1)
         }
       }
     }
-    // every lane has consumed the stage: refill it
-    __syncwarp();
-    if (!timed_out) {
-      const bool nv = issue(i + kScanStages, stage);
-      issued = (issued & ~(1u << stage)) | (uint32_t(nv) << stage);
-    } else {
-      issued &= ~(1u << stage);
-    }
+    __syncwarp();  // every lane has consumed the stage: refill it
+    issue(i + kScanStages, stage);
     if (valid) {
-      const int L = min(max(ctx[n], 0), L_max);
       const int ja = j0 + lane, jb = j0 + lane + 32;
       const bool va = ja < L, vb = jb < L;
 #pragma unroll
@@ -199,59 +363,60 @@ __global__ void __launch_bounds__(kScanWarps * 32, 1)
         float* lr = logits + row * L_pad;
         if (va) lr[ja] = acc[h].x;
         if (vb) lr[jb] = acc[h].y;
-        const float la = va ? acc[h].x : -INFINITY, lb = vb ? acc[h].y : -INFINITY;
-        const float m = warp_max(fmaxf(la, lb));
-        const float s = warp_sum((va ? __expf(la - m) : 0.f) + (vb ? __expf(lb - m) : 0.f));
-        if (lane == 0) part1[row * tiles_per_seg + tl] = make_float2(m, s);
+        write_part(acc[h].x, va, part1 + row * parts + j0 / kPartKeys, lane);
+        write_part(acc[h].y, vb, part1 + row * parts + j0 / kPartKeys + 1, lane);
       }
     }
-    if (timed_out) break;
   }
-  if constexpr (TMA) {
-    if (timed_out) {
-      if (lane == 0) record_error(err, DEV_TIMEOUT_TMA);
-      // wait (bounded) for any load still in flight before leaving
-      for (int s = 0; s < kScanStages; ++s)
-        if ((issued >> s) & 1u) (void)mbar_wait(&bars[warp][s], (phase >> s) & 1u);
-    }
-  } else {
-    cp_async_wait_all();
-  }
+  cp_async_wait_all();
 }
 
-template <int D, int G, bool TMA>
-static cudaError_t launch_scan_t(const CUtensorMap* kmap, const uint16_t* kc, const float* qbar,
-                                 const int32_t* ctx, const herald_dims& dm, float* logits,
-                                 float2* part1, const WsLayout& w, uint32_t* err, int num_sms,
-                                 cudaStream_t st) {
-  using Cfg = ScanCfg<D>;
+template <int D, int G>
+static cudaError_t launch_scan_t(const CUtensorMap* kmap, const CUtensorMap* bmap,
+                                 const uint16_t* kc, const float* qbar, const int32_t* ctx,
+                                 const herald_dims& dm, float* logits, float2* part1,
+                                 const WsLayout& w, uint32_t* err, int num_sms, cudaStream_t st) {
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(scan_kernel<D, G, TMA>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(scan_tc_kernel<D, G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         TcScanCfg<D>::kSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(scan_cc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             ScanCfg<D>::kSmem);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  const int total = dm.N * dm.Hkv * w.tiles_per_seg;
-  const int grid = total < num_sms ? total : num_sms;
-  CUtensorMap dummy{};
-  trace_before(st, "scan_kernel");
-  scan_kernel<D, G, TMA><<<grid, kScanWarps * 32, Cfg::kSmem, st>>>(
-      kmap ? *kmap : dummy, kc, qbar, ctx, dm.Hkv, dm.L_max, w.tiles_per_seg, total, w.L_pad,
-      logits, part1, err);
-  trace_after(st);
+  const int segs = dm.N * dm.Hkv;
+  if (kmap && bmap) {
+    const int total = segs * w.tiles128;
+    const int grid = total < num_sms ? total : num_sms;
+    trace_before(st, "scan_tc_kernel");
+    scan_tc_kernel<D, G><<<grid, kTcScanThreads, TcScanCfg<D>::kSmem, st>>>(
+        *kmap, *bmap, ctx, dm.Hkv, dm.L_max, w.tiles128, total, w.L_pad, w.parts, logits, part1,
+        err);
+    trace_after(st);
+  } else {
+    const int total = segs * w.tiles_per_seg;
+    const int grid = total < num_sms ? total : num_sms;
+    trace_before(st, "scan_cc_kernel");
+    scan_cc_kernel<D, G><<<grid, kScanWarps * 32, ScanCfg<D>::kSmem, st>>>(
+        kc, qbar, ctx, dm.Hkv, dm.L_max, w.tiles_per_seg, total, w.L_pad, w.parts, logits,
+        part1);
+    trace_after(st);
+  }
   return cudaGetLastError();
 }
 
-template <int D, bool TMA>
-static cudaError_t scan_dispatch_g(int G, const CUtensorMap* kmap, const uint16_t* kc,
-                                   const float* qbar, const int32_t* ctx, const herald_dims& dm,
-                                   float* logits, float2* part1, const WsLayout& w,
-                                   uint32_t* err, int num_sms, cudaStream_t st) {
-#define HERALD_SCAN_G(GG)                                                                       \
-  case GG:                                                                                      \
-    return launch_scan_t<D, GG, TMA>(kmap, kc, qbar, ctx, dm, logits, part1, w, err, num_sms, \
-                                     st);
+template <int D>
+static cudaError_t scan_dispatch_g(int G, const CUtensorMap* kmap, const CUtensorMap* bmap,
+                                   const uint16_t* kc, const float* qbar, const int32_t* ctx,
+                                   const herald_dims& dm, float* logits, float2* part1,
+                                   const WsLayout& w, uint32_t* err, int num_sms,
+                                   cudaStream_t st) {
+#define HERALD_SCAN_G(GG) \
+  case GG:                \
+    return launch_scan_t<D, GG>(kmap, bmap, kc, qbar, ctx, dm, logits, part1, w, err, num_sms, st);
   switch (G) {
     HERALD_SCAN_G(1) HERALD_SCAN_G(2) HERALD_SCAN_G(3) HERALD_SCAN_G(4)
     HERALD_SCAN_G(5) HERALD_SCAN_G(6) HERALD_SCAN_G(7) HERALD_SCAN_G(8)
@@ -260,20 +425,16 @@ static cudaError_t scan_dispatch_g(int G, const CUtensorMap* kmap, const uint16_
 #undef HERALD_SCAN_G
 }
 
-cudaError_t launch_scan(const herald_dims& dm, const CUtensorMap* kmap, const uint16_t* k_cache,
-                        bool use_tma, const float* qbar, const int32_t* ctx, float* logits,
-                        float2* part1, const WsLayout& w, uint32_t* err, int num_sms,
-                        cudaStream_t st) {
+cudaError_t launch_scan(const herald_dims& dm, const CUtensorMap* kmap, const CUtensorMap* bmap,
+                        const uint16_t* k_cache, const float* qbar, const int32_t* ctx,
+                        float* logits, float2* part1, const WsLayout& w, uint32_t* err,
+                        int num_sms, cudaStream_t st) {
   const int G = dm.Hq / dm.Hkv;
   if (dm.d == 128)
-    return use_tma ? scan_dispatch_g<128, true>(G, kmap, k_cache, qbar, ctx, dm, logits, part1,
-                                                w, err, num_sms, st)
-                   : scan_dispatch_g<128, false>(G, kmap, k_cache, qbar, ctx, dm, logits, part1,
-                                                 w, err, num_sms, st);
-  return use_tma ? scan_dispatch_g<64, true>(G, kmap, k_cache, qbar, ctx, dm, logits, part1, w,
-                                             err, num_sms, st)
-                 : scan_dispatch_g<64, false>(G, kmap, k_cache, qbar, ctx, dm, logits, part1, w,
-                                              err, num_sms, st);
+    return scan_dispatch_g<128>(G, kmap, bmap, k_cache, qbar, ctx, dm, logits, part1, w, err,
+                                num_sms, st);
+  return scan_dispatch_g<64>(G, kmap, bmap, k_cache, qbar, ctx, dm, logits, part1, w, err,
+                             num_sms, st);
 }
 
 // ================================================================ s1_hist
@@ -281,11 +442,23 @@ cudaError_t launch_scan(const herald_dims& dm, const CUtensorMap* kmap, const ui
 // its G heads into lse_h, then scores its key range and bins the fp32 bit
 // pattern of s1 (non-negative, so bit order = value order).
 constexpr int kS1Threads = 256;
+constexpr int kS1Keys = 4;  // keys per thread per round
 
+__device__ __forceinline__ void lse_merge(float& m, float& s, float2 v) {
+  if (v.x == -INFINITY) return;
+  if (v.x > m) {
+    s = s * __expf(m - v.x) + v.y;
+    m = v.x;
+  } else {
+    s += v.y * __expf(v.x - m);
+  }
+}
+
+template <int G>
 __global__ void __launch_bounds__(kS1Threads)
     s1_hist_kernel(const float* __restrict__ logits, const float2* __restrict__ part1,
-                   const int32_t* __restrict__ ctx, int Hkv, int G, int L_max, int L_pad,
-                   int tiles_per_seg, int keys_per_cta, float* __restrict__ s1,
+                   const int32_t* __restrict__ ctx, int Hkv, int L_max, int L_pad,
+                   int parts, int keys_per_cta, float* __restrict__ s1,
                    uint32_t* __restrict__ hist) {
   __shared__ uint32_t sh[kHistBins];
   __shared__ float lse[8];
@@ -298,26 +471,48 @@ __global__ void __launch_bounds__(kS1Threads)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < kHistBins; i += kS1Threads) sh[i] = 0u;
   if (warp < G) {
-    const int ntiles = (L + kScanTileKeys - 1) / kScanTileKeys;
-    const float2* p = part1 + (size_t(n) * Hq + g * G + warp) * tiles_per_seg;
+    const int ntiles = (L + kPartKeys - 1) / kPartKeys;
+    const float2* p = part1 + (size_t(n) * Hq + g * G + warp) * parts;
     float m = -INFINITY, s = 0.f;
-    for (int t = lane; t < ntiles; t += 32) {
-      const float2 v = p[t];
-      if (v.x > m) { s = s * __expf(m - v.x) + v.y; m = v.x; }
-      else s += v.y * __expf(v.x - m);
+    for (int t0 = 0; t0 < ntiles; t0 += 32 * 8) {
+      float2 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int t = t0 + k * 32 + lane;
+        v[k] = t < ntiles ? p[t] : make_float2(-INFINITY, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) lse_merge(m, s, v[k]);
     }
     const float M = warp_max(m);
     s = warp_sum(m == -INFINITY ? 0.f : s * __expf(m - M));
     if (lane == 0) lse[warp] = M + __logf(s);
   }
   __syncthreads();
+  float lse_r[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) lse_r[h] = lse[h];
   const float* lg = logits + (size_t(n) * Hq + g * G) * L_pad;
   float* out = s1 + size_t(seg) * L_pad;
-  for (int j = j_begin + threadIdx.x; j < j_end; j += kS1Threads) {
-    float acc = 0.f;
-    for (int h = 0; h < G; ++h) acc += __expf(lg[size_t(h) * L_pad + j] - lse[h]);
-    out[j] = acc;
-    atomicAdd(&sh[(__float_as_uint(acc) >> kHistShift) & (kHistBins - 1)], 1u);
+  for (int jb = j_begin; jb < j_end; jb += kS1Threads * kS1Keys) {
+    float x[G][kS1Keys];
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int i = 0; i < kS1Keys; ++i) {
+        const int j = jb + i * kS1Threads + threadIdx.x;
+        x[h][i] = j < j_end ? lg[size_t(h) * L_pad + j] : 0.f;
+      }
+#pragma unroll
+    for (int i = 0; i < kS1Keys; ++i) {
+      const int j = jb + i * kS1Threads + threadIdx.x;
+      if (j >= j_end) break;
+      float acc = 0.f;
+#pragma unroll
+      for (int h = 0; h < G; ++h) acc += __expf(x[h][i] - lse_r[h]);
+      out[j] = acc;
+      atomicAdd(&sh[(__float_as_uint(acc) >> kHistShift) & (kHistBins - 1)], 1u);
+    }
   }
   __syncthreads();
   uint32_t* gh = hist + size_t(seg) * kHistBins;
@@ -331,13 +526,21 @@ cudaError_t launch_s1_hist(const herald_dims& dm, const float* logits, const flo
   const int segs = dm.N * dm.Hkv;
   int chunks = (2 * num_sms + segs - 1) / segs;
   int keys = cdiv(dm.L_max, chunks);
-  keys = cdiv(keys, 256) * 256;
-  if (keys < 1024) keys = 1024;
+  keys = cdiv(keys, kS1Threads * kS1Keys) * kS1Threads * kS1Keys;
   chunks = cdiv(dm.L_max, keys);
+  const dim3 grid(chunks, segs);
   trace_before(st, "s1_hist_kernel");
-  s1_hist_kernel<<<dim3(chunks, segs), kS1Threads, 0, st>>>(
-      logits, part1, ctx, dm.Hkv, dm.Hq / dm.Hkv, dm.L_max, w.L_pad, w.tiles_per_seg, keys, s1,
-      hist);
+  switch (dm.Hq / dm.Hkv) {
+#define HERALD_S1_G(GG)                                                                      \
+  case GG:                                                                                   \
+    s1_hist_kernel<GG><<<grid, kS1Threads, 0, st>>>(logits, part1, ctx, dm.Hkv, dm.L_max,    \
+                                                    w.L_pad, w.parts, keys, s1, hist);         \
+    break;
+    HERALD_S1_G(1) HERALD_S1_G(2) HERALD_S1_G(3) HERALD_S1_G(4)
+    HERALD_S1_G(5) HERALD_S1_G(6) HERALD_S1_G(7) HERALD_S1_G(8)
+#undef HERALD_S1_G
+    default: break;
+  }
   trace_after(st);
   return cudaGetLastError();
 }
@@ -414,10 +617,12 @@ __device__ void find_bin_from_top(const uint32_t* h, int nb, uint32_t need, uint
 constexpr int kSelThreads = 1024;
 constexpr int kTieCap = 6144;
 
-// Block-wide exclusive scan of two counters at once (1024 threads).
+// Block-wide exclusive scan of two counters at once (NT threads).
+template <int NT = 1024>
 __device__ __forceinline__ void block_excl_scan2(uint32_t a, uint32_t b, uint32_t* wa,
                                                  uint32_t* wb, uint32_t& ea, uint32_t& eb,
                                                  uint32_t& ta, uint32_t& tb) {
+  constexpr int NW = NT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t x = a, y = b;
 #pragma unroll
@@ -429,22 +634,43 @@ __device__ __forceinline__ void block_excl_scan2(uint32_t a, uint32_t b, uint32_
   if (lane == 31) { wa[warp] = x; wb[warp] = y; }
   __syncthreads();
   if (warp == 0) {
-    uint32_t u = wa[lane], v = wb[lane];
+    uint32_t u = lane < NW ? wa[lane] : 0u, v = lane < NW ? wb[lane] : 0u;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t ua = __shfl_up_sync(0xffffffffu, u, o);
       const uint32_t vb = __shfl_up_sync(0xffffffffu, v, o);
       if (lane >= o) { u += ua; v += vb; }
     }
-    wa[lane] = u;
-    wb[lane] = v;
+    if (lane < NW) { wa[lane] = u; wb[lane] = v; }
   }
   __syncthreads();
   ea = (warp ? wa[warp - 1] : 0u) + x - a;
   eb = (warp ? wb[warp - 1] : 0u) + y - b;
-  ta = wa[31];
-  tb = wb[31];
+  ta = wa[NW - 1];
+  tb = wb[NW - 1];
   __syncthreads();
+}
+
+// Elements of s1 are processed in rounds of kSelThreads * kPerThr: thread t
+// holds the kPerThr consecutive values [base + t*kPerThr, ...) in registers,
+// loaded as independent 16-byte loads so a round costs one memory latency.
+constexpr int kPerThr = 32;
+constexpr int kRound = kSelThreads * kPerThr;
+
+__device__ __forceinline__ void load_round(const uint32_t* sv, int L, int base,
+                                           uint32_t (&v)[kPerThr]) {
+  const int j0 = base + threadIdx.x * kPerThr;
+  if (j0 + kPerThr <= L) {
+    const uint4* p = reinterpret_cast<const uint4*>(sv + j0);
+#pragma unroll
+    for (int k = 0; k < kPerThr / 4; ++k) {
+      const uint4 x = p[k];
+      v[4 * k] = x.x; v[4 * k + 1] = x.y; v[4 * k + 2] = x.z; v[4 * k + 3] = x.w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < kPerThr; ++k) v[k] = (j0 + k < L) ? sv[j0 + k] : 0u;
+  }
 }
 
 __global__ void __launch_bounds__(kSelThreads)
@@ -477,11 +703,16 @@ __global__ void __launch_bounds__(kSelThreads)
   const uint32_t b1 = uint32_t(s_bin);
   need -= s_above;
   // collect the low 19 bits of the members of bin b1
-  for (int j = threadIdx.x; j < L; j += kSelThreads) {
-    const uint32_t v = sv[j];
-    if ((v >> 19) == b1) {
-      const uint32_t slot = atomicAdd(&s_cnt, 1u);
-      if (slot < kTieCap) tie_v[slot] = v & 0x7FFFFu;
+  for (int base = 0; base < L; base += kRound) {
+    uint32_t v[kPerThr];
+    load_round(sv, L, base, v);
+    const int j0 = base + threadIdx.x * kPerThr;
+#pragma unroll
+    for (int k = 0; k < kPerThr; ++k) {
+      if (j0 + k < L && (v[k] >> 19) == b1) {
+        const uint32_t slot = atomicAdd(&s_cnt, 1u);
+        if (slot < kTieCap) tie_v[slot] = v[k] & 0x7FFFFu;
+      }
     }
   }
   __syncthreads();
@@ -521,27 +752,38 @@ __global__ void __launch_bounds__(kSelThreads)
   find_bin_from_top<kSelThreads>(h, 256, need, wt, &s_bin, &s_above);
   const uint32_t tau = (b1 << 19) | (b2 << 8) | uint32_t(s_bin);
   const uint32_t need_eq = need - s_above;  // ties at tau to keep, lowest position first
-  // ordered compaction: thread t owns positions [t*E, (t+1)*E)
-  const int E = (L + kSelThreads - 1) / kSelThreads;
-  const int j0 = threadIdx.x * E, j1 = min(L, j0 + E);
-  uint32_t n_gt = 0, n_eq = 0;
-  for (int j = j0; j < j1; ++j) {
-    const uint32_t v = sv[j];
-    n_gt += v > tau;
-    n_eq += v == tau;
-  }
-  uint32_t gt_before, eq_before, gt_tot, eq_tot;
-  block_excl_scan2(n_gt, n_eq, wt, wt2, gt_before, eq_before, gt_tot, eq_tot);
-  for (int j = j0; j < j1; ++j) {
-    const uint32_t v = sv[j];
-    if (v > tau) {
-      const uint32_t pos = gt_before + min(eq_before, need_eq);
-      if (pos < uint32_t(Ce)) out[pos] = j;
-      ++gt_before;
-    } else if (v == tau) {
-      if (eq_before < need_eq && gt_before + eq_before < uint32_t(Ce)) out[gt_before + eq_before] = j;
-      ++eq_before;
+  // ordered compaction, one round of kRound positions at a time
+  uint32_t gt_run = 0, eq_run = 0;
+  for (int base = 0; base < L; base += kRound) {
+    uint32_t v[kPerThr];
+    load_round(sv, L, base, v);
+    const int j0 = base + threadIdx.x * kPerThr;
+    uint32_t n_gt = 0, n_eq = 0;
+#pragma unroll
+    for (int k = 0; k < kPerThr; ++k) {
+      const bool in = j0 + k < L;
+      n_gt += in && v[k] > tau;
+      n_eq += in && v[k] == tau;
     }
+    uint32_t gt_before, eq_before, gt_tot, eq_tot;
+    block_excl_scan2<kSelThreads>(n_gt, n_eq, wt, wt2, gt_before, eq_before, gt_tot, eq_tot);
+    gt_before += gt_run;
+    eq_before += eq_run;
+#pragma unroll
+    for (int k = 0; k < kPerThr; ++k) {
+      if (j0 + k >= L) break;
+      if (v[k] > tau) {
+        const uint32_t pos = gt_before + min(eq_before, need_eq);
+        if (pos < uint32_t(Ce)) out[pos] = j0 + k;
+        ++gt_before;
+      } else if (v[k] == tau) {
+        if (eq_before < need_eq && gt_before + eq_before < uint32_t(Ce))
+          out[gt_before + eq_before] = j0 + k;
+        ++eq_before;
+      }
+    }
+    gt_run += gt_tot;
+    eq_run += eq_tot;
   }
 }
 
@@ -556,75 +798,111 @@ cudaError_t launch_topc(const herald_dims& dm, const float* s1, const uint32_t* 
 }
 
 // ============================================================= topk_union
-// One CTA of 1024 threads per (n, g).  s2 of the n_cand candidates is held in
-// shared memory; a 4 x 8-bit radix select finds the K-th largest, ties go to
-// the lower slot (= lower position, candidates being ascending).  The output
-// is [0, sink_end) ++ kept candidates in [sink_end, local_begin) ++
-// [local_begin, L), which is the deduplicated ascending union.
-__global__ void __launch_bounds__(kSelThreads)
+// One CTA of 512 threads per (n, g); thread t holds the stage-2 scores of the
+// candidate slots [t*E, (t+1)*E) in registers (E <= 32, C <= 16384).  Radix
+// select of the K-th largest: a 12-bit first digit over all scores, then the
+// members of that bin (in shared memory) resolve the remaining 19 bits.  Ties
+// go to the lower slot = lower position (candidates are ascending).  Output:
+// [0, sink_end) ++ kept candidates inside [sink_end, local_begin) ++
+// [local_begin, L) -- the deduplicated ascending union.
+constexpr int kTkThreads = 512;
+constexpr int kTkPer = kMaxC / kTkThreads;  // 32
+
+__global__ void __launch_bounds__(kTkThreads)
     topk_union_kernel(const int32_t* __restrict__ ctx, const int32_t* __restrict__ cand,
                       const int32_t* __restrict__ n_cand, const float* __restrict__ s2, int Hkv,
                       int L_max, int C, int K, int S, int W, int P_max, int32_t* __restrict__ idx,
                       int32_t* __restrict__ n_sel) {
-  extern __shared__ uint32_t sv[];  // [C]
-  __shared__ uint32_t h[256];
-  __shared__ uint32_t wt[32];
+  extern __shared__ uint32_t mem[];  // [C] bin members (low 19 bits)
+  __shared__ uint32_t h[kHistBins];
+  __shared__ uint32_t wt[32], wt2[32];
   __shared__ int s_bin;
-  __shared__ uint32_t s_above;
+  __shared__ uint32_t s_above, s_cnt;
   const int seg = blockIdx.x, n = seg / Hkv;
   const int L = min(max(ctx[n], 0), L_max);
   const int nc = min(max(n_cand[seg], 0), C);
   const int Ke = min(K, nc);
+  const int E = (nc + kTkThreads - 1) / kTkThreads;
+  const int i0 = threadIdx.x * E;
   const int32_t* cd = cand + size_t(seg) * C;
-  for (int i = threadIdx.x; i < nc; i += kSelThreads)
-    sv[i] = __float_as_uint(fmaxf(s2[size_t(seg) * C + i], 0.f));
-  __syncthreads();
+  const float* sc = s2 + size_t(seg) * C;
+  uint32_t v[kTkPer];
+#pragma unroll
+  for (int k = 0; k < kTkPer; ++k)
+    v[k] = (k < E && i0 + k < nc) ? __float_as_uint(fmaxf(sc[i0 + k], 0.f)) : 0u;
+  const bool take_all = (Ke == nc);
   uint32_t tau = 0, need_eq = 0;
-  bool take_all = (Ke == nc);
   if (!take_all && Ke > 0) {
-    uint32_t need = uint32_t(Ke), prefix = 0;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = threadIdx.x; i < 256; i += kSelThreads) h[i] = 0u;
-      __syncthreads();
-      for (int i = threadIdx.x; i < nc; i += kSelThreads) {
-        const uint32_t v = sv[i];
-        if (shift == 24 || (v >> (shift + 8)) == prefix) atomicAdd(&h[(v >> shift) & 255u], 1u);
-      }
-      __syncthreads();
-      find_bin_from_top<kSelThreads>(h, 256, need, wt, &s_bin, &s_above);
-      prefix = (prefix << 8) | uint32_t(s_bin);
-      need -= s_above;
-    }
-    tau = prefix;
-    need_eq = need;
+    for (int i = threadIdx.x; i < kHistBins; i += kTkThreads) h[i] = 0u;
+    if (threadIdx.x == 0) s_cnt = 0;
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kTkPer; ++k)
+      if (k < E && i0 + k < nc) atomicAdd(&h[v[k] >> 19], 1u);
+    __syncthreads();
+    uint32_t need = uint32_t(Ke);
+    find_bin_from_top<kTkThreads>(h, kHistBins, need, wt, &s_bin, &s_above);
+    const uint32_t b1 = uint32_t(s_bin);
+    need -= s_above;
+#pragma unroll
+    for (int k = 0; k < kTkPer; ++k)
+      if (k < E && i0 + k < nc && (v[k] >> 19) == b1) mem[atomicAdd(&s_cnt, 1u)] = v[k] & 0x7FFFFu;
+    for (int i = threadIdx.x; i < 2048; i += kTkThreads) h[i] = 0u;
+    __syncthreads();
+    const uint32_t cnt = s_cnt;
+    for (uint32_t i = threadIdx.x; i < cnt; i += kTkThreads) atomicAdd(&h[mem[i] >> 8], 1u);
+    __syncthreads();
+    find_bin_from_top<kTkThreads>(h, 2048, need, wt, &s_bin, &s_above);
+    const uint32_t b2 = uint32_t(s_bin);
+    need -= s_above;
+    for (int i = threadIdx.x; i < 256; i += kTkThreads) h[i] = 0u;
+    __syncthreads();
+    for (uint32_t i = threadIdx.x; i < cnt; i += kTkThreads)
+      if ((mem[i] >> 8) == b2) atomicAdd(&h[mem[i] & 255u], 1u);
+    __syncthreads();
+    find_bin_from_top<kTkThreads>(h, 256, need, wt, &s_bin, &s_above);
+    tau = (b1 << 19) | (b2 << 8) | uint32_t(s_bin);
+    need_eq = need - s_above;
   }
   const int sink_end = min(S, L);
   const int local_begin = max(L - W, sink_end);
-  int32_t* out = idx + size_t(seg) * P_max;
-  // middle part, in slot order
-  uint32_t base = 0, eq_base = 0;
-  for (int i0 = 0; i0 < nc; i0 += kSelThreads) {
-    const int i = i0 + threadIdx.x;
-    const bool in = i < nc;
-    const uint32_t v = in ? sv[i] : 0u;
-    const uint32_t is_eq = (in && !take_all && Ke > 0 && v == tau) ? 1u : 0u;
-    uint32_t eq_tot;
-    const uint32_t eq_rank = eq_base + block_excl_scan<kSelThreads>(is_eq, wt, eq_tot);
-    bool keep = in && Ke > 0 && (take_all || v > tau || (is_eq && eq_rank < need_eq));
-    int pos = in ? cd[i] : -1;
-    keep = keep && pos >= sink_end && pos < local_begin;
-    uint32_t tot;
-    const uint32_t at = base + block_excl_scan<kSelThreads>(keep ? 1u : 0u, wt, tot);
-    if (keep && sink_end + int(at) < P_max) out[sink_end + at] = pos;
-    base += tot;
-    eq_base += eq_tot;
+  // which of my slots are kept: above tau, or among the first need_eq ties
+  uint32_t n_eq = 0;
+#pragma unroll
+  for (int k = 0; k < kTkPer; ++k)
+    n_eq += (!take_all && Ke > 0 && k < E && i0 + k < nc && v[k] == tau) ? 1u : 0u;
+  uint32_t eq_before, dummy0, eq_tot, dummy1;
+  block_excl_scan2<kTkThreads>(n_eq, 0u, wt, wt2, eq_before, dummy0, eq_tot, dummy1);
+  uint32_t keep_mask = 0, n_keep = 0;
+#pragma unroll
+  for (int k = 0; k < kTkPer; ++k) {
+    const bool in = k < E && i0 + k < nc;
+    bool keep = in && Ke > 0;
+    if (keep && !take_all) {
+      if (v[k] == tau) keep = eq_before++ < need_eq;
+      else keep = v[k] > tau;
+    }
+    if (keep) {
+      const int p = cd[i0 + k];
+      keep = p >= sink_end && p < local_begin;
+    }
+    if (keep) { keep_mask |= 1u << k; ++n_keep; }
   }
-  const int n_mid = int(base);
-  for (int j = threadIdx.x; j < sink_end; j += kSelThreads) out[j] = j;
-  for (int j = local_begin + threadIdx.x; j < L; j += kSelThreads)
-    if (sink_end + n_mid + (j - local_begin) < P_max) out[sink_end + n_mid + (j - local_begin)] = j;
-  const int total = min(P_max, sink_end + n_mid + (L - local_begin));
-  for (int s = total + threadIdx.x; s < P_max; s += kSelThreads) out[s] = -1;
+  uint32_t at, dummy2, n_mid, dummy3;
+  block_excl_scan2<kTkThreads>(n_keep, 0u, wt, wt2, at, dummy2, n_mid, dummy3);
+  int32_t* out = idx + size_t(seg) * P_max;
+#pragma unroll
+  for (int k = 0; k < kTkPer; ++k)
+    if ((keep_mask >> k) & 1u) {
+      if (sink_end + int(at) < P_max) out[sink_end + at] = cd[i0 + k];
+      ++at;
+    }
+  for (int j = threadIdx.x; j < sink_end; j += kTkThreads) out[j] = j;
+  for (int j = local_begin + threadIdx.x; j < L; j += kTkThreads)
+    if (sink_end + int(n_mid) + (j - local_begin) < P_max)
+      out[sink_end + n_mid + (j - local_begin)] = j;
+  const int total = min(P_max, sink_end + int(n_mid) + (L - local_begin));
+  for (int s = total + threadIdx.x; s < P_max; s += kTkThreads) out[s] = -1;
   if (threadIdx.x == 0) n_sel[seg] = total;
 }
 
@@ -640,9 +918,9 @@ cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const i
     attr_done = true;
   }
   trace_before(st, "topk_union_kernel");
-  topk_union_kernel<<<dm.N * dm.Hkv, kSelThreads, smem, st>>>(ctx, cand, n_cand, s2, dm.Hkv,
-                                                               dm.L_max, C, K, S, W, P_max, idx,
-                                                               n_sel);
+  topk_union_kernel<<<dm.N * dm.Hkv, kTkThreads, smem, st>>>(ctx, cand, n_cand, s2, dm.Hkv,
+                                                              dm.L_max, C, K, S, W, P_max, idx,
+                                                              n_sel);
   trace_after(st);
   return cudaGetLastError();
 }

@@ -551,17 +551,15 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kTcThread
   const int n_pool = (ns + kAttnKeys - 1) / kAttnKeys;
   const int n_tiles = n_pool + (B + kAttnKeys - 1) / kAttnKeys;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // this CTA's tiles
-  int tiles[2], nk[2], nt = 0;
-  for (int k = 0; k < 2; ++k) {
-    const int t = int(rank) + k * kClusterCtas;
-    if (t < n_tiles) {
-      tiles[nt] = t;
-      nk[nt] = t < n_pool ? min(kAttnKeys, ns - t * kAttnKeys)
-                          : min(kAttnKeys, B - (t - n_pool) * kAttnKeys);
-      ++nt;
-    }
-  }
+  // this CTA's tiles: t0 = rank, t1 = rank + kClusterCtas (scalars, not
+  // arrays, so that they stay in registers)
+  const int t0 = int(rank), t1 = int(rank) + kClusterCtas;
+  const int nt = (t0 < n_tiles) + (t1 < n_tiles);
+  auto tile_keys = [&](int t) {
+    return t < n_pool ? min(kAttnKeys, ns - t * kAttnKeys)
+                      : min(kAttnKeys, B - (t - n_pool) * kAttnKeys);
+  };
+  const int nk0 = nt > 0 ? tile_keys(t0) : 0, nk1 = nt > 1 ? tile_keys(t1) : 0;
   if (threadIdx.x == 0) {
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
@@ -582,7 +580,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kTcThread
       return q + ((size_t(n) * B + b) * Hq + g * G + hl) * D;
     });
     for (int k = 0; k < nt; ++k) {
-      const int t = tiles[k], cnt = nk[k];
+      const int t = k ? t1 : t0, cnt = k ? nk1 : nk0;
       const bool pool_tile = t < n_pool;
       const int k0 = pool_tile ? t * kAttnKeys : (t - n_pool) * kAttnKeys;
       load_rows_sw128<D>(Ks[k], kAttnKeys, kAttnKeys, block_k, [&](int r) -> const uint16_t* {
@@ -593,7 +591,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kTcThread
     }
     cp_async_commit();
     for (int k = 0; k < nt; ++k) {
-      const int t = tiles[k], cnt = nk[k];
+      const int t = k ? t1 : t0, cnt = k ? nk1 : nk0;
       const bool pool_tile = t < n_pool;
       const int k0 = pool_tile ? t * kAttnKeys : (t - n_pool) * kAttnKeys;
       load_rows_sw128<D>(Vs[k], kAttnKeys, kAttnKeys, block_v, [&](int r) -> const uint16_t* {
@@ -639,7 +637,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kTcThread
       for (int i = 0; i < 32; ++i) x[k][32 + i] = v[i];
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        x[k][i] = (ch * 64 + i < nk[k]) ? x[k][i] * scale : -INFINITY;
+        x[k][i] = (ch * 64 + i < (k ? nk1 : nk0)) ? x[k][i] * scale : -INFINITY;
         m = fmaxf(m, x[k][i]);
       }
     }
@@ -706,29 +704,38 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kTcThread
     if (ch == 0) ml[row] = make_float2(-INFINITY, 0.f);
   }
   cluster_sync_all();
-  // merge: this CTA finalises rows [rank*RPC, (rank+1)*RPC)
+  // merge: this CTA finalises rows [rank*RPC, (rank+1)*RPC); every peer
+  // value of a row is requested before any is used (one remote round trip)
   constexpr int RPC = kTileM / kClusterCtas;   // 16 rows, 2 per warp
-  constexpr int E = D / 32;
+  constexpr int E = D / 32;                    // features per lane
   for (int rr = warp; rr < RPC; rr += kTcThreads / 32) {
     const int lr = int(rank) * RPC + rr;
     const int grow = mt * kTileM + lr;
-    float M = -INFINITY;
     float2 pm[kClusterCtas];
+    float o[kClusterCtas][E];
 #pragma unroll
     for (int c = 0; c < kClusterCtas; ++c) {
       pm[c] = *peer_ptr(&ml[lr], uint32_t(c));
-      M = fmaxf(M, pm[c].x);
+      const float* src = peer_ptr(Os + lr * Cfg::kORow + lane * E, uint32_t(c));
+      if constexpr (E == 4) {
+        const float4 f = *reinterpret_cast<const float4*>(src);
+        o[c][0] = f.x; o[c][1] = f.y; o[c][2] = f.z; o[c][3] = f.w;
+      } else {
+        const float2 f = *reinterpret_cast<const float2*>(src);
+        o[c][0] = f.x; o[c][1] = f.y;
+      }
     }
+    float M = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kClusterCtas; ++c) M = fmaxf(M, pm[c].x);
     float acc[E] = {};
     float L = 0.f;
 #pragma unroll
     for (int c = 0; c < kClusterCtas; ++c) {
-      if (pm[c].x == -INFINITY) continue;
-      const float wgt = __expf(pm[c].x - M);
+      const float wgt = pm[c].x == -INFINITY ? 0.f : __expf(pm[c].x - M);
       L += wgt * pm[c].y;
-      const float* o = peer_ptr(Os + lr * Cfg::kORow + lane * E, uint32_t(c));
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] += wgt * o[e];
+      for (int e = 0; e < E; ++e) acc[e] += wgt == 0.f ? 0.f : wgt * o[c][e];
     }
     if (grow < R) {
       const int b = grow / G, h = g * G + (grow - (grow / G) * G);
