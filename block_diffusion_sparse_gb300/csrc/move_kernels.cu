@@ -62,7 +62,10 @@ cudaError_t launch_gather(const herald_dims& dm, const int32_t* idx, const int32
 }
 
 // grid N, block 256: one CTA per sequence so that reading ctx_len[n] and
-// advancing it cannot race with another CTA.
+// advancing it cannot race with another CTA.  Each thread moves up to
+// kAppendBatch 16-byte chunks of K and of V per round, all loads first.
+constexpr int kAppendBatch = 8;
+
 __global__ void __launch_bounds__(256)
     append_kernel(const uint16_t* __restrict__ bk, const uint16_t* __restrict__ bv, int B,
                   int Hkv, int d, int L_max, int32_t* __restrict__ ctx,
@@ -71,15 +74,32 @@ __global__ void __launch_bounds__(256)
   const int n = blockIdx.x;
   if (threadIdx.x == 0) L0 = min(max(ctx[n], 0), L_max);
   __syncthreads();
-  const int cpr = d / 8;
-  for (int q = threadIdx.x; q < B * Hkv * cpr; q += blockDim.x) {
-    const int c = q % cpr, bg = q / cpr, g = bg % Hkv, b = bg / Hkv;
-    const int j = L0 + b;
-    if (j >= L_max) continue;
-    const size_t src = ((size_t(n) * B + b) * Hkv + g) * d + c * 8;
-    const size_t dst = ((size_t(n) * Hkv + g) * L_max + j) * d + c * 8;
-    *reinterpret_cast<uint4*>(kc + dst) = *reinterpret_cast<const uint4*>(bk + src);
-    *reinterpret_cast<uint4*>(vc + dst) = *reinterpret_cast<const uint4*>(bv + src);
+  const int cpr = d / 8, total = B * Hkv * cpr;
+  for (int q0 = 0; q0 < total; q0 += 256 * kAppendBatch) {
+    uint4 k[kAppendBatch], v[kAppendBatch];
+#pragma unroll
+    for (int u = 0; u < kAppendBatch; ++u) {
+      const int q = q0 + u * 256 + threadIdx.x;
+      if (q < total) {
+        const int c = q % cpr, bg = q / cpr, g = bg % Hkv, b = bg / Hkv;
+        const size_t src = ((size_t(n) * B + b) * Hkv + g) * d + c * 8;
+        k[u] = *reinterpret_cast<const uint4*>(bk + src);
+        v[u] = *reinterpret_cast<const uint4*>(bv + src);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kAppendBatch; ++u) {
+      const int q = q0 + u * 256 + threadIdx.x;
+      if (q < total) {
+        const int c = q % cpr, bg = q / cpr, g = bg % Hkv, b = bg / Hkv;
+        const int j = L0 + b;
+        if (j < L_max) {
+          const size_t dst = ((size_t(n) * Hkv + g) * L_max + j) * d + c * 8;
+          *reinterpret_cast<uint4*>(kc + dst) = k[u];
+          *reinterpret_cast<uint4*>(vc + dst) = v[u];
+        }
+      }
+    }
   }
   __syncthreads();
   if (advance && threadIdx.x == 0) ctx[n] = min(L0 + B, L_max);

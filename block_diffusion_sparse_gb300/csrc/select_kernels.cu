@@ -93,7 +93,10 @@ struct TcScanCfg {
   static constexpr int kTileBytes = kHalves * kHalfBytes;
   static constexpr int kBHalfBytes = kQhlRows * 128;
   static constexpr int kBBytes = kHalves * kBHalfBytes;
-  static constexpr int kSmem = kTcScanStages * kTileBytes + 2048 + 1024;
+  static constexpr int kSmem = kTcScanStages * kTileBytes + kBBytes + 1024;
+  // ring + operand + alignment slack must fit the dynamic allocation
+  static_assert(kSmem >= kTcScanStages * kTileBytes + kBBytes + 1023, "scan smem layout");
+  static_assert(kSmem <= 227 * 1024, "scan smem exceeds the per-CTA limit");
 };
 constexpr int kTcScanThreads = 192;
 
@@ -259,6 +262,7 @@ struct ScanCfg {
   static constexpr int kHalfBytes = kScanTileKeys * 128;
   static constexpr int kTileBytes = kHalves * kHalfBytes;
   static constexpr int kSmem = kScanWarps * kScanStages * kTileBytes + 1024;
+  static_assert(kSmem <= 227 * 1024, "scan smem exceeds the per-CTA limit");
 };
 
 template <int D, int G>

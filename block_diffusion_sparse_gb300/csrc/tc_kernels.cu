@@ -70,6 +70,7 @@ struct Ref1Cfg {
   static constexpr int kQBytes = kHalves * kTileM * 128;
   static constexpr int kKBytes = kHalves * kRefineChunk * 128;
   static constexpr int kSmem = kQBytes + kKBytes + 1024;
+  static_assert(kSmem <= 227 * 1024, "refine pass 1 smem exceeds the per-CTA limit");
 };
 
 template <int D>
@@ -83,6 +84,7 @@ __global__ void __launch_bounds__(kTcThreads)
   __shared__ uint64_t bar;
   __shared__ uint32_t tmem_base;
   __shared__ float2 red[2][kTileM];
+  __shared__ int32_t pos[kRefineChunk];
   uint8_t* Qs = align1024(smem_raw);
   uint8_t* Ks = Qs + Cfg::kQBytes;
   const int chunk = blockIdx.x, mt = blockIdx.y, seg = blockIdx.z;
@@ -104,11 +106,18 @@ __global__ void __launch_bounds__(kTcThreads)
     const int b = row / G, hl = row - (row / G) * G;
     return q_block + ((size_t(n) * B + b) * Hq + g * G + hl) * D;
   });
+  // candidate positions first (one coalesced load), then the row copies
   const int32_t* cd = cand + size_t(seg) * C;
+  for (int r = threadIdx.x; r < kRefineChunk; r += kTcThreads)
+    pos[r] = c0 + r < nc ? cd[c0 + r] : -1;
+  // positions outside the cache (a caller error) read as zero rows
+  for (int r = threadIdx.x; r < kRefineChunk; r += kTcThreads)
+    if (pos[r] >= L_max) pos[r] = -1;
+  __syncthreads();
   load_rows_sw128<D>(Ks, kRefineChunk, kRefineChunk, kc, [&](int r) -> const uint16_t* {
-    const int ci = c0 + r;
-    if (ci >= nc) return nullptr;
-    return kc + (size_t(seg) * L_max + cd[ci]) * D;
+    const int p = pos[r];
+    if (p < 0) return nullptr;
+    return kc + (size_t(seg) * L_max + p) * D;
   });
   cp_async_commit();
   cp_async_wait_all();
@@ -172,6 +181,7 @@ struct Ref2Cfg {
   static constexpr int kKBytes = kHalves * kRefineRows2 * 128;
   static constexpr int kQBytes = kHalves * 256 * 128;
   static constexpr int kSmem = kKBytes + kQBytes + 1024;
+  static_assert(kSmem <= 227 * 1024, "refine pass 2 smem exceeds the per-CTA limit");
 };
 
 template <int D>
@@ -187,6 +197,7 @@ __global__ void __launch_bounds__(kTcThreads)
   __shared__ uint32_t tmem_base;
   __shared__ float lse[256];
   __shared__ float red[2][kRefineRows2];
+  __shared__ int32_t pos[kRefineRows2];
   uint8_t* Ks = align1024(smem_raw);
   uint8_t* Qs = Ks + Cfg::kKBytes;
   const int seg = blockIdx.y, n = seg / Hkv, g = seg - n * Hkv, G = Hq / Hkv;
@@ -203,10 +214,13 @@ __global__ void __launch_bounds__(kTcThreads)
   const uint32_t tbase = tmem_base;
 
   const int32_t* cd = cand + size_t(seg) * C;
+  for (int r = threadIdx.x; r < kRefineRows2; r += kTcThreads)
+    pos[r] = (c0 + r < nc && cd[c0 + r] < L_max) ? cd[c0 + r] : -1;
+  __syncthreads();
   load_rows_sw128<D>(Ks, kRefineRows2, kRefineRows2, kc, [&](int r) -> const uint16_t* {
-    const int ci = c0 + r;
-    if (ci >= nc) return nullptr;
-    return kc + (size_t(seg) * L_max + cd[ci]) * D;
+    const int p = pos[r];
+    if (p < 0) return nullptr;
+    return kc + (size_t(seg) * L_max + p) * D;
   });
   load_rows_sw128<D>(Qs, Rp, 256, q_block, [&](int r) -> const uint16_t* {
     if (r >= R) return nullptr;
@@ -328,6 +342,7 @@ struct AttnCfg {
   static constexpr int kVBytes = kHalves * kAttnKeys * 128;
   static constexpr int kPBytes = 2 * kTileM * 128;  // 128 rows x 128 keys, 2 key halves
   static constexpr int kSmem = kQBytes + kKBytes + kVBytes + kPBytes + 1024;
+  static_assert(kSmem <= 227 * 1024, "attention smem exceeds the per-CTA limit");
 };
 
 template <int D>
@@ -506,6 +521,8 @@ struct AttnClCfg {
   static constexpr int kORow = D + 4;                  // fp32 row stride of the O partial
   static constexpr int kSmem = kBytes + 1024;
   static_assert(128 * kORow * 4 <= kTile + 2 * kPT, "O partial must fit over Q, P0, P1");
+  static_assert(kV1 + kTile == kBytes, "cluster attention smem layout");
+  static_assert(kSmem <= 227 * 1024, "cluster attention smem exceeds the per-CTA limit");
 };
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
