@@ -128,9 +128,17 @@ def job_value(ms_per_step: float, world: int, tokens_per_step: int) -> float:
 
 
 # --------------------------------------------------------------------------- workload
+WORKLOADS = {"qwen": "QWEN_32K", "tiny": "TINY", "llama": "LLAMA_64K",
+             "long-host": "LONG_128K_HOST"}
+_WORKLOAD = "qwen"
+
+
 def workload():
-    from block_diffusion_sparse_gb300.workloads import QWEN_32K
-    return QWEN_32K
+    """The benchmarked layer: the 32K Qwen2.5-7B-like layer unless --workload
+    names another (tiny, llama = 4 x 64K Llama-8B-like, long-host = 128K
+    context with the cache in pinned host memory)."""
+    from block_diffusion_sparse_gb300 import workloads as W
+    return getattr(W, WORKLOADS[_WORKLOAD])
 
 
 def kernel_source_hash() -> str:
@@ -167,11 +175,18 @@ class Bench:
         self.d = H.dims_of(w)
         self.P = w.P
         cache_bytes = 2 * x["k_cache"].nbytes
-        self.n_rot = max(2, int(np.ceil(2 * L2_BYTES / cache_bytes)) + 1)
-        self.n_rot += self.n_rot % 2      # even: block parity = cache-copy parity
-        k0, v0 = dev(x["k_cache"]), dev(x["v_cache"])
-        self.k = [k0] + [k0.clone() for _ in range(self.n_rot - 1)]
-        self.v = [v0] + [v0.clone() for _ in range(self.n_rot - 1)]
+        if w.kv_on_host:
+            # the cache stays in pinned host memory; kernels read it over the link
+            host = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).pin_memory()
+            self.n_rot = 2
+            k0, v0 = host(x["k_cache"]), host(x["v_cache"])
+            self.k, self.v = [k0, k0], [v0, v0]
+        else:
+            self.n_rot = max(2, int(np.ceil(2 * L2_BYTES / cache_bytes)) + 1)
+            self.n_rot += self.n_rot % 2      # even: block parity = cache-copy parity
+            k0, v0 = dev(x["k_cache"]), dev(x["v_cache"])
+            self.k = [k0] + [k0.clone() for _ in range(self.n_rot - 1)]
+            self.v = [v0] + [v0.clone() for _ in range(self.n_rot - 1)]
         self.q_merge = dev(x["q_merge"])
         self.q_steps = dev(x["q_steps"])
         self.bk, self.bv = dev(x["block_k"]), dev(x["block_v"])
@@ -247,7 +262,9 @@ def algorithmic_work(w, n_sel: np.ndarray) -> dict:
             + 2 * w.N * w.B * w.Hq * w.d * 2,
             "flops": int((4 * R * keys * w.d).sum())}
     return {
-        "scan_kernel": {"bound": "hbm", "bytes": NG * w.L * w.d * 2},
+        "scan_tc_kernel": {"bound": "hbm", "bytes": NG * w.L * w.d * 2},
+        "scan_cc_kernel": {"bound": "link" if w.kv_on_host else "hbm",
+                           "bytes": NG * w.L * w.d * 2},
         "attn_kernel": attn,
         "attn_cluster_kernel": attn,
         "gather_kernel": {"bound": "hbm", "bytes": int(ns.sum()) * w.d * 2 * 2 * 2},
@@ -415,7 +432,7 @@ def run_ours(args, rank, world, dist):
         if not wk or name not in avg:
             return None
         d_s = avg[name] * 1e-3
-        if wk["bound"] == "hbm":
+        if wk["bound"] in ("hbm", "link"):
             ach = wk["bytes"] / d_s / 1e9
             peak = pk["hbm_gbs"]
             unit = "GB/s"
@@ -426,13 +443,14 @@ def run_ours(args, rank, world, dist):
         return {"bound": wk["bound"], "achieved": ach, "peak": peak, "unit": unit,
                 "frac": ach / peak, "traffic": ncu_traffic(name, src_hash),
                 "kernel": name, "launch_us": avg[name] * 1e3,
-                "algorithmic_bytes" if wk["bound"] == "hbm" else "algorithmic_flops":
-                    wk["bytes"] if wk["bound"] == "hbm" else wk["flops"],
+                "algorithmic_bytes" if "bytes" in wk and wk["bound"] != "tensor"
+                else "algorithmic_flops":
+                    wk["bytes"] if "bytes" in wk and wk["bound"] != "tensor" else wk["flops"],
                 "peak_source": f"{pk_kind} (MEASURED_PEAKS.json)" if pk_kind == "measured"
                 else "fallback"}
 
     roofline = roof(dominant) or roof("attn_cluster_kernel") or roof("attn_kernel")
-    scan = roof("scan_kernel")
+    scan = roof("scan_tc_kernel") or roof("scan_cc_kernel")
 
     # end to end through the C ABI with host buffers
     e2e = run_e2e(b, args, dist)
@@ -444,8 +462,10 @@ def run_ours(args, rank, world, dist):
             "config": {"workload": w.name, "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
                        "ctx": w.L, "B": w.B, "T": w.T, "C": w.C, "K": w.K, "sink": w.S,
                        "local": w.W, "parallelism": f"replicas x{world}",
-                       "l2": f"cold: K/V cache rotated over {nrot} copies "
-                             f"({nrot * 2 * b.x['k_cache'].nbytes / 2**20:.0f} MiB > L2)",
+                       "l2": ("K/V cache in pinned host memory (read over the host link)"
+                              if w.kv_on_host else
+                              f"cold: K/V cache rotated over {nrot} copies "
+                              f"({nrot * 2 * b.x['k_cache'].nbytes / 2**20:.0f} MiB > L2)"),
                        "timing": "CUDA-graph replay of whole steps, CUDA events"},
             "roofline": roofline,
             "serial": {"ms_per_step": serial_ms, "value": job_value(serial_ms, world, w.N * w.B),
@@ -517,7 +537,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="qwen", choices=sorted(WORKLOADS))
     args = ap.parse_args()
+    global _WORKLOAD
+    _WORKLOAD = args.workload
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

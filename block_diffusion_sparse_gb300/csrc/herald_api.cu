@@ -170,11 +170,13 @@ herald_status run_stage1(const herald_dims& dm, const uint16_t* q_merge, const u
   float* s1 = at<float>(ws, w.s1);
   uint32_t* hist = at<uint32_t>(ws, w.hist);
   const int nsm = sm_count();
-  HERALD_TRY_CUDA(launch_merge_query(dm, q_merge, qbar, qhl, hist, st), "merge_query launch");
+  const int part_slots = scan_grid(dm, w, tma, nsm) * 4;  // one slot per (scan CTA, warp)
+  HERALD_TRY_CUDA(launch_merge_query(dm, q_merge, qbar, qhl, hist, part1, part_slots, st),
+                  "merge_query launch");
   HERALD_TRY_CUDA(launch_scan(dm, tma ? &kmap : nullptr, tma ? &bmap : nullptr, k_cache, qbar,
                               ctx_len, logits, part1, w, err, nsm, st),
                   "scan launch");
-  HERALD_TRY_CUDA(launch_s1_hist(dm, logits, part1, ctx_len, s1, hist, w, nsm, st),
+  HERALD_TRY_CUDA(launch_s1_hist(dm, logits, part1, part_slots, ctx_len, s1, hist, w, nsm, st),
                   "s1_hist launch");
   HERALD_TRY_CUDA(launch_topc(dm, s1, hist, ctx_len, C, cand, n_cand, w, st), "topc launch");
   return HERALD_OK;

@@ -16,7 +16,8 @@ constexpr int kScanWarps = 4;       // warps per CTA, each with its own ring
 constexpr int kScanStages = 3;      // stages per warp
 constexpr int kTcScanKeys = 128;    // tensor-core scan: keys per tile (UMMA M)
 constexpr int kTcScanStages = 4;    // TMA ring depth of the tensor-core scan
-constexpr int kPartKeys = 32;       // keys per stage-1 (max, sumexp) partial
+constexpr int kScanMaxCtas = 256;   // upper bound of either scan's persistent grid
+constexpr int kPartSlots = kScanMaxCtas * 4;  // stage-1 (max, sumexp) slots: one per (CTA, warp)
 constexpr int kQhlRows = 16;        // merged-query operand rows: 8 hi + 8 lo
 // ---- stage-1 score histogram (bits [30:19] of a non-negative fp32)
 constexpr int kHistBins = 4096;
@@ -37,7 +38,7 @@ struct WsLayout {
   size_t qbar;       // float [N][Hq][d]        merged queries, pre-scaled
   size_t qhl;        // bf16 [N*Hkv][16][d]     merged queries as hi/lo bf16 rows
   size_t logits;     // float [N][Hq][L_pad]    stage-1 logits
-  size_t part1;      // float2 [N][Hq][parts]   per-32-key (max, sumexp)
+  size_t part1;      // float2 [N][Hq][kPartSlots] per-(CTA, warp) (max, sumexp)
   size_t s1;         // float [N][Hkv][L_pad]   stage-1 scores
   size_t hist;       // uint32 [N*Hkv][kHistBins]
   size_t cand;       // int32 [N][Hkv][C]       (herald_select only)
@@ -47,7 +48,7 @@ struct WsLayout {
   size_t opart;      // float [N*Hkv][MT][S][128][d]      attention partials
   size_t ml;         // float2 [N*Hkv][MT][S][128]
   size_t total;
-  int L_pad, tiles_per_seg, tiles128, parts, R, MT, n_chunks, splits;
+  int L_pad, tiles_per_seg, tiles128, R, MT, n_chunks, splits;
 };
 
 inline WsLayout ws_layout(const herald_dims& dm, int C, int P_max) {
@@ -57,7 +58,6 @@ inline WsLayout ws_layout(const herald_dims& dm, int C, int P_max) {
   w.L_pad = cdiv(dm.L_max, kTcScanKeys) * kTcScanKeys;
   w.tiles_per_seg = w.L_pad / kScanTileKeys;
   w.tiles128 = w.L_pad / kTcScanKeys;
-  w.parts = w.L_pad / kPartKeys;
   w.R = dm.B * G;
   w.MT = cdiv(w.R, kTileM);
   w.n_chunks = cdiv(C, kRefineChunk);
@@ -68,7 +68,7 @@ inline WsLayout ws_layout(const herald_dims& dm, int C, int P_max) {
   w.qbar = o;   o = align_up(o + NH * dm.d * 4, A);
   w.qhl = o;    o = align_up(o + NG * kQhlRows * dm.d * 2, A);
   w.logits = o; o = align_up(o + NH * w.L_pad * 4, A);
-  w.part1 = o;  o = align_up(o + NH * w.parts * 8, A);
+  w.part1 = o;  o = align_up(o + NH * kPartSlots * 8, A);
   w.s1 = o;     o = align_up(o + NG * w.L_pad * 4, A);
   w.hist = o;   o = align_up(o + NG * kHistBins * 4, A);
   w.cand = o;   o = align_up(o + NG * C * 4, A);
@@ -88,7 +88,10 @@ void trace_after(cudaStream_t st);
 
 // ---- launchers (return the launch error; the caller maps it to a status)
 cudaError_t launch_merge_query(const herald_dims& dm, const uint16_t* q_merge, float* qbar,
-                               uint16_t* qhl, uint32_t* hist, cudaStream_t st);
+                               uint16_t* qhl, uint32_t* hist, float2* part1, int part_slots,
+                               cudaStream_t st);
+// Grid of the scan for these shapes (persistent; bounded by kScanMaxCtas).
+int scan_grid(const herald_dims& dm, const struct WsLayout& w, bool tensor_core, int num_sms);
 // kmap: the key cache as [N*Hkv*L_max][d], box 64 x 128 rows, 128B swizzle;
 // bmap: qhl as [N*Hkv*16][d], box 64 x 16 rows.  Without maps (host-resident
 // caches) the CUDA-core scan runs instead.
@@ -97,8 +100,8 @@ cudaError_t launch_scan(const herald_dims& dm, const CUtensorMap* kmap, const CU
                         float* logits, float2* part1, const WsLayout& w, uint32_t* err,
                         int num_sms, cudaStream_t st);
 cudaError_t launch_s1_hist(const herald_dims& dm, const float* logits, const float2* part1,
-                           const int32_t* ctx, float* s1, uint32_t* hist, const WsLayout& w,
-                           int num_sms, cudaStream_t st);
+                           int part_slots, const int32_t* ctx, float* s1, uint32_t* hist,
+                           const WsLayout& w, int num_sms, cudaStream_t st);
 cudaError_t launch_topc(const herald_dims& dm, const float* s1, const uint32_t* hist,
                         const int32_t* ctx, int C, int32_t* cand, int32_t* n_cand,
                         const WsLayout& w, cudaStream_t st);

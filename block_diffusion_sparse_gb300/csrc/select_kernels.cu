@@ -26,7 +26,8 @@ namespace herald {
 __global__ void merge_query_kernel(const uint16_t* __restrict__ q, int B, int Hq, int Hkv, int d,
                                    float scale, float* __restrict__ qbar,
                                    uint16_t* __restrict__ qhl, uint32_t* __restrict__ hist,
-                                   int hist_words) {
+                                   int hist_words, float2* __restrict__ part1, int part_slots,
+                                   int n_rows) {
   const int nh = blockIdx.x, n = nh / Hq, h = nh % Hq, e = threadIdx.x;
   const int G = Hq / Hkv, g = h / G, hl = h - g * G;
   if (e < d) {
@@ -54,28 +55,46 @@ __global__ void merge_query_kernel(const uint16_t* __restrict__ q, int B, int Hq
         rows[size_t(8 + r) * d + e] = 0;
       }
   }
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < hist_words; i += gridDim.x * blockDim.x)
-    hist[i] = 0u;
+  const int tid = blockIdx.x * blockDim.x + threadIdx.x, nthr = gridDim.x * blockDim.x;
+  for (int i = tid; i < hist_words; i += nthr) hist[i] = 0u;
+  // the scan's (max, sumexp) slots start empty: (-inf, 0)
+  for (int i = tid; i < n_rows * part_slots; i += nthr)
+    part1[size_t(i / part_slots) * kPartSlots + (i % part_slots)] = make_float2(-INFINITY, 0.f);
 }
 
 cudaError_t launch_merge_query(const herald_dims& dm, const uint16_t* q_merge, float* qbar,
-                               uint16_t* qhl, uint32_t* hist, cudaStream_t st) {
+                               uint16_t* qhl, uint32_t* hist, float2* part1, int part_slots,
+                               cudaStream_t st) {
   const float scale = 1.0f / sqrtf(float(dm.d));
   trace_before(st, "merge_query_kernel");
   merge_query_kernel<<<dm.N * dm.Hq, dm.d, 0, st>>>(q_merge, dm.B, dm.Hq, dm.Hkv, dm.d, scale,
-                                                    qbar, qhl, hist,
-                                                    dm.N * dm.Hkv * kHistBins);
+                                                    qbar, qhl, hist, dm.N * dm.Hkv * kHistBins,
+                                                    part1, part_slots, dm.N * dm.Hq);
   trace_after(st);
   return cudaGetLastError();
 }
 
-// Writes the (max, sumexp) of one 32-key group of logits (one per lane,
-// `valid` marks keys inside the context).
-__device__ __forceinline__ void write_part(float l, bool valid, float2* dst, int lane) {
-  const float m = warp_max(valid ? l : -INFINITY);
-  const float s = warp_sum(valid ? __expf(l - m) : 0.f);
-  if (lane == 0) *dst = make_float2(m, s);
-}
+// Running (max, sum of exp) of the logits one lane has seen; merged across
+// the warp only when a warp finishes a segment (no shuffles per tile).
+struct OnlineLse {
+  float m = -INFINITY, s = 0.f;
+  __device__ __forceinline__ void add(float l) {
+    if (l > m) {
+      s = s * __expf(m - l) + 1.f;
+      m = l;
+    } else {
+      s += __expf(l - m);
+    }
+  }
+  // Warp-wide merge; lane 0 stores the result, then the state restarts.
+  __device__ __forceinline__ void flush(float2* dst, int lane) {
+    const float M = warp_max(m);
+    const float S = warp_sum(m == -INFINITY ? 0.f : s * __expf(m - M));
+    if (lane == 0) *dst = make_float2(M, S);
+    m = -INFINITY;
+    s = 0.f;
+  }
+};
 
 // ======================================================== scan (tensor)
 // Stage-1 scan of a device-resident cache on the tensor cores.  The merged
@@ -104,7 +123,7 @@ template <int D, int G>
 __global__ void __launch_bounds__(kTcScanThreads, 1)
     scan_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap bmap, const int32_t* __restrict__ ctx,
-                   int Hkv, int L_max, int tiles_per_seg, int total_tiles, int L_pad, int parts,
+                   int Hkv, int L_max, int tiles_per_seg, int total_tiles, int L_pad,
                    float* __restrict__ logits, float2* __restrict__ part1, uint32_t* err) {
   using Cfg = TcScanCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -215,10 +234,23 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
       }
     }
   } else {  // ---- epilogue: warps 0-3, thread = key row of the tile
+    OnlineLse run[G];
+    int run_seg = -1;
+    const int slot = blockIdx.x * 4 + warp;
+    auto flush = [&](int sg) {
+      const int n = sg / Hkv, g = sg - n * Hkv;
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+        run[h].flush(part1 + (size_t(n) * Hq + g * G + h) * kPartSlots + slot, lane);
+    };
     int i = 0;
     for (int t = t_begin; t < t_end; ++t) {
       int seg, j0, L;
       if (!tile(t, seg, j0, L)) continue;
+      if (seg != run_seg) {
+        if (run_seg >= 0) flush(run_seg);
+        run_seg = seg;
+      }
       const int acc = i & 1;
       if (!mbar_wait(&tfull[acc], uint32_t(i >> 1) & 1u)) {
         record_error(err, DEV_TIMEOUT_MMA);
@@ -233,16 +265,17 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
       if (lane == 0) mbar_arrive(&tempty[acc]);
       const int n = seg / Hkv, g = seg - n * Hkv;
       const int j = j0 + warp * 32 + lane;
-      const bool valid = j < L;
+      if (j < L) {
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float l = v[h] + v[8 + h];
-        const size_t row = size_t(n) * Hq + g * G + h;
-        if (valid) logits[row * L_pad + j] = l;
-        write_part(l, valid, part1 + row * parts + (j0 / kPartKeys) + warp, lane);
+        for (int h = 0; h < G; ++h) {
+          const float l = v[h] + v[8 + h];
+          logits[(size_t(n) * Hq + g * G + h) * L_pad + j] = l;
+          run[h].add(l);
+        }
       }
       ++i;
     }
+    if (run_seg >= 0) flush(run_seg);
   }
   tc_fence_before();
   __syncthreads();
@@ -269,7 +302,7 @@ template <int D, int G>
 __global__ void __launch_bounds__(kScanWarps * 32, 1)
     scan_cc_kernel(const uint16_t* __restrict__ kc, const float* __restrict__ qbar,
                    const int32_t* __restrict__ ctx, int Hkv, int L_max, int tiles_per_seg,
-                   int total_tiles, int L_pad, int parts, float* __restrict__ logits,
+                   int total_tiles, int L_pad, float* __restrict__ logits,
                    float2* __restrict__ part1) {
   using Cfg = ScanCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -307,6 +340,15 @@ __global__ void __launch_bounds__(kScanWarps * 32, 1)
 #pragma unroll
   for (int s = 0; s < kScanStages; ++s) issue(s, s);
 
+  OnlineLse run[G];
+  int run_seg = -1;
+  const int slot = blockIdx.x * kScanWarps + warp;
+  auto flush = [&](int sg) {
+    const int n = sg / Hkv, g = sg - n * Hkv;
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+      run[h].flush(part1 + (size_t(n) * Hq + g * G + h) * kPartSlots + slot, lane);
+  };
   for (int i = 0;; ++i) {
     const int t = t_begin + warp + i * kScanWarps;
     if (t >= t_end) break;
@@ -317,6 +359,10 @@ __global__ void __launch_bounds__(kScanWarps * 32, 1)
     const int j0 = tl * kScanTileKeys;
     const int L = min(max(ctx[n], 0), L_max);
     const bool valid = j0 < L;
+    if (valid && seg != run_seg) {
+      if (run_seg >= 0) flush(run_seg);
+      run_seg = seg;
+    }
     float2 acc[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) acc[h] = make_float2(0.f, 0.f);
@@ -365,13 +411,18 @@ __global__ void __launch_bounds__(kScanWarps * 32, 1)
       for (int h = 0; h < G; ++h) {
         const size_t row = (size_t(n) * Hq + g * G + h);
         float* lr = logits + row * L_pad;
-        if (va) lr[ja] = acc[h].x;
-        if (vb) lr[jb] = acc[h].y;
-        write_part(acc[h].x, va, part1 + row * parts + j0 / kPartKeys, lane);
-        write_part(acc[h].y, vb, part1 + row * parts + j0 / kPartKeys + 1, lane);
+        if (va) {
+          lr[ja] = acc[h].x;
+          run[h].add(acc[h].x);
+        }
+        if (vb) {
+          lr[jb] = acc[h].y;
+          run[h].add(acc[h].y);
+        }
       }
     }
   }
+  if (run_seg >= 0) flush(run_seg);
   cp_async_wait_all();
 }
 
@@ -394,19 +445,17 @@ static cudaError_t launch_scan_t(const CUtensorMap* kmap, const CUtensorMap* bma
   const int segs = dm.N * dm.Hkv;
   if (kmap && bmap) {
     const int total = segs * w.tiles128;
-    const int grid = total < num_sms ? total : num_sms;
+    const int grid = scan_grid(dm, w, true, num_sms);
     trace_before(st, "scan_tc_kernel");
     scan_tc_kernel<D, G><<<grid, kTcScanThreads, TcScanCfg<D>::kSmem, st>>>(
-        *kmap, *bmap, ctx, dm.Hkv, dm.L_max, w.tiles128, total, w.L_pad, w.parts, logits, part1,
-        err);
+        *kmap, *bmap, ctx, dm.Hkv, dm.L_max, w.tiles128, total, w.L_pad, logits, part1, err);
     trace_after(st);
   } else {
     const int total = segs * w.tiles_per_seg;
-    const int grid = total < num_sms ? total : num_sms;
+    const int grid = scan_grid(dm, w, false, num_sms);
     trace_before(st, "scan_cc_kernel");
     scan_cc_kernel<D, G><<<grid, kScanWarps * 32, ScanCfg<D>::kSmem, st>>>(
-        kc, qbar, ctx, dm.Hkv, dm.L_max, w.tiles_per_seg, total, w.L_pad, w.parts, logits,
-        part1);
+        kc, qbar, ctx, dm.Hkv, dm.L_max, w.tiles_per_seg, total, w.L_pad, logits, part1);
     trace_after(st);
   }
   return cudaGetLastError();
@@ -427,6 +476,12 @@ static cudaError_t scan_dispatch_g(int G, const CUtensorMap* kmap, const CUtenso
     default: return cudaErrorInvalidValue;
   }
 #undef HERALD_SCAN_G
+}
+
+int scan_grid(const herald_dims& dm, const WsLayout& w, bool tensor_core, int num_sms) {
+  const int total = dm.N * dm.Hkv * (tensor_core ? w.tiles128 : w.tiles_per_seg);
+  int g = num_sms < kScanMaxCtas ? num_sms : kScanMaxCtas;
+  return total < g ? total : g;
 }
 
 cudaError_t launch_scan(const herald_dims& dm, const CUtensorMap* kmap, const CUtensorMap* bmap,
@@ -462,7 +517,7 @@ template <int G>
 __global__ void __launch_bounds__(kS1Threads)
     s1_hist_kernel(const float* __restrict__ logits, const float2* __restrict__ part1,
                    const int32_t* __restrict__ ctx, int Hkv, int L_max, int L_pad,
-                   int parts, int keys_per_cta, float* __restrict__ s1,
+                   int part_slots, int keys_per_cta, float* __restrict__ s1,
                    uint32_t* __restrict__ hist) {
   __shared__ uint32_t sh[kHistBins];
   __shared__ float lse[8];
@@ -475,8 +530,8 @@ __global__ void __launch_bounds__(kS1Threads)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < kHistBins; i += kS1Threads) sh[i] = 0u;
   if (warp < G) {
-    const int ntiles = (L + kPartKeys - 1) / kPartKeys;
-    const float2* p = part1 + (size_t(n) * Hq + g * G + warp) * parts;
+    const int ntiles = part_slots;
+    const float2* p = part1 + (size_t(n) * Hq + g * G + warp) * kPartSlots;
     float m = -INFINITY, s = 0.f;
     for (int t0 = 0; t0 < ntiles; t0 += 32 * 8) {
       float2 v[8];
@@ -525,8 +580,8 @@ __global__ void __launch_bounds__(kS1Threads)
 }
 
 cudaError_t launch_s1_hist(const herald_dims& dm, const float* logits, const float2* part1,
-                           const int32_t* ctx, float* s1, uint32_t* hist, const WsLayout& w,
-                           int num_sms, cudaStream_t st) {
+                           int part_slots, const int32_t* ctx, float* s1, uint32_t* hist,
+                           const WsLayout& w, int num_sms, cudaStream_t st) {
   const int segs = dm.N * dm.Hkv;
   int chunks = (2 * num_sms + segs - 1) / segs;
   int keys = cdiv(dm.L_max, chunks);
@@ -538,7 +593,7 @@ cudaError_t launch_s1_hist(const herald_dims& dm, const float* logits, const flo
 #define HERALD_S1_G(GG)                                                                      \
   case GG:                                                                                   \
     s1_hist_kernel<GG><<<grid, kS1Threads, 0, st>>>(logits, part1, ctx, dm.Hkv, dm.L_max,    \
-                                                    w.L_pad, w.parts, keys, s1, hist);         \
+                                                    w.L_pad, part_slots, keys, s1, hist);      \
     break;
     HERALD_S1_G(1) HERALD_S1_G(2) HERALD_S1_G(3) HERALD_S1_G(4)
     HERALD_S1_G(5) HERALD_S1_G(6) HERALD_S1_G(7) HERALD_S1_G(8)
@@ -547,6 +602,19 @@ cudaError_t launch_s1_hist(const herald_dims& dm, const float* logits, const flo
   }
   trace_after(st);
   return cudaGetLastError();
+}
+
+// Warp-aggregated append: lanes with `take` get consecutive slots from one
+// atomicAdd per warp on *counter.  Every lane of the warp must call it.
+__device__ __forceinline__ uint32_t warp_append_slot(bool take, uint32_t* counter) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t mask = __ballot_sync(0xffffffffu, take);
+  if (!mask) return 0xffffffffu;
+  const int leader = __ffs(mask) - 1;
+  uint32_t base = 0;
+  if (lane == leader) base = atomicAdd(counter, uint32_t(__popc(mask)));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  return take ? base + uint32_t(__popc(mask & ((1u << lane) - 1u))) : 0xffffffffu;
 }
 
 // ============================================================ block scans
@@ -658,7 +726,7 @@ __device__ __forceinline__ void block_excl_scan2(uint32_t a, uint32_t b, uint32_
 // Elements of s1 are processed in rounds of kSelThreads * kPerThr: thread t
 // holds the kPerThr consecutive values [base + t*kPerThr, ...) in registers,
 // loaded as independent 16-byte loads so a round costs one memory latency.
-constexpr int kPerThr = 32;
+constexpr int kPerThr = 16;
 constexpr int kRound = kSelThreads * kPerThr;
 
 __device__ __forceinline__ void load_round(const uint32_t* sv, int L, int base,
@@ -713,10 +781,9 @@ __global__ void __launch_bounds__(kSelThreads)
     const int j0 = base + threadIdx.x * kPerThr;
 #pragma unroll
     for (int k = 0; k < kPerThr; ++k) {
-      if (j0 + k < L && (v[k] >> 19) == b1) {
-        const uint32_t slot = atomicAdd(&s_cnt, 1u);
-        if (slot < kTieCap) tie_v[slot] = v[k] & 0x7FFFFu;
-      }
+      const bool take = j0 + k < L && (v[k] >> 19) == b1;
+      const uint32_t slot = warp_append_slot(take, &s_cnt);
+      if (take && slot < kTieCap) tie_v[slot] = v[k] & 0x7FFFFu;
     }
   }
   __syncthreads();
@@ -802,15 +869,15 @@ cudaError_t launch_topc(const herald_dims& dm, const float* s1, const uint32_t* 
 }
 
 // ============================================================= topk_union
-// One CTA of 512 threads per (n, g); thread t holds the stage-2 scores of the
-// candidate slots [t*E, (t+1)*E) in registers (E <= 32, C <= 16384).  Radix
+// One CTA of 1024 threads per (n, g); thread t holds the stage-2 scores of the
+// candidate slots [t*E, (t+1)*E) in registers (E <= 16, C <= 16384).  Radix
 // select of the K-th largest: a 12-bit first digit over all scores, then the
 // members of that bin (in shared memory) resolve the remaining 19 bits.  Ties
 // go to the lower slot = lower position (candidates are ascending).  Output:
 // [0, sink_end) ++ kept candidates inside [sink_end, local_begin) ++
 // [local_begin, L) -- the deduplicated ascending union.
-constexpr int kTkThreads = 512;
-constexpr int kTkPer = kMaxC / kTkThreads;  // 32
+constexpr int kTkThreads = 1024;
+constexpr int kTkPer = kMaxC / kTkThreads;  // 16
 
 __global__ void __launch_bounds__(kTkThreads)
     topk_union_kernel(const int32_t* __restrict__ ctx, const int32_t* __restrict__ cand,
@@ -849,8 +916,11 @@ __global__ void __launch_bounds__(kTkThreads)
     const uint32_t b1 = uint32_t(s_bin);
     need -= s_above;
 #pragma unroll
-    for (int k = 0; k < kTkPer; ++k)
-      if (k < E && i0 + k < nc && (v[k] >> 19) == b1) mem[atomicAdd(&s_cnt, 1u)] = v[k] & 0x7FFFFu;
+    for (int k = 0; k < kTkPer; ++k) {
+      const bool take = k < E && i0 + k < nc && (v[k] >> 19) == b1;
+      const uint32_t slot = warp_append_slot(take, &s_cnt);
+      if (take) mem[slot] = v[k] & 0x7FFFFu;
+    }
     for (int i = threadIdx.x; i < 2048; i += kTkThreads) h[i] = 0u;
     __syncthreads();
     const uint32_t cnt = s_cnt;

@@ -231,11 +231,24 @@ __global__ void __launch_bounds__(kTcThreads)
   // row log-sum-exp over all candidates from the pass-1 chunk partials
   const int nch = (nc + kRefineChunk - 1) / kRefineChunk;
   for (int r = threadIdx.x; r < R; r += kTcThreads) {
+    // the row's chunk partials, requested in independent batches of 8
     const float2* p = rpart + (size_t(seg) * MT * kTileM + r) * n_chunks;
-    float M = -INFINITY;
-    for (int k = 0; k < nch; ++k) M = fmaxf(M, p[k].x);
-    float S = 0.f;
-    for (int k = 0; k < nch; ++k) S += p[k].y * __expf(p[k].x - M);
+    float M = -INFINITY, S = 0.f;
+    for (int k0 = 0; k0 < nch; k0 += 8) {
+      float2 q[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) q[k] = k0 + k < nch ? p[k0 + k] : make_float2(-INFINITY, 0.f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (q[k].x == -INFINITY) continue;
+        if (q[k].x > M) {
+          S = S * __expf(M - q[k].x) + q[k].y;
+          M = q[k].x;
+        } else {
+          S += q[k].y * __expf(q[k].x - M);
+        }
+      }
+    }
     lse[r] = M + __logf(S);
   }
   cp_async_wait_all();

@@ -86,3 +86,82 @@ class BlockPipeline:
             den.wait_stream(sel)
         H.herald_append_kv(d, block_k[self.T - 1], block_v[self.T - 1], ctx, k_cache, v_cache,
                            advance, den)
+
+
+class StackPipeline:
+    """The same pipeline over a stack of layers sharing one context length.
+
+    A denoising step is a forward pass over all layers, so per block:
+    step 0 runs, layer by layer, stage 2 + gather + attention; right after a
+    layer's step-0 work is issued, stage 1 of the next block for that layer
+    starts on the selection stream (the layer's current queries exist from
+    then on).  Steps 1..T-1 run attention over all layers; after the
+    selection stream joins, every layer appends its block and the shared
+    context length advances once.
+    """
+
+    def __init__(self, dims: H.Dims, n_layers: int, C: int, K: int, S: int, W: int, P: int,
+                 T: int, sel_stream=None):
+        import torch
+        self.torch = torch
+        self.d, self.nl = dims, n_layers
+        self.C, self.K, self.S, self.W, self.P, self.T = C, K, S, W, P, T
+        NG = (dims.N, dims.Hkv)
+        dev = "cuda"
+        self.ws_bytes = H.herald_workspace_size(dims, C, P)
+        self.ws_den = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.ws_sel = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)
+        mk = lambda shape, dt, fill=0: torch.full(shape, fill, dtype=dt, device=dev)
+        self.cand = [[mk((*NG, C), torch.int32, -1) for _ in range(2)] for _ in range(n_layers)]
+        self.n_cand = [[mk(NG, torch.int32) for _ in range(2)] for _ in range(n_layers)]
+        self.idx = [mk((*NG, P), torch.int32, -1) for _ in range(n_layers)]
+        self.n_sel = [mk(NG, torch.int32) for _ in range(n_layers)]
+        self.pool_k = [[mk((*NG, P, dims.d), torch.int16) for _ in range(2)]
+                       for _ in range(n_layers)]
+        self.pool_v = [[mk((*NG, P, dims.d), torch.int16) for _ in range(2)]
+                       for _ in range(n_layers)]
+        self.sel = sel_stream if sel_stream is not None else torch.cuda.Stream()
+
+    def prime(self, q_merge, k_caches, ctx, slot: int = 0):
+        st = self.torch.cuda.current_stream()
+        for l in range(self.nl):
+            H.herald_select_stage1(self.d, q_merge[l], k_caches[l], ctx, self.C,
+                                   self.cand[l][slot], self.n_cand[l][slot], self.ws_sel,
+                                   self.ws_bytes, st)
+
+    def block(self, i: int, q_steps, block_k, block_v, k_caches, v_caches, ctx, out,
+              advance: bool = True, overlap: bool = True):
+        """q_steps[l], block_k[l], block_v[l]: layer l's [T, N, B, ...] inputs;
+        out[l][t] receives layer l's step-t output."""
+        torch = self.torch
+        den, sel = torch.cuda.current_stream(), self.sel
+        cur, nxt = i % 2, (i + 1) % 2
+        d, P = self.d, self.P
+        for t in range(self.T):
+            for l in range(self.nl):
+                if t == 0:
+                    H.herald_select_stage2(d, q_steps[l][0], k_caches[l], ctx,
+                                           self.cand[l][cur], self.n_cand[l][cur], self.C,
+                                           self.K, self.S, self.W, P, self.idx[l],
+                                           self.n_sel[l], self.ws_den, self.ws_bytes, den)
+                    H.herald_gather(d, self.idx[l], self.n_sel[l], P, k_caches[l], v_caches[l],
+                                    self.pool_k[l][cur], self.pool_v[l][cur], den)
+                H.herald_denoise_attn(d, q_steps[l][t], self.pool_k[l][cur], self.pool_v[l][cur],
+                                      self.n_sel[l], P, block_k[l][t], block_v[l][t], out[l][t],
+                                      0.0, self.ws_den, self.ws_bytes, den)
+                if t == 0:
+                    if overlap:
+                        sel.wait_stream(den)
+                        with torch.cuda.stream(sel):
+                            H.herald_select_stage1(d, q_steps[l][0], k_caches[l], ctx, self.C,
+                                                   self.cand[l][nxt], self.n_cand[l][nxt],
+                                                   self.ws_sel, self.ws_bytes, sel)
+                    else:
+                        H.herald_select_stage1(d, q_steps[l][0], k_caches[l], ctx, self.C,
+                                               self.cand[l][nxt], self.n_cand[l][nxt],
+                                               self.ws_sel, self.ws_bytes, den)
+        if overlap:
+            den.wait_stream(sel)
+        for l in range(self.nl):
+            H.herald_append_kv(d, block_k[l][self.T - 1], block_v[l][self.T - 1], ctx,
+                               k_caches[l], v_caches[l], advance and l == self.nl - 1, den)
