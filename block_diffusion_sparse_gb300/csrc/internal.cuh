@@ -86,6 +86,33 @@ inline WsLayout ws_layout(const herald_dims& dm, int C, int P_max) {
 void trace_before(cudaStream_t st, const char* name);
 void trace_after(cudaStream_t st);
 
+// Launches a kernel with programmatic stream serialisation (see
+// griddep_wait in ptx.cuh), bracketed by the tracing hooks.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(const char* name, void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                     size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  trace_before(st, name);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+  trace_after(st);
+  return e;
+}
+
+#define HERALD_CHECK_LAUNCH(x)             \
+  do {                                     \
+    const cudaError_t le_ = (x);           \
+    if (le_ != cudaSuccess) return le_;    \
+  } while (0)
+
 // ---- launchers (return the launch error; the caller maps it to a status)
 cudaError_t launch_merge_query(const herald_dims& dm, const uint16_t* q_merge, float* qbar,
                                uint16_t* qhl, uint32_t* hist, float2* part1, int part_slots,

@@ -26,6 +26,7 @@ __global__ void __launch_bounds__(256)
                   int L_max, const uint16_t* __restrict__ kc, const uint16_t* __restrict__ vc,
                   uint16_t* __restrict__ pk, uint16_t* __restrict__ pv) {
   constexpr int TPR = D / 8, RPC = 256 / TPR;
+  griddep_enter();
   const int seg = blockIdx.y;
   const int row = blockIdx.x * RPC + threadIdx.x / TPR, c = threadIdx.x % TPR;
   if (row >= P_max) return;
@@ -48,16 +49,14 @@ cudaError_t launch_gather(const herald_dims& dm, const int32_t* idx, const int32
                           int P_max, const uint16_t* k_cache, const uint16_t* v_cache,
                           uint16_t* pool_k, uint16_t* pool_v, cudaStream_t st) {
   const int segs = dm.N * dm.Hkv;
-  trace_before(st, "gather_kernel");
   if (dm.d == 128)
-    gather_kernel<128><<<dim3(cdiv(P_max, 16), segs), 256, 0, st>>>(idx, n_sel, P_max, dm.L_max,
+    HERALD_CHECK_LAUNCH(launch_k("gather_kernel", gather_kernel<128>, dim3(cdiv(P_max, 16), segs), 256, 0, st, idx, n_sel, P_max, dm.L_max,
                                                                      k_cache, v_cache, pool_k,
-                                                                     pool_v);
+                                                                     pool_v));
   else
-    gather_kernel<64><<<dim3(cdiv(P_max, 32), segs), 256, 0, st>>>(idx, n_sel, P_max, dm.L_max,
+    HERALD_CHECK_LAUNCH(launch_k("gather_kernel", gather_kernel<64>, dim3(cdiv(P_max, 32), segs), 256, 0, st, idx, n_sel, P_max, dm.L_max,
                                                                     k_cache, v_cache, pool_k,
-                                                                    pool_v);
-  trace_after(st);
+                                                                    pool_v));
   return cudaGetLastError();
 }
 
@@ -71,6 +70,7 @@ __global__ void __launch_bounds__(256)
                   int Hkv, int d, int L_max, int32_t* __restrict__ ctx,
                   uint16_t* __restrict__ kc, uint16_t* __restrict__ vc, int advance) {
   __shared__ int L0;
+  griddep_enter();
   const int n = blockIdx.x;
   if (threadIdx.x == 0) L0 = min(max(ctx[n], 0), L_max);
   __syncthreads();
@@ -108,10 +108,8 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_append(const herald_dims& dm, const uint16_t* block_k, const uint16_t* block_v,
                           int32_t* ctx, uint16_t* k_cache, uint16_t* v_cache, int advance,
                           cudaStream_t st) {
-  trace_before(st, "append_kernel");
-  append_kernel<<<dm.N, 256, 0, st>>>(block_k, block_v, dm.B, dm.Hkv, dm.d, dm.L_max, ctx,
-                                      k_cache, v_cache, advance);
-  trace_after(st);
+  HERALD_CHECK_LAUNCH(launch_k("append_kernel", append_kernel, dm.N, 256, 0, st, block_k, block_v, dm.B, dm.Hkv, dm.d, dm.L_max, ctx,
+                                      k_cache, v_cache, advance));
   return cudaGetLastError();
 }
 

@@ -72,6 +72,21 @@ HERALD_DEV bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start while its predecessor on the stream is running;
+// griddep_wait() blocks until the predecessor has completed and its memory
+// is visible (a no-op for ordinary launches), so every kernel calls it before
+// its first global memory access.  griddep_launch_dependents() lets the next
+// kernel start its own prologue early.
+HERALD_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+HERALD_DEV void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+HERALD_DEV void griddep_enter() {
+  griddep_wait();
+  griddep_launch_dependents();
+}
+
 HERALD_DEV void record_error(uint32_t* err_word, uint32_t code) {
   if (err_word) atomicCAS(err_word, 0u, code);
 }

@@ -28,6 +28,7 @@ __global__ void merge_query_kernel(const uint16_t* __restrict__ q, int B, int Hq
                                    uint16_t* __restrict__ qhl, uint32_t* __restrict__ hist,
                                    int hist_words, float2* __restrict__ part1, int part_slots,
                                    int n_rows) {
+  griddep_enter();
   const int nh = blockIdx.x, n = nh / Hq, h = nh % Hq, e = threadIdx.x;
   const int G = Hq / Hkv, g = h / G, hl = h - g * G;
   if (e < d) {
@@ -66,11 +67,9 @@ cudaError_t launch_merge_query(const herald_dims& dm, const uint16_t* q_merge, f
                                uint16_t* qhl, uint32_t* hist, float2* part1, int part_slots,
                                cudaStream_t st) {
   const float scale = 1.0f / sqrtf(float(dm.d));
-  trace_before(st, "merge_query_kernel");
-  merge_query_kernel<<<dm.N * dm.Hq, dm.d, 0, st>>>(q_merge, dm.B, dm.Hq, dm.Hkv, dm.d, scale,
+  HERALD_CHECK_LAUNCH(launch_k("merge_query_kernel", merge_query_kernel, dm.N * dm.Hq, dm.d, 0, st, q_merge, dm.B, dm.Hq, dm.Hkv, dm.d, scale,
                                                     qbar, qhl, hist, dm.N * dm.Hkv * kHistBins,
-                                                    part1, part_slots, dm.N * dm.Hq);
-  trace_after(st);
+                                                    part1, part_slots, dm.N * dm.Hq));
   return cudaGetLastError();
 }
 
@@ -158,6 +157,7 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tmem_base;
+  griddep_enter();
 
   // tile t covers keys [j0, j0 + 128) of segment seg = n*Hkv + g
   auto tile = [&](int t, int& seg, int& j0, int& L) -> bool {
@@ -313,6 +313,7 @@ __global__ void __launch_bounds__(kScanWarps * 32, 1)
   uint8_t* ring = smem + warp * kScanStages * Cfg::kTileBytes;
   const int t_begin = int((long long)blockIdx.x * total_tiles / gridDim.x);
   const int t_end = int((long long)(blockIdx.x + 1) * total_tiles / gridDim.x);
+  griddep_enter();
 
   // Issues the copies of this warp's i-th tile into `stage` (one commit
   // group per tile, empty for tiles past the context).
@@ -446,17 +447,13 @@ static cudaError_t launch_scan_t(const CUtensorMap* kmap, const CUtensorMap* bma
   if (kmap && bmap) {
     const int total = segs * w.tiles128;
     const int grid = scan_grid(dm, w, true, num_sms);
-    trace_before(st, "scan_tc_kernel");
-    scan_tc_kernel<D, G><<<grid, kTcScanThreads, TcScanCfg<D>::kSmem, st>>>(
-        *kmap, *bmap, ctx, dm.Hkv, dm.L_max, w.tiles128, total, w.L_pad, logits, part1, err);
-    trace_after(st);
+    HERALD_CHECK_LAUNCH(launch_k("scan_tc_kernel", scan_tc_kernel<D, G>, grid, kTcScanThreads, TcScanCfg<D>::kSmem, st, 
+        *kmap, *bmap, ctx, dm.Hkv, dm.L_max, w.tiles128, total, w.L_pad, logits, part1, err));
   } else {
     const int total = segs * w.tiles_per_seg;
     const int grid = scan_grid(dm, w, false, num_sms);
-    trace_before(st, "scan_cc_kernel");
-    scan_cc_kernel<D, G><<<grid, kScanWarps * 32, ScanCfg<D>::kSmem, st>>>(
-        kc, qbar, ctx, dm.Hkv, dm.L_max, w.tiles_per_seg, total, w.L_pad, logits, part1);
-    trace_after(st);
+    HERALD_CHECK_LAUNCH(launch_k("scan_cc_kernel", scan_cc_kernel<D, G>, grid, kScanWarps * 32, ScanCfg<D>::kSmem, st, 
+        kc, qbar, ctx, dm.Hkv, dm.L_max, w.tiles_per_seg, total, w.L_pad, logits, part1));
   }
   return cudaGetLastError();
 }
@@ -521,6 +518,7 @@ __global__ void __launch_bounds__(kS1Threads)
                    uint32_t* __restrict__ hist) {
   __shared__ uint32_t sh[kHistBins];
   __shared__ float lse[8];
+  griddep_enter();
   const int seg = blockIdx.y, n = seg / Hkv, g = seg - n * Hkv;
   const int Hq = Hkv * G;
   const int L = min(max(ctx[n], 0), L_max);
@@ -588,19 +586,17 @@ cudaError_t launch_s1_hist(const herald_dims& dm, const float* logits, const flo
   keys = cdiv(keys, kS1Threads * kS1Keys) * kS1Threads * kS1Keys;
   chunks = cdiv(dm.L_max, keys);
   const dim3 grid(chunks, segs);
-  trace_before(st, "s1_hist_kernel");
   switch (dm.Hq / dm.Hkv) {
 #define HERALD_S1_G(GG)                                                                      \
   case GG:                                                                                   \
-    s1_hist_kernel<GG><<<grid, kS1Threads, 0, st>>>(logits, part1, ctx, dm.Hkv, dm.L_max,    \
-                                                    w.L_pad, part_slots, keys, s1, hist);      \
+    HERALD_CHECK_LAUNCH(launch_k("s1_hist_kernel", s1_hist_kernel<GG>, grid, kS1Threads, 0, st, logits, part1, ctx, dm.Hkv, dm.L_max,    \
+                                                    w.L_pad, part_slots, keys, s1, hist));      \
     break;
     HERALD_S1_G(1) HERALD_S1_G(2) HERALD_S1_G(3) HERALD_S1_G(4)
     HERALD_S1_G(5) HERALD_S1_G(6) HERALD_S1_G(7) HERALD_S1_G(8)
 #undef HERALD_S1_G
     default: break;
   }
-  trace_after(st);
   return cudaGetLastError();
 }
 
@@ -754,6 +750,7 @@ __global__ void __launch_bounds__(kSelThreads)
   __shared__ uint32_t wt[32], wt2[32];
   __shared__ int s_bin;
   __shared__ uint32_t s_above, s_cnt;
+  griddep_enter();
   const int seg = blockIdx.x, n = seg / Hkv;
   const int L = min(max(ctx[n], 0), L_max);
   const int Ce = min(C, L);
@@ -861,10 +858,8 @@ __global__ void __launch_bounds__(kSelThreads)
 cudaError_t launch_topc(const herald_dims& dm, const float* s1, const uint32_t* hist,
                         const int32_t* ctx, int C, int32_t* cand, int32_t* n_cand,
                         const WsLayout& w, cudaStream_t st) {
-  trace_before(st, "topc_finish_kernel");
-  topc_finish_kernel<<<dm.N * dm.Hkv, kSelThreads, 0, st>>>(s1, hist, ctx, dm.Hkv, dm.L_max,
-                                                            w.L_pad, C, cand, n_cand);
-  trace_after(st);
+  HERALD_CHECK_LAUNCH(launch_k("topc_finish_kernel", topc_finish_kernel, dm.N * dm.Hkv, kSelThreads, 0, st, s1, hist, ctx, dm.Hkv, dm.L_max,
+                                                            w.L_pad, C, cand, n_cand));
   return cudaGetLastError();
 }
 
@@ -889,6 +884,7 @@ __global__ void __launch_bounds__(kTkThreads)
   __shared__ uint32_t wt[32], wt2[32];
   __shared__ int s_bin;
   __shared__ uint32_t s_above, s_cnt;
+  griddep_enter();
   const int seg = blockIdx.x, n = seg / Hkv;
   const int L = min(max(ctx[n], 0), L_max);
   const int nc = min(max(n_cand[seg], 0), C);
@@ -991,11 +987,9 @@ cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const i
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  trace_before(st, "topk_union_kernel");
-  topk_union_kernel<<<dm.N * dm.Hkv, kTkThreads, smem, st>>>(ctx, cand, n_cand, s2, dm.Hkv,
+  HERALD_CHECK_LAUNCH(launch_k("topk_union_kernel", topk_union_kernel, dm.N * dm.Hkv, kTkThreads, smem, st, ctx, cand, n_cand, s2, dm.Hkv,
                                                               dm.L_max, C, K, S, W, P_max, idx,
-                                                              n_sel);
-  trace_after(st);
+                                                              n_sel));
   return cudaGetLastError();
 }
 

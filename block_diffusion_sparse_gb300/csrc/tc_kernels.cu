@@ -87,6 +87,7 @@ __global__ void __launch_bounds__(kTcThreads)
   __shared__ int32_t pos[kRefineChunk];
   uint8_t* Qs = align1024(smem_raw);
   uint8_t* Ks = Qs + Cfg::kQBytes;
+  griddep_enter();
   const int chunk = blockIdx.x, mt = blockIdx.y, seg = blockIdx.z;
   const int n = seg / Hkv, g = seg - n * Hkv, G = Hq / Hkv;
   const int nc = min(max(n_cand[seg], 0), C);
@@ -200,6 +201,7 @@ __global__ void __launch_bounds__(kTcThreads)
   __shared__ int32_t pos[kRefineRows2];
   uint8_t* Ks = align1024(smem_raw);
   uint8_t* Qs = Ks + Cfg::kKBytes;
+  griddep_enter();
   const int seg = blockIdx.y, n = seg / Hkv, g = seg - n * Hkv, G = Hq / Hkv;
   const int nc = min(max(n_cand[seg], 0), C);
   const int c0 = blockIdx.x * kRefineRows2;
@@ -308,18 +310,14 @@ cudaError_t launch_refine(const herald_dims& dm, const uint16_t* q_block, const 
       if (e != cudaSuccess) return e;
       attr = true;
     }
-    trace_before(st, "refine_pass1_kernel");
-    refine_pass1_kernel<128><<<dim3(w.n_chunks, w.MT, segs), kTcThreads, Ref1Cfg<128>::kSmem,
-                               st>>>(q_block, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv,
-                                     dm.L_max, C, w.R, w.MT, w.n_chunks, scale, rpart, err);
-    trace_after(st);
+    HERALD_CHECK_LAUNCH(launch_k("refine_pass1_kernel", refine_pass1_kernel<128>, dim3(w.n_chunks, w.MT, segs), kTcThreads, Ref1Cfg<128>::kSmem,
+                               st, q_block, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv,
+                                     dm.L_max, C, w.R, w.MT, w.n_chunks, scale, rpart, err));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    trace_before(st, "refine_pass2_kernel");
-    refine_pass2_kernel<128><<<dim3(cdiv(C, kRefineRows2), segs), kTcThreads,
-                               Ref2Cfg<128>::kSmem, st>>>(q_block, k_cache, cand, n_cand, dm.B,
+    HERALD_CHECK_LAUNCH(launch_k("refine_pass2_kernel", refine_pass2_kernel<128>, dim3(cdiv(C, kRefineRows2), segs), kTcThreads,
+                               Ref2Cfg<128>::kSmem, st, q_block, k_cache, cand, n_cand, dm.B,
                                                           dm.Hq, dm.Hkv, dm.L_max, C, w.R, w.MT,
-                                                          w.n_chunks, scale, rpart, s2, err);
-    trace_after(st);
+                                                          w.n_chunks, scale, rpart, s2, err));
   } else {
     static bool attr = false;
     if (!attr) {
@@ -331,17 +329,13 @@ cudaError_t launch_refine(const herald_dims& dm, const uint16_t* q_block, const 
       if (e != cudaSuccess) return e;
       attr = true;
     }
-    trace_before(st, "refine_pass1_kernel");
-    refine_pass1_kernel<64><<<dim3(w.n_chunks, w.MT, segs), kTcThreads, Ref1Cfg<64>::kSmem,
-                              st>>>(q_block, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv,
-                                    dm.L_max, C, w.R, w.MT, w.n_chunks, scale, rpart, err);
-    trace_after(st);
+    HERALD_CHECK_LAUNCH(launch_k("refine_pass1_kernel", refine_pass1_kernel<64>, dim3(w.n_chunks, w.MT, segs), kTcThreads, Ref1Cfg<64>::kSmem,
+                              st, q_block, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv,
+                                    dm.L_max, C, w.R, w.MT, w.n_chunks, scale, rpart, err));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    trace_before(st, "refine_pass2_kernel");
-    refine_pass2_kernel<64><<<dim3(cdiv(C, kRefineRows2), segs), kTcThreads, Ref2Cfg<64>::kSmem,
-                              st>>>(q_block, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv,
-                                    dm.L_max, C, w.R, w.MT, w.n_chunks, scale, rpart, s2, err);
-    trace_after(st);
+    HERALD_CHECK_LAUNCH(launch_k("refine_pass2_kernel", refine_pass2_kernel<64>, dim3(cdiv(C, kRefineRows2), segs), kTcThreads, Ref2Cfg<64>::kSmem,
+                              st, q_block, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv,
+                                    dm.L_max, C, w.R, w.MT, w.n_chunks, scale, rpart, s2, err));
   }
   return cudaGetLastError();
 }
@@ -376,6 +370,7 @@ __global__ void __launch_bounds__(kTcThreads)
   uint8_t* Ks = Qs + Cfg::kQBytes;
   uint8_t* Vs = Ks + Cfg::kKBytes;
   uint8_t* Ps = Vs + Cfg::kVBytes;
+  griddep_enter();
   const int split = blockIdx.x, mt = blockIdx.y, seg = blockIdx.z;
   const int n = seg / Hkv, g = seg - n * Hkv, G = Hq / Hkv;
   const int ns = min(max(n_sel[seg], 0), P_max);
@@ -512,15 +507,17 @@ __global__ void __launch_bounds__(kTcThreads)
 }
 
 // ========================================================== attn_cluster
-// Split-KV attention whose splits are the kClusterCtas CTAs of one thread
-// block cluster per (sequence, KV head, 128-row tile).  CTA rank r owns key
-// tiles r and r + kClusterCtas (each 128 keys: pool rows, then the B block
-// rows).  Both tiles' scores share one row max, so the two P.V products
-// accumulate into one TMEM accumulator without rescaling.  The partial
-// (O, max, sum) of every CTA stays in its shared memory; after a cluster
-// barrier each CTA merges 128/kClusterCtas rows by reading its peers'
-// shared memory (distributed shared memory), and writes bf16 out.
-constexpr int kClusterCtas = 8;
+// Split-KV attention whose splits are the CS CTAs of one thread block
+// cluster per (sequence, KV head, 128-row tile).  CTA rank r owns key tiles
+// r and r + CS (each 128 keys: pool rows, then the B block rows); with
+// CS = 16 (where the device can place 16-CTA clusters) every CTA has one
+// tile, with CS = 8 some have two.  Both tiles' scores share one row max, so
+// the two P.V products accumulate into one TMEM accumulator without
+// rescaling.  The partial (O, max, sum) of every CTA stays in its shared
+// memory; after a cluster barrier each CTA merges 128/CS rows by reading its
+// peers' shared memory (distributed shared memory), and writes bf16 out.
+constexpr int kClusterCtas = 8;     // portable cluster size
+constexpr int kClusterCtasMax = 16; // non-portable size, used when it can be placed
 
 template <int D>
 struct AttnClCfg {
@@ -549,14 +546,27 @@ __device__ __forceinline__ void cluster_sync_all() {
   __cluster_barrier_arrive();
   __cluster_barrier_wait();
 }
-// Generic address of the same shared-memory object in CTA `rank` of the cluster.
-template <typename T>
-__device__ __forceinline__ const T* peer_ptr(const T* p, uint32_t rank) {
-  return static_cast<const T*>(__cluster_map_shared_rank(static_cast<const void*>(p), rank));
+// shared::cluster address of the same shared-memory location in CTA `rank`.
+__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float2 ld_peer_f2(uint32_t a) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float4 ld_peer_f4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a));
+  return v;
 }
 
-template <int D>
-__global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kTcThreads, 1)
+template <int D, int CS>
+__global__ void __launch_bounds__(kTcThreads, 1)
     attn_cluster_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ pool_k,
                         const uint16_t* __restrict__ pool_v, const int32_t* __restrict__ n_sel,
                         int P_max, const uint16_t* __restrict__ block_k,
@@ -577,19 +587,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kTcThread
   const uint32_t rank = cluster_ctarank();
   const int mt = blockIdx.y, seg = blockIdx.z;
   const int n = seg / Hkv, g = seg - n * Hkv, G = Hq / Hkv;
-  const int ns = min(max(n_sel[seg], 0), P_max);
-  const int n_pool = (ns + kAttnKeys - 1) / kAttnKeys;
-  const int n_tiles = n_pool + (B + kAttnKeys - 1) / kAttnKeys;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // this CTA's tiles: t0 = rank, t1 = rank + kClusterCtas (scalars, not
-  // arrays, so that they stay in registers)
-  const int t0 = int(rank), t1 = int(rank) + kClusterCtas;
-  const int nt = (t0 < n_tiles) + (t1 < n_tiles);
-  auto tile_keys = [&](int t) {
-    return t < n_pool ? min(kAttnKeys, ns - t * kAttnKeys)
-                      : min(kAttnKeys, B - (t - n_pool) * kAttnKeys);
-  };
-  const int nk0 = nt > 0 ? tile_keys(t0) : 0, nk1 = nt > 1 ? tile_keys(t1) : 0;
   if (threadIdx.x == 0) {
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
@@ -597,6 +595,19 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kTcThread
   }
   tmem_setup(&tmem_base, 512);
   const uint32_t tbase = tmem_base;
+  griddep_enter();
+  const int ns = min(max(n_sel[seg], 0), P_max);
+  const int n_pool = (ns + kAttnKeys - 1) / kAttnKeys;
+  const int n_tiles = n_pool + (B + kAttnKeys - 1) / kAttnKeys;
+  // this CTA's tiles: t0 = rank, t1 = rank + CS (scalars, not arrays, so
+  // that they stay in registers)
+  const int t0 = int(rank), t1 = int(rank) + CS;
+  const int nt = (t0 < n_tiles) + (t1 < n_tiles);
+  auto tile_keys = [&](int t) {
+    return t < n_pool ? min(kAttnKeys, ns - t * kAttnKeys)
+                      : min(kAttnKeys, B - (t - n_pool) * kAttnKeys);
+  };
+  const int nk0 = nt > 0 ? tile_keys(t0) : 0, nk1 = nt > 1 ? tile_keys(t1) : 0;
   const int quad = warp & 3, ch = warp >> 2;
   const int row = quad * 32 + lane;
   const uint32_t trow = tbase + (uint32_t(quad * 32) << 16);
@@ -736,32 +747,32 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kTcThread
   cluster_sync_all();
   // merge: this CTA finalises rows [rank*RPC, (rank+1)*RPC); every peer
   // value of a row is requested before any is used (one remote round trip)
-  constexpr int RPC = kTileM / kClusterCtas;   // 16 rows, 2 per warp
+  constexpr int RPC = kTileM / CS;             // rows per CTA
   constexpr int E = D / 32;                    // features per lane
   for (int rr = warp; rr < RPC; rr += kTcThreads / 32) {
     const int lr = int(rank) * RPC + rr;
     const int grow = mt * kTileM + lr;
-    float2 pm[kClusterCtas];
-    float o[kClusterCtas][E];
+    float2 pm[CS];
+    float o[CS][E];
 #pragma unroll
-    for (int c = 0; c < kClusterCtas; ++c) {
-      pm[c] = *peer_ptr(&ml[lr], uint32_t(c));
-      const float* src = peer_ptr(Os + lr * Cfg::kORow + lane * E, uint32_t(c));
+    for (int c = 0; c < CS; ++c) {
+      pm[c] = ld_peer_f2(peer_addr(&ml[lr], uint32_t(c)));
+      const uint32_t a = peer_addr(Os + lr * Cfg::kORow + lane * E, uint32_t(c));
       if constexpr (E == 4) {
-        const float4 f = *reinterpret_cast<const float4*>(src);
+        const float4 f = ld_peer_f4(a);
         o[c][0] = f.x; o[c][1] = f.y; o[c][2] = f.z; o[c][3] = f.w;
       } else {
-        const float2 f = *reinterpret_cast<const float2*>(src);
+        const float2 f = ld_peer_f2(a);
         o[c][0] = f.x; o[c][1] = f.y;
       }
     }
     float M = -INFINITY;
 #pragma unroll
-    for (int c = 0; c < kClusterCtas; ++c) M = fmaxf(M, pm[c].x);
+    for (int c = 0; c < CS; ++c) M = fmaxf(M, pm[c].x);
     float acc[E] = {};
     float L = 0.f;
 #pragma unroll
-    for (int c = 0; c < kClusterCtas; ++c) {
+    for (int c = 0; c < CS; ++c) {
       const float wgt = pm[c].x == -INFINITY ? 0.f : __expf(pm[c].x - M);
       L += wgt * pm[c].y;
 #pragma unroll
@@ -788,6 +799,7 @@ __global__ void __launch_bounds__(256)
                         const int32_t* __restrict__ n_sel, int P_max, int N, int B, int Hq,
                         int Hkv, int MT, int S_max, uint16_t* __restrict__ out) {
   constexpr int E = D / 32;
+  griddep_enter();
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (gw >= N * B * Hq) return;
   const int n = gw / (B * Hq), b = (gw / Hq) % B, h = gw % Hq;
@@ -817,8 +829,8 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// The cluster kernel covers up to 2 * kClusterCtas key tiles (P_max + B up
-// to 2048 keys); larger pools use the split kernel plus a combine pass.
+// The cluster kernel covers up to 2 * 8 key tiles (P_max + B up to 2048
+// keys); larger pools use the split kernel plus a combine pass.
 // HERALD_ATTN_SPLIT=1 in the environment forces the split path (testing).
 static bool force_split() {
   static int v = -1;
@@ -827,6 +839,68 @@ static bool force_split() {
     v = (e && e[0] == '1') ? 1 : 0;
   }
   return v == 1;
+}
+
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_cluster(const char* name, void (*kernel)(KArgs...), dim3 grid,
+                                  int cluster_x, size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster_x;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  trace_before(st, name);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+  trace_after(st);
+  return e;
+}
+
+// Whether 16-CTA clusters of the attention kernel can be resident on this
+// device (non-portable size; needs 16 SMs of one GPC).  Cached per device.
+template <int D>
+static bool cluster16_ok() {
+  static int cache[64];
+  static bool init = false;
+  if (!init) {
+    for (int& c : cache) c = -1;
+    init = true;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  if (cache[dev] < 0) {
+    int ok = 0;
+    if (cudaFuncSetAttribute(attn_cluster_kernel<D, kClusterCtasMax>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+      cudaLaunchConfig_t cfg{};
+      cfg.gridDim = dim3(kClusterCtasMax, 1, 1);
+      cfg.blockDim = dim3(kTcThreads);
+      cfg.dynamicSmemBytes = AttnClCfg<D>::kSmem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = kClusterCtasMax;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, attn_cluster_kernel<D, kClusterCtasMax>, &cfg) ==
+              cudaSuccess &&
+          n >= 1)
+        ok = 1;
+    }
+    cudaGetLastError();
+    cache[dev] = ok;
+  }
+  return cache[dev] == 1;
 }
 
 template <int D>
@@ -842,31 +916,34 @@ static cudaError_t launch_attn_t(const herald_dims& dm, const uint16_t* q, const
     e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              AttnCfg<D>::kSmem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_cluster_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             AttnClCfg<D>::kSmem);
+    e = cudaFuncSetAttribute(attn_cluster_kernel<D, kClusterCtas>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, AttnClCfg<D>::kSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(attn_cluster_kernel<D, kClusterCtasMax>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, AttnClCfg<D>::kSmem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   if (w.splits <= 2 * kClusterCtas && !force_split()) {
-    trace_before(st, "attn_cluster_kernel");
-    attn_cluster_kernel<D><<<dim3(kClusterCtas, w.MT, segs), kTcThreads, AttnClCfg<D>::kSmem,
-                             st>>>(q, pool_k, pool_v, n_sel, P_max, block_k, block_v, dm.B, dm.Hq,
-                                   dm.Hkv, w.R, scale, out, err);
-    trace_after(st);
-    return cudaGetLastError();
+    if (w.splits > kClusterCtas && cluster16_ok<D>())
+      return launch_cluster("attn_cluster_kernel", attn_cluster_kernel<D, kClusterCtasMax>,
+                            dim3(kClusterCtasMax, w.MT, segs), kClusterCtasMax,
+                            AttnClCfg<D>::kSmem, st, q, pool_k, pool_v, n_sel, P_max, block_k,
+                            block_v, dm.B, dm.Hq, dm.Hkv, w.R, scale, out, err);
+    return launch_cluster("attn_cluster_kernel", attn_cluster_kernel<D, kClusterCtas>,
+                          dim3(kClusterCtas, w.MT, segs), kClusterCtas, AttnClCfg<D>::kSmem, st,
+                          q, pool_k, pool_v, n_sel, P_max, block_k, block_v, dm.B, dm.Hq, dm.Hkv,
+                          w.R, scale, out, err);
   }
-  trace_before(st, "attn_kernel");
-  attn_kernel<D><<<dim3(w.splits, w.MT, segs), kTcThreads, AttnCfg<D>::kSmem, st>>>(
-      q, pool_k, pool_v, n_sel, P_max, block_k, block_v, dm.B, dm.Hq, dm.Hkv, w.R, w.MT,
-      w.splits, scale, opart, ml, err);
-  trace_after(st);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  HERALD_CHECK_LAUNCH(launch_k("attn_kernel", attn_kernel<D>, dim3(w.splits, w.MT, segs),
+                               kTcThreads, AttnCfg<D>::kSmem, st, q, pool_k, pool_v, n_sel, P_max,
+                               block_k, block_v, dm.B, dm.Hq, dm.Hkv, w.R, w.MT, w.splits, scale,
+                               opart, ml, err));
   const int rows = dm.N * dm.B * dm.Hq;
-  trace_before(st, "attn_combine_kernel");
-  attn_combine_kernel<D><<<cdiv(rows, 8), 256, 0, st>>>(opart, ml, n_sel, P_max, dm.N, dm.B,
-                                                        dm.Hq, dm.Hkv, w.MT, w.splits, out);
-  trace_after(st);
-  return cudaGetLastError();
+  HERALD_CHECK_LAUNCH(launch_k("attn_combine_kernel", attn_combine_kernel<D>, cdiv(rows, 8), 256,
+                               0, st, opart, ml, n_sel, P_max, dm.N, dm.B, dm.Hq, dm.Hkv, w.MT,
+                               w.splits, out));
+  return cudaSuccess;
 }
 
 cudaError_t launch_attn(const herald_dims& dm, const uint16_t* q, const uint16_t* pool_k,
