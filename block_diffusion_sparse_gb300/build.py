@@ -16,7 +16,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libherald.so")
-SOURCES = ["herald_api.cu", "select_kernels.cu", "tc_kernels.cu", "move_kernels.cu"]
+SOURCES = ["herald_api.cu", "select_kernels.cu", "tc_kernels.cu", "move_kernels.cu",
+           "herald_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-warn-spills"]

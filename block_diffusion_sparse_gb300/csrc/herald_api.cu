@@ -234,6 +234,8 @@ thread_local TraceState g_trace;
 
 namespace herald {
 
+void set_last_error(const char* msg) { snprintf(g_err, sizeof g_err, "%s", msg); }
+
 void trace_before(cudaStream_t st, const char* name) {
   TraceState& t = g_trace;
   t.in_kernel = false;

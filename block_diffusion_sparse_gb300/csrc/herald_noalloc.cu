@@ -1,0 +1,118 @@
+// herald_noalloc.cu -- herald_select_stage2_noalloc: stage 2 of the selection
+// for callers that cannot hand the library a workspace.
+//
+// Some callers cannot allocate device memory at the point where they select:
+// a decode loop that runs under CUDA stream capture (cudaMalloc and cudaFree
+// are not allowed while a stream is being captured), a plugin inside a
+// serving runtime that owns the whole device-memory budget and hands out no
+// buffers after start-up, or a host callback where a synchronising
+// allocation would stall every stream.  For them this entry point keeps its
+// scratch -- the refine row statistics, the stage-2 scores and an error word
+// -- in one file-scope device array, so the call needs only its inputs and
+// outputs.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include "../../include/herald.h"
+#include "internal.cuh"
+
+using namespace herald;
+
+namespace {
+
+// Upper bound of the scratch this entry point may use.  Every GPU that loads
+// the library holds this array until the process exits.
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;
+
+static __device__ __align__(256) unsigned char g_stage2_scratch[kStaticScratchBytes];
+
+// Errors are reported like every other entry point: a status, with the
+// detail readable through herald_last_error().
+herald_status fail(herald_status s, const char* fmt, ...) {
+  char msg[256];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(msg, sizeof msg, fmt, ap);
+  va_end(ap);
+  set_last_error(msg);
+  return s;
+}
+
+// Device address of g_stage2_scratch on the current device.  Resolved once
+// per device, with that device current; host code must not use the array's
+// name as an address.
+herald_status scratch_address(unsigned char** out) {
+  static unsigned char* addr[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(HERALD_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return fail(HERALD_ERR_CUDA, "device ordinal %d out of range", dev);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_stage2_scratch);
+    if (e != cudaSuccess)
+      return fail(HERALD_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+    addr[dev] = static_cast<unsigned char*>(p);
+  }
+  *out = addr[dev];
+  return HERALD_OK;
+}
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+herald_status herald_select_stage2_noalloc(herald_dims dims, const uint16_t* q_block,
+                                           const uint16_t* k_cache, const int32_t* ctx_len,
+                                           const int32_t* cand, const int32_t* n_cand, int C,
+                                           int K, int sink, int local, int P_max, int32_t* idx,
+                                           int32_t* n_sel, void* stream) {
+  set_last_error("");
+  // the same argument rules as herald_select_stage2; a workspace-free call
+  // validates through the workspace-size query (0 = unsupported shape)
+  if (herald_workspace_size(dims, C, P_max < 1 ? 1 : P_max) == 0)
+    return fail(HERALD_ERR_UNSUPPORTED_SHAPE, "unsupported shape or C");
+  if (P_max < 1 || K < 0 || sink < 0 || local < 0 || K > C ||
+      (long long)K + sink + local > P_max)
+    return fail(HERALD_ERR_INVALID_ARG, "need 0 <= K <= C and K+sink+local <= P_max");
+  if (!aligned16(q_block) || !aligned16(k_cache) || !aligned16(ctx_len) || !aligned16(cand) ||
+      !aligned16(n_cand) || !aligned16(idx) || !aligned16(n_sel))
+    return fail(HERALD_ERR_INVALID_ARG, "a pointer is NULL or not 16-byte aligned");
+
+  // compact scratch layout: error word | refine row statistics | s2
+  const WsLayout full = ws_layout(dims, C, P_max);
+  const size_t NG = size_t(dims.N) * dims.Hkv;
+  const size_t err_off = 0;
+  const size_t rpart_off = 256;
+  const size_t rpart_bytes = NG * size_t(full.MT) * kTileM * full.n_chunks * 8;
+  const size_t s2_off = align_up(rpart_off + rpart_bytes, 256);
+  const size_t need = s2_off + NG * size_t(C) * 4;
+  if (need > kStaticScratchBytes)
+    return fail(HERALD_ERR_WORKSPACE_TOO_SMALL,
+                "these shapes need %zu bytes of scratch; the static scratch holds %zu",
+                need, kStaticScratchBytes);
+
+  unsigned char* base = nullptr;
+  herald_status s = scratch_address(&base);
+  if (s != HERALD_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* err = reinterpret_cast<uint32_t*>(base + err_off);
+  // the array keeps the previous call's contents: the error word must start
+  // at zero; the statistics and scores are fully rewritten before use
+  cudaError_t e = cudaMemsetAsync(err, 0, sizeof(uint32_t), st);
+  if (e == cudaSuccess)
+    e = launch_refine(dims, q_block, k_cache, cand, n_cand, C,
+                      reinterpret_cast<float2*>(base + rpart_off),
+                      reinterpret_cast<float*>(base + s2_off), full, err, st);
+  if (e == cudaSuccess)
+    e = launch_topk_union(dims, ctx_len, cand, n_cand, reinterpret_cast<float*>(base + s2_off), C,
+                          K, sink, local, P_max, idx, n_sel, st);
+  if (e != cudaSuccess)
+    return fail(HERALD_ERR_CUDA, "stage-2 launch: %s", cudaGetErrorString(e));
+  return HERALD_OK;
+}
+
+}  // extern "C"

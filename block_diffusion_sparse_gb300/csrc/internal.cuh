@@ -81,6 +81,9 @@ inline WsLayout ws_layout(const herald_dims& dm, int C, int P_max) {
   return w;
 }
 
+// Sets the text returned by herald_last_error() on this host thread.
+void set_last_error(const char* msg);
+
 // ---- kernel tracing: when enabled on this host thread, every kernel launch
 // is bracketed by two caller-owned CUDA events recorded on its stream.
 void trace_before(cudaStream_t st, const char* name);

@@ -20,7 +20,8 @@ STATUS = {0: "HERALD_OK", 1: "HERALD_ERR_INVALID_ARG", 2: "HERALD_ERR_UNSUPPORTE
 EXPORTS = ("herald_workspace_size", "herald_status_string", "herald_last_error",
            "herald_workspace_error", "herald_select_stage1", "herald_select_stage2",
            "herald_select", "herald_gather", "herald_denoise_attn", "herald_append_kv",
-           "herald_trace_begin", "herald_trace_end", "herald_trace_name")
+           "herald_trace_begin", "herald_trace_end", "herald_trace_name",
+           "herald_select_stage2_noalloc")
 
 
 class HeraldError(RuntimeError):
@@ -76,6 +77,8 @@ def lib() -> C.CDLL:
         L.herald_denoise_attn.argtypes = [Dims, vp, vp, vp, vp, i32, vp, vp, vp, C.c_float, vp,
                                           sz, vp]
         L.herald_append_kv.argtypes = [Dims, vp, vp, vp, vp, vp, i32, vp]
+        L.herald_select_stage2_noalloc.argtypes = [Dims, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                                   i32, vp, vp, vp]
         L.herald_trace_begin.argtypes = [C.POINTER(vp), i32, i32]
         L.herald_trace_end.argtypes = []
         L.herald_trace_name.argtypes = [i32]
@@ -155,6 +158,16 @@ def herald_select(d, q_merge, q_block, k_cache, ctx_len, C_, K, sink, local, P_m
     _check(lib().herald_select(d, _p(q_merge), _p(q_block), _p(k_cache), _p(ctx_len), int(C_),
                                int(K), int(sink), int(local), int(P_max), _p(idx), _p(n_sel),
                                _p(ws), _nbytes(ws, ws_bytes), _s(stream)))
+
+
+def herald_select_stage2_noalloc(d, q_block, k_cache, ctx_len, cand, n_cand, C_, K, sink, local,
+                                 P_max, idx, n_sel, stream=None):
+    """Stage 2 with the library's static scratch instead of a workspace, for
+    callers that cannot allocate device memory where they select (see
+    include/herald.h); calls that overlap on the GPU must be serialised."""
+    _check(lib().herald_select_stage2_noalloc(d, _p(q_block), _p(k_cache), _p(ctx_len), _p(cand),
+                                              _p(n_cand), int(C_), int(K), int(sink), int(local),
+                                              int(P_max), _p(idx), _p(n_sel), _s(stream)))
 
 
 def herald_gather(d, idx, n_sel, P_max, k_cache, v_cache, pool_k, pool_v, stream=None):

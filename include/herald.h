@@ -121,6 +121,30 @@ herald_status herald_select(herald_dims dims, const uint16_t *q_merge, const uin
                             int sink, int local, int P_max, int32_t *idx, int32_t *n_sel,
                             void *ws, size_t ws_bytes, void *stream);
 
+/* herald_select_stage2 without a workspace, for callers that cannot allocate
+ * device memory where they select (a decode loop under CUDA stream capture,
+ * where cudaMalloc is not allowed; a plugin in a serving runtime that owns
+ * the device-memory budget; a host callback where a synchronising
+ * allocation would stall every stream).  The pages have no counterpart: this
+ * is a deployment variant of the same stage-2 computation, with the same
+ * arguments and outputs minus the workspace.
+ *   Scratch lives in one static 4 MiB device array inside the library; every
+ *   GPU that loads the library holds it until the process exits.  Shapes
+ *   whose scratch -- 256 bytes + N*Hkv*ceil(B*G/128)*128*ceil(C/256)*8 bytes
+ *   of row statistics + N*Hkv*C*4 bytes of scores -- exceed 4 MiB are
+ *   rejected with HERALD_ERR_WORKSPACE_TOO_SMALL and a message.
+ *   The first call on a device resolves the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   All calls share the array: calls that can overlap on the GPU (other
+ *   streams, other host threads) race and must be serialised by the caller.
+ *   Device-side wait timeouts are recorded in the array, not reported.
+ *   Nothing is allocated or freed by this call. */
+herald_status herald_select_stage2_noalloc(herald_dims dims, const uint16_t *q_block,
+                                           const uint16_t *k_cache, const int32_t *ctx_len,
+                                           const int32_t *cand, const int32_t *n_cand, int C,
+                                           int K, int sink, int local, int P_max,
+                                           int32_t *idx, int32_t *n_sel, void *stream);
+
 /* Gathers the selected rows into one buffer of the double-buffered sparse
  * KV pool [EA]:  pool[n][g][s] = cache[n][g][idx[n][g][s]] for s < n_sel,
  * zero rows for n_sel <= s < P_max.
