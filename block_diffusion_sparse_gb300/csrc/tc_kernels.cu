@@ -864,10 +864,11 @@ static cudaError_t launch_cluster(const char* name, void (*kernel)(KArgs...), di
   return e;
 }
 
-// Whether 16-CTA clusters of the attention kernel can be resident on this
-// device (non-portable size; needs 16 SMs of one GPC).  Cached per device.
-template <int D>
-static bool cluster16_ok() {
+// How many clusters of CS CTAs of the attention kernel can be resident at
+// once on this device (a 16-CTA cluster needs 16 free SMs of one GPC).
+// Cached per device and cluster size.
+template <int D, int CS>
+static int max_active_clusters() {
   static int cache[64];
   static bool init = false;
   if (!init) {
@@ -875,32 +876,30 @@ static bool cluster16_ok() {
     init = true;
   }
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (cache[dev] < 0) {
-    int ok = 0;
-    if (cudaFuncSetAttribute(attn_cluster_kernel<D, kClusterCtasMax>,
-                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+    int n = 0;
+    if (CS <= 8 || cudaFuncSetAttribute(attn_cluster_kernel<D, CS>,
+                                        cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                        1) == cudaSuccess) {
       cudaLaunchConfig_t cfg{};
-      cfg.gridDim = dim3(kClusterCtasMax, 1, 1);
+      cfg.gridDim = dim3(CS, 1, 1);
       cfg.blockDim = dim3(kTcThreads);
       cfg.dynamicSmemBytes = AttnClCfg<D>::kSmem;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = kClusterCtasMax;
+      attr[0].val.clusterDim.x = CS;
       attr[0].val.clusterDim.y = 1;
       attr[0].val.clusterDim.z = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, attn_cluster_kernel<D, kClusterCtasMax>, &cfg) ==
-              cudaSuccess &&
-          n >= 1)
-        ok = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, attn_cluster_kernel<D, CS>, &cfg) != cudaSuccess)
+        n = 0;
     }
     cudaGetLastError();
-    cache[dev] = ok;
+    cache[dev] = n;
   }
-  return cache[dev] == 1;
+  return cache[dev];
 }
 
 template <int D>
@@ -925,7 +924,10 @@ static cudaError_t launch_attn_t(const herald_dims& dm, const uint16_t* q, const
     attr = true;
   }
   if (w.splits <= 2 * kClusterCtas && !force_split()) {
-    if (w.splits > kClusterCtas && cluster16_ok<D>())
+    // 16-CTA clusters (one key tile per CTA) only if the whole launch fits
+    // on the device at once; otherwise 8-CTA clusters with two tiles each
+    if (w.splits > kClusterCtas &&
+        max_active_clusters<D, kClusterCtasMax>() >= w.MT * segs)
       return launch_cluster("attn_cluster_kernel", attn_cluster_kernel<D, kClusterCtasMax>,
                             dim3(kClusterCtasMax, w.MT, segs), kClusterCtasMax,
                             AttnClCfg<D>::kSmem, st, q, pool_k, pool_v, n_sel, P_max, block_k,
