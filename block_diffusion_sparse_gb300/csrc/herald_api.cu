@@ -418,9 +418,18 @@ herald_status herald_denoise_attn(herald_dims dims, const uint16_t* q, const uin
   WsLayout w;
   HERALD_RET_IF(check_ws(dims, 1, P_max, ws, ws_bytes, &w));
   if (scale == 0.f) scale = 1.0f / sqrtf(float(dims.d));
+  CUtensorMap kmap, vmap;
+  const bool pool_maps = attn_pool_ok(dims, P_max);
+  if (pool_maps) {
+    const uint64_t rows = uint64_t(dims.N) * dims.Hkv * P_max;
+    const uint32_t box = uint32_t(attn_pool_kpc(P_max));
+    HERALD_RET_IF(encode_rows_map(pool_k, rows, dims.d, box, &kmap));
+    HERALD_RET_IF(encode_rows_map(pool_v, rows, dims.d, box, &vmap));
+  }
   HERALD_TRY_CUDA(launch_attn(dims, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale,
                               w, at<float>(ws, w.opart), at<float2>(ws, w.ml),
-                              at<uint32_t>(ws, w.err), static_cast<cudaStream_t>(stream)),
+                              at<uint32_t>(ws, w.err), pool_maps ? &kmap : nullptr,
+                              pool_maps ? &vmap : nullptr, static_cast<cudaStream_t>(stream)),
                   "attention launch");
   return HERALD_OK;
 }

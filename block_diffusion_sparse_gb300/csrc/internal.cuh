@@ -144,10 +144,16 @@ cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const i
 cudaError_t launch_gather(const herald_dims& dm, const int32_t* idx, const int32_t* n_sel,
                           int P_max, const uint16_t* k_cache, const uint16_t* v_cache,
                           uint16_t* pool_k, uint16_t* pool_v, cudaStream_t st);
+// Pool attention (balanced 8-CTA clusters, TMA-loaded pool slices) applies
+// when attn_pool_ok(); it needs the pool K and V as 2-D tensor maps
+// [N*Hkv*P_max][d] with a box of 64 columns x attn_pool_kpc(P_max) rows.
+int attn_pool_kpc(int P_max);
+bool attn_pool_ok(const herald_dims& dm, int P_max);
 cudaError_t launch_attn(const herald_dims& dm, const uint16_t* q, const uint16_t* pool_k,
                         const uint16_t* pool_v, const int32_t* n_sel, int P_max,
                         const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
                         float scale, const WsLayout& w, float* opart, float2* ml, uint32_t* err,
+                        const CUtensorMap* pool_kmap, const CUtensorMap* pool_vmap,
                         cudaStream_t st);
 cudaError_t launch_append(const herald_dims& dm, const uint16_t* block_k, const uint16_t* block_v,
                           int32_t* ctx, uint16_t* k_cache, uint16_t* v_cache, int advance,

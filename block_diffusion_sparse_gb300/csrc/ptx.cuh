@@ -103,6 +103,29 @@ HERALD_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, in
       : "memory");
 }
 
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to a
+// shared::cluster address (another CTA of the cluster), completing as
+// transaction bytes on the destination CTA's mbarrier (a shared::cluster
+// address as well).
+HERALD_DEV void bulk_copy_to_peer(uint32_t dst_cluster, const void* src, uint32_t bytes,
+                                  uint32_t mbar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes"
+      " [%0], [%1], %2, [%3];" ::"r"(dst_cluster),
+      "r"(smem_u32(src)), "r"(bytes), "r"(mbar_cluster)
+      : "memory");
+}
+HERALD_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until every committed bulk copy of this thread has read its source.
+HERALD_DEV void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// shared::cluster address of the same shared-memory location in CTA `rank`.
+HERALD_DEV uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
 // ------------------------------------------------------------------ cp.async
 // 16-byte async copy global -> shared; src_bytes = 0 writes zeros.
 HERALD_DEV void cp_async_16(void* dst, const void* src, uint32_t src_bytes) {

@@ -791,6 +791,322 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tmem_teardown(tbase, 512);
 }
 
+// ============================================================= attn_pool
+// Sparse block attention, one 8-CTA cluster per (sequence, KV head, 128-row
+// tile).  The pool is split evenly: CTA r owns pool keys [r*kpc, (r+1)*kpc)
+// (kpc = ceil(P_max/8) rounded to 16, at most 192), loaded by two 2-D TMA
+// boxes each for K and V; the last CTA also owns the B block keys.  Each
+// CTA computes S = Q K^T for its keys with one UMMA (N = kpc), P = exp(S -
+// rowmax) in bf16, O = P V into TMEM, and keeps (O, max, sum) in shared
+// memory.  After one cluster barrier every CTA pushes the 16 rows that CTA c
+// finalises into c's freed operand buffers with bulk shared::cta ->
+// shared::cluster copies that complete on c's mbarrier; each CTA then merges
+// its 16 rows from local shared memory and writes bf16 out.
+constexpr int kPoolCtas = 8;
+constexpr int kPoolRows = kTileM / kPoolCtas;   // rows finalised per CTA
+constexpr int kPoolMaxKpc = 192;
+constexpr int kPoolMaxB = 64;
+
+struct PoolSmem {
+  uint32_t q, k, v, p, kb, vb, pb, recv_o, recv_ml, total;
+};
+__host__ __device__ inline PoolSmem pool_smem(int D, int kpc, int Bp) {
+  const uint32_t H = uint32_t(D / 64);
+  PoolSmem L;
+  L.q = 0;
+  L.k = H * 128u * 128u;
+  L.v = L.k + H * uint32_t(kpc) * 128u;
+  L.p = L.v + H * uint32_t(kpc) * 128u;
+  L.kb = L.p + uint32_t((kpc + 63) / 64) * 16384u;
+  L.vb = L.kb + H * uint32_t(Bp) * 128u;
+  L.pb = L.vb + H * uint32_t(Bp) * 128u;
+  const uint32_t layout_end = L.pb + 16384u;
+  const uint32_t o_bytes = 128u * uint32_t(D + 4) * 4u;  // O partial, over Q/K/...
+  L.recv_o = (o_bytes + 1023u) & ~1023u;
+  L.recv_ml = L.recv_o + uint32_t(kPoolCtas * kPoolRows) * uint32_t(D + 4) * 4u;
+  const uint32_t recv_end = L.recv_ml + uint32_t(kPoolCtas * kPoolRows) * 8u;
+  L.total = (layout_end > recv_end ? layout_end : recv_end) + 1024u;
+  return L;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    attn_pool_kernel(const __grid_constant__ CUtensorMap kmap,
+                     const __grid_constant__ CUtensorMap vmap, const uint16_t* __restrict__ q,
+                     const int32_t* __restrict__ n_sel, int P_max,
+                     const uint16_t* __restrict__ block_k, const uint16_t* __restrict__ block_v,
+                     int B, int Hq, int Hkv, int R, int kpc, float scale,
+                     uint16_t* __restrict__ out, uint32_t* err) {
+  constexpr int H = D / 64;
+  constexpr int OROW = D + 4;  // fp32 row stride of O partials (bank-conflict padding)
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t barK, barV, bar0, bar1, barR;
+  __shared__ uint32_t tmem_base;
+  __shared__ float red_m[2][kTileM];
+  __shared__ float red_s[2][kTileM];
+  __shared__ __align__(16) float2 ml[kTileM];
+  const int Bp = (B + 15) & ~15;
+  const PoolSmem S = pool_smem(D, kpc, Bp);
+  uint8_t* base = align1024(smem_raw);
+  uint8_t* Qs = base + S.q;
+  uint8_t* Ks = base + S.k;
+  uint8_t* Vs = base + S.v;
+  uint8_t* Ps = base + S.p;
+  uint8_t* Kb = base + S.kb;
+  uint8_t* Vb = base + S.vb;
+  uint8_t* Pb = base + S.pb;
+  float* Os = reinterpret_cast<float*>(base);
+  float* recv_o = reinterpret_cast<float*>(base + S.recv_o);
+  float2* recv_ml = reinterpret_cast<float2*>(base + S.recv_ml);
+  const uint32_t rank = cluster_ctarank();
+  const int mt = blockIdx.y, seg = blockIdx.z;
+  const int n = seg / Hkv, g = seg - n * Hkv, G = Hq / Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(&barK, 1);
+    mbar_init(&barV, 1);
+    mbar_init(&bar0, 1);
+    mbar_init(&bar1, 1);
+    mbar_init(&barR, 1);
+    fence_mbar_init();
+  }
+  tmem_setup(&tmem_base, 512);
+  const uint32_t tbase = tmem_base;
+  griddep_enter();
+  const int ns = min(max(n_sel[seg], 0), P_max);
+  const int k0 = int(rank) * kpc;
+  const int nkp = min(max(ns - k0, 0), kpc);           // valid pool keys of this CTA
+  const bool has_blk = rank == kPoolCtas - 1 && B > 0;  // the block keys
+  const bool any = nkp > 0 || has_blk;
+
+  if (threadIdx.x == 0 && nkp > 0) {
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+    mbar_arrive_expect_tx(&barK, uint32_t(H * kpc * 128));
+#pragma unroll
+    for (int hv = 0; hv < H; ++hv)
+      tma_load_2d(Ks + hv * kpc * 128, &kmap, &barK, hv * 64, seg * P_max + k0);
+    mbar_arrive_expect_tx(&barV, uint32_t(H * kpc * 128));
+#pragma unroll
+    for (int hv = 0; hv < H; ++hv)
+      tma_load_2d(Vs + hv * kpc * 128, &vmap, &barV, hv * 64, seg * P_max + k0);
+  }
+  if (any) {
+    load_rows_sw128<D>(Qs, kTileM, kTileM, q, [&](int r) -> const uint16_t* {
+      const int rr = mt * kTileM + r;
+      if (rr >= R) return nullptr;
+      const int b = rr / G, hl = rr - (rr / G) * G;
+      return q + ((size_t(n) * B + b) * Hq + g * G + hl) * D;
+    });
+    if (has_blk) {
+      load_rows_sw128<D>(Kb, Bp, Bp, block_k, [&](int r) -> const uint16_t* {
+        return r < B ? block_k + ((size_t(n) * B + r) * Hkv + g) * D : nullptr;
+      });
+      load_rows_sw128<D>(Vb, Bp, Bp, block_v, [&](int r) -> const uint16_t* {
+        return r < B ? block_v + ((size_t(n) * B + r) * Hkv + g) * D : nullptr;
+      });
+    }
+    cp_async_commit();
+    cp_async_wait_all();
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+  tc_fence_after();
+
+  // S = Q [K ; K_block]^T -> TMEM columns [0, kpc) and [kpc, kpc + Bp)
+  bool ok = true;
+  if (threadIdx.x == 0 && any) {
+    const uint32_t qa = smem_u32(Qs);
+    if (nkp > 0) {
+      ok = mbar_wait(&barK, 0);
+      tc_fence_after();
+      const uint32_t idesc = make_idesc_bf16(kTileM, kpc, false, false);
+      const uint32_t ka = smem_u32(Ks);
+#pragma unroll
+      for (int s = 0; s < D / 16; ++s) {
+        const uint32_t hv = s >> 2, koff = (s & 3) * 32;
+        const uint64_t a = make_sdesc_sw128(qa + hv * (kTileM * 128) + koff, 16, 1024);
+        const uint64_t b = make_sdesc_sw128(ka + hv * (kpc * 128) + koff, 16, 1024);
+        umma_bf16(tbase, a, b, idesc, s > 0 ? 1u : 0u);
+      }
+    }
+    if (has_blk) {
+      const uint32_t idesc = make_idesc_bf16(kTileM, Bp, false, false);
+      const uint32_t ka = smem_u32(Kb);
+#pragma unroll
+      for (int s = 0; s < D / 16; ++s) {
+        const uint32_t hv = s >> 2, koff = (s & 3) * 32;
+        const uint64_t a = make_sdesc_sw128(qa + hv * (kTileM * 128) + koff, 16, 1024);
+        const uint64_t b = make_sdesc_sw128(ka + hv * (Bp * 128) + koff, 16, 1024);
+        umma_bf16(tbase + uint32_t(kpc), a, b, idesc, s > 0 ? 1u : 0u);
+      }
+    }
+    umma_commit(&bar0);
+  }
+  if (any && !mbar_wait(&bar0, 0)) ok = false;
+  tc_fence_after();
+  __syncwarp();
+
+  // softmax over this CTA's columns; the 16-column chunks are split between
+  // the two warps that share a TMEM lane quadrant
+  const int quad = warp & 3, ch = warp >> 2;
+  const int row = quad * 32 + lane;
+  const uint32_t trow = tbase + (uint32_t(quad * 32) << 16);
+  const int nchunks = any ? (kpc + (has_blk ? Bp : 0)) / 16 : 0;
+  const int half = (nchunks + 1) / 2;
+  const int c_begin = ch == 0 ? 0 : half, c_end = ch == 0 ? half : nchunks;
+  constexpr int kMaxChunks = (kPoolMaxKpc + kPoolMaxB) / 32;  // per half
+  float x[kMaxChunks][16];
+  float m = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < kMaxChunks; ++c) {
+    const int ci = c_begin + c;
+    if (ci < c_end) {
+      tmem_ld16(trow + uint32_t(ci * 16), x[c]);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int kc = ci * 16 + i;
+        const bool valid = kc < kpc ? kc < nkp : kc - kpc < B;
+        x[c][i] = valid ? x[c][i] * scale : -INFINITY;
+        m = fmaxf(m, x[c][i]);
+      }
+    }
+  }
+  red_m[ch][row] = m;
+  __syncthreads();
+  m = fmaxf(red_m[0][row], red_m[1][row]);
+  float lsum = 0.f;
+#pragma unroll
+  for (int c = 0; c < kMaxChunks; ++c) {
+    const int ci = c_begin + c;
+    if (ci < c_end) {
+      float p[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        p[i] = m == -INFINITY ? 0.f : __expf(x[c][i] - m);
+        lsum += p[i];
+      }
+      const int kc = ci * 16;
+      uint8_t* blk = kc < kpc ? Ps + (kc >> 6) * 16384 : Pb;
+      const int cc = ((kc < kpc ? kc : kc - kpc) & 63) >> 3;  // 16-byte chunk (8 keys)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint4 pk;
+        pk.x = pack_bf16(p[8 * hh + 0], p[8 * hh + 1]);
+        pk.y = pack_bf16(p[8 * hh + 2], p[8 * hh + 3]);
+        pk.z = pack_bf16(p[8 * hh + 4], p[8 * hh + 5]);
+        pk.w = pack_bf16(p[8 * hh + 6], p[8 * hh + 7]);
+        *reinterpret_cast<uint4*>(blk + sw128_off(row, cc + hh)) = pk;
+      }
+    }
+  }
+  red_s[ch][row] = lsum;
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  // O = P V (+ P_block V_block) -> TMEM columns [256, 256 + D)
+  if (threadIdx.x == 0 && any) {
+    constexpr uint32_t idesc = make_idesc_bf16(kTileM, D, false, true);
+    bool acc = false;
+    if (nkp > 0) {
+      ok = mbar_wait(&barV, 0) && ok;
+      tc_fence_after();
+      const uint32_t pa = smem_u32(Ps), va = smem_u32(Vs);
+      for (int s = 0; s < kpc / 16; ++s) {
+        const uint64_t a =
+            make_sdesc_sw128(pa + uint32_t(s >> 2) * 16384u + uint32_t(s & 3) * 32u, 16, 1024);
+        const uint64_t b = make_sdesc_sw128(va + uint32_t(s) * 2048u, uint32_t(kpc) * 128u, 1024);
+        umma_bf16(tbase + 256, a, b, idesc, acc ? 1u : 0u);
+        acc = true;
+      }
+    }
+    if (has_blk) {
+      const uint32_t pa = smem_u32(Pb), va = smem_u32(Vb);
+      for (int s = 0; s < Bp / 16; ++s) {
+        const uint64_t a = make_sdesc_sw128(pa + uint32_t(s & 3) * 32u, 16, 1024);
+        const uint64_t b = make_sdesc_sw128(va + uint32_t(s) * 2048u, uint32_t(Bp) * 128u, 1024);
+        umma_bf16(tbase + 256, a, b, idesc, acc ? 1u : 0u);
+        acc = true;
+      }
+    }
+    umma_commit(&bar1);
+  }
+  if (any && !mbar_wait(&bar1, 0)) ok = false;
+  tc_fence_after();
+  __syncwarp();
+  if (!ok) record_error(err, DEV_TIMEOUT_MMA);
+
+  // O partial -> shared memory (over Q / K, now free), row-major fp32
+  if (any) {
+#pragma unroll
+    for (int k = 0; k < D / 64; ++k) {
+      float v[32];
+      const int col = ch * (D / 2) + k * 32;
+      tmem_ld32(trow + 256 + uint32_t(col), v);
+      float* orow = Os + row * OROW + col;
+#pragma unroll
+      for (int i = 0; i < 32; i += 4)
+        *reinterpret_cast<float4*>(orow + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+    }
+  }
+  if (ch == 0) ml[row] = make_float2(m, red_s[0][row] + red_s[1][row]);
+  constexpr uint32_t kSliceO = uint32_t(kPoolRows * OROW * 4);
+  constexpr uint32_t kSliceMl = uint32_t(kPoolRows * 8);
+  if (threadIdx.x == 0) mbar_arrive_expect_tx(&barR, kPoolCtas * (kSliceO + kSliceMl));
+  fence_proxy_async_smem();  // the partial is read by bulk copies (async proxy)
+  cluster_sync_all();        // every CTA: operands consumed, partial final
+
+  // push: rows [c*16, c*16+16) of this CTA's partial go to CTA c, slot `rank`
+  if (threadIdx.x == 0) {
+    for (uint32_t c = 0; c < uint32_t(kPoolCtas); ++c) {
+      const uint32_t mb = cluster_addr(&barR, c);
+      bulk_copy_to_peer(cluster_addr(reinterpret_cast<uint8_t*>(recv_o) + rank * kSliceO, c),
+                        Os + c * kPoolRows * OROW, kSliceO, mb);
+      bulk_copy_to_peer(cluster_addr(reinterpret_cast<uint8_t*>(recv_ml) + rank * kSliceMl, c),
+                        &ml[c * kPoolRows], kSliceMl, mb);
+    }
+    bulk_commit();
+  }
+  if (!mbar_wait(&barR, 0)) record_error(err, DEV_TIMEOUT_TMA);
+
+  // merge this CTA's 16 rows from the 8 received partials
+  constexpr int E = D / 32;
+  for (int rr = warp; rr < kPoolRows; rr += kTcThreads / 32) {
+    const int lr = int(rank) * kPoolRows + rr;
+    const int grow = mt * kTileM + lr;
+    float M = -INFINITY;
+    float2 pm[kPoolCtas];
+#pragma unroll
+    for (int c = 0; c < kPoolCtas; ++c) {
+      pm[c] = recv_ml[c * kPoolRows + rr];
+      M = fmaxf(M, pm[c].x);
+    }
+    float acc[E] = {};
+    float L = 0.f;
+#pragma unroll
+    for (int c = 0; c < kPoolCtas; ++c) {
+      if (pm[c].x == -INFINITY) continue;
+      const float wgt = __expf(pm[c].x - M);
+      L += wgt * pm[c].y;
+      const float* o = recv_o + (c * kPoolRows + rr) * OROW + lane * E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] += wgt * o[e];
+    }
+    if (grow < R) {
+      const int b = grow / G, h = g * G + (grow - (grow / G) * G);
+      uint16_t* dst = out + ((size_t(n) * B + b) * Hq + h) * D + lane * E;
+      const float inv = 1.f / L;
+#pragma unroll
+      for (int e = 0; e < E; e += 2)
+        *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16(acc[e] * inv, acc[e + 1] * inv);
+    }
+  }
+  if (threadIdx.x == 0) bulk_wait_read_all();  // outgoing copies have read this CTA's partial
+  tmem_teardown(tbase, 512);
+}
+
 // =========================================================== attn_combine
 // One warp per output row (n, b, h); lane owns D/32 consecutive features.
 template <int D>
@@ -902,14 +1218,38 @@ static int max_active_clusters() {
   return cache[dev];
 }
 
+int attn_pool_kpc(int P_max) { return cdiv(cdiv(P_max, kPoolCtas), 16) * 16; }
+
+bool attn_pool_ok(const herald_dims& dm, int P_max) {
+  const int kpc = attn_pool_kpc(P_max);
+  const int Bp = (dm.B + 15) & ~15;
+  return kpc <= kPoolMaxKpc && dm.B <= kPoolMaxB &&
+         pool_smem(dm.d, kpc, Bp).total <= 227u * 1024u;
+}
+
 template <int D>
 static cudaError_t launch_attn_t(const herald_dims& dm, const uint16_t* q, const uint16_t* pool_k,
                                  const uint16_t* pool_v, const int32_t* n_sel, int P_max,
                                  const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
                                  float scale, const WsLayout& w, float* opart, float2* ml,
-                                 uint32_t* err, cudaStream_t st) {
+                                 uint32_t* err, const CUtensorMap* pool_kmap,
+                                 const CUtensorMap* pool_vmap, cudaStream_t st) {
   const int segs = dm.N * dm.Hkv;
   cudaError_t e;
+  if (pool_kmap && pool_vmap && !force_split()) {
+    static bool pattr = false;
+    if (!pattr) {
+      e = cudaFuncSetAttribute(attn_pool_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               227 * 1024);
+      if (e != cudaSuccess) return e;
+      pattr = true;
+    }
+    const int kpc = attn_pool_kpc(P_max);
+    const uint32_t smem = pool_smem(D, kpc, (dm.B + 15) & ~15).total;
+    return launch_cluster("attn_pool_kernel", attn_pool_kernel<D>, dim3(kPoolCtas, w.MT, segs),
+                          kPoolCtas, smem, st, *pool_kmap, *pool_vmap, q, n_sel, P_max, block_k,
+                          block_v, dm.B, dm.Hq, dm.Hkv, w.R, kpc, scale, out, err);
+  }
   static bool attr = false;
   if (!attr) {
     e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -952,12 +1292,13 @@ cudaError_t launch_attn(const herald_dims& dm, const uint16_t* q, const uint16_t
                         const uint16_t* pool_v, const int32_t* n_sel, int P_max,
                         const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
                         float scale, const WsLayout& w, float* opart, float2* ml, uint32_t* err,
+                        const CUtensorMap* pool_kmap, const CUtensorMap* pool_vmap,
                         cudaStream_t st) {
   if (dm.d == 128)
     return launch_attn_t<128>(dm, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale,
-                              w, opart, ml, err, st);
+                              w, opart, ml, err, pool_kmap, pool_vmap, st);
   return launch_attn_t<64>(dm, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale, w,
-                           opart, ml, err, st);
+                           opart, ml, err, pool_kmap, pool_vmap, st);
 }
 
 }  // namespace herald
