@@ -1223,8 +1223,9 @@ int attn_pool_kpc(int P_max) { return cdiv(cdiv(P_max, kPoolCtas), 16) * 16; }
 bool attn_pool_ok(const herald_dims& dm, int P_max) {
   const int kpc = attn_pool_kpc(P_max);
   const int Bp = (dm.B + 15) & ~15;
+  // the dynamic allocation plus the kernel's static shared memory (~3 KB)
   return kpc <= kPoolMaxKpc && dm.B <= kPoolMaxB &&
-         pool_smem(dm.d, kpc, Bp).total <= 227u * 1024u;
+         pool_smem(dm.d, kpc, Bp).total <= 220u * 1024u;
 }
 
 template <int D>
@@ -1237,15 +1238,15 @@ static cudaError_t launch_attn_t(const herald_dims& dm, const uint16_t* q, const
   const int segs = dm.N * dm.Hkv;
   cudaError_t e;
   if (pool_kmap && pool_vmap && !force_split()) {
-    static bool pattr = false;
-    if (!pattr) {
-      e = cudaFuncSetAttribute(attn_pool_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               227 * 1024);
-      if (e != cudaSuccess) return e;
-      pattr = true;
-    }
     const int kpc = attn_pool_kpc(P_max);
     const uint32_t smem = pool_smem(D, kpc, (dm.B + 15) & ~15).total;
+    static uint32_t attr_bytes = 0;  // dynamic shared memory granted so far
+    if (smem > attr_bytes) {
+      e = cudaFuncSetAttribute(attn_pool_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               int(smem));
+      if (e != cudaSuccess) return e;
+      attr_bytes = smem;
+    }
     return launch_cluster("attn_pool_kernel", attn_pool_kernel<D>, dim3(kPoolCtas, w.MT, segs),
                           kPoolCtas, smem, st, *pool_kmap, *pool_vmap, q, n_sel, P_max, block_k,
                           block_v, dm.B, dm.Hq, dm.Hkv, w.R, kpc, scale, out, err);
