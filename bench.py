@@ -267,6 +267,7 @@ def algorithmic_work(w, n_sel: np.ndarray) -> dict:
                            "bytes": NG * w.L * w.d * 2},
         "attn_kernel": attn,
         "attn_cluster_kernel": attn,
+        "attn_pool_kernel": attn,
         "gather_kernel": {"bound": "hbm", "bytes": int(ns.sum()) * w.d * 2 * 2 * 2},
         "refine_pass1_kernel": {"bound": "tensor", "flops": 2 * R * w.C * w.d * NG},
         "refine_pass2_kernel": {"bound": "tensor", "flops": 2 * R * w.C * w.d * NG},
@@ -449,7 +450,8 @@ def run_ours(args, rank, world, dist):
                 "peak_source": f"{pk_kind} (MEASURED_PEAKS.json)" if pk_kind == "measured"
                 else "fallback"}
 
-    roofline = roof(dominant) or roof("attn_cluster_kernel") or roof("attn_kernel")
+    roofline = (roof(dominant) or roof("attn_pool_kernel") or roof("attn_cluster_kernel")
+                or roof("attn_kernel"))
     scan = roof("scan_tc_kernel") or roof("scan_cc_kernel")
 
     # end to end through the C ABI with host buffers

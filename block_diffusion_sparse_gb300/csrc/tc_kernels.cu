@@ -821,9 +821,9 @@ __host__ __device__ inline PoolSmem pool_smem(int D, int kpc, int Bp) {
   L.vb = L.kb + H * uint32_t(Bp) * 128u;
   L.pb = L.vb + H * uint32_t(Bp) * 128u;
   const uint32_t layout_end = L.pb + 16384u;
-  const uint32_t o_bytes = 128u * uint32_t(D + 4) * 4u;  // O partial, over Q/K/...
+  const uint32_t o_bytes = 128u * uint32_t(D + 8) * 2u;  // fp16 O partial, over Q/K/...
   L.recv_o = (o_bytes + 1023u) & ~1023u;
-  L.recv_ml = L.recv_o + uint32_t(kPoolCtas * kPoolRows) * uint32_t(D + 4) * 4u;
+  L.recv_ml = L.recv_o + uint32_t(kPoolCtas * kPoolRows) * uint32_t(D + 8) * 2u;
   const uint32_t recv_end = L.recv_ml + uint32_t(kPoolCtas * kPoolRows) * 8u;
   L.total = (layout_end > recv_end ? layout_end : recv_end) + 1024u;
   return L;
@@ -838,7 +838,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                      int B, int Hq, int Hkv, int R, int kpc, float scale,
                      uint16_t* __restrict__ out, uint32_t* err) {
   constexpr int H = D / 64;
-  constexpr int OROW = D + 4;  // fp32 row stride of O partials (bank-conflict padding)
+  constexpr int OROW = D + 8;  // fp16 row stride of O partials (16-byte padding)
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t barK, barV, bar0, bar1, barR;
   __shared__ uint32_t tmem_base;
@@ -947,8 +947,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   __syncwarp();
 
-  // softmax over this CTA's columns; the 16-column chunks are split between
-  // the two warps that share a TMEM lane quadrant
+  // softmax over this CTA's columns, in log2 units; the 16-column chunks are
+  // split between the two warps that share a TMEM lane quadrant
   const int quad = warp & 3, ch = warp >> 2;
   const int row = quad * 32 + lane;
   const uint32_t trow = tbase + (uint32_t(quad * 32) << 16);
@@ -956,25 +956,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int half = (nchunks + 1) / 2;
   const int c_begin = ch == 0 ? 0 : half, c_end = ch == 0 ? half : nchunks;
   constexpr int kMaxChunks = (kPoolMaxKpc + kPoolMaxB) / 32;  // per half
+  const float sl2 = scale * 1.4426950408889634f;              // scores -> log2 units
   float x[kMaxChunks][16];
-  float m = -INFINITY;
+  int nv[kMaxChunks];  // valid keys per chunk (warp-uniform)
 #pragma unroll
   for (int c = 0; c < kMaxChunks; ++c) {
     const int ci = c_begin + c;
+    const int k16 = ci * 16;
+    nv[c] = ci >= c_end ? 0
+            : k16 < kpc ? min(max(nkp - k16, 0), 16)
+                        : min(max(B - (k16 - kpc), 0), 16);
     if (ci < c_end) {
-      tmem_ld16(trow + uint32_t(ci * 16), x[c]);
+      uint32_t* r = reinterpret_cast<uint32_t*>(x[c]);
+      asm volatile(
+          "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+          "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+          : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+            "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+            "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+          : "r"(trow + uint32_t(k16)));
+    }
+  }
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  float m = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int kc = ci * 16 + i;
-        const bool valid = kc < kpc ? kc < nkp : kc - kpc < B;
-        x[c][i] = valid ? x[c][i] * scale : -INFINITY;
-        m = fmaxf(m, x[c][i]);
-      }
+  for (int c = 0; c < kMaxChunks; ++c) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      x[c][i] = i < nv[c] ? x[c][i] * sl2 : -INFINITY;
+      m = fmaxf(m, x[c][i]);
     }
   }
   red_m[ch][row] = m;
   __syncthreads();
   m = fmaxf(red_m[0][row], red_m[1][row]);
+  const float mm = m == -INFINITY ? 0.f : m;  // no valid key: every p is 2^-inf = 0
   float lsum = 0.f;
 #pragma unroll
   for (int c = 0; c < kMaxChunks; ++c) {
@@ -983,7 +999,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float p[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        p[i] = m == -INFINITY ? 0.f : __expf(x[c][i] - m);
+        p[i] = fast_exp2(x[c][i] - mm);
         lsum += p[i];
       }
       const int kc = ci * 16;
@@ -1038,21 +1054,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncwarp();
   if (!ok) record_error(err, DEV_TIMEOUT_MMA);
 
-  // O partial -> shared memory (over Q / K, now free), row-major fp32
+  // O partial -> shared memory (over Q / K, now free): each row divided by
+  // its sum and stored as fp16 (|o / l| <= max |v|); the merge re-weights by
+  // (max, sum), which stay fp32
+  const float lrow = red_s[0][row] + red_s[1][row];
   if (any) {
+    const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
+    uint16_t* orow = reinterpret_cast<uint16_t*>(Os) + row * OROW;
 #pragma unroll
     for (int k = 0; k < D / 64; ++k) {
       float v[32];
       const int col = ch * (D / 2) + k * 32;
       tmem_ld32(trow + 256 + uint32_t(col), v);
-      float* orow = Os + row * OROW + col;
 #pragma unroll
-      for (int i = 0; i < 32; i += 4)
-        *reinterpret_cast<float4*>(orow + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+      for (int i = 0; i < 32; i += 8) {
+        uint4 h;
+        h.x = pack_half2(v[i] * inv, v[i + 1] * inv);
+        h.y = pack_half2(v[i + 2] * inv, v[i + 3] * inv);
+        h.z = pack_half2(v[i + 4] * inv, v[i + 5] * inv);
+        h.w = pack_half2(v[i + 6] * inv, v[i + 7] * inv);
+        *reinterpret_cast<uint4*>(orow + col + i) = h;
+      }
     }
   }
-  if (ch == 0) ml[row] = make_float2(m, red_s[0][row] + red_s[1][row]);
-  constexpr uint32_t kSliceO = uint32_t(kPoolRows * OROW * 4);
+  if (ch == 0) ml[row] = make_float2(m, lrow);
+  constexpr uint32_t kSliceO = uint32_t(kPoolRows * OROW * 2);
   constexpr uint32_t kSliceMl = uint32_t(kPoolRows * 8);
   if (threadIdx.x == 0) mbar_arrive_expect_tx(&barR, kPoolCtas * (kSliceO + kSliceMl));
   fence_proxy_async_smem();  // the partial is read by bulk copies (async proxy)
@@ -1063,7 +1089,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (uint32_t c = 0; c < uint32_t(kPoolCtas); ++c) {
       const uint32_t mb = cluster_addr(&barR, c);
       bulk_copy_to_peer(cluster_addr(reinterpret_cast<uint8_t*>(recv_o) + rank * kSliceO, c),
-                        Os + c * kPoolRows * OROW, kSliceO, mb);
+                        reinterpret_cast<uint16_t*>(Os) + c * kPoolRows * OROW, kSliceO, mb);
       bulk_copy_to_peer(cluster_addr(reinterpret_cast<uint8_t*>(recv_ml) + rank * kSliceMl, c),
                         &ml[c * kPoolRows], kSliceMl, mb);
     }
@@ -1071,8 +1097,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   if (!mbar_wait(&barR, 0)) record_error(err, DEV_TIMEOUT_TMA);
 
-  // merge this CTA's 16 rows from the 8 received partials
+  // merge this CTA's 16 rows from the 8 received partials:
+  // out = sum_c 2^(m_c - M) l_c (o_c / l_c) / sum_c 2^(m_c - M) l_c
   constexpr int E = D / 32;
+  const uint16_t* recv_h = reinterpret_cast<const uint16_t*>(recv_o);
   for (int rr = warp; rr < kPoolRows; rr += kTcThreads / 32) {
     const int lr = int(rank) * kPoolRows + rr;
     const int grow = mt * kTileM + lr;
@@ -1087,12 +1115,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float L = 0.f;
 #pragma unroll
     for (int c = 0; c < kPoolCtas; ++c) {
-      if (pm[c].x == -INFINITY) continue;
-      const float wgt = __expf(pm[c].x - M);
-      L += wgt * pm[c].y;
-      const float* o = recv_o + (c * kPoolRows + rr) * OROW + lane * E;
+      if (pm[c].x == -INFINITY || pm[c].y <= 0.f) continue;
+      const float wgt = fast_exp2(pm[c].x - M) * pm[c].y;
+      L += wgt;
+      const __half* o = reinterpret_cast<const __half*>(recv_h + (c * kPoolRows + rr) * OROW) +
+                        lane * E;
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] += wgt * o[e];
+      for (int e = 0; e < E; ++e) acc[e] += wgt * __half2float(o[e]);
     }
     if (grow < R) {
       const int b = grow / G, h = g * G + (grow - (grow / G) * G);
