@@ -190,8 +190,9 @@ herald_status run_stage2(const herald_dims& dm, const uint16_t* q_block, const u
   HERALD_TRY_CUDA(launch_refine(dm, q_block, k_cache, cand, n_cand, C, at<float2>(ws, w.rpart),
                                 at<float>(ws, w.s2), w, err, st),
                   "refine launch");
-  HERALD_TRY_CUDA(launch_topk_union(dm, ctx_len, cand, n_cand, at<float>(ws, w.s2), C, K, sink,
-                                    local, P_max, idx, n_sel, st),
+  const int n_parts = refine_fused_ok(C) ? w.MT : 1;
+  HERALD_TRY_CUDA(launch_topk_union(dm, ctx_len, cand, n_cand, at<float>(ws, w.s2), n_parts, C, K,
+                                    sink, local, P_max, idx, n_sel, st),
                   "topk_union launch");
   return HERALD_OK;
 }

@@ -89,7 +89,8 @@ herald_status herald_select_stage2_noalloc(herald_dims dims, const uint16_t* q_b
   const size_t rpart_off = 256;
   const size_t rpart_bytes = NG * size_t(full.MT) * kTileM * full.n_chunks * 8;
   const size_t s2_off = align_up(rpart_off + rpart_bytes, 256);
-  const size_t need = s2_off + NG * size_t(C) * 4;
+  const int n_parts = refine_fused_ok(C) ? full.MT : 1;  // s2 partials per row tile
+  const size_t need = s2_off + NG * size_t(C) * 4 * size_t(n_parts);
   if (need > kStaticScratchBytes)
     return fail(HERALD_ERR_WORKSPACE_TOO_SMALL,
                 "these shapes need %zu bytes of scratch; the static scratch holds %zu",
@@ -108,8 +109,8 @@ herald_status herald_select_stage2_noalloc(herald_dims dims, const uint16_t* q_b
                       reinterpret_cast<float2*>(base + rpart_off),
                       reinterpret_cast<float*>(base + s2_off), full, err, st);
   if (e == cudaSuccess)
-    e = launch_topk_union(dims, ctx_len, cand, n_cand, reinterpret_cast<float*>(base + s2_off), C,
-                          K, sink, local, P_max, idx, n_sel, st);
+    e = launch_topk_union(dims, ctx_len, cand, n_cand, reinterpret_cast<float*>(base + s2_off),
+                          n_parts, C, K, sink, local, P_max, idx, n_sel, st);
   if (e != cudaSuccess)
     return fail(HERALD_ERR_CUDA, "stage-2 launch: %s", cudaGetErrorString(e));
   return HERALD_OK;

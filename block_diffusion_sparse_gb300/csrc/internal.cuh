@@ -44,7 +44,7 @@ struct WsLayout {
   size_t cand;       // int32 [N][Hkv][C]       (herald_select only)
   size_t n_cand;     // int32 [N][Hkv]
   size_t rpart;      // float2 [N][Hkv][R_pad][n_chunks]  refine row stats
-  size_t s2;         // float [N][Hkv][C]
+  size_t s2;         // float [MT][N][Hkv][C] stage-2 score partials
   size_t opart;      // float [N*Hkv][MT][S][128][d]      attention partials
   size_t ml;         // float2 [N*Hkv][MT][S][128]
   size_t total;
@@ -74,7 +74,7 @@ inline WsLayout ws_layout(const herald_dims& dm, int C, int P_max) {
   w.cand = o;   o = align_up(o + NG * C * 4, A);
   w.n_cand = o; o = align_up(o + NG * 4, A);
   w.rpart = o;  o = align_up(o + NG * size_t(w.MT) * kTileM * w.n_chunks * 8, A);
-  w.s2 = o;     o = align_up(o + NG * C * 4, A);
+  w.s2 = o;     o = align_up(o + NG * C * 4 * size_t(w.MT), A);  // one partial per row tile
   w.opart = o;  o = align_up(o + NG * w.MT * size_t(w.splits) * kTileM * dm.d * 4, A);
   w.ml = o;     o = align_up(o + NG * w.MT * size_t(w.splits) * kTileM * 8, A);
   w.total = o;
@@ -135,12 +135,17 @@ cudaError_t launch_s1_hist(const herald_dims& dm, const float* logits, const flo
 cudaError_t launch_topc(const herald_dims& dm, const float* s1, const uint32_t* hist,
                         const int32_t* ctx, int C, int32_t* cand, int32_t* n_cand,
                         const WsLayout& w, cudaStream_t st);
+// Whether stage 2 runs as the fused cluster kernel for this C; it then
+// writes one s2 partial per 128-row tile ([MT][N*Hkv][C]), else one.
+bool refine_fused_ok(int C);
 cudaError_t launch_refine(const herald_dims& dm, const uint16_t* q_block, const uint16_t* k_cache,
                           const int32_t* cand, const int32_t* n_cand, int C, float2* rpart,
                           float* s2, const WsLayout& w, uint32_t* err, cudaStream_t st);
+// s2 holds n_parts partial score arrays of [N*Hkv][C], summed per candidate.
 cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const int32_t* cand,
-                              const int32_t* n_cand, const float* s2, int C, int K, int S, int W,
-                              int P_max, int32_t* idx, int32_t* n_sel, cudaStream_t st);
+                              const int32_t* n_cand, const float* s2, int n_parts, int C, int K,
+                              int S, int W, int P_max, int32_t* idx, int32_t* n_sel,
+                              cudaStream_t st);
 cudaError_t launch_gather(const herald_dims& dm, const int32_t* idx, const int32_t* n_sel,
                           int P_max, const uint16_t* k_cache, const uint16_t* v_cache,
                           uint16_t* pool_k, uint16_t* pool_v, cudaStream_t st);

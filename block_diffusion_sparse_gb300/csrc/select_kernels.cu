@@ -865,22 +865,26 @@ cudaError_t launch_topc(const herald_dims& dm, const float* s1, const uint32_t* 
 
 // ============================================================= topk_union
 // One CTA of 1024 threads per (n, g); thread t holds the stage-2 scores of the
-// candidate slots [t*E, (t+1)*E) in registers (E <= 16, C <= 16384).  Radix
-// select of the K-th largest: a 12-bit first digit over all scores, then the
-// members of that bin (in shared memory) resolve the remaining 19 bits.  Ties
-// go to the lower slot = lower position (candidates are ascending).  Output:
+// candidate slots [t*E, (t+1)*E) in registers (E <= 16, C <= 16384).  The
+// K-th largest score lies in one bin of a 12-bit histogram of the fp32 bit
+// patterns; the members of that bin are ranked exactly (score descending,
+// slot ascending = position ascending, candidates being ascending), the
+// winners marked in a shared bitmap, and one block scan orders the output:
 // [0, sink_end) ++ kept candidates inside [sink_end, local_begin) ++
 // [local_begin, L) -- the deduplicated ascending union.
 constexpr int kTkThreads = 1024;
 constexpr int kTkPer = kMaxC / kTkThreads;  // 16
+constexpr int kTkRankCap = kTkThreads;      // members ranked in one shot
 
 __global__ void __launch_bounds__(kTkThreads)
     topk_union_kernel(const int32_t* __restrict__ ctx, const int32_t* __restrict__ cand,
-                      const int32_t* __restrict__ n_cand, const float* __restrict__ s2, int Hkv,
-                      int L_max, int C, int K, int S, int W, int P_max, int32_t* __restrict__ idx,
-                      int32_t* __restrict__ n_sel) {
-  extern __shared__ uint32_t mem[];  // [C] bin members (low 19 bits)
+                      const int32_t* __restrict__ n_cand, const float* __restrict__ s2,
+                      int n_parts, int Hkv, int L_max, int C, int K, int S, int W, int P_max,
+                      int32_t* __restrict__ idx, int32_t* __restrict__ n_sel) {
+  extern __shared__ uint32_t mem[];           // [C] member (low 19 bits | slot << 32?) values
   __shared__ uint32_t h[kHistBins];
+  __shared__ uint32_t taken[kMaxC / 32];      // bitmap over candidate slots
+  __shared__ uint32_t mslot[kTkRankCap];
   __shared__ uint32_t wt[32], wt2[32];
   __shared__ int s_bin;
   __shared__ uint32_t s_above, s_cnt;
@@ -893,73 +897,107 @@ __global__ void __launch_bounds__(kTkThreads)
   const int i0 = threadIdx.x * E;
   const int32_t* cd = cand + size_t(seg) * C;
   const float* sc = s2 + size_t(seg) * C;
+  const size_t part_stride = size_t(gridDim.x) * C;
   uint32_t v[kTkPer];
 #pragma unroll
-  for (int k = 0; k < kTkPer; ++k)
-    v[k] = (k < E && i0 + k < nc) ? __float_as_uint(fmaxf(sc[i0 + k], 0.f)) : 0u;
+  for (int k = 0; k < kTkPer; ++k) {
+    float x = 0.f;
+    if (k < E && i0 + k < nc)
+      for (int p = 0; p < n_parts; ++p) x += sc[p * part_stride + i0 + k];
+    v[k] = __float_as_uint(fmaxf(x, 0.f));
+  }
   const bool take_all = (Ke == nc);
-  uint32_t tau = 0, need_eq = 0;
+  uint32_t b1 = 0;  // bin of the K-th largest; bins above it are kept whole
   if (!take_all && Ke > 0) {
     for (int i = threadIdx.x; i < kHistBins; i += kTkThreads) h[i] = 0u;
+    for (int i = threadIdx.x; i < kMaxC / 32; i += kTkThreads) taken[i] = 0u;
     if (threadIdx.x == 0) s_cnt = 0;
     __syncthreads();
 #pragma unroll
     for (int k = 0; k < kTkPer; ++k)
       if (k < E && i0 + k < nc) atomicAdd(&h[v[k] >> 19], 1u);
     __syncthreads();
-    uint32_t need = uint32_t(Ke);
-    find_bin_from_top<kTkThreads>(h, kHistBins, need, wt, &s_bin, &s_above);
-    const uint32_t b1 = uint32_t(s_bin);
-    need -= s_above;
+    find_bin_from_top<kTkThreads>(h, kHistBins, uint32_t(Ke), wt, &s_bin, &s_above);
+    b1 = uint32_t(s_bin);
+    const uint32_t need = uint32_t(Ke) - s_above;  // winners to take inside bin b1
 #pragma unroll
     for (int k = 0; k < kTkPer; ++k) {
-      const bool take = k < E && i0 + k < nc && (v[k] >> 19) == b1;
-      const uint32_t slot = warp_append_slot(take, &s_cnt);
-      if (take) mem[slot] = v[k] & 0x7FFFFu;
+      const bool in = k < E && i0 + k < nc && (v[k] >> 19) == b1;
+      const uint32_t slot = warp_append_slot(in, &s_cnt);
+      if (in) {
+        mem[slot] = v[k];
+        if (slot < uint32_t(kTkRankCap)) mslot[slot] = uint32_t(i0 + k);
+      }
     }
-    for (int i = threadIdx.x; i < 2048; i += kTkThreads) h[i] = 0u;
     __syncthreads();
     const uint32_t cnt = s_cnt;
-    for (uint32_t i = threadIdx.x; i < cnt; i += kTkThreads) atomicAdd(&h[mem[i] >> 8], 1u);
+    if (cnt <= uint32_t(kTkRankCap)) {
+      // exact rank of member t among the members: higher score, or equal
+      // score at a lower slot, ranks first
+      if (threadIdx.x < cnt) {
+        const uint32_t my = mem[threadIdx.x], ms = mslot[threadIdx.x];
+        uint32_t rank = 0;
+        for (uint32_t j = 0; j < cnt; ++j) {
+          const uint32_t o = mem[j];
+          rank += (o > my) || (o == my && mslot[j] < ms);
+        }
+        if (rank < need) atomicOr(&taken[ms >> 5], 1u << (ms & 31));
+      }
+    } else {
+      // many members: resolve the remaining 19 bits with two more digits
+      for (int i = threadIdx.x; i < 2048; i += kTkThreads) h[i] = 0u;
+      __syncthreads();
+      for (uint32_t i = threadIdx.x; i < cnt; i += kTkThreads)
+        atomicAdd(&h[(mem[i] >> 8) & 2047u], 1u);
+      __syncthreads();
+      uint32_t nd = need;
+      find_bin_from_top<kTkThreads>(h, 2048, nd, wt, &s_bin, &s_above);
+      const uint32_t b2 = uint32_t(s_bin);
+      nd -= s_above;
+      for (int i = threadIdx.x; i < 256; i += kTkThreads) h[i] = 0u;
+      __syncthreads();
+      for (uint32_t i = threadIdx.x; i < cnt; i += kTkThreads)
+        if (((mem[i] >> 8) & 2047u) == b2) atomicAdd(&h[mem[i] & 255u], 1u);
+      __syncthreads();
+      find_bin_from_top<kTkThreads>(h, 256, nd, wt, &s_bin, &s_above);
+      const uint32_t tau = (b1 << 19) | (b2 << 8) | uint32_t(s_bin);
+      const uint32_t need_eq = nd - s_above;
+      // members above tau, plus the first need_eq ties in slot order
+      uint32_t n_eq = 0;
+#pragma unroll
+      for (int k = 0; k < kTkPer; ++k) n_eq += (k < E && i0 + k < nc && v[k] == tau) ? 1u : 0u;
+      uint32_t eq_before, d0, d1, d2;
+      block_excl_scan2<kTkThreads>(n_eq, 0u, wt, wt2, eq_before, d0, d1, d2);
+#pragma unroll
+      for (int k = 0; k < kTkPer; ++k) {
+        if (!(k < E && i0 + k < nc) || (v[k] >> 19) != b1) continue;
+        bool t = v[k] > tau;
+        if (v[k] == tau) t = eq_before++ < need_eq;
+        if (t) atomicOr(&taken[(i0 + k) >> 5], 1u << ((i0 + k) & 31));
+      }
+    }
     __syncthreads();
-    find_bin_from_top<kTkThreads>(h, 2048, need, wt, &s_bin, &s_above);
-    const uint32_t b2 = uint32_t(s_bin);
-    need -= s_above;
-    for (int i = threadIdx.x; i < 256; i += kTkThreads) h[i] = 0u;
-    __syncthreads();
-    for (uint32_t i = threadIdx.x; i < cnt; i += kTkThreads)
-      if ((mem[i] >> 8) == b2) atomicAdd(&h[mem[i] & 255u], 1u);
-    __syncthreads();
-    find_bin_from_top<kTkThreads>(h, 256, need, wt, &s_bin, &s_above);
-    tau = (b1 << 19) | (b2 << 8) | uint32_t(s_bin);
-    need_eq = need - s_above;
   }
   const int sink_end = min(S, L);
   const int local_begin = max(L - W, sink_end);
-  // which of my slots are kept: above tau, or among the first need_eq ties
-  uint32_t n_eq = 0;
-#pragma unroll
-  for (int k = 0; k < kTkPer; ++k)
-    n_eq += (!take_all && Ke > 0 && k < E && i0 + k < nc && v[k] == tau) ? 1u : 0u;
-  uint32_t eq_before, dummy0, eq_tot, dummy1;
-  block_excl_scan2<kTkThreads>(n_eq, 0u, wt, wt2, eq_before, dummy0, eq_tot, dummy1);
   uint32_t keep_mask = 0, n_keep = 0;
 #pragma unroll
   for (int k = 0; k < kTkPer; ++k) {
-    const bool in = k < E && i0 + k < nc;
-    bool keep = in && Ke > 0;
-    if (keep && !take_all) {
-      if (v[k] == tau) keep = eq_before++ < need_eq;
-      else keep = v[k] > tau;
-    }
+    const int slot = i0 + k;
+    if (!(k < E && slot < nc) || Ke == 0) continue;
+    bool keep = take_all || (v[k] >> 19) > b1 ||
+                ((v[k] >> 19) == b1 && ((taken[slot >> 5] >> (slot & 31)) & 1u));
     if (keep) {
-      const int p = cd[i0 + k];
+      const int p = cd[slot];
       keep = p >= sink_end && p < local_begin;
     }
-    if (keep) { keep_mask |= 1u << k; ++n_keep; }
+    if (keep) {
+      keep_mask |= 1u << k;
+      ++n_keep;
+    }
   }
-  uint32_t at, dummy2, n_mid, dummy3;
-  block_excl_scan2<kTkThreads>(n_keep, 0u, wt, wt2, at, dummy2, n_mid, dummy3);
+  uint32_t at, d3, n_mid, d4;
+  block_excl_scan2<kTkThreads>(n_keep, 0u, wt, wt2, at, d3, n_mid, d4);
   int32_t* out = idx + size_t(seg) * P_max;
 #pragma unroll
   for (int k = 0; k < kTkPer; ++k)
@@ -977,8 +1015,9 @@ __global__ void __launch_bounds__(kTkThreads)
 }
 
 cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const int32_t* cand,
-                              const int32_t* n_cand, const float* s2, int C, int K, int S, int W,
-                              int P_max, int32_t* idx, int32_t* n_sel, cudaStream_t st) {
+                              const int32_t* n_cand, const float* s2, int n_parts, int C, int K,
+                              int S, int W, int P_max, int32_t* idx, int32_t* n_sel,
+                              cudaStream_t st) {
   const size_t smem = size_t(C) * 4;
   static bool attr_done = false;
   if (!attr_done) {
@@ -987,7 +1026,7 @@ cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const i
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  HERALD_CHECK_LAUNCH(launch_k("topk_union_kernel", topk_union_kernel, dm.N * dm.Hkv, kTkThreads, smem, st, ctx, cand, n_cand, s2, dm.Hkv,
+  HERALD_CHECK_LAUNCH(launch_k("topk_union_kernel", topk_union_kernel, dm.N * dm.Hkv, kTkThreads, smem, st, ctx, cand, n_cand, s2, n_parts, dm.Hkv,
                                                               dm.L_max, C, K, S, W, P_max, idx,
                                                               n_sel));
   return cudaGetLastError();

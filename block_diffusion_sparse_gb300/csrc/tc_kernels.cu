@@ -63,6 +63,59 @@ __device__ __forceinline__ void tmem_teardown(uint32_t base, uint32_t ncols) {
   }
 }
 
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Full cluster barrier (hardware): release this CTA's shared-memory writes,
+// acquire the peers'.
+__device__ __forceinline__ void cluster_sync_all() {
+  __cluster_barrier_arrive();
+  __cluster_barrier_wait();
+}
+// shared::cluster address of the same shared-memory location in CTA `rank`.
+__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float2 ld_peer_f2(uint32_t a) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float4 ld_peer_f4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a));
+  return v;
+}
+
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_cluster(const char* name, void (*kernel)(KArgs...), dim3 grid,
+                                  int cluster_x, size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster_x;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  trace_before(st, name);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+  trace_after(st);
+  return e;
+}
+
 // ========================================================== refine_pass1
 template <int D>
 struct Ref1Cfg {
@@ -293,12 +346,228 @@ __global__ void __launch_bounds__(kTcThreads)
   tmem_teardown(tbase, 256);
 }
 
+// ========================================================== refine_fused
+// Stage 2 in one kernel for C <= 4096: one 8-CTA cluster per (sequence, KV
+// head, 128-row tile); CTA r scores candidate slots [r*cpc, (r+1)*cpc)
+// (cpc <= 512, so the scores fill TMEM and are never recomputed).  Row
+// (max, sumexp) over each CTA's candidates are merged across the cluster
+// through distributed shared memory into the row log-sum-exp; each CTA then
+// sums exp(S - lse_r) over its 128 rows (warp transpose-reductions, rows
+// past B*G excluded) and writes one partial s2 per row tile, which the top-K
+// kernel adds up.
+constexpr int kFuseCtas = 8;
+constexpr int kFuseMaxCpc = 512;
+
+// candidates per CTA: a multiple of 64 so that each warp's column half is
+// whole 32-column chunks
+__host__ __device__ inline int fuse_cpc(int C) {
+  return ((C + kFuseCtas - 1) / kFuseCtas + 63) / 64 * 64;
+}
+
+template <int D>
+struct FuseCfg {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kQBytes = kHalves * kTileM * 128;
+  static constexpr int kKBytes = kHalves * kFuseMaxCpc * 128;
+  static constexpr int kSmem = kQBytes + kKBytes + 1024;
+  static_assert(kSmem <= 200 * 1024, "fused refine smem");
+};
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    refine_fused_kernel(const uint16_t* __restrict__ q_block, const uint16_t* __restrict__ kc,
+                        const int32_t* __restrict__ cand, const int32_t* __restrict__ n_cand,
+                        int B, int Hq, int Hkv, int L_max, int C, int R, int cpc, float scale,
+                        float* __restrict__ s2p, uint32_t* err) {
+  using Cfg = FuseCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar0;
+  __shared__ uint32_t tmem_base;
+  __shared__ int32_t pos[kFuseMaxCpc];
+  __shared__ float2 half_stat[2][kTileM];
+  __shared__ __align__(16) float2 row_stat[kTileM];
+  __shared__ float colsum[2][4][kFuseMaxCpc / 2];
+  uint8_t* Qs = align1024(smem_raw);
+  uint8_t* Ks = Qs + Cfg::kQBytes;
+  const uint32_t rank = cluster_ctarank();
+  const int mt = blockIdx.y, seg = blockIdx.z;
+  const int n = seg / Hkv, g = seg - n * Hkv, G = Hq / Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar0, 1);
+    fence_mbar_init();
+  }
+  tmem_setup(&tmem_base, 512);
+  const uint32_t tbase = tmem_base;
+  griddep_enter();
+  const int nc = min(max(n_cand[seg], 0), C);
+  const int c0 = int(rank) * cpc;
+  const int ncv = min(max(nc - c0, 0), cpc);  // valid candidates of this CTA
+  const int32_t* cd = cand + size_t(seg) * C;
+  for (int r = threadIdx.x; r < cpc; r += kTcThreads) {
+    const int p = r < ncv ? cd[c0 + r] : -1;
+    pos[r] = (p >= 0 && p < L_max) ? p : -1;
+  }
+  __syncthreads();
+  if (ncv > 0) {
+    load_rows_sw128<D>(Qs, kTileM, kTileM, q_block, [&](int r) -> const uint16_t* {
+      const int row = mt * kTileM + r;
+      if (row >= R) return nullptr;
+      const int b = row / G, hl = row - (row / G) * G;
+      return q_block + ((size_t(n) * B + b) * Hq + g * G + hl) * D;
+    });
+    load_rows_sw128<D>(Ks, cpc, cpc, kc, [&](int r) -> const uint16_t* {
+      const int p = pos[r];
+      return p < 0 ? nullptr : kc + (size_t(seg) * L_max + p) * D;
+    });
+    cp_async_commit();
+    cp_async_wait_all();
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+  tc_fence_after();
+  // S = Q K_cand^T: up to two UMMAs of N = 256 -> TMEM columns [0, cpc)
+  if (threadIdx.x == 0 && ncv > 0) {
+    const uint32_t qa = smem_u32(Qs), ka = smem_u32(Ks);
+    for (int h0 = 0; h0 < cpc; h0 += 256) {
+      const int nn = min(256, cpc - h0);
+      const uint32_t idesc = make_idesc_bf16(kTileM, nn, false, false);
+#pragma unroll
+      for (int s = 0; s < D / 16; ++s) {
+        const uint32_t hv = s >> 2, koff = (s & 3) * 32;
+        const uint64_t a = make_sdesc_sw128(qa + hv * (kTileM * 128) + koff, 16, 1024);
+        const uint64_t b =
+            make_sdesc_sw128(ka + hv * uint32_t(cpc * 128) + uint32_t(h0 * 128) + koff, 16, 1024);
+        umma_bf16(tbase + uint32_t(h0), a, b, idesc, s > 0 ? 1u : 0u);
+      }
+    }
+    umma_commit(&bar0);
+  }
+  if (ncv > 0 && !mbar_wait(&bar0, 0)) record_error(err, DEV_TIMEOUT_MMA);
+  tc_fence_after();
+  __syncwarp();
+
+  // row (max, sumexp) over this CTA's candidates, log2 units; the two warps of
+  // a lane quadrant take the two column halves
+  const int quad = warp & 3, ch = warp >> 2;
+  const int row = quad * 32 + lane;
+  const uint32_t trow = tbase + (uint32_t(quad * 32) << 16);
+  const float sl2 = scale * 1.4426950408889634f;
+  const int hc0 = ch * (cpc / 2), hc1 = hc0 + cpc / 2;  // this warp's columns
+  float m = -INFINITY;
+  for (int c = hc0; c < hc1; c += 32) {
+    float v[32];
+    tmem_ld32(trow + uint32_t(c), v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (c + i < ncv) m = fmaxf(m, v[i] * sl2);
+  }
+  float l = 0.f;
+  if (m != -INFINITY)
+    for (int c = hc0; c < hc1; c += 32) {
+      float v[32];
+      tmem_ld32(trow + uint32_t(c), v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (c + i < ncv) l += fast_exp2(v[i] * sl2 - m);
+    }
+  half_stat[ch][row] = make_float2(m, l);
+  __syncthreads();
+  if (ch == 0) {
+    const float2 a = half_stat[0][row], b = half_stat[1][row];
+    const float M = fmaxf(a.x, b.x);
+    const float Lr = (a.x == -INFINITY ? 0.f : a.y * fast_exp2(a.x - M)) +
+                     (b.x == -INFINITY ? 0.f : b.y * fast_exp2(b.x - M));
+    row_stat[row] = make_float2(M, Lr);
+  }
+  cluster_sync_all();
+  // row log-sum-exp over all candidates: every peer's statistics of my row
+  float lse = 0.f;
+  {
+    float2 st[kFuseCtas];
+#pragma unroll
+    for (int c = 0; c < kFuseCtas; ++c) st[c] = ld_peer_f2(peer_addr(&row_stat[row], uint32_t(c)));
+    float M = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kFuseCtas; ++c) M = fmaxf(M, st[c].x);
+    float Lr = 0.f;
+#pragma unroll
+    for (int c = 0; c < kFuseCtas; ++c)
+      if (st[c].x != -INFINITY) Lr += st[c].y * fast_exp2(st[c].x - M);
+    lse = M + __log2f(Lr);
+  }
+  const bool row_ok = mt * kTileM + row < R;
+  // column sums over the 128 rows: per 32-column chunk, a warp
+  // transpose-reduces its 32 rows; after the butterfly, lane j holds the sum
+  // of chunk column j over the warp's rows
+  for (int c = hc0; c < hc1; c += 32) {
+    float v[32];
+    tmem_ld32(trow + uint32_t(c), v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      v[i] = (row_ok && c + i < ncv) ? fast_exp2(v[i] * sl2 - lse) : 0.f;
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) {
+      // the lane with bit w set keeps the upper w columns, its partner the lower
+      const bool up = (lane & w) != 0;
+#pragma unroll
+      for (int i = 0; i < w; ++i) {
+        const float send = up ? v[i] : v[i + w];
+        const float keep = up ? v[i + w] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+      }
+    }
+    colsum[ch][quad][c - hc0 + lane] = v[0];
+  }
+  __syncthreads();
+  float* out = s2p + (size_t(mt) * gridDim.z + seg) * C;
+  const int hw = cpc / 2;
+  for (int j = threadIdx.x; j < cpc; j += kTcThreads) {
+    if (c0 + j >= nc) continue;
+    const int chh = j / hw, jj = j - chh * hw;
+    out[c0 + j] = colsum[chh][0][jj] + colsum[chh][1][jj] + colsum[chh][2][jj] +
+                  colsum[chh][3][jj];
+  }
+  cluster_sync_all();  // peers may still read this CTA's row statistics
+  tmem_teardown(tbase, 512);
+}
+
+bool refine_fused_ok(int C) { return fuse_cpc(C) <= kFuseMaxCpc; }
+
 cudaError_t launch_refine(const herald_dims& dm, const uint16_t* q_block, const uint16_t* k_cache,
                           const int32_t* cand, const int32_t* n_cand, int C, float2* rpart,
                           float* s2, const WsLayout& w, uint32_t* err, cudaStream_t st) {
   const float scale = 1.0f / sqrtf(float(dm.d));
   const int segs = dm.N * dm.Hkv;
   cudaError_t e;
+  if (refine_fused_ok(C)) {
+    // s2 holds one partial per 128-row tile: [MT][N*Hkv][C]
+    const int cpc = fuse_cpc(C);
+    if (dm.d == 128) {
+      static bool attr = false;
+      if (!attr) {
+        e = cudaFuncSetAttribute(refine_fused_kernel<128>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, FuseCfg<128>::kSmem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+      }
+      return launch_cluster("refine_fused_kernel", refine_fused_kernel<128>,
+                            dim3(kFuseCtas, w.MT, segs), kFuseCtas, FuseCfg<128>::kSmem, st,
+                            q_block, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv, dm.L_max, C, w.R,
+                            cpc, scale, s2, err);
+    }
+    static bool attr64 = false;
+    if (!attr64) {
+      e = cudaFuncSetAttribute(refine_fused_kernel<64>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, FuseCfg<64>::kSmem);
+      if (e != cudaSuccess) return e;
+      attr64 = true;
+    }
+    return launch_cluster("refine_fused_kernel", refine_fused_kernel<64>,
+                          dim3(kFuseCtas, w.MT, segs), kFuseCtas, FuseCfg<64>::kSmem, st, q_block,
+                          k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv, dm.L_max, C, w.R, cpc, scale,
+                          s2, err);
+  }
   if (dm.d == 128) {
     static bool attr = false;
     if (!attr) {
@@ -534,36 +803,6 @@ struct AttnClCfg {
   static_assert(kV1 + kTile == kBytes, "cluster attention smem layout");
   static_assert(kSmem <= 227 * 1024, "cluster attention smem exceeds the per-CTA limit");
 };
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Full cluster barrier (hardware): release this CTA's shared-memory writes,
-// acquire the peers'.
-__device__ __forceinline__ void cluster_sync_all() {
-  __cluster_barrier_arrive();
-  __cluster_barrier_wait();
-}
-// shared::cluster address of the same shared-memory location in CTA `rank`.
-__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ float2 ld_peer_f2(uint32_t a) {
-  float2 v;
-  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
-  return v;
-}
-__device__ __forceinline__ float4 ld_peer_f4(uint32_t a) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(a));
-  return v;
-}
 
 template <int D, int CS>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -1186,28 +1425,6 @@ static bool force_split() {
   return v == 1;
 }
 
-template <typename... KArgs, typename... Args>
-static cudaError_t launch_cluster(const char* name, void (*kernel)(KArgs...), dim3 grid,
-                                  int cluster_x, size_t smem, cudaStream_t st, Args... args) {
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cluster_x;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  trace_before(st, name);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
-  trace_after(st);
-  return e;
-}
 
 // How many clusters of CS CTAs of the attention kernel can be resident at
 // once on this device (a 16-CTA cluster needs 16 free SMs of one GPC).

@@ -131,8 +131,9 @@ herald_status herald_select(herald_dims dims, const uint16_t *q_merge, const uin
  *   Scratch lives in one static 4 MiB device array inside the library; every
  *   GPU that loads the library holds it until the process exits.  Shapes
  *   whose scratch -- 256 bytes + N*Hkv*ceil(B*G/128)*128*ceil(C/256)*8 bytes
- *   of row statistics + N*Hkv*C*4 bytes of scores -- exceed 4 MiB are
- *   rejected with HERALD_ERR_WORKSPACE_TOO_SMALL and a message.
+ *   of row statistics + N*Hkv*C*4 bytes of scores per 128-row tile of the
+ *   B*G query rows (one tile when C > 4096) -- exceed 4 MiB are rejected
+ *   with HERALD_ERR_WORKSPACE_TOO_SMALL and a message.
  *   The first call on a device resolves the array's device address (with
  *   that device current); make that first call before any stream capture.
  *   All calls share the array: calls that can overlap on the GPU (other

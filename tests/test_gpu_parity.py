@@ -42,6 +42,9 @@ CASES = [
           n_planted=6, index=15),
     _case("ctx-below-c", Hq=4, Hkv=1, d=128, L=100, B=8, C=256, K=64, S=16, W=16,
           n_planted=2, index=16),
+    # C > 4096: the two-pass stage-2 refine
+    _case("c-above-4096-two-pass", Hq=8, Hkv=2, d=128, L=9000, B=16, C=5000, K=256, S=16,
+          W=64, n_planted=10, index=23),
     # a pool of more than 16 key tiles: the split-KV attention kernel + combine
     _case("large-pool-split", Hq=8, Hkv=2, d=128, L=6000, B=32, C=3000, K=2200, S=16, W=64,
           n_planted=30, index=22),
