@@ -872,10 +872,9 @@ cudaError_t launch_topc(const herald_dims& dm, const float* s1, const uint32_t* 
 // winners marked in a shared bitmap, and one block scan orders the output:
 // [0, sink_end) ++ kept candidates inside [sink_end, local_begin) ++
 // [local_begin, L) -- the deduplicated ascending union.
-constexpr int kTkThreads = 1024;
-constexpr int kTkPer = kMaxC / kTkThreads;  // 16
-constexpr int kTkRankCap = kTkThreads;      // members ranked in one shot
+constexpr int kTkPer = 16;  // scores per thread (C <= 16 * threads)
 
+template <int kTkThreads>
 __global__ void __launch_bounds__(kTkThreads)
     topk_union_kernel(const int32_t* __restrict__ ctx, const int32_t* __restrict__ cand,
                       const int32_t* __restrict__ n_cand, const float* __restrict__ s2,
@@ -884,6 +883,7 @@ __global__ void __launch_bounds__(kTkThreads)
   extern __shared__ uint32_t mem[];           // [C] member (low 19 bits | slot << 32?) values
   __shared__ uint32_t h[kHistBins];
   __shared__ uint32_t taken[kMaxC / 32];      // bitmap over candidate slots
+  constexpr int kTkRankCap = kTkThreads;  // members ranked in one shot
   __shared__ uint32_t mslot[kTkRankCap];
   __shared__ uint32_t wt[32], wt2[32];
   __shared__ int s_bin;
@@ -920,13 +920,27 @@ __global__ void __launch_bounds__(kTkThreads)
     find_bin_from_top<kTkThreads>(h, kHistBins, uint32_t(Ke), wt, &s_bin, &s_above);
     b1 = uint32_t(s_bin);
     const uint32_t need = uint32_t(Ke) - s_above;  // winners to take inside bin b1
+    // one warp-aggregated allocation for all of a thread's members
+    uint32_t my_members = 0;
+#pragma unroll
+    for (int k = 0; k < kTkPer; ++k)
+      my_members += (k < E && i0 + k < nc && (v[k] >> 19) == b1) ? 1u : 0u;
+    uint32_t incl = my_members;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if ((threadIdx.x & 31) >= o) incl += y;
+    }
+    uint32_t wbase = 0;
+    if ((threadIdx.x & 31) == 31 && incl) wbase = atomicAdd(&s_cnt, incl);
+    wbase = __shfl_sync(0xffffffffu, wbase, 31);
+    uint32_t slot = wbase + incl - my_members;
 #pragma unroll
     for (int k = 0; k < kTkPer; ++k) {
-      const bool in = k < E && i0 + k < nc && (v[k] >> 19) == b1;
-      const uint32_t slot = warp_append_slot(in, &s_cnt);
-      if (in) {
+      if (k < E && i0 + k < nc && (v[k] >> 19) == b1) {
         mem[slot] = v[k];
         if (slot < uint32_t(kTkRankCap)) mslot[slot] = uint32_t(i0 + k);
+        ++slot;
       }
     }
     __syncthreads();
@@ -1021,14 +1035,23 @@ cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const i
   const size_t smem = size_t(C) * 4;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(topk_union_kernel,
+    cudaError_t e = cudaFuncSetAttribute(topk_union_kernel<1024>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxC * 4);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk_union_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kMaxC * 4);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  HERALD_CHECK_LAUNCH(launch_k("topk_union_kernel", topk_union_kernel, dm.N * dm.Hkv, kTkThreads, smem, st, ctx, cand, n_cand, s2, n_parts, dm.Hkv,
-                                                              dm.L_max, C, K, S, W, P_max, idx,
-                                                              n_sel));
+  // the fewest threads that hold C scores at kTkPer per thread
+  if (C <= 256 * kTkPer)
+    HERALD_CHECK_LAUNCH(launch_k("topk_union_kernel", topk_union_kernel<256>, dm.N * dm.Hkv, 256,
+                                 smem, st, ctx, cand, n_cand, s2, n_parts, dm.Hkv, dm.L_max, C, K,
+                                 S, W, P_max, idx, n_sel));
+  else
+    HERALD_CHECK_LAUNCH(launch_k("topk_union_kernel", topk_union_kernel<1024>, dm.N * dm.Hkv,
+                                 1024, smem, st, ctx, cand, n_cand, s2, n_parts, dm.Hkv, dm.L_max,
+                                 C, K, S, W, P_max, idx, n_sel));
   return cudaGetLastError();
 }
 
