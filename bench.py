@@ -129,14 +129,15 @@ def job_value(ms_per_step: float, world: int, tokens_per_step: int) -> float:
 
 # --------------------------------------------------------------------------- workload
 WORKLOADS = {"qwen": "QWEN_32K", "tiny": "TINY", "llama": "LLAMA_64K",
-             "long-host": "LONG_128K_HOST"}
+             "long-host": "LONG_128K_HOST", "stack": "QWEN_STACK"}
 _WORKLOAD = "qwen"
 
 
 def workload():
     """The benchmarked layer: the 32K Qwen2.5-7B-like layer unless --workload
     names another (tiny, llama = 4 x 64K Llama-8B-like, long-host = 128K
-    context with the cache in pinned host memory)."""
+    context with the cache in pinned host memory, stack = the 28-layer
+    Qwen2.5-7B-like stack at 8 x 32K)."""
     from block_diffusion_sparse_gb300 import workloads as W
     return getattr(W, WORKLOADS[_WORKLOAD])
 
@@ -211,6 +212,15 @@ class Bench:
     def ws(self):
         return self.pipe.ws_den
 
+    n_sel_out = property(lambda self: self.pipe.n_sel)
+    trace_capacity = 64
+
+    def l2_note(self) -> str:
+        if self.w.kv_on_host:
+            return "K/V cache in pinned host memory (read over the host link)"
+        return (f"cold: K/V cache rotated over {self.n_rot} copies "
+                f"({self.n_rot * 2 * self.x['k_cache'].nbytes / 2**20:.0f} MiB > L2)")
+
     def step(self, r: int, q_merge=None, q_steps=None, bk=None, bv=None):
         """One block through the dual-stream pipeline (cache copy r; stage 1
         of the next block scans copy r+1)."""
@@ -234,7 +244,7 @@ class Bench:
         for r in range(self.n_rot):
             g = torch.cuda.CUDAGraph()
             if traced:
-                tr = self.H.Trace(capacity=64, external=True)
+                tr = self.H.Trace(capacity=self.trace_capacity, external=True)
                 with torch.cuda.graph(g):
                     with tr:
                         self.step(r)
@@ -245,6 +255,70 @@ class Bench:
             graphs.append(g)
         torch.cuda.synchronize()
         return graphs, traces
+
+
+class StackBench(Bench):
+    """The 28-layer stack (attention and selection only): one step is one
+    block through every layer with the stack pipeline (stage 2 + gather +
+    step-0 attention layer by layer, stage 1 of the next block per layer on
+    the selection stream, steps 1..T-1 over all layers, appends).
+
+    One synthetic layer is generated on the host; layer l's K/V cache,
+    queries and block K/V are that layer with its sequences rotated by l
+    positions, each layer in its own device buffers.  A step streams every
+    layer's cache, far more than L2, so the inputs are cold at each use
+    without rotating copies."""
+
+    def __init__(self, w, rank: int):
+        import torch
+        from block_diffusion_sparse_gb300 import herald as H
+        from block_diffusion_sparse_gb300 import synth
+        from block_diffusion_sparse_gb300.pipeline import StackPipeline
+        self.torch, self.H, self.w = torch, H, w
+        self.x = synth.make_layer(w)
+        x = self.x
+        nl = w.layers
+        host = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16))
+
+        def per_layer(a, axis):
+            t = host(a).cuda()
+            out = torch.empty((nl, *t.shape), dtype=torch.int16, device="cuda")
+            for l in range(nl):
+                out[l].copy_(torch.roll(t, l, dims=axis))
+            return out
+
+        self.d = H.dims_of(w)
+        self.P = w.P
+        self.k = per_layer(x["k_cache"], 0)                 # [nl, N, Hkv, L_max, d]
+        self.v = per_layer(x["v_cache"], 0)
+        self.q_merge = per_layer(x["q_merge"], 0)           # [nl, N, B, Hq, d]
+        self.q_steps = per_layer(x["q_steps"], 1)           # [nl, T, N, B, Hq, d]
+        self.bk = per_layer(x["block_k"], 1)                # [nl, T, N, B, Hkv, d]
+        self.bv = per_layer(x["block_v"], 1)
+        self.ctx = torch.from_numpy(x["ctx"]).cuda()
+        self.n_rot = 2                                      # candidate-buffer parity
+        self.pipe = StackPipeline(self.d, nl, w.C, w.K, w.S, w.W, self.P, w.T)
+        self.out = torch.zeros((nl, w.T, w.N, w.B, w.Hq, w.d), dtype=torch.int16,
+                               device="cuda")
+        self.overlap = True
+        self.trace_capacity = 24 * nl
+        self.pipe.prime(self.q_merge, self.k, self.ctx, slot=0)
+        torch.cuda.synchronize()
+
+    idx = property(lambda self: self.pipe.idx_all)
+    n_sel = property(lambda self: self.pipe.n_sel[-1])   # last layer's, for the roofline
+    n_sel_out = property(lambda self: self.pipe.n_sel_all)
+
+    def l2_note(self) -> str:
+        return (f"cold: every step streams all {self.w.layers} layers' K caches "
+                f"({self.w.layers * self.x['k_cache'].nbytes / 2**30:.1f} GiB > L2)")
+
+    def step(self, r: int, q_merge=None, q_steps=None, bk=None, bv=None):
+        qs = self.q_steps if q_steps is None else q_steps
+        bk = self.bk if bk is None else bk
+        bv = self.bv if bv is None else bv
+        self.pipe.block(r, qs, bk, bv, self.k, self.v, self.ctx, self.out, advance=False,
+                        overlap=self.overlap)
 
 
 def algorithmic_work(w, n_sel: np.ndarray) -> dict:
@@ -314,11 +388,14 @@ def cpu_baseline(w, budget_s: float = 12.0) -> dict:
     t0 = time.perf_counter()
     for _ in range(n):
         oracle_block(w, xf)
-    dt = (time.perf_counter() - t0) / n
+    dt = (time.perf_counter() - t0) / n * w.layers
+    what = (f"{n} blocks of one layer (select + gather + T={w.T} attention steps), "
+            f"x{w.layers} layers" if w.layers > 1 else
+            f"{n} full blocks of the same workload (select + gather + T={w.T} "
+            f"attention steps)")
     return {"value": w.N * w.B / dt, "unit": "tokens/s", "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": f"{n} full blocks of the same workload (select + gather + T={w.T} "
-                      f"attention steps), fp64 C + OpenMP, inputs resident in host RAM",
+            "sample": what + ", fp64 C + OpenMP, inputs resident in host RAM",
             "s_per_block": dt}
 
 
@@ -334,7 +411,7 @@ def run_reference(args, rank, world):
     t0 = time.perf_counter()
     for _ in range(args.steps):
         oracle_block(w, xf)
-    dt = (time.perf_counter() - t0) / args.steps
+    dt = (time.perf_counter() - t0) / args.steps * w.layers   # one layer timed per step
     v = w.N * w.B / dt
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -346,7 +423,8 @@ def run_reference(args, rank, world):
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": oracle.num_threads(),
                              "kind": "oracle",
                              "sample": "each step = one full block (select + gather + T "
-                                       "attention steps) of the workload"},
+                                       "attention steps) of one layer of the workload"
+                                       + (f", x{w.layers} layers" if w.layers > 1 else "")},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -357,7 +435,7 @@ def run_ours(args, rank, world, dist):
     w = workload()
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
     dev_idx = torch.cuda.current_device()
-    b = Bench(w, rank)
+    b = StackBench(w, rank) if w.layers > 1 else Bench(w, rank)
     graphs, _ = b.capture(traced=False)
     nrot = b.n_rot
     clocks = ClockSampler(dev_idx)
@@ -464,10 +542,7 @@ def run_ours(args, rank, world, dist):
             "config": {"workload": w.name, "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
                        "ctx": w.L, "B": w.B, "T": w.T, "C": w.C, "K": w.K, "sink": w.S,
                        "local": w.W, "parallelism": f"replicas x{world}",
-                       "l2": ("K/V cache in pinned host memory (read over the host link)"
-                              if w.kv_on_host else
-                              f"cold: K/V cache rotated over {nrot} copies "
-                              f"({nrot * 2 * b.x['k_cache'].nbytes / 2**20:.0f} MiB > L2)"),
+                       "layers": w.layers, "l2": b.l2_note(),
                        "timing": "CUDA-graph replay of whole steps, CUDA events"},
             "roofline": roofline,
             "serial": {"ms_per_step": serial_ms, "value": job_value(serial_ms, world, w.N * w.B),
@@ -497,7 +572,7 @@ def run_e2e(b, args, dist):
     hbk, hbv = b.bk.cpu().pin_memory(), b.bv.cpu().pin_memory()
     o_out = torch.empty(b.out.shape, dtype=b.out.dtype).pin_memory()
     o_idx = torch.empty(b.idx.shape, dtype=b.idx.dtype).pin_memory()
-    o_ns = torch.empty(b.n_sel.shape, dtype=b.n_sel.dtype).pin_memory()
+    o_ns = torch.empty(b.n_sel_out.shape, dtype=b.n_sel_out.dtype).pin_memory()
     dq_m, dq_s = torch.empty_like(b.q_merge), torch.empty_like(b.q_steps)
     dbk, dbv = torch.empty_like(b.bk), torch.empty_like(b.bv)
     h2d = sum(t.numel() * t.element_size() for t in (hq_m, hq_s, hbk, hbv))
@@ -511,7 +586,7 @@ def run_e2e(b, args, dist):
         b.step(i % b.n_rot, q_merge=dq_m, q_steps=dq_s, bk=dbk, bv=dbv)
         o_out.copy_(b.out, non_blocking=True)
         o_idx.copy_(b.idx, non_blocking=True)
-        o_ns.copy_(b.n_sel, non_blocking=True)
+        o_ns.copy_(b.n_sel_out, non_blocking=True)
 
     for i in range(args.warmup):
         one(i)

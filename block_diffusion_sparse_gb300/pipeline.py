@@ -114,8 +114,14 @@ class StackPipeline:
         mk = lambda shape, dt, fill=0: torch.full(shape, fill, dtype=dt, device=dev)
         self.cand = [[mk((*NG, C), torch.int32, -1) for _ in range(2)] for _ in range(n_layers)]
         self.n_cand = [[mk(NG, torch.int32) for _ in range(2)] for _ in range(n_layers)]
-        self.idx = [mk((*NG, P), torch.int32, -1) for _ in range(n_layers)]
-        self.n_sel = [mk(NG, torch.int32) for _ in range(n_layers)]
+        # one tensor per output kind over all layers; every layer's slice
+        # starts on a 16-byte boundary (the library's alignment rule)
+        ng = dims.N * dims.Hkv
+        rup = lambda x: (x + 3) // 4 * 4
+        self.idx_all = mk((n_layers, rup(ng * P)), torch.int32, -1)
+        self.n_sel_all = mk((n_layers, rup(ng)), torch.int32)
+        self.idx = [self.idx_all[l, : ng * P].view(*NG, P) for l in range(n_layers)]
+        self.n_sel = [self.n_sel_all[l, :ng].view(NG) for l in range(n_layers)]
         self.pool_k = [[mk((*NG, P, dims.d), torch.int16) for _ in range(2)]
                        for _ in range(n_layers)]
         self.pool_v = [[mk((*NG, P, dims.d), torch.int16) for _ in range(2)]

@@ -68,3 +68,61 @@ def test_three_blocks_match_oracle_schedule(overlap):
         cand, nc = oracle.topc(oracle.stage1_scores(qbar, kc, cx)[2], cx, w.C)
         cx, kc, vc = oracle.append(cx, f64(xb["block_k"][w.T - 1]), f64(xb["block_v"][w.T - 1]),
                                    kc, vc)
+
+
+def test_two_layer_stack_matches_oracle_schedule():
+    """The stack pipeline runs the per-layer schedule above on every layer,
+    with one shared context length that advances once per block."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_diffusion_sparse_gb300.pipeline import StackPipeline
+    nb, nl = 2, 2
+    w = Workload("stack", N=2, Hq=8, Hkv=2, d=128, L=2500, B=16, T=2, C=256, K=96, S=16, W=48,
+                 planted="points", n_planted=10, index=37, extra_rows=nb * 16, layers=nl)
+    x0 = [synth.make_layer(w, layer=l) for l in range(nl)]
+    blocks = [[synth.make_layer(w.scaled(L=64, extra_rows=0, n_planted=0), layer=10 + 2 * i + l)
+               for l in range(nl)] for i in range(nb)]
+    d = H.dims_of(w)
+    k = [dev(x["k_cache"]) for x in x0]
+    v = [dev(x["v_cache"]) for x in x0]
+    ctx = dev(x0[0]["ctx"])
+    pipe = StackPipeline(d, nl, w.C, w.K, w.S, w.W, w.P, w.T)
+    pipe.prime([dev(x["q_merge"]) for x in x0], k, ctx)
+    got = []
+    for i in range(nb):
+        out = [torch.zeros((w.T, w.N, w.B, w.Hq, w.d), dtype=torch.int16, device="cuda")
+               for _ in range(nl)]
+        pipe.block(i, [dev(b["q_steps"]) for b in blocks[i]],
+                   [dev(b["block_k"]) for b in blocks[i]], [dev(b["block_v"]) for b in blocks[i]],
+                   k, v, ctx, out, advance=True)
+        torch.cuda.synchronize()
+        got.append([(pipe.idx[l].cpu().numpy().copy(), pipe.n_sel[l].cpu().numpy().copy(),
+                     bf16_dev_to_f64(out[l])) for l in range(nl)])
+    assert H.herald_workspace_error(pipe.ws_den) == 0
+    assert H.herald_workspace_error(pipe.ws_sel) == 0
+    assert ctx.cpu().numpy().tolist() == [w.L + nb * w.B] * w.N
+
+    for l in range(nl):
+        kc, vc = f64(x0[l]["k_cache"]), f64(x0[l]["v_cache"])
+        cx = x0[l]["ctx"].copy()
+        qbar = oracle.merged_query(f64(x0[l]["q_merge"]))
+        cand, nc = oracle.topc(oracle.stage1_scores(qbar, kc, cx)[2], cx, w.C)
+        for i in range(nb):
+            xb = blocks[i][l]
+            q0 = f64(xb["q_steps"][0])
+            s2 = oracle.stage2_scores(q0, kc, cand, nc)
+            idx_o, ns_o = oracle.select_final(cx, w.L_max, cand, nc, s2, w.K, w.S, w.W, w.P)
+            gi, gn, gout = got[i][l]
+            for n in range(w.N):
+                for g in range(w.Hkv):
+                    a = set(gi[n, g, : gn[n, g]].tolist())
+                    b = set(idx_o[n, g, : ns_o[n, g]].tolist())
+                    assert len(a ^ b) <= 2, f"layer {l} block {i} n={n} g={g}"
+            for t in range(w.T):
+                ref = oracle.sparse_attn(f64(xb["q_steps"][t]), kc, vc, gi, gn,
+                                         f64(xb["block_k"][t]), f64(xb["block_v"][t]))
+                assert np.abs(gout[t] - ref).max() <= ATTN_ATOL
+            qbar = oracle.merged_query(q0)
+            cand, nc = oracle.topc(oracle.stage1_scores(qbar, kc, cx)[2], cx, w.C)
+            cx, kc, vc = oracle.append(cx, f64(xb["block_k"][w.T - 1]),
+                                       f64(xb["block_v"][w.T - 1]), kc, vc)
