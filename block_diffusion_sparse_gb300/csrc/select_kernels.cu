@@ -865,26 +865,28 @@ cudaError_t launch_topc(const herald_dims& dm, const float* s1, const uint32_t* 
 
 // ============================================================= topk_union
 // One CTA of 1024 threads per (n, g); thread t holds the stage-2 scores of the
-// candidate slots [t*E, (t+1)*E) in registers (E <= 16, C <= 16384).  The
-// K-th largest score lies in one bin of a 12-bit histogram of the fp32 bit
-// patterns; the members of that bin are ranked exactly (score descending,
-// slot ascending = position ascending, candidates being ascending), the
-// winners marked in a shared bitmap, and one block scan orders the output:
-// [0, sink_end) ++ kept candidates inside [sink_end, local_begin) ++
-// [local_begin, L) -- the deduplicated ascending union.
-constexpr int kTkPer = 16;  // scores per thread (C <= 16 * threads)
+// candidate slots [t*E, (t+1)*E) in registers (E <= kPer; 4 when C <= 4096,
+// 16 up to C = 16384), summed over the refine's row-tile partials with all
+// loads of a partial in flight at once.  The K-th largest score lies in one
+// bin of a 12-bit histogram of the fp32 bit patterns; the members of that bin
+// are ranked exactly (score descending, slot ascending = position ascending,
+// candidates being ascending), the winners marked in a shared bitmap, and one
+// block scan orders the output: [0, sink_end) ++ kept candidates inside
+// [sink_end, local_begin) ++ [local_begin, L) -- the deduplicated ascending
+// union.
+constexpr int kTkThreads = 1024;
+constexpr int kTkRankCap = 1024;  // members ranked in one shot
 
-template <int kTkThreads>
+template <int kPer>
 __global__ void __launch_bounds__(kTkThreads)
     topk_union_kernel(const int32_t* __restrict__ ctx, const int32_t* __restrict__ cand,
                       const int32_t* __restrict__ n_cand, const float* __restrict__ s2,
                       int n_parts, int Hkv, int L_max, int C, int K, int S, int W, int P_max,
                       int32_t* __restrict__ idx, int32_t* __restrict__ n_sel) {
-  extern __shared__ uint32_t mem[];           // [C] member (low 19 bits | slot << 32?) values
+  extern __shared__ uint32_t mem[];           // [C] bit patterns of the threshold-bin members
   __shared__ uint32_t h[kHistBins];
   __shared__ uint32_t taken[kMaxC / 32];      // bitmap over candidate slots
-  constexpr int kTkRankCap = kTkThreads;  // members ranked in one shot
-  __shared__ uint32_t mslot[kTkRankCap];
+  __shared__ uint2 mpair[kTkRankCap];         // (bit pattern, slot) of the first members
   __shared__ uint32_t wt[32], wt2[32];
   __shared__ int s_bin;
   __shared__ uint32_t s_above, s_cnt;
@@ -898,14 +900,20 @@ __global__ void __launch_bounds__(kTkThreads)
   const int32_t* cd = cand + size_t(seg) * C;
   const float* sc = s2 + size_t(seg) * C;
   const size_t part_stride = size_t(gridDim.x) * C;
-  uint32_t v[kTkPer];
+  float x[kPer];
 #pragma unroll
-  for (int k = 0; k < kTkPer; ++k) {
-    float x = 0.f;
-    if (k < E && i0 + k < nc)
-      for (int p = 0; p < n_parts; ++p) x += sc[p * part_stride + i0 + k];
-    v[k] = __float_as_uint(fmaxf(x, 0.f));
+  for (int k = 0; k < kPer; ++k) x[k] = 0.f;
+  for (int p = 0; p < n_parts; ++p) {
+    const float* src = sc + p * part_stride + i0;
+    float y[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) y[k] = (k < E && i0 + k < nc) ? __ldg(src + k) : 0.f;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) x[k] += y[k];
   }
+  uint32_t v[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) v[k] = __float_as_uint(fmaxf(x[k], 0.f));
   const bool take_all = (Ke == nc);
   uint32_t b1 = 0;  // bin of the K-th largest; bins above it are kept whole
   if (!take_all && Ke > 0) {
@@ -914,7 +922,7 @@ __global__ void __launch_bounds__(kTkThreads)
     if (threadIdx.x == 0) s_cnt = 0;
     __syncthreads();
 #pragma unroll
-    for (int k = 0; k < kTkPer; ++k)
+    for (int k = 0; k < kPer; ++k)
       if (k < E && i0 + k < nc) atomicAdd(&h[v[k] >> 19], 1u);
     __syncthreads();
     find_bin_from_top<kTkThreads>(h, kHistBins, uint32_t(Ke), wt, &s_bin, &s_above);
@@ -923,7 +931,7 @@ __global__ void __launch_bounds__(kTkThreads)
     // one warp-aggregated allocation for all of a thread's members
     uint32_t my_members = 0;
 #pragma unroll
-    for (int k = 0; k < kTkPer; ++k)
+    for (int k = 0; k < kPer; ++k)
       my_members += (k < E && i0 + k < nc && (v[k] >> 19) == b1) ? 1u : 0u;
     uint32_t incl = my_members;
 #pragma unroll
@@ -936,10 +944,10 @@ __global__ void __launch_bounds__(kTkThreads)
     wbase = __shfl_sync(0xffffffffu, wbase, 31);
     uint32_t slot = wbase + incl - my_members;
 #pragma unroll
-    for (int k = 0; k < kTkPer; ++k) {
+    for (int k = 0; k < kPer; ++k) {
       if (k < E && i0 + k < nc && (v[k] >> 19) == b1) {
         mem[slot] = v[k];
-        if (slot < uint32_t(kTkRankCap)) mslot[slot] = uint32_t(i0 + k);
+        if (slot < uint32_t(kTkRankCap)) mpair[slot] = make_uint2(v[k], uint32_t(i0 + k));
         ++slot;
       }
     }
@@ -949,13 +957,21 @@ __global__ void __launch_bounds__(kTkThreads)
       // exact rank of member t among the members: higher score, or equal
       // score at a lower slot, ranks first
       if (threadIdx.x < cnt) {
-        const uint32_t my = mem[threadIdx.x], ms = mslot[threadIdx.x];
-        uint32_t rank = 0;
-        for (uint32_t j = 0; j < cnt; ++j) {
-          const uint32_t o = mem[j];
-          rank += (o > my) || (o == my && mslot[j] < ms);
+        const uint2 me = mpair[threadIdx.x];
+        uint32_t r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+        uint32_t j = 0;
+        for (; j + 4 <= cnt; j += 4) {
+          const uint2 a = mpair[j], b = mpair[j + 1], c = mpair[j + 2], d = mpair[j + 3];
+          r0 += (a.x > me.x) || (a.x == me.x && a.y < me.y);
+          r1 += (b.x > me.x) || (b.x == me.x && b.y < me.y);
+          r2 += (c.x > me.x) || (c.x == me.x && c.y < me.y);
+          r3 += (d.x > me.x) || (d.x == me.x && d.y < me.y);
         }
-        if (rank < need) atomicOr(&taken[ms >> 5], 1u << (ms & 31));
+        for (; j < cnt; ++j) {
+          const uint2 a = mpair[j];
+          r0 += (a.x > me.x) || (a.x == me.x && a.y < me.y);
+        }
+        if (r0 + r1 + r2 + r3 < need) atomicOr(&taken[me.y >> 5], 1u << (me.y & 31));
       }
     } else {
       // many members: resolve the remaining 19 bits with two more digits
@@ -979,11 +995,11 @@ __global__ void __launch_bounds__(kTkThreads)
       // members above tau, plus the first need_eq ties in slot order
       uint32_t n_eq = 0;
 #pragma unroll
-      for (int k = 0; k < kTkPer; ++k) n_eq += (k < E && i0 + k < nc && v[k] == tau) ? 1u : 0u;
+      for (int k = 0; k < kPer; ++k) n_eq += (k < E && i0 + k < nc && v[k] == tau) ? 1u : 0u;
       uint32_t eq_before, d0, d1, d2;
       block_excl_scan2<kTkThreads>(n_eq, 0u, wt, wt2, eq_before, d0, d1, d2);
 #pragma unroll
-      for (int k = 0; k < kTkPer; ++k) {
+      for (int k = 0; k < kPer; ++k) {
         if (!(k < E && i0 + k < nc) || (v[k] >> 19) != b1) continue;
         bool t = v[k] > tau;
         if (v[k] == tau) t = eq_before++ < need_eq;
@@ -994,29 +1010,33 @@ __global__ void __launch_bounds__(kTkThreads)
   }
   const int sink_end = min(S, L);
   const int local_begin = max(L - W, sink_end);
-  uint32_t keep_mask = 0, n_keep = 0;
+  // the top-K slots of this thread, then their positions with all loads in flight
+  uint32_t top_mask = 0;
 #pragma unroll
-  for (int k = 0; k < kTkPer; ++k) {
+  for (int k = 0; k < kPer; ++k) {
     const int slot = i0 + k;
     if (!(k < E && slot < nc) || Ke == 0) continue;
-    bool keep = take_all || (v[k] >> 19) > b1 ||
-                ((v[k] >> 19) == b1 && ((taken[slot >> 5] >> (slot & 31)) & 1u));
-    if (keep) {
-      const int p = cd[slot];
-      keep = p >= sink_end && p < local_begin;
-    }
-    if (keep) {
+    if (take_all || (v[k] >> 19) > b1 ||
+        ((v[k] >> 19) == b1 && ((taken[slot >> 5] >> (slot & 31)) & 1u)))
+      top_mask |= 1u << k;
+  }
+  int32_t pk[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) pk[k] = ((top_mask >> k) & 1u) ? __ldg(cd + i0 + k) : -1;
+  uint32_t keep_mask = 0, n_keep = 0;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k)
+    if (((top_mask >> k) & 1u) && pk[k] >= sink_end && pk[k] < local_begin) {
       keep_mask |= 1u << k;
       ++n_keep;
     }
-  }
   uint32_t at, d3, n_mid, d4;
   block_excl_scan2<kTkThreads>(n_keep, 0u, wt, wt2, at, d3, n_mid, d4);
   int32_t* out = idx + size_t(seg) * P_max;
 #pragma unroll
-  for (int k = 0; k < kTkPer; ++k)
+  for (int k = 0; k < kPer; ++k)
     if ((keep_mask >> k) & 1u) {
-      if (sink_end + int(at) < P_max) out[sink_end + at] = cd[i0 + k];
+      if (sink_end + int(at) < P_max) out[sink_end + at] = pk[k];
       ++at;
     }
   for (int j = threadIdx.x; j < sink_end; j += kTkThreads) out[j] = j;
@@ -1032,26 +1052,27 @@ cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const i
                               const int32_t* n_cand, const float* s2, int n_parts, int C, int K,
                               int S, int W, int P_max, int32_t* idx, int32_t* n_sel,
                               cudaStream_t st) {
+  static_assert(kMaxC <= 16 * kTkThreads, "16 scores per thread cover every C");
   const size_t smem = size_t(C) * 4;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(topk_union_kernel<1024>,
+    cudaError_t e = cudaFuncSetAttribute(topk_union_kernel<4>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxC * 4);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(topk_union_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(topk_union_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kMaxC * 4);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  // the fewest threads that hold C scores at kTkPer per thread
-  if (C <= 256 * kTkPer)
-    HERALD_CHECK_LAUNCH(launch_k("topk_union_kernel", topk_union_kernel<256>, dm.N * dm.Hkv, 256,
-                                 smem, st, ctx, cand, n_cand, s2, n_parts, dm.Hkv, dm.L_max, C, K,
-                                 S, W, P_max, idx, n_sel));
+  // the fewest registers that hold C scores over 1024 threads
+  if (C <= 4 * kTkThreads)
+    HERALD_CHECK_LAUNCH(launch_k("topk_union_kernel", topk_union_kernel<4>, dm.N * dm.Hkv,
+                                 kTkThreads, smem, st, ctx, cand, n_cand, s2, n_parts, dm.Hkv,
+                                 dm.L_max, C, K, S, W, P_max, idx, n_sel));
   else
-    HERALD_CHECK_LAUNCH(launch_k("topk_union_kernel", topk_union_kernel<1024>, dm.N * dm.Hkv,
-                                 1024, smem, st, ctx, cand, n_cand, s2, n_parts, dm.Hkv, dm.L_max,
-                                 C, K, S, W, P_max, idx, n_sel));
+    HERALD_CHECK_LAUNCH(launch_k("topk_union_kernel", topk_union_kernel<16>, dm.N * dm.Hkv,
+                                 kTkThreads, smem, st, ctx, cand, n_cand, s2, n_parts, dm.Hkv,
+                                 dm.L_max, C, K, S, W, P_max, idx, n_sel));
   return cudaGetLastError();
 }
 
