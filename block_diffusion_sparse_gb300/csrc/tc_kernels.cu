@@ -1036,35 +1036,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // (kpc = ceil(P_max/8) rounded to 16, at most 192), loaded by two 2-D TMA
 // boxes each for K and V; the last CTA also owns the B block keys.  Each
 // CTA computes S = Q K^T for its keys with one UMMA (N = kpc), P = exp(S -
-// rowmax) in bf16, O = P V into TMEM, and keeps (O, max, sum) in shared
-// memory.  After one cluster barrier every CTA pushes the 16 rows that CTA c
-// finalises into c's freed operand buffers with bulk shared::cta ->
-// shared::cluster copies that complete on c's mbarrier; each CTA then merges
-// its 16 rows from local shared memory and writes bf16 out.
+// rowmax) in bf16 (written over the Q/K operands, dead once S is in TMEM),
+// O = P V into TMEM.  Rows are finalised 16 per CTA: each CTA stages its O
+// rows divided by their row sums (fp16) over the dead operands and pushes
+// rows [c*16, c*16 + 16) with their (max, sum) to CTA c by bulk
+// shared::cta -> shared::cluster copies that complete on c's mbarrier;
+// each CTA merges its 16 rows once all 8 slices have landed.  The receive
+// buffers have shared memory of their own, so no cluster-wide barrier
+// separates the attention from the exchange.
 constexpr int kPoolCtas = 8;
 constexpr int kPoolRows = kTileM / kPoolCtas;   // rows finalised per CTA
 constexpr int kPoolMaxKpc = 192;
 constexpr int kPoolMaxB = 64;
 
 struct PoolSmem {
-  uint32_t q, k, v, p, kb, vb, pb, recv_o, recv_ml, total;
+  uint32_t q, k, kb, p, pb, v, vb, recv_o, recv_ml, total;
 };
 __host__ __device__ inline PoolSmem pool_smem(int D, int kpc, int Bp) {
   const uint32_t H = uint32_t(D / 64);
   PoolSmem L;
+  // region A: Q | K | K_block, later P | P_block
   L.q = 0;
   L.k = H * 128u * 128u;
-  L.v = L.k + H * uint32_t(kpc) * 128u;
-  L.p = L.v + H * uint32_t(kpc) * 128u;
-  L.kb = L.p + uint32_t((kpc + 63) / 64) * 16384u;
-  L.vb = L.kb + H * uint32_t(Bp) * 128u;
-  L.pb = L.vb + H * uint32_t(Bp) * 128u;
-  const uint32_t layout_end = L.pb + 16384u;
-  const uint32_t o_bytes = 128u * uint32_t(D + 8) * 2u;  // fp16 O partial, over Q/K/...
-  L.recv_o = (o_bytes + 1023u) & ~1023u;
+  L.kb = L.k + H * uint32_t(kpc) * 128u;
+  const uint32_t a_end = L.kb + H * uint32_t(Bp) * 128u;
+  L.p = 0;
+  L.pb = uint32_t((kpc + 63) / 64) * 16384u;
+  const uint32_t p_end = L.pb + 16384u;
+  L.v = ((a_end > p_end ? a_end : p_end) + 1023u) & ~1023u;
+  L.vb = L.v + H * uint32_t(kpc) * 128u;
+  L.recv_o = L.vb + H * uint32_t(Bp) * 128u;
   L.recv_ml = L.recv_o + uint32_t(kPoolCtas * kPoolRows) * uint32_t(D + 8) * 2u;
-  const uint32_t recv_end = L.recv_ml + uint32_t(kPoolCtas * kPoolRows) * 8u;
-  L.total = (layout_end > recv_end ? layout_end : recv_end) + 1024u;
+  L.total = L.recv_ml + uint32_t(kPoolCtas * kPoolRows) * 8u + 1024u;
   return L;
 }
 
@@ -1084,18 +1087,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ float red_m[2][kTileM];
   __shared__ float red_s[2][kTileM];
   __shared__ __align__(16) float2 ml[kTileM];
+  constexpr uint32_t kSliceO = uint32_t(kPoolRows * OROW * 2);
+  constexpr uint32_t kSliceMl = uint32_t(kPoolRows * 8);
   const int Bp = (B + 15) & ~15;
   const PoolSmem S = pool_smem(D, kpc, Bp);
   uint8_t* base = align1024(smem_raw);
   uint8_t* Qs = base + S.q;
   uint8_t* Ks = base + S.k;
-  uint8_t* Vs = base + S.v;
-  uint8_t* Ps = base + S.p;
   uint8_t* Kb = base + S.kb;
-  uint8_t* Vb = base + S.vb;
+  uint8_t* Ps = base + S.p;
   uint8_t* Pb = base + S.pb;
-  float* Os = reinterpret_cast<float*>(base);
-  float* recv_o = reinterpret_cast<float*>(base + S.recv_o);
+  uint8_t* Vs = base + S.v;
+  uint8_t* Vb = base + S.vb;
+  uint16_t* recv_o = reinterpret_cast<uint16_t*>(base + S.recv_o);
   float2* recv_ml = reinterpret_cast<float2*>(base + S.recv_ml);
   const uint32_t rank = cluster_ctarank();
   const int mt = blockIdx.y, seg = blockIdx.z;
@@ -1107,8 +1111,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(&bar0, 1);
     mbar_init(&bar1, 1);
     mbar_init(&barR, 1);
+    mbar_arrive_expect_tx(&barR, kPoolCtas * (kSliceO + kSliceMl));
     fence_mbar_init();
   }
+  // peers' copies complete on barR: its initialisation is published
+  // cluster-wide here and awaited just before the first copy is issued
+  __cluster_barrier_arrive_relaxed();
   tmem_setup(&tmem_base, 512);
   const uint32_t tbase = tmem_base;
   griddep_enter();
@@ -1182,6 +1190,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     umma_commit(&bar0);
   }
+  // every thread waits for the commit: after it Q, K and K_block are dead
+  // and P may be written over them
   if (any && !mbar_wait(&bar0, 0)) ok = false;
   tc_fence_after();
   __syncwarp();
@@ -1293,13 +1303,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncwarp();
   if (!ok) record_error(err, DEV_TIMEOUT_MMA);
 
-  // O partial -> shared memory (over Q / K, now free): each row divided by
-  // its sum and stored as fp16 (|o / l| <= max |v|); the merge re-weights by
-  // (max, sum), which stay fp32
+  // O partial -> shared memory over the dead operands (P was the last):
+  // each row divided by its sum and stored as fp16 (|o / l| <= max |v|); the
+  // merge re-weights by (max, sum), which stay fp32
   const float lrow = red_s[0][row] + red_s[1][row];
+  uint16_t* Os = reinterpret_cast<uint16_t*>(base);
   if (any) {
     const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
-    uint16_t* orow = reinterpret_cast<uint16_t*>(Os) + row * OROW;
+    uint16_t* orow = Os + row * OROW;
 #pragma unroll
     for (int k = 0; k < D / 64; ++k) {
       float v[32];
@@ -1316,19 +1327,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
   }
-  if (ch == 0) ml[row] = make_float2(m, lrow);
-  constexpr uint32_t kSliceO = uint32_t(kPoolRows * OROW * 2);
-  constexpr uint32_t kSliceMl = uint32_t(kPoolRows * 8);
-  if (threadIdx.x == 0) mbar_arrive_expect_tx(&barR, kPoolCtas * (kSliceO + kSliceMl));
+  if (ch == 0) ml[row] = make_float2(m, any ? lrow : 0.f);
   fence_proxy_async_smem();  // the partial is read by bulk copies (async proxy)
-  cluster_sync_all();        // every CTA: operands consumed, partial final
+  __syncthreads();
+  __cluster_barrier_wait();  // every peer's barR is initialised
 
   // push: rows [c*16, c*16+16) of this CTA's partial go to CTA c, slot `rank`
   if (threadIdx.x == 0) {
     for (uint32_t c = 0; c < uint32_t(kPoolCtas); ++c) {
       const uint32_t mb = cluster_addr(&barR, c);
       bulk_copy_to_peer(cluster_addr(reinterpret_cast<uint8_t*>(recv_o) + rank * kSliceO, c),
-                        reinterpret_cast<uint16_t*>(Os) + c * kPoolRows * OROW, kSliceO, mb);
+                        Os + c * kPoolRows * OROW, kSliceO, mb);
       bulk_copy_to_peer(cluster_addr(reinterpret_cast<uint8_t*>(recv_ml) + rank * kSliceMl, c),
                         &ml[c * kPoolRows], kSliceMl, mb);
     }
@@ -1339,7 +1348,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // merge this CTA's 16 rows from the 8 received partials:
   // out = sum_c 2^(m_c - M) l_c (o_c / l_c) / sum_c 2^(m_c - M) l_c
   constexpr int E = D / 32;
-  const uint16_t* recv_h = reinterpret_cast<const uint16_t*>(recv_o);
   for (int rr = warp; rr < kPoolRows; rr += kTcThreads / 32) {
     const int lr = int(rank) * kPoolRows + rr;
     const int grow = mt * kTileM + lr;
@@ -1357,21 +1365,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (pm[c].x == -INFINITY || pm[c].y <= 0.f) continue;
       const float wgt = fast_exp2(pm[c].x - M) * pm[c].y;
       L += wgt;
-      const __half* o = reinterpret_cast<const __half*>(recv_h + (c * kPoolRows + rr) * OROW) +
+      const __half* o = reinterpret_cast<const __half*>(recv_o + (c * kPoolRows + rr) * OROW) +
                         lane * E;
 #pragma unroll
       for (int e = 0; e < E; ++e) acc[e] += wgt * __half2float(o[e]);
     }
     if (grow < R) {
       const int b = grow / G, h = g * G + (grow - (grow / G) * G);
-      uint16_t* dst = out + ((size_t(n) * B + b) * Hq + h) * D + lane * E;
-      const float inv = 1.f / L;
+      uint16_t* dstp = out + ((size_t(n) * B + b) * Hq + h) * D + lane * E;
+      const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
       for (int e = 0; e < E; e += 2)
-        *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16(acc[e] * inv, acc[e + 1] * inv);
+        *reinterpret_cast<uint32_t*>(dstp + e) = pack_bf16(acc[e] * inv, acc[e + 1] * inv);
     }
   }
-  if (threadIdx.x == 0) bulk_wait_read_all();  // outgoing copies have read this CTA's partial
+  if (threadIdx.x == 0) bulk_wait_read_all();  // outgoing copies have read the partial
   tmem_teardown(tbase, 512);
 }
 
