@@ -900,16 +900,37 @@ __global__ void __launch_bounds__(kTkThreads)
   const int32_t* cd = cand + size_t(seg) * C;
   const float* sc = s2 + size_t(seg) * C;
   const size_t part_stride = size_t(gridDim.x) * C;
+  // the candidate positions are needed only at the end; with few per thread
+  // their loads are issued here, with the scores', so that no phase waits on
+  // memory twice (with 16 per thread the registers are not there)
+  constexpr bool kEarlyPos = kPer <= 4;
+  int32_t pk[kPer];
+  if constexpr (kEarlyPos) {
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) pk[k] = (k < E && i0 + k < nc) ? __ldg(cd + i0 + k) : -1;
+  }
   float x[kPer];
 #pragma unroll
   for (int k = 0; k < kPer; ++k) x[k] = 0.f;
-  for (int p = 0; p < n_parts; ++p) {
-    const float* src = sc + p * part_stride + i0;
-    float y[kPer];
+  // partials two at a time: both loads in flight
+  int p = 0;
+  for (; p + 2 <= n_parts; p += 2) {
+    const float* s0 = sc + p * part_stride + i0;
+    const float* s1 = s0 + part_stride;
+    float y0[kPer], y1[kPer];
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) y[k] = (k < E && i0 + k < nc) ? __ldg(src + k) : 0.f;
+    for (int k = 0; k < kPer; ++k) {
+      const bool in = k < E && i0 + k < nc;
+      y0[k] = in ? __ldg(s0 + k) : 0.f;
+      y1[k] = in ? __ldg(s1 + k) : 0.f;
+    }
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) x[k] += y[k];
+    for (int k = 0; k < kPer; ++k) x[k] += y0[k] + y1[k];
+  }
+  if (p < n_parts) {
+    const float* s0 = sc + p * part_stride + i0;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) x[k] += (k < E && i0 + k < nc) ? __ldg(s0 + k) : 0.f;
   }
   uint32_t v[kPer];
 #pragma unroll
@@ -1010,7 +1031,7 @@ __global__ void __launch_bounds__(kTkThreads)
   }
   const int sink_end = min(S, L);
   const int local_begin = max(L - W, sink_end);
-  // the top-K slots of this thread, then their positions with all loads in flight
+  // the top-K slots of this thread
   uint32_t top_mask = 0;
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
@@ -1020,9 +1041,10 @@ __global__ void __launch_bounds__(kTkThreads)
         ((v[k] >> 19) == b1 && ((taken[slot >> 5] >> (slot & 31)) & 1u)))
       top_mask |= 1u << k;
   }
-  int32_t pk[kPer];
+  if constexpr (!kEarlyPos) {
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) pk[k] = ((top_mask >> k) & 1u) ? __ldg(cd + i0 + k) : -1;
+    for (int k = 0; k < kPer; ++k) pk[k] = ((top_mask >> k) & 1u) ? __ldg(cd + i0 + k) : -1;
+  }
   uint32_t keep_mask = 0, n_keep = 0;
 #pragma unroll
   for (int k = 0; k < kPer; ++k)

@@ -80,6 +80,10 @@ __device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
   return r;
 }
+__device__ __forceinline__ void st_peer_f2(uint32_t a, float2 v) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(v.x), "f"(v.y)
+               : "memory");
+}
 __device__ __forceinline__ float2 ld_peer_f2(uint32_t a) {
   float2 v;
   asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
@@ -349,12 +353,12 @@ __global__ void __launch_bounds__(kTcThreads)
 // ========================================================== refine_fused
 // Stage 2 in one kernel for C <= 4096: one 8-CTA cluster per (sequence, KV
 // head, 128-row tile); CTA r scores candidate slots [r*cpc, (r+1)*cpc)
-// (cpc <= 512, so the scores fill TMEM and are never recomputed).  Row
-// (max, sumexp) over each CTA's candidates are merged across the cluster
-// through distributed shared memory into the row log-sum-exp; each CTA then
-// sums exp(S - lse_r) over its 128 rows (warp transpose-reductions, rows
-// past B*G excluded) and writes one partial s2 per row tile, which the top-K
-// kernel adds up.
+// (cpc <= 512, so the scores fill TMEM and are never recomputed).  Each
+// CTA stores its row (max, sumexp) over its candidates into every peer's
+// shared memory; after one cluster barrier each CTA merges them into the row
+// log-sum-exp from its own shared memory, sums exp(S - lse_r) over its 128
+// rows (warp transpose-reductions, rows past B*G excluded) and writes one
+// partial s2 per row tile, which the top-K kernel adds up.
 constexpr int kFuseCtas = 8;
 constexpr int kFuseMaxCpc = 512;
 
@@ -385,7 +389,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ uint32_t tmem_base;
   __shared__ int32_t pos[kFuseMaxCpc];
   __shared__ float2 half_stat[2][kTileM];
-  __shared__ __align__(16) float2 row_stat[kTileM];
+  __shared__ __align__(16) float2 peer_stat[kFuseCtas][kTileM];  // [sender][row]
   __shared__ float colsum[2][4][kFuseMaxCpc / 2];
   uint8_t* Qs = align1024(smem_raw);
   uint8_t* Ks = Qs + Cfg::kQBytes;
@@ -397,6 +401,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(&bar0, 1);
     fence_mbar_init();
   }
+  // peers store into this CTA's shared memory before the cluster barrier
+  // below: this arrive, awaited just before those stores, shows that every
+  // CTA of the cluster has started
+  __cluster_barrier_arrive_relaxed();
   tmem_setup(&tmem_base, 512);
   const uint32_t tbase = tmem_base;
   griddep_enter();
@@ -448,7 +456,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncwarp();
 
   // row (max, sumexp) over this CTA's candidates, log2 units; the two warps of
-  // a lane quadrant take the two column halves
+  // a lane quadrant take the two column halves.  The exponentials
+  // p = 2^(s - m_half) are stored back over the scores, so the column sums
+  // below only rescale them by 2^(m_half - lse).
   const int quad = warp & 3, ch = warp >> 2;
   const int row = quad * 32 + lane;
   const uint32_t trow = tbase + (uint32_t(quad * 32) << 16);
@@ -460,33 +470,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tmem_ld32(trow + uint32_t(c), v);
 #pragma unroll
     for (int i = 0; i < 32; ++i)
-      if (c + i < ncv) m = fmaxf(m, v[i] * sl2);
+      if (c + i < ncv) m = fmaxf(m, v[i]);
   }
+  m = m == -INFINITY ? m : m * sl2;  // the scale is positive: max commutes with it
   float l = 0.f;
-  if (m != -INFINITY)
-    for (int c = hc0; c < hc1; c += 32) {
-      float v[32];
-      tmem_ld32(trow + uint32_t(c), v);
+  for (int c = hc0; c < hc1; c += 32) {
+    float v[32];
+    tmem_ld32(trow + uint32_t(c), v);
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (c + i < ncv) l += fast_exp2(v[i] * sl2 - m);
+    for (int i = 0; i < 32; ++i) {
+      v[i] = (c + i < ncv) ? fast_exp2(fmaf(v[i], sl2, -m)) : 0.f;
+      l += v[i];
     }
+    tmem_st32(trow + uint32_t(c), v);
+  }
+  tmem_wait_st();
   half_stat[ch][row] = make_float2(m, l);
   __syncthreads();
+  __cluster_barrier_wait();  // every CTA of the cluster has started
   if (ch == 0) {
     const float2 a = half_stat[0][row], b = half_stat[1][row];
     const float M = fmaxf(a.x, b.x);
     const float Lr = (a.x == -INFINITY ? 0.f : a.y * fast_exp2(a.x - M)) +
                      (b.x == -INFINITY ? 0.f : b.y * fast_exp2(b.x - M));
-    row_stat[row] = make_float2(M, Lr);
+#pragma unroll
+    for (int c = 0; c < kFuseCtas; ++c)
+      st_peer_f2(peer_addr(&peer_stat[rank][row], uint32_t(c)), make_float2(M, Lr));
   }
-  cluster_sync_all();
-  // row log-sum-exp over all candidates: every peer's statistics of my row
+  cluster_sync_all();  // releases the stores above, acquires the peers'
+  // row log-sum-exp over all candidates: every CTA's statistics of my row
   float lse = 0.f;
   {
     float2 st[kFuseCtas];
 #pragma unroll
-    for (int c = 0; c < kFuseCtas; ++c) st[c] = ld_peer_f2(peer_addr(&row_stat[row], uint32_t(c)));
+    for (int c = 0; c < kFuseCtas; ++c) st[c] = peer_stat[c][row];
     float M = -INFINITY;
 #pragma unroll
     for (int c = 0; c < kFuseCtas; ++c) M = fmaxf(M, st[c].x);
@@ -497,6 +514,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     lse = M + __log2f(Lr);
   }
   const bool row_ok = mt * kTileM + row < R;
+  // 2^(s - lse) = p * 2^(m_half - lse); rows past B*G contribute nothing
+  const float f = (row_ok && m != -INFINITY) ? fast_exp2(m - lse) : 0.f;
   // column sums over the 128 rows: per 32-column chunk, a warp
   // transpose-reduces its 32 rows; after the butterfly, lane j holds the sum
   // of chunk column j over the warp's rows
@@ -504,8 +523,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float v[32];
     tmem_ld32(trow + uint32_t(c), v);
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      v[i] = (row_ok && c + i < ncv) ? fast_exp2(v[i] * sl2 - lse) : 0.f;
+    for (int i = 0; i < 32; ++i) v[i] *= f;
 #pragma unroll
     for (int w = 16; w >= 1; w >>= 1) {
       // the lane with bit w set keeps the upper w columns, its partner the lower
@@ -528,7 +546,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     out[c0 + j] = colsum[chh][0][jj] + colsum[chh][1][jj] + colsum[chh][2][jj] +
                   colsum[chh][3][jj];
   }
-  cluster_sync_all();  // peers may still read this CTA's row statistics
+  // no peer touches this CTA's shared memory after the cluster barrier
   tmem_teardown(tbase, 512);
 }
 
