@@ -125,6 +125,24 @@ EncodeTiledFn encode_fn() {
 // 128-byte swizzle (the UMMA K-major shared-memory layout).
 herald_status encode_rows_map(const void* base, uint64_t rows, int d, uint32_t box_rows,
                               CUtensorMap* map) {
+  // a map depends only on these four values: recently encoded ones are
+  // reused (per thread, round-robin over a few entries), which keeps the
+  // per-call host cost of the steady state low
+  struct Entry {
+    const void* base;
+    uint64_t rows;
+    int d;
+    uint32_t box;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 8;
+  thread_local Entry cache[kEntries] = {};
+  thread_local int next = 0;
+  for (const Entry& e : cache)
+    if (e.base == base && e.rows == rows && e.d == d && e.box == box_rows) {
+      *map = e.map;
+      return HERALD_OK;
+    }
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(HERALD_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   const cuuint64_t dims[2] = {cuuint64_t(d), cuuint64_t(rows)};
@@ -136,18 +154,38 @@ herald_status encode_rows_map(const void* base, uint64_t rows, int d, uint32_t b
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(HERALD_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+  Entry& e = cache[next];
+  next = (next + 1) % kEntries;
+  e.base = base;
+  e.rows = rows;
+  e.d = d;
+  e.box = box_rows;
+  e.map = *map;
   return HERALD_OK;
 }
 
 // Device memory is streamed by TMA; mapped host (or managed) memory by
 // plain 16-byte copies.
+// The answer for an address does not change while its allocation lives,
+// and device and host allocations occupy disjoint ranges of the unified
+// address space, so recent answers are reused (per thread).
 bool is_device_memory(const void* p) {
+  constexpr int kEntries = 8;
+  thread_local const void* keys[kEntries] = {};
+  thread_local bool vals[kEntries] = {};
+  thread_local int next = 0;
+  for (int i = 0; i < kEntries; ++i)
+    if (keys[i] == p) return vals[i];
   cudaPointerAttributes a;
-  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+  bool dev = false;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess)
     cudaGetLastError();
-    return false;
-  }
-  return a.type == cudaMemoryTypeDevice;
+  else
+    dev = a.type == cudaMemoryTypeDevice;
+  keys[next] = p;
+  vals[next] = dev;
+  next = (next + 1) % kEntries;
+  return dev;
 }
 
 herald_status run_stage1(const herald_dims& dm, const uint16_t* q_merge, const uint16_t* k_cache,

@@ -895,7 +895,8 @@ __global__ void __launch_bounds__(kTkThreads)
   const int L = min(max(ctx[n], 0), L_max);
   const int nc = min(max(n_cand[seg], 0), C);
   const int Ke = min(K, nc);
-  const int E = (nc + kTkThreads - 1) / kTkThreads;
+  // slots per thread from C, not n_cand: the score loads need not wait for it
+  const int E = (C + kTkThreads - 1) / kTkThreads;
   const int i0 = threadIdx.x * E;
   const int32_t* cd = cand + size_t(seg) * C;
   const float* sc = s2 + size_t(seg) * C;
@@ -907,7 +908,7 @@ __global__ void __launch_bounds__(kTkThreads)
   int32_t pk[kPer];
   if constexpr (kEarlyPos) {
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) pk[k] = (k < E && i0 + k < nc) ? __ldg(cd + i0 + k) : -1;
+    for (int k = 0; k < kPer; ++k) pk[k] = (k < E && i0 + k < C) ? __ldg(cd + i0 + k) : -1;
   }
   float x[kPer];
 #pragma unroll
@@ -920,7 +921,7 @@ __global__ void __launch_bounds__(kTkThreads)
     float y0[kPer], y1[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
-      const bool in = k < E && i0 + k < nc;
+      const bool in = k < E && i0 + k < C;  // in bounds; slots >= n_cand are masked later
       y0[k] = in ? __ldg(s0 + k) : 0.f;
       y1[k] = in ? __ldg(s1 + k) : 0.f;
     }
@@ -930,7 +931,7 @@ __global__ void __launch_bounds__(kTkThreads)
   if (p < n_parts) {
     const float* s0 = sc + p * part_stride + i0;
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) x[k] += (k < E && i0 + k < nc) ? __ldg(s0 + k) : 0.f;
+    for (int k = 0; k < kPer; ++k) x[k] += (k < E && i0 + k < C) ? __ldg(s0 + k) : 0.f;
   }
   uint32_t v[kPer];
 #pragma unroll

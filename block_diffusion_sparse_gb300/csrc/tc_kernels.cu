@@ -30,16 +30,26 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 // Copies `rows` rows of D bf16 (row r from src_of(r), or zeros when src_of
 // returns nullptr) into a K-major 128B-swizzled tile: D/64 column halves,
 // each [rows_alloc][128 bytes].  `any_src` is a valid global address used
-// as the (unread) source of zero-filled chunks.
+// as the (unread) source of zero-filled chunks.  A warp copies 32/(D/8)
+// whole rows per step (one 16-byte chunk per lane), so src_of runs once
+// per lane and step, and the unrolled steps keep several rows in flight.
+// Every thread of the (kTcThreads-thread) block must call it.
 template <int D, typename SrcOf>
 __device__ __forceinline__ void load_rows_sw128(uint8_t* tile, int rows, int rows_alloc,
                                                 const uint16_t* any_src, SrcOf src_of) {
-  constexpr int CPR = D / 8;  // 16-byte chunks per row
-  for (int q = threadIdx.x; q < rows * CPR; q += blockDim.x) {
-    const int r = q / CPR, c = q - (q / CPR) * CPR;
-    const uint16_t* s = src_of(r);
-    cp_async_16(tile + (c >> 3) * (rows_alloc * 128) + sw128_off(r, c & 7),
-                s ? s + c * 8 : any_src, s ? 16u : 0u);
+  constexpr int CPR = D / 8;        // 16-byte chunks per row
+  constexpr int RPW = 32 / CPR;     // rows per warp step
+  constexpr int kStep = (kTcThreads / 32) * RPW;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = lane % CPR, sub = lane / CPR;
+  uint8_t* half = tile + (c >> 3) * (rows_alloc * 128);
+#pragma unroll 4
+  for (int r0 = warp * RPW; r0 < rows; r0 += kStep) {
+    const int r = r0 + sub;
+    if (r < rows) {
+      const uint16_t* s = src_of(r);
+      cp_async_16(half + sw128_off(r, c & 7), s ? s + c * 8 : any_src, s ? 16u : 0u);
+    }
   }
 }
 

@@ -124,6 +124,32 @@ def _check(status: int):
         raise HeraldError(status, lib().herald_last_error().decode())
 
 
+# Helpers for callers that resolve addresses once and call lib() directly
+# (the pipeline's per-block path): plain integers cross ctypes fastest.
+check = _check
+
+
+def ptr(x) -> int:
+    """Device (or mapped host) address of a tensor, or an address as is."""
+    p = _p(x)
+    if p is None:
+        raise ValueError("a NULL address where a buffer is required")
+    return p
+
+
+def step_bytes(x) -> int:
+    """Byte distance between consecutive entries of a tensor's first axis."""
+    if not x.is_contiguous():
+        raise ValueError("per-step inputs and outputs must be contiguous")
+    return x.stride(0) * x.element_size()
+
+
+def stream_handle(stream) -> int:
+    """cudaStream_t of a torch stream (0 = the legacy default stream)."""
+    h = _s(stream)
+    return 0 if h is None else h
+
+
 def herald_workspace_size(d: Dims, C_: int, P_max: int) -> int:
     return int(lib().herald_workspace_size(d, int(C_), int(P_max)))
 

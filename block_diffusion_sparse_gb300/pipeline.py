@@ -46,6 +46,16 @@ class BlockPipeline:
         self.pool_v = [torch.zeros_like(self.pool_k[0]) for _ in range(2)]
         self.den = den_stream
         self.sel = sel_stream if sel_stream is not None else torch.cuda.Stream()
+        # addresses of the persistent buffers, resolved once: a block issues
+        # ~T+5 library calls, and per-call marshalling would otherwise cost
+        # more host time than the kernels take on the GPU
+        P_ = H.ptr
+        self._ws_den, self._ws_sel = P_(self.ws_den), P_(self.ws_sel)
+        self._cand = [P_(t) for t in self.cand]
+        self._n_cand = [P_(t) for t in self.n_cand]
+        self._idx, self._n_sel = P_(self.idx), P_(self.n_sel)
+        self._pool_k = [P_(t) for t in self.pool_k]
+        self._pool_v = [P_(t) for t in self.pool_v]
 
     def _den(self):
         return self.den if self.den is not None else self.torch.cuda.current_stream()
@@ -59,33 +69,32 @@ class BlockPipeline:
               next_k_cache=None, advance: bool = True, overlap: bool = True):
         """Runs block i: q_steps/block_k/block_v hold the T steps' inputs,
         out[t] receives step t's attention output."""
-        torch = self.torch
         den, sel = self._den(), self.sel
         cur, nxt = i % 2, (i + 1) % 2
         nk = k_cache if next_k_cache is None else next_k_cache
-        d = self.d
+        d, P, L, chk = self.d, self.P, H.lib(), H.check
+        hd, hs = H.stream_handle(den), H.stream_handle(sel)
+        q0, qstep = H.ptr(q_steps), H.step_bytes(q_steps)
+        bk0, bv0, bstep = H.ptr(block_k), H.ptr(block_v), H.step_bytes(block_k)
+        o0, ostep = H.ptr(out), H.step_bytes(out)
+        kc, vc, cx = H.ptr(k_cache), H.ptr(v_cache), H.ptr(ctx)
+        pk, pv = self._pool_k[cur], self._pool_v[cur]
+        wd, wb = self._ws_den, self.ws_bytes
         # stage 1 for block i+1 can start now: block i's queries exist
         sel.wait_stream(den)
-        H.herald_select_stage2(d, q_steps[0], k_cache, ctx, self.cand[cur], self.n_cand[cur],
-                               self.C, self.K, self.S, self.W, self.P, self.idx, self.n_sel,
-                               self.ws_den, self.ws_bytes, den)
-        H.herald_gather(d, self.idx, self.n_sel, self.P, k_cache, v_cache, self.pool_k[cur],
-                        self.pool_v[cur], den)
-        if not overlap:
-            H.herald_select_stage1(d, q_steps[0], nk, ctx, self.C, self.cand[nxt],
-                                   self.n_cand[nxt], self.ws_sel, self.ws_bytes, den)
-        else:
-            with torch.cuda.stream(sel):
-                H.herald_select_stage1(d, q_steps[0], nk, ctx, self.C, self.cand[nxt],
-                                       self.n_cand[nxt], self.ws_sel, self.ws_bytes, sel)
+        chk(L.herald_select_stage2(d, q0, kc, cx, self._cand[cur], self._n_cand[cur], self.C,
+                                   self.K, self.S, self.W, P, self._idx, self._n_sel, wd, wb, hd))
+        chk(L.herald_gather(d, self._idx, self._n_sel, P, kc, vc, pk, pv, hd))
+        chk(L.herald_select_stage1(d, q0, H.ptr(nk), cx, self.C, self._cand[nxt],
+                                   self._n_cand[nxt], self._ws_sel, wb, hs if overlap else hd))
         for t in range(self.T):
-            H.herald_denoise_attn(d, q_steps[t], self.pool_k[cur], self.pool_v[cur], self.n_sel,
-                                  self.P, block_k[t], block_v[t], out[t], 0.0, self.ws_den,
-                                  self.ws_bytes, den)
+            chk(L.herald_denoise_attn(d, q0 + t * qstep, pk, pv, self._n_sel, P, bk0 + t * bstep,
+                                      bv0 + t * bstep, o0 + t * ostep, 0.0, wd, wb, hd))
         if overlap:
             den.wait_stream(sel)
-        H.herald_append_kv(d, block_k[self.T - 1], block_v[self.T - 1], ctx, k_cache, v_cache,
-                           advance, den)
+        last = self.T - 1
+        chk(L.herald_append_kv(d, bk0 + last * bstep, bv0 + last * bstep, cx, kc, vc,
+                               int(bool(advance)), hd))
 
 
 class StackPipeline:
