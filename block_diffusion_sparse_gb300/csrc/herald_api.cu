@@ -123,45 +123,73 @@ EncodeTiledFn encode_fn() {
 
 // 2-D bf16 tensor map [rows][d] with a box of 64 columns x box_rows rows and
 // 128-byte swizzle (the UMMA K-major shared-memory layout).
-herald_status encode_rows_map(const void* base, uint64_t rows, int d, uint32_t box_rows,
-                              CUtensorMap* map) {
-  // a map depends only on these four values: recently encoded ones are
-  // reused (per thread, round-robin over a few entries), which keeps the
-  // per-call host cost of the steady state low
+// bf16 tensor map of 2 or 3 dimensions, 128-byte swizzle.  A map depends
+// only on (base, rank, extents, box): recently encoded ones are reused (per
+// thread, round-robin), which keeps the per-call host cost of the steady
+// state low -- a block step encodes a few maps per attention call.
+static herald_status encode_map(const void* base, int rank, const uint64_t* extent,
+                                const uint32_t* box_in, CUtensorMap* map) {
   struct Entry {
     const void* base;
-    uint64_t rows;
-    int d;
-    uint32_t box;
+    int rank;
+    uint64_t ext[3];
+    uint32_t box[3];
     CUtensorMap map;
   };
-  constexpr int kEntries = 8;
+  constexpr int kEntries = 64;
   thread_local Entry cache[kEntries] = {};
   thread_local int next = 0;
-  for (const Entry& e : cache)
-    if (e.base == base && e.rows == rows && e.d == d && e.box == box_rows) {
+  for (const Entry& e : cache) {
+    if (e.base != base || e.rank != rank) continue;
+    bool same = true;
+    for (int i = 0; i < rank; ++i) same = same && e.ext[i] == extent[i] && e.box[i] == box_in[i];
+    if (same) {
       *map = e.map;
       return HERALD_OK;
     }
+  }
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(HERALD_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
-  const cuuint64_t dims[2] = {cuuint64_t(d), cuuint64_t(rows)};
-  const cuuint64_t strides[1] = {cuuint64_t(d) * 2};
-  const cuuint32_t box[2] = {64, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  cuuint64_t dims[3], strides[2];
+  cuuint32_t box[3], estr[3] = {1, 1, 1};
+  uint64_t stride = 2;  // bytes
+  for (int i = 0; i < rank; ++i) {
+    dims[i] = extent[i];
+    box[i] = box_in[i];
+    if (i > 0) strides[i - 1] = stride;
+    stride *= extent[i];
+  }
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank),
+                        const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(HERALD_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
   Entry& e = cache[next];
   next = (next + 1) % kEntries;
   e.base = base;
-  e.rows = rows;
-  e.d = d;
-  e.box = box_rows;
+  e.rank = rank;
+  for (int i = 0; i < rank; ++i) {
+    e.ext[i] = extent[i];
+    e.box[i] = box_in[i];
+  }
   e.map = *map;
   return HERALD_OK;
+}
+
+herald_status encode_rows_map(const void* base, uint64_t rows, int d, uint32_t box_rows,
+                              CUtensorMap* map) {
+  const uint64_t ext[2] = {uint64_t(d), rows};
+  const uint32_t box[2] = {64, box_rows};
+  return encode_map(base, 2, ext, box, map);
+}
+
+// [tokens][heads][d] with a box of 64 columns x box_heads heads x box_tokens
+// tokens (query tiles and block keys / values of one KV head).
+herald_status encode_heads_map(const void* base, uint64_t tokens, int heads, int d,
+                               uint32_t box_heads, uint32_t box_tokens, CUtensorMap* map) {
+  const uint64_t ext[3] = {uint64_t(d), uint64_t(heads), tokens};
+  const uint32_t box[3] = {64, box_heads, box_tokens};
+  return encode_map(base, 3, ext, box, map);
 }
 
 // Device memory is streamed by TMA; mapped host (or managed) memory by
@@ -190,7 +218,7 @@ bool is_device_memory(const void* p) {
 
 herald_status run_stage1(const herald_dims& dm, const uint16_t* q_merge, const uint16_t* k_cache,
                          const int32_t* ctx_len, int C, int32_t* cand, int32_t* n_cand, void* ws,
-                         const WsLayout& w, cudaStream_t st) {
+                         const WsLayout& w, int sm_budget, cudaStream_t st) {
   const bool tma = is_device_memory(k_cache);
   uint32_t* err = at<uint32_t>(ws, w.err);
   float* qbar = at<float>(ws, w.qbar);
@@ -207,7 +235,8 @@ herald_status run_stage1(const herald_dims& dm, const uint16_t* q_merge, const u
   float2* part1 = at<float2>(ws, w.part1);
   float* s1 = at<float>(ws, w.s1);
   uint32_t* hist = at<uint32_t>(ws, w.hist);
-  const int nsm = sm_count();
+  int nsm = sm_count();
+  if (sm_budget > 0 && sm_budget < nsm) nsm = sm_budget;
   const int part_slots = scan_grid(dm, w, tma, nsm) * 4;  // one slot per (scan CTA, warp)
   HERALD_TRY_CUDA(launch_merge_query(dm, q_merge, qbar, qhl, hist, part1, part_slots, st),
                   "merge_query launch");
@@ -225,9 +254,24 @@ herald_status run_stage2(const herald_dims& dm, const uint16_t* q_block, const u
                          int C, int K, int sink, int local, int P_max, int32_t* idx,
                          int32_t* n_sel, void* ws, const WsLayout& w, cudaStream_t st) {
   uint32_t* err = at<uint32_t>(ws, w.err);
-  HERALD_TRY_CUDA(launch_refine(dm, q_block, k_cache, cand, n_cand, C, at<float2>(ws, w.rpart),
-                                at<float>(ws, w.s2), w, err, st),
-                  "refine launch");
+  if (is_device_memory(k_cache)) {
+    HERALD_TRY_CUDA(launch_refine(dm, q_block, k_cache, cand, n_cand, C, at<float2>(ws, w.rpart),
+                                  at<float>(ws, w.s2), w, err, st),
+                    "refine launch");
+  } else {
+    // a host-resident cache: the candidate K rows cross the host link once,
+    // in one wide gather, into the workspace; the refine then reads them
+    // from HBM by slot (the stage-1 logits region is free during stage 2)
+    uint16_t* kstage = at<uint16_t>(ws, w.logits);
+    HERALD_TRY_CUDA(launch_gather(dm, cand, n_cand, C, k_cache, nullptr, kstage, nullptr, st,
+                                  "gather_kernel (candidate staging)"),
+                    "candidate staging launch");
+    herald_dims staged = dm;
+    staged.L_max = C;  // rows per (sequence, KV head) in the staging buffer
+    HERALD_TRY_CUDA(launch_refine(staged, q_block, kstage, nullptr, n_cand, C,
+                                  at<float2>(ws, w.rpart), at<float>(ws, w.s2), w, err, st),
+                    "refine launch");
+  }
   const int n_parts = refine_fused_ok(C) ? w.MT : 1;
   HERALD_TRY_CUDA(launch_topk_union(dm, ctx_len, cand, n_cand, at<float>(ws, w.s2), n_parts, C, K,
                                     sink, local, P_max, idx, n_sel, st),
@@ -357,10 +401,11 @@ herald_status herald_workspace_error(void* ws, void* stream, uint32_t* code) {
 herald_status herald_select_stage1(herald_dims dims, const uint16_t* q_merge,
                                    const uint16_t* k_cache, const int32_t* ctx_len, int C,
                                    int32_t* cand, int32_t* n_cand, void* ws, size_t ws_bytes,
-                                   void* stream) {
+                                   int sm_budget, void* stream) {
   g_err[0] = 0;
   HERALD_RET_IF(check_dims(dims));
   HERALD_RET_IF(check_c(C));
+  if (sm_budget < 0) return fail(HERALD_ERR_INVALID_ARG, "sm_budget=%d must be >= 0", sm_budget);
   HERALD_CHECK_PTR(q_merge);
   HERALD_CHECK_PTR(k_cache);
   HERALD_CHECK_PTR(ctx_len);
@@ -368,7 +413,7 @@ herald_status herald_select_stage1(herald_dims dims, const uint16_t* q_merge,
   HERALD_CHECK_PTR(n_cand);
   WsLayout w;
   HERALD_RET_IF(check_ws(dims, C, 1, ws, ws_bytes, &w));
-  return run_stage1(dims, q_merge, k_cache, ctx_len, C, cand, n_cand, ws, w,
+  return run_stage1(dims, q_merge, k_cache, ctx_len, C, cand, n_cand, ws, w, sm_budget,
                     static_cast<cudaStream_t>(stream));
 }
 
@@ -415,7 +460,7 @@ herald_status herald_select(herald_dims dims, const uint16_t* q_merge, const uin
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int32_t* cand = at<int32_t>(ws, w.cand);
   int32_t* n_cand = at<int32_t>(ws, w.n_cand);
-  HERALD_RET_IF(run_stage1(dims, q_merge, k_cache, ctx_len, C, cand, n_cand, ws, w, st));
+  HERALD_RET_IF(run_stage1(dims, q_merge, k_cache, ctx_len, C, cand, n_cand, ws, w, 0, st));
   return run_stage2(dims, q_block, k_cache, ctx_len, cand, n_cand, C, K, sink, local, P_max, idx,
                     n_sel, ws, w, st);
 }
@@ -457,18 +502,27 @@ herald_status herald_denoise_attn(herald_dims dims, const uint16_t* q, const uin
   WsLayout w;
   HERALD_RET_IF(check_ws(dims, 1, P_max, ws, ws_bytes, &w));
   if (scale == 0.f) scale = 1.0f / sqrtf(float(dims.d));
-  CUtensorMap kmap, vmap;
-  const bool pool_maps = attn_pool_ok(dims, P_max);
-  if (pool_maps) {
+  PoolMaps maps;
+  const bool pool = attn_pool_ok(dims, P_max);
+  if (pool) {
     const uint64_t rows = uint64_t(dims.N) * dims.Hkv * P_max;
     const uint32_t box = uint32_t(attn_pool_kpc(P_max));
-    HERALD_RET_IF(encode_rows_map(pool_k, rows, dims.d, box, &kmap));
-    HERALD_RET_IF(encode_rows_map(pool_v, rows, dims.d, box, &vmap));
+    HERALD_RET_IF(encode_rows_map(pool_k, rows, dims.d, box, &maps.k));
+    HERALD_RET_IF(encode_rows_map(pool_v, rows, dims.d, box, &maps.v));
+    maps.bpt = attn_pool_bpt(dims);
+    const int G = dims.Hq / dims.Hkv, Bp = (dims.B + 15) & ~15;
+    const uint64_t tokens = uint64_t(dims.N) * dims.B;
+    HERALD_RET_IF(encode_heads_map(q, tokens, dims.Hq, dims.d, uint32_t(G),
+                                   uint32_t(maps.bpt), &maps.q));
+    HERALD_RET_IF(encode_heads_map(block_k, tokens, dims.Hkv, dims.d, 1u, uint32_t(Bp),
+                                   &maps.bk));
+    HERALD_RET_IF(encode_heads_map(block_v, tokens, dims.Hkv, dims.d, 1u, uint32_t(Bp),
+                                   &maps.bv));
   }
   HERALD_TRY_CUDA(launch_attn(dims, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale,
                               w, at<float>(ws, w.opart), at<float2>(ws, w.ml),
-                              at<uint32_t>(ws, w.err), pool_maps ? &kmap : nullptr,
-                              pool_maps ? &vmap : nullptr, static_cast<cudaStream_t>(stream)),
+                              at<uint32_t>(ws, w.err), pool ? &maps : nullptr,
+                              static_cast<cudaStream_t>(stream)),
                   "attention launch");
   return HERALD_OK;
 }

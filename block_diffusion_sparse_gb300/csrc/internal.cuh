@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
+#include <algorithm>
 #include <stdint.h>
 
 #include "../../include/herald.h"
@@ -37,7 +38,9 @@ struct WsLayout {
   size_t err;        // uint32 device error word
   size_t qbar;       // float [N][Hq][d]        merged queries, pre-scaled
   size_t qhl;        // bf16 [N*Hkv][16][d]     merged queries as hi/lo bf16 rows
-  size_t logits;     // float [N][Hq][L_pad]    stage-1 logits
+  size_t logits;     // float [N][Hq][L_pad]    stage-1 logits; in stage 2 the same
+                     // bytes hold bf16 [N*Hkv][C][d] candidate K rows staged from
+                     // a host-resident cache (the region has room for both)
   size_t part1;      // float2 [N][Hq][kPartSlots] per-(CTA, warp) (max, sumexp)
   size_t s1;         // float [N][Hkv][L_pad]   stage-1 scores
   size_t hist;       // uint32 [N*Hkv][kHistBins]
@@ -67,7 +70,7 @@ inline WsLayout ws_layout(const herald_dims& dm, int C, int P_max) {
   w.err = o;    o = align_up(o + 16, A);
   w.qbar = o;   o = align_up(o + NH * dm.d * 4, A);
   w.qhl = o;    o = align_up(o + NG * kQhlRows * dm.d * 2, A);
-  w.logits = o; o = align_up(o + NH * w.L_pad * 4, A);
+  w.logits = o; o = align_up(o + std::max(NH * w.L_pad * 4, NG * size_t(C) * dm.d * 2), A);
   w.part1 = o;  o = align_up(o + NH * kPartSlots * 8, A);
   w.s1 = o;     o = align_up(o + NG * w.L_pad * 4, A);
   w.hist = o;   o = align_up(o + NG * kHistBins * 4, A);
@@ -146,20 +149,30 @@ cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const i
                               const int32_t* n_cand, const float* s2, int n_parts, int C, int K,
                               int S, int W, int P_max, int32_t* idx, int32_t* n_sel,
                               cudaStream_t st);
+// (name: the label the launch carries in traces)
 cudaError_t launch_gather(const herald_dims& dm, const int32_t* idx, const int32_t* n_sel,
                           int P_max, const uint16_t* k_cache, const uint16_t* v_cache,
-                          uint16_t* pool_k, uint16_t* pool_v, cudaStream_t st);
-// Pool attention (balanced 8-CTA clusters, TMA-loaded pool slices) applies
-// when attn_pool_ok(); it needs the pool K and V as 2-D tensor maps
-// [N*Hkv*P_max][d] with a box of 64 columns x attn_pool_kpc(P_max) rows.
+                          uint16_t* pool_k, uint16_t* pool_v, cudaStream_t st,
+                          const char* name = "gather_kernel");
+// Pool attention (balanced 8-CTA clusters, every operand loaded by TMA)
+// applies when attn_pool_ok(); its tensor maps, all bf16 with a box of 64
+// columns and 128-byte swizzle:
+//   k, v   pool rows [N*Hkv*P_max][d], box rows attn_pool_kpc(P_max)
+//   q      queries [N*B][Hq][d], box {G heads, bpt tokens}
+//   bk, bv block keys / values [N*B][Hkv][d], box {1 head, B rounded to 16}
+// Row tiles hold bpt = attn_pool_bpt() whole tokens (bpt * G <= 128 rows).
+struct PoolMaps {
+  CUtensorMap k, v, q, bk, bv;
+  int bpt;
+};
 int attn_pool_kpc(int P_max);
+int attn_pool_bpt(const herald_dims& dm);
 bool attn_pool_ok(const herald_dims& dm, int P_max);
 cudaError_t launch_attn(const herald_dims& dm, const uint16_t* q, const uint16_t* pool_k,
                         const uint16_t* pool_v, const int32_t* n_sel, int P_max,
                         const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
                         float scale, const WsLayout& w, float* opart, float2* ml, uint32_t* err,
-                        const CUtensorMap* pool_kmap, const CUtensorMap* pool_vmap,
-                        cudaStream_t st);
+                        const PoolMaps* maps, cudaStream_t st);
 cudaError_t launch_append(const herald_dims& dm, const uint16_t* block_k, const uint16_t* block_v,
                           int32_t* ctx, uint16_t* k_cache, uint16_t* v_cache, int advance,
                           cudaStream_t st);

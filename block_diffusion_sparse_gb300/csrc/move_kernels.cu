@@ -19,7 +19,8 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
 }
 
 // grid (ceil(P_max / rows_per_cta), N*Hkv), block 256; D/8 threads per row,
-// one 16-byte chunk each.
+// one 16-byte chunk each.  With vc == nullptr only K rows are copied (the
+// stage-2 staging of candidate rows from a host-resident cache).
 template <int D>
 __global__ void __launch_bounds__(256)
     gather_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ n_sel, int P_max,
@@ -37,24 +38,25 @@ __global__ void __launch_bounds__(256)
     if (pos >= 0 && pos < L_max) {
       const size_t off = (size_t(seg) * L_max + pos) * D + c * 8;
       kv = ld_nc_v4(kc + off);
-      vv = ld_nc_v4(vc + off);
+      if (vc) vv = ld_nc_v4(vc + off);
     }
   }
   const size_t dst = (size_t(seg) * P_max + row) * D + c * 8;
   *reinterpret_cast<uint4*>(pk + dst) = kv;
-  *reinterpret_cast<uint4*>(pv + dst) = vv;
+  if (vc) *reinterpret_cast<uint4*>(pv + dst) = vv;
 }
 
 cudaError_t launch_gather(const herald_dims& dm, const int32_t* idx, const int32_t* n_sel,
                           int P_max, const uint16_t* k_cache, const uint16_t* v_cache,
-                          uint16_t* pool_k, uint16_t* pool_v, cudaStream_t st) {
+                          uint16_t* pool_k, uint16_t* pool_v, cudaStream_t st,
+                          const char* name) {
   const int segs = dm.N * dm.Hkv;
   if (dm.d == 128)
-    HERALD_CHECK_LAUNCH(launch_k("gather_kernel", gather_kernel<128>, dim3(cdiv(P_max, 16), segs), 256, 0, st, idx, n_sel, P_max, dm.L_max,
+    HERALD_CHECK_LAUNCH(launch_k(name, gather_kernel<128>, dim3(cdiv(P_max, 16), segs), 256, 0, st, idx, n_sel, P_max, dm.L_max,
                                                                      k_cache, v_cache, pool_k,
                                                                      pool_v));
   else
-    HERALD_CHECK_LAUNCH(launch_k("gather_kernel", gather_kernel<64>, dim3(cdiv(P_max, 32), segs), 256, 0, st, idx, n_sel, P_max, dm.L_max,
+    HERALD_CHECK_LAUNCH(launch_k(name, gather_kernel<64>, dim3(cdiv(P_max, 32), segs), 256, 0, st, idx, n_sel, P_max, dm.L_max,
                                                                     k_cache, v_cache, pool_k,
                                                                     pool_v));
   return cudaGetLastError();

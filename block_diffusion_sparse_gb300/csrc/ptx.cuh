@@ -104,6 +104,15 @@ HERALD_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, in
       : "memory");
 }
 
+HERALD_DEV void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                            int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
 // Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to a
 // shared::cluster address (another CTA of the cluster), completing as
 // transaction bytes on the destination CTA's mbarrier (a shared::cluster

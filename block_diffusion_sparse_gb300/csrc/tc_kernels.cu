@@ -175,9 +175,9 @@ __global__ void __launch_bounds__(kTcThreads)
     return q_block + ((size_t(n) * B + b) * Hq + g * G + hl) * D;
   });
   // candidate positions first (one coalesced load), then the row copies
-  const int32_t* cd = cand + size_t(seg) * C;
+  const int32_t* cd = cand ? cand + size_t(seg) * C : nullptr;  // null: row = slot
   for (int r = threadIdx.x; r < kRefineChunk; r += kTcThreads)
-    pos[r] = c0 + r < nc ? cd[c0 + r] : -1;
+    pos[r] = c0 + r < nc ? (cand ? cd[c0 + r] : c0 + r) : -1;
   // positions outside the cache (a caller error) read as zero rows
   for (int r = threadIdx.x; r < kRefineChunk; r += kTcThreads)
     if (pos[r] >= L_max) pos[r] = -1;
@@ -282,9 +282,9 @@ __global__ void __launch_bounds__(kTcThreads)
   tmem_setup(&tmem_base, 256);
   const uint32_t tbase = tmem_base;
 
-  const int32_t* cd = cand + size_t(seg) * C;
+  const int32_t* cd = cand ? cand + size_t(seg) * C : nullptr;  // null: row = slot
   for (int r = threadIdx.x; r < kRefineRows2; r += kTcThreads)
-    pos[r] = (c0 + r < nc && cd[c0 + r] < L_max) ? cd[c0 + r] : -1;
+    pos[r] = c0 + r >= nc ? -1 : !cand ? c0 + r : cd[c0 + r] < L_max ? cd[c0 + r] : -1;
   __syncthreads();
   load_rows_sw128<D>(Ks, kRefineRows2, kRefineRows2, kc, [&](int r) -> const uint16_t* {
     const int p = pos[r];
@@ -421,9 +421,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int nc = min(max(n_cand[seg], 0), C);
   const int c0 = int(rank) * cpc;
   const int ncv = min(max(nc - c0, 0), cpc);  // valid candidates of this CTA
-  const int32_t* cd = cand + size_t(seg) * C;
+  const int32_t* cd = cand ? cand + size_t(seg) * C : nullptr;  // null: row = slot
   for (int r = threadIdx.x; r < cpc; r += kTcThreads) {
-    const int p = r < ncv ? cd[c0 + r] : -1;
+    const int p = r < ncv ? (cand ? cd[c0 + r] : c0 + r) : -1;
     pos[r] = (p >= 0 && p < L_max) ? p : -1;
   }
   __syncthreads();
@@ -1059,10 +1059,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 // ============================================================= attn_pool
-// Sparse block attention, one 8-CTA cluster per (sequence, KV head, 128-row
-// tile).  The pool is split evenly: CTA r owns pool keys [r*kpc, (r+1)*kpc)
-// (kpc = ceil(P_max/8) rounded to 16, at most 192), loaded by two 2-D TMA
-// boxes each for K and V; the last CTA also owns the B block keys.  Each
+// Sparse block attention, one 8-CTA cluster per (sequence, KV head, row
+// tile of bpt whole tokens = bpt*G <= 128 query rows).  The pool is split
+// evenly: CTA r owns pool keys [r*kpc, (r+1)*kpc) (kpc = ceil(P_max/8)
+// rounded to 16, kpc + B <= 256), loaded by two 2-D TMA boxes each for K and
+// V; the last CTA also owns the B block keys.  The query tile and the block
+// keys and values are 3-D TMA boxes (every operand is one bulk transfer,
+// issued by one thread as soon as the predecessor kernel is done).  Each
 // CTA computes S = Q K^T for its keys with one UMMA (N = kpc), P = exp(S -
 // rowmax) in bf16 (written over the Q/K operands, dead once S is in TMEM),
 // O = P V into TMEM.  Rows are finalised 16 per CTA: each CTA stages its O
@@ -1074,8 +1077,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // separates the attention from the exchange.
 constexpr int kPoolCtas = 8;
 constexpr int kPoolRows = kTileM / kPoolCtas;   // rows finalised per CTA
-constexpr int kPoolMaxKpc = 192;
 constexpr int kPoolMaxB = 64;
+// S takes TMEM columns [0, kpc + Bp) and O starts at column 256
+constexpr int kPoolMaxCols = 256;
 
 struct PoolSmem {
   uint32_t q, k, kb, p, pb, v, vb, recv_o, recv_ml, total;
@@ -1102,11 +1106,12 @@ __host__ __device__ inline PoolSmem pool_smem(int D, int kpc, int Bp) {
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_pool_kernel(const __grid_constant__ CUtensorMap kmap,
-                     const __grid_constant__ CUtensorMap vmap, const uint16_t* __restrict__ q,
-                     const int32_t* __restrict__ n_sel, int P_max,
-                     const uint16_t* __restrict__ block_k, const uint16_t* __restrict__ block_v,
-                     int B, int Hq, int Hkv, int R, int kpc, float scale,
-                     uint16_t* __restrict__ out, uint32_t* err) {
+                     const __grid_constant__ CUtensorMap vmap,
+                     const __grid_constant__ CUtensorMap qmap,
+                     const __grid_constant__ CUtensorMap bkmap,
+                     const __grid_constant__ CUtensorMap bvmap,
+                     const int32_t* __restrict__ n_sel, int P_max, int B, int Hq, int Hkv,
+                     int bpt, int kpc, float scale, uint16_t* __restrict__ out, uint32_t* err) {
   constexpr int H = D / 64;
   constexpr int OROW = D + 8;  // fp16 row stride of O partials (16-byte padding)
   extern __shared__ uint8_t smem_raw[];
@@ -1145,56 +1150,72 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // peers' copies complete on barR: its initialisation is published
   // cluster-wide here and awaited just before the first copy is issued
   __cluster_barrier_arrive_relaxed();
+  if (threadIdx.x == 0) {  // kernel parameters: independent of the predecessor
+    tma_prefetch_desc(&qmap);
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+    tma_prefetch_desc(&bkmap);
+    tma_prefetch_desc(&bvmap);
+  }
   tmem_setup(&tmem_base, 512);
   const uint32_t tbase = tmem_base;
+  const int b0 = mt * bpt;                  // first token of the tile
+  const int rows_t = min(bpt, B - b0) * G;  // query rows of the tile
   griddep_enter();
+  // barK: Q + pool K (if any) + block K (last CTA); barV: pool V + block V.
+  // The query tile goes first, before n_sel is known (its bytes may
+  // complete on barK before they are expected: the phase still needs the
+  // arrive below).  Boxes past the tensor's end are zero-filled; rows past
+  // this tile's tokens or past the valid keys are never used.
+  const uint32_t qbytes = uint32_t(H * G * bpt * 128);
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int hv = 0; hv < H; ++hv)
+      tma_load_3d(Qs + hv * kTileM * 128, &qmap, &barK, hv * 64, g * G, n * B + b0);
+  }
   const int ns = min(max(n_sel[seg], 0), P_max);
   const int k0 = int(rank) * kpc;
   const int nkp = min(max(ns - k0, 0), kpc);           // valid pool keys of this CTA
   const bool has_blk = rank == kPoolCtas - 1 && B > 0;  // the block keys
   const bool any = nkp > 0 || has_blk;
-
-  if (threadIdx.x == 0 && nkp > 0) {
-    tma_prefetch_desc(&kmap);
-    tma_prefetch_desc(&vmap);
-    mbar_arrive_expect_tx(&barK, uint32_t(H * kpc * 128));
+  if (threadIdx.x == 0) {
+    const uint32_t kb = nkp > 0 ? uint32_t(H * kpc * 128) : 0u;
+    const uint32_t bb = has_blk ? uint32_t(H * Bp * 128) : 0u;
+    mbar_arrive_expect_tx(&barK, qbytes + kb + bb);
+    if (nkp > 0) {
 #pragma unroll
-    for (int hv = 0; hv < H; ++hv)
-      tma_load_2d(Ks + hv * kpc * 128, &kmap, &barK, hv * 64, seg * P_max + k0);
-    mbar_arrive_expect_tx(&barV, uint32_t(H * kpc * 128));
-#pragma unroll
-    for (int hv = 0; hv < H; ++hv)
-      tma_load_2d(Vs + hv * kpc * 128, &vmap, &barV, hv * 64, seg * P_max + k0);
-  }
-  if (any) {
-    load_rows_sw128<D>(Qs, kTileM, kTileM, q, [&](int r) -> const uint16_t* {
-      const int rr = mt * kTileM + r;
-      if (rr >= R) return nullptr;
-      const int b = rr / G, hl = rr - (rr / G) * G;
-      return q + ((size_t(n) * B + b) * Hq + g * G + hl) * D;
-    });
-    if (has_blk) {
-      load_rows_sw128<D>(Kb, Bp, Bp, block_k, [&](int r) -> const uint16_t* {
-        return r < B ? block_k + ((size_t(n) * B + r) * Hkv + g) * D : nullptr;
-      });
-      load_rows_sw128<D>(Vb, Bp, Bp, block_v, [&](int r) -> const uint16_t* {
-        return r < B ? block_v + ((size_t(n) * B + r) * Hkv + g) * D : nullptr;
-      });
+      for (int hv = 0; hv < H; ++hv)
+        tma_load_2d(Ks + hv * kpc * 128, &kmap, &barK, hv * 64, seg * P_max + k0);
     }
-    cp_async_commit();
-    cp_async_wait_all();
-    fence_proxy_async_smem();
+    if (has_blk) {
+#pragma unroll
+      for (int hv = 0; hv < H; ++hv)
+        tma_load_3d(Kb + hv * Bp * 128, &bkmap, &barK, hv * 64, g, n * B);
+    }
+    if (nkp > 0 || has_blk) {
+      mbar_arrive_expect_tx(&barV, kb + bb);
+      if (nkp > 0) {
+#pragma unroll
+        for (int hv = 0; hv < H; ++hv)
+          tma_load_2d(Vs + hv * kpc * 128, &vmap, &barV, hv * 64, seg * P_max + k0);
+      }
+      if (has_blk) {
+#pragma unroll
+        for (int hv = 0; hv < H; ++hv)
+          tma_load_3d(Vb + hv * Bp * 128, &bvmap, &barV, hv * 64, g, n * B);
+      }
+    }
   }
-  __syncthreads();
-  tc_fence_after();
 
-  // S = Q [K ; K_block]^T -> TMEM columns [0, kpc) and [kpc, kpc + Bp)
+  // S = Q [K ; K_block]^T -> TMEM columns [0, kpc) and [kpc, kpc + Bp).
+  // Every CTA waits for its query tile, used or not: no copy may still be
+  // writing this CTA's shared memory when it exits.
   bool ok = true;
+  if (threadIdx.x == 0) ok = mbar_wait(&barK, 0);
   if (threadIdx.x == 0 && any) {
     const uint32_t qa = smem_u32(Qs);
+    tc_fence_after();
     if (nkp > 0) {
-      ok = mbar_wait(&barK, 0);
-      tc_fence_after();
       const uint32_t idesc = make_idesc_bf16(kTileM, kpc, false, false);
       const uint32_t ka = smem_u32(Ks);
 #pragma unroll
@@ -1232,7 +1253,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int nchunks = any ? (kpc + (has_blk ? Bp : 0)) / 16 : 0;
   const int half = (nchunks + 1) / 2;
   const int c_begin = ch == 0 ? 0 : half, c_end = ch == 0 ? half : nchunks;
-  constexpr int kMaxChunks = (kPoolMaxKpc + kPoolMaxB) / 32;  // per half
+  constexpr int kMaxChunks = kPoolMaxCols / 32;  // 16-column chunks per half
   const float sl2 = scale * 1.4426950408889634f;              // scores -> log2 units
   float x[kMaxChunks][16];
   int nv[kMaxChunks];  // valid keys per chunk (warp-uniform)
@@ -1303,9 +1324,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0 && any) {
     constexpr uint32_t idesc = make_idesc_bf16(kTileM, D, false, true);
     bool acc = false;
+    ok = mbar_wait(&barV, 0) && ok;
+    tc_fence_after();
     if (nkp > 0) {
-      ok = mbar_wait(&barV, 0) && ok;
-      tc_fence_after();
       const uint32_t pa = smem_u32(Ps), va = smem_u32(Vs);
       for (int s = 0; s < kpc / 16; ++s) {
         const uint64_t a =
@@ -1378,7 +1399,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr int E = D / 32;
   for (int rr = warp; rr < kPoolRows; rr += kTcThreads / 32) {
     const int lr = int(rank) * kPoolRows + rr;
-    const int grow = mt * kTileM + lr;
+    if (lr >= rows_t) break;  // warp-uniform: rows past the tile's tokens
+    const int grow = b0 * G + lr;
     float M = -INFINITY;
     float2 pm[kPoolCtas];
 #pragma unroll
@@ -1398,7 +1420,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
       for (int e = 0; e < E; ++e) acc[e] += wgt * __half2float(o[e]);
     }
-    if (grow < R) {
+    {
       const int b = grow / G, h = g * G + (grow - (grow / G) * G);
       uint16_t* dstp = out + ((size_t(n) * B + b) * Hq + h) * D + lane * E;
       const float inv = L > 0.f ? 1.f / L : 0.f;
@@ -1501,12 +1523,13 @@ static int max_active_clusters() {
 }
 
 int attn_pool_kpc(int P_max) { return cdiv(cdiv(P_max, kPoolCtas), 16) * 16; }
+int attn_pool_bpt(const herald_dims& dm) { return kTileM / (dm.Hq / dm.Hkv); }
 
 bool attn_pool_ok(const herald_dims& dm, int P_max) {
   const int kpc = attn_pool_kpc(P_max);
   const int Bp = (dm.B + 15) & ~15;
   // the dynamic allocation plus the kernel's static shared memory (~3 KB)
-  return kpc <= kPoolMaxKpc && dm.B <= kPoolMaxB &&
+  return kpc + Bp <= kPoolMaxCols && Bp <= kPoolMaxB &&
          pool_smem(dm.d, kpc, Bp).total <= 220u * 1024u;
 }
 
@@ -1515,11 +1538,10 @@ static cudaError_t launch_attn_t(const herald_dims& dm, const uint16_t* q, const
                                  const uint16_t* pool_v, const int32_t* n_sel, int P_max,
                                  const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
                                  float scale, const WsLayout& w, float* opart, float2* ml,
-                                 uint32_t* err, const CUtensorMap* pool_kmap,
-                                 const CUtensorMap* pool_vmap, cudaStream_t st) {
+                                 uint32_t* err, const PoolMaps* maps, cudaStream_t st) {
   const int segs = dm.N * dm.Hkv;
   cudaError_t e;
-  if (pool_kmap && pool_vmap && !force_split()) {
+  if (maps && !force_split()) {
     const int kpc = attn_pool_kpc(P_max);
     const uint32_t smem = pool_smem(D, kpc, (dm.B + 15) & ~15).total;
     static uint32_t attr_bytes = 0;  // dynamic shared memory granted so far
@@ -1529,9 +1551,10 @@ static cudaError_t launch_attn_t(const herald_dims& dm, const uint16_t* q, const
       if (e != cudaSuccess) return e;
       attr_bytes = smem;
     }
-    return launch_cluster("attn_pool_kernel", attn_pool_kernel<D>, dim3(kPoolCtas, w.MT, segs),
-                          kPoolCtas, smem, st, *pool_kmap, *pool_vmap, q, n_sel, P_max, block_k,
-                          block_v, dm.B, dm.Hq, dm.Hkv, w.R, kpc, scale, out, err);
+    const int tiles = cdiv(dm.B, maps->bpt);
+    return launch_cluster("attn_pool_kernel", attn_pool_kernel<D>, dim3(kPoolCtas, tiles, segs),
+                          kPoolCtas, smem, st, maps->k, maps->v, maps->q, maps->bk, maps->bv,
+                          n_sel, P_max, dm.B, dm.Hq, dm.Hkv, maps->bpt, kpc, scale, out, err);
   }
   static bool attr = false;
   if (!attr) {
@@ -1575,13 +1598,12 @@ cudaError_t launch_attn(const herald_dims& dm, const uint16_t* q, const uint16_t
                         const uint16_t* pool_v, const int32_t* n_sel, int P_max,
                         const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
                         float scale, const WsLayout& w, float* opart, float2* ml, uint32_t* err,
-                        const CUtensorMap* pool_kmap, const CUtensorMap* pool_vmap,
-                        cudaStream_t st) {
+                        const PoolMaps* maps, cudaStream_t st) {
   if (dm.d == 128)
     return launch_attn_t<128>(dm, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale,
-                              w, opart, ml, err, pool_kmap, pool_vmap, st);
+                              w, opart, ml, err, maps, st);
   return launch_attn_t<64>(dm, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale, w,
-                           opart, ml, err, pool_kmap, pool_vmap, st);
+                           opart, ml, err, maps, st);
 }
 
 }  // namespace herald

@@ -68,7 +68,7 @@ def lib() -> C.CDLL:
         L.herald_last_error.argtypes = []
         L.herald_last_error.restype = C.c_char_p
         L.herald_workspace_error.argtypes = [vp, vp, C.POINTER(C.c_uint32)]
-        L.herald_select_stage1.argtypes = [Dims, vp, vp, vp, i32, vp, vp, vp, sz, vp]
+        L.herald_select_stage1.argtypes = [Dims, vp, vp, vp, i32, vp, vp, vp, sz, i32, vp]
         L.herald_select_stage2.argtypes = [Dims, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                            vp, vp, vp, sz, vp]
         L.herald_select.argtypes = [Dims, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp,
@@ -165,10 +165,10 @@ def herald_workspace_error(ws, stream=None) -> int:
 
 
 def herald_select_stage1(d, q_merge, k_cache, ctx_len, C_, cand, n_cand, ws, ws_bytes=None,
-                         stream=None):
+                         stream=None, sm_budget=0):
     _check(lib().herald_select_stage1(d, _p(q_merge), _p(k_cache), _p(ctx_len), int(C_),
                                       _p(cand), _p(n_cand), _p(ws), _nbytes(ws, ws_bytes),
-                                      _s(stream)))
+                                      int(sm_budget), _s(stream)))
 
 
 def herald_select_stage2(d, q_block, k_cache, ctx_len, cand, n_cand, C_, K, sink, local, P_max,

@@ -26,11 +26,26 @@ from __future__ import annotations
 from . import herald as H
 
 
+def background_sms(dims: H.Dims) -> int:
+    """SMs the overlapped stage-1 scan may keep busy: all but those one
+    attention launch of the denoising stream occupies (8 CTAs per KV head
+    and row tile of whole tokens), and at least half of the device."""
+    import torch
+    nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    G = dims.Hq // dims.Hkv
+    tiles = -(-dims.B // (128 // G))
+    attn_ctas = 8 * tiles * dims.N * dims.Hkv
+    return nsm - min(nsm // 2, attn_ctas)
+
+
 class BlockPipeline:
     def __init__(self, dims: H.Dims, C: int, K: int, S: int, W: int, P: int, T: int,
-                 den_stream=None, sel_stream=None):
+                 den_stream=None, sel_stream=None, sel_sms=None):
         import torch
         self.torch = torch
+        # SMs the overlapped stage-1 scan may occupy (0: all); measured on the
+        # bench workloads, confining it did not shorten the step
+        self.sel_sms = 0 if sel_sms is None else int(sel_sms)
         self.d, self.C, self.K, self.S, self.W, self.P, self.T = dims, C, K, S, W, P, T
         NG = (dims.N, dims.Hkv)
         dev = "cuda"
@@ -86,7 +101,8 @@ class BlockPipeline:
                                    self.K, self.S, self.W, P, self._idx, self._n_sel, wd, wb, hd))
         chk(L.herald_gather(d, self._idx, self._n_sel, P, kc, vc, pk, pv, hd))
         chk(L.herald_select_stage1(d, q0, H.ptr(nk), cx, self.C, self._cand[nxt],
-                                   self._n_cand[nxt], self._ws_sel, wb, hs if overlap else hd))
+                                   self._n_cand[nxt], self._ws_sel, wb,
+                                   self.sel_sms if overlap else 0, hs if overlap else hd))
         for t in range(self.T):
             chk(L.herald_denoise_attn(d, q0 + t * qstep, pk, pv, self._n_sel, P, bk0 + t * bstep,
                                       bv0 + t * bstep, o0 + t * ostep, 0.0, wd, wb, hd))
@@ -136,6 +152,7 @@ class StackPipeline:
         self.pool_v = [[mk((*NG, P, dims.d), torch.int16) for _ in range(2)]
                        for _ in range(n_layers)]
         self.sel = sel_stream if sel_stream is not None else torch.cuda.Stream()
+        self.sel_sms = 0
 
     def prime(self, q_merge, k_caches, ctx, slot: int = 0):
         st = self.torch.cuda.current_stream()
@@ -170,7 +187,8 @@ class StackPipeline:
                         with torch.cuda.stream(sel):
                             H.herald_select_stage1(d, q_steps[l][0], k_caches[l], ctx, self.C,
                                                    self.cand[l][nxt], self.n_cand[l][nxt],
-                                                   self.ws_sel, self.ws_bytes, sel)
+                                                   self.ws_sel, self.ws_bytes, sel,
+                                                   sm_budget=self.sel_sms)
                     else:
                         H.herald_select_stage1(d, q_steps[l][0], k_caches[l], ctx, self.C,
                                                self.cand[l][nxt], self.n_cand[l][nxt],

@@ -92,11 +92,16 @@ herald_status herald_workspace_error(void *ws, void *stream, uint32_t *code);
  *           the largest stage-1 score s1[j] = sum over the group's heads of
  *           softmax_j(qbar_h . k_j / sqrt(d)) ([SPD] S_tgt), ascending,
  *           padded with -1.
- *   n_cand  [N][Hkv] int32 device out: min(C, ctx). */
+ *   n_cand  [N][Hkv] int32 device out: min(C, ctx).
+ *   sm_budget  the most SMs the cache scan keeps busy at once; 0 = all.
+ *           A caller that runs stage 1 beside other work (the dual-stream
+ *           pipeline of [EA] overlaps it with denoising) leaves the other
+ *           SMs to that work: the scan is persistent and would otherwise
+ *           hold every SM for its duration.  Negative values are invalid. */
 herald_status herald_select_stage1(herald_dims dims, const uint16_t *q_merge,
                                    const uint16_t *k_cache, const int32_t *ctx_len, int C,
                                    int32_t *cand, int32_t *n_cand, void *ws, size_t ws_bytes,
-                                   void *stream);
+                                   int sm_budget, void *stream);
 
 /* Stage 2 of the selection [V3] plus sink/local [SPD InfLLM-V2 decomposition].
  *   q_block [N][B][Hq][d] bf16 device: the real queries of the block being

@@ -79,9 +79,9 @@ class Run:
         self.pool_v = torch.full((*NG, self.P, w.d), 99, dtype=torch.int16, device="cuda")
         self.out = torch.zeros((w.N, w.B, w.Hq, w.d), dtype=torch.int16, device="cuda")
 
-    def stage1(self):
+    def stage1(self, sm_budget=0):
         H.herald_select_stage1(self.d, self.q_merge, self.k, self.ctx, self.w.C, self.cand,
-                               self.n_cand, self.ws)
+                               self.n_cand, self.ws, sm_budget=sm_budget)
 
     def stage2(self, cand=None, n_cand=None):
         c = self.cand if cand is None else dev(np.asarray(cand, np.int32))
@@ -115,8 +115,19 @@ def _oracle_stage1(x):
 
 @pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
 def test_stage1_candidates(w):
+    _check_stage1(w, 0)
+
+
+@pytest.mark.parametrize("budget", [1, 7, 40])
+def test_stage1_candidates_with_an_sm_budget(budget):
+    """A scan confined to a few SMs (the background stage 1 of the
+    pipeline) selects the same candidates, up to the tie band."""
+    _check_stage1(CASES[1], budget)
+
+
+def _check_stage1(w, sm_budget):
     r = Run(w)
-    r.stage1()
+    r.stage1(sm_budget)
     torch.cuda.synchronize()
     assert r.error_word() == 0
     s1 = _oracle_stage1(r.x)
@@ -288,9 +299,17 @@ def test_append_matches_oracle_bit_exact():
     np.testing.assert_array_equal(vv, v2)
 
 
-def test_host_resident_cache_matches_device_cache():
-    w = _case("host-kv", Hq=8, Hkv=2, d=128, L=4096, B=32, C=512, K=128, S=16, W=64,
-              n_planted=10, index=21)
+@pytest.mark.parametrize("w", [
+    _case("host-kv", Hq=8, Hkv=2, d=128, L=4096, B=32, C=512, K=128, S=16, W=64,
+          n_planted=10, index=21),
+    # C > 4096: staged candidate rows feed the two-pass refine
+    _case("host-kv-two-pass", Hq=8, Hkv=2, d=128, L=6000, B=16, C=4600, K=256, S=16, W=64,
+          n_planted=10, index=24),
+], ids=lambda w: w.name)
+def test_host_resident_cache_matches_device_cache(w):
+    """A cache in pinned host memory (scanned over the host link, candidate
+    rows staged into the workspace for stage 2) selects and gathers exactly
+    what the same cache in device memory does."""
     r = Run(w)
     r.select()
     r.gather()
