@@ -598,9 +598,10 @@ def run_e2e(b, args, dist):
     """Every step: that step's inputs copied from pinned host memory to the
     device, the step through the C ABI (direct calls, no graph), its
     outputs copied back to pinned host memory -- all inside the timed
-    region.  The copies run on a copy stream against two alternating sets
-    of device buffers, so step i+1's inputs travel while step i computes
-    (the double buffering a serving loop would use)."""
+    region.  Inputs and outputs travel on two copy streams of their own
+    against two alternating sets of device buffers, so step i+1's inputs
+    arrive while step i computes (the double buffering a serving loop would
+    use)."""
     torch = b.torch
     w = b.w
     pin = lambda t: t.cpu().pin_memory()
@@ -614,31 +615,35 @@ def run_e2e(b, args, dist):
     h2d = sum(t.numel() * t.element_size() for t in (hq_m, hq_s, hbk, hbv))
     d2h = sum(t.numel() * t.element_size() for t in (o_out, o_idx, o_ns))
     comp = torch.cuda.current_stream()
-    cp = torch.cuda.Stream()
+    cp = torch.cuda.Stream()     # host -> device
+    cpo = torch.cuda.Stream()    # device -> host
     h2d_done = [torch.cuda.Event() for _ in range(2)]
     comp_done = [torch.cuda.Event() for _ in range(2)]
-    for e in h2d_done + comp_done:
+    out_done = [torch.cuda.Event() for _ in range(2)]
+    for e in h2d_done + comp_done + out_done:
         e.record(comp)
 
     def one(i):
         s = i % 2
         x = din[s]
         cp.wait_event(comp_done[s])  # the step that last read these inputs is done
+        comp.wait_event(out_done[s])  # ... and its output buffer has been read back
         with torch.cuda.stream(cp):
             x["q_m"].copy_(hq_m, non_blocking=True)
             x["q_s"].copy_(hq_s, non_blocking=True)
             x["bk"].copy_(hbk, non_blocking=True)
             x["bv"].copy_(hbv, non_blocking=True)
             h2d_done[s].record(cp)
-        comp.wait_event(h2d_done[s])  # (also orders this step after slot s's last read-back)
+        comp.wait_event(h2d_done[s])
         b.step(i % b.n_rot, q_merge=x["q_m"], q_steps=x["q_s"], bk=x["bk"], bv=x["bv"],
                out=dout[s])
         o_idx.copy_(b.idx, non_blocking=True)       # small: read back in stream order
         o_ns.copy_(b.n_sel_out, non_blocking=True)
         comp_done[s].record(comp)
-        cp.wait_event(comp_done[s])
-        with torch.cuda.stream(cp):
+        cpo.wait_event(comp_done[s])
+        with torch.cuda.stream(cpo):
             o_out.copy_(dout[s], non_blocking=True)
+        out_done[s].record(cpo)
 
     for i in range(args.warmup):
         one(i)
@@ -650,6 +655,7 @@ def run_e2e(b, args, dist):
     for i in range(args.steps):
         one(i)
     comp.wait_stream(cp)
+    comp.wait_stream(cpo)
     e1.record(comp)
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, "cuda")
@@ -657,8 +663,8 @@ def run_e2e(b, args, dist):
     return {"value": job_value(ms, world, w.N * w.B), "unit": "tokens/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": ms,
-            "path": "direct C-ABI calls (no graph); pinned host buffers, copies on a second "
-                    "stream into double-buffered device inputs/outputs"}
+            "path": "direct C-ABI calls (no graph); pinned host buffers, copies on two copy "
+                    "streams into double-buffered device inputs/outputs"}
 
 
 def main():

@@ -183,12 +183,10 @@ herald_status encode_rows_map(const void* base, uint64_t rows, int d, uint32_t b
   return encode_map(base, 2, ext, box, map);
 }
 
-// [tokens][heads][d] with a box of 64 columns x box_heads heads x box_tokens
-// tokens (query tiles and block keys / values of one KV head).
-herald_status encode_heads_map(const void* base, uint64_t tokens, int heads, int d,
-                               uint32_t box_heads, uint32_t box_tokens, CUtensorMap* map) {
-  const uint64_t ext[3] = {uint64_t(d), uint64_t(heads), tokens};
-  const uint32_t box[3] = {64, box_heads, box_tokens};
+// [tokens][heads][d] maps: herald::encode_heads_map, below (shared with the
+// workspace-free entry point).
+herald_status encode_map3(const void* base, const uint64_t* ext, const uint32_t* box,
+                          CUtensorMap* map) {
   return encode_map(base, 3, ext, box, map);
 }
 
@@ -254,9 +252,14 @@ herald_status run_stage2(const herald_dims& dm, const uint16_t* q_block, const u
                          int C, int K, int sink, int local, int P_max, int32_t* idx,
                          int32_t* n_sel, void* ws, const WsLayout& w, cudaStream_t st) {
   uint32_t* err = at<uint32_t>(ws, w.err);
+  CUtensorMap qmap;
+  const int G = dm.Hq / dm.Hkv;
+  const herald_status qs = encode_heads_map(q_block, uint64_t(dm.N) * dm.B, dm.Hq, dm.d,
+                                            uint32_t(G), uint32_t(kTileM / G), &qmap);
+  if (qs != HERALD_OK) return qs;
   if (is_device_memory(k_cache)) {
     HERALD_TRY_CUDA(launch_refine(dm, q_block, k_cache, cand, n_cand, C, at<float2>(ws, w.rpart),
-                                  at<float>(ws, w.s2), w, err, st),
+                                  at<float>(ws, w.s2), w, err, &qmap, st),
                     "refine launch");
   } else {
     // a host-resident cache: the candidate K rows cross the host link once,
@@ -269,10 +272,11 @@ herald_status run_stage2(const herald_dims& dm, const uint16_t* q_block, const u
     herald_dims staged = dm;
     staged.L_max = C;  // rows per (sequence, KV head) in the staging buffer
     HERALD_TRY_CUDA(launch_refine(staged, q_block, kstage, nullptr, n_cand, C,
-                                  at<float2>(ws, w.rpart), at<float>(ws, w.s2), w, err, st),
+                                  at<float2>(ws, w.rpart), at<float>(ws, w.s2), w, err, &qmap,
+                                  st),
                     "refine launch");
   }
-  const int n_parts = refine_fused_ok(C) ? w.MT : 1;
+  const int n_parts = refine_fused_ok(C) ? w.MT_tok : 1;
   HERALD_TRY_CUDA(launch_topk_union(dm, ctx_len, cand, n_cand, at<float>(ws, w.s2), n_parts, C, K,
                                     sink, local, P_max, idx, n_sel, st),
                   "topk_union launch");
@@ -316,6 +320,15 @@ thread_local TraceState g_trace;
 }  // namespace
 
 namespace herald {
+
+// [tokens][heads][d] with a box of 64 columns x box_heads heads x box_tokens
+// tokens (query tiles and block keys / values of one KV head).
+herald_status encode_heads_map(const void* base, uint64_t tokens, int heads, int d,
+                               uint32_t box_heads, uint32_t box_tokens, CUtensorMap* map) {
+  const uint64_t ext[3] = {uint64_t(d), uint64_t(heads), tokens};
+  const uint32_t box[3] = {64, box_heads, box_tokens};
+  return encode_map3(base, ext, box, map);
+}
 
 void set_last_error(const char* msg) { snprintf(g_err, sizeof g_err, "%s", msg); }
 

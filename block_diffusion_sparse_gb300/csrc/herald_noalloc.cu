@@ -89,7 +89,7 @@ herald_status herald_select_stage2_noalloc(herald_dims dims, const uint16_t* q_b
   const size_t rpart_off = 256;
   const size_t rpart_bytes = NG * size_t(full.MT) * kTileM * full.n_chunks * 8;
   const size_t s2_off = align_up(rpart_off + rpart_bytes, 256);
-  const int n_parts = refine_fused_ok(C) ? full.MT : 1;  // s2 partials per row tile
+  const int n_parts = refine_fused_ok(C) ? full.MT_tok : 1;  // s2 partials per row tile
   const size_t need = s2_off + NG * size_t(C) * 4 * size_t(n_parts);
   if (need > kStaticScratchBytes)
     return fail(HERALD_ERR_WORKSPACE_TOO_SMALL,
@@ -101,13 +101,20 @@ herald_status herald_select_stage2_noalloc(herald_dims dims, const uint16_t* q_b
   if (s != HERALD_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* err = reinterpret_cast<uint32_t*>(base + err_off);
+  // the fused refine reads its query tiles by TMA (a host-side descriptor,
+  // no device memory)
+  CUtensorMap qmap;
+  const int G = dims.Hq / dims.Hkv;
+  s = encode_heads_map(q_block, uint64_t(dims.N) * dims.B, dims.Hq, dims.d, uint32_t(G),
+                       uint32_t(kTileM / G), &qmap);
+  if (s != HERALD_OK) return s;
   // the array keeps the previous call's contents: the error word must start
   // at zero; the statistics and scores are fully rewritten before use
   cudaError_t e = cudaMemsetAsync(err, 0, sizeof(uint32_t), st);
   if (e == cudaSuccess)
     e = launch_refine(dims, q_block, k_cache, cand, n_cand, C,
                       reinterpret_cast<float2*>(base + rpart_off),
-                      reinterpret_cast<float*>(base + s2_off), full, err, st);
+                      reinterpret_cast<float*>(base + s2_off), full, err, &qmap, st);
   if (e == cudaSuccess)
     e = launch_topk_union(dims, ctx_len, cand, n_cand, reinterpret_cast<float*>(base + s2_off),
                           n_parts, C, K, sink, local, P_max, idx, n_sel, st);

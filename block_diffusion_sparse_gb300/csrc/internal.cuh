@@ -52,6 +52,7 @@ struct WsLayout {
   size_t ml;         // float2 [N*Hkv][MT][S][128]
   size_t total;
   int L_pad, tiles_per_seg, tiles128, R, MT, n_chunks, splits;
+  int MT_tok;        // row tiles of whole tokens (floor(128 / G) tokens each)
 };
 
 inline WsLayout ws_layout(const herald_dims& dm, int C, int P_max) {
@@ -63,6 +64,7 @@ inline WsLayout ws_layout(const herald_dims& dm, int C, int P_max) {
   w.tiles128 = w.L_pad / kTcScanKeys;
   w.R = dm.B * G;
   w.MT = cdiv(w.R, kTileM);
+  w.MT_tok = cdiv(dm.B, kTileM / G);
   w.n_chunks = cdiv(C, kRefineChunk);
   w.splits = cdiv(P_max, kAttnKeys) + cdiv(dm.B, kAttnKeys);
   const size_t NH = size_t(dm.N) * dm.Hq, NG = size_t(dm.N) * dm.Hkv;
@@ -77,7 +79,7 @@ inline WsLayout ws_layout(const herald_dims& dm, int C, int P_max) {
   w.cand = o;   o = align_up(o + NG * C * 4, A);
   w.n_cand = o; o = align_up(o + NG * 4, A);
   w.rpart = o;  o = align_up(o + NG * size_t(w.MT) * kTileM * w.n_chunks * 8, A);
-  w.s2 = o;     o = align_up(o + NG * C * 4 * size_t(w.MT), A);  // one partial per row tile
+  w.s2 = o;     o = align_up(o + NG * C * 4 * size_t(std::max(w.MT, w.MT_tok)), A);  // per row tile
   w.opart = o;  o = align_up(o + NG * w.MT * size_t(w.splits) * kTileM * dm.d * 4, A);
   w.ml = o;     o = align_up(o + NG * w.MT * size_t(w.splits) * kTileM * 8, A);
   w.total = o;
@@ -140,10 +142,19 @@ cudaError_t launch_topc(const herald_dims& dm, const float* s1, const uint32_t* 
                         const WsLayout& w, cudaStream_t st);
 // Whether stage 2 runs as the fused cluster kernel for this C; it then
 // writes one s2 partial per 128-row tile ([MT][N*Hkv][C]), else one.
+// The fused kernel takes its query tiles (whole tokens, MT_tok of them) by
+// TMA: qmap is q_block as [N*B][Hq][d] with a box of 64 columns x G heads x
+// floor(128/G) tokens (encode_heads_map); the two-pass kernels ignore it.
 bool refine_fused_ok(int C);
 cudaError_t launch_refine(const herald_dims& dm, const uint16_t* q_block, const uint16_t* k_cache,
                           const int32_t* cand, const int32_t* n_cand, int C, float2* rpart,
-                          float* s2, const WsLayout& w, uint32_t* err, cudaStream_t st);
+                          float* s2, const WsLayout& w, uint32_t* err, const CUtensorMap* qmap,
+                          cudaStream_t st);
+// Host-side tensor map of a [tokens][heads][d] bf16 array, box 64 x
+// box_heads x box_tokens, 128-byte swizzle (cached per thread).
+herald_status encode_heads_map(const void* base, uint64_t tokens, int heads, int d,
+                               uint32_t box_heads, uint32_t box_tokens, CUtensorMap* map);
+
 // s2 holds n_parts partial score arrays of [N*Hkv][C], summed per candidate.
 cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const int32_t* cand,
                               const int32_t* n_cand, const float* s2, int n_parts, int C, int K,

@@ -362,7 +362,9 @@ __global__ void __launch_bounds__(kTcThreads)
 
 // ========================================================== refine_fused
 // Stage 2 in one kernel for C <= 4096: one 8-CTA cluster per (sequence, KV
-// head, 128-row tile); CTA r scores candidate slots [r*cpc, (r+1)*cpc)
+// head, row tile of bpt = floor(128/G) whole tokens, its bpt*G query rows
+// loaded by one 3-D TMA box per 64-column half); CTA r scores candidate
+// slots [r*cpc, (r+1)*cpc)
 // (cpc <= 512, so the scores fill TMEM and are never recomputed).  Each
 // CTA stores its row (max, sumexp) over its candidates into every peer's
 // shared memory; after one cluster barrier each CTA merges them into the row
@@ -389,13 +391,14 @@ struct FuseCfg {
 
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    refine_fused_kernel(const uint16_t* __restrict__ q_block, const uint16_t* __restrict__ kc,
-                        const int32_t* __restrict__ cand, const int32_t* __restrict__ n_cand,
-                        int B, int Hq, int Hkv, int L_max, int C, int R, int cpc, float scale,
-                        float* __restrict__ s2p, uint32_t* err) {
+    refine_fused_kernel(const __grid_constant__ CUtensorMap qmap,
+                        const uint16_t* __restrict__ kc, const int32_t* __restrict__ cand,
+                        const int32_t* __restrict__ n_cand, int B, int Hq, int Hkv, int L_max,
+                        int C, int bpt, int cpc, float scale, float* __restrict__ s2p,
+                        uint32_t* err) {
   using Cfg = FuseCfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar0;
+  __shared__ uint64_t bar0, barQ;
   __shared__ uint32_t tmem_base;
   __shared__ int32_t pos[kFuseMaxCpc];
   __shared__ float2 half_stat[2][kTileM];
@@ -409,7 +412,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(&bar0, 1);
+    mbar_init(&barQ, 1);
     fence_mbar_init();
+    tma_prefetch_desc(&qmap);
   }
   // peers store into this CTA's shared memory before the cluster barrier
   // below: this arrive, awaited just before those stores, shows that every
@@ -417,7 +422,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __cluster_barrier_arrive_relaxed();
   tmem_setup(&tmem_base, 512);
   const uint32_t tbase = tmem_base;
+  const int b0 = mt * bpt;                  // first token of the tile
+  const int rows_t = min(bpt, B - b0) * G;  // query rows of the tile
   griddep_enter();
+  // the query tile first (it does not depend on n_cand); every CTA waits for
+  // it before exiting, used or not
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&barQ, uint32_t((D / 64) * G * bpt * 128));
+#pragma unroll
+    for (int hv = 0; hv < D / 64; ++hv)
+      tma_load_3d(Qs + hv * kTileM * 128, &qmap, &barQ, hv * 64, g * G, n * B + b0);
+  }
   const int nc = min(max(n_cand[seg], 0), C);
   const int c0 = int(rank) * cpc;
   const int ncv = min(max(nc - c0, 0), cpc);  // valid candidates of this CTA
@@ -428,12 +443,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   __syncthreads();
   if (ncv > 0) {
-    load_rows_sw128<D>(Qs, kTileM, kTileM, q_block, [&](int r) -> const uint16_t* {
-      const int row = mt * kTileM + r;
-      if (row >= R) return nullptr;
-      const int b = row / G, hl = row - (row / G) * G;
-      return q_block + ((size_t(n) * B + b) * Hq + g * G + hl) * D;
-    });
     load_rows_sw128<D>(Ks, cpc, cpc, kc, [&](int r) -> const uint16_t* {
       const int p = pos[r];
       return p < 0 ? nullptr : kc + (size_t(seg) * L_max + p) * D;
@@ -445,6 +454,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   // S = Q K_cand^T: up to two UMMAs of N = 256 -> TMEM columns [0, cpc)
+  bool qok = true;
+  if (threadIdx.x == 0) {
+    qok = mbar_wait(&barQ, 0);
+    tc_fence_after();
+  }
   if (threadIdx.x == 0 && ncv > 0) {
     const uint32_t qa = smem_u32(Qs), ka = smem_u32(Ks);
     for (int h0 = 0; h0 < cpc; h0 += 256) {
@@ -461,6 +475,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     umma_commit(&bar0);
   }
+  if (!qok) record_error(err, DEV_TIMEOUT_TMA);
   if (ncv > 0 && !mbar_wait(&bar0, 0)) record_error(err, DEV_TIMEOUT_MMA);
   tc_fence_after();
   __syncwarp();
@@ -523,8 +538,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (st[c].x != -INFINITY) Lr += st[c].y * fast_exp2(st[c].x - M);
     lse = M + __log2f(Lr);
   }
-  const bool row_ok = mt * kTileM + row < R;
-  // 2^(s - lse) = p * 2^(m_half - lse); rows past B*G contribute nothing
+  const bool row_ok = row < rows_t;
+  // 2^(s - lse) = p * 2^(m_half - lse); rows past the tile's tokens contribute nothing
   const float f = (row_ok && m != -INFINITY) ? fast_exp2(m - lse) : 0.f;
   // column sums over the 128 rows: per 32-column chunk, a warp
   // transpose-reduces its 32 rows; after the butterfly, lane j holds the sum
@@ -532,8 +547,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   for (int c = hc0; c < hc1; c += 32) {
     float v[32];
     tmem_ld32(trow + uint32_t(c), v);
+    // a select, not a product: rows past the tile's tokens hold whatever the
+    // shared memory held (never loaded), possibly NaN
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] *= f;
+    for (int i = 0; i < 32; ++i) v[i] = row_ok ? v[i] * f : 0.f;
 #pragma unroll
     for (int w = 16; w >= 1; w >>= 1) {
       // the lane with bit w set keeps the upper w columns, its partner the lower
@@ -564,13 +581,16 @@ bool refine_fused_ok(int C) { return fuse_cpc(C) <= kFuseMaxCpc; }
 
 cudaError_t launch_refine(const herald_dims& dm, const uint16_t* q_block, const uint16_t* k_cache,
                           const int32_t* cand, const int32_t* n_cand, int C, float2* rpart,
-                          float* s2, const WsLayout& w, uint32_t* err, cudaStream_t st) {
+                          float* s2, const WsLayout& w, uint32_t* err, const CUtensorMap* qmap,
+                          cudaStream_t st) {
   const float scale = 1.0f / sqrtf(float(dm.d));
   const int segs = dm.N * dm.Hkv;
   cudaError_t e;
   if (refine_fused_ok(C)) {
-    // s2 holds one partial per 128-row tile: [MT][N*Hkv][C]
+    // s2 holds one partial per row tile of whole tokens: [MT_tok][N*Hkv][C]
     const int cpc = fuse_cpc(C);
+    const int bpt = kTileM / (dm.Hq / dm.Hkv);
+    if (!qmap) return cudaErrorInvalidValue;
     if (dm.d == 128) {
       static bool attr = false;
       if (!attr) {
@@ -580,8 +600,8 @@ cudaError_t launch_refine(const herald_dims& dm, const uint16_t* q_block, const 
         attr = true;
       }
       return launch_cluster("refine_fused_kernel", refine_fused_kernel<128>,
-                            dim3(kFuseCtas, w.MT, segs), kFuseCtas, FuseCfg<128>::kSmem, st,
-                            q_block, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv, dm.L_max, C, w.R,
+                            dim3(kFuseCtas, w.MT_tok, segs), kFuseCtas, FuseCfg<128>::kSmem, st,
+                            *qmap, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv, dm.L_max, C, bpt,
                             cpc, scale, s2, err);
     }
     static bool attr64 = false;
@@ -592,9 +612,9 @@ cudaError_t launch_refine(const herald_dims& dm, const uint16_t* q_block, const 
       attr64 = true;
     }
     return launch_cluster("refine_fused_kernel", refine_fused_kernel<64>,
-                          dim3(kFuseCtas, w.MT, segs), kFuseCtas, FuseCfg<64>::kSmem, st, q_block,
-                          k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv, dm.L_max, C, w.R, cpc, scale,
-                          s2, err);
+                          dim3(kFuseCtas, w.MT_tok, segs), kFuseCtas, FuseCfg<64>::kSmem, st,
+                          *qmap, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv, dm.L_max, C, bpt, cpc,
+                          scale, s2, err);
   }
   if (dm.d == 128) {
     static bool attr = false;
