@@ -216,6 +216,13 @@ class Bench:
     n_sel_out = property(lambda self: self.pipe.n_sel)
     trace_capacity = 64
 
+    def before_step(self, i: int):
+        """Called before step i of every timed or warm-up loop (the single
+        layer keeps its context length fixed: nothing to do)."""
+
+    def context_note(self) -> str:
+        return "fixed: each step appends the block at the same position (ctx not advanced)"
+
     def l2_note(self) -> str:
         if self.w.kv_on_host:
             return "K/V cache in pinned host memory (read over the host link)"
@@ -304,8 +311,21 @@ class StackBench(Bench):
                                device="cuda")
         self.overlap = True
         self.trace_capacity = 24 * nl
+        # blocks run in groups of 4 consecutive blocks, each appending B
+        # tokens (L_max leaves room for 4 blocks); the context length is
+        # reset before each group
+        self.group = max(1, (w.L_max - w.L) // w.B)
+        self.ctx0 = self.ctx.clone()
         self.pipe.prime(self.q_merge, self.k, self.ctx, slot=0)
         torch.cuda.synchronize()
+
+    def before_step(self, i: int):
+        if i % self.group == 0:
+            self.ctx.copy_(self.ctx0, non_blocking=True)
+
+    def context_note(self) -> str:
+        return (f"grows: groups of {self.group} consecutive blocks, each appending B tokens to "
+                f"every layer; ctx reset between groups (inside the timed region)")
 
     idx = property(lambda self: self.pipe.idx_all)
     n_sel = property(lambda self: self.pipe.n_sel[-1])   # last layer's, for the roofline
@@ -320,7 +340,7 @@ class StackBench(Bench):
         bk = self.bk if bk is None else bk
         bv = self.bv if bv is None else bv
         self.pipe.block(r, qs, bk, bv, self.k, self.v, self.ctx,
-                        self.out if out is None else out, advance=False, overlap=self.overlap)
+                        self.out if out is None else out, advance=True, overlap=self.overlap)
 
 
 def algorithmic_work(w, n_sel: np.ndarray) -> dict:
@@ -465,6 +485,7 @@ def run_ours(args, rank, world, dist):
     clocks.start()
     st = torch.cuda.current_stream()
     for i in range(args.warmup):
+        b.before_step(i)
         graphs[i % nrot].replay()
     torch.cuda.synchronize()
     if dist:
@@ -474,6 +495,7 @@ def run_ours(args, rank, world, dist):
     t0 = time.perf_counter()
     e0.record(st)
     for i in range(args.steps):
+        b.before_step(args.warmup + i)
         graphs[(args.warmup + i) % nrot].replay()
     e1.record(st)
     torch.cuda.synchronize()
@@ -489,10 +511,12 @@ def run_ours(args, rank, world, dist):
     b.overlap = False
     sgraphs, _ = b.capture(traced=False)
     for i in range(args.warmup):
+        b.before_step(i)
         sgraphs[i % nrot].replay()
     torch.cuda.synchronize()
     e0.record(st)
     for i in range(args.steps):
+        b.before_step(args.warmup + i)
         sgraphs[(args.warmup + i) % nrot].replay()
     e1.record(st)
     torch.cuda.synchronize()
@@ -513,6 +537,7 @@ def run_ours(args, rank, world, dist):
     reps = max(3, min(args.steps, 50)) if traces else 0
     for i in range(reps):
         r = i % nrot
+        b.before_step(i)
         tgraphs[r].replay()
         torch.cuda.synchronize()
         for name, dt in traces[r].durations_ms():
@@ -573,7 +598,7 @@ def run_ours(args, rank, world, dist):
             "config": {"workload": w.name, "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
                        "ctx": w.L, "B": w.B, "T": w.T, "C": w.C, "K": w.K, "sink": w.S,
                        "local": w.W, "parallelism": f"replicas x{world}",
-                       "layers": w.layers, "l2": b.l2_note(),
+                       "layers": w.layers, "l2": b.l2_note(), "context": b.context_note(),
                        "timing": "CUDA-graph replay of whole steps, CUDA events"},
             "roofline": roofline,
             "serial": {"ms_per_step": serial_ms, "value": job_value(serial_ms, world, w.N * w.B),
@@ -626,6 +651,7 @@ def run_e2e(b, args, dist):
     def one(i):
         s = i % 2
         x = din[s]
+        b.before_step(i)
         cp.wait_event(comp_done[s])  # the step that last read these inputs is done
         comp.wait_event(out_done[s])  # ... and its output buffer has been read back
         with torch.cuda.stream(cp):

@@ -411,6 +411,18 @@ herald_status herald_workspace_error(void* ws, void* stream, uint32_t* code) {
   return HERALD_OK;
 }
 
+herald_status herald_selftest_wait_timeout(uint64_t limit_ns, void* ws, void* stream) {
+  g_err[0] = 0;
+  HERALD_CHECK_PTR(ws);
+  if (limit_ns == 0 || limit_ns > 1000000000ull)
+    return fail(HERALD_ERR_INVALID_ARG, "limit_ns=%llu outside (0, 1e9]",
+                (unsigned long long)limit_ns);
+  HERALD_TRY_CUDA(launch_wait_timeout(limit_ns, static_cast<uint32_t*>(ws),
+                                      static_cast<cudaStream_t>(stream)),
+                  "timeout self-test launch");
+  return HERALD_OK;
+}
+
 herald_status herald_select_stage1(herald_dims dims, const uint16_t* q_merge,
                                    const uint16_t* k_cache, const int32_t* ctx_len, int C,
                                    int32_t* cand, int32_t* n_cand, void* ws, size_t ws_bytes,

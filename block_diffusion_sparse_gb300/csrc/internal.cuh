@@ -184,6 +184,7 @@ cudaError_t launch_attn(const herald_dims& dm, const uint16_t* q, const uint16_t
                         const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
                         float scale, const WsLayout& w, float* opart, float2* ml, uint32_t* err,
                         const PoolMaps* maps, cudaStream_t st);
+cudaError_t launch_wait_timeout(uint64_t limit_ns, uint32_t* err, cudaStream_t st);
 cudaError_t launch_append(const herald_dims& dm, const uint16_t* block_k, const uint16_t* block_v,
                           int32_t* ctx, uint16_t* k_cache, uint16_t* v_cache, int advance,
                           cudaStream_t st);

@@ -46,6 +46,23 @@ __global__ void __launch_bounds__(256)
   if (vc) *reinterpret_cast<uint4*>(pv + dst) = vv;
 }
 
+// One thread waits on an mbarrier that nothing completes, through the same
+// bounded wait every kernel uses, with a caller-chosen limit; it records the
+// timeout in the error word and returns.  Exercises the device-side failure
+// path without faulting or hanging the GPU.
+__global__ void wait_timeout_kernel(uint64_t limit_ns, uint32_t* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  if (!mbar_wait(&bar, 0, limit_ns)) record_error(err, DEV_TIMEOUT_TMA);
+}
+
+cudaError_t launch_wait_timeout(uint64_t limit_ns, uint32_t* err, cudaStream_t st) {
+  wait_timeout_kernel<<<1, 32, 0, st>>>(limit_ns, err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gather(const herald_dims& dm, const int32_t* idx, const int32_t* n_sel,
                           int P_max, const uint16_t* k_cache, const uint16_t* v_cache,
                           uint16_t* pool_k, uint16_t* pool_v, cudaStream_t st,

@@ -62,14 +62,15 @@ HERALD_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Waits for the phase with the given parity to complete.  Gives up after
-// about kWaitLimitNs and returns false; the caller records the error.
-HERALD_DEV bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// about limit_ns (kWaitLimitNs by default) and returns false; the caller
+// records the error.
+HERALD_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 

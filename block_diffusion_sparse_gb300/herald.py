@@ -21,7 +21,7 @@ EXPORTS = ("herald_workspace_size", "herald_status_string", "herald_last_error",
            "herald_workspace_error", "herald_select_stage1", "herald_select_stage2",
            "herald_select", "herald_gather", "herald_denoise_attn", "herald_append_kv",
            "herald_trace_begin", "herald_trace_end", "herald_trace_name",
-           "herald_select_stage2_noalloc")
+           "herald_select_stage2_noalloc", "herald_selftest_wait_timeout")
 
 
 class HeraldError(RuntimeError):
@@ -79,6 +79,7 @@ def lib() -> C.CDLL:
         L.herald_append_kv.argtypes = [Dims, vp, vp, vp, vp, vp, i32, vp]
         L.herald_select_stage2_noalloc.argtypes = [Dims, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                    i32, vp, vp, vp]
+        L.herald_selftest_wait_timeout.argtypes = [C.c_uint64, vp, vp]
         L.herald_trace_begin.argtypes = [C.POINTER(vp), i32, i32]
         L.herald_trace_end.argtypes = []
         L.herald_trace_name.argtypes = [i32]
@@ -194,6 +195,11 @@ def herald_select_stage2_noalloc(d, q_block, k_cache, ctx_len, cand, n_cand, C_,
     _check(lib().herald_select_stage2_noalloc(d, _p(q_block), _p(k_cache), _p(ctx_len), _p(cand),
                                               _p(n_cand), int(C_), int(K), int(sink), int(local),
                                               int(P_max), _p(idx), _p(n_sel), _s(stream)))
+
+
+def herald_selftest_wait_timeout(limit_ns, ws, stream=None):
+    """Runs one bounded wait that nothing completes (see include/herald.h)."""
+    _check(lib().herald_selftest_wait_timeout(int(limit_ns), _p(ws), _s(stream)))
 
 
 def herald_gather(d, idx, n_sel, P_max, k_cache, v_cache, pool_k, pool_v, stream=None):

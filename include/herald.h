@@ -186,6 +186,17 @@ herald_status herald_append_kv(herald_dims dims, const uint16_t *block_k,
                                const uint16_t *block_v, int32_t *ctx_len, uint16_t *k_cache,
                                uint16_t *v_cache, int advance, void *stream);
 
+/* Self-test of the device-side failure path (the pages have no
+ * counterpart).  Every wait inside the library's kernels gives up after
+ * about one second, records a code in the workspace's error word and lets
+ * the kernel return, so a lost copy or commit is reported instead of
+ * hanging the GPU.  This call launches one thread that waits, with that
+ * same bounded wait, on a barrier nothing completes, for limit_ns
+ * nanoseconds (0 < limit_ns <= 1e9); afterwards herald_workspace_error()
+ * on `ws` reads 1 and the context remains usable.  ws: any workspace (its
+ * first 4 bytes are the error word). */
+herald_status herald_selftest_wait_timeout(uint64_t limit_ns, void *ws, void *stream);
+
 /* Kernel tracing, a profiling aid that is off by default.  While enabled on
  * the calling host thread, every kernel the library launches is bracketed
  * by two caller-created CUDA events (cudaEvent_t, timing enabled) recorded
