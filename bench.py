@@ -131,6 +131,7 @@ def job_value(ms_per_step: float, world: int, tokens_per_step: int) -> float:
 WORKLOADS = {"qwen": "QWEN_32K", "tiny": "TINY", "llama": "LLAMA_64K",
              "long-host": "LONG_128K_HOST", "stack": "QWEN_STACK"}
 _WORKLOAD = "qwen"
+_SELECTION = "merged"
 
 
 def workload():
@@ -194,7 +195,8 @@ class Bench:
         self.bk, self.bv = dev(x["block_k"]), dev(x["block_v"])
         self.ctx = torch.from_numpy(x["ctx"]).cuda()
         from block_diffusion_sparse_gb300.pipeline import BlockPipeline
-        self.pipe = BlockPipeline(self.d, w.C, w.K, w.S, w.W, self.P, w.T)
+        self.exact = _SELECTION == "exact"
+        self.pipe = BlockPipeline(self.d, w.C, w.K, w.S, w.W, self.P, w.T, exact=self.exact)
         self.out = torch.zeros((w.T, w.N, w.B, w.Hq, w.d), dtype=torch.int16, device="cuda")
         self.overlap = True
         # stage 1 of the first block (its own queries; no predecessor)
@@ -236,6 +238,10 @@ class Bench:
         bk = self.bk if bk is None else bk
         bv = self.bv if bv is None else bv
         nxt = (r + 1) % self.n_rot
+        if self.exact:
+            self.pipe.block_exact(r, qs, bk, bv, self.k[r], self.v[r], self.ctx,
+                                  self.out if out is None else out, advance=False)
+            return
         self.pipe.block(r, qs, bk, bv, self.k[r], self.v[r], self.ctx,
                         self.out if out is None else out, next_k_cache=self.k[nxt],
                         advance=False, overlap=self.overlap)
@@ -599,6 +605,7 @@ def run_ours(args, rank, world, dist):
                        "ctx": w.L, "B": w.B, "T": w.T, "C": w.C, "K": w.K, "sink": w.S,
                        "local": w.W, "parallelism": f"replicas x{world}",
                        "layers": w.layers, "l2": b.l2_note(), "context": b.context_note(),
+                       "selection": _SELECTION,
                        "timing": "CUDA-graph replay of whole steps, CUDA events"},
             "roofline": roofline,
             "serial": {"ms_per_step": serial_ms, "value": job_value(serial_ms, world, w.N * w.B),
@@ -701,9 +708,13 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="qwen", choices=sorted(WORKLOADS))
+    ap.add_argument("--selection", default="merged", choices=["merged", "exact"],
+                    help="merged: the two-stage selection (default); exact: every cached "
+                         "position scored with the block's real queries (one stream)")
     args = ap.parse_args()
-    global _WORKLOAD
+    global _WORKLOAD, _SELECTION
     _WORKLOAD = args.workload
+    _SELECTION = args.selection
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -252,14 +252,18 @@ herald_status run_stage2(const herald_dims& dm, const uint16_t* q_block, const u
                          int C, int K, int sink, int local, int P_max, int32_t* idx,
                          int32_t* n_sel, void* ws, const WsLayout& w, cudaStream_t st) {
   uint32_t* err = at<uint32_t>(ws, w.err);
-  CUtensorMap qmap;
+  CUtensorMap qmap, qmap_all;
   const int G = dm.Hq / dm.Hkv;
-  const herald_status qs = encode_heads_map(q_block, uint64_t(dm.N) * dm.B, dm.Hq, dm.d,
-                                            uint32_t(G), uint32_t(kTileM / G), &qmap);
+  herald_status qs = encode_heads_map(q_block, uint64_t(dm.N) * dm.B, dm.Hq, dm.d, uint32_t(G),
+                                      uint32_t(kTileM / G), &qmap);
+  if (qs == HERALD_OK)
+    qs = encode_heads_map(q_block, uint64_t(dm.N) * dm.B, dm.Hq, dm.d, uint32_t(G),
+                          uint32_t(dm.B), &qmap_all);
   if (qs != HERALD_OK) return qs;
+  float* rlse = at<float>(ws, w.rlse);
   if (is_device_memory(k_cache)) {
     HERALD_TRY_CUDA(launch_refine(dm, q_block, k_cache, cand, n_cand, C, at<float2>(ws, w.rpart),
-                                  at<float>(ws, w.s2), w, err, &qmap, st),
+                                  rlse, at<float>(ws, w.s2), w, err, &qmap, &qmap_all, st),
                     "refine launch");
   } else {
     // a host-resident cache: the candidate K rows cross the host link once,
@@ -272,8 +276,8 @@ herald_status run_stage2(const herald_dims& dm, const uint16_t* q_block, const u
     herald_dims staged = dm;
     staged.L_max = C;  // rows per (sequence, KV head) in the staging buffer
     HERALD_TRY_CUDA(launch_refine(staged, q_block, kstage, nullptr, n_cand, C,
-                                  at<float2>(ws, w.rpart), at<float>(ws, w.s2), w, err, &qmap,
-                                  st),
+                                  at<float2>(ws, w.rpart), rlse, at<float>(ws, w.s2), w, err,
+                                  &qmap, &qmap_all, st),
                     "refine launch");
   }
   const int n_parts = refine_fused_ok(C) ? w.MT_tok : 1;
@@ -408,6 +412,86 @@ herald_status herald_workspace_error(void* ws, void* stream, uint32_t* code) {
   HERALD_TRY_CUDA(cudaMemcpy(&v, ws, sizeof v, cudaMemcpyDeviceToHost), "read error word");
   *code = v;
   if (v) HERALD_TRY_CUDA(cudaMemsetAsync(ws, 0, sizeof v, st), "clear error word");
+  return HERALD_OK;
+}
+
+// Workspace of the exact selection: error word, histograms, the top-K
+// positions, counts, refine row statistics over every cached position, and
+// the score partials [parts][N*Hkv][L_pad].
+struct ExactLayout {
+  size_t err, hist, cand, n_cand, rpart, rlse, s, total;
+};
+static ExactLayout exact_layout(const herald_dims& dm, int K, const WsLayout& w) {
+  ExactLayout x{};
+  const size_t A = 256, NG = size_t(dm.N) * dm.Hkv;
+  size_t o = 0;
+  x.err = o;    o = align_up(o + 16, A);
+  x.hist = o;   o = align_up(o + NG * kHistBins * 4, A);
+  x.cand = o;   o = align_up(o + NG * size_t(K) * 4, A);
+  x.n_cand = o; o = align_up(o + NG * 4, A);
+  x.rpart = o;  o = align_up(o + NG * size_t(w.MT) * kTileM * w.n_chunks * 8, A);
+  x.rlse = o;   o = align_up(o + NG * size_t(w.MT) * kTileM * 4, A);
+  x.s = o;      o = align_up(o + NG * size_t(w.L_pad) * 4 * std::max(w.MT, w.MT_tok), A);
+  x.total = o;
+  return x;
+}
+
+size_t herald_workspace_size_exact(herald_dims dims, int K, int P_max) {
+  if (check_dims(dims) != HERALD_OK || K < 1 || K > kMaxC || P_max < 1) return 0;
+  const WsLayout w = ws_layout(dims, cdiv(dims.L_max, kTcScanKeys) * kTcScanKeys, P_max);
+  return exact_layout(dims, K, w).total;
+}
+
+herald_status herald_select_exact(herald_dims dims, const uint16_t* q_block,
+                                  const uint16_t* k_cache, const int32_t* ctx_len, int K,
+                                  int sink, int local, int P_max, int32_t* idx, int32_t* n_sel,
+                                  void* ws, size_t ws_bytes, void* stream) {
+  g_err[0] = 0;
+  HERALD_RET_IF(check_dims(dims));
+  HERALD_RET_IF(check_pmax(dims, P_max));
+  if (K < 1 || K > kMaxC)
+    return fail(HERALD_ERR_UNSUPPORTED_SHAPE, "K=%d outside [1, %d]", K, kMaxC);
+  HERALD_RET_IF(check_budget(K, K, sink, local, P_max));
+  HERALD_CHECK_PTR(q_block);
+  HERALD_CHECK_PTR(k_cache);
+  HERALD_CHECK_PTR(ctx_len);
+  HERALD_CHECK_PTR(idx);
+  HERALD_CHECK_PTR(n_sel);
+  HERALD_CHECK_PTR(ws);
+  const int L_pad = cdiv(dims.L_max, kTcScanKeys) * kTcScanKeys;
+  const WsLayout w = ws_layout(dims, L_pad, P_max);  // tile counts of a refine over L_pad slots
+  const ExactLayout x = exact_layout(dims, K, w);
+  if (ws_bytes < x.total)
+    return fail(HERALD_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", ws_bytes,
+                x.total);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* err = at<uint32_t>(ws, x.err);
+  int32_t* n_cand = at<int32_t>(ws, x.n_cand);
+  float* s = at<float>(ws, x.s);
+  uint32_t* hist = at<uint32_t>(ws, x.hist);
+  CUtensorMap qmap, qmap_all;
+  const int G = dims.Hq / dims.Hkv;
+  HERALD_RET_IF(encode_heads_map(q_block, uint64_t(dims.N) * dims.B, dims.Hq, dims.d,
+                                 uint32_t(G), uint32_t(kTileM / G), &qmap));
+  HERALD_RET_IF(encode_heads_map(q_block, uint64_t(dims.N) * dims.B, dims.Hq, dims.d,
+                                 uint32_t(G), uint32_t(dims.B), &qmap_all));
+  HERALD_TRY_CUDA(cudaMemsetAsync(hist, 0, size_t(dims.N) * dims.Hkv * kHistBins * 4, st),
+                  "clear histograms");
+  HERALD_TRY_CUDA(launch_exact_counts(dims, ctx_len, n_cand, st), "exact counts launch");
+  // every cached position is a candidate (row = slot, stride L_pad)
+  HERALD_TRY_CUDA(launch_refine(dims, q_block, k_cache, nullptr, n_cand, L_pad,
+                                at<float2>(ws, x.rpart), at<float>(ws, x.rlse), s, w, err,
+                                &qmap, &qmap_all, st),
+                  "refine launch");
+  const int n_parts = refine_fused_ok(L_pad) ? w.MT_tok : 1;
+  HERALD_TRY_CUDA(launch_exact_sum_hist(dims, s, n_parts, L_pad, ctx_len, hist, sm_count(), st),
+                  "exact histogram launch");
+  int32_t* cand = at<int32_t>(ws, x.cand);
+  HERALD_TRY_CUDA(launch_topc(dims, s, hist, ctx_len, K, cand, n_cand, w, st), "top-K launch");
+  // the K positions are all kept; the union adds sink and local and orders
+  HERALD_TRY_CUDA(launch_topk_union(dims, ctx_len, cand, n_cand, s, 1, K, K, sink, local, P_max,
+                                    idx, n_sel, st),
+                  "union launch");
   return HERALD_OK;
 }
 

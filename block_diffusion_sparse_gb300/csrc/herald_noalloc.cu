@@ -82,13 +82,15 @@ herald_status herald_select_stage2_noalloc(herald_dims dims, const uint16_t* q_b
       !aligned16(n_cand) || !aligned16(idx) || !aligned16(n_sel))
     return fail(HERALD_ERR_INVALID_ARG, "a pointer is NULL or not 16-byte aligned");
 
-  // compact scratch layout: error word | refine row statistics | s2
+  // compact scratch layout: error word | refine row statistics | row lse | s2
   const WsLayout full = ws_layout(dims, C, P_max);
   const size_t NG = size_t(dims.N) * dims.Hkv;
   const size_t err_off = 0;
   const size_t rpart_off = 256;
   const size_t rpart_bytes = NG * size_t(full.MT) * kTileM * full.n_chunks * 8;
-  const size_t s2_off = align_up(rpart_off + rpart_bytes, 256);
+  const size_t rlse_off = align_up(rpart_off + rpart_bytes, 256);
+  const size_t rlse_bytes = NG * size_t(full.MT) * kTileM * 4;
+  const size_t s2_off = align_up(rlse_off + rlse_bytes, 256);
   const int n_parts = refine_fused_ok(C) ? full.MT_tok : 1;  // s2 partials per row tile
   const size_t need = s2_off + NG * size_t(C) * 4 * size_t(n_parts);
   if (need > kStaticScratchBytes)
@@ -103,10 +105,13 @@ herald_status herald_select_stage2_noalloc(herald_dims dims, const uint16_t* q_b
   uint32_t* err = reinterpret_cast<uint32_t*>(base + err_off);
   // the fused refine reads its query tiles by TMA (a host-side descriptor,
   // no device memory)
-  CUtensorMap qmap;
+  CUtensorMap qmap, qmap_all;
   const int G = dims.Hq / dims.Hkv;
   s = encode_heads_map(q_block, uint64_t(dims.N) * dims.B, dims.Hq, dims.d, uint32_t(G),
                        uint32_t(kTileM / G), &qmap);
+  if (s == HERALD_OK)
+    s = encode_heads_map(q_block, uint64_t(dims.N) * dims.B, dims.Hq, dims.d, uint32_t(G),
+                         uint32_t(dims.B), &qmap_all);
   if (s != HERALD_OK) return s;
   // the array keeps the previous call's contents: the error word must start
   // at zero; the statistics and scores are fully rewritten before use
@@ -114,7 +119,8 @@ herald_status herald_select_stage2_noalloc(herald_dims dims, const uint16_t* q_b
   if (e == cudaSuccess)
     e = launch_refine(dims, q_block, k_cache, cand, n_cand, C,
                       reinterpret_cast<float2*>(base + rpart_off),
-                      reinterpret_cast<float*>(base + s2_off), full, err, &qmap, st);
+                      reinterpret_cast<float*>(base + rlse_off),
+                      reinterpret_cast<float*>(base + s2_off), full, err, &qmap, &qmap_all, st);
   if (e == cudaSuccess)
     e = launch_topk_union(dims, ctx_len, cand, n_cand, reinterpret_cast<float*>(base + s2_off),
                           n_parts, C, K, sink, local, P_max, idx, n_sel, st);

@@ -47,6 +47,7 @@ struct WsLayout {
   size_t cand;       // int32 [N][Hkv][C]       (herald_select only)
   size_t n_cand;     // int32 [N][Hkv]
   size_t rpart;      // float2 [N][Hkv][R_pad][n_chunks]  refine row stats
+  size_t rlse;       // float [N][Hkv][R_pad]   refine row log-sum-exp (two-pass refine)
   size_t s2;         // float [MT][N][Hkv][C] stage-2 score partials
   size_t opart;      // float [N*Hkv][MT][S][128][d]      attention partials
   size_t ml;         // float2 [N*Hkv][MT][S][128]
@@ -79,6 +80,7 @@ inline WsLayout ws_layout(const herald_dims& dm, int C, int P_max) {
   w.cand = o;   o = align_up(o + NG * C * 4, A);
   w.n_cand = o; o = align_up(o + NG * 4, A);
   w.rpart = o;  o = align_up(o + NG * size_t(w.MT) * kTileM * w.n_chunks * 8, A);
+  w.rlse = o;   o = align_up(o + NG * size_t(w.MT) * kTileM * 4, A);
   w.s2 = o;     o = align_up(o + NG * C * 4 * size_t(std::max(w.MT, w.MT_tok)), A);  // per row tile
   w.opart = o;  o = align_up(o + NG * w.MT * size_t(w.splits) * kTileM * dm.d * 4, A);
   w.ml = o;     o = align_up(o + NG * w.MT * size_t(w.splits) * kTileM * 8, A);
@@ -142,14 +144,16 @@ cudaError_t launch_topc(const herald_dims& dm, const float* s1, const uint32_t* 
                         const WsLayout& w, cudaStream_t st);
 // Whether stage 2 runs as the fused cluster kernel for this C; it then
 // writes one s2 partial per 128-row tile ([MT][N*Hkv][C]), else one.
-// The fused kernel takes its query tiles (whole tokens, MT_tok of them) by
-// TMA: qmap is q_block as [N*B][Hq][d] with a box of 64 columns x G heads x
-// floor(128/G) tokens (encode_heads_map); the two-pass kernels ignore it.
+// The refine kernels take the queries by TMA (q_block as [N*B][Hq][d],
+// encode_heads_map): qmap with a box of 64 columns x G heads x floor(128/G)
+// tokens (row tiles of whole tokens, MT_tok of them), qmap_all with a box
+// of all B tokens (the two-pass refine's second pass; may be null when
+// C <= 4096).  rlse: [N*Hkv][MT*128] floats for the two-pass refine.
 bool refine_fused_ok(int C);
 cudaError_t launch_refine(const herald_dims& dm, const uint16_t* q_block, const uint16_t* k_cache,
                           const int32_t* cand, const int32_t* n_cand, int C, float2* rpart,
-                          float* s2, const WsLayout& w, uint32_t* err, const CUtensorMap* qmap,
-                          cudaStream_t st);
+                          float* rlse, float* s2, const WsLayout& w, uint32_t* err,
+                          const CUtensorMap* qmap, const CUtensorMap* qmap_all, cudaStream_t st);
 // Host-side tensor map of a [tokens][heads][d] bf16 array, box 64 x
 // box_heads x box_tokens, 128-byte swizzle (cached per thread).
 herald_status encode_heads_map(const void* base, uint64_t tokens, int heads, int d,
@@ -184,6 +188,14 @@ cudaError_t launch_attn(const herald_dims& dm, const uint16_t* q, const uint16_t
                         const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
                         float scale, const WsLayout& w, float* opart, float2* ml, uint32_t* err,
                         const PoolMaps* maps, cudaStream_t st);
+// exact selection: per-segment candidate counts = context lengths; the
+// refine's score partials summed in place (stride floats per segment) and
+// histogrammed for the top-K radix select
+cudaError_t launch_exact_counts(const herald_dims& dm, const int32_t* ctx, int32_t* n_cand,
+                                cudaStream_t st);
+cudaError_t launch_exact_sum_hist(const herald_dims& dm, float* s, int n_parts, int stride,
+                                  const int32_t* ctx, uint32_t* hist, int num_sms,
+                                  cudaStream_t st);
 cudaError_t launch_wait_timeout(uint64_t limit_ns, uint32_t* err, cudaStream_t st);
 cudaError_t launch_append(const herald_dims& dm, const uint16_t* block_k, const uint16_t* block_v,
                           int32_t* ctx, uint16_t* k_cache, uint16_t* v_cache, int advance,

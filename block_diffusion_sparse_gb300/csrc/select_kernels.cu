@@ -863,6 +863,70 @@ cudaError_t launch_topc(const herald_dims& dm, const float* s1, const uint32_t* 
   return cudaGetLastError();
 }
 
+// ============================================================ exact selection
+// Helpers of the exact selection (every cached position a candidate):
+// the candidate count of each (sequence, KV head) is its context length,
+// and the refine's score partials are summed in place into partial 0 while
+// their 12-bit histogram (the first radix digit of the top-K) is built.
+__global__ void exact_counts_kernel(const int32_t* __restrict__ ctx, int segs, int Hkv, int L_max,
+                                    int32_t* __restrict__ n_cand) {
+  griddep_enter();
+  const int seg = blockIdx.x * blockDim.x + threadIdx.x;
+  if (seg < segs) n_cand[seg] = min(max(ctx[seg / Hkv], 0), L_max);
+}
+
+// grid (chunks, N*Hkv), block 256: s[p][seg][j] (stride per partial:
+// segs * stride) summed over the n_parts partials into s[0][seg][j] for
+// j < ctx, and binned by the top 12 bits of the (non-negative) fp32 pattern.
+__global__ void __launch_bounds__(256)
+    exact_sum_hist_kernel(float* __restrict__ s, int n_parts, int stride,
+                          const int32_t* __restrict__ ctx, int Hkv, int L_max, int keys_per_cta,
+                          uint32_t* __restrict__ hist) {
+  __shared__ uint32_t sh[kHistBins];
+  griddep_enter();
+  const int seg = blockIdx.y, n = seg / Hkv;
+  const int L = min(max(ctx[n], 0), L_max);
+  const int j_begin = blockIdx.x * keys_per_cta;
+  if (j_begin >= L) return;
+  const int j_end = min(L, j_begin + keys_per_cta);
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) sh[i] = 0u;
+  __syncthreads();
+  const size_t part_stride = size_t(gridDim.y) * stride;
+  float* row = s + size_t(seg) * stride;
+  for (int j = j_begin + threadIdx.x; j < j_end; j += blockDim.x) {
+    float v = 0.f;
+    for (int p = 0; p < n_parts; ++p) v += row[p * part_stride + j];
+    v = fmaxf(v, 0.f);
+    row[j] = v;
+    atomicAdd(&sh[(__float_as_uint(v) >> kHistShift) & (kHistBins - 1)], 1u);
+  }
+  __syncthreads();
+  uint32_t* gh = hist + size_t(seg) * kHistBins;
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x)
+    if (sh[i]) atomicAdd(&gh[i], sh[i]);
+}
+
+cudaError_t launch_exact_counts(const herald_dims& dm, const int32_t* ctx, int32_t* n_cand,
+                                cudaStream_t st) {
+  const int segs = dm.N * dm.Hkv;
+  HERALD_CHECK_LAUNCH(launch_k("exact_counts_kernel", exact_counts_kernel, cdiv(segs, 128), 128,
+                               0, st, ctx, segs, dm.Hkv, dm.L_max, n_cand));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_exact_sum_hist(const herald_dims& dm, float* s, int n_parts, int stride,
+                                  const int32_t* ctx, uint32_t* hist, int num_sms,
+                                  cudaStream_t st) {
+  const int segs = dm.N * dm.Hkv;
+  int chunks = (2 * num_sms + segs - 1) / segs;
+  int keys = cdiv(cdiv(dm.L_max, chunks), 256) * 256;
+  chunks = cdiv(dm.L_max, keys);
+  HERALD_CHECK_LAUNCH(launch_k("exact_sum_hist_kernel", exact_sum_hist_kernel,
+                               dim3(chunks, segs), 256, 0, st, s, n_parts, stride, ctx, dm.Hkv,
+                               dm.L_max, keys, hist));
+  return cudaGetLastError();
+}
+
 // ============================================================= topk_union
 // One CTA of 1024 threads per (n, g); thread t holds the stage-2 scores of the
 // candidate slots [t*E, (t+1)*E) in registers (E <= kPer; 4 when C <= 4096,

@@ -140,15 +140,19 @@ struct Ref1Cfg {
   static_assert(kSmem <= 227 * 1024, "refine pass 1 smem exceeds the per-CTA limit");
 };
 
+// Pass 1 for C > 4096: per (segment, row tile of bpt whole tokens, chunk of
+// 256 candidates) the row (max, sumexp) of S = Q K_cand^T, the query tile
+// loaded by one 3-D TMA box per half.
 template <int D>
 __global__ void __launch_bounds__(kTcThreads)
-    refine_pass1_kernel(const uint16_t* __restrict__ q_block, const uint16_t* __restrict__ kc,
-                        const int32_t* __restrict__ cand, const int32_t* __restrict__ n_cand,
-                        int B, int Hq, int Hkv, int L_max, int C, int R, int MT, int n_chunks,
-                        float scale, float2* __restrict__ rpart, uint32_t* err) {
+    refine_pass1_kernel(const __grid_constant__ CUtensorMap qmap,
+                        const uint16_t* __restrict__ kc, const int32_t* __restrict__ cand,
+                        const int32_t* __restrict__ n_cand, int B, int Hq, int Hkv, int L_max,
+                        int C, int bpt, int MT, int n_chunks, float scale,
+                        float2* __restrict__ rpart, uint32_t* err) {
   using Cfg = Ref1Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar;
+  __shared__ uint64_t bar, barQ;
   __shared__ uint32_t tmem_base;
   __shared__ float2 red[2][kTileM];
   __shared__ int32_t pos[kRefineChunk];
@@ -161,19 +165,19 @@ __global__ void __launch_bounds__(kTcThreads)
   const int c0 = chunk * kRefineChunk;
   if (c0 >= nc) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b0 = mt * bpt, rows_t = min(bpt, B - b0) * G;
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
+    mbar_init(&barQ, 1);
     fence_mbar_init();
+    mbar_arrive_expect_tx(&barQ, uint32_t((D / 64) * G * bpt * 128));
+#pragma unroll
+    for (int hv = 0; hv < D / 64; ++hv)
+      tma_load_3d(Qs + hv * kTileM * 128, &qmap, &barQ, hv * 64, g * G, n * B + b0);
   }
   tmem_setup(&tmem_base, 256);
   const uint32_t tbase = tmem_base;
 
-  load_rows_sw128<D>(Qs, kTileM, kTileM, q_block, [&](int r) -> const uint16_t* {
-    const int row = mt * kTileM + r;
-    if (row >= R) return nullptr;
-    const int b = row / G, hl = row - (row / G) * G;
-    return q_block + ((size_t(n) * B + b) * Hq + g * G + hl) * D;
-  });
   // candidate positions first (one coalesced load), then the row copies
   const int32_t* cd = cand ? cand + size_t(seg) * C : nullptr;  // null: row = slot
   for (int r = threadIdx.x; r < kRefineChunk; r += kTcThreads)
@@ -194,6 +198,8 @@ __global__ void __launch_bounds__(kTcThreads)
   tc_fence_after();
 
   if (threadIdx.x == 0) {
+    if (!mbar_wait(&barQ, 0)) record_error(err, DEV_TIMEOUT_TMA);
+    tc_fence_after();
     constexpr uint32_t idesc = make_idesc_bf16(kTileM, kRefineChunk, false, false);
     const uint32_t qa = smem_u32(Qs), ka = smem_u32(Ks);
 #pragma unroll
@@ -236,8 +242,8 @@ __global__ void __launch_bounds__(kTcThreads)
     const float M = fmaxf(a.x, b.x);
     const float S = (a.x == -INFINITY ? 0.f : a.y * __expf(a.x - M)) +
                     (b.x == -INFINITY ? 0.f : b.y * __expf(b.x - M));
-    const int grow = mt * kTileM + row;
-    if (grow < R) rpart[(size_t(seg) * MT * kTileM + grow) * n_chunks + chunk] = make_float2(M, S);
+    if (row < rows_t)
+      rpart[(size_t(seg) * MT * kTileM + b0 * G + row) * n_chunks + chunk] = make_float2(M, S);
   }
   tmem_teardown(tbase, 256);
 }
@@ -252,16 +258,55 @@ struct Ref2Cfg {
   static_assert(kSmem <= 227 * 1024, "refine pass 2 smem exceeds the per-CTA limit");
 };
 
+// Row log-sum-exp over all candidates, once per row, from pass 1's chunk
+// partials: grid (ceil(R / 8), N*Hkv), block 256 -- one warp per row, the
+// lanes striding over the chunks, then a warp reduction of (max, sumexp).
+__global__ void __launch_bounds__(256)
+    refine_lse_kernel(const float2* __restrict__ rpart, const int32_t* __restrict__ n_cand,
+                      int C, int R, int MT, int n_chunks, float* __restrict__ rlse) {
+  griddep_enter();
+  const int seg = blockIdx.y;
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (r >= R) return;
+  const int nc = min(max(n_cand[seg], 0), C);
+  const int nch = (nc + kRefineChunk - 1) / kRefineChunk;
+  const float2* p = rpart + (size_t(seg) * MT * kTileM + r) * n_chunks;
+  float M = -INFINITY, S = 0.f;
+  for (int k0 = lane; k0 < nch; k0 += 32 * 4) {  // four loads in flight per lane
+    float2 q[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int k = k0 + u * 32;
+      q[u] = k < nch ? p[k] : make_float2(-INFINITY, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (q[u].x == -INFINITY) continue;
+      if (q[u].x > M) {
+        S = S * __expf(M - q[u].x) + q[u].y;
+        M = q[u].x;
+      } else {
+        S += q[u].y * __expf(q[u].x - M);
+      }
+    }
+  }
+  const float Mw = warp_max(M);
+  S = warp_sum(M == -INFINITY ? 0.f : S * __expf(M - Mw));
+  if (lane == 0) rlse[size_t(seg) * MT * kTileM + r] = Mw + __logf(S);
+}
+
+// Pass 2: per (segment, 128 candidates) S^T = K_cand Q^T with all B*G query
+// rows (one 3-D TMA box per half) and s2[c] = sum_r exp(S[r,c] - lse_r).
 template <int D>
 __global__ void __launch_bounds__(kTcThreads)
-    refine_pass2_kernel(const uint16_t* __restrict__ q_block, const uint16_t* __restrict__ kc,
-                        const int32_t* __restrict__ cand, const int32_t* __restrict__ n_cand,
-                        int B, int Hq, int Hkv, int L_max, int C, int R, int MT, int n_chunks,
-                        float scale, const float2* __restrict__ rpart, float* __restrict__ s2,
-                        uint32_t* err) {
+    refine_pass2_kernel(const __grid_constant__ CUtensorMap qmap_all,
+                        const uint16_t* __restrict__ kc, const int32_t* __restrict__ cand,
+                        const int32_t* __restrict__ n_cand, int B, int Hq, int Hkv, int L_max,
+                        int C, int R, int MT, float scale, const float* __restrict__ rlse,
+                        float* __restrict__ s2, uint32_t* err) {
   using Cfg = Ref2Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar;
+  __shared__ uint64_t bar, barQ;
   __shared__ uint32_t tmem_base;
   __shared__ float lse[256];
   __shared__ float red[2][kRefineRows2];
@@ -277,7 +322,13 @@ __global__ void __launch_bounds__(kTcThreads)
   const int Rp = (R + 15) & ~15;  // MMA N: multiple of 16
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
+    mbar_init(&barQ, 1);
     fence_mbar_init();
+    // all B*G query rows; rows [R, Rp) of the operand are never used
+    mbar_arrive_expect_tx(&barQ, uint32_t((D / 64) * R * 128));
+#pragma unroll
+    for (int hv = 0; hv < D / 64; ++hv)
+      tma_load_3d(Qs + hv * 256 * 128, &qmap_all, &barQ, hv * 64, g * G, n * B);
   }
   tmem_setup(&tmem_base, 256);
   const uint32_t tbase = tmem_base;
@@ -291,41 +342,17 @@ __global__ void __launch_bounds__(kTcThreads)
     if (p < 0) return nullptr;
     return kc + (size_t(seg) * L_max + p) * D;
   });
-  load_rows_sw128<D>(Qs, Rp, 256, q_block, [&](int r) -> const uint16_t* {
-    if (r >= R) return nullptr;
-    const int b = r / G, hl = r - (r / G) * G;
-    return q_block + ((size_t(n) * B + b) * Hq + g * G + hl) * D;
-  });
   cp_async_commit();
-  // row log-sum-exp over all candidates from the pass-1 chunk partials
-  const int nch = (nc + kRefineChunk - 1) / kRefineChunk;
-  for (int r = threadIdx.x; r < R; r += kTcThreads) {
-    // the row's chunk partials, requested in independent batches of 8
-    const float2* p = rpart + (size_t(seg) * MT * kTileM + r) * n_chunks;
-    float M = -INFINITY, S = 0.f;
-    for (int k0 = 0; k0 < nch; k0 += 8) {
-      float2 q[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) q[k] = k0 + k < nch ? p[k0 + k] : make_float2(-INFINITY, 0.f);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        if (q[k].x == -INFINITY) continue;
-        if (q[k].x > M) {
-          S = S * __expf(M - q[k].x) + q[k].y;
-          M = q[k].x;
-        } else {
-          S += q[k].y * __expf(q[k].x - M);
-        }
-      }
-    }
-    lse[r] = M + __logf(S);
-  }
+  for (int r = threadIdx.x; r < R; r += kTcThreads)
+    lse[r] = rlse[size_t(seg) * MT * kTileM + r];
   cp_async_wait_all();
   fence_proxy_async_smem();
   __syncthreads();
   tc_fence_after();
 
   if (threadIdx.x == 0) {
+    if (!mbar_wait(&barQ, 0)) record_error(err, DEV_TIMEOUT_TMA);
+    tc_fence_after();
     const uint32_t idesc = make_idesc_bf16(kRefineRows2, Rp, false, false);
     const uint32_t ka = smem_u32(Ks), qa = smem_u32(Qs);
 #pragma unroll
@@ -579,10 +606,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 bool refine_fused_ok(int C) { return fuse_cpc(C) <= kFuseMaxCpc; }
 
+// Pass 1 -> row lse -> pass 2 (C > 4096).
+template <int D>
+static cudaError_t launch_refine_two_pass(const herald_dims& dm, const uint16_t* k_cache,
+                                          const int32_t* cand, const int32_t* n_cand, int C,
+                                          float2* rpart, float* rlse, float* s2,
+                                          const WsLayout& w, uint32_t* err,
+                                          const CUtensorMap& qmap, const CUtensorMap& qmap_all,
+                                          int bpt, float scale, cudaStream_t st) {
+  const int segs = dm.N * dm.Hkv;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(refine_pass1_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Ref1Cfg<D>::kSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(refine_pass2_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Ref2Cfg<D>::kSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  HERALD_CHECK_LAUNCH(launch_k("refine_pass1_kernel", refine_pass1_kernel<D>,
+                               dim3(w.n_chunks, w.MT_tok, segs), kTcThreads, Ref1Cfg<D>::kSmem,
+                               st, qmap, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv, dm.L_max, C,
+                               bpt, w.MT, w.n_chunks, scale, rpart, err));
+  HERALD_CHECK_LAUNCH(launch_k("refine_lse_kernel", refine_lse_kernel,
+                               dim3(cdiv(w.R, 8), segs), 256, 0, st, rpart, n_cand, C, w.R, w.MT,
+                               w.n_chunks, rlse));
+  HERALD_CHECK_LAUNCH(launch_k("refine_pass2_kernel", refine_pass2_kernel<D>,
+                               dim3(cdiv(C, kRefineRows2), segs), kTcThreads, Ref2Cfg<D>::kSmem,
+                               st, qmap_all, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv,
+                               dm.L_max, C, w.R, w.MT, scale, rlse, s2, err));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_refine(const herald_dims& dm, const uint16_t* q_block, const uint16_t* k_cache,
                           const int32_t* cand, const int32_t* n_cand, int C, float2* rpart,
-                          float* s2, const WsLayout& w, uint32_t* err, const CUtensorMap* qmap,
-                          cudaStream_t st) {
+                          float* rlse, float* s2, const WsLayout& w, uint32_t* err,
+                          const CUtensorMap* qmap, const CUtensorMap* qmap_all, cudaStream_t st) {
   const float scale = 1.0f / sqrtf(float(dm.d));
   const int segs = dm.N * dm.Hkv;
   cudaError_t e;
@@ -616,45 +677,13 @@ cudaError_t launch_refine(const herald_dims& dm, const uint16_t* q_block, const 
                           *qmap, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv, dm.L_max, C, bpt, cpc,
                           scale, s2, err);
   }
-  if (dm.d == 128) {
-    static bool attr = false;
-    if (!attr) {
-      e = cudaFuncSetAttribute(refine_pass1_kernel<128>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, Ref1Cfg<128>::kSmem);
-      if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(refine_pass2_kernel<128>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, Ref2Cfg<128>::kSmem);
-      if (e != cudaSuccess) return e;
-      attr = true;
-    }
-    HERALD_CHECK_LAUNCH(launch_k("refine_pass1_kernel", refine_pass1_kernel<128>, dim3(w.n_chunks, w.MT, segs), kTcThreads, Ref1Cfg<128>::kSmem,
-                               st, q_block, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv,
-                                     dm.L_max, C, w.R, w.MT, w.n_chunks, scale, rpart, err));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    HERALD_CHECK_LAUNCH(launch_k("refine_pass2_kernel", refine_pass2_kernel<128>, dim3(cdiv(C, kRefineRows2), segs), kTcThreads,
-                               Ref2Cfg<128>::kSmem, st, q_block, k_cache, cand, n_cand, dm.B,
-                                                          dm.Hq, dm.Hkv, dm.L_max, C, w.R, w.MT,
-                                                          w.n_chunks, scale, rpart, s2, err));
-  } else {
-    static bool attr = false;
-    if (!attr) {
-      e = cudaFuncSetAttribute(refine_pass1_kernel<64>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, Ref1Cfg<64>::kSmem);
-      if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(refine_pass2_kernel<64>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, Ref2Cfg<64>::kSmem);
-      if (e != cudaSuccess) return e;
-      attr = true;
-    }
-    HERALD_CHECK_LAUNCH(launch_k("refine_pass1_kernel", refine_pass1_kernel<64>, dim3(w.n_chunks, w.MT, segs), kTcThreads, Ref1Cfg<64>::kSmem,
-                              st, q_block, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv,
-                                    dm.L_max, C, w.R, w.MT, w.n_chunks, scale, rpart, err));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    HERALD_CHECK_LAUNCH(launch_k("refine_pass2_kernel", refine_pass2_kernel<64>, dim3(cdiv(C, kRefineRows2), segs), kTcThreads, Ref2Cfg<64>::kSmem,
-                              st, q_block, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv,
-                                    dm.L_max, C, w.R, w.MT, w.n_chunks, scale, rpart, s2, err));
-  }
-  return cudaGetLastError();
+  if (!qmap || !qmap_all) return cudaErrorInvalidValue;
+  const int bpt = kTileM / (dm.Hq / dm.Hkv);
+  if (dm.d == 128)
+    return launch_refine_two_pass<128>(dm, k_cache, cand, n_cand, C, rpart, rlse, s2, w, err,
+                                       *qmap, *qmap_all, bpt, scale, st);
+  return launch_refine_two_pass<64>(dm, k_cache, cand, n_cand, C, rpart, rlse, s2, w, err, *qmap,
+                                    *qmap_all, bpt, scale, st);
 }
 
 // ================================================================== attn

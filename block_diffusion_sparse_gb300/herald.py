@@ -21,7 +21,8 @@ EXPORTS = ("herald_workspace_size", "herald_status_string", "herald_last_error",
            "herald_workspace_error", "herald_select_stage1", "herald_select_stage2",
            "herald_select", "herald_gather", "herald_denoise_attn", "herald_append_kv",
            "herald_trace_begin", "herald_trace_end", "herald_trace_name",
-           "herald_select_stage2_noalloc", "herald_selftest_wait_timeout")
+           "herald_select_stage2_noalloc", "herald_selftest_wait_timeout",
+           "herald_workspace_size_exact", "herald_select_exact")
 
 
 class HeraldError(RuntimeError):
@@ -80,12 +81,17 @@ def lib() -> C.CDLL:
         L.herald_select_stage2_noalloc.argtypes = [Dims, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                    i32, vp, vp, vp]
         L.herald_selftest_wait_timeout.argtypes = [C.c_uint64, vp, vp]
+        L.herald_workspace_size_exact.argtypes = [Dims, i32, i32]
+        L.herald_workspace_size_exact.restype = sz
+        L.herald_select_exact.argtypes = [Dims, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, sz,
+                                          vp]
         L.herald_trace_begin.argtypes = [C.POINTER(vp), i32, i32]
         L.herald_trace_end.argtypes = []
         L.herald_trace_name.argtypes = [i32]
         L.herald_trace_name.restype = C.c_char_p
         for name in EXPORTS:
-            if name not in ("herald_workspace_size", "herald_status_string",
+            if name not in ("herald_workspace_size", "herald_workspace_size_exact",
+                            "herald_status_string",
                             "herald_last_error", "herald_trace_name"):
                 getattr(L, name).restype = C.c_int
         _lib = L
@@ -195,6 +201,19 @@ def herald_select_stage2_noalloc(d, q_block, k_cache, ctx_len, cand, n_cand, C_,
     _check(lib().herald_select_stage2_noalloc(d, _p(q_block), _p(k_cache), _p(ctx_len), _p(cand),
                                               _p(n_cand), int(C_), int(K), int(sink), int(local),
                                               int(P_max), _p(idx), _p(n_sel), _s(stream)))
+
+
+def herald_workspace_size_exact(d: Dims, K: int, P_max: int) -> int:
+    return int(lib().herald_workspace_size_exact(d, int(K), int(P_max)))
+
+
+def herald_select_exact(d, q_block, k_cache, ctx_len, K, sink, local, P_max, idx, n_sel, ws,
+                        ws_bytes=None, stream=None):
+    """Exact selection over the whole cache with all the block's queries
+    (see include/herald.h)."""
+    _check(lib().herald_select_exact(d, _p(q_block), _p(k_cache), _p(ctx_len), int(K), int(sink),
+                                     int(local), int(P_max), _p(idx), _p(n_sel), _p(ws),
+                                     _nbytes(ws, ws_bytes), _s(stream)))
 
 
 def herald_selftest_wait_timeout(limit_ns, ws, stream=None):

@@ -40,7 +40,7 @@ def background_sms(dims: H.Dims) -> int:
 
 class BlockPipeline:
     def __init__(self, dims: H.Dims, C: int, K: int, S: int, W: int, P: int, T: int,
-                 den_stream=None, sel_stream=None, sel_sms=None):
+                 den_stream=None, sel_stream=None, sel_sms=None, exact: bool = False):
         import torch
         self.torch = torch
         # SMs the overlapped stage-1 scan may occupy (0: all); measured on the
@@ -71,6 +71,14 @@ class BlockPipeline:
         self._idx, self._n_sel = P_(self.idx), P_(self.n_sel)
         self._pool_k = [P_(t) for t in self.pool_k]
         self._pool_v = [P_(t) for t in self.pool_v]
+        # the exact selection's own workspace (block_exact)
+        self.ws_exact = None
+        if exact:
+            nb = H.herald_workspace_size_exact(dims, K, P)
+            if nb == 0:
+                raise ValueError("exact selection does not support these shapes")
+            self.ws_exact = torch.zeros(nb, dtype=torch.uint8, device=dev)
+            self._ws_exact, self._ws_exact_bytes = P_(self.ws_exact), nb
 
     def _den(self):
         return self.den if self.den is not None else self.torch.cuda.current_stream()
@@ -108,6 +116,32 @@ class BlockPipeline:
                                       bv0 + t * bstep, o0 + t * ostep, 0.0, wd, wb, hd))
         if overlap:
             den.wait_stream(sel)
+        last = self.T - 1
+        chk(L.herald_append_kv(d, bk0 + last * bstep, bv0 + last * bstep, cx, kc, vc,
+                               int(bool(advance)), hd))
+
+
+    def block_exact(self, i: int, q_steps, block_k, block_v, k_cache, v_cache, ctx, out,
+                    advance: bool = True):
+        """Block i with the exact selection (every cached position scored
+        with the block's real queries) in place of the two stages: nothing
+        of it can run ahead of the block, so the step is one stream."""
+        den = self._den()
+        cur = i % 2
+        d, P, L, chk = self.d, self.P, H.lib(), H.check
+        hd = H.stream_handle(den)
+        q0, qstep = H.ptr(q_steps), H.step_bytes(q_steps)
+        bk0, bv0, bstep = H.ptr(block_k), H.ptr(block_v), H.step_bytes(block_k)
+        o0, ostep = H.ptr(out), H.step_bytes(out)
+        kc, vc, cx = H.ptr(k_cache), H.ptr(v_cache), H.ptr(ctx)
+        pk, pv = self._pool_k[cur], self._pool_v[cur]
+        wd, wb = self._ws_den, self.ws_bytes
+        chk(L.herald_select_exact(d, q0, kc, cx, self.K, self.S, self.W, P, self._idx,
+                                  self._n_sel, self._ws_exact, self._ws_exact_bytes, hd))
+        chk(L.herald_gather(d, self._idx, self._n_sel, P, kc, vc, pk, pv, hd))
+        for t in range(self.T):
+            chk(L.herald_denoise_attn(d, q0 + t * qstep, pk, pv, self._n_sel, P, bk0 + t * bstep,
+                                      bv0 + t * bstep, o0 + t * ostep, 0.0, wd, wb, hd))
         last = self.T - 1
         chk(L.herald_append_kv(d, bk0 + last * bstep, bv0 + last * bstep, cx, kc, vc,
                                int(bool(advance)), hd))

@@ -135,10 +135,10 @@ herald_status herald_select(herald_dims dims, const uint16_t *q_merge, const uin
  * arguments and outputs minus the workspace.
  *   Scratch lives in one static 4 MiB device array inside the library; every
  *   GPU that loads the library holds it until the process exits.  Shapes
- *   whose scratch -- 256 bytes + N*Hkv*ceil(B*G/128)*128*ceil(C/256)*8 bytes
- *   of row statistics + N*Hkv*C*4 bytes of scores per 128-row tile of the
- *   B*G query rows (one tile when C > 4096) -- exceed 4 MiB are rejected
- *   with HERALD_ERR_WORKSPACE_TOO_SMALL and a message.
+ *   whose scratch -- 256 bytes + N*Hkv*ceil(B*G/128)*128*(ceil(C/256)*8 + 4)
+ *   bytes of row statistics + N*Hkv*C*4 bytes of scores per row tile of
+ *   floor(128/G) whole tokens (one tile when C > 4096) -- exceed 4 MiB are
+ *   rejected with HERALD_ERR_WORKSPACE_TOO_SMALL and a message.
  *   The first call on a device resolves the array's device address (with
  *   that device current); make that first call before any stream capture.
  *   All calls share the array: calls that can overlap on the GPU (other
@@ -185,6 +185,26 @@ herald_status herald_denoise_attn(herald_dims dims, const uint16_t *q, const uin
 herald_status herald_append_kv(herald_dims dims, const uint16_t *block_k,
                                const uint16_t *block_v, int32_t *ctx_len, uint16_t *k_cache,
                                uint16_t *v_cache, int advance, void *stream);
+
+/* Exact selection, the accuracy reference for the merged-query stage 1
+ * ([MG]: exact attention of the block's queries predicts the important
+ * entries; [V3] approximates it with one merged query).  Every cached
+ * position is scored with all B*G real query rows of the block:
+ *   s[j] = sum over the rows r of softmax_j(q_r . k_j / sqrt(d)), j < ctx,
+ * (stage 2's score with the whole context as the candidate list); the K
+ * largest (lowest position on ties) are kept and the sink and local
+ * positions added exactly as herald_select_stage2 does.
+ *   q_block, k_cache, ctx_len, sink, local, P_max, idx, n_sel: as in
+ *           herald_select_stage2; 1 <= K <= 16384, K+sink+local <= P_max.
+ *   ws:     herald_workspace_size_exact(dims, K, P_max) bytes (0 = shape not
+ *           supported).
+ * Cost: two tensor-core passes over the whole cache per block (B*G times
+ * the merged query's contraction) instead of one merged-query scan. */
+size_t herald_workspace_size_exact(herald_dims dims, int K, int P_max);
+herald_status herald_select_exact(herald_dims dims, const uint16_t *q_block,
+                                  const uint16_t *k_cache, const int32_t *ctx_len, int K,
+                                  int sink, int local, int P_max, int32_t *idx, int32_t *n_sel,
+                                  void *ws, size_t ws_bytes, void *stream);
 
 /* Self-test of the device-side failure path (the pages have no
  * counterpart).  Every wait inside the library's kernels gives up after

@@ -131,6 +131,32 @@ def select(q_merge, q_block, k_cache, ctx, C_, K, S, W, P=None):
                 s2=s2, idx=idx, n_sel=n_sel)
 
 
+def exact_scores(q_block, k_cache, ctx):
+    """Exact selection score (MAGE author page, abstract: exact attention of
+    the block's queries predicts the important entries; HERALD v3 abstract:
+    the merged query approximates it): every cached position j < ctx is a
+    candidate of step 4, so s[j] = sum over the B*G rows of the softmax over
+    the whole context.  Returns (cand = arange padded with -1, n_cand, s)."""
+    k = np.asarray(k_cache)
+    N, Hkv, L_max, _ = k.shape
+    cx = np.asarray(ctx, np.int64)
+    cand = np.full((N, Hkv, L_max), -1, np.int32)
+    n_cand = np.empty((N, Hkv), np.int32)
+    for n in range(N):
+        L = int(min(max(cx[n], 0), L_max))
+        cand[n, :, :L] = np.arange(L, dtype=np.int32)
+        n_cand[n, :] = L
+    return cand, n_cand, stage2_scores(q_block, k_cache, cand, n_cand)
+
+
+def select_exact(q_block, k_cache, ctx, K, S, W, P=None):
+    """The exact selection: step 5 (top-K, then the sink/local union) over
+    the exact scores."""
+    cand, n_cand, s = exact_scores(q_block, k_cache, ctx)
+    idx, n_sel = select_final(ctx, np.shape(k_cache)[2], cand, n_cand, s, K, S, W, P)
+    return dict(cand=cand, n_cand=n_cand, s=s, idx=idx, n_sel=n_sel)
+
+
 def sparse_attn(q, k_cache, v_cache, idx, n_sel, block_k, block_v, scale=None,
                 with_wsum=False):
     """Step 6: out [N,B,Hq,d] over the selected rows plus the B block keys."""

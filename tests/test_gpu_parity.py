@@ -388,3 +388,48 @@ def test_full_size_llama_layer_sampled_segments():
         s2 = oracle.stage2_scores(f64(xs["q_steps"][0]), f64(xs["k_cache"]), cand_o, nc_o)
         idx_o, ns_o = oracle.select_final(xs["ctx"], w.L_max, cand_o, nc_o, s2, w.K, w.S, w.W, w.P)
         assert len(set(idx[n, g, : ns[n, g]].tolist()) ^ set(idx_o[0, 0, : ns_o[0, 0]].tolist())) <= 4
+
+
+@pytest.mark.parametrize("w", [
+    TINY.scaled(T=1),                                   # L_pad <= 4096: the fused refine
+    _case("exact-g7-ragged", Hq=14, Hkv=2, d=128, L=5000, B=32, C=512, K=200, S=8, W=40,
+          n_planted=20, index=25),                      # two-pass refine over 5120 slots
+    _case("exact-n2-d64", N=2, Hq=8, Hkv=2, d=64, L=3001, B=16, C=256, K=100, S=4, W=33,
+          n_planted=12, index=26),
+], ids=lambda w: w.name)
+def test_exact_selection(w):
+    """Every cached position scored with all the block's real queries, top-K
+    plus sink/local, against the oracle's exact selection."""
+    r = Run(w)
+    x = r.x
+    if w.name == "exact-n2-d64":
+        x["ctx"] = np.array([3001, 2500], np.int32)  # ragged contexts
+        r.ctx = dev(x["ctx"])
+    d = r.d
+    ws_bytes = H.herald_workspace_size_exact(d, w.K, w.P)
+    assert ws_bytes > 0
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    H.herald_select_exact(d, r.q_steps[0], r.k, r.ctx, w.K, w.S, w.W, w.P, r.idx, r.n_sel, ws)
+    torch.cuda.synchronize()
+    assert H.herald_workspace_error(ws) == 0
+    o = oracle.select_exact(f64(x["q_steps"][0]), f64(x["k_cache"]), x["ctx"], w.K, w.S, w.W,
+                            w.P)
+    idx, ns = r.idx.cpu().numpy(), r.n_sel.cpu().numpy()
+    for n in range(w.N):
+        for g in range(w.Hkv):
+            check_selection(idx[n, g], int(ns[n, g]), o["idx"][n, g], int(o["n_sel"][n, g]),
+                            o["cand"][n, g], o["n_cand"][n, g], o["s"][n, g], w,
+                            int(x["ctx"][n]), f"{w.name} n={n} g={g}")
+
+
+def test_exact_selection_workspace_checks():
+    w = TINY
+    d = H.dims_of(w)
+    need = H.herald_workspace_size_exact(d, w.K, w.P)
+    assert H.herald_workspace_size_exact(d, 0, w.P) == 0
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    idx = torch.zeros((w.N, w.Hkv, w.P), dtype=torch.int32, device="cuda")
+    ns = torch.zeros((w.N, w.Hkv), dtype=torch.int32, device="cuda")
+    with pytest.raises(H.HeraldError) as e:
+        H.herald_select_exact(d, idx, idx, ns, w.K, w.S, w.W, w.P, idx, ns, ws, need - 256)
+    assert e.value.status == 3

@@ -343,3 +343,41 @@ def test_bf16_helpers_round_to_nearest_even():
     np.testing.assert_allclose(back[4], 3.0e-3, rtol=2 ** -8)
     ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     np.testing.assert_array_equal(bits, ref)
+
+
+def test_exact_selection_with_one_row_is_the_top_k_of_dot_products():
+    """B = G = 1: the exact score is the softmax of the single query's dot
+    products over the whole context, so its top-K are the K largest dot
+    products (numpy argsort), before the sink/local union."""
+    rng = np.random.default_rng(5)
+    N, Hkv, L, d, K = 1, 2, 300, 16, 20
+    q = rng.standard_normal((N, 1, Hkv, d))
+    k = rng.standard_normal((N, Hkv, L, d))
+    ctx = np.array([L], np.int32)
+    r = oracle.select_exact(q, k, ctx, K, 0, 0)
+    for g in range(Hkv):
+        dots = k[0, g] @ q[0, 0, g]
+        want = np.sort(np.argsort(-dots, kind="stable")[:K])
+        assert r["n_sel"][0, g] == K
+        np.testing.assert_array_equal(r["idx"][0, g, :K], want)
+        p = np.exp(dots / np.sqrt(d) - np.max(dots / np.sqrt(d)))
+        np.testing.assert_allclose(r["s"][0, g, :L], p / p.sum(), rtol=1e-12)
+
+
+def test_exact_scores_sum_to_rows_and_ignore_positions_past_the_context():
+    rng = np.random.default_rng(6)
+    N, B, Hq, Hkv, Lm, d = 2, 3, 4, 2, 50, 8
+    q = rng.standard_normal((N, B, Hq, d))
+    k = rng.standard_normal((N, Hkv, Lm, d))
+    ctx = np.array([50, 31], np.int32)
+    cand, nc, s = oracle.exact_scores(q, k, ctx)
+    G = Hq // Hkv
+    for n in range(N):
+        for g in range(Hkv):
+            L = ctx[n]
+            assert nc[n, g] == L
+            np.testing.assert_allclose(s[n, g, :L].sum(), B * G, rtol=1e-12)
+    # changing a key past the context changes nothing
+    k2 = k.copy()
+    k2[1, :, 40:] += 5.0
+    np.testing.assert_array_equal(oracle.exact_scores(q, k2, ctx)[2][1, :, :31], s[1, :, :31])
