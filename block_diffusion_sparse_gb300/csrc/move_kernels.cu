@@ -79,12 +79,14 @@ cudaError_t launch_gather(const herald_dims& dm, const int32_t* idx, const int32
   return cudaGetLastError();
 }
 
-// grid N, block 256: one CTA per sequence so that reading ctx_len[n] and
+// grid N, block 1024: one CTA per sequence so that reading ctx_len[n] and
 // advancing it cannot race with another CTA.  Each thread moves up to
-// kAppendBatch 16-byte chunks of K and of V per round, all loads first.
-constexpr int kAppendBatch = 8;
+// kAppendBatch 16-byte chunks of K and of V per round, all loads first
+// (1024 threads x 4: a block of 32 tokens x 8 KV heads x d = 128 is one round).
+constexpr int kAppendBatch = 4;
+constexpr int kAppendThreads = 1024;
 
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kAppendThreads)
     append_kernel(const uint16_t* __restrict__ bk, const uint16_t* __restrict__ bv, int B,
                   int Hkv, int d, int L_max, int32_t* __restrict__ ctx,
                   uint16_t* __restrict__ kc, uint16_t* __restrict__ vc, int advance) {
@@ -94,11 +96,11 @@ __global__ void __launch_bounds__(256)
   if (threadIdx.x == 0) L0 = min(max(ctx[n], 0), L_max);
   __syncthreads();
   const int cpr = d / 8, total = B * Hkv * cpr;
-  for (int q0 = 0; q0 < total; q0 += 256 * kAppendBatch) {
+  for (int q0 = 0; q0 < total; q0 += kAppendThreads * kAppendBatch) {
     uint4 k[kAppendBatch], v[kAppendBatch];
 #pragma unroll
     for (int u = 0; u < kAppendBatch; ++u) {
-      const int q = q0 + u * 256 + threadIdx.x;
+      const int q = q0 + u * kAppendThreads + threadIdx.x;
       if (q < total) {
         const int c = q % cpr, bg = q / cpr, g = bg % Hkv, b = bg / Hkv;
         const size_t src = ((size_t(n) * B + b) * Hkv + g) * d + c * 8;
@@ -108,7 +110,7 @@ __global__ void __launch_bounds__(256)
     }
 #pragma unroll
     for (int u = 0; u < kAppendBatch; ++u) {
-      const int q = q0 + u * 256 + threadIdx.x;
+      const int q = q0 + u * kAppendThreads + threadIdx.x;
       if (q < total) {
         const int c = q % cpr, bg = q / cpr, g = bg % Hkv, b = bg / Hkv;
         const int j = L0 + b;
@@ -127,7 +129,7 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_append(const herald_dims& dm, const uint16_t* block_k, const uint16_t* block_v,
                           int32_t* ctx, uint16_t* k_cache, uint16_t* v_cache, int advance,
                           cudaStream_t st) {
-  HERALD_CHECK_LAUNCH(launch_k("append_kernel", append_kernel, dm.N, 256, 0, st, block_k, block_v, dm.B, dm.Hkv, dm.d, dm.L_max, ctx,
+  HERALD_CHECK_LAUNCH(launch_k("append_kernel", append_kernel, dm.N, kAppendThreads, 0, st, block_k, block_v, dm.B, dm.Hkv, dm.d, dm.L_max, ctx,
                                       k_cache, v_cache, advance));
   return cudaGetLastError();
 }
