@@ -121,12 +121,11 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor map [rows][d] with a box of 64 columns x box_rows rows and
-// 128-byte swizzle (the UMMA K-major shared-memory layout).
 // bf16 tensor map of 2 or 3 dimensions, 128-byte swizzle.  A map depends
 // only on (base, rank, extents, box): recently encoded ones are reused (per
-// thread, round-robin), which keeps the per-call host cost of the steady
-// state low -- a block step encodes a few maps per attention call.
+// thread, a direct-mapped table of 64 entries), which keeps the per-call
+// host cost of the steady state low -- a block step encodes a few maps per
+// attention call.
 static herald_status encode_map(const void* base, int rank, const uint64_t* extent,
                                 const uint32_t* box_in, CUtensorMap* map) {
   struct Entry {
@@ -136,17 +135,17 @@ static herald_status encode_map(const void* base, int rank, const uint64_t* exte
     uint32_t box[3];
     CUtensorMap map;
   };
+  // direct-mapped: one slot per key hash, a lookup is one comparison
   constexpr int kEntries = 64;
   thread_local Entry cache[kEntries] = {};
-  thread_local int next = 0;
-  for (const Entry& e : cache) {
-    if (e.base != base || e.rank != rank) continue;
-    bool same = true;
-    for (int i = 0; i < rank; ++i) same = same && e.ext[i] == extent[i] && e.box[i] == box_in[i];
-    if (same) {
-      *map = e.map;
-      return HERALD_OK;
-    }
+  uint64_t hkey = reinterpret_cast<uintptr_t>(base) >> 4;
+  for (int i = 0; i < rank; ++i) hkey = hkey * 1000003u ^ (extent[i] * 31u + box_in[i]);
+  Entry& e = cache[(hkey ^ (hkey >> 17) ^ (hkey >> 33)) % kEntries];
+  bool same = e.base == base && e.rank == rank;
+  for (int i = 0; same && i < rank; ++i) same = e.ext[i] == extent[i] && e.box[i] == box_in[i];
+  if (same) {
+    *map = e.map;
+    return HERALD_OK;
   }
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(HERALD_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
@@ -164,8 +163,6 @@ static herald_status encode_map(const void* base, int rank, const uint64_t* exte
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(HERALD_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
-  Entry& e = cache[next];
-  next = (next + 1) % kEntries;
   e.base = base;
   e.rank = rank;
   for (int i = 0; i < rank; ++i) {
@@ -176,6 +173,8 @@ static herald_status encode_map(const void* base, int rank, const uint64_t* exte
   return HERALD_OK;
 }
 
+// 2-D bf16 tensor map [rows][d] with a box of 64 columns x box_rows rows and
+// 128-byte swizzle (the UMMA K-major shared-memory layout).
 herald_status encode_rows_map(const void* base, uint64_t rows, int d, uint32_t box_rows,
                               CUtensorMap* map) {
   const uint64_t ext[2] = {uint64_t(d), rows};

@@ -974,6 +974,10 @@ __global__ void __launch_bounds__(kTkThreads)
 #pragma unroll
     for (int k = 0; k < kPer; ++k) pk[k] = (k < E && i0 + k < C) ? __ldg(cd + i0 + k) : -1;
   }
+  // shared state cleared while the loads are in flight
+  for (int i = threadIdx.x; i < kHistBins; i += kTkThreads) h[i] = 0u;
+  for (int i = threadIdx.x; i < kMaxC / 32; i += kTkThreads) taken[i] = 0u;
+  if (threadIdx.x == 0) s_cnt = 0;
   float x[kPer];
 #pragma unroll
   for (int k = 0; k < kPer; ++k) x[k] = 0.f;
@@ -1003,9 +1007,6 @@ __global__ void __launch_bounds__(kTkThreads)
   const bool take_all = (Ke == nc);
   uint32_t b1 = 0;  // bin of the K-th largest; bins above it are kept whole
   if (!take_all && Ke > 0) {
-    for (int i = threadIdx.x; i < kHistBins; i += kTkThreads) h[i] = 0u;
-    for (int i = threadIdx.x; i < kMaxC / 32; i += kTkThreads) taken[i] = 0u;
-    if (threadIdx.x == 0) s_cnt = 0;
     __syncthreads();
 #pragma unroll
     for (int k = 0; k < kPer; ++k)
