@@ -13,7 +13,8 @@ pytestmark = pytest.mark.gpu
 import oracle
 from block_diffusion_sparse_gb300 import herald as H
 from block_diffusion_sparse_gb300 import synth
-from block_diffusion_sparse_gb300.workloads import LLAMA_64K, QWEN_32K, TINY, Workload
+from block_diffusion_sparse_gb300.workloads import (LLAMA_64K, LONG_128K_HOST, QWEN_32K, QWEN_STACK,
+                                                    TINY, Workload)
 from helpers import ATTN_ATOL, BAND, assert_sets_within_band, bf16_dev_to_f64, dev, f64, segment
 
 
@@ -388,6 +389,61 @@ def test_full_size_llama_layer_sampled_segments():
         s2 = oracle.stage2_scores(f64(xs["q_steps"][0]), f64(xs["k_cache"]), cand_o, nc_o)
         idx_o, ns_o = oracle.select_final(xs["ctx"], w.L_max, cand_o, nc_o, s2, w.K, w.S, w.W, w.P)
         assert len(set(idx[n, g, : ns[n, g]].tolist()) ^ set(idx_o[0, 0, : ns_o[0, 0]].tolist())) <= 4
+
+
+def _check_sampled_segments(r, w, pairs, tol_diff=4):
+    """Oracle end to end on sampled (sequence, KV head) segments of a full-size
+    run: planted keys kept, selection within the tie band's reach, attention
+    within tolerance."""
+    idx, ns = r.idx.cpu().numpy(), r.n_sel.cpu().numpy()
+    out = bf16_dev_to_f64(r.out)
+    for n, g in pairs:
+        xs = segment(r.x, w, n, g)
+        qbar = oracle.merged_query(f64(xs["q_merge"]))
+        _, _, s1 = oracle.stage1_scores(qbar, f64(xs["k_cache"]), xs["ctx"])
+        cand_o, nc_o = oracle.topc(s1, xs["ctx"], w.C)
+        planted = set(int(p) for p in r.x["planted"][n])
+        if len(planted) <= w.K:  # (the 128K workload plants more keys than K keeps)
+            assert planted <= set(idx[n, g, : ns[n, g]].tolist())
+        ref = oracle.sparse_attn(f64(xs["q_steps"][0]), f64(xs["k_cache"]), f64(xs["v_cache"]),
+                                 idx[n:n + 1, g:g + 1], ns[n:n + 1, g:g + 1],
+                                 f64(xs["block_k"][0]), f64(xs["block_v"][0]))
+        hs = slice(g * w.G, (g + 1) * w.G)
+        assert np.abs(out[n:n + 1, :, hs] - ref).max() <= ATTN_ATOL
+        s2 = oracle.stage2_scores(f64(xs["q_steps"][0]), f64(xs["k_cache"]), cand_o, nc_o)
+        idx_o, ns_o = oracle.select_final(xs["ctx"], w.L_max, cand_o, nc_o, s2, w.K, w.S, w.W,
+                                          w.P)
+        diff = set(idx[n, g, : ns[n, g]].tolist()) ^ set(idx_o[0, 0, : ns_o[0, 0]].tolist())
+        assert len(diff) <= tol_diff, f"n={n} g={g}: {sorted(diff)[:8]}"
+
+
+def test_full_size_long_context_host_resident_sampled_segments():
+    """128K context with the cache in pinned host memory (scan over the host
+    link, candidate rows staged for the two-pass refine, pool gathered over
+    the link): two sampled segments end to end against the oracle."""
+    w = LONG_128K_HOST.scaled(T=1)
+    r = Run(w)
+    r.k = torch.from_numpy(r.x["k_cache"].view(np.int16)).pin_memory()
+    r.v = torch.from_numpy(r.x["v_cache"].view(np.int16)).pin_memory()
+    r.select()
+    r.gather()
+    r.attn(0)
+    torch.cuda.synchronize()
+    assert r.error_word() == 0
+    _check_sampled_segments(r, w, ((0, 0), (0, 5)))
+
+
+def test_full_size_stack_layer_sampled_segments():
+    """One layer of the 28-layer stack (8 sequences x 32K): two sampled
+    segments end to end against the oracle."""
+    w = QWEN_STACK.scaled(T=1)
+    r = Run(w)
+    r.select()
+    r.gather()
+    r.attn(0)
+    torch.cuda.synchronize()
+    assert r.error_word() == 0
+    _check_sampled_segments(r, w, ((0, 1), (7, 3)))
 
 
 @pytest.mark.parametrize("w", [
