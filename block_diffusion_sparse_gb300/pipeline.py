@@ -61,6 +61,7 @@ class BlockPipeline:
         self.pool_v = [torch.zeros_like(self.pool_k[0]) for _ in range(2)]
         self.den = den_stream
         self.sel = sel_stream if sel_stream is not None else torch.cuda.Stream()
+        self._graphs = {}  # captured blocks, by buffers and parity (block(graph=True))
         # addresses of the persistent buffers, resolved once: a block issues
         # ~T+5 library calls, and per-call marshalling would otherwise cost
         # more host time than the kernels take on the GPU
@@ -89,9 +90,41 @@ class BlockPipeline:
                                self.n_cand[slot], self.ws_sel, self.ws_bytes, self._den())
 
     def block(self, i: int, q_steps, block_k, block_v, k_cache, v_cache, ctx, out,
-              next_k_cache=None, advance: bool = True, overlap: bool = True):
+              next_k_cache=None, advance: bool = True, overlap: bool = True,
+              graph: bool = False):
         """Runs block i: q_steps/block_k/block_v hold the T steps' inputs,
-        out[t] receives step t's attention output."""
+        out[t] receives step t's attention output.
+
+        graph=True replays a CUDA graph of the block's library calls, captured
+        the first time these buffers (and the block's parity) are seen; that
+        first call runs the block directly.  The calls then cost one graph
+        launch of host time instead of ~T+5 library calls."""
+        if not graph:
+            return self._block(i, q_steps, block_k, block_v, k_cache, v_cache, ctx, out,
+                               next_k_cache, advance, overlap)
+        torch = self.torch
+        P_ = H.ptr
+        key = (i % 2, P_(q_steps), P_(block_k), P_(block_v), P_(k_cache), P_(v_cache), P_(ctx),
+               P_(out), P_(k_cache if next_k_cache is None else next_k_cache), bool(advance),
+               bool(overlap))
+        g = self._graphs.get(key)
+        if g is not None:
+            g.replay()
+            return
+        self._block(i, q_steps, block_k, block_v, k_cache, v_cache, ctx, out, next_k_cache,
+                    advance, overlap)
+        g = torch.cuda.CUDAGraph()
+        den = torch.cuda.current_stream()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(den)
+        with torch.cuda.graph(g, stream=cap):
+            self._block(i, q_steps, block_k, block_v, k_cache, v_cache, ctx, out, next_k_cache,
+                        advance, overlap)
+        den.wait_stream(cap)
+        self._graphs[key] = g
+
+    def _block(self, i, q_steps, block_k, block_v, k_cache, v_cache, ctx, out, next_k_cache,
+               advance, overlap):
         den, sel = self._den(), self.sel
         cur, nxt = i % 2, (i + 1) % 2
         nk = k_cache if next_k_cache is None else next_k_cache

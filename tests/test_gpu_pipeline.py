@@ -17,8 +17,10 @@ from block_diffusion_sparse_gb300.workloads import Workload
 from helpers import ATTN_ATOL, bf16_dev_to_f64, dev, f64
 
 
-@pytest.mark.parametrize("overlap", [True, False])
-def test_three_blocks_match_oracle_schedule(overlap):
+@pytest.mark.parametrize("overlap,graph", [(True, False), (False, False), (True, True)])
+def test_three_blocks_match_oracle_schedule(overlap, graph):
+    """graph=True: every block's inputs are copied into the same buffers, so
+    block 2 replays the CUDA graph captured for block 0 (same parity)."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     nb = 3
@@ -33,10 +35,17 @@ def test_three_blocks_match_oracle_schedule(overlap):
     pipe = BlockPipeline(d, w.C, w.K, w.S, w.W, w.P, w.T)
     pipe.prime(dev(x0["q_merge"]), k, ctx)
     got = []
+    fixed = None
     for i, xb in enumerate(blocks):
         out = torch.zeros((w.T, w.N, w.B, w.Hq, w.d), dtype=torch.int16, device="cuda")
-        pipe.block(i, dev(xb["q_steps"]), dev(xb["block_k"]), dev(xb["block_v"]), k, v, ctx,
-                   out, advance=True, overlap=overlap)
+        qs, bk, bv = dev(xb["q_steps"]), dev(xb["block_k"]), dev(xb["block_v"])
+        if graph:  # the same device buffers for every block
+            if fixed is None:
+                fixed = [torch.empty_like(t) for t in (qs, bk, bv, out)]
+            for dst, src in zip(fixed, (qs, bk, bv, out)):
+                dst.copy_(src)
+            qs, bk, bv, out = fixed
+        pipe.block(i, qs, bk, bv, k, v, ctx, out, advance=True, overlap=overlap, graph=graph)
         torch.cuda.synchronize()
         got.append((pipe.idx.cpu().numpy().copy(), pipe.n_sel.cpu().numpy().copy(),
                     bf16_dev_to_f64(out)))
