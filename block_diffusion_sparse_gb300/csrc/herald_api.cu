@@ -261,7 +261,7 @@ herald_status run_stage2(const herald_dims& dm, const uint16_t* q_block, const u
   if (qs != HERALD_OK) return qs;
   float* rlse = at<float>(ws, w.rlse);
   if (is_device_memory(k_cache)) {
-    HERALD_TRY_CUDA(launch_refine(dm, q_block, k_cache, cand, n_cand, C, at<float2>(ws, w.rpart),
+    HERALD_TRY_CUDA(launch_refine(dm, k_cache, cand, n_cand, C, at<float2>(ws, w.rpart),
                                   rlse, at<float>(ws, w.s2), w, err, &qmap, &qmap_all, st),
                     "refine launch");
   } else {
@@ -274,7 +274,7 @@ herald_status run_stage2(const herald_dims& dm, const uint16_t* q_block, const u
                     "candidate staging launch");
     herald_dims staged = dm;
     staged.L_max = C;  // rows per (sequence, KV head) in the staging buffer
-    HERALD_TRY_CUDA(launch_refine(staged, q_block, kstage, nullptr, n_cand, C,
+    HERALD_TRY_CUDA(launch_refine(staged, kstage, nullptr, n_cand, C,
                                   at<float2>(ws, w.rpart), rlse, at<float>(ws, w.s2), w, err,
                                   &qmap, &qmap_all, st),
                     "refine launch");
@@ -478,7 +478,7 @@ herald_status herald_select_exact(herald_dims dims, const uint16_t* q_block,
                   "clear histograms");
   HERALD_TRY_CUDA(launch_exact_counts(dims, ctx_len, n_cand, st), "exact counts launch");
   // every cached position is a candidate (row = slot, stride L_pad)
-  HERALD_TRY_CUDA(launch_refine(dims, q_block, k_cache, nullptr, n_cand, L_pad,
+  HERALD_TRY_CUDA(launch_refine(dims, k_cache, nullptr, n_cand, L_pad,
                                 at<float2>(ws, x.rpart), at<float>(ws, x.rlse), s, w, err,
                                 &qmap, &qmap_all, st),
                   "refine launch");
@@ -591,11 +591,13 @@ herald_status herald_gather(herald_dims dims, const int32_t* idx, const int32_t*
   return HERALD_OK;
 }
 
-herald_status herald_denoise_attn(herald_dims dims, const uint16_t* q, const uint16_t* pool_k,
-                                  const uint16_t* pool_v, const int32_t* n_sel, int P_max,
-                                  const uint16_t* block_k, const uint16_t* block_v,
-                                  uint16_t* out, float scale, void* ws, size_t ws_bytes,
-                                  void* stream) {
+}  // extern "C"
+
+namespace {
+herald_status denoise_attn(herald_dims dims, const uint16_t* q, const uint16_t* pool_k,
+                           const uint16_t* pool_v, const int32_t* n_sel, int P_max,
+                           const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
+                           float scale, void* ws, size_t ws_bytes, bool settled, void* stream) {
   g_err[0] = 0;
   HERALD_RET_IF(check_dims(dims));
   HERALD_RET_IF(check_pmax(dims, P_max));
@@ -629,10 +631,32 @@ herald_status herald_denoise_attn(herald_dims dims, const uint16_t* q, const uin
   }
   HERALD_TRY_CUDA(launch_attn(dims, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale,
                               w, at<float>(ws, w.opart), at<float2>(ws, w.ml),
-                              at<uint32_t>(ws, w.err), pool ? &maps : nullptr,
+                              at<uint32_t>(ws, w.err), pool ? &maps : nullptr, settled,
                               static_cast<cudaStream_t>(stream)),
                   "attention launch");
   return HERALD_OK;
+}
+}  // namespace
+
+extern "C" {
+
+herald_status herald_denoise_attn(herald_dims dims, const uint16_t* q, const uint16_t* pool_k,
+                                  const uint16_t* pool_v, const int32_t* n_sel, int P_max,
+                                  const uint16_t* block_k, const uint16_t* block_v,
+                                  uint16_t* out, float scale, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  return denoise_attn(dims, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale, ws,
+                      ws_bytes, false, stream);
+}
+
+herald_status herald_denoise_attn_settled(herald_dims dims, const uint16_t* q,
+                                          const uint16_t* pool_k, const uint16_t* pool_v,
+                                          const int32_t* n_sel, int P_max,
+                                          const uint16_t* block_k, const uint16_t* block_v,
+                                          uint16_t* out, float scale, void* ws, size_t ws_bytes,
+                                          void* stream) {
+  return denoise_attn(dims, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale, ws,
+                      ws_bytes, true, stream);
 }
 
 herald_status herald_append_kv(herald_dims dims, const uint16_t* block_k, const uint16_t* block_v,

@@ -117,7 +117,7 @@ herald_status herald_select_stage2_noalloc(herald_dims dims, const uint16_t* q_b
   // at zero; the statistics and scores are fully rewritten before use
   cudaError_t e = cudaMemsetAsync(err, 0, sizeof(uint32_t), st);
   if (e == cudaSuccess)
-    e = launch_refine(dims, q_block, k_cache, cand, n_cand, C,
+    e = launch_refine(dims, k_cache, cand, n_cand, C,
                       reinterpret_cast<float2*>(base + rpart_off),
                       reinterpret_cast<float*>(base + rlse_off),
                       reinterpret_cast<float*>(base + s2_off), full, err, &qmap, &qmap_all, st);

@@ -150,8 +150,8 @@ cudaError_t launch_topc(const herald_dims& dm, const float* s1, const uint32_t* 
 // of all B tokens (the two-pass refine's second pass; may be null when
 // C <= 4096).  rlse: [N*Hkv][MT*128] floats for the two-pass refine.
 bool refine_fused_ok(int C);
-cudaError_t launch_refine(const herald_dims& dm, const uint16_t* q_block, const uint16_t* k_cache,
-                          const int32_t* cand, const int32_t* n_cand, int C, float2* rpart,
+cudaError_t launch_refine(const herald_dims& dm, const uint16_t* k_cache, const int32_t* cand,
+                           const int32_t* n_cand, int C, float2* rpart,
                           float* rlse, float* s2, const WsLayout& w, uint32_t* err,
                           const CUtensorMap* qmap, const CUtensorMap* qmap_all, cudaStream_t st);
 // Host-side tensor map of a [tokens][heads][d] bf16 array, box 64 x
@@ -187,7 +187,7 @@ cudaError_t launch_attn(const herald_dims& dm, const uint16_t* q, const uint16_t
                         const uint16_t* pool_v, const int32_t* n_sel, int P_max,
                         const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
                         float scale, const WsLayout& w, float* opart, float2* ml, uint32_t* err,
-                        const PoolMaps* maps, cudaStream_t st);
+                        const PoolMaps* maps, bool settled, cudaStream_t st);
 // exact selection: per-segment candidate counts = context lengths; the
 // refine's score partials summed in place (stride floats per segment) and
 // histogrammed for the top-K radix select

@@ -640,9 +640,8 @@ static cudaError_t launch_refine_two_pass(const herald_dims& dm, const uint16_t*
   return cudaGetLastError();
 }
 
-cudaError_t launch_refine(const herald_dims& dm, const uint16_t* q_block, const uint16_t* k_cache,
-                          const int32_t* cand, const int32_t* n_cand, int C, float2* rpart,
-                          float* rlse, float* s2, const WsLayout& w, uint32_t* err,
+cudaError_t launch_refine(const herald_dims& dm, const uint16_t* k_cache, const int32_t* cand,
+                          const int32_t* n_cand, int C, float2* rpart, float* rlse, float* s2, const WsLayout& w, uint32_t* err,
                           const CUtensorMap* qmap, const CUtensorMap* qmap_all, cudaStream_t st) {
   const float scale = 1.0f / sqrtf(float(dm.d));
   const int segs = dm.N * dm.Hkv;
@@ -1160,7 +1159,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                      const __grid_constant__ CUtensorMap bkmap,
                      const __grid_constant__ CUtensorMap bvmap,
                      const int32_t* __restrict__ n_sel, int P_max, int B, int Hq, int Hkv,
-                     int bpt, int kpc, float scale, uint16_t* __restrict__ out, uint32_t* err) {
+                     int bpt, int kpc, float scale, int settled, uint16_t* __restrict__ out,
+                     uint32_t* err) {
   constexpr int H = D / 64;
   constexpr int OROW = D + 8;  // fp16 row stride of O partials (16-byte padding)
   extern __shared__ uint8_t smem_raw[];
@@ -1210,50 +1210,56 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tbase = tmem_base;
   const int b0 = mt * bpt;                  // first token of the tile
   const int rows_t = min(bpt, B - b0) * G;  // query rows of the tile
-  griddep_enter();
-  // barK: Q + pool K (if any) + block K (last CTA); barV: pool V + block V.
-  // The query tile goes first, before n_sel is known (its bytes may
-  // complete on barK before they are expected: the phase still needs the
-  // arrive below).  Boxes past the tensor's end are zero-filled; rows past
-  // this tile's tokens or past the valid keys are never used.
   const uint32_t qbytes = uint32_t(H * G * bpt * 128);
+  const int k0 = int(rank) * kpc;
+  const bool has_blk = rank == kPoolCtas - 1 && B > 0;  // the block keys
+  // barK: Q + pool K (if any) + block K (last CTA); barV: pool V + block V.
+  // Boxes past the tensor's end are zero-filled; rows past this tile's
+  // tokens or past the valid keys are never used.
+  auto pool_loads = [&](int nkp) {  // thread 0: the expected bytes + pool K/V
+    const uint32_t kb = nkp > 0 ? uint32_t(H * kpc * 128) : 0u;
+    const uint32_t bb = has_blk ? uint32_t(H * Bp * 128) : 0u;
+    mbar_arrive_expect_tx(&barK, qbytes + kb + bb);
+    if (nkp > 0 || has_blk) mbar_arrive_expect_tx(&barV, kb + bb);
+    if (nkp > 0) {
+#pragma unroll
+      for (int hv = 0; hv < H; ++hv)
+        tma_load_2d(Ks + hv * kpc * 128, &kmap, &barK, hv * 64, seg * P_max + k0);
+#pragma unroll
+      for (int hv = 0; hv < H; ++hv)
+        tma_load_2d(Vs + hv * kpc * 128, &vmap, &barV, hv * 64, seg * P_max + k0);
+    }
+  };
+  int nkp = 0;  // valid pool keys of this CTA
+  if (settled) {
+    // The caller guarantees that the pool and n_sel were written before the
+    // previous launch on the stream began; that launch started this one only
+    // after waiting for its own predecessor (every kernel here does), so
+    // they are final: load them while the predecessor finishes.  n_sel is
+    // read through L2, the point of coherence.
+    nkp = min(max(min(max(__ldcg(n_sel + seg), 0), P_max) - k0, 0), kpc);
+    if (threadIdx.x == 0) pool_loads(nkp);
+  }
+  griddep_enter();
+  // the query tile first, before n_sel is known (its bytes may complete on
+  // barK before they are expected: the phase still needs the arrive)
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int hv = 0; hv < H; ++hv)
       tma_load_3d(Qs + hv * kTileM * 128, &qmap, &barK, hv * 64, g * G, n * B + b0);
   }
-  const int ns = min(max(n_sel[seg], 0), P_max);
-  const int k0 = int(rank) * kpc;
-  const int nkp = min(max(ns - k0, 0), kpc);           // valid pool keys of this CTA
-  const bool has_blk = rank == kPoolCtas - 1 && B > 0;  // the block keys
+  if (!settled) {
+    nkp = min(max(min(max(n_sel[seg], 0), P_max) - k0, 0), kpc);
+    if (threadIdx.x == 0) pool_loads(nkp);
+  }
   const bool any = nkp > 0 || has_blk;
-  if (threadIdx.x == 0) {
-    const uint32_t kb = nkp > 0 ? uint32_t(H * kpc * 128) : 0u;
-    const uint32_t bb = has_blk ? uint32_t(H * Bp * 128) : 0u;
-    mbar_arrive_expect_tx(&barK, qbytes + kb + bb);
-    if (nkp > 0) {
+  if (threadIdx.x == 0 && has_blk) {
 #pragma unroll
-      for (int hv = 0; hv < H; ++hv)
-        tma_load_2d(Ks + hv * kpc * 128, &kmap, &barK, hv * 64, seg * P_max + k0);
-    }
-    if (has_blk) {
+    for (int hv = 0; hv < H; ++hv)
+      tma_load_3d(Kb + hv * Bp * 128, &bkmap, &barK, hv * 64, g, n * B);
 #pragma unroll
-      for (int hv = 0; hv < H; ++hv)
-        tma_load_3d(Kb + hv * Bp * 128, &bkmap, &barK, hv * 64, g, n * B);
-    }
-    if (nkp > 0 || has_blk) {
-      mbar_arrive_expect_tx(&barV, kb + bb);
-      if (nkp > 0) {
-#pragma unroll
-        for (int hv = 0; hv < H; ++hv)
-          tma_load_2d(Vs + hv * kpc * 128, &vmap, &barV, hv * 64, seg * P_max + k0);
-      }
-      if (has_blk) {
-#pragma unroll
-        for (int hv = 0; hv < H; ++hv)
-          tma_load_3d(Vb + hv * Bp * 128, &bvmap, &barV, hv * 64, g, n * B);
-      }
-    }
+    for (int hv = 0; hv < H; ++hv)
+      tma_load_3d(Vb + hv * Bp * 128, &bvmap, &barV, hv * 64, g, n * B);
   }
 
   // S = Q [K ; K_block]^T -> TMEM columns [0, kpc) and [kpc, kpc + Bp).
@@ -1587,7 +1593,8 @@ static cudaError_t launch_attn_t(const herald_dims& dm, const uint16_t* q, const
                                  const uint16_t* pool_v, const int32_t* n_sel, int P_max,
                                  const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
                                  float scale, const WsLayout& w, float* opart, float2* ml,
-                                 uint32_t* err, const PoolMaps* maps, cudaStream_t st) {
+                                 uint32_t* err, const PoolMaps* maps, bool settled,
+                                 cudaStream_t st) {
   const int segs = dm.N * dm.Hkv;
   cudaError_t e;
   if (maps && !force_split()) {
@@ -1603,7 +1610,8 @@ static cudaError_t launch_attn_t(const herald_dims& dm, const uint16_t* q, const
     const int tiles = cdiv(dm.B, maps->bpt);
     return launch_cluster("attn_pool_kernel", attn_pool_kernel<D>, dim3(kPoolCtas, tiles, segs),
                           kPoolCtas, smem, st, maps->k, maps->v, maps->q, maps->bk, maps->bv,
-                          n_sel, P_max, dm.B, dm.Hq, dm.Hkv, maps->bpt, kpc, scale, out, err);
+                          n_sel, P_max, dm.B, dm.Hq, dm.Hkv, maps->bpt, kpc, scale,
+                          int(settled), out, err);
   }
   static bool attr = false;
   if (!attr) {
@@ -1647,12 +1655,12 @@ cudaError_t launch_attn(const herald_dims& dm, const uint16_t* q, const uint16_t
                         const uint16_t* pool_v, const int32_t* n_sel, int P_max,
                         const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
                         float scale, const WsLayout& w, float* opart, float2* ml, uint32_t* err,
-                        const PoolMaps* maps, cudaStream_t st) {
+                        const PoolMaps* maps, bool settled, cudaStream_t st) {
   if (dm.d == 128)
     return launch_attn_t<128>(dm, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale,
-                              w, opart, ml, err, maps, st);
+                              w, opart, ml, err, maps, settled, st);
   return launch_attn_t<64>(dm, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale, w,
-                           opart, ml, err, maps, st);
+                           opart, ml, err, maps, settled, st);
 }
 
 }  // namespace herald

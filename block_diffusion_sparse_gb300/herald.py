@@ -19,7 +19,8 @@ STATUS = {0: "HERALD_OK", 1: "HERALD_ERR_INVALID_ARG", 2: "HERALD_ERR_UNSUPPORTE
 
 EXPORTS = ("herald_workspace_size", "herald_status_string", "herald_last_error",
            "herald_workspace_error", "herald_select_stage1", "herald_select_stage2",
-           "herald_select", "herald_gather", "herald_denoise_attn", "herald_append_kv",
+           "herald_select", "herald_gather", "herald_denoise_attn",
+           "herald_denoise_attn_settled", "herald_append_kv",
            "herald_trace_begin", "herald_trace_end", "herald_trace_name",
            "herald_select_stage2_noalloc", "herald_selftest_wait_timeout",
            "herald_workspace_size_exact", "herald_select_exact")
@@ -77,6 +78,7 @@ def lib() -> C.CDLL:
         L.herald_gather.argtypes = [Dims, vp, vp, i32, vp, vp, vp, vp, vp]
         L.herald_denoise_attn.argtypes = [Dims, vp, vp, vp, vp, i32, vp, vp, vp, C.c_float, vp,
                                           sz, vp]
+        L.herald_denoise_attn_settled.argtypes = L.herald_denoise_attn.argtypes
         L.herald_append_kv.argtypes = [Dims, vp, vp, vp, vp, vp, i32, vp]
         L.herald_select_stage2_noalloc.argtypes = [Dims, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                    i32, vp, vp, vp]
@@ -231,6 +233,14 @@ def herald_denoise_attn(d, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, ou
     _check(lib().herald_denoise_attn(d, _p(q), _p(pool_k), _p(pool_v), _p(n_sel), int(P_max),
                                      _p(block_k), _p(block_v), _p(out), float(scale), _p(ws),
                                      _nbytes(ws, ws_bytes), _s(stream)))
+
+
+def herald_denoise_attn_settled(d, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out,
+                                scale=0.0, ws=None, ws_bytes=None, stream=None):
+    _check(lib().herald_denoise_attn_settled(d, _p(q), _p(pool_k), _p(pool_v), _p(n_sel),
+                                             int(P_max), _p(block_k), _p(block_v), _p(out),
+                                             float(scale), _p(ws), _nbytes(ws, ws_bytes),
+                                             _s(stream)))
 
 
 def herald_append_kv(d, block_k, block_v, ctx_len, k_cache, v_cache, advance=True,

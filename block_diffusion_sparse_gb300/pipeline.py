@@ -26,18 +26,6 @@ from __future__ import annotations
 from . import herald as H
 
 
-def background_sms(dims: H.Dims) -> int:
-    """SMs the overlapped stage-1 scan may keep busy: all but those one
-    attention launch of the denoising stream occupies (8 CTAs per KV head
-    and row tile of whole tokens), and at least half of the device."""
-    import torch
-    nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    G = dims.Hq // dims.Hkv
-    tiles = -(-dims.B // (128 // G))
-    attn_ctas = 8 * tiles * dims.N * dims.Hkv
-    return nsm - min(nsm // 2, attn_ctas)
-
-
 class BlockPipeline:
     def __init__(self, dims: H.Dims, C: int, K: int, S: int, W: int, P: int, T: int,
                  den_stream=None, sel_stream=None, sel_sms=None, exact: bool = False):
@@ -145,8 +133,11 @@ class BlockPipeline:
                                    self._n_cand[nxt], self._ws_sel, wb,
                                    self.sel_sms if overlap else 0, hs if overlap else hd))
         for t in range(self.T):
-            chk(L.herald_denoise_attn(d, q0 + t * qstep, pk, pv, self._n_sel, P, bk0 + t * bstep,
-                                      bv0 + t * bstep, o0 + t * ostep, 0.0, wd, wb, hd))
+            # steps after the first: the pool and n_sel were written before
+            # step 0, a herald call on this stream, so they are loaded early
+            attn = L.herald_denoise_attn_settled if t > 0 else L.herald_denoise_attn
+            chk(attn(d, q0 + t * qstep, pk, pv, self._n_sel, P, bk0 + t * bstep, bv0 + t * bstep,
+                     o0 + t * ostep, 0.0, wd, wb, hd))
         if overlap:
             den.wait_stream(sel)
         last = self.T - 1
@@ -173,8 +164,11 @@ class BlockPipeline:
                                   self._n_sel, self._ws_exact, self._ws_exact_bytes, hd))
         chk(L.herald_gather(d, self._idx, self._n_sel, P, kc, vc, pk, pv, hd))
         for t in range(self.T):
-            chk(L.herald_denoise_attn(d, q0 + t * qstep, pk, pv, self._n_sel, P, bk0 + t * bstep,
-                                      bv0 + t * bstep, o0 + t * ostep, 0.0, wd, wb, hd))
+            # steps after the first: the pool and n_sel were written before
+            # step 0, a herald call on this stream, so they are loaded early
+            attn = L.herald_denoise_attn_settled if t > 0 else L.herald_denoise_attn
+            chk(attn(d, q0 + t * qstep, pk, pv, self._n_sel, P, bk0 + t * bstep, bv0 + t * bstep,
+                     o0 + t * ostep, 0.0, wd, wb, hd))
         last = self.T - 1
         chk(L.herald_append_kv(d, bk0 + last * bstep, bv0 + last * bstep, cx, kc, vc,
                                int(bool(advance)), hd))
@@ -245,9 +239,10 @@ class StackPipeline:
                                            self.n_sel[l], self.ws_den, self.ws_bytes, den)
                     H.herald_gather(d, self.idx[l], self.n_sel[l], P, k_caches[l], v_caches[l],
                                     self.pool_k[l][cur], self.pool_v[l][cur], den)
-                H.herald_denoise_attn(d, q_steps[l][t], self.pool_k[l][cur], self.pool_v[l][cur],
-                                      self.n_sel[l], P, block_k[l][t], block_v[l][t], out[l][t],
-                                      0.0, self.ws_den, self.ws_bytes, den)
+                attn = H.herald_denoise_attn_settled if t > 0 else H.herald_denoise_attn
+                attn(d, q_steps[l][t], self.pool_k[l][cur], self.pool_v[l][cur], self.n_sel[l], P,
+                     block_k[l][t], block_v[l][t], out[l][t], 0.0, self.ws_den, self.ws_bytes,
+                     den)
                 if t == 0:
                     if overlap:
                         sel.wait_stream(den)

@@ -100,9 +100,10 @@ class Run:
         H.herald_gather(self.d, self.idx, self.n_sel, self.P, self.k, self.v, self.pool_k,
                         self.pool_v)
 
-    def attn(self, t):
-        H.herald_denoise_attn(self.d, self.q_steps[t], self.pool_k, self.pool_v, self.n_sel,
-                              self.P, self.bk[t], self.bv[t], self.out, 0.0, self.ws)
+    def attn(self, t, out=None, settled=False):
+        f = H.herald_denoise_attn_settled if settled else H.herald_denoise_attn
+        f(self.d, self.q_steps[t], self.pool_k, self.pool_v, self.n_sel, self.P, self.bk[t],
+          self.bv[t], self.out if out is None else out, 0.0, self.ws)
 
     def error_word(self):
         return H.herald_workspace_error(self.ws)
@@ -204,14 +205,22 @@ def test_gather_and_attention(w):
             np.testing.assert_array_equal(pk[n, g, :m], k[n, g, idx[n, g, :m]])
             np.testing.assert_array_equal(pv[n, g, :m], v[n, g, idx[n, g, :m]])
             assert (pk[n, g, m:] == 0).all() and (pv[n, g, m:] == 0).all()
+    # the T steps back to back, as a block runs them: steps after the first
+    # load the (settled) pool before waiting for their predecessor
+    outs = [torch.zeros_like(r.out) for _ in range(w.T)]
     for t in range(w.T):
-        r.attn(t)
-        torch.cuda.synchronize()
-        out = bf16_dev_to_f64(r.out)
+        r.attn(t, outs[t], settled=t > 0)
+    torch.cuda.synchronize()
+    for t in range(w.T):
+        out = bf16_dev_to_f64(outs[t])
         ref = oracle.sparse_attn(f64(r.x["q_steps"][t]), f64(k), f64(v), idx, ns,
                                  f64(r.x["block_k"][t]), f64(r.x["block_v"][t]))
         err = np.abs(out - ref).max()
         assert err <= ATTN_ATOL, f"{w.name} step {t}: max abs err {err}"
+    # the early loads change no result: the plain call gives the same bits
+    r.attn(w.T - 1)
+    torch.cuda.synchronize()
+    assert torch.equal(r.out, outs[w.T - 1])
     assert r.error_word() == 0
 
 
