@@ -1213,54 +1213,46 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t qbytes = uint32_t(H * G * bpt * 128);
   const int k0 = int(rank) * kpc;
   const bool has_blk = rank == kPoolCtas - 1 && B > 0;  // the block keys
-  // barK: Q + pool K (if any) + block K (last CTA); barV: pool V + block V.
-  // Boxes past the tensor's end are zero-filled; rows past this tile's
-  // tokens or past the valid keys are never used.
-  auto pool_loads = [&](int nkp) {  // thread 0: the expected bytes + pool K/V
-    const uint32_t kb = nkp > 0 ? uint32_t(H * kpc * 128) : 0u;
-    const uint32_t bb = has_blk ? uint32_t(H * Bp * 128) : 0u;
+  // barK: Q + pool K + block K (last CTA); barV: pool V + block V.  The
+  // pool slices are loaded whole whatever n_sel is (rows past it are never
+  // used), so no load waits for n_sel; boxes past the tensor's end are
+  // zero-filled, and rows past this tile's tokens are never used either.
+  const uint32_t kb = uint32_t(H * kpc * 128);
+  const uint32_t bb = has_blk ? uint32_t(H * Bp * 128) : 0u;
+  auto pool_k_loads = [&]() {  // thread 0: the expected bytes + the pool keys
     mbar_arrive_expect_tx(&barK, qbytes + kb + bb);
-    if (nkp > 0 || has_blk) mbar_arrive_expect_tx(&barV, kb + bb);
-    if (nkp > 0) {
+    mbar_arrive_expect_tx(&barV, kb + bb);
 #pragma unroll
-      for (int hv = 0; hv < H; ++hv)
-        tma_load_2d(Ks + hv * kpc * 128, &kmap, &barK, hv * 64, seg * P_max + k0);
-#pragma unroll
-      for (int hv = 0; hv < H; ++hv)
-        tma_load_2d(Vs + hv * kpc * 128, &vmap, &barV, hv * 64, seg * P_max + k0);
-    }
+    for (int hv = 0; hv < H; ++hv)
+      tma_load_2d(Ks + hv * kpc * 128, &kmap, &barK, hv * 64, seg * P_max + k0);
   };
-  int nkp = 0;  // valid pool keys of this CTA
-  if (settled) {
-    // The caller guarantees that the pool and n_sel were written before the
-    // previous launch on the stream began; that launch started this one only
-    // after waiting for its own predecessor (every kernel here does), so
-    // they are final: load them while the predecessor finishes.  n_sel is
-    // read through L2, the point of coherence.
-    nkp = min(max(min(max(__ldcg(n_sel + seg), 0), P_max) - k0, 0), kpc);
-    if (threadIdx.x == 0) pool_loads(nkp);
-  }
+  // settled != 0: the caller guarantees that the pool was written before the
+  // previous launch on the stream began; that launch started this one only
+  // after waiting for its own predecessor (every kernel here does), so the
+  // pool is final: fetch its keys while the predecessor finishes.
+  if (settled && threadIdx.x == 0) pool_k_loads();
   griddep_enter();
-  // the query tile first, before n_sel is known (its bytes may complete on
-  // barK before they are expected: the phase still needs the arrive)
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int hv = 0; hv < H; ++hv)
       tma_load_3d(Qs + hv * kTileM * 128, &qmap, &barK, hv * 64, g * G, n * B + b0);
+    if (!settled) pool_k_loads();
+    if (has_blk) {
+#pragma unroll
+      for (int hv = 0; hv < H; ++hv)
+        tma_load_3d(Kb + hv * Bp * 128, &bkmap, &barK, hv * 64, g, n * B);
+    }
+#pragma unroll
+    for (int hv = 0; hv < H; ++hv)
+      tma_load_2d(Vs + hv * kpc * 128, &vmap, &barV, hv * 64, seg * P_max + k0);
+    if (has_blk) {
+#pragma unroll
+      for (int hv = 0; hv < H; ++hv)
+        tma_load_3d(Vb + hv * Bp * 128, &bvmap, &barV, hv * 64, g, n * B);
+    }
   }
-  if (!settled) {
-    nkp = min(max(min(max(n_sel[seg], 0), P_max) - k0, 0), kpc);
-    if (threadIdx.x == 0) pool_loads(nkp);
-  }
+  const int nkp = min(max(min(max(n_sel[seg], 0), P_max) - k0, 0), kpc);  // valid pool keys
   const bool any = nkp > 0 || has_blk;
-  if (threadIdx.x == 0 && has_blk) {
-#pragma unroll
-    for (int hv = 0; hv < H; ++hv)
-      tma_load_3d(Kb + hv * Bp * 128, &bkmap, &barK, hv * 64, g, n * B);
-#pragma unroll
-    for (int hv = 0; hv < H; ++hv)
-      tma_load_3d(Vb + hv * Bp * 128, &bvmap, &barV, hv * 64, g, n * B);
-  }
 
   // S = Q [K ; K_block]^T -> TMEM columns [0, kpc) and [kpc, kpc + Bp).
   // Every CTA waits for its query tile, used or not: no copy may still be
@@ -1402,6 +1394,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     umma_commit(&bar1);
   }
+  // a CTA without keys still lets its value copies land before it exits
+  if (threadIdx.x == 0 && !any) ok = mbar_wait(&barV, 0) && ok;
   if (any && !mbar_wait(&bar1, 0)) ok = false;
   tc_fence_after();
   __syncwarp();
@@ -1577,6 +1571,43 @@ static int max_active_clusters() {
   return cache[dev];
 }
 
+// How many 8-CTA clusters of the pool attention kernel with `smem` bytes of
+// dynamic shared memory can be resident at once; cached per device for the
+// last few sizes asked.
+template <int D>
+static int pool_resident_clusters(uint32_t smem) {
+  struct Entry {
+    int dev;
+    uint32_t smem;
+    int n;
+  };
+  static Entry cache[8] = {};
+  static int next = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  for (const Entry& e : cache)
+    if (e.n > 0 && e.dev == dev && e.smem == smem) return e.n;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(kPoolCtas, 1, 1);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kPoolCtas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, attn_pool_kernel<D>, &cfg) != cudaSuccess) n = 0;
+  cudaGetLastError();
+  if (n > 0) {
+    cache[next] = Entry{dev, smem, n};
+    next = (next + 1) % 8;
+  }
+  return n;
+}
+
 int attn_pool_kpc(int P_max) { return cdiv(cdiv(P_max, kPoolCtas), 16) * 16; }
 int attn_pool_bpt(const herald_dims& dm) { return kTileM / (dm.Hq / dm.Hkv); }
 
@@ -1608,10 +1639,13 @@ static cudaError_t launch_attn_t(const herald_dims& dm, const uint16_t* q, const
       attr_bytes = smem;
     }
     const int tiles = cdiv(dm.B, maps->bpt);
+    // early loads pay only when every CTA of the grid is resident at once:
+    // with a second wave they measured slower (on the 4 x 64K layer)
+    const int early = settled && tiles * segs <= pool_resident_clusters<D>(smem) ? 1 : 0;
     return launch_cluster("attn_pool_kernel", attn_pool_kernel<D>, dim3(kPoolCtas, tiles, segs),
                           kPoolCtas, smem, st, maps->k, maps->v, maps->q, maps->bk, maps->bv,
                           n_sel, P_max, dm.B, dm.Hq, dm.Hkv, maps->bpt, kpc, scale,
-                          int(settled), out, err);
+                          early, out, err);
   }
   static bool attr = false;
   if (!attr) {

@@ -176,16 +176,17 @@ herald_status herald_denoise_attn(herald_dims dims, const uint16_t *q, const uin
                                   void *stream);
 
 /* herald_denoise_attn for steps 1..T-1 of a block: the same arguments and
- * result; the pool rows and n_sel are loaded while the work before the call
- * on `stream` is still finishing, instead of after it.  The pool is fixed
- * across a block's T steps ([EA]: one selection serves all of them), so
- * these loads leave only the step's queries and block keys on the path.
- * Precondition: pool_k, pool_v and n_sel were written before some earlier
- * herald_* call on `stream` (and nothing writes them since): every herald
- * kernel lets its successor start only after its own predecessor has
- * finished, so that data is final when this kernel starts.  A call right
- * after the herald_gather (or stage 2) that wrote the pool must use
- * herald_denoise_attn; breaking the precondition races with that write. */
+ * result; the pool keys are loaded while the work before the call on
+ * `stream` is still finishing, instead of after it.  The pool is fixed
+ * across a block's T steps ([EA]: one selection serves all of them).  Done
+ * only when the whole grid is resident at once (otherwise this call is
+ * herald_denoise_attn).
+ * Precondition: pool_k was written before some earlier herald_* call on
+ * `stream` (and nothing writes it since): every herald kernel lets its
+ * successor start only after its own predecessor has finished, so the pool
+ * is final when this kernel starts.  A call right after the herald_gather
+ * that wrote the pool must use herald_denoise_attn; breaking the
+ * precondition races with that write. */
 herald_status herald_denoise_attn_settled(herald_dims dims, const uint16_t *q,
                                           const uint16_t *pool_k, const uint16_t *pool_v,
                                           const int32_t *n_sel, int P_max,
