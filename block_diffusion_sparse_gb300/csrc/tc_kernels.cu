@@ -1262,8 +1262,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0 && any) {
     const uint32_t qa = smem_u32(Qs);
     tc_fence_after();
-    if (nkp > 0) {
-      const uint32_t idesc = make_idesc_bf16(kTileM, kpc, false, false);
+    if (nkp > 0) {  // the pool rows up to the last 16-key chunk holding a valid key
+      const uint32_t idesc = make_idesc_bf16(kTileM, (nkp + 15) & ~15, false, false);
       const uint32_t ka = smem_u32(Ks);
 #pragma unroll
       for (int s = 0; s < D / 16; ++s) {
@@ -1292,26 +1292,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   __syncwarp();
 
-  // softmax over this CTA's columns, in log2 units; the 16-column chunks are
-  // split between the two warps that share a TMEM lane quadrant
+  // softmax over this CTA's columns, in log2 units, over the 16-key chunks
+  // that hold a valid key (pool chunks, then block chunks), split between
+  // the two warps that share a TMEM lane quadrant
   const int quad = warp & 3, ch = warp >> 2;
   const int row = quad * 32 + lane;
   const uint32_t trow = tbase + (uint32_t(quad * 32) << 16);
-  const int nchunks = any ? (kpc + (has_blk ? Bp : 0)) / 16 : 0;
-  const int half = (nchunks + 1) / 2;
-  const int c_begin = ch == 0 ? 0 : half, c_end = ch == 0 ? half : nchunks;
+  const int npc = (nkp + 15) >> 4;                // pool chunks
+  const int nbc = has_blk ? (B + 15) >> 4 : 0;   // block chunks
+  const int nchunks = npc + nbc;
+  const int half = (nchunks + 1) >> 1;
+  const int c_begin = ch == 0 ? 0 : half, cnt = ch == 0 ? half : nchunks - half;
   constexpr int kMaxChunks = kPoolMaxCols / 32;  // 16-column chunks per half
   const float sl2 = scale * 1.4426950408889634f;              // scores -> log2 units
   float x[kMaxChunks][16];
   int nv[kMaxChunks];  // valid keys per chunk (warp-uniform)
 #pragma unroll
   for (int c = 0; c < kMaxChunks; ++c) {
-    const int ci = c_begin + c;
-    const int k16 = ci * 16;
-    nv[c] = ci >= c_end ? 0
-            : k16 < kpc ? min(max(nkp - k16, 0), 16)
-                        : min(max(B - (k16 - kpc), 0), 16);
-    if (ci < c_end) {
+    const int j = c_begin + c;
+    const bool pool_j = j < npc;
+    nv[c] = c >= cnt ? 0 : pool_j ? min(nkp - j * 16, 16) : min(B - (j - npc) * 16, 16);
+    if (c < cnt) {
+      const int col = pool_j ? j * 16 : kpc + (j - npc) * 16;
       uint32_t* r = reinterpret_cast<uint32_t*>(x[c]);
       asm volatile(
           "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
@@ -1319,48 +1321,63 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
             "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
             "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-          : "r"(trow + uint32_t(k16)));
+          : "r"(trow + uint32_t(col)));
     }
   }
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  // the row max of the raw scores (a positive scale keeps the arg max), the
+  // keys past the valid ones set to -inf in the one partial chunk
   float m = -INFINITY;
 #pragma unroll
   for (int c = 0; c < kMaxChunks; ++c) {
+    if (c < cnt) {
+      if (nv[c] < 16) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      x[c][i] = i < nv[c] ? x[c][i] * sl2 : -INFINITY;
-      m = fmaxf(m, x[c][i]);
+        for (int i = 0; i < 16; ++i) x[c][i] = i < nv[c] ? x[c][i] : -INFINITY;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; i += 2) m = fmax3f(m, x[c][i], x[c][i + 1]);
     }
   }
   red_m[ch][row] = m;
   __syncthreads();
-  m = fmaxf(red_m[0][row], red_m[1][row]);
-  const float mm = m == -INFINITY ? 0.f : m;  // no valid key: every p is 2^-inf = 0
-  float lsum = 0.f;
+  m = fmaxf(red_m[0][row], red_m[1][row]) * sl2;  // log2 units; -inf stays -inf
+  const float mm = m == -INFINITY ? 0.f : m;      // no valid key: every p is 2^-inf = 0
+  // p = 2^(x sl2 - m): the scaling and the shift as one paired fma for two
+  // keys, the row sum as paired adds
+  const uint64_t sl2x2 = f2_pack(sl2, sl2), nmx2 = f2_pack(-mm, -mm);
+  uint64_t lsum2 = f2_pack(0.f, 0.f);
 #pragma unroll
   for (int c = 0; c < kMaxChunks; ++c) {
-    const int ci = c_begin + c;
-    if (ci < c_end) {
-      float p[16];
+    if (c < cnt) {
+      uint32_t pk[8];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        p[i] = fast_exp2(x[c][i] - mm);
-        lsum += p[i];
+      for (int i = 0; i < 8; ++i) {
+        float t0, t1;
+        f2_unpack(f2_fma(f2_pack(x[c][2 * i], x[c][2 * i + 1]), sl2x2, nmx2), t0, t1);
+        const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
+        lsum2 = f2_add(lsum2, f2_pack(p0, p1));
+        pk[i] = pack_bf16(p0, p1);
       }
-      const int kc = ci * 16;
-      uint8_t* blk = kc < kpc ? Ps + (kc >> 6) * 16384 : Pb;
-      const int cc = ((kc < kpc ? kc : kc - kpc) & 63) >> 3;  // 16-byte chunk (8 keys)
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint4 pk;
-        pk.x = pack_bf16(p[8 * hh + 0], p[8 * hh + 1]);
-        pk.y = pack_bf16(p[8 * hh + 2], p[8 * hh + 3]);
-        pk.z = pack_bf16(p[8 * hh + 4], p[8 * hh + 5]);
-        pk.w = pack_bf16(p[8 * hh + 6], p[8 * hh + 7]);
-        *reinterpret_cast<uint4*>(blk + sw128_off(row, cc + hh)) = pk;
+      const int j = c_begin + c;
+      uint8_t* blk;
+      int kc;  // key index within the pool slice or within the block
+      if (j < npc) {
+        kc = j * 16;
+        blk = Ps + (kc >> 6) * 16384;
+      } else {
+        kc = (j - npc) * 16;
+        blk = Pb;
       }
+      const int cc = (kc & 63) >> 3;  // 16-byte chunk (8 keys)
+      *reinterpret_cast<uint4*>(blk + sw128_off(row, cc)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      *reinterpret_cast<uint4*>(blk + sw128_off(row, cc + 1)) =
+          make_uint4(pk[4], pk[5], pk[6], pk[7]);
     }
   }
+  float lsum, lsum_hi;
+  f2_unpack(lsum2, lsum, lsum_hi);
+  lsum += lsum_hi;
   red_s[ch][row] = lsum;
   fence_proxy_async_smem();
   tc_fence_before();
@@ -1373,9 +1390,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bool acc = false;
     ok = mbar_wait(&barV, 0) && ok;
     tc_fence_after();
-    if (nkp > 0) {
+    if (nkp > 0) {  // the chunks the softmax wrote
       const uint32_t pa = smem_u32(Ps), va = smem_u32(Vs);
-      for (int s = 0; s < kpc / 16; ++s) {
+      for (int s = 0; s < npc; ++s) {
         const uint64_t a =
             make_sdesc_sw128(pa + uint32_t(s >> 2) * 16384u + uint32_t(s & 3) * 32u, 16, 1024);
         const uint64_t b = make_sdesc_sw128(va + uint32_t(s) * 2048u, uint32_t(kpc) * 128u, 1024);
@@ -1385,7 +1402,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     if (has_blk) {
       const uint32_t pa = smem_u32(Pb), va = smem_u32(Vb);
-      for (int s = 0; s < Bp / 16; ++s) {
+      for (int s = 0; s < nbc; ++s) {
         const uint64_t a = make_sdesc_sw128(pa + uint32_t(s & 3) * 32u, 16, 1024);
         const uint64_t b = make_sdesc_sw128(va + uint32_t(s) * 2048u, uint32_t(Bp) * 128u, 1024);
         umma_bf16(tbase + 256, a, b, idesc, acc ? 1u : 0u);
