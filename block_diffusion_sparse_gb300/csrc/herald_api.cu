@@ -597,8 +597,19 @@ namespace {
 herald_status denoise_attn(herald_dims dims, const uint16_t* q, const uint16_t* pool_k,
                            const uint16_t* pool_v, const int32_t* n_sel, int P_max,
                            const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
-                           float scale, void* ws, size_t ws_bytes, bool settled, void* stream) {
+                           float scale, unsigned flags, int32_t* ctx_len, uint16_t* k_cache,
+                           uint16_t* v_cache, void* ws, size_t ws_bytes, void* stream) {
   g_err[0] = 0;
+  constexpr unsigned kKnown = HERALD_ATTN_SETTLED | HERALD_ATTN_APPEND | HERALD_ATTN_ADVANCE;
+  if (flags & ~kKnown) return fail(HERALD_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags & ~kKnown);
+  const bool append = (flags & HERALD_ATTN_APPEND) != 0;
+  if ((flags & HERALD_ATTN_ADVANCE) && !append)
+    return fail(HERALD_ERR_INVALID_ARG, "HERALD_ATTN_ADVANCE needs HERALD_ATTN_APPEND");
+  if (append) {
+    HERALD_CHECK_PTR(ctx_len);
+    HERALD_CHECK_PTR(k_cache);
+    HERALD_CHECK_PTR(v_cache);
+  }
   HERALD_RET_IF(check_dims(dims));
   HERALD_RET_IF(check_pmax(dims, P_max));
   HERALD_CHECK_PTR(q);
@@ -629,11 +640,23 @@ herald_status denoise_attn(herald_dims dims, const uint16_t* q, const uint16_t* 
     HERALD_RET_IF(encode_heads_map(block_v, tokens, dims.Hkv, dims.d, 1u, uint32_t(Bp),
                                    &maps.bv));
   }
+  // the append rides along with the step when the cache is in device memory
+  // (its stores stay on the device); a host-resident cache gets the append
+  // kernel after it
+  const bool fused = append && is_device_memory(k_cache) && is_device_memory(v_cache);
+  const AppendArgs app{block_k, block_v, ctx_len, k_cache, v_cache,
+                       (flags & HERALD_ATTN_ADVANCE) ? 1 : 0};
   HERALD_TRY_CUDA(launch_attn(dims, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale,
                               w, at<float>(ws, w.opart), at<float2>(ws, w.ml),
-                              at<uint32_t>(ws, w.err), pool ? &maps : nullptr, settled,
+                              at<uint32_t>(ws, w.err), pool ? &maps : nullptr,
+                              (flags & HERALD_ATTN_SETTLED) != 0, fused ? &app : nullptr,
                               static_cast<cudaStream_t>(stream)),
                   "attention launch");
+  if (append && !fused)  // a cache in host memory: the append kernel after the step
+    HERALD_TRY_CUDA(launch_append(dims, block_k, block_v, ctx_len, k_cache, v_cache,
+                                  (flags & HERALD_ATTN_ADVANCE) != 0,
+                                  static_cast<cudaStream_t>(stream)),
+                    "append launch");
   return HERALD_OK;
 }
 }  // namespace
@@ -645,18 +668,18 @@ herald_status herald_denoise_attn(herald_dims dims, const uint16_t* q, const uin
                                   const uint16_t* block_k, const uint16_t* block_v,
                                   uint16_t* out, float scale, void* ws, size_t ws_bytes,
                                   void* stream) {
-  return denoise_attn(dims, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale, ws,
-                      ws_bytes, false, stream);
+  return denoise_attn(dims, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale, 0u,
+                      nullptr, nullptr, nullptr, ws, ws_bytes, stream);
 }
 
-herald_status herald_denoise_attn_settled(herald_dims dims, const uint16_t* q,
-                                          const uint16_t* pool_k, const uint16_t* pool_v,
-                                          const int32_t* n_sel, int P_max,
-                                          const uint16_t* block_k, const uint16_t* block_v,
-                                          uint16_t* out, float scale, void* ws, size_t ws_bytes,
-                                          void* stream) {
-  return denoise_attn(dims, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale, ws,
-                      ws_bytes, true, stream);
+herald_status herald_denoise_attn_ex(herald_dims dims, const uint16_t* q, const uint16_t* pool_k,
+                                     const uint16_t* pool_v, const int32_t* n_sel, int P_max,
+                                     const uint16_t* block_k, const uint16_t* block_v,
+                                     uint16_t* out, float scale, unsigned flags,
+                                     int32_t* ctx_len, uint16_t* k_cache, uint16_t* v_cache,
+                                     void* ws, size_t ws_bytes, void* stream) {
+  return denoise_attn(dims, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale, flags,
+                      ctx_len, k_cache, v_cache, ws, ws_bytes, stream);
 }
 
 herald_status herald_append_kv(herald_dims dims, const uint16_t* block_k, const uint16_t* block_v,

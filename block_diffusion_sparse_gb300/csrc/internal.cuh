@@ -183,11 +183,13 @@ struct PoolMaps {
 int attn_pool_kpc(int P_max);
 int attn_pool_bpt(const herald_dims& dm);
 bool attn_pool_ok(const herald_dims& dm, int P_max);
+struct AppendArgs;  // below
 cudaError_t launch_attn(const herald_dims& dm, const uint16_t* q, const uint16_t* pool_k,
                         const uint16_t* pool_v, const int32_t* n_sel, int P_max,
                         const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
                         float scale, const WsLayout& w, float* opart, float2* ml, uint32_t* err,
-                        const PoolMaps* maps, bool settled, cudaStream_t st);
+                        const PoolMaps* maps, bool settled, const AppendArgs* app,
+                        cudaStream_t st);
 // exact selection: per-segment candidate counts = context lengths; the
 // refine's score partials summed in place (stride floats per segment) and
 // histogrammed for the top-K radix select
@@ -200,5 +202,58 @@ cudaError_t launch_wait_timeout(uint64_t limit_ns, uint32_t* err, cudaStream_t s
 cudaError_t launch_append(const herald_dims& dm, const uint16_t* block_k, const uint16_t* block_v,
                           int32_t* ctx, uint16_t* k_cache, uint16_t* v_cache, int advance,
                           cudaStream_t st);
+
+// The append of a decoded block, done inside another kernel: the rows of
+// block[n][b][g] (bf16, [N][B][Hkv][d]) go to cache[n][g][L0 + b], rows at or
+// past L_max skipped; `tid` of `nthreads` threads, kBatch 16-byte chunks of K
+// and of V in flight per thread and round.
+#ifdef __CUDACC__
+template <int kBatch>
+__device__ __forceinline__ void append_block_rows(const uint16_t* __restrict__ bk,
+                                                  const uint16_t* __restrict__ bv, int n, int B,
+                                                  int Hkv, int d, int L_max, int L0,
+                                                  uint16_t* __restrict__ kc,
+                                                  uint16_t* __restrict__ vc, int tid,
+                                                  int nthreads) {
+  const int cpr = d / 8, total = B * Hkv * cpr;
+  for (int q0 = 0; q0 < total; q0 += nthreads * kBatch) {
+    uint4 k[kBatch], v[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int q = q0 + u * nthreads + tid;
+      if (q < total) {
+        const int c = q % cpr, bg = q / cpr, g = bg % Hkv, b = bg / Hkv;
+        const size_t src = ((size_t(n) * B + b) * Hkv + g) * d + c * 8;
+        k[u] = *reinterpret_cast<const uint4*>(bk + src);
+        v[u] = *reinterpret_cast<const uint4*>(bv + src);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int q = q0 + u * nthreads + tid;
+      if (q < total) {
+        const int c = q % cpr, bg = q / cpr, g = bg % Hkv, b = bg / Hkv;
+        const int j = L0 + b;
+        if (j < L_max) {
+          const size_t dst = ((size_t(n) * Hkv + g) * L_max + j) * d + c * 8;
+          *reinterpret_cast<uint4*>(kc + dst) = k[u];
+          *reinterpret_cast<uint4*>(vc + dst) = v[u];
+        }
+      }
+    }
+  }
+}
+#endif
+
+// The append fused into a denoising step (the pool attention kernel): the
+// step's own block keys/values, the cache and its lengths.
+struct AppendArgs {
+  const uint16_t* bk;
+  const uint16_t* bv;
+  int32_t* ctx;
+  uint16_t* kc;
+  uint16_t* vc;
+  int advance;
+};
 
 }  // namespace herald

@@ -95,33 +95,8 @@ __global__ void __launch_bounds__(kAppendThreads)
   const int n = blockIdx.x;
   if (threadIdx.x == 0) L0 = min(max(ctx[n], 0), L_max);
   __syncthreads();
-  const int cpr = d / 8, total = B * Hkv * cpr;
-  for (int q0 = 0; q0 < total; q0 += kAppendThreads * kAppendBatch) {
-    uint4 k[kAppendBatch], v[kAppendBatch];
-#pragma unroll
-    for (int u = 0; u < kAppendBatch; ++u) {
-      const int q = q0 + u * kAppendThreads + threadIdx.x;
-      if (q < total) {
-        const int c = q % cpr, bg = q / cpr, g = bg % Hkv, b = bg / Hkv;
-        const size_t src = ((size_t(n) * B + b) * Hkv + g) * d + c * 8;
-        k[u] = *reinterpret_cast<const uint4*>(bk + src);
-        v[u] = *reinterpret_cast<const uint4*>(bv + src);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kAppendBatch; ++u) {
-      const int q = q0 + u * kAppendThreads + threadIdx.x;
-      if (q < total) {
-        const int c = q % cpr, bg = q / cpr, g = bg % Hkv, b = bg / Hkv;
-        const int j = L0 + b;
-        if (j < L_max) {
-          const size_t dst = ((size_t(n) * Hkv + g) * L_max + j) * d + c * 8;
-          *reinterpret_cast<uint4*>(kc + dst) = k[u];
-          *reinterpret_cast<uint4*>(vc + dst) = v[u];
-        }
-      }
-    }
-  }
+  append_block_rows<kAppendBatch>(bk, bv, n, B, Hkv, d, L_max, L0, kc, vc, threadIdx.x,
+                                  kAppendThreads);
   __syncthreads();
   if (advance && threadIdx.x == 0) ctx[n] = min(L0 + B, L_max);
 }

@@ -469,6 +469,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     pos[r] = (p >= 0 && p < L_max) ? p : -1;
   }
   __syncthreads();
+  // the tile's rows past its G*bpt query rows are never loaded: zeroed, so
+  // that every score row is finite and the column sums below can weight
+  // rows with a product (rows past the tile's tokens get weight 0)
+  for (int u = G * bpt * 8 + threadIdx.x; u < kTileM * 8; u += kTcThreads) {
+#pragma unroll
+    for (int hv = 0; hv < D / 64; ++hv)
+      *reinterpret_cast<uint4*>(Qs + hv * kTileM * 128 + u * 16) = make_uint4(0u, 0u, 0u, 0u);
+  }
   if (ncv > 0) {
     load_rows_sw128<D>(Ks, cpc, cpc, kc, [&](int r) -> const uint16_t* {
       const int p = pos[r];
@@ -476,8 +484,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     });
     cp_async_commit();
     cp_async_wait_all();
-    fence_proxy_async_smem();
   }
+  fence_proxy_async_smem();  // the zeroed rows and the copied K rows, for the UMMA
   __syncthreads();
   tc_fence_after();
   // S = Q K_cand^T: up to two UMMAs of N = 256 -> TMEM columns [0, cpc)
@@ -515,27 +523,46 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int row = quad * 32 + lane;
   const uint32_t trow = tbase + (uint32_t(quad * 32) << 16);
   const float sl2 = scale * 1.4426950408889634f;
-  const int hc0 = ch * (cpc / 2), hc1 = hc0 + cpc / 2;  // this warp's columns
+  const int hc0 = ch * (cpc / 2);                        // this warp's columns
+  const int hc1 = min(hc0 + cpc / 2, ncv + 31 & ~31);   // up to the last valid chunk
   float m = -INFINITY;
   for (int c = hc0; c < hc1; c += 32) {
     float v[32];
     tmem_ld32(trow + uint32_t(c), v);
+    if (c + 32 > ncv) {  // the one partial chunk
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (c + i < ncv) m = fmaxf(m, v[i]);
+      for (int i = 0; i < 32; ++i) v[i] = c + i < ncv ? v[i] : -INFINITY;
+    }
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) m = fmax3f(m, v[i], v[i + 1]);
   }
   m = m == -INFINITY ? m : m * sl2;  // the scale is positive: max commutes with it
-  float l = 0.f;
+  // p = 2^(s sl2 - m) two columns at a time (one paired fma), the row sum
+  // as paired adds over the valid columns
+  const uint64_t sl2x2 = f2_pack(sl2, sl2);
+  const uint64_t nmx2 = m == -INFINITY ? f2_pack(0.f, 0.f) : f2_pack(-m, -m);
+  uint64_t l2 = f2_pack(0.f, 0.f);
   for (int c = hc0; c < hc1; c += 32) {
     float v[32];
     tmem_ld32(trow + uint32_t(c), v);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      v[i] = (c + i < ncv) ? fast_exp2(fmaf(v[i], sl2, -m)) : 0.f;
-      l += v[i];
+    for (int i = 0; i < 32; i += 2) {
+      float t0, t1;
+      f2_unpack(f2_fma(f2_pack(v[i], v[i + 1]), sl2x2, nmx2), t0, t1);
+      v[i] = fast_exp2(t0);
+      v[i + 1] = fast_exp2(t1);
     }
     tmem_st32(trow + uint32_t(c), v);
+    if (c + 32 > ncv) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = c + i < ncv ? v[i] : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) l2 = f2_add(l2, f2_pack(v[i], v[i + 1]));
   }
+  float l, l_hi;
+  f2_unpack(l2, l, l_hi);
+  l += l_hi;
   tmem_wait_st();
   half_stat[ch][row] = make_float2(m, l);
   __syncthreads();
@@ -568,28 +595,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const bool row_ok = row < rows_t;
   // 2^(s - lse) = p * 2^(m_half - lse); rows past the tile's tokens contribute nothing
   const float f = (row_ok && m != -INFINITY) ? fast_exp2(m - lse) : 0.f;
-  // column sums over the 128 rows: per 32-column chunk, a warp
-  // transpose-reduces its 32 rows; after the butterfly, lane j holds the sum
-  // of chunk column j over the warp's rows
+  // column sums over the 128 rows: per 32-column chunk, each warp
+  // transposes its 32 x 32 block through shared memory (the dead query
+  // tile, 4 KB per warp; 16-byte units XOR-swizzled by row, so that both the
+  // row stores and the column loads are free of bank conflicts) and lane j
+  // adds up column j over the warp's rows.  Rows past the tile's tokens are
+  // finite (zeroed or real queries) and weighted 0.
+  float* tb = reinterpret_cast<float*>(Qs) + warp * 1024;
+  const uint64_t ff = f2_pack(f, f);
   for (int c = hc0; c < hc1; c += 32) {
     float v[32];
     tmem_ld32(trow + uint32_t(c), v);
-    // a select, not a product: rows past the tile's tokens hold whatever the
-    // shared memory held (never loaded), possibly NaN
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = row_ok ? v[i] * f : 0.f;
+    for (int i = 0; i < 32; i += 2) f2_unpack(f2_mul(f2_pack(v[i], v[i + 1]), ff), v[i], v[i + 1]);
+    __syncwarp();  // the previous chunk's column loads are done
 #pragma unroll
-    for (int w = 16; w >= 1; w >>= 1) {
-      // the lane with bit w set keeps the upper w columns, its partner the lower
-      const bool up = (lane & w) != 0;
+    for (int u = 0; u < 8; ++u)
+      *reinterpret_cast<float4*>(tb + lane * 32 + 4 * (u ^ (lane & 7))) =
+          make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+    __syncwarp();
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-      for (int i = 0; i < w; ++i) {
-        const float send = up ? v[i] : v[i + w];
-        const float keep = up ? v[i + w] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
-      }
+    for (int r = 0; r < 32; r += 4) {
+      const int cl = lane & 3, cu = lane >> 2;
+      a0 += tb[(r + 0) * 32 + 4 * (cu ^ ((r + 0) & 7)) + cl];
+      a1 += tb[(r + 1) * 32 + 4 * (cu ^ ((r + 1) & 7)) + cl];
+      a2 += tb[(r + 2) * 32 + 4 * (cu ^ ((r + 2) & 7)) + cl];
+      a3 += tb[(r + 3) * 32 + 4 * (cu ^ ((r + 3) & 7)) + cl];
     }
-    colsum[ch][quad][c - hc0 + lane] = v[0];
+    colsum[ch][quad][c - hc0 + lane] = (a0 + a1) + (a2 + a3);
   }
   __syncthreads();
   float* out = s2p + (size_t(mt) * gridDim.z + seg) * C;
@@ -1160,7 +1194,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                      const __grid_constant__ CUtensorMap bvmap,
                      const int32_t* __restrict__ n_sel, int P_max, int B, int Hq, int Hkv,
                      int bpt, int kpc, float scale, int settled, uint16_t* __restrict__ out,
-                     uint32_t* err) {
+                     uint32_t* err, AppendArgs app, int L_max) {
   constexpr int H = D / 64;
   constexpr int OROW = D + 8;  // fp16 row stride of O partials (16-byte padding)
   extern __shared__ uint8_t smem_raw[];
@@ -1253,6 +1287,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   const int nkp = min(max(min(max(n_sel[seg], 0), P_max) - k0, 0), kpc);  // valid pool keys
   const bool any = nkp > 0 || has_blk;
+  // The fused append (app.bk set): per sequence, the 8 CTAs of the cluster
+  // of the first row tile of KV head 0 copy the block's rows of every KV
+  // head into the cache, an eighth each, while their operands are in
+  // flight.  No other CTA reads ctx.  CTA 0 advances it once every peer's
+  // partial has landed: each peer pushes after all its threads have read it.
+  const bool appender = app.bk != nullptr && mt == 0 && g == 0;
+  int L0 = 0;
+  if (appender) {
+    L0 = min(max(app.ctx[n], 0), L_max);
+    append_block_rows<1>(app.bk, app.bv, n, B, Hkv, D, L_max, L0, app.kc, app.vc,
+                         int(rank) * kTcThreads + threadIdx.x, kPoolCtas * kTcThreads);
+  }
 
   // S = Q [K ; K_block]^T -> TMEM columns [0, kpc) and [kpc, kpc + Bp).
   // Every CTA waits for its query tile, used or not: no copy may still be
@@ -1458,7 +1504,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     bulk_commit();
   }
-  if (!mbar_wait(&barR, 0)) record_error(err, DEV_TIMEOUT_TMA);
+  if (!mbar_wait(&barR, 0)) {
+    record_error(err, DEV_TIMEOUT_TMA);
+  } else if (appender && app.advance && rank == 0 && threadIdx.x == 0) {
+    app.ctx[n] = min(L0 + B, L_max);
+  }
 
   // merge this CTA's 16 rows from the 8 received partials:
   // out = sum_c 2^(m_c - M) l_c (o_c / l_c) / sum_c 2^(m_c - M) l_c
@@ -1636,34 +1686,16 @@ bool attn_pool_ok(const herald_dims& dm, int P_max) {
          pool_smem(dm.d, kpc, Bp).total <= 220u * 1024u;
 }
 
+// the attention without the pool kernel: whole-cluster or split-key kernels
 template <int D>
-static cudaError_t launch_attn_t(const herald_dims& dm, const uint16_t* q, const uint16_t* pool_k,
-                                 const uint16_t* pool_v, const int32_t* n_sel, int P_max,
-                                 const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
-                                 float scale, const WsLayout& w, float* opart, float2* ml,
-                                 uint32_t* err, const PoolMaps* maps, bool settled,
-                                 cudaStream_t st) {
+static cudaError_t launch_attn_split(const herald_dims& dm, const uint16_t* q,
+                                     const uint16_t* pool_k, const uint16_t* pool_v,
+                                     const int32_t* n_sel, int P_max, const uint16_t* block_k,
+                                     const uint16_t* block_v, uint16_t* out, float scale,
+                                     const WsLayout& w, float* opart, float2* ml, uint32_t* err,
+                                     cudaStream_t st) {
   const int segs = dm.N * dm.Hkv;
   cudaError_t e;
-  if (maps && !force_split()) {
-    const int kpc = attn_pool_kpc(P_max);
-    const uint32_t smem = pool_smem(D, kpc, (dm.B + 15) & ~15).total;
-    static uint32_t attr_bytes = 0;  // dynamic shared memory granted so far
-    if (smem > attr_bytes) {
-      e = cudaFuncSetAttribute(attn_pool_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               int(smem));
-      if (e != cudaSuccess) return e;
-      attr_bytes = smem;
-    }
-    const int tiles = cdiv(dm.B, maps->bpt);
-    // early loads pay only when every CTA of the grid is resident at once:
-    // with a second wave they measured slower (on the 4 x 64K layer)
-    const int early = settled && tiles * segs <= pool_resident_clusters<D>(smem) ? 1 : 0;
-    return launch_cluster("attn_pool_kernel", attn_pool_kernel<D>, dim3(kPoolCtas, tiles, segs),
-                          kPoolCtas, smem, st, maps->k, maps->v, maps->q, maps->bk, maps->bv,
-                          n_sel, P_max, dm.B, dm.Hq, dm.Hkv, maps->bpt, kpc, scale,
-                          early, out, err);
-  }
   static bool attr = false;
   if (!attr) {
     e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1702,16 +1734,52 @@ static cudaError_t launch_attn_t(const herald_dims& dm, const uint16_t* q, const
   return cudaSuccess;
 }
 
+template <int D>
+static cudaError_t launch_attn_t(const herald_dims& dm, const uint16_t* q, const uint16_t* pool_k,
+                                 const uint16_t* pool_v, const int32_t* n_sel, int P_max,
+                                 const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
+                                 float scale, const WsLayout& w, float* opart, float2* ml,
+                                 uint32_t* err, const PoolMaps* maps, bool settled,
+                                 const AppendArgs* app, cudaStream_t st) {
+  const int segs = dm.N * dm.Hkv;
+  cudaError_t e;
+  if (maps && !force_split()) {
+    const int kpc = attn_pool_kpc(P_max);
+    const uint32_t smem = pool_smem(D, kpc, (dm.B + 15) & ~15).total;
+    static uint32_t attr_bytes = 0;  // dynamic shared memory granted so far
+    if (smem > attr_bytes) {
+      e = cudaFuncSetAttribute(attn_pool_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               int(smem));
+      if (e != cudaSuccess) return e;
+      attr_bytes = smem;
+    }
+    const int tiles = cdiv(dm.B, maps->bpt);
+    // early loads pay only when every CTA of the grid is resident at once:
+    // with a second wave they measured slower (on the 4 x 64K layer)
+    const int early = settled && tiles * segs <= pool_resident_clusters<D>(smem) ? 1 : 0;
+    const AppendArgs none{nullptr, nullptr, nullptr, nullptr, nullptr, 0};
+    return launch_cluster("attn_pool_kernel", attn_pool_kernel<D>, dim3(kPoolCtas, tiles, segs),
+                          kPoolCtas, smem, st, maps->k, maps->v, maps->q, maps->bk, maps->bv,
+                          n_sel, P_max, dm.B, dm.Hq, dm.Hkv, maps->bpt, kpc, scale, early, out,
+                          err, app ? *app : none, dm.L_max);
+  }
+  e = launch_attn_split<D>(dm, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale, w,
+                           opart, ml, err, st);
+  if (e != cudaSuccess || !app) return e;
+  return launch_append(dm, app->bk, app->bv, app->ctx, app->kc, app->vc, app->advance, st);
+}
+
 cudaError_t launch_attn(const herald_dims& dm, const uint16_t* q, const uint16_t* pool_k,
                         const uint16_t* pool_v, const int32_t* n_sel, int P_max,
                         const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
                         float scale, const WsLayout& w, float* opart, float2* ml, uint32_t* err,
-                        const PoolMaps* maps, bool settled, cudaStream_t st) {
+                        const PoolMaps* maps, bool settled, const AppendArgs* app,
+                        cudaStream_t st) {
   if (dm.d == 128)
     return launch_attn_t<128>(dm, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale,
-                              w, opart, ml, err, maps, settled, st);
+                              w, opart, ml, err, maps, settled, app, st);
   return launch_attn_t<64>(dm, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale, w,
-                           opart, ml, err, maps, settled, st);
+                           opart, ml, err, maps, settled, app, st);
 }
 
 }  // namespace herald

@@ -14,13 +14,15 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libherald.so")
 
 HERALD_OK = 0
+# flags of herald_denoise_attn_ex (include/herald.h)
+HERALD_ATTN_SETTLED, HERALD_ATTN_APPEND, HERALD_ATTN_ADVANCE = 1, 2, 4
 STATUS = {0: "HERALD_OK", 1: "HERALD_ERR_INVALID_ARG", 2: "HERALD_ERR_UNSUPPORTED_SHAPE",
           3: "HERALD_ERR_WORKSPACE_TOO_SMALL", 4: "HERALD_ERR_CUDA"}
 
 EXPORTS = ("herald_workspace_size", "herald_status_string", "herald_last_error",
            "herald_workspace_error", "herald_select_stage1", "herald_select_stage2",
            "herald_select", "herald_gather", "herald_denoise_attn",
-           "herald_denoise_attn_settled", "herald_append_kv",
+           "herald_denoise_attn_ex", "herald_append_kv",
            "herald_trace_begin", "herald_trace_end", "herald_trace_name",
            "herald_select_stage2_noalloc", "herald_selftest_wait_timeout",
            "herald_workspace_size_exact", "herald_select_exact")
@@ -78,7 +80,8 @@ def lib() -> C.CDLL:
         L.herald_gather.argtypes = [Dims, vp, vp, i32, vp, vp, vp, vp, vp]
         L.herald_denoise_attn.argtypes = [Dims, vp, vp, vp, vp, i32, vp, vp, vp, C.c_float, vp,
                                           sz, vp]
-        L.herald_denoise_attn_settled.argtypes = L.herald_denoise_attn.argtypes
+        L.herald_denoise_attn_ex.argtypes = [Dims, vp, vp, vp, vp, i32, vp, vp, vp, C.c_float,
+                                             C.c_uint, vp, vp, vp, vp, sz, vp]
         L.herald_append_kv.argtypes = [Dims, vp, vp, vp, vp, vp, i32, vp]
         L.herald_select_stage2_noalloc.argtypes = [Dims, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                    i32, vp, vp, vp]
@@ -235,12 +238,13 @@ def herald_denoise_attn(d, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, ou
                                      _nbytes(ws, ws_bytes), _s(stream)))
 
 
-def herald_denoise_attn_settled(d, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out,
-                                scale=0.0, ws=None, ws_bytes=None, stream=None):
-    _check(lib().herald_denoise_attn_settled(d, _p(q), _p(pool_k), _p(pool_v), _p(n_sel),
-                                             int(P_max), _p(block_k), _p(block_v), _p(out),
-                                             float(scale), _p(ws), _nbytes(ws, ws_bytes),
-                                             _s(stream)))
+def herald_denoise_attn_ex(d, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale=0.0,
+                           flags=0, ctx_len=None, k_cache=None, v_cache=None, ws=None,
+                           ws_bytes=None, stream=None):
+    _check(lib().herald_denoise_attn_ex(d, _p(q), _p(pool_k), _p(pool_v), _p(n_sel), int(P_max),
+                                        _p(block_k), _p(block_v), _p(out), float(scale),
+                                        int(flags), _p(ctx_len), _p(k_cache), _p(v_cache),
+                                        _p(ws), _nbytes(ws, ws_bytes), _s(stream)))
 
 
 def herald_append_kv(d, block_k, block_v, ctx_len, k_cache, v_cache, advance=True,

@@ -13,8 +13,10 @@ selection stream:
     den: gather -> pool[i%2]
     sel: stage 1 for block i+1 from block i's first-step queries
          -> cand[(i+1)%2]                         (overlaps the T steps below)
-    den: T x sparse block attention over pool[i%2]
-    den: wait for sel; append block i's final K/V
+    den: T-1 x sparse block attention over pool[i%2] (steps after the first
+         load the settled pool before their predecessor ends)
+    den: wait for sel; the last attention step, which also appends block i's
+         final K/V to the cache (one kernel)
 
 Stage 1 of block i+1 scans the cache before block i is appended; block i's
 positions reach block i+1's selection through the local window.  The two
@@ -24,6 +26,17 @@ every step of the path is a call into libherald.so.
 from __future__ import annotations
 
 from . import herald as H
+
+
+def step_flags(t: int, T: int, advance: bool) -> int:
+    """herald_denoise_attn_ex flags of denoising step t of T: steps after the
+    first find the pool settled (written before step 0, a herald call on the
+    same stream); the last also appends the block to the cache (and advances
+    the context when asked)."""
+    flags = H.HERALD_ATTN_SETTLED if t > 0 else 0
+    if t == T - 1:
+        flags |= H.HERALD_ATTN_APPEND | (H.HERALD_ATTN_ADVANCE if advance else 0)
+    return flags
 
 
 class BlockPipeline:
@@ -133,16 +146,11 @@ class BlockPipeline:
                                    self._n_cand[nxt], self._ws_sel, wb,
                                    self.sel_sms if overlap else 0, hs if overlap else hd))
         for t in range(self.T):
-            # steps after the first: the pool and n_sel were written before
-            # step 0, a herald call on this stream, so they are loaded early
-            attn = L.herald_denoise_attn_settled if t > 0 else L.herald_denoise_attn
-            chk(attn(d, q0 + t * qstep, pk, pv, self._n_sel, P, bk0 + t * bstep, bv0 + t * bstep,
-                     o0 + t * ostep, 0.0, wd, wb, hd))
-        if overlap:
-            den.wait_stream(sel)
-        last = self.T - 1
-        chk(L.herald_append_kv(d, bk0 + last * bstep, bv0 + last * bstep, cx, kc, vc,
-                               int(bool(advance)), hd))
+            if t == self.T - 1 and overlap:
+                den.wait_stream(sel)  # stage 1 reads the cache the last step appends to
+            chk(L.herald_denoise_attn_ex(d, q0 + t * qstep, pk, pv, self._n_sel, P,
+                                         bk0 + t * bstep, bv0 + t * bstep, o0 + t * ostep, 0.0,
+                                         step_flags(t, self.T, advance), cx, kc, vc, wd, wb, hd))
 
 
     def block_exact(self, i: int, q_steps, block_k, block_v, k_cache, v_cache, ctx, out,
@@ -164,14 +172,9 @@ class BlockPipeline:
                                   self._n_sel, self._ws_exact, self._ws_exact_bytes, hd))
         chk(L.herald_gather(d, self._idx, self._n_sel, P, kc, vc, pk, pv, hd))
         for t in range(self.T):
-            # steps after the first: the pool and n_sel were written before
-            # step 0, a herald call on this stream, so they are loaded early
-            attn = L.herald_denoise_attn_settled if t > 0 else L.herald_denoise_attn
-            chk(attn(d, q0 + t * qstep, pk, pv, self._n_sel, P, bk0 + t * bstep, bv0 + t * bstep,
-                     o0 + t * ostep, 0.0, wd, wb, hd))
-        last = self.T - 1
-        chk(L.herald_append_kv(d, bk0 + last * bstep, bv0 + last * bstep, cx, kc, vc,
-                               int(bool(advance)), hd))
+            chk(L.herald_denoise_attn_ex(d, q0 + t * qstep, pk, pv, self._n_sel, P,
+                                         bk0 + t * bstep, bv0 + t * bstep, o0 + t * ostep, 0.0,
+                                         step_flags(t, self.T, advance), cx, kc, vc, wd, wb, hd))
 
 
 class StackPipeline:
@@ -230,6 +233,9 @@ class StackPipeline:
         den, sel = torch.cuda.current_stream(), self.sel
         cur, nxt = i % 2, (i + 1) % 2
         d, P = self.d, self.P
+        # the last step appends each layer's block (with T = 1 it would come
+        # before that layer's stage 1, which must see the cache without it)
+        fuse = self.T > 1
         for t in range(self.T):
             for l in range(self.nl):
                 if t == 0:
@@ -239,10 +245,14 @@ class StackPipeline:
                                            self.n_sel[l], self.ws_den, self.ws_bytes, den)
                     H.herald_gather(d, self.idx[l], self.n_sel[l], P, k_caches[l], v_caches[l],
                                     self.pool_k[l][cur], self.pool_v[l][cur], den)
-                attn = H.herald_denoise_attn_settled if t > 0 else H.herald_denoise_attn
-                attn(d, q_steps[l][t], self.pool_k[l][cur], self.pool_v[l][cur], self.n_sel[l], P,
-                     block_k[l][t], block_v[l][t], out[l][t], 0.0, self.ws_den, self.ws_bytes,
-                     den)
+                if fuse and t == self.T - 1 and l == 0 and overlap:
+                    den.wait_stream(sel)  # stage 1 reads the caches the last step appends to
+                flags = step_flags(t, self.T, advance and l == self.nl - 1) if fuse else \
+                    (H.HERALD_ATTN_SETTLED if t > 0 else 0)
+                H.herald_denoise_attn_ex(d, q_steps[l][t], self.pool_k[l][cur],
+                                         self.pool_v[l][cur], self.n_sel[l], P, block_k[l][t],
+                                         block_v[l][t], out[l][t], 0.0, flags, ctx, k_caches[l],
+                                         v_caches[l], self.ws_den, self.ws_bytes, den)
                 if t == 0:
                     if overlap:
                         sel.wait_stream(den)
@@ -255,8 +265,9 @@ class StackPipeline:
                         H.herald_select_stage1(d, q_steps[l][0], k_caches[l], ctx, self.C,
                                                self.cand[l][nxt], self.n_cand[l][nxt],
                                                self.ws_sel, self.ws_bytes, den)
-        if overlap:
-            den.wait_stream(sel)
-        for l in range(self.nl):
-            H.herald_append_kv(d, block_k[l][self.T - 1], block_v[l][self.T - 1], ctx,
-                               k_caches[l], v_caches[l], advance and l == self.nl - 1, den)
+        if not fuse:  # one step per block: its stage 1 follows it, the appends come last
+            if overlap:
+                den.wait_stream(sel)
+            for l in range(self.nl):
+                H.herald_append_kv(d, block_k[l][self.T - 1], block_v[l][self.T - 1], ctx,
+                                   k_caches[l], v_caches[l], advance and l == self.nl - 1, den)

@@ -175,24 +175,40 @@ herald_status herald_denoise_attn(herald_dims dims, const uint16_t *q, const uin
                                   uint16_t *out, float scale, void *ws, size_t ws_bytes,
                                   void *stream);
 
-/* herald_denoise_attn for steps 1..T-1 of a block: the same arguments and
- * result; the pool keys are loaded while the work before the call on
- * `stream` is still finishing, instead of after it.  The pool is fixed
- * across a block's T steps ([EA]: one selection serves all of them).  Done
- * only when the whole grid is resident at once (otherwise this call is
- * herald_denoise_attn).
- * Precondition: pool_k was written before some earlier herald_* call on
- * `stream` (and nothing writes it since): every herald kernel lets its
- * successor start only after its own predecessor has finished, so the pool
- * is final when this kernel starts.  A call right after the herald_gather
- * that wrote the pool must use herald_denoise_attn; breaking the
- * precondition races with that write. */
-herald_status herald_denoise_attn_settled(herald_dims dims, const uint16_t *q,
-                                          const uint16_t *pool_k, const uint16_t *pool_v,
-                                          const int32_t *n_sel, int P_max,
-                                          const uint16_t *block_k, const uint16_t *block_v,
-                                          uint16_t *out, float scale, void *ws,
-                                          size_t ws_bytes, void *stream);
+/* Flags of herald_denoise_attn_ex. */
+#define HERALD_ATTN_SETTLED 1u /* the pool was written before an earlier herald call  */
+#define HERALD_ATTN_APPEND 2u  /* also append block_k/block_v to the cache            */
+#define HERALD_ATTN_ADVANCE 4u /* with APPEND: then advance ctx_len                    */
+
+/* herald_denoise_attn with options for the steps of a block (flags = 0 is
+ * herald_denoise_attn; ctx_len, k_cache, v_cache are used only with
+ * HERALD_ATTN_APPEND and may be NULL otherwise).
+ *   HERALD_ATTN_SETTLED (steps 1..T-1): the pool keys are loaded while the
+ *     work before the call on `stream` is still finishing, instead of after
+ *     it.  The pool is fixed across a block's T steps ([EA]: one selection
+ *     serves all of them).  Precondition: pool_k was written before some
+ *     earlier herald_* call on `stream` (and nothing writes it since): every
+ *     herald kernel lets its successor start only after its own predecessor
+ *     has finished, so the pool is final when this kernel starts.  A call
+ *     right after the herald_gather that wrote the pool must not set it;
+ *     breaking the precondition races with that write.  Applied only when
+ *     the whole grid is resident at once (otherwise ignored).
+ *   HERALD_ATTN_APPEND (the last step): the result of herald_append_kv(dims,
+ *     block_k, block_v, ctx_len, k_cache, v_cache, flags & ADVANCE) as
+ *     well, in the same kernel when the cache is in device memory (one
+ *     launch fewer per block; [V3]: the decoded block joins the cache), by
+ *     the append kernel after the step when it is in host memory.  The
+ *     cache and ctx_len must not be read by work that can run concurrently
+ *     (the dual-stream pipeline joins its stage-1 stream before this call).
+ *   HERALD_ATTN_ADVANCE: with APPEND, ctx_len[n] = min(ctx_len[n] + B, L_max).
+ * Unknown flag bits, ADVANCE without APPEND, or APPEND with a null ctx_len,
+ * k_cache or v_cache: HERALD_ERR_INVALID_ARG. */
+herald_status herald_denoise_attn_ex(herald_dims dims, const uint16_t *q, const uint16_t *pool_k,
+                                     const uint16_t *pool_v, const int32_t *n_sel, int P_max,
+                                     const uint16_t *block_k, const uint16_t *block_v,
+                                     uint16_t *out, float scale, unsigned flags,
+                                     int32_t *ctx_len, uint16_t *k_cache, uint16_t *v_cache,
+                                     void *ws, size_t ws_bytes, void *stream);
 
 /* Appends a decoded block to the cache ([V3]: the cache grows with every
  * decoded block):  cache[n][g][ctx_len[n] + b] = block[n][b][g] for b < B

@@ -101,6 +101,17 @@ def test_attention_and_gather_argument_errors():
     with pytest.raises(H.HeraldError) as e:
         H.herald_denoise_attn(d, ok, ok, ok, ok, 208, ok, ok, ok, -1.0, ok, ws)
     assert e.value.status == 1
+    # the options of a denoising step: unknown bits, ADVANCE without APPEND,
+    # APPEND without a cache
+    for flags, extra in [(8, {}), (H.HERALD_ATTN_ADVANCE, {}),
+                         (H.HERALD_ATTN_APPEND, dict(ctx_len=None, k_cache=ok, v_cache=ok)),
+                         (H.HERALD_ATTN_APPEND, dict(ctx_len=ok, k_cache=ok, v_cache=None))]:
+        a = dict(ctx_len=ok, k_cache=ok, v_cache=ok)
+        a.update(extra)
+        with pytest.raises(H.HeraldError) as e:
+            H.herald_denoise_attn_ex(d, ok, ok, ok, ok, 208, ok, ok, ok, 0.0, flags,
+                                     a["ctx_len"], a["k_cache"], a["v_cache"], ok, ws)
+        assert e.value.status == 1, (flags, extra)
     with pytest.raises(H.HeraldError) as e:
         H.herald_gather(d, ok, ok, 0, ok, ok, ok, ok)
     assert e.value.status == 1

@@ -100,10 +100,10 @@ class Run:
         H.herald_gather(self.d, self.idx, self.n_sel, self.P, self.k, self.v, self.pool_k,
                         self.pool_v)
 
-    def attn(self, t, out=None, settled=False):
-        f = H.herald_denoise_attn_settled if settled else H.herald_denoise_attn
-        f(self.d, self.q_steps[t], self.pool_k, self.pool_v, self.n_sel, self.P, self.bk[t],
-          self.bv[t], self.out if out is None else out, 0.0, self.ws)
+    def attn(self, t, out=None, flags=0):
+        H.herald_denoise_attn_ex(self.d, self.q_steps[t], self.pool_k, self.pool_v, self.n_sel,
+                                 self.P, self.bk[t], self.bv[t], self.out if out is None else out,
+                                 0.0, flags, self.ctx, self.k, self.v, self.ws)
 
     def error_word(self):
         return H.herald_workspace_error(self.ws)
@@ -209,7 +209,7 @@ def test_gather_and_attention(w):
     # load the (settled) pool before waiting for their predecessor
     outs = [torch.zeros_like(r.out) for _ in range(w.T)]
     for t in range(w.T):
-        r.attn(t, outs[t], settled=t > 0)
+        r.attn(t, outs[t], H.HERALD_ATTN_SETTLED if t > 0 else 0)
     torch.cuda.synchronize()
     for t in range(w.T):
         out = bf16_dev_to_f64(outs[t])
@@ -303,6 +303,44 @@ def test_append_matches_oracle_bit_exact():
     # the second sequence overflows L_max = 340: rows past it are skipped and
     # the context is capped
     assert r.ctx.cpu().numpy().tolist() == [316, 340]
+    kk = synth.bf16_to_f64(r.k.cpu().numpy().view(np.uint16))
+    vv = synth.bf16_to_f64(r.v.cpu().numpy().view(np.uint16))
+    np.testing.assert_array_equal(kk, k2)
+    np.testing.assert_array_equal(vv, v2)
+
+
+@pytest.mark.parametrize("advance", [True, False])
+@pytest.mark.parametrize("placement", ["device", "host"])
+def test_last_step_appends_like_append_kv(placement, advance):
+    """A denoising step with HERALD_ATTN_APPEND writes the cache rows and the
+    context lengths bit-exactly as herald_append_kv does (fused into the
+    attention kernel for a device cache, the append kernel after it for a
+    host-resident one), and its attention output is the plain step's."""
+    w = _case("append-step", N=2, Hq=8, Hkv=2, d=128, L=300, B=16, C=64, K=32, S=4, W=4,
+              extra_rows=40, index=20)
+    r = Run(w, ctx=[300, 330])
+    r.select()
+    r.gather()
+    t = w.T - 1
+    r.attn(t)
+    torch.cuda.synchronize()
+    out_plain = r.out.clone()
+    r.out.zero_()
+    if placement == "host":
+        r.k = torch.from_numpy(r.x["k_cache"].view(np.int16).copy()).pin_memory()
+        r.v = torch.from_numpy(r.x["v_cache"].view(np.int16).copy()).pin_memory()
+    flags = H.HERALD_ATTN_SETTLED | H.HERALD_ATTN_APPEND
+    if advance:
+        flags |= H.HERALD_ATTN_ADVANCE
+    r.attn(t, flags=flags)
+    torch.cuda.synchronize()
+    assert r.error_word() == 0
+    assert torch.equal(r.out, out_plain)
+    _, k2, v2 = oracle.append(r.x["ctx"], f64(r.x["block_k"][t]), f64(r.x["block_v"][t]),
+                              f64(r.x["k_cache"]), f64(r.x["v_cache"]))
+    # the second sequence overflows L_max = 340: its rows past it are
+    # skipped and its length is capped at the cache's capacity
+    assert r.ctx.cpu().numpy().tolist() == ([316, 340] if advance else [300, 330])
     kk = synth.bf16_to_f64(r.k.cpu().numpy().view(np.uint16))
     vv = synth.bf16_to_f64(r.v.cpu().numpy().view(np.uint16))
     np.testing.assert_array_equal(kk, k2)
