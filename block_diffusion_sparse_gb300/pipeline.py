@@ -28,6 +28,28 @@ from __future__ import annotations
 from . import herald as H
 
 
+# cache bytes one SM of the background scan streams: ~7 us at the ~150 GB/s
+# one SM sustains, well inside the denoising steps the scan hides behind
+SCAN_BYTES_PER_SM = 1 << 20
+
+
+def background_sms(dims: H.Dims) -> int:
+    """SMs for the stage-1 scan that runs beside the denoising steps (0 = all).
+
+    A persistent scan over every SM delays the denoising kernels, whose CTAs
+    (and, with programmatic launch, those of the next step) need SMs of
+    their own; confined to about one SM per MiB of keys it still ends in
+    time.  On the 32K layer (34 MB of keys) 24-40 SMs took the block step
+    from 94.7 to 92 us, 16 made stage 1 the longer stream (109 us); a cache
+    that needs most of the SMs' bandwidth anyway (4 x 64K: 537 MB) keeps
+    them all (32 SMs: 674 against 521 us)."""
+    import torch
+    n_sm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    key_bytes = dims.N * dims.Hkv * dims.L_max * dims.d * 2
+    want = max(32, -(-key_bytes // SCAN_BYTES_PER_SM))
+    return 0 if want >= n_sm // 2 else want
+
+
 def step_flags(t: int, T: int, advance: bool) -> int:
     """herald_denoise_attn_ex flags of denoising step t of T: steps after the
     first find the pool settled (written before step 0, a herald call on the
@@ -44,9 +66,8 @@ class BlockPipeline:
                  den_stream=None, sel_stream=None, sel_sms=None, exact: bool = False):
         import torch
         self.torch = torch
-        # SMs the overlapped stage-1 scan may occupy (0: all); measured on the
-        # bench workloads, confining it did not shorten the step
-        self.sel_sms = 0 if sel_sms is None else int(sel_sms)
+        # SMs the overlapped stage-1 scan may occupy (0: all)
+        self.sel_sms = background_sms(dims) if sel_sms is None else int(sel_sms)
         self.d, self.C, self.K, self.S, self.W, self.P, self.T = dims, C, K, S, W, P, T
         NG = (dims.N, dims.Hkv)
         dev = "cuda"
@@ -216,7 +237,7 @@ class StackPipeline:
         self.pool_v = [[mk((*NG, P, dims.d), torch.int16) for _ in range(2)]
                        for _ in range(n_layers)]
         self.sel = sel_stream if sel_stream is not None else torch.cuda.Stream()
-        self.sel_sms = 0
+        self.sel_sms = background_sms(dims)
 
     def prime(self, q_merge, k_caches, ctx, slot: int = 0):
         st = self.torch.cuda.current_stream()
