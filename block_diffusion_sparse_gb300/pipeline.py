@@ -25,15 +25,26 @@ every step of the path is a call into libherald.so.
 """
 from __future__ import annotations
 
+import functools
+
 from . import herald as H
 
 
 # cache bytes one SM of the background scan streams: ~7 us at the ~150 GB/s
 # one SM sustains, well inside the denoising steps the scan hides behind
 SCAN_BYTES_PER_SM = 1 << 20
+# SMs of the background scan of a cache in host memory: the host link, not
+# the SMs, bounds it
+HOST_SCAN_SMS = 64
 
 
-def background_sms(dims: H.Dims) -> int:
+@functools.lru_cache(maxsize=None)
+def _sm_count(device: int) -> int:
+    import torch
+    return torch.cuda.get_device_properties(device).multi_processor_count
+
+
+def background_sms(dims: H.Dims, host: bool = False) -> int:
     """SMs for the stage-1 scan that runs beside the denoising steps (0 = all).
 
     A persistent scan over every SM delays the denoising kernels, whose CTAs
@@ -42,12 +53,25 @@ def background_sms(dims: H.Dims) -> int:
     time.  On the 32K layer (34 MB of keys) 24-40 SMs took the block step
     from 94.7 to 92 us, 16 made stage 1 the longer stream (109 us); a cache
     that needs most of the SMs' bandwidth anyway (4 x 64K: 537 MB) keeps
-    them all (32 SMs: 674 against 521 us)."""
+    them all (32 SMs: 674 against 521 us).  A cache in host memory is read
+    at the link's rate by a few dozen SMs: 64 took the 128K host-resident
+    layer from 1661 to 1494 us per block (32: 1517, 96: 1528)."""
     import torch
-    n_sm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    n_sm = _sm_count(torch.cuda.current_device())
+    if host:
+        return min(HOST_SCAN_SMS, n_sm)
     key_bytes = dims.N * dims.Hkv * dims.L_max * dims.d * 2
     want = max(32, -(-key_bytes // SCAN_BYTES_PER_SM))
     return 0 if want >= n_sm // 2 else want
+
+
+def scan_sms(dims: H.Dims, k_cache, fixed=None) -> int:
+    """The background scan's SM budget for this cache: `fixed` if given, else
+    background_sms for a cache in device or (a CPU tensor) pinned host memory."""
+    if fixed is not None:
+        return fixed
+    host = getattr(k_cache, "device", None) is not None and k_cache.device.type == "cpu"
+    return background_sms(dims, host=host)
 
 
 def step_flags(t: int, T: int, advance: bool) -> int:
@@ -67,7 +91,8 @@ class BlockPipeline:
         import torch
         self.torch = torch
         # SMs the overlapped stage-1 scan may occupy (0: all)
-        self.sel_sms = background_sms(dims) if sel_sms is None else int(sel_sms)
+        # None: background_sms for the cache each block reads
+        self.sel_sms = None if sel_sms is None else int(sel_sms)
         self.d, self.C, self.K, self.S, self.W, self.P, self.T = dims, C, K, S, W, P, T
         NG = (dims.N, dims.Hkv)
         dev = "cuda"
@@ -145,6 +170,9 @@ class BlockPipeline:
         den.wait_stream(cap)
         self._graphs[key] = g
 
+    def _scan_sms(self, k_cache) -> int:
+        return scan_sms(self.d, k_cache, self.sel_sms)
+
     def _block(self, i, q_steps, block_k, block_v, k_cache, v_cache, ctx, out, next_k_cache,
                advance, overlap):
         den, sel = self._den(), self.sel
@@ -165,7 +193,7 @@ class BlockPipeline:
         chk(L.herald_gather(d, self._idx, self._n_sel, P, kc, vc, pk, pv, hd))
         chk(L.herald_select_stage1(d, q0, H.ptr(nk), cx, self.C, self._cand[nxt],
                                    self._n_cand[nxt], self._ws_sel, wb,
-                                   self.sel_sms if overlap else 0, hs if overlap else hd))
+                                   self._scan_sms(nk) if overlap else 0, hs if overlap else hd))
         for t in range(self.T):
             if t == self.T - 1 and overlap:
                 den.wait_stream(sel)  # stage 1 reads the cache the last step appends to
@@ -237,7 +265,10 @@ class StackPipeline:
         self.pool_v = [[mk((*NG, P, dims.d), torch.int16) for _ in range(2)]
                        for _ in range(n_layers)]
         self.sel = sel_stream if sel_stream is not None else torch.cuda.Stream()
-        self.sel_sms = background_sms(dims)
+        self.sel_sms = None  # None: background_sms for the caches each block reads
+
+    def _scan_sms(self, k_cache) -> int:
+        return scan_sms(self.d, k_cache, self.sel_sms)
 
     def prime(self, q_merge, k_caches, ctx, slot: int = 0):
         st = self.torch.cuda.current_stream()
@@ -281,7 +312,7 @@ class StackPipeline:
                             H.herald_select_stage1(d, q_steps[l][0], k_caches[l], ctx, self.C,
                                                    self.cand[l][nxt], self.n_cand[l][nxt],
                                                    self.ws_sel, self.ws_bytes, sel,
-                                                   sm_budget=self.sel_sms)
+                                                   sm_budget=self._scan_sms(k_caches[l]))
                     else:
                         H.herald_select_stage1(d, q_steps[l][0], k_caches[l], ctx, self.C,
                                                self.cand[l][nxt], self.n_cand[l][nxt],
