@@ -31,10 +31,12 @@ __global__ void __launch_bounds__(256)
   const int seg = blockIdx.y;
   const int row = blockIdx.x * RPC + threadIdx.x / TPR, c = threadIdx.x % TPR;
   if (row >= P_max) return;
+  // idx is read with n_sel, not after it: the row lies inside the index
+  // buffer either way, and its entry is used only below n_sel
+  const int pos = idx[size_t(seg) * P_max + row];
   const int ns = min(max(n_sel[seg], 0), P_max);
   uint4 kv = make_uint4(0, 0, 0, 0), vv = kv;
   if (row < ns) {
-    const int pos = idx[size_t(seg) * P_max + row];
     if (pos >= 0 && pos < L_max) {
       const size_t off = (size_t(seg) * L_max + pos) * D + c * 8;
       kv = ld_nc_v4(kc + off);

@@ -460,13 +460,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int hv = 0; hv < D / 64; ++hv)
       tma_load_3d(Qs + hv * kTileM * 128, &qmap, &barQ, hv * 64, g * G, n * B + b0);
   }
-  const int nc = min(max(n_cand[seg], 0), C);
+  // the candidate positions are read with n_cand, not after it: every slot
+  // below C lies inside the list, and rows past n_cand are masked below
   const int c0 = int(rank) * cpc;
-  const int ncv = min(max(nc - c0, 0), cpc);  // valid candidates of this CTA
   const int32_t* cd = cand ? cand + size_t(seg) * C : nullptr;  // null: row = slot
-  for (int r = threadIdx.x; r < cpc; r += kTcThreads) {
-    const int p = r < ncv ? (cand ? cd[c0 + r] : c0 + r) : -1;
-    pos[r] = (p >= 0 && p < L_max) ? p : -1;
+  int pr[kFuseMaxCpc / kTcThreads];
+#pragma unroll
+  for (int k = 0; k < kFuseMaxCpc / kTcThreads; ++k) {
+    const int r = threadIdx.x + k * kTcThreads;
+    pr[k] = (cd && r < cpc && c0 + r < C) ? cd[c0 + r] : -1;
+  }
+  const int nc = min(max(n_cand[seg], 0), C);
+  const int ncv = min(max(nc - c0, 0), cpc);  // valid candidates of this CTA
+#pragma unroll
+  for (int k = 0; k < kFuseMaxCpc / kTcThreads; ++k) {
+    const int r = threadIdx.x + k * kTcThreads;
+    if (r < cpc) {
+      const int p = r < ncv ? (cand ? pr[k] : c0 + r) : -1;
+      pos[r] = (p >= 0 && p < L_max) ? p : -1;
+    }
   }
   __syncthreads();
   // the tile's rows past its G*bpt query rows are never loaded: zeroed, so
