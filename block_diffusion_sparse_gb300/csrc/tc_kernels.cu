@@ -8,10 +8,18 @@
 //   refine_pass2  S^T = K_cand . Q_blk^T for 128 candidates x all B*G rows;
 //                 each thread owns one candidate and sums the row-softmax
 //                 probabilities over the rows -> s2 (column sum)
-//   attn          one 128-key split of sparse block attention (HERALD early
+//   refine_fused  stage 2 in one pass when C <= 4096: an 8-CTA cluster per
+//                 row tile shares the row statistics, exponentials are kept
+//                 in TMEM and summed by column
+//   attn_pool     sparse block attention over the pool (HERALD early
 //                 abstract: the selected subset is reused for every
 //                 denoising step; block keys are visible to every block
-//                 query): S = Q K^T, P = exp(S - rowmax), O = P V
+//                 query): one 8-CTA cluster per row tile, the pool split
+//                 between its CTAs; optionally appends the decoded block
+//   attn_cluster  the same with cp.async operands, for shapes the pool
+//                 kernel does not take
+//   attn          one 128-key split of sparse block attention (pools beyond
+//                 shared memory): S = Q K^T, P = exp(S - rowmax), O = P V
 //   attn_combine  merges the splits by their (max, sum) into bf16 out
 #include <cuda_bf16.h>
 #include <stdlib.h>
@@ -1168,7 +1176,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // shared::cta -> shared::cluster copies that complete on c's mbarrier;
 // each CTA merges its 16 rows once all 8 slices have landed.  The receive
 // buffers have shared memory of their own, so no cluster-wide barrier
-// separates the attention from the exchange.
+// separates the attention from the exchange.  Only the 16-key chunks that
+// hold a valid key enter S, the softmax and P V.  Two options of the entry
+// point: the pool keys loaded before the grid-dependency wait (steps after
+// a block's first, when the pool is settled), and the append of the block
+// to the cache by one cluster per sequence (the last step).
 constexpr int kPoolCtas = 8;
 constexpr int kPoolRows = kTileM / kPoolCtas;   // rows finalised per CTA
 constexpr int kPoolMaxB = 64;
