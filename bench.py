@@ -25,6 +25,7 @@ import ctypes
 import hashlib
 import json
 import os
+import re
 import sys
 import threading
 import time
@@ -144,10 +145,14 @@ def workload():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources without their comments and blank lines: a
+    committed ncu summary stays valid across edits that change no code."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_diffusion_sparse_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        text = re.sub(r"/\*.*?\*/", "", open(os.path.join(csrc, f)).read(), flags=re.S)
+        lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.split("\n"))
+        h.update("\n".join(ln for ln in lines if ln.strip()).encode())
     return h.hexdigest()[:16]
 
 
