@@ -249,7 +249,8 @@ herald_status run_stage1(const herald_dims& dm, const uint16_t* q_merge, const u
 herald_status run_stage2(const herald_dims& dm, const uint16_t* q_block, const uint16_t* k_cache,
                          const int32_t* ctx_len, const int32_t* cand, const int32_t* n_cand,
                          int C, int K, int sink, int local, int P_max, int32_t* idx,
-                         int32_t* n_sel, void* ws, const WsLayout& w, cudaStream_t st) {
+                         int32_t* n_sel, void* ws, const WsLayout& w, cudaStream_t st,
+                         const PoolGather* gather) {
   uint32_t* err = at<uint32_t>(ws, w.err);
   CUtensorMap qmap, qmap_all;
   const int G = dm.Hq / dm.Hkv;
@@ -281,7 +282,7 @@ herald_status run_stage2(const herald_dims& dm, const uint16_t* q_block, const u
   }
   const int n_parts = refine_fused_ok(C) ? w.MT_tok : 1;
   HERALD_TRY_CUDA(launch_topk_union(dm, ctx_len, cand, n_cand, at<float>(ws, w.s2), n_parts, C, K,
-                                    sink, local, P_max, idx, n_sel, st),
+                                    sink, local, P_max, idx, n_sel, st, gather),
                   "topk_union launch");
   return HERALD_OK;
 }
@@ -545,7 +546,55 @@ herald_status herald_select_stage2(herald_dims dims, const uint16_t* q_block,
   WsLayout w;
   HERALD_RET_IF(check_ws(dims, C, P_max, ws, ws_bytes, &w));
   return run_stage2(dims, q_block, k_cache, ctx_len, cand, n_cand, C, K, sink, local, P_max, idx,
-                    n_sel, ws, w, static_cast<cudaStream_t>(stream));
+                    n_sel, ws, w, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+// The gather rides with the top-K when there are many (sequence, KV head)
+// pairs: each then has a few top-K CTAs, one per slice of its pool.  With few
+// pairs the separate wide gather kernel measured faster (32K layer, 4 pairs:
+// 91.7 against 93.3 us per block at 8 copies, 101.5 at 16; 4 x 64K layer,
+// 32 pairs: 503.5 against 518.5 us at 4 copies, 505.6 at 8).
+constexpr int kFusedGatherMinSegs = 16;
+constexpr int kFusedGatherMaxCopies = 4;
+
+herald_status herald_select_stage2_gather(herald_dims dims, const uint16_t* q_block,
+                                          const uint16_t* k_cache, const uint16_t* v_cache,
+                                          const int32_t* ctx_len, const int32_t* cand,
+                                          const int32_t* n_cand, int C, int K, int sink,
+                                          int local, int P_max, int32_t* idx, int32_t* n_sel,
+                                          uint16_t* pool_k, uint16_t* pool_v, void* ws,
+                                          size_t ws_bytes, void* stream) {
+  g_err[0] = 0;
+  HERALD_RET_IF(check_dims(dims));
+  HERALD_RET_IF(check_c(C));
+  HERALD_RET_IF(check_pmax(dims, P_max));
+  HERALD_RET_IF(check_budget(C, K, sink, local, P_max));
+  HERALD_CHECK_PTR(q_block);
+  HERALD_CHECK_PTR(k_cache);
+  HERALD_CHECK_PTR(v_cache);
+  HERALD_CHECK_PTR(ctx_len);
+  HERALD_CHECK_PTR(cand);
+  HERALD_CHECK_PTR(n_cand);
+  HERALD_CHECK_PTR(idx);
+  HERALD_CHECK_PTR(n_sel);
+  HERALD_CHECK_PTR(pool_k);
+  HERALD_CHECK_PTR(pool_v);
+  WsLayout w;
+  HERALD_RET_IF(check_ws(dims, C, P_max, ws, ws_bytes, &w));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int segs = dims.N * dims.Hkv;
+  if (segs >= kFusedGatherMinSegs && is_device_memory(k_cache) && is_device_memory(v_cache)) {
+    int copies = std::max(1, std::min(kFusedGatherMaxCopies, sm_count() / segs));
+    const PoolGather pg{k_cache, v_cache, pool_k, pool_v, dims.d, copies};
+    return run_stage2(dims, q_block, k_cache, ctx_len, cand, n_cand, C, K, sink, local, P_max,
+                      idx, n_sel, ws, w, st, &pg);
+  }
+  // a cache in host memory: the wide gather kernel keeps the host link busy
+  HERALD_RET_IF(run_stage2(dims, q_block, k_cache, ctx_len, cand, n_cand, C, K, sink, local,
+                           P_max, idx, n_sel, ws, w, st, nullptr));
+  HERALD_TRY_CUDA(launch_gather(dims, idx, n_sel, P_max, k_cache, v_cache, pool_k, pool_v, st),
+                  "gather launch");
+  return HERALD_OK;
 }
 
 herald_status herald_select(herald_dims dims, const uint16_t* q_merge, const uint16_t* q_block,
@@ -570,7 +619,7 @@ herald_status herald_select(herald_dims dims, const uint16_t* q_merge, const uin
   int32_t* n_cand = at<int32_t>(ws, w.n_cand);
   HERALD_RET_IF(run_stage1(dims, q_merge, k_cache, ctx_len, C, cand, n_cand, ws, w, 0, st));
   return run_stage2(dims, q_block, k_cache, ctx_len, cand, n_cand, C, K, sink, local, P_max, idx,
-                    n_sel, ws, w, st);
+                    n_sel, ws, w, st, nullptr);
 }
 
 herald_status herald_gather(herald_dims dims, const int32_t* idx, const int32_t* n_sel,

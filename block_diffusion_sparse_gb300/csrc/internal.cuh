@@ -159,11 +159,23 @@ cudaError_t launch_refine(const herald_dims& dm, const uint16_t* k_cache, const 
 herald_status encode_heads_map(const void* base, uint64_t tokens, int heads, int d,
                                uint32_t box_heads, uint32_t box_tokens, CUtensorMap* map);
 
-// s2 holds n_parts partial score arrays of [N*Hkv][C], summed per candidate.
+// The pool gather fused into the top-K: `copies` CTAs per (sequence, KV
+// head) select alike and each copies one slice of the selected rows of the
+// cache (device memory) into the pool.
+struct PoolGather {
+  const uint16_t* kc;
+  const uint16_t* vc;
+  uint16_t* pk;
+  uint16_t* pv;
+  int d;
+  int copies;
+};
+// s2 holds n_parts partial score arrays of [N*Hkv][C], summed per candidate;
+// gather (optional) also fills the pool.
 cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const int32_t* cand,
                               const int32_t* n_cand, const float* s2, int n_parts, int C, int K,
                               int S, int W, int P_max, int32_t* idx, int32_t* n_sel,
-                              cudaStream_t st);
+                              cudaStream_t st, const PoolGather* gather = nullptr);
 // (name: the label the launch carries in traces)
 cudaError_t launch_gather(const herald_dims& dm, const int32_t* idx, const int32_t* n_sel,
                           int P_max, const uint16_t* k_cache, const uint16_t* v_cache,

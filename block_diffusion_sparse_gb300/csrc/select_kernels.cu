@@ -946,8 +946,10 @@ __global__ void __launch_bounds__(kTkThreads)
     topk_union_kernel(const int32_t* __restrict__ ctx, const int32_t* __restrict__ cand,
                       const int32_t* __restrict__ n_cand, const float* __restrict__ s2,
                       int n_parts, int Hkv, int L_max, int C, int K, int S, int W, int P_max,
-                      int32_t* __restrict__ idx, int32_t* __restrict__ n_sel) {
-  extern __shared__ uint32_t mem[];           // [C] bit patterns of the threshold-bin members
+                      int32_t* __restrict__ idx, int32_t* __restrict__ n_sel, PoolGather pg) {
+  // [C] bit patterns of the threshold-bin members, then (with the gather)
+  // [P_max] selected positions
+  extern __shared__ uint32_t mem[];
   __shared__ uint32_t h[kHistBins];
   __shared__ uint32_t taken[kMaxC / 32];      // bitmap over candidate slots
   __shared__ uint2 mpair[kTkRankCap];         // (bit pattern, slot) of the first members
@@ -955,7 +957,11 @@ __global__ void __launch_bounds__(kTkThreads)
   __shared__ int s_bin;
   __shared__ uint32_t s_above, s_cnt;
   griddep_enter();
-  const int seg = blockIdx.x, n = seg / Hkv;
+  // with the gather, pg.copies CTAs per (n, g) select alike (the selection
+  // is deterministic) and each gathers one slice of the pool; copy 0 writes
+  // idx and n_sel
+  const int copies = pg.pk ? pg.copies : 1;
+  const int seg = blockIdx.x / copies, copy = blockIdx.x - seg * copies, n = seg / Hkv;
   const int L = min(max(ctx[n], 0), L_max);
   const int nc = min(max(n_cand[seg], 0), C);
   const int Ke = min(K, nc);
@@ -964,7 +970,7 @@ __global__ void __launch_bounds__(kTkThreads)
   const int i0 = threadIdx.x * E;
   const int32_t* cd = cand + size_t(seg) * C;
   const float* sc = s2 + size_t(seg) * C;
-  const size_t part_stride = size_t(gridDim.x) * C;
+  const size_t part_stride = size_t(gridDim.x / copies) * C;  // [part][N*Hkv][C]
   // the candidate positions are needed only at the end; with few per thread
   // their loads are issued here, with the scores', so that no phase waits on
   // memory twice (with 16 per thread the registers are not there)
@@ -1121,46 +1127,75 @@ __global__ void __launch_bounds__(kTkThreads)
   uint32_t at, d3, n_mid, d4;
   block_excl_scan2<kTkThreads>(n_keep, 0u, wt, wt2, at, d3, n_mid, d4);
   int32_t* out = idx + size_t(seg) * P_max;
+  int32_t* sidx = reinterpret_cast<int32_t*>(mem + C);
+  const bool to_global = copy == 0;
+  auto put = [&](int slot, int32_t v) {
+    if (to_global) out[slot] = v;
+    if (pg.pk) sidx[slot] = v;
+  };
 #pragma unroll
   for (int k = 0; k < kPer; ++k)
     if ((keep_mask >> k) & 1u) {
-      if (sink_end + int(at) < P_max) out[sink_end + at] = pk[k];
+      if (sink_end + int(at) < P_max) put(sink_end + at, pk[k]);
       ++at;
     }
-  for (int j = threadIdx.x; j < sink_end; j += kTkThreads) out[j] = j;
+  for (int j = threadIdx.x; j < sink_end; j += kTkThreads) put(j, j);
   for (int j = local_begin + threadIdx.x; j < L; j += kTkThreads)
     if (sink_end + int(n_mid) + (j - local_begin) < P_max)
-      out[sink_end + n_mid + (j - local_begin)] = j;
+      put(sink_end + n_mid + (j - local_begin), j);
   const int total = min(P_max, sink_end + int(n_mid) + (L - local_begin));
-  for (int s = total + threadIdx.x; s < P_max; s += kTkThreads) out[s] = -1;
-  if (threadIdx.x == 0) n_sel[seg] = total;
+  for (int s = total + threadIdx.x; s < P_max; s += kTkThreads) put(s, -1);
+  if (to_global && threadIdx.x == 0) n_sel[seg] = total;
+  if (!pg.pk) return;
+  // the gather of this copy's slice of the pool: rows [r0, r1) of (n, g),
+  // zero rows from n_sel on, 16-byte chunks of K and V per thread
+  __syncthreads();
+  const int rpc = (P_max + copies - 1) / copies;
+  const int r0 = copy * rpc, r1 = min(P_max, r0 + rpc);
+  const int cpr = pg.d / 8;
+  const size_t seg_rows = size_t(seg) * L_max, pool_rows = size_t(seg) * P_max;
+  for (int u = threadIdx.x; u < (r1 - r0) * cpr; u += kTkThreads) {
+    const int r = r0 + u / cpr, c = u - (u / cpr) * cpr;
+    const int pos = r < total ? sidx[r] : -1;
+    uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
+    if (pos >= 0 && pos < L_max) {
+      const size_t off = (seg_rows + pos) * pg.d + c * 8;
+      kv = *reinterpret_cast<const uint4*>(pg.kc + off);
+      vv = *reinterpret_cast<const uint4*>(pg.vc + off);
+    }
+    const size_t dst = (pool_rows + r) * pg.d + c * 8;
+    *reinterpret_cast<uint4*>(pg.pk + dst) = kv;
+    *reinterpret_cast<uint4*>(pg.pv + dst) = vv;
+  }
 }
 
 cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const int32_t* cand,
                               const int32_t* n_cand, const float* s2, int n_parts, int C, int K,
                               int S, int W, int P_max, int32_t* idx, int32_t* n_sel,
-                              cudaStream_t st) {
+                              cudaStream_t st, const PoolGather* gather) {
   static_assert(kMaxC <= 16 * kTkThreads, "16 scores per thread cover every C");
-  const size_t smem = size_t(C) * 4;
-  static bool attr_done = false;
-  if (!attr_done) {
+  const PoolGather pg = gather ? *gather : PoolGather{nullptr, nullptr, nullptr, nullptr, 0, 1};
+  const size_t smem = size_t(C) * 4 + (pg.pk ? size_t(P_max) * 4 : 0u);
+  static size_t attr_bytes = 0;  // dynamic shared memory granted so far
+  if (smem > attr_bytes) {
     cudaError_t e = cudaFuncSetAttribute(topk_union_kernel<4>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxC * 4);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(topk_union_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kMaxC * 4);
+                             int(smem));
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    attr_bytes = smem;
   }
+  const int grid = dm.N * dm.Hkv * (pg.pk ? pg.copies : 1);
   // the fewest registers that hold C scores over 1024 threads
   if (C <= 4 * kTkThreads)
-    HERALD_CHECK_LAUNCH(launch_k("topk_union_kernel", topk_union_kernel<4>, dm.N * dm.Hkv,
-                                 kTkThreads, smem, st, ctx, cand, n_cand, s2, n_parts, dm.Hkv,
-                                 dm.L_max, C, K, S, W, P_max, idx, n_sel));
+    HERALD_CHECK_LAUNCH(launch_k("topk_union_kernel", topk_union_kernel<4>, grid, kTkThreads, smem,
+                                 st, ctx, cand, n_cand, s2, n_parts, dm.Hkv, dm.L_max, C, K, S, W,
+                                 P_max, idx, n_sel, pg));
   else
-    HERALD_CHECK_LAUNCH(launch_k("topk_union_kernel", topk_union_kernel<16>, dm.N * dm.Hkv,
-                                 kTkThreads, smem, st, ctx, cand, n_cand, s2, n_parts, dm.Hkv,
-                                 dm.L_max, C, K, S, W, P_max, idx, n_sel));
+    HERALD_CHECK_LAUNCH(launch_k("topk_union_kernel", topk_union_kernel<16>, grid, kTkThreads,
+                                 smem, st, ctx, cand, n_cand, s2, n_parts, dm.Hkv, dm.L_max, C, K,
+                                 S, W, P_max, idx, n_sel, pg));
   return cudaGetLastError();
 }
 

@@ -21,8 +21,8 @@ STATUS = {0: "HERALD_OK", 1: "HERALD_ERR_INVALID_ARG", 2: "HERALD_ERR_UNSUPPORTE
 
 EXPORTS = ("herald_workspace_size", "herald_status_string", "herald_last_error",
            "herald_workspace_error", "herald_select_stage1", "herald_select_stage2",
-           "herald_select", "herald_gather", "herald_denoise_attn",
-           "herald_denoise_attn_ex", "herald_append_kv",
+           "herald_select", "herald_select_stage2_gather", "herald_gather",
+           "herald_denoise_attn", "herald_denoise_attn_ex", "herald_append_kv",
            "herald_trace_begin", "herald_trace_end", "herald_trace_name",
            "herald_select_stage2_noalloc", "herald_selftest_wait_timeout",
            "herald_workspace_size_exact", "herald_select_exact")
@@ -77,6 +77,8 @@ def lib() -> C.CDLL:
                                            vp, vp, vp, sz, vp]
         L.herald_select.argtypes = [Dims, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp,
                                     sz, vp]
+        L.herald_select_stage2_gather.argtypes = [Dims, vp, vp, vp, vp, vp, vp, i32, i32, i32,
+                                                  i32, i32, vp, vp, vp, vp, vp, sz, vp]
         L.herald_gather.argtypes = [Dims, vp, vp, i32, vp, vp, vp, vp, vp]
         L.herald_denoise_attn.argtypes = [Dims, vp, vp, vp, vp, i32, vp, vp, vp, C.c_float, vp,
                                           sz, vp]
@@ -224,6 +226,16 @@ def herald_select_exact(d, q_block, k_cache, ctx_len, K, sink, local, P_max, idx
 def herald_selftest_wait_timeout(limit_ns, ws, stream=None):
     """Runs one bounded wait that nothing completes (see include/herald.h)."""
     _check(lib().herald_selftest_wait_timeout(int(limit_ns), _p(ws), _s(stream)))
+
+
+def herald_select_stage2_gather(d, q_block, k_cache, v_cache, ctx_len, cand, n_cand, C, K, sink,
+                                local, P_max, idx, n_sel, pool_k, pool_v, ws=None,
+                                ws_bytes=None, stream=None):
+    _check(lib().herald_select_stage2_gather(d, _p(q_block), _p(k_cache), _p(v_cache),
+                                             _p(ctx_len), _p(cand), _p(n_cand), int(C), int(K),
+                                             int(sink), int(local), int(P_max), _p(idx),
+                                             _p(n_sel), _p(pool_k), _p(pool_v), _p(ws),
+                                             _nbytes(ws, ws_bytes), _s(stream)))
 
 
 def herald_gather(d, idx, n_sel, P_max, k_cache, v_cache, pool_k, pool_v, stream=None):

@@ -9,8 +9,8 @@ candidates with the next block's real queries.
 Per block i (one layer), with `den` the denoising stream and `sel` the
 selection stream:
 
-    den: stage 2 (cand[i%2], block i's first-step queries) -> idx, n_sel
-    den: gather -> pool[i%2]
+    den: stage 2 (cand[i%2], block i's first-step queries) -> idx, n_sel,
+         with the gather -> pool[i%2] (herald_select_stage2_gather)
     sel: stage 1 for block i+1 from block i's first-step queries
          -> cand[(i+1)%2]                         (overlaps the T steps below)
     den: T-1 x sparse block attention over pool[i%2] (steps after the first
@@ -188,9 +188,10 @@ class BlockPipeline:
         wd, wb = self._ws_den, self.ws_bytes
         # stage 1 for block i+1 can start now: block i's queries exist
         sel.wait_stream(den)
-        chk(L.herald_select_stage2(d, q0, kc, cx, self._cand[cur], self._n_cand[cur], self.C,
-                                   self.K, self.S, self.W, P, self._idx, self._n_sel, wd, wb, hd))
-        chk(L.herald_gather(d, self._idx, self._n_sel, P, kc, vc, pk, pv, hd))
+        # stage 2 and the gather into pool[i%2] (one step for a device cache)
+        chk(L.herald_select_stage2_gather(d, q0, kc, vc, cx, self._cand[cur], self._n_cand[cur],
+                                          self.C, self.K, self.S, self.W, P, self._idx,
+                                          self._n_sel, pk, pv, wd, wb, hd))
         chk(L.herald_select_stage1(d, q0, H.ptr(nk), cx, self.C, self._cand[nxt],
                                    self._n_cand[nxt], self._ws_sel, wb,
                                    self._scan_sms(nk) if overlap else 0, hs if overlap else hd))
@@ -291,12 +292,12 @@ class StackPipeline:
         for t in range(self.T):
             for l in range(self.nl):
                 if t == 0:
-                    H.herald_select_stage2(d, q_steps[l][0], k_caches[l], ctx,
-                                           self.cand[l][cur], self.n_cand[l][cur], self.C,
-                                           self.K, self.S, self.W, P, self.idx[l],
-                                           self.n_sel[l], self.ws_den, self.ws_bytes, den)
-                    H.herald_gather(d, self.idx[l], self.n_sel[l], P, k_caches[l], v_caches[l],
-                                    self.pool_k[l][cur], self.pool_v[l][cur], den)
+                    H.herald_select_stage2_gather(d, q_steps[l][0], k_caches[l], v_caches[l],
+                                                  ctx, self.cand[l][cur], self.n_cand[l][cur],
+                                                  self.C, self.K, self.S, self.W, P,
+                                                  self.idx[l], self.n_sel[l],
+                                                  self.pool_k[l][cur], self.pool_v[l][cur],
+                                                  self.ws_den, self.ws_bytes, den)
                 if fuse and t == self.T - 1 and l == 0 and overlap:
                     den.wait_stream(sel)  # stage 1 reads the caches the last step appends to
                 flags = step_flags(t, self.T, advance and l == self.nl - 1) if fuse else \

@@ -119,6 +119,23 @@ herald_status herald_select_stage2(herald_dims dims, const uint16_t *q_block,
                                    int sink, int local, int P_max, int32_t *idx,
                                    int32_t *n_sel, void *ws, size_t ws_bytes, void *stream);
 
+/* herald_select_stage2 followed by herald_gather, in one step where the
+ * cache is in device memory: several top-K CTAs per (sequence, KV head)
+ * make the same (deterministic) selection and each copies one slice of the
+ * selected rows into the pool, so the gather needs no launch of its own
+ * ([EA]: the pool is filled once per block).  Outputs: idx, n_sel as from
+ * herald_select_stage2 and pool_k, pool_v as from herald_gather, bit for
+ * bit.  A cache in mapped pinned host memory gets the two calls.
+ *   v_cache   [N][Hkv][L_max][d] bf16, the same placement as k_cache.
+ *   pool_k/v  [N][Hkv][P_max][d] bf16 device out. */
+herald_status herald_select_stage2_gather(herald_dims dims, const uint16_t *q_block,
+                                          const uint16_t *k_cache, const uint16_t *v_cache,
+                                          const int32_t *ctx_len, const int32_t *cand,
+                                          const int32_t *n_cand, int C, int K, int sink,
+                                          int local, int P_max, int32_t *idx, int32_t *n_sel,
+                                          uint16_t *pool_k, uint16_t *pool_v, void *ws,
+                                          size_t ws_bytes, void *stream);
+
 /* Both stages in order (candidates kept in the workspace).  Passing
  * q_merge == q_block is the non-speculative case. */
 herald_status herald_select(herald_dims dims, const uint16_t *q_merge, const uint16_t *q_block,

@@ -224,6 +224,36 @@ def test_gather_and_attention(w):
     assert r.error_word() == 0
 
 
+MANY_PAIRS = [  # >= 16 (sequence, KV head) pairs: the gather rides with the top-K
+    _case("pairs16-d128", N=4, Hq=16, Hkv=4, d=128, L=2000, B=16, C=256, K=64, S=8, W=32,
+          n_planted=4, index=41),
+    _case("pairs16-d64-ragged", N=8, Hq=6, Hkv=2, d=64, L=900, B=20, C=300, K=100, S=4, W=21,
+          n_planted=4, index=42),
+]
+
+
+@pytest.mark.parametrize("w", CASES + MANY_PAIRS + [QWEN_32K], ids=lambda w: w.name)
+def test_stage2_with_gather_equals_stage2_then_gather(w):
+    """herald_select_stage2_gather writes the same idx, n_sel and pool bits
+    as herald_select_stage2 followed by herald_gather: with many (sequence,
+    KV head) pairs the gather runs inside the top-K, split over several CTAs
+    per pair; with few, the two kernels run in turn."""
+    r = Run(w)
+    r.stage1()
+    r.stage2()
+    r.gather()
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in (r.idx, r.n_sel, r.pool_k, r.pool_v)]
+    for t in (r.idx, r.n_sel, r.pool_k, r.pool_v):
+        t.fill_(7)
+    H.herald_select_stage2_gather(r.d, r.q_steps[0], r.k, r.v, r.ctx, r.cand, r.n_cand, w.C, w.K,
+                                  w.S, w.W, r.P, r.idx, r.n_sel, r.pool_k, r.pool_v, r.ws)
+    torch.cuda.synchronize()
+    assert r.error_word() == 0
+    for got, want in zip((r.idx, r.n_sel, r.pool_k, r.pool_v), ref):
+        assert torch.equal(got, want)
+
+
 def test_dense_equals_sparse_when_budget_covers_context():
     w = _case("dense", Hq=8, Hkv=2, d=128, L=600, B=16, C=600, K=600, S=0, W=0,
               n_planted=3, index=17)
@@ -370,6 +400,16 @@ def test_host_resident_cache_matches_device_cache(w):
     H.herald_select(r.d, r.q_merge, r.q_steps[0], kh, r.ctx, w_.C, w_.K, w_.S, w_.W, r.P, r.idx,
                     r.n_sel, r.ws)
     H.herald_gather(r.d, r.idx, r.n_sel, r.P, kh, vh, r.pool_k, r.pool_v)
+    torch.cuda.synchronize()
+    assert r.error_word() == 0
+    assert torch.equal(idx_dev, r.idx) and torch.equal(ns_dev, r.n_sel)
+    assert torch.equal(pk_dev, r.pool_k)
+    # the combined stage 2 + gather on the host-resident cache (two kernels
+    # there) from the same stage-1 candidates
+    H.herald_select_stage1(r.d, r.q_merge, kh, r.ctx, w_.C, r.cand, r.n_cand, r.ws)
+    r.pool_k.fill_(7)
+    H.herald_select_stage2_gather(r.d, r.q_steps[0], kh, vh, r.ctx, r.cand, r.n_cand, w_.C, w_.K,
+                                  w_.S, w_.W, r.P, r.idx, r.n_sel, r.pool_k, r.pool_v, r.ws)
     torch.cuda.synchronize()
     assert r.error_word() == 0
     assert torch.equal(idx_dev, r.idx) and torch.equal(ns_dev, r.n_sel)
