@@ -4,18 +4,20 @@ One step = one block of one layer of the 32K Qwen2.5-7B-like workload
 (N=1, Hq=28, Hkv=4, d=128, ctx 32768, B=32, T=8, C=4096, K=1024, sink 64,
 local 256) through the dual-stream block pipeline: stage 2 (refine + top-K
 with sink/local) -> gather into one of two pool buffers -> T x sparse
-block attention -> append, on the denoising stream, while stage 1
-(merged-query scan + top-C) for the next block runs on the selection
-stream.  Metric: block tokens/s = N*B / (time per step).  The same step
-without the overlap is reported as `serial`.
+block attention, the last step appending the block, on the denoising
+stream, while stage 1 (merged-query scan + top-C) for the next block runs
+on the selection stream.  Metric: block tokens/s = N*B / (time per step).
+The same step without the overlap is reported as `serial`.
 
-Timing: the step is captured once per cache copy into a CUDA graph and the
-graphs are replayed; the K cache and V cache are rotated over enough copies
-that the data touched between two uses of a copy exceeds L2 (cold-L2
-inputs).  A second, traced replay brackets every kernel with graph event
-nodes to time the dominant kernel for the roofline.  e2e: the same step
-through direct C-ABI calls with the step's inputs copied from pinned host
-buffers and its outputs read back, copies inside the timed region.
+Timing: consecutive steps are captured into CUDA graphs (up to 8 blocks
+per graph, the count dividing the number of timed steps; one per graph for
+the layer stack) and the graphs are replayed; the K cache and V cache are
+rotated over enough copies that the data touched between two uses of a
+copy exceeds L2 (cold-L2 inputs).  A second, traced replay brackets every
+kernel with graph event nodes to time the dominant kernel for the
+roofline.  e2e: the same step through the pipeline's public call (one
+graph per block) with the step's inputs copied from pinned host buffers
+and its outputs read back, copies inside the timed region.
 `--impl reference`: the fp64 CPU oracle timed on the host cores.
 """
 from __future__ import annotations
@@ -253,6 +255,16 @@ class Bench:
                         self.out if out is None else out, next_k_cache=self.k[nxt],
                         advance=False, overlap=self.overlap, graph=graph)
 
+    def capture_chunk(self, start: int, g: int):
+        """One CUDA graph of g consecutive blocks (cache copies start, start+1,
+        ... modulo the rotation), captured after capture()'s eager warm-up."""
+        torch = self.torch
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for t in range(g):
+                self.step((start + t) % self.n_rot)
+        return graph
+
     def capture(self, traced: bool = False):
         torch = self.torch
         graphs, traces = [], []
@@ -487,6 +499,57 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def blocks_per_graph(b, steps: int) -> int:
+    """Consecutive blocks held by one timed CUDA graph: for a single layer the
+    largest divisor of the step count up to 8: inside a graph one block's
+    last kernel hands over to the next block's first like the kernels inside
+    a block do, where a graph launch per block cost 7.5 us more per block on
+    the 32K layer (86.9 against 90.6 us with two blocks per graph); 1 for the
+    stack, whose step is 28 layers long and resets the context between
+    groups of blocks from the host."""
+    if isinstance(b, StackBench):
+        return 1
+    return max(g for g in range(1, 9) if steps % g == 0)
+
+
+def time_blocks(b, args, st, dist, graphs):
+    """Warm-up blocks, then exactly args.steps blocks between two CUDA
+    events on `st`; block i uses cache copy i % n_rot.  Per-block graphs
+    (`graphs`) or chunk graphs of blocks_per_graph consecutive blocks (the
+    warm-up then rounded up to whole chunks).  Returns (ms per block, g, and
+    the host clock at the start and end of the timed region)."""
+    torch = b.torch
+    g = blocks_per_graph(b, args.steps)
+    nw = -(-args.warmup // g) * g
+    chunks = {}
+    run = []
+    for i in range(0, nw + args.steps, g):
+        if g == 1:
+            run.append((i, graphs[i % b.n_rot]))
+            continue
+        start = i % b.n_rot
+        if start not in chunks:
+            chunks[start] = b.capture_chunk(start, g)
+        run.append((i, chunks[start]))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i, graph in run:
+        if i == nw:
+            torch.cuda.synchronize()
+            if dist:
+                dist.barrier()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            e0.record(st)
+        if g == 1:
+            b.before_step(i)
+        graph.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    return e0.elapsed_time(e1) / args.steps, g, t0, t1
+
+
 def run_ours(args, rank, world, dist):
     import torch
     w = workload()
@@ -495,46 +558,22 @@ def run_ours(args, rank, world, dist):
     b = StackBench(w, rank) if w.layers > 1 else Bench(w, rank)
     graphs, _ = b.capture(traced=False)
     nrot = b.n_rot
+    st = torch.cuda.current_stream()
     clocks = ClockSampler(dev_idx)
     clocks.start()
-    st = torch.cuda.current_stream()
-    for i in range(args.warmup):
-        b.before_step(i)
-        graphs[i % nrot].replay()
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    e0.record(st)
-    for i in range(args.steps):
-        b.before_step(args.warmup + i)
-        graphs[(args.warmup + i) % nrot].replay()
-    e1.record(st)
-    torch.cuda.synchronize()
-    t1 = time.perf_counter()
+    ms, chunk, t0, t1 = time_blocks(b, args, st, dist, graphs)
     if dist:
         dist.barrier()
     clocks.stop()
-    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, "cuda")
+    ms = max_over_ranks(ms, dist, "cuda")
     value = job_value(ms, world, w.N * w.B)
     err = b.H.herald_workspace_error(b.ws)
 
     # the same step without the selection/denoise overlap, for reference
     b.overlap = False
     sgraphs, _ = b.capture(traced=False)
-    for i in range(args.warmup):
-        b.before_step(i)
-        sgraphs[i % nrot].replay()
-    torch.cuda.synchronize()
-    e0.record(st)
-    for i in range(args.steps):
-        b.before_step(args.warmup + i)
-        sgraphs[(args.warmup + i) % nrot].replay()
-    e1.record(st)
-    torch.cuda.synchronize()
-    serial_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, "cuda")
+    serial_ms = time_blocks(b, args, st, dist, sgraphs)[0]
+    serial_ms = max_over_ranks(serial_ms, dist, "cuda")
     b.overlap = True
     del sgraphs
 
@@ -614,7 +653,10 @@ def run_ours(args, rank, world, dist):
                        "local": w.W, "parallelism": f"replicas x{world}",
                        "layers": w.layers, "l2": b.l2_note(), "context": b.context_note(),
                        "selection": _SELECTION,
-                       "timing": "CUDA-graph replay of whole steps, CUDA events"},
+                       "timing": (f"CUDA-graph replay, {chunk} consecutive blocks per graph "
+                                  f"(one graph launch per {chunk} blocks), CUDA events"
+                                  if chunk > 1 else
+                                  "CUDA-graph replay of whole steps, CUDA events")},
             "roofline": roofline,
             "serial": {"ms_per_step": serial_ms, "value": job_value(serial_ms, world, w.N * w.B),
                        "what": "same step with stage 1 on the denoising stream (no overlap)"},
