@@ -553,7 +553,9 @@ herald_status herald_select_stage2(herald_dims dims, const uint16_t* q_block,
 // pairs: each then has a few top-K CTAs, one per slice of its pool.  With few
 // pairs the separate wide gather kernel measured faster (32K layer, 4 pairs:
 // 91.7 against 93.3 us per block at 8 copies, 101.5 at 16; 4 x 64K layer,
-// 32 pairs: 503.5 against 518.5 us at 4 copies, 505.6 at 8).
+// 32 pairs: 503.5 against 518.5 us at 4 copies, 505.6 at 8).  At least two
+// copies per pair (fewer than half as many pairs as SMs): one CTA gathering a
+// whole pool is not measured.
 constexpr int kFusedGatherMinSegs = 16;
 constexpr int kFusedGatherMaxCopies = 4;
 
@@ -583,8 +585,9 @@ herald_status herald_select_stage2_gather(herald_dims dims, const uint16_t* q_bl
   HERALD_RET_IF(check_ws(dims, C, P_max, ws, ws_bytes, &w));
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int segs = dims.N * dims.Hkv;
-  if (segs >= kFusedGatherMinSegs && is_device_memory(k_cache) && is_device_memory(v_cache)) {
-    int copies = std::max(1, std::min(kFusedGatherMaxCopies, sm_count() / segs));
+  const int copies = std::min(kFusedGatherMaxCopies, sm_count() / segs);
+  if (segs >= kFusedGatherMinSegs && copies >= 2 && is_device_memory(k_cache) &&
+      is_device_memory(v_cache)) {
     const PoolGather pg{k_cache, v_cache, pool_k, pool_v, dims.d, copies};
     return run_stage2(dims, q_block, k_cache, ctx_len, cand, n_cand, C, K, sink, local, P_max,
                       idx, n_sel, ws, w, st, &pg);
