@@ -17,14 +17,16 @@ from block_diffusion_sparse_gb300.workloads import Workload
 from helpers import ATTN_ATOL, bf16_dev_to_f64, dev, f64
 
 
-@pytest.mark.parametrize("overlap,graph", [(True, False), (False, False), (True, True)])
-def test_three_blocks_match_oracle_schedule(overlap, graph):
+@pytest.mark.parametrize("overlap,graph,T", [(True, False, 2), (False, False, 2),
+                                             (True, True, 2), (True, False, 1)])
+def test_three_blocks_match_oracle_schedule(overlap, graph, T):
     """graph=True: every block's inputs are copied into the same buffers, so
-    block 2 replays the CUDA graph captured for block 0 (same parity)."""
+    block 2 replays the CUDA graph captured for block 0 (same parity).
+    T=1: the only denoising step also appends the block."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     nb = 3
-    w = Workload("pipe", N=2, Hq=8, Hkv=2, d=128, L=3000, B=16, T=2, C=256, K=128, S=16, W=64,
+    w = Workload("pipe", N=2, Hq=8, Hkv=2, d=128, L=3000, B=16, T=T, C=256, K=128, S=16, W=64,
                  planted="points", n_planted=10, index=31, extra_rows=nb * 16)
     x0 = synth.make_layer(w)
     blocks = [synth.make_layer(w.scaled(L=64, extra_rows=0, n_planted=0), layer=i + 1)
@@ -79,14 +81,16 @@ def test_three_blocks_match_oracle_schedule(overlap, graph):
                                    kc, vc)
 
 
-def test_two_layer_stack_matches_oracle_schedule():
+@pytest.mark.parametrize("T", [2, 1])
+def test_two_layer_stack_matches_oracle_schedule(T):
     """The stack pipeline runs the per-layer schedule above on every layer,
-    with one shared context length that advances once per block."""
+    with one shared context length that advances once per block (T=1: the
+    appends follow every layer's stage 1 instead of riding with the step)."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from block_diffusion_sparse_gb300.pipeline import StackPipeline
     nb, nl = 2, 2
-    w = Workload("stack", N=2, Hq=8, Hkv=2, d=128, L=2500, B=16, T=2, C=256, K=96, S=16, W=48,
+    w = Workload("stack", N=2, Hq=8, Hkv=2, d=128, L=2500, B=16, T=T, C=256, K=96, S=16, W=48,
                  planted="points", n_planted=10, index=37, extra_rows=nb * 16, layers=nl)
     x0 = [synth.make_layer(w, layer=l) for l in range(nl)]
     blocks = [[synth.make_layer(w.scaled(L=64, extra_rows=0, n_planted=0), layer=10 + 2 * i + l)
