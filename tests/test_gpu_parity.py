@@ -339,6 +339,31 @@ def test_append_matches_oracle_bit_exact():
     np.testing.assert_array_equal(vv, v2)
 
 
+def test_append_with_the_split_attention():
+    """A pool too large for the pool kernel (the cluster/split attention
+    kernels) appends through the append kernel after the step: the same
+    cache rows, lengths and attention output."""
+    w = _case("append-split", N=2, Hq=8, Hkv=2, d=128, L=3000, B=16, C=2600, K=2300, S=16,
+              W=64, extra_rows=40, index=43)
+    r = Run(w, ctx=[3000, 3030])
+    r.select()
+    r.gather()
+    t = w.T - 1
+    r.attn(t)
+    torch.cuda.synchronize()
+    out_plain = r.out.clone()
+    r.out.zero_()
+    r.attn(t, flags=H.HERALD_ATTN_SETTLED | H.HERALD_ATTN_APPEND | H.HERALD_ATTN_ADVANCE)
+    torch.cuda.synchronize()
+    assert r.error_word() == 0
+    assert torch.equal(r.out, out_plain)
+    _, k2, v2 = oracle.append(r.x["ctx"], f64(r.x["block_k"][t]), f64(r.x["block_v"][t]),
+                              f64(r.x["k_cache"]), f64(r.x["v_cache"]))
+    assert r.ctx.cpu().numpy().tolist() == [3016, 3040]  # L_max = 3040 caps the second
+    np.testing.assert_array_equal(synth.bf16_to_f64(r.k.cpu().numpy().view(np.uint16)), k2)
+    np.testing.assert_array_equal(synth.bf16_to_f64(r.v.cpu().numpy().view(np.uint16)), v2)
+
+
 @pytest.mark.parametrize("advance", [True, False])
 @pytest.mark.parametrize("placement", ["device", "host"])
 def test_last_step_appends_like_append_kv(placement, advance):
