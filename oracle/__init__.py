@@ -157,6 +157,58 @@ def select_exact(q_block, k_cache, ctx, K, S, W, P=None):
     return dict(cand=cand, n_cand=n_cand, s=s, idx=idx, n_sel=n_sel)
 
 
+def pooled_keys(k_cache, ctx, Bk):
+    """Block-granular stage 1, the compressed keys (SparDA summary, Method
+    section: InfLLM-V2 selects whole blocks of the context next to the
+    initial tokens and the local window): key block b of (n, g) is the mean
+    of cache rows [b*Bk, min((b+1)*Bk, ctx)) -- the last block below ctx may
+    be partial -- and blocks at or past ctx are zero.  Returns
+    (kp [N, Hkv, ceil(L_max/Bk), d], ctx_b [N] = ceil(ctx/Bk))."""
+    k = _f64(k_cache)
+    N, Hkv, L_max, d = k.shape
+    nb_max = -(-L_max // Bk)
+    kp = np.zeros((N, Hkv, nb_max, d))
+    ctx_b = np.zeros(N, np.int32)
+    for n in range(N):
+        L = int(min(max(int(ctx[n]), 0), L_max))
+        ctx_b[n] = -(-L // Bk)
+        for b in range(ctx_b[n]):
+            kp[n, :, b] = k[n, :, b * Bk: min((b + 1) * Bk, L)].mean(axis=1)
+    return kp, ctx_b
+
+
+def expand_blocks(cand_b, n_cand_b, ctx, Bk):
+    """Candidate positions of the selected blocks: every position below ctx
+    of each block in cand_b, ascending (blocks ascending), in rows of
+    C_blocks*Bk slots padded with -1.  Returns (cand, n_cand)."""
+    cb = np.asarray(cand_b)
+    N, Hkv, Cb = cb.shape
+    cand = np.full((N, Hkv, Cb * Bk), -1, np.int32)
+    n_cand = np.zeros((N, Hkv), np.int32)
+    for n in range(N):
+        L = int(ctx[n])
+        for g in range(Hkv):
+            pos = [j for b in cb[n, g, : int(n_cand_b[n, g])]
+                   for j in range(int(b) * Bk, min((int(b) + 1) * Bk, L))]
+            cand[n, g, : len(pos)] = pos
+            n_cand[n, g] = len(pos)
+    return cand, n_cand
+
+
+def stage1_blocks(qbar, k_cache, ctx, Bk, C_blocks):
+    """Block-granular stage 1: the stage-1 rule (steps 2-3) with the pooled
+    block keys in place of the keys -- s1b[b] = sum over the group's heads of
+    softmax over the blocks of qbar_h . kp_b / sqrt(d) -- then the top
+    C_blocks blocks expanded to their positions.  Returns a dict with the
+    pooled keys, block scores, selected blocks and the candidates."""
+    kp, ctx_b = pooled_keys(k_cache, ctx, Bk)
+    l1b, lse1b, s1b = stage1_scores(qbar, kp, ctx_b)
+    cand_b, n_cand_b = topc(s1b, ctx_b, C_blocks)
+    cand, n_cand = expand_blocks(cand_b, n_cand_b, np.asarray(ctx), Bk)
+    return dict(kp=kp, ctx_b=ctx_b, l1b=l1b, s1b=s1b, cand_b=cand_b, n_cand_b=n_cand_b,
+                cand=cand, n_cand=n_cand)
+
+
 def sparse_attn(q, k_cache, v_cache, idx, n_sel, block_k, block_v, scale=None,
                 with_wsum=False):
     """Step 6: out [N,B,Hq,d] over the selected rows plus the B block keys."""

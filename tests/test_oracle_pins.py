@@ -381,3 +381,64 @@ def test_exact_scores_sum_to_rows_and_ignore_positions_past_the_context():
     k2 = k.copy()
     k2[1, :, 40:] += 5.0
     np.testing.assert_array_equal(oracle.exact_scores(q, k2, ctx)[2][1, :, :31], s[1, :, :31])
+
+
+# --------------------------------------------------------------------------
+# block-granular stage 1 (pooled block keys)
+
+def test_block_stage1_with_one_key_per_block_is_stage1():
+    """Bk = 1: every block is one key, so the block-granular stage 1 selects
+    exactly what the (separately pinned) per-key stage 1 selects."""
+    rng = np.random.default_rng(80)
+    N, Hq, Hkv, d, L_max = 2, 6, 2, 16, 90
+    qbar = _rand(rng, (N, Hq, d))
+    k = _rand(rng, (N, Hkv, L_max, d))
+    ctx = np.array([90, 57], np.int32)
+    r = oracle.stage1_blocks(qbar, k, ctx, 1, 20)
+    _, _, s1 = oracle.stage1_scores(qbar, k, ctx)
+    cand, nc = oracle.topc(s1, ctx, 20)
+    np.testing.assert_array_equal(r["cand"][..., :20], cand)
+    np.testing.assert_array_equal(r["n_cand"], nc)
+
+
+def test_block_logit_is_the_mean_of_its_keys_logits():
+    """q . mean(k) = mean(q . k): a block's stage-1 logit is the mean of the
+    per-key logits of its (valid) keys, the last block partial."""
+    rng = np.random.default_rng(81)
+    N, Hq, Hkv, d, L_max, Bk = 1, 4, 2, 8, 100, 16
+    qbar = _rand(rng, (N, Hq, d))
+    k = _rand(rng, (N, Hkv, L_max, d))
+    ctx = np.array([75], np.int32)                    # 4 full blocks + 11 keys
+    r = oracle.stage1_blocks(qbar, k, ctx, Bk, 3)
+    l1, _, _ = oracle.stage1_scores(qbar, k, ctx)
+    assert r["ctx_b"].tolist() == [5]
+    for h in range(Hq):
+        for b in range(5):
+            want = l1[0, h, b * Bk: min((b + 1) * Bk, 75)].mean()
+            assert abs(r["l1b"][0, h, b] - want) < 1e-12
+    assert np.all(r["kp"][0, :, 5:] == 0)             # blocks past the context
+
+
+def test_block_candidates_expand_whole_blocks_ascending():
+    """The candidates are exactly the positions below ctx of the selected
+    blocks, ascending; a block holding planted heavy keys is selected."""
+    rng = np.random.default_rng(82)
+    N, Hq, Hkv, d, L_max, Bk = 1, 4, 2, 32, 300, 32
+    qbar = _rand(rng, (N, Hq, d))
+    k = _rand(rng, (N, Hkv, L_max, d))
+    ctx = np.array([270], np.int32)                   # blocks 0..8, the last with 14 keys
+    for g in range(Hkv):                              # block 5 aligned with the group's queries
+        q_g = qbar[0, g * 2:(g + 1) * 2].mean(axis=0)
+        k[0, g, 5 * Bk:6 * Bk] = 3.0 * q_g + 0.1 * _rand(rng, (Bk, d))
+    r = oracle.stage1_blocks(qbar, k, ctx, Bk, 3)
+    for g in range(Hkv):
+        blocks = r["cand_b"][0, g, : r["n_cand_b"][0, g]].tolist()
+        assert 5 in blocks and blocks == sorted(blocks)
+        want = [j for b in blocks for j in range(b * Bk, min((b + 1) * Bk, 270))]
+        got = r["cand"][0, g, : r["n_cand"][0, g]].tolist()
+        assert got == want and len(set(got)) == len(got)
+        assert np.all(r["cand"][0, g, r["n_cand"][0, g]:] == -1)
+    # every block selected when C_blocks covers the context
+    r = oracle.stage1_blocks(qbar, k, ctx, Bk, 16)
+    assert r["n_cand"].tolist() == [[270, 270]]
+    assert (r["cand"][0, :, :270] == np.arange(270)).all()
