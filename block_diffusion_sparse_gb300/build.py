@@ -17,6 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libherald.so")
 SOURCES = ["herald_api.cu", "select_kernels.cu", "tc_kernels.cu", "move_kernels.cu",
+           "block_select.cu",
            "herald_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

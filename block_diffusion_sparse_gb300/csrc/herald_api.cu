@@ -526,6 +526,71 @@ herald_status herald_select_stage1(herald_dims dims, const uint16_t* q_merge,
                     static_cast<cudaStream_t>(stream));
 }
 
+herald_status herald_pool_keys(herald_dims dims, const uint16_t* k_cache,
+                               const int32_t* ctx_len, int Bk, int n_tail, float* pooled,
+                               void* stream) {
+  g_err[0] = 0;
+  HERALD_RET_IF(check_dims(dims));
+  if (Bk < 1 || Bk > dims.L_max) return fail(HERALD_ERR_INVALID_ARG, "Bk=%d outside [1, L_max]", Bk);
+  if (n_tail < 0) return fail(HERALD_ERR_INVALID_ARG, "n_tail=%d must be >= 0", n_tail);
+  HERALD_CHECK_PTR(k_cache);
+  HERALD_CHECK_PTR(ctx_len);
+  HERALD_CHECK_PTR(pooled);
+  HERALD_TRY_CUDA(launch_pool_keys(dims, k_cache, ctx_len, Bk, n_tail, pooled,
+                                   static_cast<cudaStream_t>(stream)),
+                  "pool_keys launch");
+  return HERALD_OK;
+}
+
+herald_status herald_select_stage1_blocks(herald_dims dims, const uint16_t* q_merge,
+                                          const float* pooled, const int32_t* ctx_len, int Bk,
+                                          int C_blocks, int32_t* cand, int32_t* n_cand, void* ws,
+                                          size_t ws_bytes, void* stream) {
+  g_err[0] = 0;
+  HERALD_RET_IF(check_dims(dims));
+  if (Bk < 1 || Bk > dims.L_max) return fail(HERALD_ERR_INVALID_ARG, "Bk=%d outside [1, L_max]", Bk);
+  if (C_blocks < 1 || (long long)C_blocks * Bk > kMaxC)
+    return fail(HERALD_ERR_UNSUPPORTED_SHAPE, "C_blocks*Bk=%lld outside [1, %d]",
+                (long long)C_blocks * Bk, kMaxC);
+  HERALD_CHECK_PTR(q_merge);
+  HERALD_CHECK_PTR(pooled);
+  HERALD_CHECK_PTR(ctx_len);
+  HERALD_CHECK_PTR(cand);
+  HERALD_CHECK_PTR(n_cand);
+  // the selection runs over the blocks: the per-key stage 1's workspace
+  // layout for a cache of ceil(L_max/Bk) rows and C_blocks candidates
+  herald_dims bd = dims;
+  bd.L_max = cdiv(dims.L_max, Bk);
+  WsLayout w;
+  HERALD_RET_IF(check_ws(bd, C_blocks, 1, ws, ws_bytes, &w));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int chunks = block_scan_chunks(bd, sm_count());
+  const int part_slots = chunks * 4;
+  float* qbar = at<float>(ws, w.qbar);
+  float2* part1 = at<float2>(ws, w.part1);
+  uint32_t* hist = at<uint32_t>(ws, w.hist);
+  int32_t* cand_b = at<int32_t>(ws, w.cand);
+  int32_t* n_cand_b = at<int32_t>(ws, w.n_cand);
+  // block counts ceil(ctx/Bk), written by the block scan, read by the rest
+  int32_t* ctx_b = at<int32_t>(ws, w.s2);
+  HERALD_TRY_CUDA(launch_merge_query(dims, q_merge, qbar, at<uint16_t>(ws, w.qhl), hist, part1,
+                                     part_slots, st),
+                  "merge_query launch");
+  HERALD_TRY_CUDA(launch_block_scan(dims, pooled, qbar, ctx_len, Bk, w.L_pad,
+                                    at<float>(ws, w.logits), part1, ctx_b, chunks, st),
+                  "block_scan launch");
+  HERALD_TRY_CUDA(launch_s1_hist(bd, at<float>(ws, w.logits), part1, part_slots, ctx_b,
+                                 at<float>(ws, w.s1), hist, w, sm_count(), st),
+                  "s1_hist launch");
+  HERALD_TRY_CUDA(launch_topc(bd, at<float>(ws, w.s1), hist, ctx_b, C_blocks, cand_b, n_cand_b,
+                              w, st),
+                  "topc launch");
+  HERALD_TRY_CUDA(launch_expand_blocks(dims, cand_b, n_cand_b, ctx_len, Bk, C_blocks, cand,
+                                       n_cand, st),
+                  "expand launch");
+  return HERALD_OK;
+}
+
 herald_status herald_select_stage2(herald_dims dims, const uint16_t* q_block,
                                    const uint16_t* k_cache, const int32_t* ctx_len,
                                    const int32_t* cand, const int32_t* n_cand, int C, int K,

@@ -214,6 +214,16 @@ cudaError_t launch_wait_timeout(uint64_t limit_ns, uint32_t* err, cudaStream_t s
 cudaError_t launch_append(const herald_dims& dm, const uint16_t* block_k, const uint16_t* block_v,
                           int32_t* ctx, uint16_t* k_cache, uint16_t* v_cache, int advance,
                           cudaStream_t st);
+// block-granular stage 1 (block_select.cu)
+cudaError_t launch_pool_keys(const herald_dims& dm, const uint16_t* k_cache, const int32_t* ctx,
+                             int Bk, int n_tail, float* pooled, cudaStream_t st);
+int block_scan_chunks(const herald_dims& dm, int num_sms);
+cudaError_t launch_block_scan(const herald_dims& dm, const float* pooled, const float* qbar,
+                              const int32_t* ctx, int Bk, int L_pad, float* logits,
+                              float2* part1, int32_t* ctx_b, int chunks, cudaStream_t st);
+cudaError_t launch_expand_blocks(const herald_dims& dm, const int32_t* cand_b,
+                                 const int32_t* n_cand_b, const int32_t* ctx, int Bk,
+                                 int C_blocks, int32_t* cand, int32_t* n_cand, cudaStream_t st);
 
 // The append of a decoded block, done inside another kernel: the rows of
 // block[n][b][g] (bf16, [N][B][Hkv][d]) go to cache[n][g][L0 + b], rows at or

@@ -25,7 +25,8 @@ EXPORTS = ("herald_workspace_size", "herald_status_string", "herald_last_error",
            "herald_denoise_attn", "herald_denoise_attn_ex", "herald_append_kv",
            "herald_trace_begin", "herald_trace_end", "herald_trace_name",
            "herald_select_stage2_noalloc", "herald_selftest_wait_timeout",
-           "herald_workspace_size_exact", "herald_select_exact")
+           "herald_workspace_size_exact", "herald_select_exact", "herald_pool_keys",
+           "herald_select_stage1_blocks")
 
 
 class HeraldError(RuntimeError):
@@ -92,6 +93,9 @@ def lib() -> C.CDLL:
         L.herald_workspace_size_exact.restype = sz
         L.herald_select_exact.argtypes = [Dims, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, sz,
                                           vp]
+        L.herald_pool_keys.argtypes = [Dims, vp, vp, i32, i32, vp, vp]
+        L.herald_select_stage1_blocks.argtypes = [Dims, vp, vp, vp, i32, i32, vp, vp, vp, sz,
+                                                  vp]
         L.herald_trace_begin.argtypes = [C.POINTER(vp), i32, i32]
         L.herald_trace_end.argtypes = []
         L.herald_trace_name.argtypes = [i32]
@@ -235,6 +239,18 @@ def herald_select_stage2_gather(d, q_block, k_cache, v_cache, ctx_len, cand, n_c
                                              _p(ctx_len), _p(cand), _p(n_cand), int(C), int(K),
                                              int(sink), int(local), int(P_max), _p(idx),
                                              _p(n_sel), _p(pool_k), _p(pool_v), _p(ws),
+                                             _nbytes(ws, ws_bytes), _s(stream)))
+
+
+def herald_pool_keys(d, k_cache, ctx_len, Bk, pooled, n_tail=0, stream=None):
+    _check(lib().herald_pool_keys(d, _p(k_cache), _p(ctx_len), int(Bk), int(n_tail), _p(pooled),
+                                  _s(stream)))
+
+
+def herald_select_stage1_blocks(d, q_merge, pooled, ctx_len, Bk, C_blocks, cand, n_cand,
+                                ws=None, ws_bytes=None, stream=None):
+    _check(lib().herald_select_stage1_blocks(d, _p(q_merge), _p(pooled), _p(ctx_len), int(Bk),
+                                             int(C_blocks), _p(cand), _p(n_cand), _p(ws),
                                              _nbytes(ws, ws_bytes), _s(stream)))
 
 

@@ -103,6 +103,34 @@ herald_status herald_select_stage1(herald_dims dims, const uint16_t *q_merge,
                                    int32_t *cand, int32_t *n_cand, void *ws, size_t ws_bytes,
                                    int sm_budget, void *stream);
 
+/* Block-granular stage 1 ([SPD]: InfLLM-V2 selects whole blocks of the
+ * context; here stage 1's rule is applied to blocks, not keys).  The cache is
+ * summarised by its block means -- the "compressed keys" --
+ *   pooled[n][g][b] = mean of k_cache[n][g][j] over j in [b*Bk, min((b+1)*Bk,
+ *   ctx_len[n])),  fp32 [N][Hkv][ceil(L_max/Bk)][d] device,
+ * zero for blocks at or past ctx_len[n].  herald_pool_keys builds it
+ * (n_tail = 0: every block) or refreshes the last n_tail blocks below
+ * ctx_len of each sequence (after an append grew the cache: ceil(B/Bk) + 1
+ * blocks cover the ones it touched).  k_cache may be mapped pinned host
+ * memory.  Bk in [1, L_max], n_tail >= 0. */
+herald_status herald_pool_keys(herald_dims dims, const uint16_t *k_cache,
+                               const int32_t *ctx_len, int Bk, int n_tail, float *pooled,
+                               void *stream);
+
+/* Stage 1 over the blocks: s1b[b] = sum over the group's heads of softmax
+ * over the blocks below ceil(ctx/Bk) of qbar_h . pooled_b / sqrt(d) (qbar as
+ * in herald_select_stage1); the C_blocks best blocks (lowest index on ties)
+ * are expanded to their positions below ctx_len.
+ *   cand   [N][Hkv][C_blocks*Bk] int32 device out, ascending, -1 padded
+ *   n_cand [N][Hkv] int32 device out
+ * 1 <= C_blocks*Bk <= 16384.  ws: herald_workspace_size(dims, C_blocks*Bk,
+ * P_max) bytes (the workspace stage 2 uses) are enough.  The candidates
+ * feed herald_select_stage2 with C = C_blocks*Bk. */
+herald_status herald_select_stage1_blocks(herald_dims dims, const uint16_t *q_merge,
+                                          const float *pooled, const int32_t *ctx_len, int Bk,
+                                          int C_blocks, int32_t *cand, int32_t *n_cand,
+                                          void *ws, size_t ws_bytes, void *stream);
+
 /* Stage 2 of the selection [V3] plus sink/local [SPD InfLLM-V2 decomposition].
  *   q_block [N][B][Hq][d] bf16 device: the real queries of the block being
  *           selected for.

@@ -601,3 +601,68 @@ def test_exact_selection_workspace_checks():
     with pytest.raises(H.HeraldError) as e:
         H.herald_select_exact(d, idx, idx, ns, w.K, w.S, w.W, w.P, idx, ns, ws, need - 256)
     assert e.value.status == 3
+
+
+# --------------------------------------------------------------------------
+# block-granular stage 1
+
+BLOCK_CASES = [
+    _case("blocks-g7", Hq=14, Hkv=2, d=128, L=5000, B=32, C=512, K=200, S=8, W=40,
+          n_planted=20, index=44),
+    _case("blocks-n2-d64", N=2, Hq=8, Hkv=2, d=64, L=3001, B=16, C=256, K=100, S=4, W=33,
+          n_planted=10, index=45),
+]
+
+
+@pytest.mark.parametrize("Bk", [64, 16])
+@pytest.mark.parametrize("w", BLOCK_CASES, ids=lambda w: w.name)
+def test_block_stage1_matches_oracle(w, Bk):
+    """Pooled keys (fp32 block means) within fp32 rounding of the oracle's
+    fp64 means; the selected blocks equal the oracle's up to its tie band;
+    the candidates are exactly those blocks' positions below ctx."""
+    ctx = [w.L - 7] + [w.L - 100 * i for i in range(1, w.N)]  # ragged last blocks
+    r = Run(w, ctx=ctx)
+    x = r.x
+    nb_max = -(-w.L_max // Bk)
+    pooled = torch.full((w.N, w.Hkv, nb_max, w.d), 5.0, dtype=torch.float32, device="cuda")
+    H.herald_pool_keys(r.d, r.k, r.ctx, Bk, pooled)
+    C_blocks = w.C // Bk
+    cand = torch.full((w.N, w.Hkv, C_blocks * Bk), -7, dtype=torch.int32, device="cuda")
+    n_cand = torch.zeros((w.N, w.Hkv), dtype=torch.int32, device="cuda")
+    H.herald_select_stage1_blocks(r.d, r.q_merge, pooled, r.ctx, Bk, C_blocks, cand, n_cand,
+                                  r.ws)
+    torch.cuda.synchronize()
+    assert r.error_word() == 0
+    o = oracle.stage1_blocks(oracle.merged_query(f64(x["q_merge"])), f64(x["k_cache"]),
+                             x["ctx"], Bk, C_blocks)
+    np.testing.assert_allclose(pooled.cpu().numpy(), o["kp"], rtol=1e-5, atol=1e-6)
+    cand, n_cand = cand.cpu().numpy(), n_cand.cpu().numpy()
+    for n in range(w.N):
+        L = int(x["ctx"][n])
+        for g in range(w.Hkv):
+            m = int(o["n_cand_b"][n, g])
+            row = cand[n, g, : n_cand[n, g]]
+            blocks = sorted(set((row // Bk).tolist()))
+            assert_sets_within_band(blocks, o["cand_b"][n, g, :m], o["s1b"][n, g], m,
+                                    f"blocks n={n} g={g}")
+            want = [j for b in blocks for j in range(b * Bk, min((b + 1) * Bk, L))]
+            assert row.tolist() == want
+            assert (cand[n, g, n_cand[n, g]:] == -1).all()
+
+
+def test_pooled_keys_tail_refresh_after_appends():
+    """After appends grow the context, refreshing the last ceil(B/Bk) + 1
+    blocks gives the pooled keys a full rebuild gives."""
+    w = BLOCK_CASES[1]
+    Bk = 16
+    r = Run(w, ctx=[w.L - 40, w.L - 90])
+    nb_max = -(-w.L_max // Bk)
+    pooled = torch.zeros((w.N, w.Hkv, nb_max, w.d), dtype=torch.float32, device="cuda")
+    H.herald_pool_keys(r.d, r.k, r.ctx, Bk, pooled)
+    for t in range(2):  # two appends of B rows each
+        H.herald_append_kv(r.d, r.bk[t], r.bv[t], r.ctx, r.k, r.v, advance=True)
+        H.herald_pool_keys(r.d, r.k, r.ctx, Bk, pooled, n_tail=-(-w.B // Bk) + 1)
+    full = torch.zeros_like(pooled)
+    H.herald_pool_keys(r.d, r.k, r.ctx, Bk, full)
+    torch.cuda.synchronize()
+    assert torch.equal(pooled, full)
