@@ -135,6 +135,7 @@ WORKLOADS = {"qwen": "QWEN_32K", "tiny": "TINY", "llama": "LLAMA_64K",
              "long-host": "LONG_128K_HOST", "stack": "QWEN_STACK"}
 _WORKLOAD = "qwen"
 _SELECTION = "merged"
+BLOCK_KEYS = 64  # keys per block of the block-granular stage 1 (--selection blocks)
 
 
 def workload():
@@ -203,7 +204,8 @@ class Bench:
         self.ctx = torch.from_numpy(x["ctx"]).cuda()
         from block_diffusion_sparse_gb300.pipeline import BlockPipeline
         self.exact = _SELECTION == "exact"
-        self.pipe = BlockPipeline(self.d, w.C, w.K, w.S, w.W, self.P, w.T, exact=self.exact)
+        self.pipe = BlockPipeline(self.d, w.C, w.K, w.S, w.W, self.P, w.T, exact=self.exact,
+                                  blocks=BLOCK_KEYS if _SELECTION == "blocks" else 0)
         self.out = torch.zeros((w.T, w.N, w.B, w.Hq, w.d), dtype=torch.int16, device="cuda")
         self.overlap = True
         # stage 1 of the first block (its own queries; no predecessor)
@@ -442,8 +444,16 @@ def oracle_block(w, xf, T_sample=None):
     """One block through the fp64 oracle: select, then T attention steps."""
     import oracle
     T = w.T if T_sample is None else T_sample
-    r = oracle.select(xf["q_merge"], xf["q_steps"][0], xf["k_cache"], xf["ctx"], w.C, w.K, w.S,
-                      w.W, w.P)
+    if _SELECTION == "blocks":  # block-granular stage 1, then steps 4-5
+        qbar = oracle.merged_query(xf["q_merge"])
+        b = oracle.stage1_blocks(qbar, xf["k_cache"], xf["ctx"], BLOCK_KEYS, w.C // BLOCK_KEYS)
+        s2 = oracle.stage2_scores(xf["q_steps"][0], xf["k_cache"], b["cand"], b["n_cand"])
+        idx, n_sel = oracle.select_final(xf["ctx"], np.shape(xf["k_cache"])[2], b["cand"],
+                                         b["n_cand"], s2, w.K, w.S, w.W, w.P)
+        r = dict(idx=idx, n_sel=n_sel)
+    else:
+        r = oracle.select(xf["q_merge"], xf["q_steps"][0], xf["k_cache"], xf["ctx"], w.C, w.K,
+                          w.S, w.W, w.P)
     for t in range(T):
         oracle.sparse_attn(xf["q_steps"][t], xf["k_cache"], xf["v_cache"], r["idx"], r["n_sel"],
                            xf["block_k"][t], xf["block_v"][t])
@@ -824,9 +834,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="qwen", choices=sorted(WORKLOADS))
-    ap.add_argument("--selection", default="merged", choices=["merged", "exact"],
+    ap.add_argument("--selection", default="merged", choices=["merged", "exact", "blocks"],
                     help="merged: the two-stage selection (default); exact: every cached "
-                         "position scored with the block's real queries (one stream)")
+                         "position scored with the block's real queries (one stream); "
+                         "blocks: stage 1 over 64-key block means")
     args = ap.parse_args()
     global _WORKLOAD, _SELECTION
     _WORKLOAD = args.workload

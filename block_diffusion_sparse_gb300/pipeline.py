@@ -87,9 +87,18 @@ def step_flags(t: int, T: int, advance: bool) -> int:
 
 class BlockPipeline:
     def __init__(self, dims: H.Dims, C: int, K: int, S: int, W: int, P: int, T: int,
-                 den_stream=None, sel_stream=None, sel_sms=None, exact: bool = False):
+                 den_stream=None, sel_stream=None, sel_sms=None, exact: bool = False,
+                 blocks: int = 0):
+        """blocks > 0: stage 1 selects C // blocks blocks of `blocks` keys
+        over the cache's pooled block keys (herald_select_stage1_blocks),
+        which the pipeline builds for each cache it meets and refreshes at
+        the tail after every append."""
         import torch
         self.torch = torch
+        self.Bk = int(blocks)
+        if self.Bk and C % self.Bk:
+            raise ValueError(f"C={C} is not a multiple of the block size {self.Bk}")
+        self._pooled = {}  # cache address -> fp32 block means (blocks > 0)
         # SMs the overlapped stage-1 scan may occupy (0: all)
         # None: background_sms for the cache each block reads
         self.sel_sms = None if sel_sms is None else int(sel_sms)
@@ -131,10 +140,35 @@ class BlockPipeline:
     def _den(self):
         return self.den if self.den is not None else self.torch.cuda.current_stream()
 
+    def pooled(self, k_cache, ctx):
+        """The block keys of `k_cache` (built on first use, on the current
+        stream; refreshed by every block that appends to that cache)."""
+        key = H.ptr(k_cache)
+        t = self._pooled.get(key)
+        if t is None:
+            d = self.d
+            nb = -(-d.L_max // self.Bk)
+            t = self.torch.zeros((d.N, d.Hkv, nb, d.d), dtype=self.torch.float32, device="cuda")
+            H.herald_pool_keys(d, k_cache, ctx, self.Bk, t, stream=self._den())
+            self._pooled[key] = t
+        return t
+
+    def _stage1(self, q_merge, k_cache, ctx, slot, stream, sms=0):
+        """Stage 1 (per key, or over the pooled blocks) into cand[slot]."""
+        if self.Bk:
+            H.check(H.lib().herald_select_stage1_blocks(
+                self.d, H.ptr(q_merge), H.ptr(self.pooled(k_cache, ctx)), H.ptr(ctx), self.Bk,
+                self.C // self.Bk, self._cand[slot], self._n_cand[slot], self._ws_sel,
+                self.ws_bytes, H.stream_handle(stream)))
+        else:
+            H.check(H.lib().herald_select_stage1(
+                self.d, H.ptr(q_merge), H.ptr(k_cache), H.ptr(ctx), self.C, self._cand[slot],
+                self._n_cand[slot], self._ws_sel, self.ws_bytes, sms,
+                H.stream_handle(stream)))
+
     def prime(self, q_merge, k_cache, ctx, slot: int = 0):
         """Stage 1 for the first block (no predecessor: its own queries)."""
-        H.herald_select_stage1(self.d, q_merge, k_cache, ctx, self.C, self.cand[slot],
-                               self.n_cand[slot], self.ws_sel, self.ws_bytes, self._den())
+        self._stage1(q_merge, k_cache, ctx, slot, self._den())
 
     def block(self, i: int, q_steps, block_k, block_v, k_cache, v_cache, ctx, out,
               next_k_cache=None, advance: bool = True, overlap: bool = True,
@@ -192,15 +226,17 @@ class BlockPipeline:
         chk(L.herald_select_stage2_gather(d, q0, kc, vc, cx, self._cand[cur], self._n_cand[cur],
                                           self.C, self.K, self.S, self.W, P, self._idx,
                                           self._n_sel, pk, pv, wd, wb, hd))
-        chk(L.herald_select_stage1(d, q0, H.ptr(nk), cx, self.C, self._cand[nxt],
-                                   self._n_cand[nxt], self._ws_sel, wb,
-                                   self._scan_sms(nk) if overlap else 0, hs if overlap else hd))
+        self._stage1(q_steps, nk, ctx, nxt, sel if overlap else den,
+                     self._scan_sms(nk) if overlap else 0)
         for t in range(self.T):
             if t == self.T - 1 and overlap:
                 den.wait_stream(sel)  # stage 1 reads the cache the last step appends to
             chk(L.herald_denoise_attn_ex(d, q0 + t * qstep, pk, pv, self._n_sel, P,
                                          bk0 + t * bstep, bv0 + t * bstep, o0 + t * ostep, 0.0,
                                          step_flags(t, self.T, advance), cx, kc, vc, wd, wb, hd))
+        if self.Bk:  # the appended rows change the cache's last blocks
+            chk(L.herald_pool_keys(d, kc, cx, self.Bk, -(-d.B // self.Bk) + 1,
+                                   H.ptr(self.pooled(k_cache, ctx)), hd))
 
 
     def block_exact(self, i: int, q_steps, block_k, block_v, k_cache, v_cache, ctx, out,

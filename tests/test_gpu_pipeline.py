@@ -17,12 +17,14 @@ from block_diffusion_sparse_gb300.workloads import Workload
 from helpers import ATTN_ATOL, bf16_dev_to_f64, dev, f64
 
 
-@pytest.mark.parametrize("overlap,graph,T", [(True, False, 2), (False, False, 2),
-                                             (True, True, 2), (True, False, 1)])
-def test_three_blocks_match_oracle_schedule(overlap, graph, T):
+@pytest.mark.parametrize("overlap,graph,T,Bk", [(True, False, 2, 0), (False, False, 2, 0),
+                                                (True, True, 2, 0), (True, False, 1, 0),
+                                                (True, False, 2, 16), (True, True, 2, 32)])
+def test_three_blocks_match_oracle_schedule(overlap, graph, T, Bk):
     """graph=True: every block's inputs are copied into the same buffers, so
     block 2 replays the CUDA graph captured for block 0 (same parity).
-    T=1: the only denoising step also appends the block."""
+    T=1: the only denoising step also appends the block.  Bk > 0: stage 1
+    over the cache's pooled blocks of Bk keys, refreshed after each append."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     nb = 3
@@ -34,7 +36,7 @@ def test_three_blocks_match_oracle_schedule(overlap, graph, T):
     d = H.dims_of(w)
     k, v = dev(x0["k_cache"]), dev(x0["v_cache"])
     ctx = dev(x0["ctx"])
-    pipe = BlockPipeline(d, w.C, w.K, w.S, w.W, w.P, w.T)
+    pipe = BlockPipeline(d, w.C, w.K, w.S, w.W, w.P, w.T, blocks=Bk)
     pipe.prime(dev(x0["q_merge"]), k, ctx)
     got = []
     fixed = None
@@ -58,8 +60,14 @@ def test_three_blocks_match_oracle_schedule(overlap, graph, T):
     # oracle replay of the same schedule
     kc, vc = f64(x0["k_cache"]), f64(x0["v_cache"])
     cx = x0["ctx"].copy()
+    def stage1(qbar, kc, cx):
+        if Bk:
+            r = oracle.stage1_blocks(qbar, kc, cx, Bk, w.C // Bk)
+            return r["cand"], r["n_cand"]
+        return oracle.topc(oracle.stage1_scores(qbar, kc, cx)[2], cx, w.C)
+
     qbar = oracle.merged_query(f64(x0["q_merge"]))
-    cand, nc = oracle.topc(oracle.stage1_scores(qbar, kc, cx)[2], cx, w.C)
+    cand, nc = stage1(qbar, kc, cx)
     for i, xb in enumerate(blocks):
         q0 = f64(xb["q_steps"][0])
         s2 = oracle.stage2_scores(q0, kc, cand, nc)
@@ -76,7 +84,7 @@ def test_three_blocks_match_oracle_schedule(overlap, graph, T):
             assert np.abs(gout[t] - ref).max() <= ATTN_ATOL
         # stage 1 for the next block: before this block is appended
         qbar = oracle.merged_query(q0)
-        cand, nc = oracle.topc(oracle.stage1_scores(qbar, kc, cx)[2], cx, w.C)
+        cand, nc = stage1(qbar, kc, cx)
         cx, kc, vc = oracle.append(cx, f64(xb["block_k"][w.T - 1]), f64(xb["block_v"][w.T - 1]),
                                    kc, vc)
 
