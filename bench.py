@@ -205,7 +205,12 @@ class Bench:
         from block_diffusion_sparse_gb300.pipeline import BlockPipeline
         self.exact = _SELECTION == "exact"
         self.pipe = BlockPipeline(self.d, w.C, w.K, w.S, w.W, self.P, w.T, exact=self.exact,
-                                  blocks=BLOCK_KEYS if _SELECTION == "blocks" else 0)
+                                  blocks=BLOCK_KEYS if _SELECTION == "blocks" else 0,
+                                  # a host-resident cache with the block stage 1: the
+                                  # next block's candidate rows cross the link beside
+                                  # the denoising steps (with the per-key stage 1 the
+                                  # link is the scan's: 1,544 against 1,494 us)
+                                  prefetch=w.kv_on_host and _SELECTION == "blocks")
         self.out = torch.zeros((w.T, w.N, w.B, w.Hq, w.d), dtype=torch.int16, device="cuda")
         self.overlap = True
         # stage 1 of the first block (its own queries; no predecessor)

@@ -250,7 +250,7 @@ herald_status run_stage2(const herald_dims& dm, const uint16_t* q_block, const u
                          const int32_t* ctx_len, const int32_t* cand, const int32_t* n_cand,
                          int C, int K, int sink, int local, int P_max, int32_t* idx,
                          int32_t* n_sel, void* ws, const WsLayout& w, cudaStream_t st,
-                         const PoolGather* gather) {
+                         const PoolGather* gather, const uint16_t* staged_k = nullptr) {
   uint32_t* err = at<uint32_t>(ws, w.err);
   CUtensorMap qmap, qmap_all;
   const int G = dm.Hq / dm.Hkv;
@@ -261,7 +261,15 @@ herald_status run_stage2(const herald_dims& dm, const uint16_t* q_block, const u
                           uint32_t(dm.B), &qmap_all);
   if (qs != HERALD_OK) return qs;
   float* rlse = at<float>(ws, w.rlse);
-  if (is_device_memory(k_cache)) {
+  if (staged_k) {
+    // the candidate K rows were staged by slot beforehand
+    herald_dims staged = dm;
+    staged.L_max = C;
+    HERALD_TRY_CUDA(launch_refine(staged, staged_k, nullptr, n_cand, C,
+                                  at<float2>(ws, w.rpart), rlse, at<float>(ws, w.s2), w, err,
+                                  &qmap, &qmap_all, st),
+                    "refine launch");
+  } else if (is_device_memory(k_cache)) {
     HERALD_TRY_CUDA(launch_refine(dm, k_cache, cand, n_cand, C, at<float2>(ws, w.rpart),
                                   rlse, at<float>(ws, w.s2), w, err, &qmap, &qmap_all, st),
                     "refine launch");
@@ -663,6 +671,51 @@ herald_status herald_select_stage2_gather(herald_dims dims, const uint16_t* q_bl
   HERALD_TRY_CUDA(launch_gather(dims, idx, n_sel, P_max, k_cache, v_cache, pool_k, pool_v, st),
                   "gather launch");
   return HERALD_OK;
+}
+
+constexpr int kStageCtas = 128;  // CTAs of the background candidate copy
+
+herald_status herald_stage_candidates(herald_dims dims, const uint16_t* k_cache,
+                                      const int32_t* cand, const int32_t* n_cand, int C,
+                                      uint16_t* staged_k, void* stream) {
+  g_err[0] = 0;
+  HERALD_RET_IF(check_dims(dims));
+  HERALD_RET_IF(check_c(C));
+  HERALD_CHECK_PTR(k_cache);
+  HERALD_CHECK_PTR(cand);
+  HERALD_CHECK_PTR(n_cand);
+  HERALD_CHECK_PTR(staged_k);
+  // a bounded grid: the copy runs beside the denoising kernels and is held
+  // by the host link, not by SMs
+  HERALD_TRY_CUDA(launch_gather(dims, cand, n_cand, C, k_cache, nullptr, staged_k, nullptr,
+                                static_cast<cudaStream_t>(stream),
+                                "gather_kernel (candidate staging)", kStageCtas),
+                  "candidate staging launch");
+  return HERALD_OK;
+}
+
+herald_status herald_select_stage2_staged(herald_dims dims, const uint16_t* q_block,
+                                          const uint16_t* staged_k, const int32_t* ctx_len,
+                                          const int32_t* cand, const int32_t* n_cand, int C,
+                                          int K, int sink, int local, int P_max, int32_t* idx,
+                                          int32_t* n_sel, void* ws, size_t ws_bytes,
+                                          void* stream) {
+  g_err[0] = 0;
+  HERALD_RET_IF(check_dims(dims));
+  HERALD_RET_IF(check_c(C));
+  HERALD_RET_IF(check_pmax(dims, P_max));
+  HERALD_RET_IF(check_budget(C, K, sink, local, P_max));
+  HERALD_CHECK_PTR(q_block);
+  HERALD_CHECK_PTR(staged_k);
+  HERALD_CHECK_PTR(ctx_len);
+  HERALD_CHECK_PTR(cand);
+  HERALD_CHECK_PTR(n_cand);
+  HERALD_CHECK_PTR(idx);
+  HERALD_CHECK_PTR(n_sel);
+  WsLayout w;
+  HERALD_RET_IF(check_ws(dims, C, P_max, ws, ws_bytes, &w));
+  return run_stage2(dims, q_block, staged_k, ctx_len, cand, n_cand, C, K, sink, local, P_max,
+                    idx, n_sel, ws, w, static_cast<cudaStream_t>(stream), nullptr, staged_k);
 }
 
 herald_status herald_select(herald_dims dims, const uint16_t* q_merge, const uint16_t* q_block,

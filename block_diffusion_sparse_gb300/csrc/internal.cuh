@@ -180,7 +180,7 @@ cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const i
 cudaError_t launch_gather(const herald_dims& dm, const int32_t* idx, const int32_t* n_sel,
                           int P_max, const uint16_t* k_cache, const uint16_t* v_cache,
                           uint16_t* pool_k, uint16_t* pool_v, cudaStream_t st,
-                          const char* name = "gather_kernel");
+                          const char* name = "gather_kernel", int max_ctas = 0);
 // Pool attention (balanced 8-CTA clusters, every operand loaded by TMA)
 // applies when attn_pool_ok(); its tensor maps, all bf16 with a box of 64
 // columns and 128-byte swizzle:

@@ -29,23 +29,26 @@ __global__ void __launch_bounds__(256)
   constexpr int TPR = D / 8, RPC = 256 / TPR;
   griddep_enter();
   const int seg = blockIdx.y;
-  const int row = blockIdx.x * RPC + threadIdx.x / TPR, c = threadIdx.x % TPR;
-  if (row >= P_max) return;
-  // idx is read with n_sel, not after it: the row lies inside the index
-  // buffer either way, and its entry is used only below n_sel
-  const int pos = idx[size_t(seg) * P_max + row];
-  const int ns = min(max(n_sel[seg], 0), P_max);
-  uint4 kv = make_uint4(0, 0, 0, 0), vv = kv;
-  if (row < ns) {
-    if (pos >= 0 && pos < L_max) {
-      const size_t off = (size_t(seg) * L_max + pos) * D + c * 8;
-      kv = ld_nc_v4(kc + off);
-      if (vc) vv = ld_nc_v4(vc + off);
+  const int c = threadIdx.x % TPR;
+  // rows blockIdx.x*RPC + ..., then a grid stride (a grid smaller than the
+  // rows leaves SMs to kernels on other streams)
+  for (int row = blockIdx.x * RPC + threadIdx.x / TPR; row < P_max; row += gridDim.x * RPC) {
+    // idx is read with n_sel, not after it: the row lies inside the index
+    // buffer either way, and its entry is used only below n_sel
+    const int pos = idx[size_t(seg) * P_max + row];
+    const int ns = min(max(n_sel[seg], 0), P_max);
+    uint4 kv = make_uint4(0, 0, 0, 0), vv = kv;
+    if (row < ns) {
+      if (pos >= 0 && pos < L_max) {
+        const size_t off = (size_t(seg) * L_max + pos) * D + c * 8;
+        kv = ld_nc_v4(kc + off);
+        if (vc) vv = ld_nc_v4(vc + off);
+      }
     }
+    const size_t dst = (size_t(seg) * P_max + row) * D + c * 8;
+    *reinterpret_cast<uint4*>(pk + dst) = kv;
+    if (vc) *reinterpret_cast<uint4*>(pv + dst) = vv;
   }
-  const size_t dst = (size_t(seg) * P_max + row) * D + c * 8;
-  *reinterpret_cast<uint4*>(pk + dst) = kv;
-  if (vc) *reinterpret_cast<uint4*>(pv + dst) = vv;
 }
 
 // One thread waits on an mbarrier that nothing completes, through the same
@@ -68,16 +71,17 @@ cudaError_t launch_wait_timeout(uint64_t limit_ns, uint32_t* err, cudaStream_t s
 cudaError_t launch_gather(const herald_dims& dm, const int32_t* idx, const int32_t* n_sel,
                           int P_max, const uint16_t* k_cache, const uint16_t* v_cache,
                           uint16_t* pool_k, uint16_t* pool_v, cudaStream_t st,
-                          const char* name) {
+                          const char* name, int max_ctas) {
   const int segs = dm.N * dm.Hkv;
+  const int rpc = dm.d == 128 ? 16 : 32;  // rows per CTA and round
+  int gx = cdiv(P_max, rpc);
+  if (max_ctas > 0) gx = std::max(1, std::min(gx, max_ctas / segs));
   if (dm.d == 128)
-    HERALD_CHECK_LAUNCH(launch_k(name, gather_kernel<128>, dim3(cdiv(P_max, 16), segs), 256, 0, st, idx, n_sel, P_max, dm.L_max,
-                                                                     k_cache, v_cache, pool_k,
-                                                                     pool_v));
+    HERALD_CHECK_LAUNCH(launch_k(name, gather_kernel<128>, dim3(gx, segs), 256, 0, st, idx, n_sel,
+                                 P_max, dm.L_max, k_cache, v_cache, pool_k, pool_v));
   else
-    HERALD_CHECK_LAUNCH(launch_k(name, gather_kernel<64>, dim3(cdiv(P_max, 32), segs), 256, 0, st, idx, n_sel, P_max, dm.L_max,
-                                                                    k_cache, v_cache, pool_k,
-                                                                    pool_v));
+    HERALD_CHECK_LAUNCH(launch_k(name, gather_kernel<64>, dim3(gx, segs), 256, 0, st, idx, n_sel,
+                                 P_max, dm.L_max, k_cache, v_cache, pool_k, pool_v));
   return cudaGetLastError();
 }
 

@@ -88,17 +88,22 @@ def step_flags(t: int, T: int, advance: bool) -> int:
 class BlockPipeline:
     def __init__(self, dims: H.Dims, C: int, K: int, S: int, W: int, P: int, T: int,
                  den_stream=None, sel_stream=None, sel_sms=None, exact: bool = False,
-                 blocks: int = 0):
+                 blocks: int = 0, prefetch: bool = False):
         """blocks > 0: stage 1 selects C // blocks blocks of `blocks` keys
         over the cache's pooled block keys (herald_select_stage1_blocks),
         which the pipeline builds for each cache it meets and refreshes at
-        the tail after every append."""
+        the tail after every append.  prefetch: stage 1 is followed, on its
+        stream, by the copy of the next block's candidate K rows into HBM
+        (herald_stage_candidates), so that the next block's stage 2 reads
+        them there (herald_select_stage2_staged) -- for a cache in host
+        memory, whose link the denoising steps leave idle."""
         import torch
         self.torch = torch
         self.Bk = int(blocks)
         if self.Bk and C % self.Bk:
             raise ValueError(f"C={C} is not a multiple of the block size {self.Bk}")
         self._pooled = {}  # cache address -> fp32 block means (blocks > 0)
+        self.prefetch = bool(prefetch)
         # SMs the overlapped stage-1 scan may occupy (0: all)
         # None: background_sms for the cache each block reads
         self.sel_sms = None if sel_sms is None else int(sel_sms)
@@ -115,6 +120,9 @@ class BlockPipeline:
         self.pool_k = [torch.zeros((*NG, P, dims.d), dtype=torch.int16, device=dev)
                        for _ in range(2)]
         self.pool_v = [torch.zeros_like(self.pool_k[0]) for _ in range(2)]
+        # the candidates' K rows by slot, per candidate buffer (prefetch)
+        self.staged = [torch.zeros((*NG, C, dims.d), dtype=torch.int16, device=dev)
+                       for _ in range(2)] if prefetch else None
         self.den = den_stream
         self.sel = sel_stream if sel_stream is not None else torch.cuda.Stream()
         self._graphs = {}  # captured blocks, by buffers and parity (block(graph=True))
@@ -165,6 +173,10 @@ class BlockPipeline:
                 self.d, H.ptr(q_merge), H.ptr(k_cache), H.ptr(ctx), self.C, self._cand[slot],
                 self._n_cand[slot], self._ws_sel, self.ws_bytes, sms,
                 H.stream_handle(stream)))
+        if self.prefetch:
+            H.check(H.lib().herald_stage_candidates(
+                self.d, H.ptr(k_cache), self._cand[slot], self._n_cand[slot], self.C,
+                H.ptr(self.staged[slot]), H.stream_handle(stream)))
 
     def prime(self, q_merge, k_cache, ctx, slot: int = 0):
         """Stage 1 for the first block (no predecessor: its own queries)."""
@@ -222,10 +234,16 @@ class BlockPipeline:
         wd, wb = self._ws_den, self.ws_bytes
         # stage 1 for block i+1 can start now: block i's queries exist
         sel.wait_stream(den)
-        # stage 2 and the gather into pool[i%2] (one step for a device cache)
-        chk(L.herald_select_stage2_gather(d, q0, kc, vc, cx, self._cand[cur], self._n_cand[cur],
-                                          self.C, self.K, self.S, self.W, P, self._idx,
-                                          self._n_sel, pk, pv, wd, wb, hd))
+        if self.prefetch:  # stage 2 over the prefetched candidate rows, then the gather
+            chk(L.herald_select_stage2_staged(d, q0, H.ptr(self.staged[cur]), cx,
+                                              self._cand[cur], self._n_cand[cur], self.C,
+                                              self.K, self.S, self.W, P, self._idx, self._n_sel,
+                                              wd, wb, hd))
+            chk(L.herald_gather(d, self._idx, self._n_sel, P, kc, vc, pk, pv, hd))
+        else:  # stage 2 and the gather into pool[i%2] (one step for a device cache)
+            chk(L.herald_select_stage2_gather(d, q0, kc, vc, cx, self._cand[cur],
+                                              self._n_cand[cur], self.C, self.K, self.S, self.W,
+                                              P, self._idx, self._n_sel, pk, pv, wd, wb, hd))
         self._stage1(q_steps, nk, ctx, nxt, sel if overlap else den,
                      self._scan_sms(nk) if overlap else 0)
         for t in range(self.T):

@@ -103,6 +103,25 @@ herald_status herald_select_stage1(herald_dims dims, const uint16_t *q_merge,
                                    int32_t *cand, int32_t *n_cand, void *ws, size_t ws_bytes,
                                    int sm_budget, void *stream);
 
+/* Stage 2 split around the host link for a cache in mapped pinned host
+ * memory ([EA]: the subset crosses the link once per block; the candidates'
+ * K rows can cross it while the previous block is denoised):
+ * herald_stage_candidates copies the candidates' K rows by slot,
+ *   staged_k[n][g][c] = k_cache[n][g][cand[n][g][c]] for c < n_cand, zero
+ *   rows after, bf16 [N][Hkv][C][d] device out;
+ * herald_select_stage2_staged is herald_select_stage2 reading the candidate
+ * rows from staged_k (the same idx and n_sel, bit for bit).  The cache rows
+ * below ctx_len must not change between the two calls. */
+herald_status herald_stage_candidates(herald_dims dims, const uint16_t *k_cache,
+                                      const int32_t *cand, const int32_t *n_cand, int C,
+                                      uint16_t *staged_k, void *stream);
+herald_status herald_select_stage2_staged(herald_dims dims, const uint16_t *q_block,
+                                          const uint16_t *staged_k, const int32_t *ctx_len,
+                                          const int32_t *cand, const int32_t *n_cand, int C,
+                                          int K, int sink, int local, int P_max, int32_t *idx,
+                                          int32_t *n_sel, void *ws, size_t ws_bytes,
+                                          void *stream);
+
 /* Block-granular stage 1 ([SPD]: InfLLM-V2 selects whole blocks of the
  * context; here stage 1's rule is applied to blocks, not keys).  The cache is
  * summarised by its block means -- the "compressed keys" --

@@ -429,6 +429,17 @@ def test_host_resident_cache_matches_device_cache(w):
     assert r.error_word() == 0
     assert torch.equal(idx_dev, r.idx) and torch.equal(ns_dev, r.n_sel)
     assert torch.equal(pk_dev, r.pool_k)
+    # stage 2 over candidate rows staged beforehand (the prefetch of a
+    # host-resident cache): the same selection, bit for bit
+    staged = torch.full((w_.N, w_.Hkv, w_.C, w_.d), 99, dtype=torch.int16, device="cuda")
+    H.herald_select_stage1(r.d, r.q_merge, kh, r.ctx, w_.C, r.cand, r.n_cand, r.ws)
+    H.herald_stage_candidates(r.d, kh, r.cand, r.n_cand, w_.C, staged)
+    r.idx.fill_(7)
+    H.herald_select_stage2_staged(r.d, r.q_steps[0], staged, r.ctx, r.cand, r.n_cand, w_.C, w_.K,
+                                  w_.S, w_.W, r.P, r.idx, r.n_sel, r.ws)
+    torch.cuda.synchronize()
+    assert r.error_word() == 0
+    assert torch.equal(idx_dev, r.idx) and torch.equal(ns_dev, r.n_sel)
     # the combined stage 2 + gather on the host-resident cache (two kernels
     # there) from the same stage-1 candidates
     H.herald_select_stage1(r.d, r.q_merge, kh, r.ctx, w_.C, r.cand, r.n_cand, r.ws)

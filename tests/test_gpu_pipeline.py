@@ -17,14 +17,17 @@ from block_diffusion_sparse_gb300.workloads import Workload
 from helpers import ATTN_ATOL, bf16_dev_to_f64, dev, f64
 
 
-@pytest.mark.parametrize("overlap,graph,T,Bk", [(True, False, 2, 0), (False, False, 2, 0),
-                                                (True, True, 2, 0), (True, False, 1, 0),
-                                                (True, False, 2, 16), (True, True, 2, 32)])
-def test_three_blocks_match_oracle_schedule(overlap, graph, T, Bk):
+@pytest.mark.parametrize("overlap,graph,T,Bk,host", [
+    (True, False, 2, 0, False), (False, False, 2, 0, False), (True, True, 2, 0, False),
+    (True, False, 1, 0, False), (True, False, 2, 16, False), (True, True, 2, 32, False),
+    (True, False, 2, 16, True)])
+def test_three_blocks_match_oracle_schedule(overlap, graph, T, Bk, host):
     """graph=True: every block's inputs are copied into the same buffers, so
     block 2 replays the CUDA graph captured for block 0 (same parity).
     T=1: the only denoising step also appends the block.  Bk > 0: stage 1
-    over the cache's pooled blocks of Bk keys, refreshed after each append."""
+    over the cache's pooled blocks of Bk keys, refreshed after each append.
+    host: the cache in pinned host memory, the next block's candidate rows
+    prefetched beside the denoising steps."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     nb = 3
@@ -34,9 +37,13 @@ def test_three_blocks_match_oracle_schedule(overlap, graph, T, Bk):
     blocks = [synth.make_layer(w.scaled(L=64, extra_rows=0, n_planted=0), layer=i + 1)
               for i in range(nb)]
     d = H.dims_of(w)
-    k, v = dev(x0["k_cache"]), dev(x0["v_cache"])
+    if host:
+        k = torch.from_numpy(x0["k_cache"].view(np.int16).copy()).pin_memory()
+        v = torch.from_numpy(x0["v_cache"].view(np.int16).copy()).pin_memory()
+    else:
+        k, v = dev(x0["k_cache"]), dev(x0["v_cache"])
     ctx = dev(x0["ctx"])
-    pipe = BlockPipeline(d, w.C, w.K, w.S, w.W, w.P, w.T, blocks=Bk)
+    pipe = BlockPipeline(d, w.C, w.K, w.S, w.W, w.P, w.T, blocks=Bk, prefetch=host)
     pipe.prime(dev(x0["q_merge"]), k, ctx)
     got = []
     fixed = None
