@@ -120,6 +120,28 @@ def test_attention_and_gather_argument_errors():
     assert e.value.status == 1
 
 
+def test_block_stage1_and_staging_argument_errors():
+    _built()
+    d = H.dims(1, 4, 1, 64, 16, 2048)
+    ok = 1 << 12
+    ws = H.herald_workspace_size(d, 256, 208)
+    for Bk, n_tail, status in [(0, 0, 1), (4096, 0, 1), (64, -1, 1)]:
+        with pytest.raises(H.HeraldError) as e:
+            H.herald_pool_keys(d, ok, ok, Bk, ok, n_tail=n_tail)
+        assert e.value.status == status, (Bk, n_tail)
+    for Bk, Cb, status in [(0, 4, 1), (64, 0, 2), (64, 300, 2)]:   # C_blocks*Bk <= 16384
+        with pytest.raises(H.HeraldError) as e:
+            H.herald_select_stage1_blocks(d, ok, ok, ok, Bk, Cb, ok, ok, ok, ws)
+        assert e.value.status == status, (Bk, Cb)
+    with pytest.raises(H.HeraldError) as e:
+        H.herald_stage_candidates(d, ok, ok, ok, 256, None)
+    assert e.value.status == 1
+    with pytest.raises(H.HeraldError) as e:
+        H.herald_select_stage2_staged(d, ok, None, ok, ok, ok, 256, 128, 16, 64, 208, ok, ok, ok,
+                                      ws)
+    assert e.value.status == 1
+
+
 def test_status_strings():
     _built()
     for s in range(5):
