@@ -135,6 +135,7 @@ WORKLOADS = {"qwen": "QWEN_32K", "tiny": "TINY", "llama": "LLAMA_64K",
              "long-host": "LONG_128K_HOST", "stack": "QWEN_STACK"}
 _WORKLOAD = "qwen"
 _SELECTION = "merged"
+_PREFETCH = "kv"  # --prefetch: the candidate rows prefetched for a host-resident cache
 BLOCK_KEYS = 64  # keys per block of the block-granular stage 1 (--selection blocks)
 
 
@@ -210,11 +211,12 @@ class Bench:
                                   # next block's candidate rows cross the link beside
                                   # the denoising steps (with the per-key stage 1 the
                                   # link is the scan's: 1,544 against 1,494 us)
-                                  prefetch=w.kv_on_host and _SELECTION == "blocks")
+                                  prefetch=(_PREFETCH if w.kv_on_host and _SELECTION == "blocks"
+                                            else False))
         self.out = torch.zeros((w.T, w.N, w.B, w.Hq, w.d), dtype=torch.int16, device="cuda")
         self.overlap = True
         # stage 1 of the first block (its own queries; no predecessor)
-        self.pipe.prime(self.q_merge, self.k[0], self.ctx, slot=0)
+        self.pipe.prime(self.q_merge, self.k[0], self.ctx, slot=0, v_cache=self.v[0])
         torch.cuda.synchronize()
 
     @property
@@ -239,6 +241,13 @@ class Bench:
     def context_note(self) -> str:
         return "fixed: each step appends the block at the same position (ctx not advanced)"
 
+    def prefetch_note(self) -> str:
+        p = getattr(self, "pipe", None)
+        if not getattr(p, "prefetch", False):
+            return "none"
+        return ("next block's candidate K and V rows (top-K pool rows gathered from HBM)"
+                if p.prefetch_v else "next block's candidate K rows")
+
     def l2_note(self) -> str:
         if self.w.kv_on_host:
             return "K/V cache in pinned host memory (read over the host link)"
@@ -260,7 +269,8 @@ class Bench:
             return
         self.pipe.block(r, qs, bk, bv, self.k[r], self.v[r], self.ctx,
                         self.out if out is None else out, next_k_cache=self.k[nxt],
-                        advance=False, overlap=self.overlap, graph=graph)
+                        next_v_cache=self.v[nxt], advance=False, overlap=self.overlap,
+                        graph=graph)
 
     def attn_operands(self):
         """(pool_k, pool_v, n_sel, q_steps, block_k, block_v, out, ws) of one
@@ -724,6 +734,7 @@ def run_ours(args, rank, world, dist):
                        "local": w.W, "parallelism": f"replicas x{world}",
                        "layers": w.layers, "l2": b.l2_note(), "context": b.context_note(),
                        "selection": _SELECTION,
+                       "prefetch": b.prefetch_note(),
                        "timing": (f"CUDA-graph replay, {chunk} consecutive blocks per graph "
                                   f"(one graph launch per {chunk} blocks), CUDA events"
                                   if chunk > 1 else
@@ -843,10 +854,16 @@ def main():
                     help="merged: the two-stage selection (default); exact: every cached "
                          "position scored with the block's real queries (one stream); "
                          "blocks: stage 1 over 64-key block means")
+    ap.add_argument("--prefetch", default="kv", choices=["k", "kv"],
+                    help="host-resident cache with --selection blocks: the next block's "
+                         "candidate rows copied beside the denoising steps -- K rows for "
+                         "stage 2 (k), or K and V rows with the top-K pool rows gathered "
+                         "from HBM (kv, default)")
     args = ap.parse_args()
-    global _WORKLOAD, _SELECTION
+    global _WORKLOAD, _SELECTION, _PREFETCH
     _WORKLOAD = args.workload
     _SELECTION = args.selection
+    _PREFETCH = args.prefetch
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

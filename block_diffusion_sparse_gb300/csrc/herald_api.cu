@@ -250,7 +250,8 @@ herald_status run_stage2(const herald_dims& dm, const uint16_t* q_block, const u
                          const int32_t* ctx_len, const int32_t* cand, const int32_t* n_cand,
                          int C, int K, int sink, int local, int P_max, int32_t* idx,
                          int32_t* n_sel, void* ws, const WsLayout& w, cudaStream_t st,
-                         const PoolGather* gather, const uint16_t* staged_k = nullptr) {
+                         const PoolGather* gather, const uint16_t* staged_k = nullptr,
+                         int32_t* slot_out = nullptr) {
   uint32_t* err = at<uint32_t>(ws, w.err);
   CUtensorMap qmap, qmap_all;
   const int G = dm.Hq / dm.Hkv;
@@ -290,7 +291,7 @@ herald_status run_stage2(const herald_dims& dm, const uint16_t* q_block, const u
   }
   const int n_parts = refine_fused_ok(C) ? w.MT_tok : 1;
   HERALD_TRY_CUDA(launch_topk_union(dm, ctx_len, cand, n_cand, at<float>(ws, w.s2), n_parts, C, K,
-                                    sink, local, P_max, idx, n_sel, st, gather),
+                                    sink, local, P_max, idx, n_sel, st, gather, slot_out),
                   "topk_union launch");
   return HERALD_OK;
 }
@@ -673,11 +674,17 @@ herald_status herald_select_stage2_gather(herald_dims dims, const uint16_t* q_bl
   return HERALD_OK;
 }
 
-constexpr int kStageCtas = 128;  // CTAs of the background candidate copy
+// CTAs of the background candidate copy.  Each one holds an SM that an
+// attention CTA (all of an SM's registers) then cannot use; the copy is
+// bounded by the host link, not by SMs.  128K host-resident layer, block
+// stage 1, per block: K rows 378 / 344 / 344 us at 128 / 64 / 32 CTAs, K and
+// V rows 384 / 327 / 330 us.
+constexpr int kStageCtas = 64;
 
 herald_status herald_stage_candidates(herald_dims dims, const uint16_t* k_cache,
-                                      const int32_t* cand, const int32_t* n_cand, int C,
-                                      uint16_t* staged_k, void* stream) {
+                                      const uint16_t* v_cache, const int32_t* cand,
+                                      const int32_t* n_cand, int C, uint16_t* staged_k,
+                                      uint16_t* staged_v, void* stream) {
   g_err[0] = 0;
   HERALD_RET_IF(check_dims(dims));
   HERALD_RET_IF(check_c(C));
@@ -685,9 +692,11 @@ herald_status herald_stage_candidates(herald_dims dims, const uint16_t* k_cache,
   HERALD_CHECK_PTR(cand);
   HERALD_CHECK_PTR(n_cand);
   HERALD_CHECK_PTR(staged_k);
+  if ((v_cache == nullptr) != (staged_v == nullptr))
+    return fail(HERALD_ERR_INVALID_ARG, "v_cache and staged_v must both be given or both null");
   // a bounded grid: the copy runs beside the denoising kernels and is held
   // by the host link, not by SMs
-  HERALD_TRY_CUDA(launch_gather(dims, cand, n_cand, C, k_cache, nullptr, staged_k, nullptr,
+  HERALD_TRY_CUDA(launch_gather(dims, cand, n_cand, C, k_cache, v_cache, staged_k, staged_v,
                                 static_cast<cudaStream_t>(stream),
                                 "gather_kernel (candidate staging)", kStageCtas),
                   "candidate staging launch");
@@ -716,6 +725,43 @@ herald_status herald_select_stage2_staged(herald_dims dims, const uint16_t* q_bl
   HERALD_RET_IF(check_ws(dims, C, P_max, ws, ws_bytes, &w));
   return run_stage2(dims, q_block, staged_k, ctx_len, cand, n_cand, C, K, sink, local, P_max,
                     idx, n_sel, ws, w, static_cast<cudaStream_t>(stream), nullptr, staged_k);
+}
+
+herald_status herald_select_stage2_staged_gather(
+    herald_dims dims, const uint16_t* q_block, const uint16_t* staged_k, const uint16_t* staged_v,
+    const uint16_t* k_cache, const uint16_t* v_cache, const int32_t* ctx_len, const int32_t* cand,
+    const int32_t* n_cand, int C, int K, int sink, int local, int P_max, int32_t* idx,
+    int32_t* n_sel, uint16_t* pool_k, uint16_t* pool_v, void* ws, size_t ws_bytes,
+    void* stream) {
+  g_err[0] = 0;
+  HERALD_RET_IF(check_dims(dims));
+  HERALD_RET_IF(check_c(C));
+  HERALD_RET_IF(check_pmax(dims, P_max));
+  HERALD_RET_IF(check_budget(C, K, sink, local, P_max));
+  HERALD_CHECK_PTR(q_block);
+  HERALD_CHECK_PTR(staged_k);
+  HERALD_CHECK_PTR(staged_v);
+  HERALD_CHECK_PTR(k_cache);
+  HERALD_CHECK_PTR(v_cache);
+  HERALD_CHECK_PTR(ctx_len);
+  HERALD_CHECK_PTR(cand);
+  HERALD_CHECK_PTR(n_cand);
+  HERALD_CHECK_PTR(idx);
+  HERALD_CHECK_PTR(n_sel);
+  HERALD_CHECK_PTR(pool_k);
+  HERALD_CHECK_PTR(pool_v);
+  WsLayout w;
+  HERALD_RET_IF(check_ws(dims, C, P_max, ws, ws_bytes, &w));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t* slot = at<int32_t>(ws, w.slot);
+  HERALD_RET_IF(run_stage2(dims, q_block, staged_k, ctx_len, cand, n_cand, C, K, sink, local,
+                           P_max, idx, n_sel, ws, w, st, nullptr, staged_k, slot));
+  // the top-K rows from the staged candidates (HBM), the sink and local rows
+  // from the cache
+  HERALD_TRY_CUDA(launch_gather_staged(dims, idx, n_sel, P_max, slot, C, staged_k, staged_v,
+                                       k_cache, v_cache, pool_k, pool_v, st),
+                  "staged gather launch");
+  return HERALD_OK;
 }
 
 herald_status herald_select(herald_dims dims, const uint16_t* q_merge, const uint16_t* q_block,

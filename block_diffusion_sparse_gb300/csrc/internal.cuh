@@ -51,6 +51,7 @@ struct WsLayout {
   size_t s2;         // float [MT][N][Hkv][C] stage-2 score partials
   size_t opart;      // float [N*Hkv][MT][S][128][d]      attention partials
   size_t ml;         // float2 [N*Hkv][MT][S][128]
+  size_t slot;       // int32 [N][Hkv][P_max]   candidate slot per selected row
   size_t total;
   int L_pad, tiles_per_seg, tiles128, R, MT, n_chunks, splits;
   int MT_tok;        // row tiles of whole tokens (floor(128 / G) tokens each)
@@ -84,6 +85,7 @@ inline WsLayout ws_layout(const herald_dims& dm, int C, int P_max) {
   w.s2 = o;     o = align_up(o + NG * C * 4 * size_t(std::max(w.MT, w.MT_tok)), A);  // per row tile
   w.opart = o;  o = align_up(o + NG * w.MT * size_t(w.splits) * kTileM * dm.d * 4, A);
   w.ml = o;     o = align_up(o + NG * w.MT * size_t(w.splits) * kTileM * 8, A);
+  w.slot = o;   o = align_up(o + NG * size_t(P_max) * 4, A);
   w.total = o;
   return w;
 }
@@ -171,16 +173,27 @@ struct PoolGather {
   int copies;
 };
 // s2 holds n_parts partial score arrays of [N*Hkv][C], summed per candidate;
-// gather (optional) also fills the pool.
+// gather (optional) also fills the pool; slot_out (optional, [N*Hkv][P_max])
+// receives the candidate slot of every selected row taken from the top-K,
+// -1 for sink, local and padding rows.
 cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const int32_t* cand,
                               const int32_t* n_cand, const float* s2, int n_parts, int C, int K,
                               int S, int W, int P_max, int32_t* idx, int32_t* n_sel,
-                              cudaStream_t st, const PoolGather* gather = nullptr);
+                              cudaStream_t st, const PoolGather* gather = nullptr,
+                              int32_t* slot_out = nullptr);
 // (name: the label the launch carries in traces)
 cudaError_t launch_gather(const herald_dims& dm, const int32_t* idx, const int32_t* n_sel,
                           int P_max, const uint16_t* k_cache, const uint16_t* v_cache,
                           uint16_t* pool_k, uint16_t* pool_v, cudaStream_t st,
                           const char* name = "gather_kernel", int max_ctas = 0);
+// The gather with the candidate rows read from HBM: row r of (n, g) comes
+// from staged_k/staged_v [N*Hkv][C][d] at slot src[n][g][r] when that is
+// >= 0 (rows taken from the candidates), else from the cache at idx.
+cudaError_t launch_gather_staged(const herald_dims& dm, const int32_t* idx, const int32_t* n_sel,
+                                 int P_max, const int32_t* src, int C, const uint16_t* staged_k,
+                                 const uint16_t* staged_v, const uint16_t* k_cache,
+                                 const uint16_t* v_cache, uint16_t* pool_k, uint16_t* pool_v,
+                                 cudaStream_t st);
 // Pool attention (balanced 8-CTA clusters, every operand loaded by TMA)
 // applies when attn_pool_ok(); its tensor maps, all bf16 with a box of 64
 // columns and 128-byte swizzle:

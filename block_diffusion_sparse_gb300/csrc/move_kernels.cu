@@ -20,12 +20,16 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
 
 // grid (ceil(P_max / rows_per_cta), N*Hkv), block 256; D/8 threads per row,
 // one 16-byte chunk each.  With vc == nullptr only K rows are copied (the
-// stage-2 staging of candidate rows from a host-resident cache).
+// stage-2 staging of candidate rows from a host-resident cache).  With src,
+// a row whose src entry is a candidate slot s >= 0 is read from the rows
+// staged by slot (sk, sv: [N*Hkv][C][D]) instead of the cache.
 template <int D>
 __global__ void __launch_bounds__(256)
     gather_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ n_sel, int P_max,
                   int L_max, const uint16_t* __restrict__ kc, const uint16_t* __restrict__ vc,
-                  uint16_t* __restrict__ pk, uint16_t* __restrict__ pv) {
+                  uint16_t* __restrict__ pk, uint16_t* __restrict__ pv,
+                  const int32_t* __restrict__ src, int C, const uint16_t* __restrict__ sk,
+                  const uint16_t* __restrict__ sv) {
   constexpr int TPR = D / 8, RPC = 256 / TPR;
   griddep_enter();
   const int seg = blockIdx.y;
@@ -33,13 +37,18 @@ __global__ void __launch_bounds__(256)
   // rows blockIdx.x*RPC + ..., then a grid stride (a grid smaller than the
   // rows leaves SMs to kernels on other streams)
   for (int row = blockIdx.x * RPC + threadIdx.x / TPR; row < P_max; row += gridDim.x * RPC) {
-    // idx is read with n_sel, not after it: the row lies inside the index
-    // buffer either way, and its entry is used only below n_sel
+    // idx (and src) are read with n_sel, not after it: the row lies inside
+    // the index buffer either way, and its entry is used only below n_sel
     const int pos = idx[size_t(seg) * P_max + row];
+    const int s = src ? src[size_t(seg) * P_max + row] : -1;
     const int ns = min(max(n_sel[seg], 0), P_max);
     uint4 kv = make_uint4(0, 0, 0, 0), vv = kv;
     if (row < ns) {
-      if (pos >= 0 && pos < L_max) {
+      if (s >= 0 && s < C) {  // a candidate row staged in HBM by slot
+        const size_t off = (size_t(seg) * C + s) * D + c * 8;
+        kv = ld_nc_v4(sk + off);
+        if (vc) vv = ld_nc_v4(sv + off);
+      } else if (pos >= 0 && pos < L_max) {
         const size_t off = (size_t(seg) * L_max + pos) * D + c * 8;
         kv = ld_nc_v4(kc + off);
         if (vc) vv = ld_nc_v4(vc + off);
@@ -68,21 +77,42 @@ cudaError_t launch_wait_timeout(uint64_t limit_ns, uint32_t* err, cudaStream_t s
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather(const herald_dims& dm, const int32_t* idx, const int32_t* n_sel,
-                          int P_max, const uint16_t* k_cache, const uint16_t* v_cache,
-                          uint16_t* pool_k, uint16_t* pool_v, cudaStream_t st,
-                          const char* name, int max_ctas) {
+static cudaError_t gather_launch(const herald_dims& dm, const int32_t* idx,
+                                 const int32_t* n_sel, int P_max, const uint16_t* k_cache,
+                                 const uint16_t* v_cache, uint16_t* pool_k, uint16_t* pool_v,
+                                 const int32_t* src, int C, const uint16_t* staged_k,
+                                 const uint16_t* staged_v, cudaStream_t st, const char* name,
+                                 int max_ctas) {
   const int segs = dm.N * dm.Hkv;
   const int rpc = dm.d == 128 ? 16 : 32;  // rows per CTA and round
   int gx = cdiv(P_max, rpc);
   if (max_ctas > 0) gx = std::max(1, std::min(gx, max_ctas / segs));
   if (dm.d == 128)
     HERALD_CHECK_LAUNCH(launch_k(name, gather_kernel<128>, dim3(gx, segs), 256, 0, st, idx, n_sel,
-                                 P_max, dm.L_max, k_cache, v_cache, pool_k, pool_v));
+                                 P_max, dm.L_max, k_cache, v_cache, pool_k, pool_v, src, C,
+                                 staged_k, staged_v));
   else
     HERALD_CHECK_LAUNCH(launch_k(name, gather_kernel<64>, dim3(gx, segs), 256, 0, st, idx, n_sel,
-                                 P_max, dm.L_max, k_cache, v_cache, pool_k, pool_v));
+                                 P_max, dm.L_max, k_cache, v_cache, pool_k, pool_v, src, C,
+                                 staged_k, staged_v));
   return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const herald_dims& dm, const int32_t* idx, const int32_t* n_sel,
+                          int P_max, const uint16_t* k_cache, const uint16_t* v_cache,
+                          uint16_t* pool_k, uint16_t* pool_v, cudaStream_t st,
+                          const char* name, int max_ctas) {
+  return gather_launch(dm, idx, n_sel, P_max, k_cache, v_cache, pool_k, pool_v, nullptr, 0,
+                       nullptr, nullptr, st, name, max_ctas);
+}
+
+cudaError_t launch_gather_staged(const herald_dims& dm, const int32_t* idx, const int32_t* n_sel,
+                                 int P_max, const int32_t* src, int C, const uint16_t* staged_k,
+                                 const uint16_t* staged_v, const uint16_t* k_cache,
+                                 const uint16_t* v_cache, uint16_t* pool_k, uint16_t* pool_v,
+                                 cudaStream_t st) {
+  return gather_launch(dm, idx, n_sel, P_max, k_cache, v_cache, pool_k, pool_v, src, C, staged_k,
+                       staged_v, st, "gather_kernel (staged)", 0);
 }
 
 // grid N, block 1024: one CTA per sequence so that reading ctx_len[n] and

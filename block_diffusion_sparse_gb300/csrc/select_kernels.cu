@@ -937,7 +937,9 @@ cudaError_t launch_exact_sum_hist(const herald_dims& dm, float* s, int n_parts, 
 // candidates being ascending), the winners marked in a shared bitmap, and one
 // block scan orders the output: [0, sink_end) ++ kept candidates inside
 // [sink_end, local_begin) ++ [local_begin, L) -- the deduplicated ascending
-// union.
+// union.  With slot_out, each output row also records the candidate slot it
+// came from (-1 for sink, local and padding rows), so that a gather can read
+// candidate rows staged by slot.
 constexpr int kTkThreads = 1024;
 constexpr int kTkRankCap = 1024;  // members ranked in one shot
 
@@ -946,7 +948,8 @@ __global__ void __launch_bounds__(kTkThreads)
     topk_union_kernel(const int32_t* __restrict__ ctx, const int32_t* __restrict__ cand,
                       const int32_t* __restrict__ n_cand, const float* __restrict__ s2,
                       int n_parts, int Hkv, int L_max, int C, int K, int S, int W, int P_max,
-                      int32_t* __restrict__ idx, int32_t* __restrict__ n_sel, PoolGather pg) {
+                      int32_t* __restrict__ idx, int32_t* __restrict__ n_sel, PoolGather pg,
+                      int32_t* __restrict__ slot_out) {
   // [C] bit patterns of the threshold-bin members, then (with the gather)
   // [P_max] selected positions
   extern __shared__ uint32_t mem[];
@@ -1129,22 +1132,28 @@ __global__ void __launch_bounds__(kTkThreads)
   int32_t* out = idx + size_t(seg) * P_max;
   int32_t* sidx = reinterpret_cast<int32_t*>(mem + C);
   const bool to_global = copy == 0;
-  auto put = [&](int slot, int32_t v) {
-    if (to_global) out[slot] = v;
+  int32_t* so = slot_out ? slot_out + size_t(seg) * P_max : nullptr;
+  // row `slot` of the selection holds position v, taken from candidate slot
+  // src (-1: a sink, local or padding row)
+  auto put = [&](int slot, int32_t v, int32_t src) {
+    if (to_global) {
+      out[slot] = v;
+      if (so) so[slot] = src;
+    }
     if (pg.pk) sidx[slot] = v;
   };
 #pragma unroll
   for (int k = 0; k < kPer; ++k)
     if ((keep_mask >> k) & 1u) {
-      if (sink_end + int(at) < P_max) put(sink_end + at, pk[k]);
+      if (sink_end + int(at) < P_max) put(sink_end + at, pk[k], i0 + k);
       ++at;
     }
-  for (int j = threadIdx.x; j < sink_end; j += kTkThreads) put(j, j);
+  for (int j = threadIdx.x; j < sink_end; j += kTkThreads) put(j, j, -1);
   for (int j = local_begin + threadIdx.x; j < L; j += kTkThreads)
     if (sink_end + int(n_mid) + (j - local_begin) < P_max)
-      put(sink_end + n_mid + (j - local_begin), j);
+      put(sink_end + n_mid + (j - local_begin), j, -1);
   const int total = min(P_max, sink_end + int(n_mid) + (L - local_begin));
-  for (int s = total + threadIdx.x; s < P_max; s += kTkThreads) put(s, -1);
+  for (int s = total + threadIdx.x; s < P_max; s += kTkThreads) put(s, -1, -1);
   if (to_global && threadIdx.x == 0) n_sel[seg] = total;
   if (!pg.pk) return;
   // the gather of this copy's slice of the pool: rows [r0, r1) of (n, g),
@@ -1172,7 +1181,7 @@ __global__ void __launch_bounds__(kTkThreads)
 cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const int32_t* cand,
                               const int32_t* n_cand, const float* s2, int n_parts, int C, int K,
                               int S, int W, int P_max, int32_t* idx, int32_t* n_sel,
-                              cudaStream_t st, const PoolGather* gather) {
+                              cudaStream_t st, const PoolGather* gather, int32_t* slot_out) {
   static_assert(kMaxC <= 16 * kTkThreads, "16 scores per thread cover every C");
   const PoolGather pg = gather ? *gather : PoolGather{nullptr, nullptr, nullptr, nullptr, 0, 1};
   const size_t smem = size_t(C) * 4 + (pg.pk ? size_t(P_max) * 4 : 0u);
@@ -1191,11 +1200,11 @@ cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const i
   if (C <= 4 * kTkThreads)
     HERALD_CHECK_LAUNCH(launch_k("topk_union_kernel", topk_union_kernel<4>, grid, kTkThreads, smem,
                                  st, ctx, cand, n_cand, s2, n_parts, dm.Hkv, dm.L_max, C, K, S, W,
-                                 P_max, idx, n_sel, pg));
+                                 P_max, idx, n_sel, pg, slot_out));
   else
     HERALD_CHECK_LAUNCH(launch_k("topk_union_kernel", topk_union_kernel<16>, grid, kTkThreads,
                                  smem, st, ctx, cand, n_cand, s2, n_parts, dm.Hkv, dm.L_max, C, K,
-                                 S, W, P_max, idx, n_sel, pg));
+                                 S, W, P_max, idx, n_sel, pg, slot_out));
   return cudaGetLastError();
 }
 

@@ -27,7 +27,7 @@ EXPORTS = ("herald_workspace_size", "herald_status_string", "herald_last_error",
            "herald_select_stage2_noalloc", "herald_selftest_wait_timeout",
            "herald_workspace_size_exact", "herald_select_exact", "herald_pool_keys",
            "herald_select_stage1_blocks", "herald_stage_candidates",
-           "herald_select_stage2_staged")
+           "herald_select_stage2_staged", "herald_select_stage2_staged_gather")
 
 
 class HeraldError(RuntimeError):
@@ -95,9 +95,12 @@ def lib() -> C.CDLL:
         L.herald_select_exact.argtypes = [Dims, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, sz,
                                           vp]
         L.herald_pool_keys.argtypes = [Dims, vp, vp, i32, i32, vp, vp]
-        L.herald_stage_candidates.argtypes = [Dims, vp, vp, vp, i32, vp, vp]
+        L.herald_stage_candidates.argtypes = [Dims, vp, vp, vp, vp, i32, vp, vp, vp]
         L.herald_select_stage2_staged.argtypes = [Dims, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                   i32, vp, vp, vp, sz, vp]
+        L.herald_select_stage2_staged_gather.argtypes = [Dims, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                         i32, i32, i32, i32, i32, vp, vp, vp, vp,
+                                                         vp, sz, vp]
         L.herald_select_stage1_blocks.argtypes = [Dims, vp, vp, vp, i32, i32, vp, vp, vp, sz,
                                                   vp]
         L.herald_trace_begin.argtypes = [C.POINTER(vp), i32, i32]
@@ -258,9 +261,10 @@ def herald_select_stage1_blocks(d, q_merge, pooled, ctx_len, Bk, C_blocks, cand,
                                              _nbytes(ws, ws_bytes), _s(stream)))
 
 
-def herald_stage_candidates(d, k_cache, cand, n_cand, C, staged_k, stream=None):
-    _check(lib().herald_stage_candidates(d, _p(k_cache), _p(cand), _p(n_cand), int(C),
-                                         _p(staged_k), _s(stream)))
+def herald_stage_candidates(d, k_cache, cand, n_cand, C, staged_k, v_cache=None, staged_v=None,
+                            stream=None):
+    _check(lib().herald_stage_candidates(d, _p(k_cache), _p(v_cache), _p(cand), _p(n_cand),
+                                         int(C), _p(staged_k), _p(staged_v), _s(stream)))
 
 
 def herald_select_stage2_staged(d, q_block, staged_k, ctx_len, cand, n_cand, C, K, sink, local,
@@ -269,6 +273,15 @@ def herald_select_stage2_staged(d, q_block, staged_k, ctx_len, cand, n_cand, C, 
                                              _p(n_cand), int(C), int(K), int(sink), int(local),
                                              int(P_max), _p(idx), _p(n_sel), _p(ws),
                                              _nbytes(ws, ws_bytes), _s(stream)))
+
+
+def herald_select_stage2_staged_gather(d, q_block, staged_k, staged_v, k_cache, v_cache, ctx_len,
+                                       cand, n_cand, C, K, sink, local, P_max, idx, n_sel,
+                                       pool_k, pool_v, ws=None, ws_bytes=None, stream=None):
+    _check(lib().herald_select_stage2_staged_gather(
+        d, _p(q_block), _p(staged_k), _p(staged_v), _p(k_cache), _p(v_cache), _p(ctx_len),
+        _p(cand), _p(n_cand), int(C), int(K), int(sink), int(local), int(P_max), _p(idx),
+        _p(n_sel), _p(pool_k), _p(pool_v), _p(ws), _nbytes(ws, ws_bytes), _s(stream)))
 
 
 def herald_gather(d, idx, n_sel, P_max, k_cache, v_cache, pool_k, pool_v, stream=None):

@@ -88,7 +88,7 @@ def step_flags(t: int, T: int, advance: bool) -> int:
 class BlockPipeline:
     def __init__(self, dims: H.Dims, C: int, K: int, S: int, W: int, P: int, T: int,
                  den_stream=None, sel_stream=None, sel_sms=None, exact: bool = False,
-                 blocks: int = 0, prefetch: bool = False):
+                 blocks: int = 0, prefetch=False):
         """blocks > 0: stage 1 selects C // blocks blocks of `blocks` keys
         over the cache's pooled block keys (herald_select_stage1_blocks),
         which the pipeline builds for each cache it meets and refreshes at
@@ -96,14 +96,20 @@ class BlockPipeline:
         stream, by the copy of the next block's candidate K rows into HBM
         (herald_stage_candidates), so that the next block's stage 2 reads
         them there (herald_select_stage2_staged) -- for a cache in host
-        memory, whose link the denoising steps leave idle."""
+        memory, whose link the denoising steps leave idle.  prefetch="kv":
+        the candidates' V rows too, and the gather reads the top-K rows from
+        HBM (herald_select_stage2_staged_gather; only the sink and local
+        rows cross the link inside the step)."""
         import torch
         self.torch = torch
         self.Bk = int(blocks)
         if self.Bk and C % self.Bk:
             raise ValueError(f"C={C} is not a multiple of the block size {self.Bk}")
         self._pooled = {}  # cache address -> fp32 block means (blocks > 0)
+        if prefetch not in (False, True, "k", "kv"):
+            raise ValueError(f"prefetch={prefetch!r}: False, True (= 'k') or 'kv'")
         self.prefetch = bool(prefetch)
+        self.prefetch_v = prefetch == "kv"
         # SMs the overlapped stage-1 scan may occupy (0: all)
         # None: background_sms for the cache each block reads
         self.sel_sms = None if sel_sms is None else int(sel_sms)
@@ -120,9 +126,11 @@ class BlockPipeline:
         self.pool_k = [torch.zeros((*NG, P, dims.d), dtype=torch.int16, device=dev)
                        for _ in range(2)]
         self.pool_v = [torch.zeros_like(self.pool_k[0]) for _ in range(2)]
-        # the candidates' K rows by slot, per candidate buffer (prefetch)
+        # the candidates' K and V rows by slot, per candidate buffer (prefetch)
         self.staged = [torch.zeros((*NG, C, dims.d), dtype=torch.int16, device=dev)
                        for _ in range(2)] if prefetch else None
+        self.staged_v = ([torch.zeros_like(t) for t in self.staged] if self.prefetch_v
+                         else None)
         self.den = den_stream
         self.sel = sel_stream if sel_stream is not None else torch.cuda.Stream()
         self._graphs = {}  # captured blocks, by buffers and parity (block(graph=True))
@@ -161,8 +169,9 @@ class BlockPipeline:
             self._pooled[key] = t
         return t
 
-    def _stage1(self, q_merge, k_cache, ctx, slot, stream, sms=0):
-        """Stage 1 (per key, or over the pooled blocks) into cand[slot]."""
+    def _stage1(self, q_merge, k_cache, ctx, slot, stream, sms=0, v_cache=None):
+        """Stage 1 (per key, or over the pooled blocks) into cand[slot]; with
+        prefetch, then the candidates' K (and V) rows into staged[slot]."""
         if self.Bk:
             H.check(H.lib().herald_select_stage1_blocks(
                 self.d, H.ptr(q_merge), H.ptr(self.pooled(k_cache, ctx)), H.ptr(ctx), self.Bk,
@@ -174,17 +183,22 @@ class BlockPipeline:
                 self._n_cand[slot], self._ws_sel, self.ws_bytes, sms,
                 H.stream_handle(stream)))
         if self.prefetch:
+            if self.prefetch_v and v_cache is None:
+                raise ValueError("prefetch='kv' stages the candidates' V rows: pass v_cache")
             H.check(H.lib().herald_stage_candidates(
-                self.d, H.ptr(k_cache), self._cand[slot], self._n_cand[slot], self.C,
-                H.ptr(self.staged[slot]), H.stream_handle(stream)))
+                self.d, H.ptr(k_cache), H.ptr(v_cache) if self.prefetch_v else None,
+                self._cand[slot], self._n_cand[slot], self.C, H.ptr(self.staged[slot]),
+                H.ptr(self.staged_v[slot]) if self.prefetch_v else None,
+                H.stream_handle(stream)))
 
-    def prime(self, q_merge, k_cache, ctx, slot: int = 0):
-        """Stage 1 for the first block (no predecessor: its own queries)."""
-        self._stage1(q_merge, k_cache, ctx, slot, self._den())
+    def prime(self, q_merge, k_cache, ctx, slot: int = 0, v_cache=None):
+        """Stage 1 for the first block (no predecessor: its own queries);
+        v_cache is needed with prefetch='kv'."""
+        self._stage1(q_merge, k_cache, ctx, slot, self._den(), v_cache=v_cache)
 
     def block(self, i: int, q_steps, block_k, block_v, k_cache, v_cache, ctx, out,
               next_k_cache=None, advance: bool = True, overlap: bool = True,
-              graph: bool = False):
+              graph: bool = False, next_v_cache=None):
         """Runs block i: q_steps/block_k/block_v hold the T steps' inputs,
         out[t] receives step t's attention output.
 
@@ -194,25 +208,26 @@ class BlockPipeline:
         launch of host time instead of ~T+5 library calls."""
         if not graph:
             return self._block(i, q_steps, block_k, block_v, k_cache, v_cache, ctx, out,
-                               next_k_cache, advance, overlap)
+                               next_k_cache, advance, overlap, next_v_cache)
         torch = self.torch
         P_ = H.ptr
         key = (i % 2, P_(q_steps), P_(block_k), P_(block_v), P_(k_cache), P_(v_cache), P_(ctx),
-               P_(out), P_(k_cache if next_k_cache is None else next_k_cache), bool(advance),
+               P_(out), P_(k_cache if next_k_cache is None else next_k_cache),
+               P_(v_cache if next_v_cache is None else next_v_cache), bool(advance),
                bool(overlap))
         g = self._graphs.get(key)
         if g is not None:
             g.replay()
             return
         self._block(i, q_steps, block_k, block_v, k_cache, v_cache, ctx, out, next_k_cache,
-                    advance, overlap)
+                    advance, overlap, next_v_cache)
         g = torch.cuda.CUDAGraph()
         den = torch.cuda.current_stream()
         cap = torch.cuda.Stream()
         cap.wait_stream(den)
         with torch.cuda.graph(g, stream=cap):
             self._block(i, q_steps, block_k, block_v, k_cache, v_cache, ctx, out, next_k_cache,
-                        advance, overlap)
+                        advance, overlap, next_v_cache)
         den.wait_stream(cap)
         self._graphs[key] = g
 
@@ -220,10 +235,11 @@ class BlockPipeline:
         return scan_sms(self.d, k_cache, self.sel_sms)
 
     def _block(self, i, q_steps, block_k, block_v, k_cache, v_cache, ctx, out, next_k_cache,
-               advance, overlap):
+               advance, overlap, next_v_cache=None):
         den, sel = self._den(), self.sel
         cur, nxt = i % 2, (i + 1) % 2
         nk = k_cache if next_k_cache is None else next_k_cache
+        nv = v_cache if next_v_cache is None else next_v_cache
         d, P, L, chk = self.d, self.P, H.lib(), H.check
         hd, hs = H.stream_handle(den), H.stream_handle(sel)
         q0, qstep = H.ptr(q_steps), H.step_bytes(q_steps)
@@ -234,7 +250,12 @@ class BlockPipeline:
         wd, wb = self._ws_den, self.ws_bytes
         # stage 1 for block i+1 can start now: block i's queries exist
         sel.wait_stream(den)
-        if self.prefetch:  # stage 2 over the prefetched candidate rows, then the gather
+        if self.prefetch_v:  # stage 2 and the gather over the prefetched K and V rows
+            chk(L.herald_select_stage2_staged_gather(
+                d, q0, H.ptr(self.staged[cur]), H.ptr(self.staged_v[cur]), kc, vc, cx,
+                self._cand[cur], self._n_cand[cur], self.C, self.K, self.S, self.W, P,
+                self._idx, self._n_sel, pk, pv, wd, wb, hd))
+        elif self.prefetch:  # stage 2 over the prefetched K rows, then the gather
             chk(L.herald_select_stage2_staged(d, q0, H.ptr(self.staged[cur]), cx,
                                               self._cand[cur], self._n_cand[cur], self.C,
                                               self.K, self.S, self.W, P, self._idx, self._n_sel,
@@ -245,7 +266,7 @@ class BlockPipeline:
                                               self._n_cand[cur], self.C, self.K, self.S, self.W,
                                               P, self._idx, self._n_sel, pk, pv, wd, wb, hd))
         self._stage1(q_steps, nk, ctx, nxt, sel if overlap else den,
-                     self._scan_sms(nk) if overlap else 0)
+                     self._scan_sms(nk) if overlap else 0, v_cache=nv)
         for t in range(self.T):
             if t == self.T - 1 and overlap:
                 den.wait_stream(sel)  # stage 1 reads the cache the last step appends to

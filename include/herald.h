@@ -105,22 +105,36 @@ herald_status herald_select_stage1(herald_dims dims, const uint16_t *q_merge,
 
 /* Stage 2 split around the host link for a cache in mapped pinned host
  * memory ([EA]: the subset crosses the link once per block; the candidates'
- * K rows can cross it while the previous block is denoised):
- * herald_stage_candidates copies the candidates' K rows by slot,
+ * rows can cross it while the previous block is denoised):
+ * herald_stage_candidates copies the candidates' K rows (and V rows, when
+ *   v_cache and staged_v are given; both null = K only) by slot,
  *   staged_k[n][g][c] = k_cache[n][g][cand[n][g][c]] for c < n_cand, zero
- *   rows after, bf16 [N][Hkv][C][d] device out;
+ *   rows after, bf16 [N][Hkv][C][d] device out (staged_v likewise);
+ *   HERALD_ERR_INVALID_ARG if exactly one of v_cache, staged_v is null;
  * herald_select_stage2_staged is herald_select_stage2 reading the candidate
- * rows from staged_k (the same idx and n_sel, bit for bit).  The cache rows
- * below ctx_len must not change between the two calls. */
+ *   rows from staged_k (the same idx and n_sel, bit for bit);
+ * herald_select_stage2_staged_gather is herald_select_stage2_gather with the
+ *   candidate rows read from staged_k / staged_v: the refine reads staged_k,
+ *   and the pool rows taken from the top-K come from the staged rows, those
+ *   of the sink and local window from the cache -- the same idx, n_sel and
+ *   pool, bit for bit, with only the sink and local rows crossing the link.
+ * The cache rows below ctx_len must not change between the calls. */
 herald_status herald_stage_candidates(herald_dims dims, const uint16_t *k_cache,
-                                      const int32_t *cand, const int32_t *n_cand, int C,
-                                      uint16_t *staged_k, void *stream);
+                                      const uint16_t *v_cache, const int32_t *cand,
+                                      const int32_t *n_cand, int C, uint16_t *staged_k,
+                                      uint16_t *staged_v, void *stream);
 herald_status herald_select_stage2_staged(herald_dims dims, const uint16_t *q_block,
                                           const uint16_t *staged_k, const int32_t *ctx_len,
                                           const int32_t *cand, const int32_t *n_cand, int C,
                                           int K, int sink, int local, int P_max, int32_t *idx,
                                           int32_t *n_sel, void *ws, size_t ws_bytes,
                                           void *stream);
+herald_status herald_select_stage2_staged_gather(
+    herald_dims dims, const uint16_t *q_block, const uint16_t *staged_k, const uint16_t *staged_v,
+    const uint16_t *k_cache, const uint16_t *v_cache, const int32_t *ctx_len, const int32_t *cand,
+    const int32_t *n_cand, int C, int K, int sink, int local, int P_max, int32_t *idx,
+    int32_t *n_sel, uint16_t *pool_k, uint16_t *pool_v, void *ws, size_t ws_bytes,
+    void *stream);
 
 /* Block-granular stage 1 ([SPD]: InfLLM-V2 selects whole blocks of the
  * context; here stage 1's rule is applied to blocks, not keys).  The cache is

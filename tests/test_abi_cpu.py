@@ -140,6 +140,24 @@ def test_block_stage1_and_staging_argument_errors():
         H.herald_select_stage2_staged(d, ok, None, ok, ok, ok, 256, 128, 16, 64, 208, ok, ok, ok,
                                       ws)
     assert e.value.status == 1
+    # the V rows need both the cache and the staging buffer
+    for vc, sv in [(ok, None), (None, ok)]:
+        with pytest.raises(H.HeraldError) as e:
+            H.herald_stage_candidates(d, ok, ok, ok, 256, ok, v_cache=vc, staged_v=sv)
+        assert e.value.status == 1, (vc, sv)
+    # stage 2 + gather over staged rows: every pointer is required
+    args = [ok, ok, ok, ok, ok, ok, ok, ok]  # q, staged_k, staged_v, k, v, ctx, cand, n_cand
+    for miss in range(len(args)):
+        a = list(args)
+        a[miss] = None
+        with pytest.raises(H.HeraldError) as e:
+            H.herald_select_stage2_staged_gather(d, *a, 256, 128, 16, 64, 208, ok, ok, ok, ok,
+                                                 ok, ws)
+        assert e.value.status == 1, miss
+    with pytest.raises(H.HeraldError) as e:   # K > C
+        H.herald_select_stage2_staged_gather(d, *args, 256, 300, 16, 64, 400, ok, ok, ok, ok, ok,
+                                             ws)
+    assert e.value.status == 1
 
 
 def test_status_strings():

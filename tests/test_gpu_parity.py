@@ -418,7 +418,7 @@ def test_host_resident_cache_matches_device_cache(w):
     r.gather()
     torch.cuda.synchronize()
     idx_dev, ns_dev = r.idx.clone(), r.n_sel.clone()
-    pk_dev = r.pool_k.clone()
+    pk_dev, pv_dev = r.pool_k.clone(), r.pool_v.clone()
     kh = torch.from_numpy(r.x["k_cache"].view(np.int16)).pin_memory()
     vh = torch.from_numpy(r.x["v_cache"].view(np.int16)).pin_memory()
     w_ = r.w
@@ -450,6 +450,49 @@ def test_host_resident_cache_matches_device_cache(w):
     assert r.error_word() == 0
     assert torch.equal(idx_dev, r.idx) and torch.equal(ns_dev, r.n_sel)
     assert torch.equal(pk_dev, r.pool_k)
+    # the candidates' K and V rows staged beforehand, then stage 2 and the
+    # gather over them: the same selection and pool, bit for bit
+    staged_v = torch.full_like(staged, 99)
+    H.herald_stage_candidates(r.d, kh, r.cand, r.n_cand, w_.C, staged, v_cache=vh,
+                              staged_v=staged_v)
+    torch.cuda.synchronize()
+    cand, nc = r.cand.cpu().numpy(), r.n_cand.cpu().numpy()
+    vx = r.x["v_cache"].view(np.int16)
+    sv = staged_v.cpu().numpy()
+    for n in range(w_.N):
+        for g in range(w_.Hkv):
+            c = int(nc[n, g])
+            np.testing.assert_array_equal(sv[n, g, :c], vx[n, g, cand[n, g, :c]])
+            assert (sv[n, g, c:] == 0).all()
+    r.pool_k.fill_(7)
+    r.pool_v.fill_(7)
+    H.herald_select_stage2_staged_gather(r.d, r.q_steps[0], staged, staged_v, kh, vh, r.ctx,
+                                         r.cand, r.n_cand, w_.C, w_.K, w_.S, w_.W, r.P, r.idx,
+                                         r.n_sel, r.pool_k, r.pool_v, r.ws)
+    torch.cuda.synchronize()
+    assert r.error_word() == 0
+    assert torch.equal(idx_dev, r.idx) and torch.equal(ns_dev, r.n_sel)
+    assert torch.equal(pk_dev, r.pool_k) and torch.equal(pv_dev, r.pool_v)
+    # the top-K rows come from the staged rows, the sink and local rows from
+    # the cache: with the staged values overwritten, exactly the rows at
+    # positions in [S, L - W) carry the new value
+    staged_v.fill_(5)
+    r.pool_v.fill_(7)
+    H.herald_select_stage2_staged_gather(r.d, r.q_steps[0], staged, staged_v, kh, vh, r.ctx,
+                                         r.cand, r.n_cand, w_.C, w_.K, w_.S, w_.W, r.P, r.idx,
+                                         r.n_sel, r.pool_k, r.pool_v, r.ws)
+    torch.cuda.synchronize()
+    idx, ns, pv = r.idx.cpu().numpy(), r.n_sel.cpu().numpy(), r.pool_v.cpu().numpy()
+    for n in range(w_.N):
+        L = int(r.x["ctx"][n])
+        for g in range(w_.Hkv):
+            m = int(ns[n, g])
+            pos = idx[n, g, :m]
+            mid = (pos >= w_.S) & (pos < L - w_.W)
+            assert mid.any() and (~mid).any()
+            assert (pv[n, g, :m][mid] == 5).all()
+            np.testing.assert_array_equal(pv[n, g, :m][~mid], vx[n, g, pos[~mid]])
+            assert (pv[n, g, m:] == 0).all()
 
 
 @pytest.mark.parametrize("w", [QWEN_32K], ids=lambda w: w.name)

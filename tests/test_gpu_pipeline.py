@@ -20,14 +20,15 @@ from helpers import ATTN_ATOL, bf16_dev_to_f64, dev, f64
 @pytest.mark.parametrize("overlap,graph,T,Bk,host", [
     (True, False, 2, 0, False), (False, False, 2, 0, False), (True, True, 2, 0, False),
     (True, False, 1, 0, False), (True, False, 2, 16, False), (True, True, 2, 32, False),
-    (True, False, 2, 16, True)])
+    (True, False, 2, 16, "k"), (True, True, 2, 16, "kv")])
 def test_three_blocks_match_oracle_schedule(overlap, graph, T, Bk, host):
     """graph=True: every block's inputs are copied into the same buffers, so
     block 2 replays the CUDA graph captured for block 0 (same parity).
     T=1: the only denoising step also appends the block.  Bk > 0: stage 1
     over the cache's pooled blocks of Bk keys, refreshed after each append.
     host: the cache in pinned host memory, the next block's candidate rows
-    prefetched beside the denoising steps."""
+    prefetched beside the denoising steps ("k": K rows for stage 2; "kv": K
+    and V rows, the top-K pool rows gathered from them)."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     nb = 3
@@ -43,8 +44,8 @@ def test_three_blocks_match_oracle_schedule(overlap, graph, T, Bk, host):
     else:
         k, v = dev(x0["k_cache"]), dev(x0["v_cache"])
     ctx = dev(x0["ctx"])
-    pipe = BlockPipeline(d, w.C, w.K, w.S, w.W, w.P, w.T, blocks=Bk, prefetch=host)
-    pipe.prime(dev(x0["q_merge"]), k, ctx)
+    pipe = BlockPipeline(d, w.C, w.K, w.S, w.W, w.P, w.T, blocks=Bk, prefetch=host or False)
+    pipe.prime(dev(x0["q_merge"]), k, ctx, v_cache=v)
     got = []
     fixed = None
     for i, xb in enumerate(blocks):
