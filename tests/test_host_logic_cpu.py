@@ -1,6 +1,6 @@
 """Host-side scheduling logic that needs no GPU: the flags of a block's
-denoising steps, the SM budget of the background scan, and how the bench
-groups timed blocks into CUDA graphs."""
+denoising steps, the SM budget of the background scan, how the bench groups
+timed blocks into CUDA graphs, and the pipeline's option checks."""
 import pytest
 
 import bench
@@ -51,3 +51,12 @@ def test_blocks_per_graph_divides_the_timed_steps(steps, g):
     assert bench.blocks_per_graph(_Layer(), steps) == g
     assert steps % g == 0 and g <= 8
     assert bench.blocks_per_graph(_Stack(), steps) == 1
+
+
+@pytest.mark.parametrize("kw", [dict(prefetch="v"), dict(prefetch="kvv"), dict(blocks=48)])
+def test_pipeline_rejects_bad_options_before_allocating(kw):
+    """An unknown prefetch mode, or a candidate count C that is not a whole
+    number of blocks, is refused before any device memory is touched."""
+    d = H.dims_of(TINY)
+    with pytest.raises(ValueError):
+        P.BlockPipeline(d, TINY.C, TINY.K, TINY.S, TINY.W, TINY.P, TINY.T, **kw)
