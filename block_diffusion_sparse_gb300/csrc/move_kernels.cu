@@ -20,7 +20,8 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
 
 // grid (ceil(P_max / rows_per_cta), N*Hkv), block 256; D/8 threads per row,
 // one 16-byte chunk each.  With vc == nullptr only K rows are copied (the
-// stage-2 staging of candidate rows from a host-resident cache).  With src,
+// staging of candidate K rows from a host-resident cache; the staging of K
+// and V rows passes both).  With src,
 // a row whose src entry is a candidate slot s >= 0 is read from the rows
 // staged by slot (sk, sv: [N*Hkv][C][D]) instead of the cache.
 template <int D>
