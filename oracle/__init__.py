@@ -3,9 +3,10 @@
 Only the tests, the smoke check and the bench's CPU-baseline / reference leg
 may import this package.  The product (the CUDA library and its binding)
 never does, and it shares no code with it.  `herald_oracle.c` holds the
-arithmetic, written step by step from the pages (HERALD v3 abstract, HERALD
-early abstract, SparDA method section); this module only compiles it with gcc
-and marshals numpy arrays through ctypes.
+arithmetic of the steps, written step by step from the pages (HERALD v3
+abstract, HERALD early abstract, SparDA method section); this module compiles
+it with gcc, marshals numpy arrays through ctypes, and states the variants
+built on those steps (block-granular stage 1, adaptive budget) in numpy.
 """
 from __future__ import annotations
 
@@ -117,6 +118,41 @@ def select_final(ctx, L_max, cand, n_cand, s2, K, S, W, P=None):
     idx = np.empty((N, Hkv, P), np.int32); ns = np.empty((N, Hkv), np.int32)
     _load().oracle_select_final(N, Hkv, int(L_max), _p(cx), _p(c), _p(nc), _p(s),
                                 C_, int(K), int(S), int(W), int(P), _p(idx), _p(ns))
+    return idx, ns
+
+
+def adaptive_budget(s2, n_cand, tau, K_min, K_max):
+    """Per-block budget from the first denoising step (MAGE author page,
+    abstract: the first step predicts how much budget the block needs; the
+    mechanism is not given).  Reading: the budget of (n, g) is the smallest k
+    whose k largest stage-2 scores hold a fraction tau of the scores' total
+    (the stage-2 scores of the first step's queries are their attention mass
+    per candidate), then clamped to [K_min, K_max].  Returns K_b [N, Hkv]."""
+    s, nc = _f64(s2), _i32(n_cand)
+    N, Hkv, _ = s.shape
+    kb = np.zeros((N, Hkv), np.int32)
+    for n in range(N):
+        for g in range(Hkv):
+            m = int(nc[n, g])
+            x = np.sort(np.maximum(s[n, g, :m], 0.0))[::-1]
+            cum = np.cumsum(x)
+            hit = np.nonzero(cum >= tau * (cum[-1] if m else 0.0))[0]
+            k = int(hit[0]) + 1 if len(hit) else m
+            kb[n, g] = max(K_min, min(K_max, min(k, m)))
+    return kb
+
+
+def select_final_per_head(ctx, L_max, cand, n_cand, s2, K_b, S, W, P):
+    """Step 5 with a budget of its own per (n, g): K_b [N, Hkv]."""
+    c = _i32(cand)
+    N, Hkv, _ = c.shape
+    idx = np.empty((N, Hkv, P), np.int32); ns = np.empty((N, Hkv), np.int32)
+    cx, nc, s = _i32(ctx), _i32(n_cand), _f64(s2)
+    for n in range(N):
+        for g in range(Hkv):
+            i, m = select_final(cx[n:n + 1], L_max, c[n:n + 1, g:g + 1], nc[n:n + 1, g:g + 1],
+                                s[n:n + 1, g:g + 1], int(K_b[n, g]), S, W, P)
+            idx[n, g], ns[n, g] = i[0, 0], m[0, 0]
     return idx, ns
 
 

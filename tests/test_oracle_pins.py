@@ -442,3 +442,61 @@ def test_block_candidates_expand_whole_blocks_ascending():
     r = oracle.stage1_blocks(qbar, k, ctx, Bk, 16)
     assert r["n_cand"].tolist() == [[270, 270]]
     assert (r["cand"][0, :, :270] == np.arange(270)).all()
+
+
+# --------------------------------------------------------------------------
+# adaptive budget (the first step's attention mass decides the block's K)
+
+def test_adaptive_budget_is_the_smallest_subset_holding_the_mass():
+    """Brute force over every subset of a few candidates: the budget is the
+    size of the smallest subset whose scores reach tau of the total; zero
+    scores, ragged n_cand and the clamps behave as stated."""
+    rng = np.random.default_rng(91)
+    N, Hkv, C = 2, 3, 7
+    s2 = rng.random((N, Hkv, C)) ** 3
+    s2[0, 1, 2] = s2[0, 1, 5] = 0.0                 # zero mass never helps
+    nc = np.array([[7, 7, 4], [1, 6, 7]], np.int32)
+    for tau in (0.3, 0.5, 0.8, 0.95, 1.0):
+        kb = oracle.adaptive_budget(s2, nc, tau, 0, C)
+        for n in range(N):
+            for g in range(Hkv):
+                m = int(nc[n, g])
+                x = list(s2[n, g, :m])
+                tot = sum(x)
+                want = next(k for k in range(1, m + 1)
+                            if any(sum(sub) >= tau * tot
+                                   for sub in itertools.combinations(x, k)))
+                assert kb[n, g] == want, (tau, n, g)
+    # tau = 1: every non-zero score is needed, the zeros are not
+    assert oracle.adaptive_budget(s2, nc, 1.0, 0, C)[0, 1] == 5
+    # the clamps: never below K_min, never above K_max
+    assert (oracle.adaptive_budget(s2, nc, 0.01, 3, C) == 3).all()
+    assert (oracle.adaptive_budget(s2, nc, 1.0, 0, 2) <= 2).all()
+    # no candidates: the budget is K_min
+    assert oracle.adaptive_budget(s2, np.zeros((N, Hkv), np.int32), 0.5, 4, C).tolist() == \
+        [[4] * Hkv] * N
+
+
+def test_per_head_selection_with_one_budget_is_the_selection():
+    """select_final_per_head with the same K everywhere is select_final."""
+    rng = np.random.default_rng(92)
+    N, Hkv, C, L_max = 2, 2, 40, 200
+    cand = np.zeros((N, Hkv, C), np.int32)
+    for n in range(N):
+        for g in range(Hkv):
+            cand[n, g] = np.sort(rng.choice(np.arange(8, 180), size=C, replace=False))
+    nc = np.full((N, Hkv), C, np.int32); nc[1, 0] = 25
+    s2 = rng.random((N, Hkv, C))
+    ctx = np.array([200, 190], np.int32)
+    a = oracle.select_final(ctx, L_max, cand, nc, s2, 12, 4, 16, 40)
+    b = oracle.select_final_per_head(ctx, L_max, cand, nc, s2, np.full((N, Hkv), 12), 4, 16, 40)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    # a smaller budget for one head changes only that head, and keeps its top scores
+    kb = np.full((N, Hkv), 12); kb[0, 1] = 5
+    c = oracle.select_final_per_head(ctx, L_max, cand, nc, s2, kb, 4, 16, 40)
+    mid = lambda i, m, L: [p for p in i[:m] if 4 <= p < L - 16]
+    assert len(mid(c[0][0, 1], c[1][0, 1], 200)) == 5
+    top5 = set(cand[0, 1, np.argsort(-s2[0, 1], kind="stable")[:5]].tolist())
+    assert set(mid(c[0][0, 1], c[1][0, 1], 200)) == top5
+    for n, g in ((0, 0), (1, 0), (1, 1)):
+        assert np.array_equal(c[0][n, g], a[0][n, g])
