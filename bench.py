@@ -135,6 +135,7 @@ WORKLOADS = {"qwen": "QWEN_32K", "tiny": "TINY", "llama": "LLAMA_64K",
              "long-host": "LONG_128K_HOST", "stack": "QWEN_STACK"}
 _WORKLOAD = "qwen"
 _SELECTION = "merged"
+_BUDGET = None  # --budget TAU: the adaptive per-block budget (K_min = K/8)
 _PREFETCH = "kv"  # --prefetch: the candidate rows prefetched for a host-resident cache
 BLOCK_KEYS = 64  # keys per block of the block-granular stage 1 (--selection blocks)
 
@@ -212,7 +213,8 @@ class Bench:
                                   # the denoising steps (with the per-key stage 1 the
                                   # link is the scan's: 1,544 against 1,494 us)
                                   prefetch=(_PREFETCH if w.kv_on_host and _SELECTION == "blocks"
-                                            else False))
+                                            else False),
+                                  budget=None if _BUDGET is None else (w.K // 8, _BUDGET))
         self.out = torch.zeros((w.T, w.N, w.B, w.Hq, w.d), dtype=torch.int16, device="cuda")
         self.overlap = True
         # stage 1 of the first block (its own queries; no predecessor)
@@ -240,6 +242,15 @@ class Bench:
 
     def context_note(self) -> str:
         return "fixed: each step appends the block at the same position (ctx not advanced)"
+
+    def budget_note(self):
+        p = getattr(self, "pipe", None)
+        if getattr(p, "budget", None) is None:
+            return "fixed K"
+        ks = p.k_sel.cpu().numpy()
+        return {"tau": p.budget[1], "K_min": p.budget[0], "K_max": p.K,
+                "last_block_mean_K": float(ks.mean()), "last_block_K_range": [int(ks.min()),
+                                                                             int(ks.max())]}
 
     def prefetch_note(self) -> str:
         p = getattr(self, "pipe", None)
@@ -735,6 +746,7 @@ def run_ours(args, rank, world, dist):
                        "layers": w.layers, "l2": b.l2_note(), "context": b.context_note(),
                        "selection": _SELECTION,
                        "prefetch": b.prefetch_note(),
+                       "budget": b.budget_note(),
                        "timing": (f"CUDA-graph replay, {chunk} consecutive blocks per graph "
                                   f"(one graph launch per {chunk} blocks), CUDA events"
                                   if chunk > 1 else
@@ -854,16 +866,24 @@ def main():
                     help="merged: the two-stage selection (default); exact: every cached "
                          "position scored with the block's real queries (one stream); "
                          "blocks: stage 1 over 64-key block means")
+    ap.add_argument("--budget", type=float, default=None, metavar="TAU",
+                    help="per-key merged selection with an adaptive budget per block and KV "
+                         "head: the smallest K (at least K/8, at most K) whose top scores "
+                         "hold TAU of the first step's stage-2 mass")
     ap.add_argument("--prefetch", default="kv", choices=["k", "kv"],
                     help="host-resident cache with --selection blocks: the next block's "
                          "candidate rows copied beside the denoising steps -- K rows for "
                          "stage 2 (k), or K and V rows with the top-K pool rows gathered "
                          "from HBM (kv, default)")
     args = ap.parse_args()
-    global _WORKLOAD, _SELECTION, _PREFETCH
+    global _WORKLOAD, _SELECTION, _PREFETCH, _BUDGET
     _WORKLOAD = args.workload
     _SELECTION = args.selection
     _PREFETCH = args.prefetch
+    _BUDGET = args.budget
+    if _BUDGET is not None and (args.selection != "merged" or args.workload == "stack"
+                                or not 0.0 < _BUDGET <= 1.0):
+        ap.error("--budget takes a TAU in (0, 1], the merged selection and one layer")
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

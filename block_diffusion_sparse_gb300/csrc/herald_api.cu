@@ -246,12 +246,20 @@ herald_status run_stage1(const herald_dims& dm, const uint16_t* q_merge, const u
   return HERALD_OK;
 }
 
+// The adaptive budget of herald_select_stage2_adaptive, between the refine
+// and the top-K.
+struct BudgetArgs {
+  int K_min, K_max;
+  float tau;
+  int32_t* k_sel;
+};
+
 herald_status run_stage2(const herald_dims& dm, const uint16_t* q_block, const uint16_t* k_cache,
                          const int32_t* ctx_len, const int32_t* cand, const int32_t* n_cand,
                          int C, int K, int sink, int local, int P_max, int32_t* idx,
                          int32_t* n_sel, void* ws, const WsLayout& w, cudaStream_t st,
                          const PoolGather* gather, const uint16_t* staged_k = nullptr,
-                         int32_t* slot_out = nullptr) {
+                         int32_t* slot_out = nullptr, const BudgetArgs* budget = nullptr) {
   uint32_t* err = at<uint32_t>(ws, w.err);
   CUtensorMap qmap, qmap_all;
   const int G = dm.Hq / dm.Hkv;
@@ -290,8 +298,13 @@ herald_status run_stage2(const herald_dims& dm, const uint16_t* q_block, const u
                     "refine launch");
   }
   const int n_parts = refine_fused_ok(C) ? w.MT_tok : 1;
+  if (budget)
+    HERALD_TRY_CUDA(launch_budget(dm, n_cand, at<float>(ws, w.s2), n_parts, C, budget->K_min,
+                                  budget->K_max, budget->tau, budget->k_sel, st),
+                    "budget launch");
   HERALD_TRY_CUDA(launch_topk_union(dm, ctx_len, cand, n_cand, at<float>(ws, w.s2), n_parts, C, K,
-                                    sink, local, P_max, idx, n_sel, st, gather, slot_out),
+                                    sink, local, P_max, idx, n_sel, st, gather, slot_out,
+                                    budget ? budget->k_sel : nullptr),
                   "topk_union launch");
   return HERALD_OK;
 }
@@ -762,6 +775,38 @@ herald_status herald_select_stage2_staged_gather(
                                        k_cache, v_cache, pool_k, pool_v, st),
                   "staged gather launch");
   return HERALD_OK;
+}
+
+herald_status herald_select_stage2_adaptive(herald_dims dims, const uint16_t* q_block,
+                                           const uint16_t* k_cache, const int32_t* ctx_len,
+                                           const int32_t* cand, const int32_t* n_cand, int C,
+                                           int K_min, int K_max, float tau, int sink, int local,
+                                           int P_max, int32_t* idx, int32_t* n_sel,
+                                           int32_t* k_sel, void* ws, size_t ws_bytes,
+                                           void* stream) {
+  g_err[0] = 0;
+  HERALD_RET_IF(check_dims(dims));
+  HERALD_RET_IF(check_c(C));
+  HERALD_RET_IF(check_pmax(dims, P_max));
+  HERALD_RET_IF(check_budget(C, K_max, sink, local, P_max));
+  if (K_min < 0 || K_min > K_max)
+    return fail(HERALD_ERR_INVALID_ARG, "K_min=%d must lie in [0, K_max=%d]", K_min, K_max);
+  if (!(tau > 0.f && tau <= 1.f))
+    return fail(HERALD_ERR_INVALID_ARG, "tau=%g must lie in (0, 1]", double(tau));
+  HERALD_CHECK_PTR(q_block);
+  HERALD_CHECK_PTR(k_cache);
+  HERALD_CHECK_PTR(ctx_len);
+  HERALD_CHECK_PTR(cand);
+  HERALD_CHECK_PTR(n_cand);
+  HERALD_CHECK_PTR(idx);
+  HERALD_CHECK_PTR(n_sel);
+  HERALD_CHECK_PTR(k_sel);
+  WsLayout w;
+  HERALD_RET_IF(check_ws(dims, C, P_max, ws, ws_bytes, &w));
+  const BudgetArgs b{K_min, K_max, tau, k_sel};
+  return run_stage2(dims, q_block, k_cache, ctx_len, cand, n_cand, C, K_max, sink, local, P_max,
+                    idx, n_sel, ws, w, static_cast<cudaStream_t>(stream), nullptr, nullptr,
+                    nullptr, &b);
 }
 
 herald_status herald_select(herald_dims dims, const uint16_t* q_merge, const uint16_t* q_block,

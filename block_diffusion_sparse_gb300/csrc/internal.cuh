@@ -175,12 +175,19 @@ struct PoolGather {
 // s2 holds n_parts partial score arrays of [N*Hkv][C], summed per candidate;
 // gather (optional) also fills the pool; slot_out (optional, [N*Hkv][P_max])
 // receives the candidate slot of every selected row taken from the top-K,
-// -1 for sink, local and padding rows.
+// -1 for sink, local and padding rows; k_seg (optional, [N*Hkv]) gives each
+// (n, g) a budget of its own, at most K.
 cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const int32_t* cand,
                               const int32_t* n_cand, const float* s2, int n_parts, int C, int K,
                               int S, int W, int P_max, int32_t* idx, int32_t* n_sel,
                               cudaStream_t st, const PoolGather* gather = nullptr,
-                              int32_t* slot_out = nullptr);
+                              int32_t* slot_out = nullptr, const int32_t* k_seg = nullptr);
+// The adaptive budget of every (n, g) from the summed stage-2 scores (same
+// partial layout as topk_union): the smallest k whose k largest scores hold
+// tau of their total, clamped to [K_min, K_max]; k_sel [N*Hkv] out.
+cudaError_t launch_budget(const herald_dims& dm, const int32_t* n_cand, const float* s2,
+                          int n_parts, int C, int K_min, int K_max, float tau, int32_t* k_sel,
+                          cudaStream_t st);
 // (name: the label the launch carries in traces)
 cudaError_t launch_gather(const herald_dims& dm, const int32_t* idx, const int32_t* n_sel,
                           int P_max, const uint16_t* k_cache, const uint16_t* v_cache,

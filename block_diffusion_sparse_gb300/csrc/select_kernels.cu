@@ -10,6 +10,7 @@
 //   topk_union    exact radix top-K of the stage-2 score, union with sink
 //                 and local windows (InfLLM-V2 decomposition in the SparDA
 //                 method section), ascending positions
+#include <climits>
 #include <cuda_bf16.h>
 
 #include "internal.cuh"
@@ -949,7 +950,7 @@ __global__ void __launch_bounds__(kTkThreads)
                       const int32_t* __restrict__ n_cand, const float* __restrict__ s2,
                       int n_parts, int Hkv, int L_max, int C, int K, int S, int W, int P_max,
                       int32_t* __restrict__ idx, int32_t* __restrict__ n_sel, PoolGather pg,
-                      int32_t* __restrict__ slot_out) {
+                      int32_t* __restrict__ slot_out, const int32_t* __restrict__ k_seg) {
   // [C] bit patterns of the threshold-bin members, then (with the gather)
   // [P_max] selected positions
   extern __shared__ uint32_t mem[];
@@ -967,7 +968,8 @@ __global__ void __launch_bounds__(kTkThreads)
   const int seg = blockIdx.x / copies, copy = blockIdx.x - seg * copies, n = seg / Hkv;
   const int L = min(max(ctx[n], 0), L_max);
   const int nc = min(max(n_cand[seg], 0), C);
-  const int Ke = min(K, nc);
+  // the budget: K, or this (n, g)'s own (at most K) when k_seg is given
+  const int Ke = min(k_seg ? min(max(k_seg[seg], 0), K) : K, nc);
   // slots per thread from C, not n_cand: the score loads need not wait for it
   const int E = (C + kTkThreads - 1) / kTkThreads;
   const int i0 = threadIdx.x * E;
@@ -1181,7 +1183,8 @@ __global__ void __launch_bounds__(kTkThreads)
 cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const int32_t* cand,
                               const int32_t* n_cand, const float* s2, int n_parts, int C, int K,
                               int S, int W, int P_max, int32_t* idx, int32_t* n_sel,
-                              cudaStream_t st, const PoolGather* gather, int32_t* slot_out) {
+                              cudaStream_t st, const PoolGather* gather, int32_t* slot_out,
+                              const int32_t* k_seg) {
   static_assert(kMaxC <= 16 * kTkThreads, "16 scores per thread cover every C");
   const PoolGather pg = gather ? *gather : PoolGather{nullptr, nullptr, nullptr, nullptr, 0, 1};
   const size_t smem = size_t(C) * 4 + (pg.pk ? size_t(P_max) * 4 : 0u);
@@ -1200,11 +1203,118 @@ cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const i
   if (C <= 4 * kTkThreads)
     HERALD_CHECK_LAUNCH(launch_k("topk_union_kernel", topk_union_kernel<4>, grid, kTkThreads, smem,
                                  st, ctx, cand, n_cand, s2, n_parts, dm.Hkv, dm.L_max, C, K, S, W,
-                                 P_max, idx, n_sel, pg, slot_out));
+                                 P_max, idx, n_sel, pg, slot_out, k_seg));
   else
     HERALD_CHECK_LAUNCH(launch_k("topk_union_kernel", topk_union_kernel<16>, grid, kTkThreads,
                                  smem, st, ctx, cand, n_cand, s2, n_parts, dm.Hkv, dm.L_max, C, K,
-                                 S, W, P_max, idx, n_sel, pg, slot_out));
+                                 S, W, P_max, idx, n_sel, pg, slot_out, k_seg));
+  return cudaGetLastError();
+}
+
+// ============================================================= budget
+// One CTA of 1024 threads per (n, g): the stage-2 scores of the n_cand valid
+// slots, summed over the row-tile partials exactly as topk_union sums them
+// (so both kernels see the same fp32 values), are sorted descending in shared
+// memory (bitonic, over the next power of two >= C, padded with zeros); a
+// block scan of the sorted scores gives the running mass, and the budget is
+// one past the first index whose running mass reaches tau times the total,
+// clamped to [K_min, K_max] (and to n_cand before the clamp).
+constexpr int kBudgetThreads = 1024;
+
+__global__ void __launch_bounds__(kBudgetThreads)
+    budget_kernel(const int32_t* __restrict__ n_cand, const float* __restrict__ s2, int n_parts,
+                  int C, int pow2, int K_min, int K_max, float tau, int32_t* __restrict__ k_sel) {
+  extern __shared__ uint32_t key[];  // [pow2] bit patterns of non-negative scores
+  __shared__ float wsum[kBudgetThreads / 32];
+  __shared__ int s_first;
+  griddep_enter();
+  const int seg = blockIdx.x;
+  const int nc = min(max(n_cand[seg], 0), C);
+  const float* sc = s2 + size_t(seg) * C;
+  const size_t part_stride = size_t(gridDim.x) * C;  // [part][N*Hkv][C]
+  for (int i = threadIdx.x; i < pow2; i += kBudgetThreads) {
+    float x = 0.f;
+    if (i < nc) {
+      int p = 0;
+      for (; p + 2 <= n_parts; p += 2) x += sc[p * part_stride + i] + sc[(p + 1) * part_stride + i];
+      if (p < n_parts) x += sc[p * part_stride + i];
+    }
+    key[i] = i < nc ? __float_as_uint(fmaxf(x, 0.f)) : 0u;
+  }
+  if (threadIdx.x == 0) s_first = INT_MAX;
+  __syncthreads();
+  // bitonic sort, descending (a non-negative float orders as its bit pattern)
+  for (int k = 2; k <= pow2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < pow2; i += kBudgetThreads) {
+        const int l = i ^ j;
+        if (l > i) {
+          const uint32_t a = key[i], b = key[l];
+          if ((i & k) == 0 ? a < b : a > b) {
+            key[i] = b;
+            key[l] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // thread t owns sorted slots [t*per, (t+1)*per): its sum, then a block scan
+  const int per = max(1, pow2 / kBudgetThreads);
+  const int b0 = threadIdx.x * per, b1 = min(b0 + per, pow2);
+  float local = 0.f;
+  for (int i = b0; i < b1; ++i) local += __uint_as_float(key[i]);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    float w = wsum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    wsum[lane] = w;
+  }
+  __syncthreads();
+  const float total = wsum[kBudgetThreads / 32 - 1];
+  const float target = tau * total;
+  float cum = (warp > 0 ? wsum[warp - 1] : 0.f) + (incl - local);
+  for (int i = b0; i < b1 && i < nc; ++i) {
+    cum += __uint_as_float(key[i]);
+    if (cum >= target) {
+      atomicMin(&s_first, i);
+      break;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int kb = s_first == INT_MAX ? nc : min(s_first + 1, nc);
+    k_sel[seg] = max(K_min, min(K_max, kb));
+  }
+}
+
+cudaError_t launch_budget(const herald_dims& dm, const int32_t* n_cand, const float* s2,
+                          int n_parts, int C, int K_min, int K_max, float tau, int32_t* k_sel,
+                          cudaStream_t st) {
+  int pow2 = 1;
+  while (pow2 < C) pow2 <<= 1;
+  const size_t smem = size_t(pow2) * 4;
+  static size_t attr_bytes = 0;
+  if (smem > attr_bytes) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(budget_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    attr_bytes = smem;
+  }
+  HERALD_CHECK_LAUNCH(launch_k("budget_kernel", budget_kernel, dm.N * dm.Hkv, kBudgetThreads, smem,
+                               st, n_cand, s2, n_parts, C, pow2, K_min, K_max, tau, k_sel));
   return cudaGetLastError();
 }
 

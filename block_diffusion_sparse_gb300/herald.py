@@ -27,7 +27,8 @@ EXPORTS = ("herald_workspace_size", "herald_status_string", "herald_last_error",
            "herald_select_stage2_noalloc", "herald_selftest_wait_timeout",
            "herald_workspace_size_exact", "herald_select_exact", "herald_pool_keys",
            "herald_select_stage1_blocks", "herald_stage_candidates",
-           "herald_select_stage2_staged", "herald_select_stage2_staged_gather")
+           "herald_select_stage2_staged", "herald_select_stage2_staged_gather",
+           "herald_select_stage2_adaptive")
 
 
 class HeraldError(RuntimeError):
@@ -98,6 +99,9 @@ def lib() -> C.CDLL:
         L.herald_stage_candidates.argtypes = [Dims, vp, vp, vp, vp, i32, vp, vp, vp]
         L.herald_select_stage2_staged.argtypes = [Dims, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                   i32, vp, vp, vp, sz, vp]
+        L.herald_select_stage2_adaptive.argtypes = [Dims, vp, vp, vp, vp, vp, i32, i32, i32,
+                                                    C.c_float, i32, i32, i32, vp, vp, vp, vp,
+                                                    sz, vp]
         L.herald_select_stage2_staged_gather.argtypes = [Dims, vp, vp, vp, vp, vp, vp, vp, vp,
                                                          i32, i32, i32, i32, i32, vp, vp, vp, vp,
                                                          vp, sz, vp]
@@ -282,6 +286,15 @@ def herald_select_stage2_staged_gather(d, q_block, staged_k, staged_v, k_cache, 
         d, _p(q_block), _p(staged_k), _p(staged_v), _p(k_cache), _p(v_cache), _p(ctx_len),
         _p(cand), _p(n_cand), int(C), int(K), int(sink), int(local), int(P_max), _p(idx),
         _p(n_sel), _p(pool_k), _p(pool_v), _p(ws), _nbytes(ws, ws_bytes), _s(stream)))
+
+
+def herald_select_stage2_adaptive(d, q_block, k_cache, ctx_len, cand, n_cand, C, K_min, K_max,
+                                  tau, sink, local, P_max, idx, n_sel, k_sel, ws=None,
+                                  ws_bytes=None, stream=None):
+    _check(lib().herald_select_stage2_adaptive(
+        d, _p(q_block), _p(k_cache), _p(ctx_len), _p(cand), _p(n_cand), int(C), int(K_min),
+        int(K_max), float(tau), int(sink), int(local), int(P_max), _p(idx), _p(n_sel),
+        _p(k_sel), _p(ws), _nbytes(ws, ws_bytes), _s(stream)))
 
 
 def herald_gather(d, idx, n_sel, P_max, k_cache, v_cache, pool_k, pool_v, stream=None):

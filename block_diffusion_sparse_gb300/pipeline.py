@@ -88,7 +88,7 @@ def step_flags(t: int, T: int, advance: bool) -> int:
 class BlockPipeline:
     def __init__(self, dims: H.Dims, C: int, K: int, S: int, W: int, P: int, T: int,
                  den_stream=None, sel_stream=None, sel_sms=None, exact: bool = False,
-                 blocks: int = 0, prefetch=False):
+                 blocks: int = 0, prefetch=False, budget=None):
         """blocks > 0: stage 1 selects C // blocks blocks of `blocks` keys
         over the cache's pooled block keys (herald_select_stage1_blocks),
         which the pipeline builds for each cache it meets and refreshes at
@@ -99,7 +99,10 @@ class BlockPipeline:
         memory, whose link the denoising steps leave idle.  prefetch="kv":
         the candidates' V rows too, and the gather reads the top-K rows from
         HBM (herald_select_stage2_staged_gather; only the sink and local
-        rows cross the link inside the step)."""
+        rows cross the link inside the step).  budget=(K_min, tau): each
+        block's K per KV head from its first step's stage-2 mass
+        (herald_select_stage2_adaptive, at most K; k_sel holds the last
+        block's budgets), then the gather."""
         import torch
         self.torch = torch
         self.Bk = int(blocks)
@@ -110,6 +113,9 @@ class BlockPipeline:
             raise ValueError(f"prefetch={prefetch!r}: False, True (= 'k') or 'kv'")
         self.prefetch = bool(prefetch)
         self.prefetch_v = prefetch == "kv"
+        if budget is not None and (prefetch or exact):
+            raise ValueError("the adaptive budget runs with the plain stage 2 only")
+        self.budget = None if budget is None else (int(budget[0]), float(budget[1]))
         # SMs the overlapped stage-1 scan may occupy (0: all)
         # None: background_sms for the cache each block reads
         self.sel_sms = None if sel_sms is None else int(sel_sms)
@@ -123,6 +129,7 @@ class BlockPipeline:
         self.n_cand = [torch.zeros(NG, dtype=torch.int32, device=dev) for _ in range(2)]
         self.idx = torch.full((*NG, P), -1, dtype=torch.int32, device=dev)
         self.n_sel = torch.zeros(NG, dtype=torch.int32, device=dev)
+        self.k_sel = torch.zeros(NG, dtype=torch.int32, device=dev)
         self.pool_k = [torch.zeros((*NG, P, dims.d), dtype=torch.int16, device=dev)
                        for _ in range(2)]
         self.pool_v = [torch.zeros_like(self.pool_k[0]) for _ in range(2)]
@@ -255,6 +262,12 @@ class BlockPipeline:
                 d, q0, H.ptr(self.staged[cur]), H.ptr(self.staged_v[cur]), kc, vc, cx,
                 self._cand[cur], self._n_cand[cur], self.C, self.K, self.S, self.W, P,
                 self._idx, self._n_sel, pk, pv, wd, wb, hd))
+        elif self.budget:  # stage 2 with each KV head's own budget, then the gather
+            chk(L.herald_select_stage2_adaptive(
+                d, q0, kc, cx, self._cand[cur], self._n_cand[cur], self.C, self.budget[0],
+                self.K, self.budget[1], self.S, self.W, P, self._idx, self._n_sel,
+                H.ptr(self.k_sel), wd, wb, hd))
+            chk(L.herald_gather(d, self._idx, self._n_sel, P, kc, vc, pk, pv, hd))
         elif self.prefetch:  # stage 2 over the prefetched K rows, then the gather
             chk(L.herald_select_stage2_staged(d, q0, H.ptr(self.staged[cur]), cx,
                                               self._cand[cur], self._n_cand[cur], self.C,

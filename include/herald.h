@@ -6,6 +6,8 @@
  *         Cooperative KV Cache Retrieval", arXiv 2606.21633 v3, abstract.
  *   [EA]  HERALD early abstract (mlsift.com, "KV cache offloading" listing).
  *   [SPD] SparDA summary (hyper.ai, arXiv 2606.04511), Method section.
+ *   [MG]  "MAGE: All-[MASK] Block Already Knows Where to Look in Diffusion
+ *         LLM", author page, abstract.
  *
  * One block of a block-diffusion LLM layer is decoded as:
  *   select (once per block)  ->  gather into a sparse pool  ->  T x attention.
@@ -135,6 +137,26 @@ herald_status herald_select_stage2_staged_gather(
     const int32_t *n_cand, int C, int K, int sink, int local, int P_max, int32_t *idx,
     int32_t *n_sel, uint16_t *pool_k, uint16_t *pool_v, void *ws, size_t ws_bytes,
     void *stream);
+
+/* herald_select_stage2 with a budget of its own per (sequence, KV head),
+ * predicted from the first denoising step ([MG]: the first step predicts
+ * the block's budget; the pages give no mechanism, so this is a reading):
+ *   k_sel[n][g] = the smallest k whose k largest stage-2 scores s2 hold a
+ *   fraction tau of their total over the n_cand valid slots (at most
+ *   n_cand), clamped to [K_min, K_max]; int32 [N][Hkv] device out;
+ * then step 5 with K = k_sel[n][g] for that (n, g): idx and n_sel as in
+ * herald_select_stage2.  The scores are summed and compared in fp32 on the
+ * device, so near the tau boundary k_sel may differ by a few from an exact
+ * computation.  Errors: HERALD_ERR_INVALID_ARG for K_min outside [0, K_max],
+ * tau outside (0, 1], K_max > C or K_max + sink + local > P_max, or a null
+ * pointer. */
+herald_status herald_select_stage2_adaptive(herald_dims dims, const uint16_t *q_block,
+                                           const uint16_t *k_cache, const int32_t *ctx_len,
+                                           const int32_t *cand, const int32_t *n_cand, int C,
+                                           int K_min, int K_max, float tau, int sink, int local,
+                                           int P_max, int32_t *idx, int32_t *n_sel,
+                                           int32_t *k_sel, void *ws, size_t ws_bytes,
+                                           void *stream);
 
 /* Block-granular stage 1 ([SPD]: InfLLM-V2 selects whole blocks of the
  * context; here stage 1's rule is applied to blocks, not keys).  The cache is

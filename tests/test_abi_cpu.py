@@ -154,6 +154,17 @@ def test_block_stage1_and_staging_argument_errors():
             H.herald_select_stage2_staged_gather(d, *a, 256, 128, 16, 64, 208, ok, ok, ok, ok,
                                                  ok, ws)
         assert e.value.status == 1, miss
+    # the adaptive budget: K_min in [0, K_max], tau in (0, 1], every pointer
+    for K_min, K_max, tau in [(-1, 128, 0.5), (129, 128, 0.5), (0, 128, 0.0), (0, 128, 1.5),
+                              (0, 128, float("nan")), (0, 300, 0.5)]:
+        with pytest.raises(H.HeraldError) as e:
+            H.herald_select_stage2_adaptive(d, ok, ok, ok, ok, ok, 256, K_min, K_max, tau, 16, 64,
+                                            400, ok, ok, ok, ok, ws)
+        assert e.value.status == 1, (K_min, K_max, tau)
+    with pytest.raises(H.HeraldError) as e:
+        H.herald_select_stage2_adaptive(d, ok, ok, ok, ok, ok, 256, 8, 128, 0.5, 16, 64, 208, ok,
+                                        ok, None, ok, ws)
+    assert e.value.status == 1
     with pytest.raises(H.HeraldError) as e:   # K > C
         H.herald_select_stage2_staged_gather(d, *args, 256, 300, 16, 64, 400, ok, ok, ok, ok, ok,
                                              ws)

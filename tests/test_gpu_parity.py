@@ -720,3 +720,45 @@ def test_pooled_keys_tail_refresh_after_appends():
     H.herald_pool_keys(r.d, r.k, r.ctx, Bk, full)
     torch.cuda.synchronize()
     assert torch.equal(pooled, full)
+
+
+@pytest.mark.parametrize("w", [c for c in CASES if c.name in
+                               ("g7-d128-ragged", "g4-d128-n2", "ctx-below-c",
+                                "c-above-4096-two-pass")], ids=lambda w: w.name)
+@pytest.mark.parametrize("tau", [0.3, 0.8])
+def test_adaptive_budget_stage2(w, tau):
+    """The per-(n, g) budget from the first step's stage-2 mass (the MAGE
+    author page's first-step budget prediction, in the reading stated with
+    the oracle): the device's budget is a valid one for the oracle's fp64
+    scores (its top-k mass reaches tau of the total, the top k-1 do not,
+    both within a relative 1e-3), within 2 of the oracle's, and the
+    selection with it matches the oracle's selection with the same budget."""
+    r = Run(w)
+    x = r.x
+    s1 = _oracle_stage1(x)
+    cand_o, nc_o = oracle.topc(s1, x["ctx"], w.C)
+    s2 = oracle.stage2_scores(f64(x["q_steps"][0]), f64(x["k_cache"]), cand_o, nc_o)
+    K_min, K_max = max(1, w.K // 8), w.K
+    k_sel = torch.full((w.N, w.Hkv), -7, dtype=torch.int32, device="cuda")
+    H.herald_select_stage2_adaptive(r.d, r.q_steps[0], r.k, r.ctx, dev(cand_o), dev(nc_o), w.C,
+                                    K_min, K_max, tau, w.S, w.W, r.P, r.idx, r.n_sel, k_sel,
+                                    r.ws)
+    torch.cuda.synchronize()
+    assert r.error_word() == 0
+    kb = k_sel.cpu().numpy()
+    kb_o = oracle.adaptive_budget(s2, nc_o, tau, K_min, K_max)
+    assert np.abs(kb.astype(int) - kb_o).max() <= 2, (kb, kb_o)
+    idx_o, ns_o = oracle.select_final_per_head(x["ctx"], w.L_max, cand_o, nc_o, s2, kb, w.S, w.W,
+                                               w.P)
+    idx, ns = r.idx.cpu().numpy(), r.n_sel.cpu().numpy()
+    for n in range(w.N):
+        for g in range(w.Hkv):
+            m, k = int(nc_o[n, g]), int(kb[n, g])
+            cum = np.cumsum(np.sort(s2[n, g, :m])[::-1])
+            if m and K_min < k < min(K_max, m):   # the budget was not clamped
+                target = tau * cum[-1]
+                assert cum[k - 1] >= target * (1 - 1e-3), (n, g, k)
+                assert k == 1 or cum[k - 2] < target * (1 + 1e-3), (n, g, k)
+            check_selection(idx[n, g], int(ns[n, g]), idx_o[n, g], int(ns_o[n, g]),
+                            cand_o[n, g], nc_o[n, g], s2[n, g], w.scaled(K=k), int(x["ctx"][n]),
+                            f"{w.name} tau={tau} n={n} g={g}")
