@@ -1212,100 +1212,174 @@ cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const i
 }
 
 // ============================================================= budget
-// One CTA of 1024 threads per (n, g): the stage-2 scores of the n_cand valid
-// slots, summed over the row-tile partials exactly as topk_union sums them
-// (so both kernels see the same fp32 values), are sorted descending in shared
-// memory (bitonic, over the next power of two >= C, padded with zeros); a
-// block scan of the sorted scores gives the running mass, and the budget is
-// one past the first index whose running mass reaches tau times the total,
+// One CTA of 1024 threads per (n, g).  The stage-2 scores of the n_cand
+// valid slots, summed over the row-tile partials exactly as topk_union sums
+// them (both kernels see the same fp32 values), go to shared memory as bit
+// patterns (a non-negative float orders as its pattern).  The budget is one
+// past the first sorted position whose running mass reaches tau times the
+// total; it is found without sorting, by a radix search from the top over
+// the 12 / 11 / 8-bit digits of the patterns with mass-weighted histograms:
+// each pass finds the bin where the mass above it (carried from the earlier
+// passes) plus its own reaches the target, and the last pass's bin is one
+// value t, of which ceil((target - mass above) / t) ties are taken.  Then
 // clamped to [K_min, K_max] (and to n_cand before the clamp).
 constexpr int kBudgetThreads = 1024;
 
+// Inclusive block scan of (mass, count) in thread order; totals in *tm, *tc.
+__device__ __forceinline__ void budget_scan(float& m, uint32_t& c, float* wm, uint32_t* wc,
+                                            float* tm, uint32_t* tc) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float ym = __shfl_up_sync(0xffffffffu, m, o);
+    const uint32_t yc = __shfl_up_sync(0xffffffffu, c, o);
+    if (lane >= o) {
+      m += ym;
+      c += yc;
+    }
+  }
+  if (lane == 31) {
+    wm[warp] = m;
+    wc[warp] = c;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float a = wm[lane];
+    uint32_t b = wc[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float ya = __shfl_up_sync(0xffffffffu, a, o);
+      const uint32_t yb = __shfl_up_sync(0xffffffffu, b, o);
+      if (lane >= o) {
+        a += ya;
+        b += yb;
+      }
+    }
+    wm[lane] = a;
+    wc[lane] = b;
+  }
+  __syncthreads();
+  if (warp > 0) {
+    m += wm[warp - 1];
+    c += wc[warp - 1];
+  }
+  *tm = wm[31];
+  *tc = wc[31];
+}
+
 __global__ void __launch_bounds__(kBudgetThreads)
     budget_kernel(const int32_t* __restrict__ n_cand, const float* __restrict__ s2, int n_parts,
-                  int C, int pow2, int K_min, int K_max, float tau, int32_t* __restrict__ k_sel) {
-  extern __shared__ uint32_t key[];  // [pow2] bit patterns of non-negative scores
-  __shared__ float wsum[kBudgetThreads / 32];
-  __shared__ int s_first;
+                  int C, int K_min, int K_max, float tau, int32_t* __restrict__ k_sel) {
+  extern __shared__ uint32_t key[];  // [C] bit patterns of the summed scores
+  __shared__ float hm[kHistBins];
+  __shared__ uint32_t hc[kHistBins];
+  __shared__ float wm[32];
+  __shared__ uint32_t wc[32];
+  __shared__ int s_bin;
+  __shared__ float s_run;
+  __shared__ uint32_t s_cnt;
   griddep_enter();
-  const int seg = blockIdx.x;
+  const int seg = blockIdx.x, tid = threadIdx.x;
   const int nc = min(max(n_cand[seg], 0), C);
   const float* sc = s2 + size_t(seg) * C;
   const size_t part_stride = size_t(gridDim.x) * C;  // [part][N*Hkv][C]
-  for (int i = threadIdx.x; i < pow2; i += kBudgetThreads) {
+  float part = 0.f;
+  for (int i = tid; i < nc; i += kBudgetThreads) {
     float x = 0.f;
-    if (i < nc) {
-      int p = 0;
-      for (; p + 2 <= n_parts; p += 2) x += sc[p * part_stride + i] + sc[(p + 1) * part_stride + i];
-      if (p < n_parts) x += sc[p * part_stride + i];
-    }
-    key[i] = i < nc ? __float_as_uint(fmaxf(x, 0.f)) : 0u;
+    int p = 0;
+    for (; p + 2 <= n_parts; p += 2) x += sc[p * part_stride + i] + sc[(p + 1) * part_stride + i];
+    if (p < n_parts) x += sc[p * part_stride + i];
+    key[i] = __float_as_uint(fmaxf(x, 0.f));
+    part += __uint_as_float(key[i]);
   }
-  if (threadIdx.x == 0) s_first = INT_MAX;
-  __syncthreads();
-  // bitonic sort, descending (a non-negative float orders as its bit pattern)
-  for (int k = 2; k <= pow2; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < pow2; i += kBudgetThreads) {
-        const int l = i ^ j;
-        if (l > i) {
-          const uint32_t a = key[i], b = key[l];
-          if ((i & k) == 0 ? a < b : a > b) {
-            key[i] = b;
-            key[l] = a;
-          }
+  float total;
+  uint32_t zero = 0u, n_unused;
+  budget_scan(part, zero, wm, wc, &total, &n_unused);
+  const float target = tau * total;
+  int kb = nc;
+  if (!(target > 0.f)) {
+    kb = min(1, nc);  // no mass: one key reaches it
+  } else {
+    float run = 0.f;     // mass of the values above the current prefix's bin
+    uint32_t cnt = 0;    // and their count
+    uint32_t prefix = 0;  // the digits fixed so far
+    for (int pass = 0; pass < 3; ++pass) {
+      const int shift = pass == 0 ? 19 : pass == 1 ? 8 : 0;
+      const int nb = pass == 0 ? 4096 : pass == 1 ? 2048 : 256;
+      const uint32_t fixed = pass == 0 ? 0u : pass == 1 ? 0xFFF80000u : 0xFFFFFF00u;
+      __syncthreads();  // the previous pass's readers of hm, hc and s_bin are done
+      for (int b = tid; b < nb; b += kBudgetThreads) {
+        hm[b] = 0.f;
+        hc[b] = 0u;
+      }
+      if (tid == 0) s_bin = -1;
+      __syncthreads();
+      for (int i = tid; i < nc; i += kBudgetThreads) {
+        const uint32_t v = key[i];
+        if ((v & fixed) == prefix) {
+          const int dgt = int((v >> shift) & uint32_t(nb - 1));
+          atomicAdd(&hm[dgt], __uint_as_float(v));
+          atomicAdd(&hc[dgt], 1u);
         }
       }
       __syncthreads();
+      // thread t owns bins [lo, hi); the mass of the bins above its range is
+      // the block total minus its inclusive prefix
+      const int per = nb >= kBudgetThreads ? nb / kBudgetThreads : 1;
+      const int lo = min(tid * per, nb), hi = min(lo + per, nb);
+      float lm = 0.f;
+      uint32_t lc = 0u;
+      for (int b = lo; b < hi; ++b) {
+        lm += hm[b];
+        lc += hc[b];
+      }
+      float tm;
+      uint32_t tcn;
+      budget_scan(lm, lc, wm, wc, &tm, &tcn);
+      float above = run + (tm - lm);
+      for (int b = hi - 1; b >= lo; --b) {
+        if (above < target && above + hm[b] >= target) {
+          atomicMax(&s_bin, b);  // rounding may let two ranges claim a crossing: the top one
+          break;
+        }
+        above += hm[b];
+      }
+      __syncthreads();
+      const int bin = s_bin;
+      if (bin < 0) {  // the target is not reached by rounding: every member is needed
+        kb = int(cnt + tcn);
+        break;
+      }
+      if (bin >= lo && bin < hi) {  // the owner recomputes the mass and count above it
+        float a = run + (tm - lm);
+        uint32_t ac = cnt + (tcn - lc);
+        for (int b = hi - 1; b > bin; --b) {
+          a += hm[b];
+          ac += hc[b];
+        }
+        s_run = a;
+        s_cnt = ac;
+      }
+      __syncthreads();
+      run = s_run;
+      cnt = s_cnt;
+      prefix |= uint32_t(bin) << shift;
+      if (pass == 2) {
+        const float t = __uint_as_float(prefix);
+        const uint32_t ties = hc[bin];
+        uint32_t take = t > 0.f ? uint32_t(ceilf((target - run) / t)) : 1u;
+        take = max(1u, min(take, ties));
+        kb = int(cnt + take);
+      }
     }
   }
-  // thread t owns sorted slots [t*per, (t+1)*per): its sum, then a block scan
-  const int per = max(1, pow2 / kBudgetThreads);
-  const int b0 = threadIdx.x * per, b1 = min(b0 + per, pow2);
-  float local = 0.f;
-  for (int i = b0; i < b1; ++i) local += __uint_as_float(key[i]);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) wsum[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    float w = wsum[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    wsum[lane] = w;
-  }
-  __syncthreads();
-  const float total = wsum[kBudgetThreads / 32 - 1];
-  const float target = tau * total;
-  float cum = (warp > 0 ? wsum[warp - 1] : 0.f) + (incl - local);
-  for (int i = b0; i < b1 && i < nc; ++i) {
-    cum += __uint_as_float(key[i]);
-    if (cum >= target) {
-      atomicMin(&s_first, i);
-      break;
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const int kb = s_first == INT_MAX ? nc : min(s_first + 1, nc);
-    k_sel[seg] = max(K_min, min(K_max, kb));
-  }
+  if (tid == 0) k_sel[seg] = max(K_min, min(K_max, min(kb, nc)));
 }
 
 cudaError_t launch_budget(const herald_dims& dm, const int32_t* n_cand, const float* s2,
                           int n_parts, int C, int K_min, int K_max, float tau, int32_t* k_sel,
                           cudaStream_t st) {
-  int pow2 = 1;
-  while (pow2 < C) pow2 <<= 1;
-  const size_t smem = size_t(pow2) * 4;
+  const size_t smem = size_t(C) * 4;
   static size_t attr_bytes = 0;
   if (smem > attr_bytes) {
     const cudaError_t e =
@@ -1314,7 +1388,7 @@ cudaError_t launch_budget(const herald_dims& dm, const int32_t* n_cand, const fl
     attr_bytes = smem;
   }
   HERALD_CHECK_LAUNCH(launch_k("budget_kernel", budget_kernel, dm.N * dm.Hkv, kBudgetThreads, smem,
-                               st, n_cand, s2, n_parts, C, pow2, K_min, K_max, tau, k_sel));
+                               st, n_cand, s2, n_parts, C, K_min, K_max, tau, k_sel));
   return cudaGetLastError();
 }
 
