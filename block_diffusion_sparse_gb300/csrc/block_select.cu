@@ -191,4 +191,6 @@ cudaError_t launch_expand_blocks(const herald_dims& dm, const int32_t* cand_b,
   return cudaGetLastError();
 }
 
+HERALD_DEBUG_WORD_READER(debug_take_blocks)
+
 }  // namespace herald

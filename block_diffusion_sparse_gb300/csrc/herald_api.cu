@@ -8,7 +8,9 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <map>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "../../include/herald.h"
@@ -358,6 +360,64 @@ herald_status encode_heads_map(const void* base, uint64_t tokens, int heads, int
 
 void set_last_error(const char* msg) { snprintf(g_err, sizeof g_err, "%s", msg); }
 
+herald_status check_stage2_args(const herald_dims& dims, int C, int K, int sink, int local,
+                                int P_max) {
+  HERALD_RET_IF(check_dims(dims));
+  HERALD_RET_IF(check_c(C));
+  HERALD_RET_IF(check_pmax(dims, P_max));
+  return check_budget(C, K, sink, local, P_max);
+}
+
+bool device_resident(const void* p) { return is_device_memory(p); }
+
+// herald_inject_launch_failure's state, per host thread: the number of
+// launches still to pass (-1: disarmed) and the error the next one returns
+thread_local int g_inject_after = -1;
+thread_local cudaError_t g_inject_error = cudaSuccess;
+
+cudaError_t injected_launch_error() {
+  if (g_inject_after < 0) return cudaSuccess;
+  if (g_inject_after-- > 0) return cudaSuccess;
+  return g_inject_error;  // this launch fails; the hook is now disarmed (-1)
+}
+
+cudaError_t ensure_smem(const void* fn, size_t bytes) {
+  // (a kernel's static shared memory counts against the default 48 KB too,
+  // so every nonzero dynamic amount is granted explicitly)
+  if (bytes == 0) return cudaSuccess;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  // a per-thread memo of recent grants in front of the shared record, so
+  // the steady state takes no lock
+  struct Memo {
+    const void* fn;
+    int dev;
+    size_t bytes;
+  };
+  constexpr int kMemo = 16;
+  thread_local Memo memo[kMemo] = {};
+  thread_local int next = 0;
+  for (const Memo& m : memo)
+    if (m.fn == fn && m.dev == dev && m.bytes >= bytes) return cudaSuccess;
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, size_t> granted;
+  size_t now;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    size_t& g = granted[{fn, dev}];
+    if (g < bytes) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+      if (e != cudaSuccess) return e;
+      g = bytes;
+    }
+    now = g;
+  }
+  memo[next] = Memo{fn, dev, now};
+  next = (next + 1) % kMemo;
+  return cudaSuccess;
+}
+
 void trace_before(cudaStream_t st, const char* name) {
   TraceState& t = g_trace;
   t.in_kernel = false;
@@ -424,6 +484,32 @@ const char* herald_status_string(herald_status s) {
 }
 
 const char* herald_last_error(void) { return g_err; }
+
+int herald_debug_build(void) {
+#ifdef HERALD_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+herald_status herald_debug_status(uint32_t* code) {
+  if (!code) return fail(HERALD_ERR_INVALID_ARG, "code is NULL");
+  *code = 0;
+#ifdef HERALD_DEBUG
+  HERALD_TRY_CUDA(cudaDeviceSynchronize(), "device synchronize");
+  *code = debug_take_select() | debug_take_tc() | debug_take_move() | debug_take_blocks();
+#endif
+  return HERALD_OK;
+}
+
+herald_status herald_inject_launch_failure(int after, int cuda_error) {
+  if (after >= 0 && cuda_error == 0)
+    return fail(HERALD_ERR_INVALID_ARG, "the injected error must be a CUDA error code");
+  g_inject_after = after < 0 ? -1 : after;
+  g_inject_error = static_cast<cudaError_t>(cuda_error);
+  return HERALD_OK;
+}
 
 herald_status herald_workspace_error(void* ws, void* stream, uint32_t* code) {
   HERALD_CHECK_PTR(ws);

@@ -14,6 +14,9 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "../../include/herald.h"
 #include "internal.cuh"
 
@@ -41,21 +44,32 @@ herald_status fail(herald_status s, const char* fmt, ...) {
 
 // Device address of g_stage2_scratch on the current device.  Resolved once
 // per device, with that device current; host code must not use the array's
-// name as an address.
+// name as an address.  Host threads that make their first calls at the
+// same time resolve it under one lock; later calls read the published
+// address without locking.
 herald_status scratch_address(unsigned char** out) {
-  static unsigned char* addr[64] = {nullptr};
+  constexpr int kMaxDevices = 64;
+  static std::atomic<unsigned char*> addr[kMaxDevices];
+  static std::mutex mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(HERALD_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-  if (dev < 0 || dev >= 64) return fail(HERALD_ERR_CUDA, "device ordinal %d out of range", dev);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_stage2_scratch);
-    if (e != cudaSuccess)
-      return fail(HERALD_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
-    addr[dev] = static_cast<unsigned char*>(p);
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(HERALD_ERR_CUDA, "device ordinal %d out of range", dev);
+  unsigned char* p = addr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    std::lock_guard<std::mutex> lock(mu);
+    p = addr[dev].load(std::memory_order_relaxed);
+    if (!p) {
+      void* q = nullptr;
+      e = cudaGetSymbolAddress(&q, g_stage2_scratch);
+      if (e != cudaSuccess)
+        return fail(HERALD_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+      p = static_cast<unsigned char*>(q);
+      addr[dev].store(p, std::memory_order_release);
+    }
   }
-  *out = addr[dev];
+  *out = p;
   return HERALD_OK;
 }
 
@@ -71,13 +85,9 @@ herald_status herald_select_stage2_noalloc(herald_dims dims, const uint16_t* q_b
                                            int K, int sink, int local, int P_max, int32_t* idx,
                                            int32_t* n_sel, void* stream) {
   set_last_error("");
-  // the same argument rules as herald_select_stage2; a workspace-free call
-  // validates through the workspace-size query (0 = unsupported shape)
-  if (herald_workspace_size(dims, C, P_max < 1 ? 1 : P_max) == 0)
-    return fail(HERALD_ERR_UNSUPPORTED_SHAPE, "unsupported shape or C");
-  if (P_max < 1 || K < 0 || sink < 0 || local < 0 || K > C ||
-      (long long)K + sink + local > P_max)
-    return fail(HERALD_ERR_INVALID_ARG, "need 0 <= K <= C and K+sink+local <= P_max");
+  // the argument rules of herald_select_stage2 (shapes, C, P_max, budget)
+  herald_status s = check_stage2_args(dims, C, K, sink, local, P_max);
+  if (s != HERALD_OK) return s;
   if (!aligned16(q_block) || !aligned16(k_cache) || !aligned16(ctx_len) || !aligned16(cand) ||
       !aligned16(n_cand) || !aligned16(idx) || !aligned16(n_sel))
     return fail(HERALD_ERR_INVALID_ARG, "a pointer is NULL or not 16-byte aligned");
@@ -97,9 +107,15 @@ herald_status herald_select_stage2_noalloc(herald_dims dims, const uint16_t* q_b
     return fail(HERALD_ERR_WORKSPACE_TOO_SMALL,
                 "these shapes need %zu bytes of scratch; the static scratch holds %zu",
                 need, kStaticScratchBytes);
+  // herald_select_stage2 stages a host-resident cache's candidate rows in
+  // its workspace before the refine; this call has no room for them
+  if (!device_resident(k_cache))
+    return fail(HERALD_ERR_INVALID_ARG,
+                "k_cache is not device memory: the workspace-free stage 2 takes a cache in "
+                "HBM only (use herald_select_stage2 for a host-resident cache)");
 
   unsigned char* base = nullptr;
-  herald_status s = scratch_address(&base);
+  s = scratch_address(&base);
   if (s != HERALD_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* err = reinterpret_cast<uint32_t*>(base + err_off);

@@ -93,6 +93,38 @@ inline WsLayout ws_layout(const herald_dims& dm, int C, int P_max) {
 // Sets the text returned by herald_last_error() on this host thread.
 void set_last_error(const char* msg);
 
+// The argument rules of herald_select_stage2 on shapes and counts (dims, C,
+// P_max, K/sink/local against C and P_max); the message of a failure is
+// set as herald_last_error().
+herald_status check_stage2_args(const herald_dims& dims, int C, int K, int sink, int local,
+                                int P_max);
+
+// Whether p points into device memory (else mapped host memory: read over
+// the host link).
+bool device_resident(const void* p);
+
+// Grants the kernel `fn` at least `bytes` of dynamic shared memory on the
+// current device.  The attribute belongs to that device's context, so each
+// grant is recorded per (kernel, device); safe to call from several host
+// threads.
+cudaError_t ensure_smem(const void* fn, size_t bytes);
+template <typename... A>
+inline cudaError_t ensure_smem(void (*fn)(A...), size_t bytes) {
+  return ensure_smem(reinterpret_cast<const void*>(fn), bytes);
+}
+
+// The debug build's device check words, one per translation unit with
+// kernels: each returns and clears its word (always 0 in release builds).
+uint32_t debug_take_select();
+uint32_t debug_take_tc();
+uint32_t debug_take_move();
+uint32_t debug_take_blocks();
+
+// A launch failure injected on the host (herald_inject_launch_failure, a
+// test hook of the error paths): returns the injected error for the launch
+// it was armed for on this host thread, cudaSuccess otherwise.
+cudaError_t injected_launch_error();
+
 // ---- kernel tracing: when enabled on this host thread, every kernel launch
 // is bracketed by two caller-owned CUDA events recorded on its stream.
 void trace_before(cudaStream_t st, const char* name);
@@ -113,6 +145,7 @@ cudaError_t launch_k(const char* name, void (*kernel)(KArgs...), dim3 grid, dim3
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (const cudaError_t ie = injected_launch_error()) return ie;
   trace_before(st, name);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
   trace_after(st);

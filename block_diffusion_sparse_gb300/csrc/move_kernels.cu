@@ -42,7 +42,9 @@ __global__ void __launch_bounds__(256)
     // the index buffer either way, and its entry is used only below n_sel
     const int pos = idx[size_t(seg) * P_max + row];
     const int s = src ? src[size_t(seg) * P_max + row] : -1;
-    const int ns = min(max(n_sel[seg], 0), P_max);
+    const int ns_raw = n_sel[seg];
+    debug_flag(ns_raw < 0 || ns_raw > P_max, DEV_BAD_COUNT);
+    const int ns = min(max(ns_raw, 0), P_max);
     uint4 kv = make_uint4(0, 0, 0, 0), vv = kv;
     if (row < ns) {
       if (s >= 0 && s < C) {  // a candidate row staged in HBM by slot
@@ -53,6 +55,8 @@ __global__ void __launch_bounds__(256)
         const size_t off = (size_t(seg) * L_max + pos) * D + c * 8;
         kv = ld_nc_v4(kc + off);
         if (vc) vv = ld_nc_v4(vc + off);
+      } else {
+        debug_flag(true, DEV_BAD_INDEX);  // a selected row outside the cache
       }
     }
     const size_t dst = (size_t(seg) * P_max + row) * D + c * 8;
@@ -130,7 +134,10 @@ __global__ void __launch_bounds__(kAppendThreads)
   __shared__ int L0;
   griddep_enter();
   const int n = blockIdx.x;
-  if (threadIdx.x == 0) L0 = min(max(ctx[n], 0), L_max);
+  if (threadIdx.x == 0) {
+    debug_flag(ctx[n] < 0 || ctx[n] > L_max, DEV_BAD_COUNT);
+    L0 = min(max(ctx[n], 0), L_max);
+  }
   __syncthreads();
   append_block_rows<kAppendBatch>(bk, bv, n, B, Hkv, d, L_max, L0, kc, vc, threadIdx.x,
                                   kAppendThreads);
@@ -145,5 +152,7 @@ cudaError_t launch_append(const herald_dims& dm, const uint16_t* block_k, const 
                                       k_cache, v_cache, advance));
   return cudaGetLastError();
 }
+
+HERALD_DEBUG_WORD_READER(debug_take_move)
 
 }  // namespace herald

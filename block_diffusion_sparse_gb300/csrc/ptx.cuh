@@ -21,6 +21,46 @@ enum : uint32_t {
   DEV_TIMEOUT_MMA = 2,   // a tcgen05 commit wait ran out
 };
 
+// Checks of the debug build (compiled with -DHERALD_DEBUG): a kernel compares
+// the indices and counts it reads or writes -- candidate and selected
+// positions against the cache's rows or the context length, selection rows
+// against P_max, context lengths against [0, L_max] -- with their ranges
+// and sets a bit of its translation unit's debug word on a violation
+// (herald_debug_status reads and clears them).  The access itself is
+// skipped or clamped as in every build: a check never traps.  Release
+// builds compile the checks out.
+enum : uint32_t {
+  DEV_BAD_INDEX = 0x10,  // a position outside the cache rows or the context
+  DEV_BAD_COUNT = 0x20,  // a count or context length outside its range
+};
+#ifdef HERALD_DEBUG
+static __device__ uint32_t g_debug_word;  // one per translation unit
+#endif
+HERALD_DEV void debug_flag(bool bad, uint32_t code) {
+#ifdef HERALD_DEBUG
+  if (bad) atomicOr(&g_debug_word, code);
+#else
+  (void)bad;
+  (void)code;
+#endif
+}
+// Defines the host function `fn` that returns and clears this translation
+// unit's debug word (0 in release builds).  The caller synchronises first.
+#ifdef HERALD_DEBUG
+#define HERALD_DEBUG_WORD_READER(fn)                                     \
+  uint32_t fn() {                                                        \
+    uint32_t v = 0;                                                      \
+    if (cudaMemcpyFromSymbol(&v, g_debug_word, sizeof v) != cudaSuccess) \
+      return DEV_BAD_COUNT | DEV_BAD_INDEX;                              \
+    const uint32_t z = 0;                                                \
+    if (v) cudaMemcpyToSymbol(g_debug_word, &z, sizeof z);               \
+    return v;                                                            \
+  }
+#else
+#define HERALD_DEBUG_WORD_READER(fn) \
+  uint32_t fn() { return 0; }
+#endif
+
 // ~1 s bound on any single wait (globaltimer is in ns).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 

@@ -433,24 +433,15 @@ static cudaError_t launch_scan_t(const CUtensorMap* kmap, const CUtensorMap* bma
                                  const uint16_t* kc, const float* qbar, const int32_t* ctx,
                                  const herald_dims& dm, float* logits, float2* part1,
                                  const WsLayout& w, uint32_t* err, int num_sms, cudaStream_t st) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(scan_tc_kernel<D, G>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         TcScanCfg<D>::kSmem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(scan_cc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             ScanCfg<D>::kSmem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
   const int segs = dm.N * dm.Hkv;
   if (kmap && bmap) {
+    HERALD_CHECK_LAUNCH(ensure_smem(scan_tc_kernel<D, G>, TcScanCfg<D>::kSmem));
     const int total = segs * w.tiles128;
     const int grid = scan_grid(dm, w, true, num_sms);
     HERALD_CHECK_LAUNCH(launch_k("scan_tc_kernel", scan_tc_kernel<D, G>, grid, kTcScanThreads, TcScanCfg<D>::kSmem, st, 
         *kmap, *bmap, ctx, dm.Hkv, dm.L_max, w.tiles128, total, w.L_pad, logits, part1, err));
   } else {
+    HERALD_CHECK_LAUNCH(ensure_smem(scan_cc_kernel<D, G>, ScanCfg<D>::kSmem));
     const int total = segs * w.tiles_per_seg;
     const int grid = scan_grid(dm, w, false, num_sms);
     HERALD_CHECK_LAUNCH(launch_k("scan_cc_kernel", scan_cc_kernel<D, G>, grid, kScanWarps * 32, ScanCfg<D>::kSmem, st, 
@@ -754,6 +745,7 @@ __global__ void __launch_bounds__(kSelThreads)
   griddep_enter();
   const int seg = blockIdx.x, n = seg / Hkv;
   const int L = min(max(ctx[n], 0), L_max);
+  debug_flag(threadIdx.x == 0 && (ctx[n] < 0 || ctx[n] > L_max), DEV_BAD_COUNT);
   const int Ce = min(C, L);
   int32_t* out = cand + size_t(seg) * C;
   const uint32_t* sv = reinterpret_cast<const uint32_t*>(s1 + size_t(seg) * L_pad);
@@ -967,6 +959,7 @@ __global__ void __launch_bounds__(kTkThreads)
   const int copies = pg.pk ? pg.copies : 1;
   const int seg = blockIdx.x / copies, copy = blockIdx.x - seg * copies, n = seg / Hkv;
   const int L = min(max(ctx[n], 0), L_max);
+  debug_flag(threadIdx.x == 0 && (ctx[n] < 0 || ctx[n] > L_max), DEV_BAD_COUNT);
   const int nc = min(max(n_cand[seg], 0), C);
   // the budget: K, or this (n, g)'s own (at most K) when k_seg is given
   const int Ke = min(k_seg ? min(max(k_seg[seg], 0), K) : K, nc);
@@ -1138,6 +1131,7 @@ __global__ void __launch_bounds__(kTkThreads)
   // row `slot` of the selection holds position v, taken from candidate slot
   // src (-1: a sink, local or padding row)
   auto put = [&](int slot, int32_t v, int32_t src) {
+    debug_flag(v < -1 || v >= L, DEV_BAD_INDEX);  // a selected position past the context
     if (to_global) {
       out[slot] = v;
       if (so) so[slot] = src;
@@ -1147,13 +1141,18 @@ __global__ void __launch_bounds__(kTkThreads)
 #pragma unroll
   for (int k = 0; k < kPer; ++k)
     if ((keep_mask >> k) & 1u) {
-      if (sink_end + int(at) < P_max) put(sink_end + at, pk[k], i0 + k);
+      if (sink_end + int(at) < P_max)
+        put(sink_end + at, pk[k], i0 + k);
+      else
+        debug_flag(true, DEV_BAD_COUNT);  // a selection row past P_max
       ++at;
     }
   for (int j = threadIdx.x; j < sink_end; j += kTkThreads) put(j, j, -1);
   for (int j = local_begin + threadIdx.x; j < L; j += kTkThreads)
     if (sink_end + int(n_mid) + (j - local_begin) < P_max)
       put(sink_end + n_mid + (j - local_begin), j, -1);
+    else
+      debug_flag(true, DEV_BAD_COUNT);
   const int total = min(P_max, sink_end + int(n_mid) + (L - local_begin));
   for (int s = total + threadIdx.x; s < P_max; s += kTkThreads) put(s, -1, -1);
   if (to_global && threadIdx.x == 0) n_sel[seg] = total;
@@ -1188,16 +1187,8 @@ cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const i
   static_assert(kMaxC <= 16 * kTkThreads, "16 scores per thread cover every C");
   const PoolGather pg = gather ? *gather : PoolGather{nullptr, nullptr, nullptr, nullptr, 0, 1};
   const size_t smem = size_t(C) * 4 + (pg.pk ? size_t(P_max) * 4 : 0u);
-  static size_t attr_bytes = 0;  // dynamic shared memory granted so far
-  if (smem > attr_bytes) {
-    cudaError_t e = cudaFuncSetAttribute(topk_union_kernel<4>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(topk_union_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(smem));
-    if (e != cudaSuccess) return e;
-    attr_bytes = smem;
-  }
+  HERALD_CHECK_LAUNCH(C <= 4 * kTkThreads ? ensure_smem(topk_union_kernel<4>, smem)
+                                          : ensure_smem(topk_union_kernel<16>, smem));
   const int grid = dm.N * dm.Hkv * (pg.pk ? pg.copies : 1);
   // the fewest registers that hold C scores over 1024 threads
   if (C <= 4 * kTkThreads)
@@ -1267,11 +1258,25 @@ __device__ __forceinline__ void budget_scan(float& m, uint32_t& c, float* wm, ui
   *tc = wc[31];
 }
 
+// The budget's bin masses are accumulated as unsigned 64-bit fixed point
+// (2^-40 units; a score is at most B*G <= 256, so C <= 16384 of them stay
+// below 2^62): integer atomics add in any order to the same sum, so the
+// budget of an input is the same on every run.
+constexpr float kMassScale = 1099511627776.0f;        // 2^40
+constexpr float kMassUnit = 1.0f / 1099511627776.0f;  // 2^-40
+__device__ __forceinline__ unsigned long long mass_fixed(float x) {
+  return __float2ull_rz(x * kMassScale);
+}
+__device__ __forceinline__ float mass_float(unsigned long long m) {
+  return __ull2float_rn(m) * kMassUnit;
+}
+
 __global__ void __launch_bounds__(kBudgetThreads)
     budget_kernel(const int32_t* __restrict__ n_cand, const float* __restrict__ s2, int n_parts,
                   int C, int K_min, int K_max, float tau, int32_t* __restrict__ k_sel) {
-  extern __shared__ uint32_t key[];  // [C] bit patterns of the summed scores
-  __shared__ float hm[kHistBins];
+  // dynamic: [C] bit patterns of the summed scores, then the bin masses
+  extern __shared__ __align__(16) uint32_t key[];
+  unsigned long long* hm = reinterpret_cast<unsigned long long*>(key + ((C + 3) & ~3));
   __shared__ uint32_t hc[kHistBins];
   __shared__ float wm[32];
   __shared__ uint32_t wc[32];
@@ -1309,7 +1314,7 @@ __global__ void __launch_bounds__(kBudgetThreads)
       const uint32_t fixed = pass == 0 ? 0u : pass == 1 ? 0xFFF80000u : 0xFFFFFF00u;
       __syncthreads();  // the previous pass's readers of hm, hc and s_bin are done
       for (int b = tid; b < nb; b += kBudgetThreads) {
-        hm[b] = 0.f;
+        hm[b] = 0ull;
         hc[b] = 0u;
       }
       if (tid == 0) s_bin = -1;
@@ -1318,7 +1323,7 @@ __global__ void __launch_bounds__(kBudgetThreads)
         const uint32_t v = key[i];
         if ((v & fixed) == prefix) {
           const int dgt = int((v >> shift) & uint32_t(nb - 1));
-          atomicAdd(&hm[dgt], __uint_as_float(v));
+          atomicAdd(&hm[dgt], mass_fixed(__uint_as_float(v)));
           atomicAdd(&hc[dgt], 1u);
         }
       }
@@ -1330,7 +1335,7 @@ __global__ void __launch_bounds__(kBudgetThreads)
       float lm = 0.f;
       uint32_t lc = 0u;
       for (int b = lo; b < hi; ++b) {
-        lm += hm[b];
+        lm += mass_float(hm[b]);
         lc += hc[b];
       }
       float tm;
@@ -1338,11 +1343,12 @@ __global__ void __launch_bounds__(kBudgetThreads)
       budget_scan(lm, lc, wm, wc, &tm, &tcn);
       float above = run + (tm - lm);
       for (int b = hi - 1; b >= lo; --b) {
-        if (above < target && above + hm[b] >= target) {
+        const float mb = mass_float(hm[b]);
+        if (above < target && above + mb >= target) {
           atomicMax(&s_bin, b);  // rounding may let two ranges claim a crossing: the top one
           break;
         }
-        above += hm[b];
+        above += mb;
       }
       __syncthreads();
       const int bin = s_bin;
@@ -1354,7 +1360,7 @@ __global__ void __launch_bounds__(kBudgetThreads)
         float a = run + (tm - lm);
         uint32_t ac = cnt + (tcn - lc);
         for (int b = hi - 1; b > bin; --b) {
-          a += hm[b];
+          a += mass_float(hm[b]);
           ac += hc[b];
         }
         s_run = a;
@@ -1379,17 +1385,14 @@ __global__ void __launch_bounds__(kBudgetThreads)
 cudaError_t launch_budget(const herald_dims& dm, const int32_t* n_cand, const float* s2,
                           int n_parts, int C, int K_min, int K_max, float tau, int32_t* k_sel,
                           cudaStream_t st) {
-  const size_t smem = size_t(C) * 4;
-  static size_t attr_bytes = 0;
-  if (smem > attr_bytes) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(budget_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
-    attr_bytes = smem;
-  }
+  // the scores' bit patterns, then kHistBins fixed-point bin masses
+  const size_t smem = size_t((C + 3) & ~3) * 4 + size_t(kHistBins) * 8;
+  HERALD_CHECK_LAUNCH(ensure_smem(budget_kernel, smem));
   HERALD_CHECK_LAUNCH(launch_k("budget_kernel", budget_kernel, dm.N * dm.Hkv, kBudgetThreads, smem,
                                st, n_cand, s2, n_parts, C, K_min, K_max, tau, k_sel));
   return cudaGetLastError();
 }
+
+HERALD_DEBUG_WORD_READER(debug_take_select)
 
 }  // namespace herald

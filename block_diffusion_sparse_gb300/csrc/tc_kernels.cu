@@ -132,6 +132,7 @@ static cudaError_t launch_cluster(const char* name, void (*kernel)(KArgs...), di
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
+  if (const cudaError_t ie = injected_launch_error()) return ie;
   trace_before(st, name);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
   trace_after(st);
@@ -191,8 +192,10 @@ __global__ void __launch_bounds__(kTcThreads)
   for (int r = threadIdx.x; r < kRefineChunk; r += kTcThreads)
     pos[r] = c0 + r < nc ? (cand ? cd[c0 + r] : c0 + r) : -1;
   // positions outside the cache (a caller error) read as zero rows
-  for (int r = threadIdx.x; r < kRefineChunk; r += kTcThreads)
+  for (int r = threadIdx.x; r < kRefineChunk; r += kTcThreads) {
+    debug_flag(c0 + r < nc && (pos[r] < 0 || pos[r] >= L_max), DEV_BAD_INDEX);
     if (pos[r] >= L_max) pos[r] = -1;
+  }
   __syncthreads();
   load_rows_sw128<D>(Ks, kRefineChunk, kRefineChunk, kc, [&](int r) -> const uint16_t* {
     const int p = pos[r];
@@ -342,8 +345,10 @@ __global__ void __launch_bounds__(kTcThreads)
   const uint32_t tbase = tmem_base;
 
   const int32_t* cd = cand ? cand + size_t(seg) * C : nullptr;  // null: row = slot
-  for (int r = threadIdx.x; r < kRefineRows2; r += kTcThreads)
+  for (int r = threadIdx.x; r < kRefineRows2; r += kTcThreads) {
     pos[r] = c0 + r >= nc ? -1 : !cand ? c0 + r : cd[c0 + r] < L_max ? cd[c0 + r] : -1;
+    debug_flag(c0 + r < nc && cand && (cd[c0 + r] < 0 || cd[c0 + r] >= L_max), DEV_BAD_INDEX);
+  }
   __syncthreads();
   load_rows_sw128<D>(Ks, kRefineRows2, kRefineRows2, kc, [&](int r) -> const uint16_t* {
     const int p = pos[r];
@@ -485,6 +490,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int r = threadIdx.x + k * kTcThreads;
     if (r < cpc) {
       const int p = r < ncv ? (cand ? pr[k] : c0 + r) : -1;
+      debug_flag(r < ncv && (p < 0 || p >= L_max), DEV_BAD_INDEX);  // a candidate past the cache
       pos[r] = (p >= 0 && p < L_max) ? p : -1;
     }
   }
@@ -669,17 +675,8 @@ static cudaError_t launch_refine_two_pass(const herald_dims& dm, const uint16_t*
                                           const CUtensorMap& qmap, const CUtensorMap& qmap_all,
                                           int bpt, float scale, cudaStream_t st) {
   const int segs = dm.N * dm.Hkv;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(refine_pass1_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Ref1Cfg<D>::kSmem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(refine_pass2_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Ref2Cfg<D>::kSmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  HERALD_CHECK_LAUNCH(ensure_smem(refine_pass1_kernel<D>, Ref1Cfg<D>::kSmem));
+  HERALD_CHECK_LAUNCH(ensure_smem(refine_pass2_kernel<D>, Ref2Cfg<D>::kSmem));
   HERALD_CHECK_LAUNCH(launch_k("refine_pass1_kernel", refine_pass1_kernel<D>,
                                dim3(w.n_chunks, w.MT_tok, segs), kTcThreads, Ref1Cfg<D>::kSmem,
                                st, qmap, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv, dm.L_max, C,
@@ -706,25 +703,15 @@ cudaError_t launch_refine(const herald_dims& dm, const uint16_t* k_cache, const 
     const int bpt = kTileM / (dm.Hq / dm.Hkv);
     if (!qmap) return cudaErrorInvalidValue;
     if (dm.d == 128) {
-      static bool attr = false;
-      if (!attr) {
-        e = cudaFuncSetAttribute(refine_fused_kernel<128>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, FuseCfg<128>::kSmem);
-        if (e != cudaSuccess) return e;
-        attr = true;
-      }
+      e = ensure_smem(refine_fused_kernel<128>, FuseCfg<128>::kSmem);
+      if (e != cudaSuccess) return e;
       return launch_cluster("refine_fused_kernel", refine_fused_kernel<128>,
                             dim3(kFuseCtas, w.MT_tok, segs), kFuseCtas, FuseCfg<128>::kSmem, st,
                             *qmap, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv, dm.L_max, C, bpt,
                             cpc, scale, s2, err);
     }
-    static bool attr64 = false;
-    if (!attr64) {
-      e = cudaFuncSetAttribute(refine_fused_kernel<64>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, FuseCfg<64>::kSmem);
-      if (e != cudaSuccess) return e;
-      attr64 = true;
-    }
+    e = ensure_smem(refine_fused_kernel<64>, FuseCfg<64>::kSmem);
+    if (e != cudaSuccess) return e;
     return launch_cluster("refine_fused_kernel", refine_fused_kernel<64>,
                           dim3(kFuseCtas, w.MT_tok, segs), kFuseCtas, FuseCfg<64>::kSmem, st,
                           *qmap, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv, dm.L_max, C, bpt, cpc,
@@ -1310,6 +1297,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   }
   const int nkp = min(max(min(max(n_sel[seg], 0), P_max) - k0, 0), kpc);  // valid pool keys
+  debug_flag(threadIdx.x == 0 && (n_sel[seg] < 0 || n_sel[seg] > P_max), DEV_BAD_COUNT);
   const bool any = nkp > 0 || has_blk;
   // The fused append (app.bk set): per sequence, the 8 CTAs of the cluster
   // of the first row tile of KV head 0 copy the block's rows of every KV
@@ -1319,6 +1307,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const bool appender = app.bk != nullptr && mt == 0 && g == 0;
   int L0 = 0;
   if (appender) {
+    debug_flag(threadIdx.x == 0 && (app.ctx[n] < 0 || app.ctx[n] > L_max), DEV_BAD_COUNT);
     L0 = min(max(app.ctx[n], 0), L_max);
     append_block_rows<1>(app.bk, app.bv, n, B, Hkv, D, L_max, L0, app.kc, app.vc,
                          int(rank) * kTcThreads + threadIdx.x, kPoolCtas * kTcThreads);
@@ -1719,20 +1708,9 @@ static cudaError_t launch_attn_split(const herald_dims& dm, const uint16_t* q,
                                      const WsLayout& w, float* opart, float2* ml, uint32_t* err,
                                      cudaStream_t st) {
   const int segs = dm.N * dm.Hkv;
-  cudaError_t e;
-  static bool attr = false;
-  if (!attr) {
-    e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             AttnCfg<D>::kSmem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_cluster_kernel<D, kClusterCtas>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, AttnClCfg<D>::kSmem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_cluster_kernel<D, kClusterCtasMax>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, AttnClCfg<D>::kSmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  HERALD_CHECK_LAUNCH(ensure_smem(attn_kernel<D>, AttnCfg<D>::kSmem));
+  HERALD_CHECK_LAUNCH(ensure_smem(attn_cluster_kernel<D, kClusterCtas>, AttnClCfg<D>::kSmem));
+  HERALD_CHECK_LAUNCH(ensure_smem(attn_cluster_kernel<D, kClusterCtasMax>, AttnClCfg<D>::kSmem));
   if (w.splits <= 2 * kClusterCtas && !force_split()) {
     // 16-CTA clusters (one key tile per CTA) only if the whole launch fits
     // on the device at once; otherwise 8-CTA clusters with two tiles each
@@ -1770,13 +1748,8 @@ static cudaError_t launch_attn_t(const herald_dims& dm, const uint16_t* q, const
   if (maps && !force_split()) {
     const int kpc = attn_pool_kpc(P_max);
     const uint32_t smem = pool_smem(D, kpc, (dm.B + 15) & ~15).total;
-    static uint32_t attr_bytes = 0;  // dynamic shared memory granted so far
-    if (smem > attr_bytes) {
-      e = cudaFuncSetAttribute(attn_pool_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               int(smem));
-      if (e != cudaSuccess) return e;
-      attr_bytes = smem;
-    }
+    e = ensure_smem(attn_pool_kernel<D>, smem);
+    if (e != cudaSuccess) return e;
     const int tiles = cdiv(dm.B, maps->bpt);
     // early loads pay only when every CTA of the grid is resident at once:
     // with a second wave they measured slower (on the 4 x 64K layer)
@@ -1805,5 +1778,7 @@ cudaError_t launch_attn(const herald_dims& dm, const uint16_t* q, const uint16_t
   return launch_attn_t<64>(dm, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale, w,
                            opart, ml, err, maps, settled, app, st);
 }
+
+HERALD_DEBUG_WORD_READER(debug_take_tc)
 
 }  // namespace herald

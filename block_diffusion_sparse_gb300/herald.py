@@ -11,7 +11,12 @@ import ctypes as C
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libherald.so")
+RELEASE_LIB = os.path.join(_HERE, "_build", "libherald.so")
+DEBUG_LIB = os.path.join(_HERE, "_build_debug", "libherald.so")
+# HERALD_LIB=debug selects the debug build (device checks of indices and
+# counts); any other value is taken as the library's path
+LIB_PATH = {"": RELEASE_LIB, "debug": DEBUG_LIB}.get(os.environ.get("HERALD_LIB", ""),
+                                                      os.environ.get("HERALD_LIB", ""))
 
 HERALD_OK = 0
 # flags of herald_denoise_attn_ex (include/herald.h)
@@ -28,7 +33,8 @@ EXPORTS = ("herald_workspace_size", "herald_status_string", "herald_last_error",
            "herald_workspace_size_exact", "herald_select_exact", "herald_pool_keys",
            "herald_select_stage1_blocks", "herald_stage_candidates",
            "herald_select_stage2_staged", "herald_select_stage2_staged_gather",
-           "herald_select_stage2_adaptive")
+           "herald_select_stage2_adaptive", "herald_debug_build", "herald_debug_status",
+           "herald_inject_launch_failure")
 
 
 class HeraldError(RuntimeError):
@@ -99,6 +105,10 @@ def lib() -> C.CDLL:
         L.herald_stage_candidates.argtypes = [Dims, vp, vp, vp, vp, i32, vp, vp, vp]
         L.herald_select_stage2_staged.argtypes = [Dims, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                   i32, vp, vp, vp, sz, vp]
+        L.herald_debug_build.argtypes = []
+        L.herald_debug_build.restype = i32
+        L.herald_debug_status.argtypes = [C.POINTER(C.c_uint32)]
+        L.herald_inject_launch_failure.argtypes = [i32, i32]
         L.herald_select_stage2_adaptive.argtypes = [Dims, vp, vp, vp, vp, vp, i32, i32, i32,
                                                     C.c_float, i32, i32, i32, vp, vp, vp, vp,
                                                     sz, vp]
@@ -185,6 +195,26 @@ def herald_workspace_size(d: Dims, C_: int, P_max: int) -> int:
 
 def herald_status_string(status: int) -> str:
     return lib().herald_status_string(int(status)).decode()
+
+
+def herald_debug_build() -> bool:
+    """Whether the loaded library is the debug build (device checks)."""
+    return bool(lib().herald_debug_build())
+
+
+def herald_debug_status() -> int:
+    """The debug build's device check word (waits for the device, then
+    reads and clears it); 0 in release builds."""
+    code = C.c_uint32(0)
+    _check(lib().herald_debug_status(C.byref(code)))
+    return int(code.value)
+
+
+def herald_inject_launch_failure(after: int, cuda_error: int = 719):
+    """Test hook: the launch after `after` more launches on this host
+    thread fails with `cuda_error` (default cudaErrorLaunchFailure); a
+    negative `after` disarms it."""
+    _check(lib().herald_inject_launch_failure(int(after), int(cuda_error)))
 
 
 def herald_workspace_error(ws, stream=None) -> int:

@@ -80,6 +80,28 @@ const char *herald_status_string(herald_status s);
 /* Detail of the last error raised on this host thread ("" if none). */
 const char *herald_last_error(void);
 
+/* The debug build (compiled with -DHERALD_DEBUG) checks, on the device, the
+ * indices and counts its kernels read and write: candidate and selected
+ * positions against the cache rows and the context length (idx < ctx_len),
+ * selection rows against P_max, n_sel in [0, P_max], ctx_len values in
+ * [0, L_max].  A failed check sets a bit in a device check word and the
+ * access is skipped or clamped as in every build; nothing traps.
+ * herald_debug_build() returns 1 in that build, 0 otherwise.
+ * herald_debug_status() waits for the whole device, then returns and clears
+ * the check word in *code: 0 = every check passed, bit 0x10 = an index out
+ * of range, bit 0x20 = a count or context length out of range (always 0 in
+ * release builds).  The word is shared by every stream and thread. */
+int herald_debug_build(void);
+herald_status herald_debug_status(uint32_t *code);
+
+/* Test hook of the host-side error paths: after `after` further kernel
+ * launches by this host thread, the next launch does not happen and
+ * returns the CUDA error code `cuda_error` instead, which the calling entry
+ * point reports as HERALD_ERR_CUDA with the launch named in
+ * herald_last_error().  The hook then disarms itself; after < 0 disarms it
+ * at once.  cuda_error must be nonzero when arming. */
+herald_status herald_inject_launch_failure(int after, int cuda_error);
+
 /* Synchronously reads and clears the device error word of a workspace
  * (0 = no kernel gave up on a wait; 1 = a copy wait, 2 = a tensor-core wait
  * ran out).  Synchronises `stream` first. */
@@ -243,6 +265,11 @@ herald_status herald_select(herald_dims dims, const uint16_t *q_merge, const uin
  *   that device current); make that first call before any stream capture.
  *   All calls share the array: calls that can overlap on the GPU (other
  *   streams, other host threads) race and must be serialised by the caller.
+ *   k_cache must be device memory: a cache in mapped host memory, whose
+ *   candidate rows herald_select_stage2 stages in its workspace first, is
+ *   rejected with HERALD_ERR_INVALID_ARG.  The other argument rules are
+ *   herald_select_stage2's.  Host threads may make their first calls at the
+ *   same time (the address is resolved under a lock).
  *   Device-side wait timeouts are recorded in the array, not reported.
  *   Nothing is allocated or freed by this call. */
 herald_status herald_select_stage2_noalloc(herald_dims dims, const uint16_t *q_block,

@@ -176,3 +176,37 @@ def test_status_strings():
     for s in range(5):
         assert H.herald_status_string(s)
     assert H.herald_status_string(99) == "unknown status"
+
+
+def test_an_injected_launch_failure_is_reported_as_a_cuda_error():
+    """The host-side error path of a failed launch, without a GPU: the hook
+    makes the gather's launch return cudaErrorLaunchFailure (719), which the
+    entry point reports as HERALD_ERR_CUDA naming the launch; the hook then
+    disarms itself."""
+    _built()
+    d = H.dims(1, 8, 2, 128, 16, 1024)
+    p = 1 << 12  # aligned addresses: nothing reaches the device
+    H.herald_inject_launch_failure(0, 719)
+    with pytest.raises(H.HeraldError) as e:
+        H.herald_gather(d, p, p, 64, p, p, p, p)
+    assert e.value.status == 4
+    assert "gather launch" in str(e.value) and "cudaErrorLaunchFailure" in str(e.value)
+    # disarmed: the next call reaches the real launch (which, with no GPU
+    # here, fails for its own reason -- not the injected one)
+    try:
+        H.herald_gather(d, p, p, 64, p, p, p, p)
+    except H.HeraldError as e2:
+        assert "cudaErrorLaunchFailure" not in str(e2)
+    # arming needs an error code; a negative count disarms
+    with pytest.raises(H.HeraldError) as e:
+        H.herald_inject_launch_failure(0, 0)
+    assert e.value.status == 1
+    H.herald_inject_launch_failure(-1, 0)
+
+
+def test_release_build_reports_no_debug_checks():
+    """The release library has the device checks compiled out: its check
+    word reads 0 without touching a device."""
+    _built()
+    assert not H.herald_debug_build()
+    assert H.herald_debug_status() == 0

@@ -50,3 +50,37 @@ def test_self_test_rejects_limits_outside_its_range():
         with pytest.raises(H.HeraldError) as e:
             H.herald_selftest_wait_timeout(bad, ws)
         assert e.value.status == 1
+
+
+@pytest.mark.gpu
+def test_a_launch_failure_inside_a_call_is_reported_and_the_context_stays_usable():
+    """An injected failure of the second launch of stage 2 (the top-K after
+    the refine): HERALD_ERR_CUDA naming that launch; the next, untouched call
+    selects exactly what a clean run selects."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    w = TINY
+    d = H.dims_of(w)
+    x = synth.make_layer(w)
+    ws = torch.zeros(H.herald_workspace_size(d, w.C, w.P), dtype=torch.uint8, device="cuda")
+    NG = (w.N, w.Hkv)
+    cand = torch.zeros((*NG, w.C), dtype=torch.int32, device="cuda")
+    n_cand = torch.zeros(NG, dtype=torch.int32, device="cuda")
+    idx = torch.full((*NG, w.P), -1, dtype=torch.int32, device="cuda")
+    n_sel = torch.zeros(NG, dtype=torch.int32, device="cuda")
+    q, k, ctx = dev(x["q_steps"][0]), dev(x["k_cache"]), dev(x["ctx"])
+    H.herald_select_stage1(d, dev(x["q_merge"]), k, ctx, w.C, cand, n_cand, ws)
+    H.herald_select_stage2(d, q, k, ctx, cand, n_cand, w.C, w.K, w.S, w.W, w.P, idx, n_sel, ws)
+    torch.cuda.synchronize()
+    ref = (idx.clone(), n_sel.clone())
+    idx.fill_(-5)
+    H.herald_inject_launch_failure(1, 719)
+    with pytest.raises(H.HeraldError) as e:
+        H.herald_select_stage2(d, q, k, ctx, cand, n_cand, w.C, w.K, w.S, w.W, w.P, idx, n_sel,
+                               ws)
+    assert e.value.status == 4 and "topk_union launch" in str(e.value)
+    torch.cuda.synchronize()
+    H.herald_select_stage2(d, q, k, ctx, cand, n_cand, w.C, w.K, w.S, w.W, w.P, idx, n_sel, ws)
+    torch.cuda.synchronize()
+    assert H.herald_workspace_error(ws) == 0
+    assert torch.equal(idx, ref[0]) and torch.equal(n_sel, ref[1])

@@ -66,3 +66,77 @@ def test_noalloc_rejects_shapes_beyond_the_static_scratch():
         H.herald_select_stage2_noalloc(d, ok, ok, ok, ok, ok, 8192, 1024, 64, 256, 1344, ok, ok)
     assert e.value.status == 3
     assert "scratch" in str(e.value)
+
+
+@pytest.mark.gpu
+def test_noalloc_two_pass_refine_matches_workspace_stage2():
+    """C > 4096 (the two-pass refine, its row log-sum-exp at its own offset
+    in the static scratch) with few enough segments to fit the 4 MiB."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    w = Workload("noalloc-two-pass", N=1, Hq=8, Hkv=2, d=128, L=12000, B=16, T=1, C=8192, K=256,
+                 S=16, W=64, planted="points", n_planted=12, index=46, extra_rows=16)
+    x = synth.make_layer(w)
+    d = H.dims_of(w)
+    q_merge, q = _dev(torch, x["q_merge"]), _dev(torch, x["q_steps"][0])
+    k, ctx = _dev(torch, x["k_cache"]), _dev(torch, x["ctx"])
+    NG = (w.N, w.Hkv)
+    ws = torch.zeros(H.herald_workspace_size(d, w.C, w.P), dtype=torch.uint8, device="cuda")
+    cand = torch.empty((*NG, w.C), dtype=torch.int32, device="cuda")
+    n_cand = torch.empty(NG, dtype=torch.int32, device="cuda")
+    H.herald_select_stage1(d, q_merge, k, ctx, w.C, cand, n_cand, ws)
+    ref_idx = torch.full((*NG, w.P), -7, dtype=torch.int32, device="cuda")
+    ref_ns = torch.zeros(NG, dtype=torch.int32, device="cuda")
+    H.herald_select_stage2(d, q, k, ctx, cand, n_cand, w.C, w.K, w.S, w.W, w.P, ref_idx, ref_ns,
+                           ws)
+    for call in range(2):
+        idx = torch.full((*NG, w.P), -9, dtype=torch.int32, device="cuda")
+        ns = torch.full(NG, -9, dtype=torch.int32, device="cuda")
+        H.herald_select_stage2_noalloc(d, q, k, ctx, cand, n_cand, w.C, w.K, w.S, w.W, w.P, idx,
+                                       ns)
+        torch.cuda.synchronize()
+        assert torch.equal(ns, ref_ns), f"call {call}: n_sel differs"
+        assert torch.equal(idx, ref_idx), f"call {call}: idx differs"
+
+
+@pytest.mark.gpu
+def test_noalloc_rejects_a_host_resident_cache():
+    """A cache in pinned host memory needs its candidate rows staged, which
+    this call has no room for: rejected before anything is launched."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    w = Workload("noalloc-host", N=1, Hq=8, Hkv=2, d=128, L=2000, B=16, T=1, C=256, K=64, S=8,
+                 W=32, planted="points", n_planted=4, index=47, extra_rows=16)
+    x = synth.make_layer(w)
+    d = H.dims_of(w)
+    kh = torch.from_numpy(x["k_cache"].view(np.int16)).pin_memory()
+    q, ctx = _dev(torch, x["q_steps"][0]), _dev(torch, x["ctx"])
+    NG = (w.N, w.Hkv)
+    cand = torch.zeros((*NG, w.C), dtype=torch.int32, device="cuda")
+    n_cand = torch.zeros(NG, dtype=torch.int32, device="cuda")
+    idx = torch.zeros((*NG, w.P), dtype=torch.int32, device="cuda")
+    ns = torch.zeros(NG, dtype=torch.int32, device="cuda")
+    with pytest.raises(H.HeraldError) as e:
+        H.herald_select_stage2_noalloc(d, q, kh, ctx, cand, n_cand, w.C, w.K, w.S, w.W, w.P, idx,
+                                       ns)
+    assert e.value.status == 1
+    assert "device memory" in str(e.value)
+
+
+def test_noalloc_applies_the_stage2_argument_rules():
+    """Host-side checks (launch nothing): the same rules as
+    herald_select_stage2, including the N*Hkv*P_max bound of the int32 index
+    layout, which the scratch limit alone would not catch."""
+    ok = 1 << 12
+    d = H.dims(1, 8, 2, 128, 16, 4096)
+    with pytest.raises(H.HeraldError) as e:   # K > C
+        H.herald_select_stage2_noalloc(d, ok, ok, ok, ok, ok, 64, 65, 0, 0, 65, ok, ok)
+    assert e.value.status == 1
+    with pytest.raises(H.HeraldError) as e:   # K + sink + local > P_max
+        H.herald_select_stage2_noalloc(d, ok, ok, ok, ok, ok, 64, 32, 16, 32, 64, ok, ok)
+    assert e.value.status == 1
+    with pytest.raises(H.HeraldError) as e:   # N*Hkv*P_max >= 2^31
+        H.herald_select_stage2_noalloc(d, ok, ok, ok, ok, ok, 64, 32, 0, 0, 1 << 30, ok, ok)
+    assert e.value.status == 2
