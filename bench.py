@@ -15,9 +15,15 @@ the layer stack) and the graphs are replayed; the K cache and V cache are
 rotated over enough copies that the data touched between two uses of a
 copy exceeds L2 (cold-L2 inputs).  A second, traced replay brackets every
 kernel with graph event nodes to time the dominant kernel for the
-roofline.  e2e: the same step through the pipeline's public call (one
-graph per block) with the step's inputs copied from pinned host buffers
-and its outputs read back, copies inside the timed region.
+roofline.  The timed region of --steps steps is repeated until the repeats
+add up to --min-timed-ms (the median per step is reported).  e2e: the same
+step through the pipeline's public call (one graph per block) with the
+step's inputs copied from pinned host buffers and its outputs read back,
+copies inside the timed region; e2e.direct_calls: the same with the
+library's C-ABI calls issued directly every step (their host cost inside
+the timed region).  `range`: the metric's other workloads (4 x 64K, 128K
+with the cache in host memory, the 28-layer stack), each timed the same way
+with its scan and attention rooflines.
 `--impl reference`: the fp64 CPU oracle timed on the host cores.
 """
 from __future__ import annotations
@@ -162,18 +168,18 @@ def kernel_source_hash() -> str:
 
 
 def ncu_traffic(kernel: str, src_hash: str, workload: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if
-    the summary was taken on the current kernel sources and this workload;
-    else None."""
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary, if the summary was taken on the current kernel sources; else
+    None."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         d = json.load(open(p))
     except Exception:
         return None
-    e = d.get("kernels", {}).get(kernel)
-    if not e or d.get("source_hash") != src_hash or d.get("workload") != workload:
+    if d.get("source_hash") != src_hash:
         return None
-    return e.get("dram_bytes_per_launch_full_workload")
+    e = d.get("workloads", {}).get(workload, {}).get("kernels", {}).get(kernel)
+    return e.get("dram_bytes_per_launch_full_workload") if e else None
 
 
 class Bench:
@@ -560,12 +566,15 @@ def blocks_per_graph(b, steps: int) -> int:
     return max(g for g in range(1, 9) if steps % g == 0)
 
 
-def time_blocks(b, args, st, dist, graphs):
+def time_blocks(b, args, st, dist, graphs, min_ms: float = 0.0):
     """Warm-up blocks, then exactly args.steps blocks between two CUDA
-    events on `st`; block i uses cache copy i % n_rot.  Per-block graphs
-    (`graphs`) or chunk graphs of blocks_per_graph consecutive blocks (the
-    warm-up then rounded up to whole chunks).  Returns (ms per block, g, and
-    the host clock at the start and end of the timed region)."""
+    events on `st` (a barrier and a device synchronise on both sides),
+    repeated until the timed regions add up to `min_ms` (at least once); block
+    i uses cache copy i % n_rot.  Per-block graphs (`graphs`) or chunk graphs
+    of blocks_per_graph consecutive blocks (the warm-up then rounded up to
+    whole chunks).  Returns (median ms per block over the repeats, g, the host
+    clock at the start of the first and the end of the last timed region,
+    the repeat count)."""
     torch = b.torch
     g = blocks_per_graph(b, args.steps)
     nw = -(-args.warmup // g) * g
@@ -581,21 +590,30 @@ def time_blocks(b, args, st, dist, graphs):
         run.append((i, chunks[start]))
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for i, graph in run:
-        if i == nw:
-            torch.cuda.synchronize()
-            if dist:
-                dist.barrier()
-            torch.cuda.synchronize()
-            t0 = time.perf_counter()
-            e0.record(st)
+    for i, graph in run[: nw // g]:      # warm-up
         if g == 1:
             b.before_step(i)
         graph.replay()
-    e1.record(st)
-    torch.cuda.synchronize()
+    per_rep, t_first, total = [], None, 0.0
+    while not per_rep or total < min_ms:
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        if t_first is None:
+            t_first = time.perf_counter()
+        e0.record(st)
+        for i, graph in run[nw // g:]:
+            if g == 1:
+                b.before_step(i - nw)  # every repeat starts a group of blocks afresh
+            graph.replay()
+        e1.record(st)
+        torch.cuda.synchronize()
+        rep_ms = e0.elapsed_time(e1)
+        total += rep_ms
+        per_rep.append(rep_ms / args.steps)
     t1 = time.perf_counter()
-    return e0.elapsed_time(e1) / args.steps, g, t0, t1
+    return float(np.median(per_rep)), g, t_first, t1, len(per_rep)
 
 
 def attn_chain_ms(b, rounds: int = 8, reps: int = 5) -> float:
@@ -631,32 +649,37 @@ def attn_chain_ms(b, rounds: int = 8, reps: int = 5) -> float:
     return e0.elapsed_time(e1) / (reps * rounds * w.T)
 
 
-def run_ours(args, rank, world, dist):
+def measure(w, args, dist, world, min_ms: float, serial: bool = True, e2e: bool = False):
+    """One workload, timed as the headline is: the dual-stream block step
+    (graph replay, repeated timed regions, median), the same step without the
+    overlap (serial), a traced replay of the serial step for per-kernel
+    durations, the pool attention's chain duration, the roofline of the
+    dominant kernel and of the stage-1 scan; with e2e, the end-to-end legs.
+    Returns (the line's fields for this workload, the bench object)."""
     import torch
-    w = workload()
-    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
     dev_idx = torch.cuda.current_device()
-    b = StackBench(w, rank) if w.layers > 1 else Bench(w, rank)
+    b = StackBench(w, 0) if w.layers > 1 else Bench(w, 0)
     graphs, _ = b.capture(traced=False)
     nrot = b.n_rot
     st = torch.cuda.current_stream()
     clocks = ClockSampler(dev_idx)
     clocks.start()
-    ms, chunk, t0, t1 = time_blocks(b, args, st, dist, graphs)
+    ms, chunk, t0, t1, reps_timed = time_blocks(b, args, st, dist, graphs, min_ms)
     if dist:
         dist.barrier()
     clocks.stop()
     ms = max_over_ranks(ms, dist, "cuda")
-    value = job_value(ms, world, w.N * w.B)
     err = b.H.herald_workspace_error(b.ws)
+    del graphs
 
-    # the same step without the selection/denoise overlap, for reference
-    b.overlap = False
-    sgraphs, _ = b.capture(traced=False)
-    serial_ms = time_blocks(b, args, st, dist, sgraphs)[0]
-    serial_ms = max_over_ranks(serial_ms, dist, "cuda")
-    b.overlap = True
-    del sgraphs
+    serial_ms = None
+    if serial:  # the same step without the selection/denoise overlap
+        b.overlap = False
+        sgraphs, _ = b.capture(traced=False)
+        serial_ms = max_over_ranks(time_blocks(b, args, st, dist, sgraphs, min_ms / 4)[0], dist,
+                                   "cuda")
+        b.overlap = True
+        del sgraphs
 
     # traced replay of the serial step: per-kernel durations (graph event
     # nodes) for the roofline, each kernel timed without the other stream's
@@ -683,6 +706,7 @@ def run_ours(args, rank, world, dist):
             b.step(0)
         torch.cuda.synchronize()
         launches_per_step = tr.count
+    del tgraphs
     b.overlap = True
     tot = {k: float(np.sum(v)) / reps for k, v in per.items()}     # ms per step
     avg = {k: float(np.mean(v)) for k, v in per.items()}           # ms per launch
@@ -731,46 +755,97 @@ def run_ours(args, rank, world, dist):
 
     roofline = (roof(dominant) or roof("attn_pool_kernel") or roof("attn_cluster_kernel")
                 or roof("attn_kernel"))
+    attention = roof("attn_pool_kernel") or roof("attn_cluster_kernel") or roof("attn_kernel")
     scan = roof("scan_tc_kernel") or roof("scan_cc_kernel")
+    out = {"value": job_value(ms, world, w.N * w.B), "ms_per_step": ms,
+           "config": {"workload": w.name, "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
+                      "ctx": w.L, "B": w.B, "T": w.T, "C": w.C, "K": w.K, "sink": w.S,
+                      "local": w.W, "layers": w.layers, "l2": b.l2_note(),
+                      "context": b.context_note(), "selection": _SELECTION,
+                      "prefetch": b.prefetch_note(), "budget": b.budget_note(),
+                      "timing": (f"CUDA-graph replay, {chunk} consecutive blocks per graph "
+                                 f"(one graph launch per {chunk} blocks), CUDA events; "
+                                 if chunk > 1 else
+                                 "CUDA-graph replay of whole steps, CUDA events; ")
+                                + f"{reps_timed} timed regions of {args.steps} steps, median"},
+           "timed_regions": reps_timed,
+           "roofline": roofline, "attention": attention,
+           "scan": {"achieved_gbs": scan["achieved"] if scan else None,
+                    "frac": scan["frac"] if scan else None,
+                    "peak": scan["peak"] if scan else None,
+                    "unit": "GB/s", "bound": scan["bound"] if scan else None,
+                    "kernel": scan["kernel"] if scan else None,
+                    "launch_us": scan["launch_us"] if scan else None,
+                    "traffic": scan["traffic"] if scan else None},
+           "kernels_ms_per_step": {k: round(v, 5) for k, v in sorted(tot.items(),
+                                                                     key=lambda kv: -kv[1])},
+           "gpu_launches": launches_per_step * args.steps,
+           "launches_per_step": launches_per_step,
+           "clocks": clocks.summary(t0, t1), "device_error_word": err}
+    if serial_ms is not None:
+        out["serial"] = {"ms_per_step": serial_ms,
+                         "value": job_value(serial_ms, world, w.N * w.B),
+                         "what": "same step with stage 1 on the denoising stream (no overlap)"}
+    if e2e:
+        out["e2e"] = run_e2e(b, args, dist, graph=True)
+        out["e2e"]["direct_calls"] = run_e2e(b, args, dist, graph=False)
+    return out, b
 
-    # end to end through the C ABI with host buffers
-    e2e = run_e2e(b, args, dist)
 
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+RANGE = {"llama": "LLAMA_64K", "long-host": "LONG_128K_HOST", "stack": "QWEN_STACK"}
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    w = workload()
+    main, b = measure(w, args, dist, world, args.min_timed_ms, e2e=True)
+    del b
+    torch.cuda.empty_cache()
+    line = {"metric": METRIC, "value": main["value"], "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": main["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": w.name, "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
-                       "ctx": w.L, "B": w.B, "T": w.T, "C": w.C, "K": w.K, "sink": w.S,
-                       "local": w.W, "parallelism": f"replicas x{world}",
-                       "layers": w.layers, "l2": b.l2_note(), "context": b.context_note(),
-                       "selection": _SELECTION,
-                       "prefetch": b.prefetch_note(),
-                       "budget": b.budget_note(),
-                       "timing": (f"CUDA-graph replay, {chunk} consecutive blocks per graph "
-                                  f"(one graph launch per {chunk} blocks), CUDA events"
-                                  if chunk > 1 else
-                                  "CUDA-graph replay of whole steps, CUDA events")},
-            "roofline": roofline,
-            "serial": {"ms_per_step": serial_ms, "value": job_value(serial_ms, world, w.N * w.B),
-                       "what": "same step with stage 1 on the denoising stream (no overlap)"},
-            "scan": {"achieved_gbs": scan["achieved"] if scan else None,
-                     "frac": scan["frac"] if scan else None,
-                     "launch_us": scan["launch_us"] if scan else None},
-            "kernels_ms_per_step": {k: round(v, 5) for k, v in sorted(tot.items(),
-                                                                      key=lambda kv: -kv[1])},
+            "config": dict(main["config"], parallelism=f"replicas x{world}"),
+            "roofline": main["roofline"], "attention": main["attention"],
+            "serial": main["serial"], "scan": main["scan"],
+            "kernels_ms_per_step": main["kernels_ms_per_step"],
             "kernels_timing": "traced replay of the serial step (CUDA events around each "
                               "kernel; no cross-stream overlap)",
-            "gpu_launches": launches_per_step * args.steps,
-            "clocks": clocks.summary(t0, t1), "e2e": e2e,
-            "device_error_word": err, "source_hash": src_hash}
+            "gpu_launches": main["gpu_launches"], "timed_regions": main["timed_regions"],
+            "clocks": main["clocks"], "e2e": main["e2e"],
+            "device_error_word": main["device_error_word"],
+            "source_hash": kernel_source_hash()}
+
+    # the rest of the metric's range (32K-128K), each workload at full size,
+    # timed the same way: block tokens/s, the scan's and the attention's
+    # rooflines
+    from block_diffusion_sparse_gb300 import workloads as W
+    rng = {}
+    for key in [r for r in args.range.split(",") if r and r != "none"]:
+        wr = getattr(W, RANGE[key])
+        if wr.name == w.name:
+            continue
+        try:
+            r, b = measure(wr, args, dist, world, args.min_timed_ms / 2, serial=False)
+            del b
+        except Exception as ex:  # one failing range entry must not hide the headline
+            r = {"error": f"{type(ex).__name__}: {ex}"}
+        torch.cuda.empty_cache()
+        rng[wr.name] = {k: r.get(k) for k in ("value", "ms_per_step", "config", "scan",
+                                               "attention", "kernels_ms_per_step",
+                                               "timed_regions", "clocks", "device_error_word",
+                                               "error") if k in r}
+        rng[wr.name]["gpu_launches"] = r.get("gpu_launches")
+    if rng:
+        line["range"] = rng
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(b, args, dist):
+def run_e2e(b, args, dist, graph: bool = True):
     """Every step: that step's inputs (the T steps' queries and block K/V)
     copied from pinned host memory to the device, the step through the
     pipeline's public call (BlockPipeline.block with graph=True: the first
@@ -803,7 +878,7 @@ def run_e2e(b, args, dist):
     # the pipeline's graph cache is keyed by buffers: one graph per (cache
     # copy, input slot); with many rotated cache copies (tiny workloads) the
     # direct calls are used instead
-    use_graph = b.n_rot <= 8
+    use_graph = graph and b.n_rot <= 8
 
     def one(i):
         s = i % 2
@@ -849,9 +924,10 @@ def run_e2e(b, args, dist):
             "ms_per_step": ms,
             "path": ("BlockPipeline.block(graph=True): C-ABI calls captured once per buffer "
                      "set (during the warm-up), then replayed" if use_graph else
-                     "direct C-ABI calls") + "; pinned host buffers, copies on two copy streams "
-                    "into double-buffered device inputs/outputs; the cache rotates as in the "
-                    "device-timed run"}
+                     "direct C-ABI calls every step (argument checks, tensor-map lookups and "
+                     "launches inside the timed region)")
+                    + "; pinned host buffers, copies on two copy streams into double-buffered "
+                    "device inputs/outputs; the cache rotates as in the device-timed run"}
 
 
 def main():
@@ -861,6 +937,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--min-timed-ms", type=float, default=200.0,
+                    help="the timed region of --steps steps is repeated until the repeats add "
+                         "up to this (the median per step is reported)")
+    ap.add_argument("--range", default="llama,long-host,stack",
+                    help="other workloads of the metric's range measured after the headline "
+                         "(comma-separated: llama, long-host, stack; none)")
     ap.add_argument("--workload", default="qwen", choices=sorted(WORKLOADS))
     ap.add_argument("--selection", default="merged", choices=["merged", "exact", "blocks"],
                     help="merged: the two-stage selection (default); exact: every cached "
