@@ -340,8 +340,9 @@ void oracle_dense_attn(int N, int B, int Hq, int Hkv, int d, int L_max,
 }
 
 /* Step 8 (the cache grows by the decoded block): cache[n][g][ctx[n] + b] =
- * block_kv[n][b][g] for b < B, then ctx[n] += B.  Rows past L_max are a
- * caller error and are not written. */
+ * block_kv[n][b][g] for b < B, then ctx[n] = min(ctx[n] + B, L_max): the
+ * context cannot grow past the cache's capacity, and rows past L_max are
+ * not written. */
 void oracle_append(int N, int B, int Hkv, int d, int L_max, int *ctx,
                    const double *block_k, const double *block_v,
                    double *k_cache, double *v_cache) {
@@ -355,6 +356,7 @@ void oracle_append(int N, int B, int Hkv, int d, int L_max, int *ctx,
                 memcpy(k_cache + dst, block_k + src, sizeof(double) * (size_t)d);
                 memcpy(v_cache + dst, block_v + src, sizeof(double) * (size_t)d);
             }
-        ctx[n] += B;
+        /* the context grows by the block, up to the cache's capacity */
+        ctx[n] = ctx[n] + B < L_max ? ctx[n] + B : L_max;
     }
 }

@@ -330,6 +330,13 @@ def test_append_writes_rows_and_advances_context():
         np.testing.assert_array_equal(k2[n, :, ctx[n]: ctx[n] + B], bk[n].transpose(1, 0, 2))
         np.testing.assert_array_equal(v2[n, :, ctx[n]: ctx[n] + B], bv[n].transpose(1, 0, 2))
         np.testing.assert_array_equal(k2[n, :, : ctx[n]], k[n, :, : ctx[n]])
+    # a block that overflows the cache: the rows that fit are written, the
+    # rest skipped, and the context stops at the capacity L_max
+    ctx = np.array([8, 10], np.int32)
+    c3, k3, _ = oracle.append(ctx, bk, bv, k, v)
+    assert c3.tolist() == [10, 10]
+    np.testing.assert_array_equal(k3[0, :, 8:10], bk[0, :2].transpose(1, 0, 2))
+    np.testing.assert_array_equal(k3[1], k[1])
 
 
 def test_bf16_helpers_round_to_nearest_even():
