@@ -436,6 +436,7 @@ def algorithmic_work(w, n_sel: np.ndarray) -> dict:
         "attn_kernel": attn,
         "attn_cluster_kernel": attn,
         "attn_pool_kernel": attn,
+        "attn_flash_kernel": attn,
         "gather_kernel": {"bound": "link" if w.kv_on_host else "hbm",
                           "bytes": int(ns.sum()) * w.d * 2 * 2 * 2},
         "refine_pass1_kernel": {"bound": "tensor", "flops": 2 * R * w.C * w.d * NG},
@@ -721,8 +722,10 @@ def measure(w, args, dist, world, min_ms: float, serial: bool = True, e2e: bool 
     # the pool attention's launch duration in its chain (the dominant kernel of
     # the device-resident workloads); the isolated traced one is kept beside it
     chain = {}
-    if "attn_pool_kernel" in avg and not getattr(b, "exact", False):
-        chain["attn_pool_kernel"] = attn_chain_ms(b)
+    for name in ("attn_flash_kernel", "attn_pool_kernel"):
+        if name in avg and not getattr(b, "exact", False):
+            chain[name] = attn_chain_ms(b)
+            break
 
     def roof(name):
         wk = work.get(name)
@@ -753,9 +756,10 @@ def measure(w, args, dist, world, min_ms: float, serial: bool = True, e2e: bool 
                                 f"{pk_kind} (MEASURED_PEAKS.json)" if pk_kind == "measured"
                                 else "fallback")}
 
-    roofline = (roof(dominant) or roof("attn_pool_kernel") or roof("attn_cluster_kernel")
-                or roof("attn_kernel"))
-    attention = roof("attn_pool_kernel") or roof("attn_cluster_kernel") or roof("attn_kernel")
+    roofline = (roof(dominant) or roof("attn_flash_kernel") or roof("attn_pool_kernel")
+                or roof("attn_cluster_kernel") or roof("attn_kernel"))
+    attention = (roof("attn_flash_kernel") or roof("attn_pool_kernel") or roof("attn_cluster_kernel")
+                 or roof("attn_kernel"))
     scan = roof("scan_tc_kernel") or roof("scan_cc_kernel")
     out = {"value": job_value(ms, world, w.N * w.B), "ms_per_step": ms,
            "config": {"workload": w.name, "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,

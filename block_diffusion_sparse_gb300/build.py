@@ -20,9 +20,8 @@ LIB = os.path.join(OUT_DIR, "libherald.so")
 # indices and counts, read through herald_debug_status)
 DEBUG_DIR = os.path.join(HERE, "_build_debug")
 DEBUG_LIB = os.path.join(DEBUG_DIR, "libherald.so")
-SOURCES = ["herald_api.cu", "select_kernels.cu", "tc_kernels.cu", "move_kernels.cu",
-           "block_select.cu",
-           "herald_noalloc.cu"]
+SOURCES = ["herald_api.cu", "select_kernels.cu", "tc_kernels.cu", "attn_flash.cu",
+           "move_kernels.cu", "block_select.cu", "herald_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-warn-spills"]

@@ -498,7 +498,8 @@ herald_status herald_debug_status(uint32_t* code) {
   *code = 0;
 #ifdef HERALD_DEBUG
   HERALD_TRY_CUDA(cudaDeviceSynchronize(), "device synchronize");
-  *code = debug_take_select() | debug_take_tc() | debug_take_move() | debug_take_blocks();
+  *code = debug_take_select() | debug_take_tc() | debug_take_move() | debug_take_blocks() |
+          debug_take_flash();
 #endif
   return HERALD_OK;
 }
@@ -947,8 +948,12 @@ herald_status denoise_attn(herald_dims dims, const uint16_t* q, const uint16_t* 
                            float scale, unsigned flags, int32_t* ctx_len, uint16_t* k_cache,
                            uint16_t* v_cache, void* ws, size_t ws_bytes, void* stream) {
   g_err[0] = 0;
-  constexpr unsigned kKnown = HERALD_ATTN_SETTLED | HERALD_ATTN_APPEND | HERALD_ATTN_ADVANCE;
+  constexpr unsigned kKnown =
+      HERALD_ATTN_SETTLED | HERALD_ATTN_APPEND | HERALD_ATTN_ADVANCE | (0xFu << 8);
   if (flags & ~kKnown) return fail(HERALD_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags & ~kKnown);
+  const unsigned kernel = (flags >> 8) & 0xFu;
+  if (kernel > (HERALD_ATTN_KERNEL_FLASH_CS8 >> 8))
+    return fail(HERALD_ERR_INVALID_ARG, "unknown kernel choice %u", kernel);
   const bool append = (flags & HERALD_ATTN_APPEND) != 0;
   if ((flags & HERALD_ATTN_ADVANCE) && !append)
     return fail(HERALD_ERR_INVALID_ARG, "HERALD_ATTN_ADVANCE needs HERALD_ATTN_APPEND");
@@ -971,12 +976,19 @@ herald_status denoise_attn(herald_dims dims, const uint16_t* q, const uint16_t* 
   HERALD_RET_IF(check_ws(dims, 1, P_max, ws, ws_bytes, &w));
   if (scale == 0.f) scale = 1.0f / sqrtf(float(dims.d));
   PoolMaps maps;
-  const bool pool = attn_pool_ok(dims, P_max);
+  const bool pool_ok = attn_pool_ok(dims, P_max), flash_ok = attn_flash_ok(dims);
+  const bool pool = pool_ok || flash_ok;
   if (pool) {
     const uint64_t rows = uint64_t(dims.N) * dims.Hkv * P_max;
-    const uint32_t box = uint32_t(attn_pool_kpc(P_max));
-    HERALD_RET_IF(encode_rows_map(pool_k, rows, dims.d, box, &maps.k));
-    HERALD_RET_IF(encode_rows_map(pool_v, rows, dims.d, box, &maps.v));
+    if (pool_ok) {
+      const uint32_t box = uint32_t(attn_pool_kpc(P_max));
+      HERALD_RET_IF(encode_rows_map(pool_k, rows, dims.d, box, &maps.k));
+      HERALD_RET_IF(encode_rows_map(pool_v, rows, dims.d, box, &maps.v));
+    }
+    if (flash_ok) {
+      HERALD_RET_IF(encode_rows_map(pool_k, rows, dims.d, kFlashTileKeys, &maps.kt));
+      HERALD_RET_IF(encode_rows_map(pool_v, rows, dims.d, kFlashTileKeys, &maps.vt));
+    }
     maps.bpt = attn_pool_bpt(dims);
     const int G = dims.Hq / dims.Hkv, Bp = (dims.B + 15) & ~15;
     const uint64_t tokens = uint64_t(dims.N) * dims.B;
@@ -997,6 +1009,7 @@ herald_status denoise_attn(herald_dims dims, const uint16_t* q, const uint16_t* 
                               w, at<float>(ws, w.opart), at<float2>(ws, w.ml),
                               at<uint32_t>(ws, w.err), pool ? &maps : nullptr,
                               (flags & HERALD_ATTN_SETTLED) != 0, fused ? &app : nullptr,
+                              int(kernel) | (pool_ok ? 0x100 : 0) | (flash_ok ? 0x200 : 0),
                               static_cast<cudaStream_t>(stream)),
                   "attention launch");
   if (append && !fused)  // a cache in host memory: the append kernel after the step

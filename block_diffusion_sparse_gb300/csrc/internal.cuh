@@ -119,6 +119,7 @@ uint32_t debug_take_select();
 uint32_t debug_take_tc();
 uint32_t debug_take_move();
 uint32_t debug_take_blocks();
+uint32_t debug_take_flash();
 
 // A launch failure injected on the host (herald_inject_launch_failure, a
 // test hook of the error paths): returns the injected error for the launch
@@ -241,20 +242,32 @@ cudaError_t launch_gather_staged(const herald_dims& dm, const int32_t* idx, cons
 //   q      queries [N*B][Hq][d], box {G heads, bpt tokens}
 //   bk, bv block keys / values [N*B][Hkv][d], box {1 head, B rounded to 16}
 // Row tiles hold bpt = attn_pool_bpt() whole tokens (bpt * G <= 128 rows).
+struct AppendArgs;  // below
+// The pipelined kernel (attn_flash.cu) takes the same q / bk / bv maps and
+// pool maps with a box of kFlashTileKeys rows (kt, vt).
 struct PoolMaps {
-  CUtensorMap k, v, q, bk, bv;
+  CUtensorMap k, v, q, bk, bv, kt, vt;
   int bpt;
 };
+constexpr int kFlashTileKeys = 128;
+// Whether the pipelined attention kernel takes these shapes (any P_max).
+bool attn_flash_ok(const herald_dims& dm);
+// The pipelined attention kernel with `cs` CTAs per row tile (8, 4 or 2;
+// 0 = the largest that keeps every cluster resident at once).
+cudaError_t launch_attn_flash(const herald_dims& dm, const int32_t* n_sel, int P_max,
+                              uint16_t* out, float scale, uint32_t* err, const PoolMaps& maps,
+                              const AppendArgs* app, int cs, bool settled, cudaStream_t st);
 int attn_pool_kpc(int P_max);
 int attn_pool_bpt(const herald_dims& dm);
 bool attn_pool_ok(const herald_dims& dm, int P_max);
-struct AppendArgs;  // below
 cudaError_t launch_attn(const herald_dims& dm, const uint16_t* q, const uint16_t* pool_k,
                         const uint16_t* pool_v, const int32_t* n_sel, int P_max,
                         const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
                         float scale, const WsLayout& w, float* opart, float2* ml, uint32_t* err,
                         const PoolMaps* maps, bool settled, const AppendArgs* app,
-                        cudaStream_t st);
+                        int kernel, cudaStream_t st);
+// (kernel: bits 0-3 the HERALD_ATTN_KERNEL_* choice >> 8; 0x100: the pool
+// kernel takes these shapes; 0x200: the pipelined kernel does)
 // exact selection: per-segment candidate counts = context lengths; the
 // refine's score partials summed in place (stride floats per segment) and
 // histogrammed for the top-K radix select

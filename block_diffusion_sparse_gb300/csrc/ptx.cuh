@@ -14,11 +14,21 @@
 
 namespace herald {
 
-// Device-side error codes written to the workspace error word.
+// Device-side error codes written to the workspace error word: the kind of
+// wait in bits 0-7, the kernel that gave up in bits 8-15 (the first error
+// recorded is kept).
 enum : uint32_t {
   DEV_OK = 0,
-  DEV_TIMEOUT_TMA = 1,   // a TMA / cp.async completion wait ran out
-  DEV_TIMEOUT_MMA = 2,   // a tcgen05 commit wait ran out
+  DEV_TIMEOUT_TMA = 1,   // a TMA / cp.async / bulk-copy completion wait ran out
+  DEV_TIMEOUT_MMA = 2,   // a tcgen05 commit (or a pipeline stage) wait ran out
+  DEV_K_REFINE_PASS1 = 1u << 8,
+  DEV_K_REFINE_PASS2 = 2u << 8,
+  DEV_K_REFINE_FUSED = 3u << 8,
+  DEV_K_ATTN_SPLIT = 4u << 8,
+  DEV_K_ATTN_CLUSTER = 5u << 8,
+  DEV_K_ATTN_POOL = 6u << 8,
+  DEV_K_SCAN = 7u << 8,
+  DEV_K_ATTN_FLASH = 8u << 8,
 };
 
 // Checks of the debug build (compiled with -DHERALD_DEBUG): a kernel compares
@@ -224,6 +234,18 @@ HERALD_DEV void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uin
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem]^T: A (M x K, bf16) held in tensor memory --
+// row i in lane i, two consecutive K elements per 32-bit column -- and B
+// from a shared-memory descriptor; fp32 accumulator.
+HERALD_DEV void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // Arrive once on the mbarrier when all previously issued tcgen05.mma of this

@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
         const int stage = i % kTcScanStages;
         if (i >= kTcScanStages &&
             !mbar_wait(&empty[stage], uint32_t((i / kTcScanStages) - 1) & 1u)) {
-          record_error(err, DEV_TIMEOUT_MMA);
+          record_error(err, DEV_TIMEOUT_MMA | DEV_K_SCAN);
           break;
         }
         mbar_arrive_expect_tx(&full[stage], Cfg::kTileBytes);
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
         ok = ok && mbar_wait(&full[stage], uint32_t(i / kTcScanStages) & 1u);
         if (i >= 2) ok = ok && mbar_wait(&tempty[acc], uint32_t((i >> 1) - 1) & 1u);
         if (!ok) {
-          record_error(err, DEV_TIMEOUT_TMA);
+          record_error(err, DEV_TIMEOUT_TMA | DEV_K_SCAN);
           break;
         }
         tc_fence_after();
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
       }
       const int acc = i & 1;
       if (!mbar_wait(&tfull[acc], uint32_t(i >> 1) & 1u)) {
-        record_error(err, DEV_TIMEOUT_MMA);
+        record_error(err, DEV_TIMEOUT_MMA | DEV_K_SCAN);
         break;
       }
       tc_fence_after();

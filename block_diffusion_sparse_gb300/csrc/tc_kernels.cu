@@ -26,14 +26,11 @@
 
 #include "internal.cuh"
 #include "ptx.cuh"
+#include "tc_common.cuh"
 
 namespace herald {
 
 constexpr int kTcThreads = 256;  // 8 warps: lane quadrant = warp % 4
-
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
 
 // Copies `rows` rows of D bf16 (row r from src_of(r), or zeros when src_of
 // returns nullptr) into a K-major 128B-swizzled tile: D/64 column halves,
@@ -61,31 +58,6 @@ __device__ __forceinline__ void load_rows_sw128(uint8_t* tile, int rows, int row
   }
 }
 
-// TMEM allocation protocol: warp 0 allocates, everybody syncs.
-__device__ __forceinline__ void tmem_setup(uint32_t* slot, uint32_t ncols) {
-  __syncwarp();
-  if ((threadIdx.x >> 5) == 0) {
-    tmem_alloc(slot, ncols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-}
-__device__ __forceinline__ void tmem_teardown(uint32_t base, uint32_t ncols) {
-  tc_fence_before();
-  __syncthreads();
-  if ((threadIdx.x >> 5) == 0) {
-    tc_fence_after();
-    tmem_dealloc(base, ncols);
-  }
-}
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
 // Full cluster barrier (hardware): release this CTA's shared-memory writes,
 // acquire the peers'.
 __device__ __forceinline__ void cluster_sync_all() {
@@ -118,25 +90,8 @@ __device__ __forceinline__ float4 ld_peer_f4(uint32_t a) {
 template <typename... KArgs, typename... Args>
 static cudaError_t launch_cluster(const char* name, void (*kernel)(KArgs...), dim3 grid,
                                   int cluster_x, size_t smem, cudaStream_t st, Args... args) {
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cluster_x;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  if (const cudaError_t ie = injected_launch_error()) return ie;
-  trace_before(st, name);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
-  trace_after(st);
-  return e;
+  return launch_cluster_threads(name, kernel, grid, dim3(kTcThreads), cluster_x, smem, st,
+                                args...);
 }
 
 // ========================================================== refine_pass1
@@ -209,7 +164,7 @@ __global__ void __launch_bounds__(kTcThreads)
   tc_fence_after();
 
   if (threadIdx.x == 0) {
-    if (!mbar_wait(&barQ, 0)) record_error(err, DEV_TIMEOUT_TMA);
+    if (!mbar_wait(&barQ, 0)) record_error(err, DEV_TIMEOUT_TMA | DEV_K_REFINE_PASS1);
     tc_fence_after();
     constexpr uint32_t idesc = make_idesc_bf16(kTileM, kRefineChunk, false, false);
     const uint32_t qa = smem_u32(Qs), ka = smem_u32(Ks);
@@ -222,7 +177,7 @@ __global__ void __launch_bounds__(kTcThreads)
     }
     umma_commit(&bar);
   }
-  if (!mbar_wait(&bar, 0)) record_error(err, DEV_TIMEOUT_MMA);
+  if (!mbar_wait(&bar, 0)) record_error(err, DEV_TIMEOUT_MMA | DEV_K_REFINE_PASS1);
   tc_fence_after();
   __syncwarp();
 
@@ -364,7 +319,7 @@ __global__ void __launch_bounds__(kTcThreads)
   tc_fence_after();
 
   if (threadIdx.x == 0) {
-    if (!mbar_wait(&barQ, 0)) record_error(err, DEV_TIMEOUT_TMA);
+    if (!mbar_wait(&barQ, 0)) record_error(err, DEV_TIMEOUT_TMA | DEV_K_REFINE_PASS2);
     tc_fence_after();
     const uint32_t idesc = make_idesc_bf16(kRefineRows2, Rp, false, false);
     const uint32_t ka = smem_u32(Ks), qa = smem_u32(Qs);
@@ -377,7 +332,7 @@ __global__ void __launch_bounds__(kTcThreads)
     }
     umma_commit(&bar);
   }
-  if (!mbar_wait(&bar, 0)) record_error(err, DEV_TIMEOUT_MMA);
+  if (!mbar_wait(&bar, 0)) record_error(err, DEV_TIMEOUT_MMA | DEV_K_REFINE_PASS2);
   tc_fence_after();
   __syncwarp();
 
@@ -536,8 +491,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     umma_commit(&bar0);
   }
-  if (!qok) record_error(err, DEV_TIMEOUT_TMA);
-  if (ncv > 0 && !mbar_wait(&bar0, 0)) record_error(err, DEV_TIMEOUT_MMA);
+  if (!qok) record_error(err, DEV_TIMEOUT_TMA | DEV_K_REFINE_FUSED);
+  if (ncv > 0 && !mbar_wait(&bar0, 0)) record_error(err, DEV_TIMEOUT_MMA | DEV_K_REFINE_FUSED);
   tc_fence_after();
   __syncwarp();
 
@@ -810,7 +765,7 @@ __global__ void __launch_bounds__(kTcThreads)
     }
     umma_commit(&bar[0]);
   }
-  if (!mbar_wait(&bar[0], 0)) record_error(err, DEV_TIMEOUT_MMA);
+  if (!mbar_wait(&bar[0], 0)) record_error(err, DEV_TIMEOUT_MMA | DEV_K_ATTN_SPLIT);
   tc_fence_after();
   __syncwarp();
 
@@ -873,7 +828,7 @@ __global__ void __launch_bounds__(kTcThreads)
     }
     umma_commit(&bar[1]);
   }
-  if (!mbar_wait(&bar[1], 0)) record_error(err, DEV_TIMEOUT_MMA);
+  if (!mbar_wait(&bar[1], 0)) record_error(err, DEV_TIMEOUT_MMA | DEV_K_ATTN_SPLIT);
   tc_fence_after();
   __syncwarp();
 
@@ -1018,7 +973,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       umma_commit(&bar[0]);
     }
-    if (!mbar_wait(&bar[0], 0)) record_error(err, DEV_TIMEOUT_MMA);
+    if (!mbar_wait(&bar[0], 0)) record_error(err, DEV_TIMEOUT_MMA | DEV_K_ATTN_CLUSTER);
     tc_fence_after();
     __syncwarp();
     // scores of both tiles -> one row max
@@ -1082,7 +1037,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       umma_commit(&bar[1]);
     }
-    if (!mbar_wait(&bar[1], 0)) record_error(err, DEV_TIMEOUT_MMA);
+    if (!mbar_wait(&bar[1], 0)) record_error(err, DEV_TIMEOUT_MMA | DEV_K_ATTN_CLUSTER);
     tc_fence_after();
     __syncwarp();
     // O partial -> shared memory (row-major fp32, padded rows)
@@ -1475,7 +1430,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (any && !mbar_wait(&bar1, 0)) ok = false;
   tc_fence_after();
   __syncwarp();
-  if (!ok) record_error(err, DEV_TIMEOUT_MMA);
+  if (!ok) record_error(err, DEV_TIMEOUT_MMA | DEV_K_ATTN_POOL);
 
   // O partial -> shared memory over the dead operands (P was the last):
   // each row divided by its sum and stored as fp16 (|o / l| <= max |v|); the
@@ -1518,7 +1473,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bulk_commit();
   }
   if (!mbar_wait(&barR, 0)) {
-    record_error(err, DEV_TIMEOUT_TMA);
+    record_error(err, DEV_TIMEOUT_TMA | DEV_K_ATTN_POOL);
+    // a peer whose own wait ran out pushes late: this CTA must not exit
+    // (its shared memory is the copies' destination) before they land
+    mbar_wait(&barR, 0, 20ull * kWaitLimitNs);
   } else if (appender && app.advance && rank == 0 && threadIdx.x == 0) {
     app.ctx[n] = min(L0 + B, L_max);
   }
@@ -1742,23 +1700,38 @@ static cudaError_t launch_attn_t(const herald_dims& dm, const uint16_t* q, const
                                  const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
                                  float scale, const WsLayout& w, float* opart, float2* ml,
                                  uint32_t* err, const PoolMaps* maps, bool settled,
-                                 const AppendArgs* app, cudaStream_t st) {
+                                 const AppendArgs* app, int kernel, cudaStream_t st) {
   const int segs = dm.N * dm.Hkv;
   cudaError_t e;
+  const bool pool_ok = (kernel & 0x100) != 0, flash_ok = (kernel & 0x200) != 0;
+  const int choice = kernel & 0xF;  // HERALD_ATTN_KERNEL_* >> 8
   if (maps && !force_split()) {
-    const int kpc = attn_pool_kpc(P_max);
-    const uint32_t smem = pool_smem(D, kpc, (dm.B + 15) & ~15).total;
-    e = ensure_smem(attn_pool_kernel<D>, smem);
-    if (e != cudaSuccess) return e;
     const int tiles = cdiv(dm.B, maps->bpt);
-    // early loads pay only when every CTA of the grid is resident at once:
-    // with a second wave they measured slower (on the 4 x 64K layer)
-    const int early = settled && tiles * segs <= pool_resident_clusters<D>(smem) ? 1 : 0;
-    const AppendArgs none{nullptr, nullptr, nullptr, nullptr, nullptr, 0};
-    return launch_cluster("attn_pool_kernel", attn_pool_kernel<D>, dim3(kPoolCtas, tiles, segs),
-                          kPoolCtas, smem, st, maps->k, maps->v, maps->q, maps->bk, maps->bv,
-                          n_sel, P_max, dm.B, dm.Hq, dm.Hkv, maps->bpt, kpc, scale, early, out,
-                          err, app ? *app : none, dm.L_max);
+    const int kpc = attn_pool_kpc(P_max);
+    const uint32_t smem = pool_ok ? pool_smem(D, kpc, (dm.B + 15) & ~15).total : 0u;
+    if (pool_ok) {  // granted before the occupancy query, which needs it
+      e = ensure_smem(attn_pool_kernel<D>, smem);
+      if (e != cudaSuccess) return e;
+    }
+    // the pool kernel while its clusters fit the device at once, else the
+    // pipelined kernel (one wave with fewer CTAs per row tile)
+    bool use_pool = pool_ok && (choice == 1 || !flash_ok ||
+                                (choice == 0 && tiles * segs <= pool_resident_clusters<D>(smem)));
+    if (choice >= 2 && flash_ok) use_pool = false;
+    if (use_pool) {
+      // early loads pay only when every CTA of the grid is resident at once:
+      // with a second wave they measured slower (on the 4 x 64K layer)
+      const int early = settled && tiles * segs <= pool_resident_clusters<D>(smem) ? 1 : 0;
+      const AppendArgs none{nullptr, nullptr, nullptr, nullptr, nullptr, 0};
+      return launch_cluster("attn_pool_kernel", attn_pool_kernel<D>,
+                            dim3(kPoolCtas, tiles, segs), kPoolCtas, smem, st, maps->k, maps->v,
+                            maps->q, maps->bk, maps->bv, n_sel, P_max, dm.B, dm.Hq, dm.Hkv,
+                            maps->bpt, kpc, scale, early, out, err, app ? *app : none, dm.L_max);
+    }
+    if (flash_ok) {
+      const int cs = choice == 3 ? 2 : choice == 4 ? 4 : choice == 5 ? 8 : 0;
+      return launch_attn_flash(dm, n_sel, P_max, out, scale, err, *maps, app, cs, settled, st);
+    }
   }
   e = launch_attn_split<D>(dm, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale, w,
                            opart, ml, err, st);
@@ -1770,13 +1743,13 @@ cudaError_t launch_attn(const herald_dims& dm, const uint16_t* q, const uint16_t
                         const uint16_t* pool_v, const int32_t* n_sel, int P_max,
                         const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,
                         float scale, const WsLayout& w, float* opart, float2* ml, uint32_t* err,
-                        const PoolMaps* maps, bool settled, const AppendArgs* app,
+                        const PoolMaps* maps, bool settled, const AppendArgs* app, int kernel,
                         cudaStream_t st) {
   if (dm.d == 128)
     return launch_attn_t<128>(dm, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale,
-                              w, opart, ml, err, maps, settled, app, st);
+                              w, opart, ml, err, maps, settled, app, kernel, st);
   return launch_attn_t<64>(dm, q, pool_k, pool_v, n_sel, P_max, block_k, block_v, out, scale, w,
-                           opart, ml, err, maps, settled, app, st);
+                           opart, ml, err, maps, settled, app, kernel, st);
 }
 
 HERALD_DEBUG_WORD_READER(debug_take_tc)

@@ -103,8 +103,16 @@ herald_status herald_debug_status(uint32_t *code);
 herald_status herald_inject_launch_failure(int after, int cuda_error);
 
 /* Synchronously reads and clears the device error word of a workspace
- * (0 = no kernel gave up on a wait; 1 = a copy wait, 2 = a tensor-core wait
- * ran out).  Synchronises `stream` first. */
+ * (0 = no kernel gave up on a wait).  Bits 0-7: the kind of wait that ran
+ * out first (1 = a copy wait, 2 = a tensor-core or pipeline-stage wait);
+ * bits 8-15: the kernel (1 refine pass 1, 2 refine pass 2, 3 fused refine,
+ * 4 split attention, 5 cluster attention, 6 pool attention, 7 stage-1 scan,
+ * 8 pipelined attention); bits 16-31: which of the kernel's waits (the
+ * pipelined attention: 0x1 K ring slot, 0x2 V ring slot, 0x4 query tile,
+ * 0x8 K tile, 0x10 S buffer free, 0x20 P ready, 0x40 V tile, 0x80 S ready,
+ * 0x100 O ready for a rescale, 0x200 every MMA done, 0x400 the peers'
+ * partials, 0x800 the previous tile's P V done).
+ * Synchronises `stream` first. */
 herald_status herald_workspace_error(void *ws, void *stream, uint32_t *code);
 
 /* Stage 1 of the selection [V3]: merged query + full-cache scan + top-C.
@@ -306,6 +314,16 @@ herald_status herald_denoise_attn(herald_dims dims, const uint16_t *q, const uin
 #define HERALD_ATTN_SETTLED 1u /* the pool was written before an earlier herald call  */
 #define HERALD_ATTN_APPEND 2u  /* also append block_k/block_v to the cache            */
 #define HERALD_ATTN_ADVANCE 4u /* with APPEND: then advance ctx_len                    */
+/* Kernel choice (bits 8-11; for tests and tuning -- the default picks by
+ * shape): the cluster kernel holding a whole pool slice per CTA, or the
+ * pipelined kernel streaming key tiles (with 8, 4 or 2 CTAs per row tile,
+ * or chosen by shape).  A choice the shapes do not allow falls back to
+ * the default. */
+#define HERALD_ATTN_KERNEL_POOL (1u << 8)
+#define HERALD_ATTN_KERNEL_FLASH (2u << 8)
+#define HERALD_ATTN_KERNEL_FLASH_CS2 (3u << 8)
+#define HERALD_ATTN_KERNEL_FLASH_CS4 (4u << 8)
+#define HERALD_ATTN_KERNEL_FLASH_CS8 (5u << 8)
 
 /* herald_denoise_attn with options for the steps of a block (flags = 0 is
  * herald_denoise_attn; ctx_len, k_cache, v_cache are used only with
