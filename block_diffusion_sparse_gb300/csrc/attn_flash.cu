@@ -138,21 +138,20 @@ __global__ void __launch_bounds__(kFlashThreads, 1)
   // launch on the stream began (that launch waited for its own predecessor
   // before starting this one), so the producers fetch the first pool tiles
   // while the predecessor finishes
-  int pre = 0;  // pool tiles loaded before the grid-dependency wait
   // pool keys [k0, k_hi) of this CTA: the last CTA takes the rest
   const int k_hi = int(rank) == CS - 1 ? P_max : min(P_max, k0 + kpc);
-  if (settled && (warp == kFlashKWarp || warp == kFlashVWarp) && lane == 0) {
+  // Only the first K tile goes before the wait: every CTA of the grid loads
+  // at once at the start, and the query tile and the first K tile are what
+  // S_0 needs; the other tiles follow once the first one has landed.
+  int pre = 0;  // pool K tiles loaded before the grid-dependency wait
+  if (settled && warp == kFlashKWarp && lane == 0) {
     const int nkp0 = max(min(max(n_sel[seg], 0), k_hi) - k0, 0);
-    pre = min((nkp0 + kFT - 1) / kFT, 2);
-    const CUtensorMap* map = warp == kFlashKWarp ? &kmap : &vmap;
-    uint8_t* ring = warp == kFlashKWarp ? Kr : Vr;
-    uint64_t* full = warp == kFlashKWarp ? kfull : vfull;
-    for (int t = 0; t < pre; ++t) {
-      mbar_arrive_expect_tx(&full[t], kStage);
+    pre = min((nkp0 + kFT - 1) / kFT, 1);
+    if (pre) {
+      mbar_arrive_expect_tx(&kfull[0], kStage);
 #pragma unroll
       for (int hv = 0; hv < H; ++hv)
-        tma_load_2d(ring + t * kStage + hv * kFT * 128, map, &full[t], hv * 64,
-                    seg * P_max + k0 + t * kFT);
+        tma_load_2d(Kr + hv * kFT * 128, &kmap, &kfull[0], hv * 64, seg * P_max + k0);
     }
   }
   griddep_enter();
@@ -184,6 +183,7 @@ __global__ void __launch_bounds__(kFlashThreads, 1)
         tma_load_3d(Qs + hv * kTileM * 128, &qmap, &barQ, hv * 64, g * G, n * B + b0);
       for (int t = pre; t < nt; ++t) {
         const int s = t & 1;
+        if (t == 1 && !mbar_wait(&kfull[0], 0)) bad |= 1u;  // the first tile has landed
         if (t >= 2 && !mbar_wait(&kempty[s], ((t >> 1) - 1) & 1)) bad |= 1u;
         uint8_t* dst = Kr + s * kStage;
         if (t < npt) {
@@ -203,7 +203,10 @@ __global__ void __launch_bounds__(kFlashThreads, 1)
   } else if (warp == kFlashVWarp) {
     // ---------------------------------------------------------- V tiles
     if (lane == 0) {
-      for (int t = pre; t < nt; ++t) {
+      // V_0 is needed after the first softmax step: after the query tile
+      // (issued with the first K tile; a single-use barrier)
+      if (nt > 0 && !mbar_wait(&barQ, 0)) bad |= 2u;
+      for (int t = 0; t < nt; ++t) {
         const int s = t & 1;
         if (t >= 2 && !mbar_wait(&vempty[s], ((t >> 1) - 1) & 1)) bad |= 2u;
         uint8_t* dst = Vr + s * kStage;
