@@ -155,31 +155,44 @@ def workload():
     return getattr(W, WORKLOADS[_WORKLOAD])
 
 
-def kernel_source_hash() -> str:
+def _code_only(path: str) -> str:
+    """A source file without its comments and blank lines."""
+    text = re.sub(r"/\*.*?\*/", "", open(path).read(), flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.split("\n"))
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
+def kernel_source_hash(kernel: str = None) -> str:
     """Hash of the kernel sources without their comments and blank lines: a
-    committed ncu summary stays valid across edits that change no code."""
+    committed ncu summary stays valid across edits that change no code.  With
+    `kernel`, only the .cu file that defines it and the device headers (.cuh)
+    are hashed, so that a summary of one kernel survives edits to another."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_diffusion_sparse_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        text = re.sub(r"/\*.*?\*/", "", open(os.path.join(csrc, f)).read(), flags=re.S)
-        lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.split("\n"))
-        h.update("\n".join(ln for ln in lines if ln.strip()).encode())
+    files = sorted(os.listdir(csrc))
+    if kernel is not None:
+        pat = re.compile(r"__global__[^;{]*?\b" + re.escape(kernel) + r"\s*\(", re.S)
+        defining = [f for f in files if f.endswith(".cu") and
+                    pat.search(open(os.path.join(csrc, f)).read())]
+        files = defining + [f for f in files if f.endswith(".cuh")]
+    for f in files:
+        h.update(_code_only(os.path.join(csrc, f)).encode())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, src_hash: str, workload: str):
+def ncu_traffic(kernel: str, workload: str):
     """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
-    summary, if the summary was taken on the current kernel sources; else
-    None."""
+    summary, if the summary was taken on the current source of that kernel;
+    else None."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         d = json.load(open(p))
     except Exception:
         return None
-    if d.get("source_hash") != src_hash:
-        return None
     e = d.get("workloads", {}).get(workload, {}).get("kernels", {}).get(kernel)
-    return e.get("dram_bytes_per_launch_full_workload") if e else None
+    if not e or e.get("source_hash") != kernel_source_hash(kernel):
+        return None
+    return e.get("dram_bytes_per_launch_full_workload")
 
 
 class Bench:
@@ -715,8 +728,6 @@ def measure(w, args, dist, world, min_ms: float, serial: bool = True, e2e: bool 
     work = algorithmic_work(w, ns)
     pk, pk_kind = peaks()
     dominant = max(tot, key=tot.get) if tot else None
-    src_hash = kernel_source_hash()
-
     link_gbs = link_peak_gbs() if w.kv_on_host else None
 
     # the pool attention's launch duration in its chain (the dominant kernel of
@@ -741,7 +752,7 @@ def measure(w, args, dist, world, min_ms: float, serial: bool = True, e2e: bool 
             peak = pk["bf16_tflops"]
             unit = "TFLOP/s"
         return {"bound": wk["bound"], "achieved": ach, "peak": peak, "unit": unit,
-                "frac": ach / peak, "traffic": ncu_traffic(name, src_hash, w.name),
+                "frac": ach / peak, "traffic": ncu_traffic(name, w.name),
                 "kernel": name, "launch_us": d_s * 1e6,
                 "launch_timing": ("mean of back-to-back launches in a graph (a block's T "
                                   "steps, programmatic launch), CUDA events"
