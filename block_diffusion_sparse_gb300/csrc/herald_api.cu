@@ -10,6 +10,7 @@
 
 #include <map>
 #include <mutex>
+#include <set>
 #include <utility>
 #include <vector>
 
@@ -418,6 +419,30 @@ cudaError_t ensure_smem(const void* fn, size_t bytes) {
   return cudaSuccess;
 }
 
+cudaError_t ensure_nonportable_cluster(const void* fn) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  constexpr int kMemo = 8;
+  thread_local std::pair<const void*, int> memo[kMemo] = {};
+  thread_local int next = 0;
+  for (const auto& m : memo)
+    if (m.first == fn && m.second == dev) return cudaSuccess;
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> allowed;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!allowed.count({fn, dev})) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+      allowed.insert({fn, dev});
+    }
+  }
+  memo[next] = {fn, dev};
+  next = (next + 1) % kMemo;
+  return cudaSuccess;
+}
+
 void trace_before(cudaStream_t st, const char* name) {
   TraceState& t = g_trace;
   t.in_kernel = false;
@@ -758,10 +783,10 @@ herald_status herald_select_stage2_gather(herald_dims dims, const uint16_t* q_bl
   WsLayout w;
   HERALD_RET_IF(check_ws(dims, C, P_max, ws, ws_bytes, &w));
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool on_device = is_device_memory(k_cache) && is_device_memory(v_cache);
   const int segs = dims.N * dims.Hkv;
   const int copies = std::min(kFusedGatherMaxCopies, sm_count() / segs);
-  if (segs >= kFusedGatherMinSegs && copies >= 2 && is_device_memory(k_cache) &&
-      is_device_memory(v_cache)) {
+  if (segs >= kFusedGatherMinSegs && copies >= 2 && on_device) {
     const PoolGather pg{k_cache, v_cache, pool_k, pool_v, dims.d, copies};
     return run_stage2(dims, q_block, k_cache, ctx_len, cand, n_cand, C, K, sink, local, P_max,
                       idx, n_sel, ws, w, st, &pg);
@@ -952,7 +977,7 @@ herald_status denoise_attn(herald_dims dims, const uint16_t* q, const uint16_t* 
       HERALD_ATTN_SETTLED | HERALD_ATTN_APPEND | HERALD_ATTN_ADVANCE | (0xFu << 8);
   if (flags & ~kKnown) return fail(HERALD_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags & ~kKnown);
   const unsigned kernel = (flags >> 8) & 0xFu;
-  if (kernel > (HERALD_ATTN_KERNEL_FLASH_CS8 >> 8))
+  if (kernel > (HERALD_ATTN_KERNEL_POOL_CS16 >> 8))
     return fail(HERALD_ERR_INVALID_ARG, "unknown kernel choice %u", kernel);
   const bool append = (flags & HERALD_ATTN_APPEND) != 0;
   if ((flags & HERALD_ATTN_ADVANCE) && !append)
@@ -976,12 +1001,14 @@ herald_status denoise_attn(herald_dims dims, const uint16_t* q, const uint16_t* 
   HERALD_RET_IF(check_ws(dims, 1, P_max, ws, ws_bytes, &w));
   if (scale == 0.f) scale = 1.0f / sqrtf(float(dims.d));
   PoolMaps maps;
-  const bool pool_ok = attn_pool_ok(dims, P_max), flash_ok = attn_flash_ok(dims);
+  const int pool_cs = attn_pool_cs(dims, P_max, int(kernel));
+  const bool pool_ok = pool_cs > 0, flash_ok = attn_flash_ok(dims);
   const bool pool = pool_ok || flash_ok;
+  maps.pool_cs = pool_cs;
   if (pool) {
     const uint64_t rows = uint64_t(dims.N) * dims.Hkv * P_max;
     if (pool_ok) {
-      const uint32_t box = uint32_t(attn_pool_kpc(P_max));
+      const uint32_t box = uint32_t(attn_pool_kpc(P_max, pool_cs));
       HERALD_RET_IF(encode_rows_map(pool_k, rows, dims.d, box, &maps.k));
       HERALD_RET_IF(encode_rows_map(pool_v, rows, dims.d, box, &maps.v));
     }

@@ -14,6 +14,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.cuh"
+#include "block_scan.cuh"
 #include "ptx.cuh"
 
 namespace herald {
@@ -605,68 +606,6 @@ __device__ __forceinline__ uint32_t warp_append_slot(bool take, uint32_t* counte
   return take ? base + uint32_t(__popc(mask & ((1u << lane) - 1u))) : 0xffffffffu;
 }
 
-// ============================================================ block scans
-// Block-wide exclusive prefix sum for 1024 threads; returns the total.
-template <int NT>
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* warp_tot,
-                                                    uint32_t& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) warp_tot[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t t = lane < NT / 32 ? warp_tot[lane] : 0u;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, t, o);
-      if (lane >= o) t += y;
-    }
-    if (lane < NT / 32) warp_tot[lane] = t;  // inclusive
-  }
-  __syncthreads();
-  const uint32_t before = (warp ? warp_tot[warp - 1] : 0u) + x - v;
-  total = warp_tot[NT / 32 - 1];
-  __syncthreads();
-  return before;
-}
-
-// Given a histogram h[0..nb) (in shared memory) and a rank `need` (1-based
-// count of largest elements wanted), finds the bin b holding the need-th
-// largest element; returns b and the count strictly above it.
-template <int NT>
-__device__ void find_bin_from_top(const uint32_t* h, int nb, uint32_t need, uint32_t* warp_tot,
-                                  int* out_bin, uint32_t* out_above) {
-  // thread t owns bins [t*per, (t+1)*per) counted from the TOP
-  const int per = (nb + NT - 1) / NT;
-  uint32_t local = 0;
-  for (int k = 0; k < per; ++k) {
-    const int rb = threadIdx.x * per + k;  // rank-order bin (0 = highest)
-    if (rb < nb) local += h[nb - 1 - rb];
-  }
-  uint32_t total;
-  const uint32_t before = block_excl_scan<NT>(local, warp_tot, total);
-  if (before < need && need <= before + local) {
-    uint32_t acc = before;
-    for (int k = 0; k < per; ++k) {
-      const int rb = threadIdx.x * per + k;
-      if (rb >= nb) break;
-      const uint32_t c = h[nb - 1 - rb];
-      if (acc + c >= need) {
-        *out_bin = nb - 1 - rb;
-        *out_above = acc;
-        break;
-      }
-      acc += c;
-    }
-  }
-  __syncthreads();
-}
-
 // ============================================================ topc_finish
 // One CTA of 1024 threads per (n, g).  Radix select of the C-th largest s1:
 // the first 12-bit digit comes from the global histogram; the members of
@@ -676,40 +615,6 @@ __device__ void find_bin_from_top(const uint32_t* h, int nb, uint32_t need, uint
 // lowest-position ties, with one two-counter block scan.
 constexpr int kSelThreads = 1024;
 constexpr int kTieCap = 6144;
-
-// Block-wide exclusive scan of two counters at once (NT threads).
-template <int NT = 1024>
-__device__ __forceinline__ void block_excl_scan2(uint32_t a, uint32_t b, uint32_t* wa,
-                                                 uint32_t* wb, uint32_t& ea, uint32_t& eb,
-                                                 uint32_t& ta, uint32_t& tb) {
-  constexpr int NW = NT / 32;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t x = a, y = b;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t xa = __shfl_up_sync(0xffffffffu, x, o);
-    const uint32_t yb = __shfl_up_sync(0xffffffffu, y, o);
-    if (lane >= o) { x += xa; y += yb; }
-  }
-  if (lane == 31) { wa[warp] = x; wb[warp] = y; }
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t u = lane < NW ? wa[lane] : 0u, v = lane < NW ? wb[lane] : 0u;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t ua = __shfl_up_sync(0xffffffffu, u, o);
-      const uint32_t vb = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) { u += ua; v += vb; }
-    }
-    if (lane < NW) { wa[lane] = u; wb[lane] = v; }
-  }
-  __syncthreads();
-  ea = (warp ? wa[warp - 1] : 0u) + x - a;
-  eb = (warp ? wb[warp - 1] : 0u) + y - b;
-  ta = wa[NW - 1];
-  tb = wb[NW - 1];
-  __syncthreads();
-}
 
 // Elements of s1 are processed in rounds of kSelThreads * kPerThr: thread t
 // holds the kPerThr consecutive values [base + t*kPerThr, ...) in registers,

@@ -48,6 +48,51 @@ __device__ __forceinline__ void st_cluster_f2(uint32_t addr, float x, float y) {
                : "memory");
 }
 
+constexpr int kTcThreads = 256;  // 8 warps: lane quadrant = warp % 4
+
+// Copies `rows` rows of D bf16 (row r from src_of(r), or zeros when src_of
+// returns nullptr) into a K-major 128B-swizzled tile: D/64 column halves,
+// each [rows_alloc][128 bytes].  `any_src` is a valid global address used
+// as the (unread) source of zero-filled chunks.  A warp copies 32/(D/8)
+// whole rows per step (one 16-byte chunk per lane), so src_of runs once
+// per lane and step, and the unrolled steps keep several rows in flight.
+// Every thread of the (kTcThreads-thread) block must call it.
+template <int D, typename SrcOf>
+__device__ __forceinline__ void load_rows_sw128(uint8_t* tile, int rows, int rows_alloc,
+                                                const uint16_t* any_src, SrcOf src_of) {
+  constexpr int CPR = D / 8;        // 16-byte chunks per row
+  constexpr int RPW = 32 / CPR;     // rows per warp step
+  constexpr int kStep = (kTcThreads / 32) * RPW;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = lane % CPR, sub = lane / CPR;
+  uint8_t* half = tile + (c >> 3) * (rows_alloc * 128);
+#pragma unroll 4
+  for (int r0 = warp * RPW; r0 < rows; r0 += kStep) {
+    const int r = r0 + sub;
+    if (r < rows) {
+      const uint16_t* s = src_of(r);
+      cp_async_16(half + sw128_off(r, c & 7), s ? s + c * 8 : any_src, s ? 16u : 0u);
+    }
+  }
+}
+
+// Full cluster barrier (hardware): release this CTA's shared-memory writes,
+// acquire the peers'.
+__device__ __forceinline__ void cluster_sync_all() {
+  __cluster_barrier_arrive();
+  __cluster_barrier_wait();
+}
+// shared::cluster address of the same shared-memory location in CTA `rank`.
+__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_peer_f2(uint32_t a, float2 v) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(v.x), "f"(v.y)
+               : "memory");
+}
+
 // Launches a kernel as clusters of cluster_x CTAs along x, with programmatic
 // stream serialisation, bracketed by the tracing hooks.
 template <typename... KArgs, typename... Args>

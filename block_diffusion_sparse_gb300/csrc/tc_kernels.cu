@@ -24,56 +24,14 @@
 #include <cuda_bf16.h>
 #include <stdlib.h>
 
+#include <mutex>
+
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "tc_common.cuh"
 
 namespace herald {
 
-constexpr int kTcThreads = 256;  // 8 warps: lane quadrant = warp % 4
-
-// Copies `rows` rows of D bf16 (row r from src_of(r), or zeros when src_of
-// returns nullptr) into a K-major 128B-swizzled tile: D/64 column halves,
-// each [rows_alloc][128 bytes].  `any_src` is a valid global address used
-// as the (unread) source of zero-filled chunks.  A warp copies 32/(D/8)
-// whole rows per step (one 16-byte chunk per lane), so src_of runs once
-// per lane and step, and the unrolled steps keep several rows in flight.
-// Every thread of the (kTcThreads-thread) block must call it.
-template <int D, typename SrcOf>
-__device__ __forceinline__ void load_rows_sw128(uint8_t* tile, int rows, int rows_alloc,
-                                                const uint16_t* any_src, SrcOf src_of) {
-  constexpr int CPR = D / 8;        // 16-byte chunks per row
-  constexpr int RPW = 32 / CPR;     // rows per warp step
-  constexpr int kStep = (kTcThreads / 32) * RPW;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c = lane % CPR, sub = lane / CPR;
-  uint8_t* half = tile + (c >> 3) * (rows_alloc * 128);
-#pragma unroll 4
-  for (int r0 = warp * RPW; r0 < rows; r0 += kStep) {
-    const int r = r0 + sub;
-    if (r < rows) {
-      const uint16_t* s = src_of(r);
-      cp_async_16(half + sw128_off(r, c & 7), s ? s + c * 8 : any_src, s ? 16u : 0u);
-    }
-  }
-}
-
-// Full cluster barrier (hardware): release this CTA's shared-memory writes,
-// acquire the peers'.
-__device__ __forceinline__ void cluster_sync_all() {
-  __cluster_barrier_arrive();
-  __cluster_barrier_wait();
-}
-// shared::cluster address of the same shared-memory location in CTA `rank`.
-__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void st_peer_f2(uint32_t a, float2 v) {
-  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(v.x), "f"(v.y)
-               : "memory");
-}
 __device__ __forceinline__ float2 ld_peer_f2(uint32_t a) {
   float2 v;
   asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
@@ -1103,28 +1061,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 // ============================================================= attn_pool
-// Sparse block attention, one 8-CTA cluster per (sequence, KV head, row
-// tile of bpt whole tokens = bpt*G <= 128 query rows).  The pool is split
-// evenly: CTA r owns pool keys [r*kpc, (r+1)*kpc) (kpc = ceil(P_max/8)
-// rounded to 16, kpc + B <= 256), loaded by two 2-D TMA boxes each for K and
+// Sparse block attention, one cluster of CS = 8 or 16 CTAs per (sequence,
+// KV head, row tile of bpt whole tokens = bpt*G <= 128 query rows).  The
+// pool is split evenly: CTA r owns pool keys [r*kpc, (r+1)*kpc) (kpc =
+// ceil(P_max/CS) rounded to 16, kpc + B <= 256), loaded by two 2-D TMA boxes each for K and
 // V; the last CTA also owns the B block keys.  The query tile and the block
 // keys and values are 3-D TMA boxes (every operand is one bulk transfer,
 // issued by one thread as soon as the predecessor kernel is done).  Each
 // CTA computes S = Q K^T for its keys with one UMMA (N = kpc), P = exp(S -
 // rowmax) in bf16 (written over the Q/K operands, dead once S is in TMEM),
-// O = P V into TMEM.  Rows are finalised 16 per CTA: each CTA stages its O
-// rows divided by their row sums (fp16) over the dead operands and pushes
-// rows [c*16, c*16 + 16) with their (max, sum) to CTA c by bulk
-// shared::cta -> shared::cluster copies that complete on c's mbarrier;
-// each CTA merges its 16 rows once all 8 slices have landed.  The receive
+// O = P V into TMEM.  Rows are finalised 128/CS per CTA: each CTA stages
+// its O rows divided by their row sums (fp16) over the dead operands and
+// pushes rows [c*128/CS, (c+1)*128/CS) with their (max, sum) to CTA c by
+// bulk shared::cta -> shared::cluster copies that complete on c's mbarrier;
+// each CTA merges its rows once all CS slices have landed.  16-CTA clusters
+// (a non-portable size) halve each CTA's keys -- its UMMAs and its share of
+// the exponentials -- where every cluster of the launch is resident at once.  The receive
 // buffers have shared memory of their own, so no cluster-wide barrier
 // separates the attention from the exchange.  Only the 16-key chunks that
 // hold a valid key enter S, the softmax and P V.  Two options of the entry
 // point: the pool keys loaded before the grid-dependency wait (steps after
 // a block's first, when the pool is settled), and the append of the block
 // to the cache by one cluster per sequence (the last step).
-constexpr int kPoolCtas = 8;
-constexpr int kPoolRows = kTileM / kPoolCtas;   // rows finalised per CTA
 constexpr int kPoolMaxB = 64;
 // S takes TMEM columns [0, kpc + Bp) and O starts at column 256
 constexpr int kPoolMaxCols = 256;
@@ -1146,12 +1104,13 @@ __host__ __device__ inline PoolSmem pool_smem(int D, int kpc, int Bp) {
   L.v = ((a_end > p_end ? a_end : p_end) + 1023u) & ~1023u;
   L.vb = L.v + H * uint32_t(kpc) * 128u;
   L.recv_o = L.vb + H * uint32_t(Bp) * 128u;
-  L.recv_ml = L.recv_o + uint32_t(kPoolCtas * kPoolRows) * uint32_t(D + 8) * 2u;
-  L.total = L.recv_ml + uint32_t(kPoolCtas * kPoolRows) * 8u + 1024u;
+  // CS slices of 128/CS rows each: 128 rows whatever the cluster size
+  L.recv_ml = L.recv_o + uint32_t(kTileM) * uint32_t(D + 8) * 2u;
+  L.total = L.recv_ml + uint32_t(kTileM) * 8u + 1024u;
   return L;
 }
 
-template <int D>
+template <int D, int CS>
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_pool_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap,
@@ -1163,6 +1122,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                      uint32_t* err, AppendArgs app, int L_max) {
   constexpr int H = D / 64;
   constexpr int OROW = D + 8;  // fp16 row stride of O partials (16-byte padding)
+  constexpr int kPoolCtas = CS;
+  constexpr int kPoolRows = kTileM / CS;  // rows finalised per CTA
+  static_assert(CS == 8 || CS == 16, "pool attention clusters of 8 or 16 CTAs");
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t barK, barV, bar0, bar1, barR;
   __shared__ uint32_t tmem_base;
@@ -1481,7 +1443,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     app.ctx[n] = min(L0 + B, L_max);
   }
 
-  // merge this CTA's 16 rows from the 8 received partials:
+  // merge this CTA's rows from the CS received partials:
   // out = sum_c 2^(m_c - M) l_c (o_c / l_c) / sum_c 2^(m_c - M) l_c
   constexpr int E = D / 32;
   for (int rr = warp; rr < kPoolRows; rr += kTcThreads / 32) {
@@ -1609,10 +1571,12 @@ static int max_active_clusters() {
   return cache[dev];
 }
 
-// How many 8-CTA clusters of the pool attention kernel with `smem` bytes of
-// dynamic shared memory can be resident at once; cached per device for the
-// last few sizes asked.
-template <int D>
+// How many CS-CTA clusters of the pool attention kernel with `smem` bytes of
+// dynamic shared memory can be resident at once (a 16-CTA cluster needs 16
+// free SMs of one GPC); cached per device for the last few sizes asked.
+// The kernel's shared-memory grant (and, for 16, the non-portable cluster
+// size) is made first: the query needs it.
+template <int D, int CS>
 static int pool_resident_clusters(uint32_t smem) {
   struct Entry {
     int dev;
@@ -1621,40 +1585,73 @@ static int pool_resident_clusters(uint32_t smem) {
   };
   static Entry cache[8] = {};
   static int next = 0;
+  static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  for (const Entry& e : cache)
-    if (e.n > 0 && e.dev == dev && e.smem == smem) return e.n;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry& e : cache)
+      if (e.n > 0 && e.dev == dev && e.smem == smem) return e.n;
+  }
+  if (ensure_smem(attn_pool_kernel<D, CS>, smem) != cudaSuccess ||
+      (CS > 8 && ensure_nonportable_cluster(attn_pool_kernel<D, CS>) != cudaSuccess)) {
+    cudaGetLastError();
+    return 0;
+  }
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(kPoolCtas, 1, 1);
+  cfg.gridDim = dim3(CS, 1, 1);
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kPoolCtas;
+  attr[0].val.clusterDim.x = CS;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, attn_pool_kernel<D>, &cfg) != cudaSuccess) n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, attn_pool_kernel<D, CS>, &cfg) != cudaSuccess) n = 0;
   cudaGetLastError();
   if (n > 0) {
+    std::lock_guard<std::mutex> lock(mu);
     cache[next] = Entry{dev, smem, n};
     next = (next + 1) % 8;
   }
   return n;
 }
 
-int attn_pool_kpc(int P_max) { return cdiv(cdiv(P_max, kPoolCtas), 16) * 16; }
+int attn_pool_kpc(int P_max, int cs) { return cdiv(cdiv(P_max, cs), 16) * 16; }
 int attn_pool_bpt(const herald_dims& dm) { return kTileM / (dm.Hq / dm.Hkv); }
 
-bool attn_pool_ok(const herald_dims& dm, int P_max) {
-  const int kpc = attn_pool_kpc(P_max);
+static uint32_t attn_pool_smem(const herald_dims& dm, int P_max, int cs) {
+  return pool_smem(dm.d, attn_pool_kpc(P_max, cs), (dm.B + 15) & ~15).total;
+}
+
+static bool attn_pool_fits(const herald_dims& dm, int P_max, int cs) {
+  const int kpc = attn_pool_kpc(P_max, cs);
   const int Bp = (dm.B + 15) & ~15;
   // the dynamic allocation plus the kernel's static shared memory (~3 KB)
   return kpc + Bp <= kPoolMaxCols && Bp <= kPoolMaxB &&
-         pool_smem(dm.d, kpc, Bp).total <= 220u * 1024u;
+         attn_pool_smem(dm, P_max, cs) <= 220u * 1024u;
+}
+
+static int pool_resident(const herald_dims& dm, int P_max, int cs) {
+  const uint32_t smem = attn_pool_smem(dm, P_max, cs);
+  if (dm.d == 128)
+    return cs == 16 ? pool_resident_clusters<128, 16>(smem) : pool_resident_clusters<128, 8>(smem);
+  return cs == 16 ? pool_resident_clusters<64, 16>(smem) : pool_resident_clusters<64, 8>(smem);
+}
+
+int attn_pool_cs(const herald_dims& dm, int P_max, int choice) {
+  const bool f8 = attn_pool_fits(dm, P_max, 8), f16 = attn_pool_fits(dm, P_max, 16);
+  if (choice == 6) return f8 ? 8 : 0;
+  if (choice == 7) return f16 && pool_resident(dm, P_max, 16) > 0 ? 16 : 0;
+  // 16-CTA clusters when every cluster of the launch is resident at once
+  // (32K layer, 1 x 4 KV heads, 8 row tiles: 7.2 -> X us per step), else 8
+  const int units = cdiv(dm.B, attn_pool_bpt(dm)) * dm.N * dm.Hkv;
+  if (f16 && units <= pool_resident(dm, P_max, 16)) return 16;
+  if (f8) return 8;
+  return f16 && pool_resident(dm, P_max, 16) > 0 ? 16 : 0;
 }
 
 // the attention without the pool kernel: whole-cluster or split-key kernels
@@ -1703,30 +1700,34 @@ static cudaError_t launch_attn_t(const herald_dims& dm, const uint16_t* q, const
                                  const AppendArgs* app, int kernel, cudaStream_t st) {
   const int segs = dm.N * dm.Hkv;
   cudaError_t e;
-  const bool pool_ok = (kernel & 0x100) != 0, flash_ok = (kernel & 0x200) != 0;
+  const bool pool_ok = (kernel & 0x100) != 0 && maps && maps->pool_cs > 0;
+  const bool flash_ok = (kernel & 0x200) != 0;
   const int choice = kernel & 0xF;  // HERALD_ATTN_KERNEL_* >> 8
   if (maps && !force_split()) {
     const int tiles = cdiv(dm.B, maps->bpt);
-    const int kpc = attn_pool_kpc(P_max);
-    const uint32_t smem = pool_ok ? pool_smem(D, kpc, (dm.B + 15) & ~15).total : 0u;
-    if (pool_ok) {  // granted before the occupancy query, which needs it
-      e = ensure_smem(attn_pool_kernel<D>, smem);
-      if (e != cudaSuccess) return e;
-    }
+    const int cs = maps->pool_cs;
     // the pool kernel while its clusters fit the device at once, else the
     // pipelined kernel (one wave with fewer CTAs per row tile)
-    bool use_pool = pool_ok && (choice == 1 || !flash_ok ||
-                                (choice == 0 && tiles * segs <= pool_resident_clusters<D>(smem)));
-    if (choice >= 2 && flash_ok) use_pool = false;
+    const int resident = pool_ok ? pool_resident(dm, P_max, cs) : 0;
+    bool use_pool = pool_ok && (choice == 1 || choice == 6 || choice == 7 || !flash_ok ||
+                                (choice == 0 && tiles * segs <= resident));
+    if (choice >= 2 && choice <= 5 && flash_ok) use_pool = false;
     if (use_pool) {
+      const int kpc = attn_pool_kpc(P_max, cs);
+      const uint32_t smem = attn_pool_smem(dm, P_max, cs);
       // early loads pay only when every CTA of the grid is resident at once:
       // with a second wave they measured slower (on the 4 x 64K layer)
-      const int early = settled && tiles * segs <= pool_resident_clusters<D>(smem) ? 1 : 0;
+      const int early = settled && tiles * segs <= resident ? 1 : 0;
       const AppendArgs none{nullptr, nullptr, nullptr, nullptr, nullptr, 0};
-      return launch_cluster("attn_pool_kernel", attn_pool_kernel<D>,
-                            dim3(kPoolCtas, tiles, segs), kPoolCtas, smem, st, maps->k, maps->v,
-                            maps->q, maps->bk, maps->bv, n_sel, P_max, dm.B, dm.Hq, dm.Hkv,
-                            maps->bpt, kpc, scale, early, out, err, app ? *app : none, dm.L_max);
+      if (cs == 16)
+        return launch_cluster("attn_pool_kernel", attn_pool_kernel<D, 16>, dim3(16, tiles, segs),
+                              16, smem, st, maps->k, maps->v, maps->q, maps->bk, maps->bv, n_sel,
+                              P_max, dm.B, dm.Hq, dm.Hkv, maps->bpt, kpc, scale, early, out, err,
+                              app ? *app : none, dm.L_max);
+      return launch_cluster("attn_pool_kernel", attn_pool_kernel<D, 8>, dim3(8, tiles, segs), 8,
+                            smem, st, maps->k, maps->v, maps->q, maps->bk, maps->bv, n_sel, P_max,
+                            dm.B, dm.Hq, dm.Hkv, maps->bpt, kpc, scale, early, out, err,
+                            app ? *app : none, dm.L_max);
     }
     if (flash_ok) {
       const int cs = choice == 3 ? 2 : choice == 4 ? 4 : choice == 5 ? 8 : 0;

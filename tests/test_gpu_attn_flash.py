@@ -1,6 +1,7 @@
 """The pipelined attention kernel (key tiles streamed through shared
-memory, 8, 4 or 2 CTAs per row tile) against the fp64 oracle and against
-the cluster pool kernel, over the shapes of the workloads: GQA groups that
+memory, 8, 4 or 2 CTAs per row tile) and the cluster pool kernel (a whole
+pool slice per CTA, 8 or 16 CTAs per row tile) against the fp64 oracle and
+against each other, over the shapes of the workloads: GQA groups that
 fill one row tile or need two, both head dimensions, single-token blocks,
 ragged and empty selections, pools larger than the pool kernel takes, and
 the append of the last denoising step.  Attention outputs within 2e-2 of
@@ -27,6 +28,7 @@ def _cuda():
 
 CS_FLAGS = {2: H.HERALD_ATTN_KERNEL_FLASH_CS2, 4: H.HERALD_ATTN_KERNEL_FLASH_CS4,
             8: H.HERALD_ATTN_KERNEL_FLASH_CS8}
+POOL_FLAGS = {8: H.HERALD_ATTN_KERNEL_POOL_CS8, 16: H.HERALD_ATTN_KERNEL_POOL_CS16}
 
 
 def _w(name, **kw):
@@ -91,33 +93,51 @@ def test_flash_attention_matches_oracle(w, cs):
         assert err <= ATTN_ATOL, f"{w.name} CS={cs} step {t}: max abs err {err}"
 
 
+@pytest.mark.parametrize("cs", [16, 8])
+@pytest.mark.parametrize("w", SHAPES, ids=lambda w: w.name)
+def test_pool_attention_matches_oracle(w, cs):
+    """The cluster pool kernel with 16 CTAs per row tile (kpc = P/16 keys
+    each, 8 rows merged per CTA) and with 8; the 8-CTA form does not take
+    the big pool (kpc + B > 256), which the 16-CTA form does."""
+    x, idx, ns, pk, pv = _setup(w, seed=20 + cs)
+    for t in range(w.T):
+        out = _run(w, x, pk, pv, ns, t, POOL_FLAGS[cs] | (H.HERALD_ATTN_SETTLED if t else 0))
+        ref = oracle.sparse_attn(f64(x["q_steps"][t]), f64(x["k_cache"]), f64(x["v_cache"]), idx,
+                                 ns, f64(x["block_k"][t]), f64(x["block_v"][t]))
+        err = np.abs(bf16_dev_to_f64(out) - ref).max()
+        assert err <= ATTN_ATOL, f"{w.name} pool CS={cs} step {t}: max abs err {err}"
+
+
 @pytest.mark.parametrize("w", SHAPES[:4], ids=lambda w: w.name)
 def test_flash_and_pool_kernels_agree(w):
     """Both kernels compute the same softmax over the same keys; they differ
     only in the order of fp32 sums and in where P is rounded to bf16."""
     x, idx, ns, pk, pv = _setup(w, seed=7)
     a = bf16_dev_to_f64(_run(w, x, pk, pv, ns, 0, H.HERALD_ATTN_KERNEL_POOL))
-    for cs in (8, 4, 2):
-        b = bf16_dev_to_f64(_run(w, x, pk, pv, ns, 0, CS_FLAGS[cs]))
-        assert np.abs(a - b).max() <= ATTN_ATOL, cs
+    for f in (CS_FLAGS[8], CS_FLAGS[4], CS_FLAGS[2], POOL_FLAGS[8], POOL_FLAGS[16]):
+        b = bf16_dev_to_f64(_run(w, x, pk, pv, ns, 0, f))
+        assert np.abs(a - b).max() <= ATTN_ATOL, hex(f)
 
 
-@pytest.mark.parametrize("cs", [8, 2])
-def test_flash_last_step_appends_like_append_kv(cs):
-    """The append rides with the pipelined kernel too (the softmax warps of
-    the first row tile's cluster of KV head 0): the cache rows and the
-    context lengths bit-exactly as herald_append_kv, the same output."""
+@pytest.mark.parametrize("kf", ["flash8", "flash2", "pool8", "pool16"])
+def test_flash_last_step_appends_like_append_kv(kf):
+    """The append rides with the attention (in the pipelined kernel the
+    softmax warps of the first row tile's cluster of KV head 0, in the pool
+    kernel that cluster's CTAs): the cache rows and the context lengths
+    bit-exactly as herald_append_kv, the same output."""
+    flag = {"flash8": CS_FLAGS[8], "flash2": CS_FLAGS[2], "pool8": POOL_FLAGS[8],
+            "pool16": POOL_FLAGS[16]}[kf]
     w = _w("append", L=300, C=64, K=32, S=4, W=4, extra_rows=40, index=96)
     x, idx, ns, pk, pv = _setup(w, seed=3)
     x["ctx"] = np.array([300, 330], np.int32)
     d = H.dims_of(w)
-    out_plain = _run(w, x, pk, pv, ns, 0, CS_FLAGS[cs])
+    out_plain = _run(w, x, pk, pv, ns, 0, flag)
     k, v, ctx = dev(x["k_cache"]), dev(x["v_cache"]), dev(x["ctx"])
     ws = torch.zeros(H.herald_workspace_size(d, 1, w.P), dtype=torch.uint8, device="cuda")
     out = torch.zeros_like(out_plain)
     H.herald_denoise_attn_ex(d, dev(x["q_steps"][0]), dev(pk), dev(pv), dev(ns), w.P,
                              dev(x["block_k"][0]), dev(x["block_v"][0]), out, 0.0,
-                             CS_FLAGS[cs] | H.HERALD_ATTN_APPEND | H.HERALD_ATTN_ADVANCE, ctx, k,
+                             flag | H.HERALD_ATTN_APPEND | H.HERALD_ATTN_ADVANCE, ctx, k,
                              v, ws)
     torch.cuda.synchronize()
     assert H.herald_workspace_error(ws) == 0

@@ -13,7 +13,8 @@ exactly, stage by stage:
   stage 1      top-C of s1 with more copies than C
   stage 2      top-K of s2 with more copies than K (fused refine, and the
                two-pass refine with 16 scores per top-K thread), also through
-               the stage-2 + gather call with many (sequence, KV head) pairs
+               the stage-2 + gather call (many (sequence, KV head) pairs, and
+               few with one and with two row tiles)
   exact        top-K of the exact score with more copies than K
   blocks       top-C_blocks over block means, with whole copied blocks
 """
@@ -145,11 +146,18 @@ def test_stage2_ties_take_the_lowest_positions(w, copies):
     np.testing.assert_array_equal(b["idx"].cpu().numpy(), idx_o)
 
 
-def test_stage2_gather_ties_with_many_pairs():
-    """>= 16 (sequence, KV head) pairs: the top-K runs as several copies per
-    pair that each gather a slice of the pool; every copy must break the
-    ties alike, and the pool rows must be the lowest copies' rows."""
-    w = _w("s2-pairs16", N=4, Hq=16, Hkv=4, L=2000, C=256, K=40, index=65)
+@pytest.mark.parametrize("w", [
+    _w("s2-pairs16", N=4, Hq=16, Hkv=4, L=2000, C=256, K=40, index=65),
+    _w("s2-few-pairs-one-tile", N=2, Hq=8, Hkv=2, L=2000, C=256, K=40, index=67),
+    _w("s2-few-pairs-two-tiles", N=1, Hq=14, Hkv=2, B=32, L=2500, C=512, K=40, index=68),
+], ids=lambda w: w.name)
+def test_stage2_gather_ties(w):
+    """The stage-2 + gather call.  With >= 16 (sequence, KV head) pairs the
+    top-K runs as several copies per pair that each gather a slice of the
+    pool: every copy must break the ties alike.  With few pairs the gather
+    is a kernel of its own after the top-K (the group's query rows in one
+    128-row tile, or in two, whose s2 partials the top-K adds).  The pool
+    rows must be the lowest copies' rows."""
     x, pos = _tied_layer(w, 90, seed=73)
     b = _bufs(w)
     kf = f64(x["k_cache"])
