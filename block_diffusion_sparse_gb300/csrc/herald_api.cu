@@ -977,7 +977,7 @@ herald_status denoise_attn(herald_dims dims, const uint16_t* q, const uint16_t* 
       HERALD_ATTN_SETTLED | HERALD_ATTN_APPEND | HERALD_ATTN_ADVANCE | (0xFu << 8);
   if (flags & ~kKnown) return fail(HERALD_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags & ~kKnown);
   const unsigned kernel = (flags >> 8) & 0xFu;
-  if (kernel > (HERALD_ATTN_KERNEL_POOL_CS16 >> 8))
+  if (kernel > (HERALD_ATTN_KERNEL_POOL_CS12 >> 8))
     return fail(HERALD_ERR_INVALID_ARG, "unknown kernel choice %u", kernel);
   const bool append = (flags & HERALD_ATTN_APPEND) != 0;
   if ((flags & HERALD_ATTN_ADVANCE) && !append)
@@ -1008,7 +1008,7 @@ herald_status denoise_attn(herald_dims dims, const uint16_t* q, const uint16_t* 
   if (pool) {
     const uint64_t rows = uint64_t(dims.N) * dims.Hkv * P_max;
     if (pool_ok) {
-      const uint32_t box = uint32_t(attn_pool_kpc(P_max, pool_cs));
+      const uint32_t box = uint32_t(attn_pool_kpc(P_max, dims.B, pool_cs));
       HERALD_RET_IF(encode_rows_map(pool_k, rows, dims.d, box, &maps.k));
       HERALD_RET_IF(encode_rows_map(pool_v, rows, dims.d, box, &maps.v));
     }

@@ -242,10 +242,10 @@ cudaError_t launch_gather_staged(const herald_dims& dm, const int32_t* idx, cons
                                  const uint16_t* staged_v, const uint16_t* k_cache,
                                  const uint16_t* v_cache, uint16_t* pool_k, uint16_t* pool_v,
                                  cudaStream_t st);
-// Pool attention (balanced clusters of pool_cs = 8 or 16 CTAs, every
+// Pool attention (balanced clusters of pool_cs = 8, 12 or 16 CTAs, every
 // operand loaded by TMA) applies when attn_pool_cs() > 0; its tensor maps,
 // all bf16 with a box of 64 columns and 128-byte swizzle:
-//   k, v   pool rows [N*Hkv*P_max][d], box rows attn_pool_kpc(P_max, pool_cs)
+//   k, v   pool rows [N*Hkv*P_max][d], box rows attn_pool_kpc(P_max, B, pool_cs)
 //   q      queries [N*B][Hq][d], box {G heads, bpt tokens}
 //   bk, bv block keys / values [N*B][Hkv][d], box {1 head, B rounded to 16}
 // Row tiles hold bpt = attn_pool_bpt() whole tokens (bpt * G <= 128 rows).
@@ -265,11 +265,11 @@ bool attn_flash_ok(const herald_dims& dm);
 cudaError_t launch_attn_flash(const herald_dims& dm, const int32_t* n_sel, int P_max,
                               uint16_t* out, float scale, uint32_t* err, const PoolMaps& maps,
                               const AppendArgs* app, int cs, bool settled, cudaStream_t st);
-int attn_pool_kpc(int P_max, int cs);
+int attn_pool_kpc(int P_max, int B, int cs);
 int attn_pool_bpt(const herald_dims& dm);
 // The pool kernel's cluster size for these shapes and kernel choice
-// (HERALD_ATTN_KERNEL_* >> 8): 16 where every cluster of the launch can be
-// resident at once, else 8; 0 where the pool kernel does not apply.
+// (HERALD_ATTN_KERNEL_* >> 8): 16 or 12 where every cluster of the launch
+// can be resident at once, else 8; 0 where the pool kernel does not apply.
 int attn_pool_cs(const herald_dims& dm, int P_max, int choice);
 cudaError_t launch_attn(const herald_dims& dm, const uint16_t* q, const uint16_t* pool_k,
                         const uint16_t* pool_v, const int32_t* n_sel, int P_max,

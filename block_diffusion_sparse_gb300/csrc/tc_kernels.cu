@@ -1090,7 +1090,13 @@ constexpr int kPoolMaxCols = 256;
 struct PoolSmem {
   uint32_t q, k, kb, p, pb, v, vb, recv_o, recv_ml, total;
 };
-__host__ __device__ inline PoolSmem pool_smem(int D, int kpc, int Bp) {
+// Rows each CTA of a cs-CTA cluster finalises (even, so that every slice
+// of (max, sum) pairs is a whole number of 16-byte units).
+__host__ __device__ constexpr int pool_rows_per_cta(int cs) {
+  return ((kTileM + cs - 1) / cs + 1) & ~1;
+}
+
+__host__ __device__ inline PoolSmem pool_smem(int D, int kpc, int Bp, int cs) {
   const uint32_t H = uint32_t(D / 64);
   PoolSmem L;
   // region A: Q | K | K_block, later P | P_block
@@ -1104,9 +1110,10 @@ __host__ __device__ inline PoolSmem pool_smem(int D, int kpc, int Bp) {
   L.v = ((a_end > p_end ? a_end : p_end) + 1023u) & ~1023u;
   L.vb = L.v + H * uint32_t(kpc) * 128u;
   L.recv_o = L.vb + H * uint32_t(Bp) * 128u;
-  // CS slices of 128/CS rows each: 128 rows whatever the cluster size
-  L.recv_ml = L.recv_o + uint32_t(kTileM) * uint32_t(D + 8) * 2u;
-  L.total = L.recv_ml + uint32_t(kTileM) * 8u + 1024u;
+  // one slice of pool_rows_per_cta(cs) rows from each of the cs CTAs
+  const uint32_t recv_rows = uint32_t(cs * pool_rows_per_cta(cs));
+  L.recv_ml = L.recv_o + recv_rows * uint32_t(D + 8) * 2u;
+  L.total = L.recv_ml + recv_rows * 8u + 1024u;
   return L;
 }
 
@@ -1123,18 +1130,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr int H = D / 64;
   constexpr int OROW = D + 8;  // fp16 row stride of O partials (16-byte padding)
   constexpr int kPoolCtas = CS;
-  constexpr int kPoolRows = kTileM / CS;  // rows finalised per CTA
-  static_assert(CS == 8 || CS == 16, "pool attention clusters of 8 or 16 CTAs");
+  constexpr int kPoolRows = pool_rows_per_cta(CS);  // rows finalised per CTA (the last ones fewer)
+  static_assert(CS == 8 || CS == 12 || CS == 16, "pool attention clusters of 8, 12 or 16 CTAs");
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t barK, barV, bar0, bar1, barR;
   __shared__ uint32_t tmem_base;
   __shared__ float red_m[2][kTileM];
   __shared__ float red_s[2][kTileM];
   __shared__ __align__(16) float2 ml[kTileM];
-  constexpr uint32_t kSliceO = uint32_t(kPoolRows * OROW * 2);
+  constexpr uint32_t kSliceO = uint32_t(kPoolRows * OROW * 2);  // receive slot per sender
   constexpr uint32_t kSliceMl = uint32_t(kPoolRows * 8);
   const int Bp = (B + 15) & ~15;
-  const PoolSmem S = pool_smem(D, kpc, Bp);
+  const PoolSmem S = pool_smem(D, kpc, Bp, CS);
   uint8_t* base = align1024(smem_raw);
   uint8_t* Qs = base + S.q;
   uint8_t* Ks = base + S.k;
@@ -1149,13 +1156,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int mt = blockIdx.y, seg = blockIdx.z;
   const int n = seg / Hkv, g = seg - n * Hkv, G = Hq / Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // rows [c*kPoolRows, c*kPoolRows + rows_of(c)) are finalised by CTA c
+  auto rows_of = [](int c) { return min(max(kTileM - c * kPoolRows, 0), kPoolRows); };
+  const int my_rows = rows_of(int(rank));
   if (threadIdx.x == 0) {
     mbar_init(&barK, 1);
     mbar_init(&barV, 1);
     mbar_init(&bar0, 1);
     mbar_init(&bar1, 1);
     mbar_init(&barR, 1);
-    mbar_arrive_expect_tx(&barR, kPoolCtas * (kSliceO + kSliceMl));
+    mbar_arrive_expect_tx(&barR, uint32_t(kPoolCtas * my_rows) * uint32_t(OROW * 2 + 8));
     fence_mbar_init();
   }
   // peers' copies complete on barR: its initialisation is published
@@ -1423,14 +1433,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   __cluster_barrier_wait();  // every peer's barR is initialised
 
-  // push: rows [c*16, c*16+16) of this CTA's partial go to CTA c, slot `rank`
+  // push: rows [c*kPoolRows, c*kPoolRows + rows_of(c)) of this CTA's
+  // partial go to CTA c, slot `rank`
   if (threadIdx.x == 0) {
     for (uint32_t c = 0; c < uint32_t(kPoolCtas); ++c) {
+      const uint32_t rc = uint32_t(rows_of(int(c)));
+      if (rc == 0) continue;
       const uint32_t mb = cluster_addr(&barR, c);
       bulk_copy_to_peer(cluster_addr(reinterpret_cast<uint8_t*>(recv_o) + rank * kSliceO, c),
-                        Os + c * kPoolRows * OROW, kSliceO, mb);
+                        Os + c * kPoolRows * OROW, rc * uint32_t(OROW * 2), mb);
       bulk_copy_to_peer(cluster_addr(reinterpret_cast<uint8_t*>(recv_ml) + rank * kSliceMl, c),
-                        &ml[c * kPoolRows], kSliceMl, mb);
+                        &ml[c * kPoolRows], rc * 8u, mb);
     }
     bulk_commit();
   }
@@ -1446,7 +1459,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // merge this CTA's rows from the CS received partials:
   // out = sum_c 2^(m_c - M) l_c (o_c / l_c) / sum_c 2^(m_c - M) l_c
   constexpr int E = D / 32;
-  for (int rr = warp; rr < kPoolRows; rr += kTcThreads / 32) {
+  for (int rr = warp; rr < my_rows; rr += kTcThreads / 32) {
     const int lr = int(rank) * kPoolRows + rr;
     if (lr >= rows_t) break;  // warp-uniform: rows past the tile's tokens
     const int grow = b0 * G + lr;
@@ -1620,15 +1633,19 @@ static int pool_resident_clusters(uint32_t smem) {
   return n;
 }
 
-int attn_pool_kpc(int P_max, int cs) { return cdiv(cdiv(P_max, cs), 16) * 16; }
+// Pool keys per CTA: the pool and the block keys (which the last CTA takes
+// after its share of the pool) split evenly, in whole 16-key chunks.
+int attn_pool_kpc(int P_max, int B, int cs) {
+  return cdiv(cdiv(P_max + ((B + 15) & ~15), cs), 16) * 16;
+}
 int attn_pool_bpt(const herald_dims& dm) { return kTileM / (dm.Hq / dm.Hkv); }
 
 static uint32_t attn_pool_smem(const herald_dims& dm, int P_max, int cs) {
-  return pool_smem(dm.d, attn_pool_kpc(P_max, cs), (dm.B + 15) & ~15).total;
+  return pool_smem(dm.d, attn_pool_kpc(P_max, dm.B, cs), (dm.B + 15) & ~15, cs).total;
 }
 
 static bool attn_pool_fits(const herald_dims& dm, int P_max, int cs) {
-  const int kpc = attn_pool_kpc(P_max, cs);
+  const int kpc = attn_pool_kpc(P_max, dm.B, cs);
   const int Bp = (dm.B + 15) & ~15;
   // the dynamic allocation plus the kernel's static shared memory (~3 KB)
   return kpc + Bp <= kPoolMaxCols && Bp <= kPoolMaxB &&
@@ -1638,19 +1655,27 @@ static bool attn_pool_fits(const herald_dims& dm, int P_max, int cs) {
 static int pool_resident(const herald_dims& dm, int P_max, int cs) {
   const uint32_t smem = attn_pool_smem(dm, P_max, cs);
   if (dm.d == 128)
-    return cs == 16 ? pool_resident_clusters<128, 16>(smem) : pool_resident_clusters<128, 8>(smem);
-  return cs == 16 ? pool_resident_clusters<64, 16>(smem) : pool_resident_clusters<64, 8>(smem);
+    return cs == 16   ? pool_resident_clusters<128, 16>(smem)
+           : cs == 12 ? pool_resident_clusters<128, 12>(smem)
+                      : pool_resident_clusters<128, 8>(smem);
+  return cs == 16   ? pool_resident_clusters<64, 16>(smem)
+         : cs == 12 ? pool_resident_clusters<64, 12>(smem)
+                    : pool_resident_clusters<64, 8>(smem);
 }
 
 int attn_pool_cs(const herald_dims& dm, int P_max, int choice) {
-  const bool f8 = attn_pool_fits(dm, P_max, 8), f16 = attn_pool_fits(dm, P_max, 16);
+  const bool f8 = attn_pool_fits(dm, P_max, 8), f12 = attn_pool_fits(dm, P_max, 12),
+             f16 = attn_pool_fits(dm, P_max, 16);
   if (choice == 6) return f8 ? 8 : 0;
   if (choice == 7) return f16 && pool_resident(dm, P_max, 16) > 0 ? 16 : 0;
-  // 16-CTA clusters when every cluster of the launch is resident at once
-  // (32K layer, 1 x 4 KV heads, 8 row tiles: 7.2 -> X us per step), else 8
+  if (choice == 8) return f12 && pool_resident(dm, P_max, 12) > 0 ? 12 : 0;
+  // the largest cluster whose clusters are all resident at once (fewer keys
+  // per CTA shorten each step's chain), else 8
   const int units = cdiv(dm.B, attn_pool_bpt(dm)) * dm.N * dm.Hkv;
   if (f16 && units <= pool_resident(dm, P_max, 16)) return 16;
+  if (f12 && units <= pool_resident(dm, P_max, 12)) return 12;
   if (f8) return 8;
+  if (f12 && pool_resident(dm, P_max, 12) > 0) return 12;
   return f16 && pool_resident(dm, P_max, 16) > 0 ? 16 : 0;
 }
 
@@ -1709,11 +1734,11 @@ static cudaError_t launch_attn_t(const herald_dims& dm, const uint16_t* q, const
     // the pool kernel while its clusters fit the device at once, else the
     // pipelined kernel (one wave with fewer CTAs per row tile)
     const int resident = pool_ok ? pool_resident(dm, P_max, cs) : 0;
-    bool use_pool = pool_ok && (choice == 1 || choice == 6 || choice == 7 || !flash_ok ||
+    bool use_pool = pool_ok && (choice == 1 || choice >= 6 || !flash_ok ||
                                 (choice == 0 && tiles * segs <= resident));
     if (choice >= 2 && choice <= 5 && flash_ok) use_pool = false;
     if (use_pool) {
-      const int kpc = attn_pool_kpc(P_max, cs);
+      const int kpc = attn_pool_kpc(P_max, dm.B, cs);
       const uint32_t smem = attn_pool_smem(dm, P_max, cs);
       // early loads pay only when every CTA of the grid is resident at once:
       // with a second wave they measured slower (on the 4 x 64K layer)
@@ -1722,6 +1747,11 @@ static cudaError_t launch_attn_t(const herald_dims& dm, const uint16_t* q, const
       if (cs == 16)
         return launch_cluster("attn_pool_kernel", attn_pool_kernel<D, 16>, dim3(16, tiles, segs),
                               16, smem, st, maps->k, maps->v, maps->q, maps->bk, maps->bv, n_sel,
+                              P_max, dm.B, dm.Hq, dm.Hkv, maps->bpt, kpc, scale, early, out, err,
+                              app ? *app : none, dm.L_max);
+      if (cs == 12)
+        return launch_cluster("attn_pool_kernel", attn_pool_kernel<D, 12>, dim3(12, tiles, segs),
+                              12, smem, st, maps->k, maps->v, maps->q, maps->bk, maps->bv, n_sel,
                               P_max, dm.B, dm.Hq, dm.Hkv, maps->bpt, kpc, scale, early, out, err,
                               app ? *app : none, dm.L_max);
       return launch_cluster("attn_pool_kernel", attn_pool_kernel<D, 8>, dim3(8, tiles, segs), 8,

@@ -25,7 +25,8 @@ HERALD_ATTN_SETTLED, HERALD_ATTN_APPEND, HERALD_ATTN_ADVANCE = 1, 2, 4
 HERALD_ATTN_KERNEL_POOL, HERALD_ATTN_KERNEL_FLASH = 1 << 8, 2 << 8
 HERALD_ATTN_KERNEL_FLASH_CS2, HERALD_ATTN_KERNEL_FLASH_CS4, HERALD_ATTN_KERNEL_FLASH_CS8 = (
     3 << 8, 4 << 8, 5 << 8)
-HERALD_ATTN_KERNEL_POOL_CS8, HERALD_ATTN_KERNEL_POOL_CS16 = 6 << 8, 7 << 8
+HERALD_ATTN_KERNEL_POOL_CS8, HERALD_ATTN_KERNEL_POOL_CS16, HERALD_ATTN_KERNEL_POOL_CS12 = (
+    6 << 8, 7 << 8, 8 << 8)
 STATUS = {0: "HERALD_OK", 1: "HERALD_ERR_INVALID_ARG", 2: "HERALD_ERR_UNSUPPORTED_SHAPE",
           3: "HERALD_ERR_WORKSPACE_TOO_SMALL", 4: "HERALD_ERR_CUDA"}
 

@@ -315,8 +315,8 @@ herald_status herald_denoise_attn(herald_dims dims, const uint16_t *q, const uin
 #define HERALD_ATTN_APPEND 2u  /* also append block_k/block_v to the cache            */
 #define HERALD_ATTN_ADVANCE 4u /* with APPEND: then advance ctx_len                    */
 /* Kernel choice (bits 8-11; for tests and tuning -- the default picks by
- * shape): the cluster kernel holding a whole pool slice per CTA (with 8 or
- * 16 CTAs per row tile, or chosen by shape), or the pipelined kernel
+ * shape): the cluster kernel holding a whole pool slice per CTA (with 8,
+ * 12 or 16 CTAs per row tile, or chosen by shape), or the pipelined kernel
  * streaming key tiles (with 8, 4 or 2 CTAs per row tile, or chosen by
  * shape).  A choice the shapes do not allow falls back to the default. */
 #define HERALD_ATTN_KERNEL_POOL (1u << 8)
@@ -326,6 +326,7 @@ herald_status herald_denoise_attn(herald_dims dims, const uint16_t *q, const uin
 #define HERALD_ATTN_KERNEL_FLASH_CS8 (5u << 8)
 #define HERALD_ATTN_KERNEL_POOL_CS8 (6u << 8)
 #define HERALD_ATTN_KERNEL_POOL_CS16 (7u << 8)
+#define HERALD_ATTN_KERNEL_POOL_CS12 (8u << 8)
 
 /* herald_denoise_attn with options for the steps of a block (flags = 0 is
  * herald_denoise_attn; ctx_len, k_cache, v_cache are used only with

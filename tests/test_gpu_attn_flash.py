@@ -28,7 +28,8 @@ def _cuda():
 
 CS_FLAGS = {2: H.HERALD_ATTN_KERNEL_FLASH_CS2, 4: H.HERALD_ATTN_KERNEL_FLASH_CS4,
             8: H.HERALD_ATTN_KERNEL_FLASH_CS8}
-POOL_FLAGS = {8: H.HERALD_ATTN_KERNEL_POOL_CS8, 16: H.HERALD_ATTN_KERNEL_POOL_CS16}
+POOL_FLAGS = {8: H.HERALD_ATTN_KERNEL_POOL_CS8, 12: H.HERALD_ATTN_KERNEL_POOL_CS12,
+              16: H.HERALD_ATTN_KERNEL_POOL_CS16}
 
 
 def _w(name, **kw):
@@ -93,12 +94,13 @@ def test_flash_attention_matches_oracle(w, cs):
         assert err <= ATTN_ATOL, f"{w.name} CS={cs} step {t}: max abs err {err}"
 
 
-@pytest.mark.parametrize("cs", [16, 8])
+@pytest.mark.parametrize("cs", [16, 12, 8])
 @pytest.mark.parametrize("w", SHAPES, ids=lambda w: w.name)
 def test_pool_attention_matches_oracle(w, cs):
-    """The cluster pool kernel with 16 CTAs per row tile (kpc = P/16 keys
-    each, 8 rows merged per CTA) and with 8; the 8-CTA form does not take
-    the big pool (kpc + B > 256), which the 16-CTA form does."""
+    """The cluster pool kernel with 16 CTAs per row tile (8 rows merged per
+    CTA), with 12 (12 rows per CTA, the last CTA 8, so that 11 CTAs hold the
+    128 rows) and with 8; the pool and block keys split evenly.  The 8-CTA
+    form does not take the big pool (kpc + B > 256), the others do."""
     x, idx, ns, pk, pv = _setup(w, seed=20 + cs)
     for t in range(w.T):
         out = _run(w, x, pk, pv, ns, t, POOL_FLAGS[cs] | (H.HERALD_ATTN_SETTLED if t else 0))
@@ -114,19 +116,20 @@ def test_flash_and_pool_kernels_agree(w):
     only in the order of fp32 sums and in where P is rounded to bf16."""
     x, idx, ns, pk, pv = _setup(w, seed=7)
     a = bf16_dev_to_f64(_run(w, x, pk, pv, ns, 0, H.HERALD_ATTN_KERNEL_POOL))
-    for f in (CS_FLAGS[8], CS_FLAGS[4], CS_FLAGS[2], POOL_FLAGS[8], POOL_FLAGS[16]):
+    for f in (CS_FLAGS[8], CS_FLAGS[4], CS_FLAGS[2], POOL_FLAGS[8], POOL_FLAGS[12],
+              POOL_FLAGS[16]):
         b = bf16_dev_to_f64(_run(w, x, pk, pv, ns, 0, f))
         assert np.abs(a - b).max() <= ATTN_ATOL, hex(f)
 
 
-@pytest.mark.parametrize("kf", ["flash8", "flash2", "pool8", "pool16"])
+@pytest.mark.parametrize("kf", ["flash8", "flash2", "pool8", "pool12", "pool16"])
 def test_flash_last_step_appends_like_append_kv(kf):
     """The append rides with the attention (in the pipelined kernel the
     softmax warps of the first row tile's cluster of KV head 0, in the pool
     kernel that cluster's CTAs): the cache rows and the context lengths
     bit-exactly as herald_append_kv, the same output."""
     flag = {"flash8": CS_FLAGS[8], "flash2": CS_FLAGS[2], "pool8": POOL_FLAGS[8],
-            "pool16": POOL_FLAGS[16]}[kf]
+            "pool12": POOL_FLAGS[12], "pool16": POOL_FLAGS[16]}[kf]
     w = _w("append", L=300, C=64, K=32, S=4, W=4, extra_rows=40, index=96)
     x, idx, ns, pk, pv = _setup(w, seed=3)
     x["ctx"] = np.array([300, 330], np.int32)
