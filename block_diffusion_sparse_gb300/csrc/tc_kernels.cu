@@ -322,15 +322,16 @@ __global__ void __launch_bounds__(kTcThreads)
 // CTA stores its row (max, sumexp) over its candidates into every peer's
 // shared memory; after one cluster barrier each CTA merges them into the row
 // log-sum-exp from its own shared memory, sums exp(S - lse_r) over its 128
-// rows (warp transpose-reductions, rows past B*G excluded) and writes one
-// partial s2 per row tile, which the top-K kernel adds up.
-constexpr int kFuseCtas = 8;
+// rows (warp shuffle reductions, rows past B*G excluded) and writes one
+// partial s2 per row tile, which the top-K kernel adds up.  Clusters of 12
+// CTAs (cpc = C/12: three quarters of the UMMA and exponential work per
+// CTA) where every cluster of the launch is resident at once, else 8.
 constexpr int kFuseMaxCpc = 512;
 
-// candidates per CTA: a multiple of 64 so that each warp's column half is
-// whole 32-column chunks
-__host__ __device__ inline int fuse_cpc(int C) {
-  return ((C + kFuseCtas - 1) / kFuseCtas + 63) / 64 * 64;
+// candidates per CTA of a cs-CTA cluster: a multiple of 64 so that each
+// warp's column half is whole 32-column chunks
+__host__ __device__ inline int fuse_cpc(int C, int cs = 8) {
+  return ((C + cs - 1) / cs + 63) / 64 * 64;
 }
 
 template <int D>
@@ -342,7 +343,7 @@ struct FuseCfg {
   static_assert(kSmem <= 200 * 1024, "fused refine smem");
 };
 
-template <int D>
+template <int D, int kFuseCtas>
 __global__ void __launch_bounds__(kTcThreads, 1)
     refine_fused_kernel(const __grid_constant__ CUtensorMap qmap,
                         const uint16_t* __restrict__ kc, const int32_t* __restrict__ cand,
@@ -534,35 +535,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const bool row_ok = row < rows_t;
   // 2^(s - lse) = p * 2^(m_half - lse); rows past the tile's tokens contribute nothing
   const float f = (row_ok && m != -INFINITY) ? fast_exp2(m - lse) : 0.f;
-  // column sums over the 128 rows: per 32-column chunk, each warp
-  // transposes its 32 x 32 block through shared memory (the dead query
-  // tile, 4 KB per warp; 16-byte units XOR-swizzled by row, so that both the
-  // row stores and the column loads are free of bank conflicts) and lane j
-  // adds up column j over the warp's rows.  Rows past the tile's tokens are
-  // finite (zeroed or real queries) and weighted 0.
-  float* tb = reinterpret_cast<float*>(Qs) + warp * 1024;
+  // column sums over the 128 rows: per 32-column chunk each warp sums its
+  // 32 rows by a butterfly of shuffles (after the step of distance sd each
+  // lane keeps the columns whose bit sd matches its own, so lane j ends
+  // with column j); the four lane quadrants' sums meet in shared memory.
+  // Rows past the tile's tokens are finite (zeroed or real queries) and
+  // weighted 0.
   const uint64_t ff = f2_pack(f, f);
   for (int c = hc0; c < hc1; c += 32) {
     float v[32];
     tmem_ld32(trow + uint32_t(c), v);
 #pragma unroll
     for (int i = 0; i < 32; i += 2) f2_unpack(f2_mul(f2_pack(v[i], v[i + 1]), ff), v[i], v[i + 1]);
-    __syncwarp();  // the previous chunk's column loads are done
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-      *reinterpret_cast<float4*>(tb + lane * 32 + 4 * (u ^ (lane & 7))) =
-          make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-    __syncwarp();
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    for (int sd = 16; sd >= 1; sd >>= 1) {
+      const bool upper = (lane & sd) != 0;
 #pragma unroll
-    for (int r = 0; r < 32; r += 4) {
-      const int cl = lane & 3, cu = lane >> 2;
-      a0 += tb[(r + 0) * 32 + 4 * (cu ^ ((r + 0) & 7)) + cl];
-      a1 += tb[(r + 1) * 32 + 4 * (cu ^ ((r + 1) & 7)) + cl];
-      a2 += tb[(r + 2) * 32 + 4 * (cu ^ ((r + 2) & 7)) + cl];
-      a3 += tb[(r + 3) * 32 + 4 * (cu ^ ((r + 3) & 7)) + cl];
+      for (int j = 0; j < sd; ++j) {
+        const float lo = v[j], hi = v[j + sd];
+        v[j] = (upper ? hi : lo) + __shfl_xor_sync(0xffffffffu, upper ? lo : hi, sd);
+      }
     }
-    colsum[ch][quad][c - hc0 + lane] = (a0 + a1) + (a2 + a3);
+    colsum[ch][quad][c - hc0 + lane] = v[0];
   }
   __syncthreads();
   float* out = s2p + (size_t(mt) * gridDim.z + seg) * C;
@@ -578,6 +572,71 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 bool refine_fused_ok(int C) { return fuse_cpc(C) <= kFuseMaxCpc; }
+
+// Clusters of 12 where every cluster of the launch is resident at once.
+template <int D>
+static int refine_cluster_size(int clusters) {
+  static std::mutex mu;
+  static int cache[64];
+  static bool init = false;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
+  int n;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!init) {
+      for (int& c : cache) c = -1;
+      init = true;
+    }
+    n = cache[dev];
+  }
+  if (n < 0) {
+    n = 0;
+    if (ensure_smem(refine_fused_kernel<D, 12>, FuseCfg<D>::kSmem) == cudaSuccess &&
+        ensure_nonportable_cluster(refine_fused_kernel<D, 12>) == cudaSuccess) {
+      cudaLaunchConfig_t cfg{};
+      cfg.gridDim = dim3(12, 1, 1);
+      cfg.blockDim = dim3(kTcThreads);
+      cfg.dynamicSmemBytes = FuseCfg<D>::kSmem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 12;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, refine_fused_kernel<D, 12>, &cfg) != cudaSuccess)
+        n = 0;
+    }
+    cudaGetLastError();
+    std::lock_guard<std::mutex> lock(mu);
+    cache[dev] = n;
+  }
+  return clusters <= n ? 12 : 8;
+}
+
+template <int D>
+static cudaError_t launch_refine_fused(const herald_dims& dm, const uint16_t* k_cache,
+                                       const int32_t* cand, const int32_t* n_cand, int C,
+                                       float* s2, const WsLayout& w, uint32_t* err,
+                                       const CUtensorMap& qmap, cudaStream_t st) {
+  const int segs = dm.N * dm.Hkv;
+  const int bpt = kTileM / (dm.Hq / dm.Hkv);
+  const float scale = 1.0f / sqrtf(float(dm.d));
+  if (refine_cluster_size<D>(w.MT_tok * segs) == 12) {
+    const int cpc = fuse_cpc(C, 12);
+    HERALD_CHECK_LAUNCH(ensure_smem(refine_fused_kernel<D, 12>, FuseCfg<D>::kSmem));
+    return launch_cluster("refine_fused_kernel", refine_fused_kernel<D, 12>,
+                          dim3(12, w.MT_tok, segs), 12, FuseCfg<D>::kSmem, st, qmap, k_cache,
+                          cand, n_cand, dm.B, dm.Hq, dm.Hkv, dm.L_max, C, bpt, cpc, scale, s2,
+                          err);
+  }
+  const int cpc = fuse_cpc(C, 8);
+  HERALD_CHECK_LAUNCH(ensure_smem(refine_fused_kernel<D, 8>, FuseCfg<D>::kSmem));
+  return launch_cluster("refine_fused_kernel", refine_fused_kernel<D, 8>, dim3(8, w.MT_tok, segs),
+                        8, FuseCfg<D>::kSmem, st, qmap, k_cache, cand, n_cand, dm.B, dm.Hq,
+                        dm.Hkv, dm.L_max, C, bpt, cpc, scale, s2, err);
+}
 
 // Pass 1 -> row lse -> pass 2 (C > 4096).
 template <int D>
@@ -608,27 +667,12 @@ cudaError_t launch_refine(const herald_dims& dm, const uint16_t* k_cache, const 
                           const int32_t* n_cand, int C, float2* rpart, float* rlse, float* s2, const WsLayout& w, uint32_t* err,
                           const CUtensorMap* qmap, const CUtensorMap* qmap_all, cudaStream_t st) {
   const float scale = 1.0f / sqrtf(float(dm.d));
-  const int segs = dm.N * dm.Hkv;
-  cudaError_t e;
   if (refine_fused_ok(C)) {
     // s2 holds one partial per row tile of whole tokens: [MT_tok][N*Hkv][C]
-    const int cpc = fuse_cpc(C);
-    const int bpt = kTileM / (dm.Hq / dm.Hkv);
     if (!qmap) return cudaErrorInvalidValue;
-    if (dm.d == 128) {
-      e = ensure_smem(refine_fused_kernel<128>, FuseCfg<128>::kSmem);
-      if (e != cudaSuccess) return e;
-      return launch_cluster("refine_fused_kernel", refine_fused_kernel<128>,
-                            dim3(kFuseCtas, w.MT_tok, segs), kFuseCtas, FuseCfg<128>::kSmem, st,
-                            *qmap, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv, dm.L_max, C, bpt,
-                            cpc, scale, s2, err);
-    }
-    e = ensure_smem(refine_fused_kernel<64>, FuseCfg<64>::kSmem);
-    if (e != cudaSuccess) return e;
-    return launch_cluster("refine_fused_kernel", refine_fused_kernel<64>,
-                          dim3(kFuseCtas, w.MT_tok, segs), kFuseCtas, FuseCfg<64>::kSmem, st,
-                          *qmap, k_cache, cand, n_cand, dm.B, dm.Hq, dm.Hkv, dm.L_max, C, bpt, cpc,
-                          scale, s2, err);
+    if (dm.d == 128)
+      return launch_refine_fused<128>(dm, k_cache, cand, n_cand, C, s2, w, err, *qmap, st);
+    return launch_refine_fused<64>(dm, k_cache, cand, n_cand, C, s2, w, err, *qmap, st);
   }
   if (!qmap || !qmap_all) return cudaErrorInvalidValue;
   const int bpt = kTileM / (dm.Hq / dm.Hkv);
