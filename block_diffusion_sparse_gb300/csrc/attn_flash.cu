@@ -562,9 +562,10 @@ bool attn_flash_ok(const herald_dims& dm) {
 // The cluster size for `units` clusters: the largest of 8, 4, 2 CTAs per
 // unit whose clusters are all resident at once (one wave); 2 if none.
 template <int D>
-static int flash_pick_cs(int units) {
-  if (units <= flash_resident_clusters<D, 8>()) return 8;
-  if (units <= flash_resident_clusters<D, 4>()) return 4;
+static int flash_pick_cs(int units, int sm_budget) {
+  const int cap = sm_budget > 0 ? sm_budget : 1 << 30;
+  if (units * 8 <= cap && units <= flash_resident_clusters<D, 8>()) return 8;
+  if (units * 4 <= cap && units <= flash_resident_clusters<D, 4>()) return 4;
   return 2;
 }
 
@@ -589,7 +590,7 @@ static cudaError_t launch_flash_t(const herald_dims& dm, const int32_t* n_sel, i
                                   uint16_t* out, float scale, uint32_t* err,
                                   const PoolMaps& maps, const AppendArgs& app, int cs,
                                   bool settled, cudaStream_t st) {
-  if (cs == 0) cs = flash_pick_cs<D>(cdiv(dm.B, maps.bpt) * dm.N * dm.Hkv);
+  if (cs == 0) cs = flash_pick_cs<D>(cdiv(dm.B, maps.bpt) * dm.N * dm.Hkv, maps.sm_budget);
   switch (cs) {
     case 8:
       return launch_flash_cs<D, 8>(dm, n_sel, P_max, out, scale, err, maps, app, settled, st);
@@ -612,7 +613,7 @@ cudaError_t launch_attn_flash(const herald_dims& dm, const int32_t* n_sel, int P
 }
 
 int attn_flash_units_resident(const herald_dims& dm, int units) {
-  return dm.d == 128 ? flash_pick_cs<128>(units) : flash_pick_cs<64>(units);
+  return dm.d == 128 ? flash_pick_cs<128>(units, 0) : flash_pick_cs<64>(units, 0);
 }
 
 HERALD_DEBUG_WORD_READER(debug_take_flash)

@@ -974,7 +974,7 @@ herald_status denoise_attn(herald_dims dims, const uint16_t* q, const uint16_t* 
                            uint16_t* v_cache, void* ws, size_t ws_bytes, void* stream) {
   g_err[0] = 0;
   constexpr unsigned kKnown =
-      HERALD_ATTN_SETTLED | HERALD_ATTN_APPEND | HERALD_ATTN_ADVANCE | (0xFu << 8);
+      HERALD_ATTN_SETTLED | HERALD_ATTN_APPEND | HERALD_ATTN_ADVANCE | (0xFu << 8) | (0xFFu << 16);
   if (flags & ~kKnown) return fail(HERALD_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags & ~kKnown);
   const unsigned kernel = (flags >> 8) & 0xFu;
   if (kernel > (HERALD_ATTN_KERNEL_POOL_CS12 >> 8))
@@ -1001,10 +1001,12 @@ herald_status denoise_attn(herald_dims dims, const uint16_t* q, const uint16_t* 
   HERALD_RET_IF(check_ws(dims, 1, P_max, ws, ws_bytes, &w));
   if (scale == 0.f) scale = 1.0f / sqrtf(float(dims.d));
   PoolMaps maps;
-  const int pool_cs = attn_pool_cs(dims, P_max, int(kernel));
+  const int sm_budget = int((flags >> 16) & 0xFFu) * 4;  // HERALD_ATTN_SMS
+  const int pool_cs = attn_pool_cs(dims, P_max, int(kernel), sm_budget);
   const bool pool_ok = pool_cs > 0, flash_ok = attn_flash_ok(dims);
   const bool pool = pool_ok || flash_ok;
   maps.pool_cs = pool_cs;
+  maps.sm_budget = sm_budget;
   if (pool) {
     const uint64_t rows = uint64_t(dims.N) * dims.Hkv * P_max;
     if (pool_ok) {

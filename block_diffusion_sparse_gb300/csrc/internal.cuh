@@ -255,7 +255,8 @@ struct AppendArgs;  // below
 struct PoolMaps {
   CUtensorMap k, v, q, bk, bv, kt, vt;
   int bpt;
-  int pool_cs;  // CTAs per cluster of the pool kernel (0: it does not apply)
+  int pool_cs;    // CTAs per cluster of the pool kernel (0: it does not apply)
+  int sm_budget;  // SMs the call may count on (others busy with other streams; 0 = all)
 };
 constexpr int kFlashTileKeys = 128;
 // Whether the pipelined attention kernel takes these shapes (any P_max).
@@ -269,8 +270,9 @@ int attn_pool_kpc(int P_max, int B, int cs);
 int attn_pool_bpt(const herald_dims& dm);
 // The pool kernel's cluster size for these shapes and kernel choice
 // (HERALD_ATTN_KERNEL_* >> 8): 16 or 12 where every cluster of the launch
-// can be resident at once, else 8; 0 where the pool kernel does not apply.
-int attn_pool_cs(const herald_dims& dm, int P_max, int choice);
+// can be resident at once within sm_budget SMs (0 = all), else 8; 0 where
+// the pool kernel does not apply.
+int attn_pool_cs(const herald_dims& dm, int P_max, int choice, int sm_budget);
 cudaError_t launch_attn(const herald_dims& dm, const uint16_t* q, const uint16_t* pool_k,
                         const uint16_t* pool_v, const int32_t* n_sel, int P_max,
                         const uint16_t* block_k, const uint16_t* block_v, uint16_t* out,

@@ -1707,17 +1707,19 @@ static int pool_resident(const herald_dims& dm, int P_max, int cs) {
                     : pool_resident_clusters<64, 8>(smem);
 }
 
-int attn_pool_cs(const herald_dims& dm, int P_max, int choice) {
+int attn_pool_cs(const herald_dims& dm, int P_max, int choice, int sm_budget) {
   const bool f8 = attn_pool_fits(dm, P_max, 8), f12 = attn_pool_fits(dm, P_max, 12),
              f16 = attn_pool_fits(dm, P_max, 16);
   if (choice == 6) return f8 ? 8 : 0;
   if (choice == 7) return f16 && pool_resident(dm, P_max, 16) > 0 ? 16 : 0;
   if (choice == 8) return f12 && pool_resident(dm, P_max, 12) > 0 ? 12 : 0;
-  // the largest cluster whose clusters are all resident at once (fewer keys
-  // per CTA shorten each step's chain), else 8
+  // the largest cluster whose clusters are all resident at once, on the SMs
+  // the caller leaves to the call (fewer keys per CTA shorten each step's
+  // chain; a second wave would cost a whole chain), else 8
   const int units = cdiv(dm.B, attn_pool_bpt(dm)) * dm.N * dm.Hkv;
-  if (f16 && units <= pool_resident(dm, P_max, 16)) return 16;
-  if (f12 && units <= pool_resident(dm, P_max, 12)) return 12;
+  const int cap = sm_budget > 0 ? sm_budget : 1 << 30;
+  if (f16 && units * 16 <= cap && units <= pool_resident(dm, P_max, 16)) return 16;
+  if (f12 && units * 12 <= cap && units <= pool_resident(dm, P_max, 12)) return 12;
   if (f8) return 8;
   if (f12 && pool_resident(dm, P_max, 12) > 0) return 12;
   return f16 && pool_resident(dm, P_max, 16) > 0 ? 16 : 0;
@@ -1777,7 +1779,8 @@ static cudaError_t launch_attn_t(const herald_dims& dm, const uint16_t* q, const
     const int cs = maps->pool_cs;
     // the pool kernel while its clusters fit the device at once, else the
     // pipelined kernel (one wave with fewer CTAs per row tile)
-    const int resident = pool_ok ? pool_resident(dm, P_max, cs) : 0;
+    int resident = pool_ok ? pool_resident(dm, P_max, cs) : 0;
+    if (maps->sm_budget > 0) resident = std::min(resident, maps->sm_budget / cs);
     bool use_pool = pool_ok && (choice == 1 || choice >= 6 || !flash_ok ||
                                 (choice == 0 && tiles * segs <= resident));
     if (choice >= 2 && choice <= 5 && flash_ok) use_pool = false;

@@ -27,6 +27,12 @@ HERALD_ATTN_KERNEL_FLASH_CS2, HERALD_ATTN_KERNEL_FLASH_CS4, HERALD_ATTN_KERNEL_F
     3 << 8, 4 << 8, 5 << 8)
 HERALD_ATTN_KERNEL_POOL_CS8, HERALD_ATTN_KERNEL_POOL_CS16, HERALD_ATTN_KERNEL_POOL_CS12 = (
     6 << 8, 7 << 8, 8 << 8)
+
+
+def HERALD_ATTN_SMS(n: int) -> int:
+    """The SM-budget bits of herald_denoise_attn_ex's flags (units of 4 SMs)."""
+    return ((int(n) // 4) & 0xFF) << 16
+
 STATUS = {0: "HERALD_OK", 1: "HERALD_ERR_INVALID_ARG", 2: "HERALD_ERR_UNSUPPORTED_SHAPE",
           3: "HERALD_ERR_WORKSPACE_TOO_SMALL", 4: "HERALD_ERR_CUDA"}
 

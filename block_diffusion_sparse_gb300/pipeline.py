@@ -74,6 +74,22 @@ def scan_sms(dims: H.Dims, k_cache, fixed=None) -> int:
     return background_sms(dims, host=host)
 
 
+# CTAs of herald_stage_candidates's copy (a bounded grid on the selection
+# stream; the library's constant)
+STAGE_CTAS = 64
+
+
+def attn_sm_flags(background: int) -> int:
+    """herald_denoise_attn_ex's SM-budget bits when `background` SMs are held
+    by the selection stream's work (0 = none, or every SM: no budget), so
+    that every cluster of an attention step still fits at once."""
+    import torch
+    n_sm = _sm_count(torch.cuda.current_device())
+    if background <= 0 or background >= n_sm:
+        return 0
+    return H.HERALD_ATTN_SMS(n_sm - background)
+
+
 def step_flags(t: int, T: int, advance: bool) -> int:
     """herald_denoise_attn_ex flags of denoising step t of T: steps after the
     first find the pool settled (written before step 0, a herald call on the
@@ -280,12 +296,20 @@ class BlockPipeline:
                                               P, self._idx, self._n_sel, pk, pv, wd, wb, hd))
         self._stage1(q_steps, nk, ctx, nxt, sel if overlap else den,
                      self._scan_sms(nk) if overlap else 0, v_cache=nv)
+        # the SMs the selection stream's work holds beside the steps: the
+        # per-key scan's budget (0: every SM, no budget), then the candidate
+        # copy's CTAs
+        scan_bg = 0 if self.Bk else self._scan_sms(nk)
+        bg = 0 if (not self.Bk and scan_bg == 0) else \
+            max(scan_bg, STAGE_CTAS if self.prefetch else 0)
+        sm_flags = attn_sm_flags(bg) if overlap else 0
         for t in range(self.T):
             if t == self.T - 1 and overlap:
                 den.wait_stream(sel)  # stage 1 reads the cache the last step appends to
             chk(L.herald_denoise_attn_ex(d, q0 + t * qstep, pk, pv, self._n_sel, P,
                                          bk0 + t * bstep, bv0 + t * bstep, o0 + t * ostep, 0.0,
-                                         step_flags(t, self.T, advance), cx, kc, vc, wd, wb, hd))
+                                         step_flags(t, self.T, advance) | sm_flags, cx, kc, vc,
+                                         wd, wb, hd))
         if self.Bk:  # the appended rows change the cache's last blocks
             chk(L.herald_pool_keys(d, kc, cx, self.Bk, -(-d.B // self.Bk) + 1,
                                    H.ptr(self.pooled(k_cache, ctx)), hd))

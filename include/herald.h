@@ -327,6 +327,11 @@ herald_status herald_denoise_attn(herald_dims dims, const uint16_t *q, const uin
 #define HERALD_ATTN_KERNEL_POOL_CS8 (6u << 8)
 #define HERALD_ATTN_KERNEL_POOL_CS16 (7u << 8)
 #define HERALD_ATTN_KERNEL_POOL_CS12 (8u << 8)
+/* SM budget (bits 16-23, in units of 4 SMs; 0 = every SM): how many SMs the
+ * call may count on while work on other streams holds the rest (a stage-1
+ * scan or a copy confined to a few SMs).  The kernels' cluster sizes are
+ * chosen so that the whole launch fits that many SMs at once. */
+#define HERALD_ATTN_SMS(n) ((((unsigned)(n) / 4u) & 0xFFu) << 16)
 
 /* herald_denoise_attn with options for the steps of a block (flags = 0 is
  * herald_denoise_attn; ctx_len, k_cache, v_cache are used only with
