@@ -101,9 +101,9 @@ def test_attention_and_gather_argument_errors():
     with pytest.raises(H.HeraldError) as e:
         H.herald_denoise_attn(d, ok, ok, ok, ok, 208, ok, ok, ok, -1.0, ok, ws)
     assert e.value.status == 1
-    # the options of a denoising step: unknown bits, ADVANCE without APPEND,
-    # APPEND without a cache
-    for flags, extra in [(8, {}), (H.HERALD_ATTN_ADVANCE, {}),
+    # the options of a denoising step: unknown bits, an unknown kernel
+    # choice, ADVANCE without APPEND, APPEND without a cache
+    for flags, extra in [(8, {}), (1 << 24, {}), (9 << 8, {}), (H.HERALD_ATTN_ADVANCE, {}),
                          (H.HERALD_ATTN_APPEND, dict(ctx_len=None, k_cache=ok, v_cache=ok)),
                          (H.HERALD_ATTN_APPEND, dict(ctx_len=ok, k_cache=ok, v_cache=None))]:
         a = dict(ctx_len=ok, k_cache=ok, v_cache=ok)

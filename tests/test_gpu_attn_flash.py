@@ -110,6 +110,23 @@ def test_pool_attention_matches_oracle(w, cs):
         assert err <= ATTN_ATOL, f"{w.name} pool CS={cs} step {t}: max abs err {err}"
 
 
+@pytest.mark.parametrize("sms", [0, 152, 64, 24])
+def test_attention_within_an_sm_budget_matches_oracle(sms):
+    """HERALD_ATTN_SMS(n): the cluster sizes are picked so that a step's
+    clusters fit n SMs at once (12 or 16 CTAs per row tile when they do,
+    else 8 for the pool kernel; 8, 4 or 2 for the pipelined one); the
+    output is the oracle's whichever is picked."""
+    for w in (SHAPES[1], SHAPES[4]):
+        x, idx, ns, pk, pv = _setup(w, seed=40 + sms)
+        for t in range(w.T):
+            flags = H.HERALD_ATTN_SMS(sms) | (H.HERALD_ATTN_SETTLED if t else 0)
+            out = _run(w, x, pk, pv, ns, t, flags)
+            ref = oracle.sparse_attn(f64(x["q_steps"][t]), f64(x["k_cache"]), f64(x["v_cache"]),
+                                     idx, ns, f64(x["block_k"][t]), f64(x["block_v"][t]))
+            err = np.abs(bf16_dev_to_f64(out) - ref).max()
+            assert err <= ATTN_ATOL, f"{w.name} budget {sms} step {t}: max abs err {err}"
+
+
 @pytest.mark.parametrize("w", SHAPES[:4], ids=lambda w: w.name)
 def test_flash_and_pool_kernels_agree(w):
     """Both kernels compute the same softmax over the same keys; they differ

@@ -1,5 +1,6 @@
 """Host-side scheduling logic that needs no GPU: the flags of a block's
-denoising steps, the SM budget of the background scan, how the bench groups
+denoising steps, the SM budgets of the background scan and of the
+attention beside it, how the bench groups
 timed blocks into CUDA graphs, and the pipeline's option checks."""
 import pytest
 
@@ -33,6 +34,15 @@ def test_background_scan_budget(sms_152):
     assert P.background_sms(H.dims_of(LLAMA_64K)) == 0      # 537 MB: every SM
     assert P.background_sms(H.dims_of(QWEN_32K), host=True) == P.HOST_SCAN_SMS
     assert P.scan_sms(H.dims_of(QWEN_32K), None, fixed=7) == 7
+
+
+def test_attention_sm_budget_leaves_the_background_its_sms(sms_152):
+    # the selection stream holds `bg` SMs: the attention may count on the
+    # rest, in units of 4 SMs in bits 16-23; none or every SM: no budget
+    assert P.attn_sm_flags(33) == H.HERALD_ATTN_SMS(119) == (29 << 16)
+    assert P.attn_sm_flags(64) == (22 << 16)
+    assert P.attn_sm_flags(0) == 0 and P.attn_sm_flags(152) == 0
+    assert (P.attn_sm_flags(64) & 0xFFFF) == 0  # touches no other flag
 
 
 class _Stack(bench.StackBench):
