@@ -8,14 +8,15 @@
 //   refine_pass2  S^T = K_cand . Q_blk^T for 128 candidates x all B*G rows;
 //                 each thread owns one candidate and sums the row-softmax
 //                 probabilities over the rows -> s2 (column sum)
-//   refine_fused  stage 2 in one pass when C <= 4096: an 8-CTA cluster per
-//                 row tile shares the row statistics, exponentials are kept
-//                 in TMEM and summed by column
+//   refine_fused  stage 2 in one pass when C <= 4096: a cluster of 12 (or
+//                 8) CTAs per row tile shares the row statistics,
+//                 exponentials are kept in TMEM and summed by column
 //   attn_pool     sparse block attention over the pool (HERALD early
 //                 abstract: the selected subset is reused for every
 //                 denoising step; block keys are visible to every block
-//                 query): one 8-CTA cluster per row tile, the pool split
-//                 between its CTAs; optionally appends the decoded block
+//                 query): one cluster of 8, 12 or 16 CTAs per row tile,
+//                 the pool split between its CTAs; optionally appends the
+//                 decoded block
 //   attn_cluster  the same with cp.async operands, for shapes the pool
 //                 kernel does not take
 //   attn          one 128-key split of sparse block attention (pools beyond
@@ -314,8 +315,8 @@ __global__ void __launch_bounds__(kTcThreads)
 }
 
 // ========================================================== refine_fused
-// Stage 2 in one kernel for C <= 4096: one 8-CTA cluster per (sequence, KV
-// head, row tile of bpt = floor(128/G) whole tokens, its bpt*G query rows
+// Stage 2 in one kernel for C <= 4096: one cluster of kFuseCtas CTAs per
+// (sequence, KV head, row tile of bpt = floor(128/G) whole tokens, its bpt*G query rows
 // loaded by one 3-D TMA box per 64-column half); CTA r scores candidate
 // slots [r*cpc, (r+1)*cpc)
 // (cpc <= 512, so the scores fill TMEM and are never recomputed).  Each
@@ -1270,9 +1271,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int nkp = min(max(min(max(n_sel[seg], 0), P_max) - k0, 0), kpc);  // valid pool keys
   debug_flag(threadIdx.x == 0 && (n_sel[seg] < 0 || n_sel[seg] > P_max), DEV_BAD_COUNT);
   const bool any = nkp > 0 || has_blk;
-  // The fused append (app.bk set): per sequence, the 8 CTAs of the cluster
+  // The fused append (app.bk set): per sequence, the CS CTAs of the cluster
   // of the first row tile of KV head 0 copy the block's rows of every KV
-  // head into the cache, an eighth each, while their operands are in
+  // head into the cache, a share each, while their operands are in
   // flight.  No other CTA reads ctx.  CTA 0 advances it once every peer's
   // partial has landed: each peer pushes after all its threads have read it.
   const bool appender = app.bk != nullptr && mt == 0 && g == 0;
