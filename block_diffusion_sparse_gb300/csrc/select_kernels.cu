@@ -102,9 +102,10 @@ struct OnlineLse {
 // queries of a KV group form a 16-row bf16 operand (8 hi rows + 8 lo rows);
 // a 128-key tile of the cache is the other operand, so one 128 x 16 x d UMMA
 // per tile yields every head's logit for 128 keys (hi + lo columns summed).
-// Persistent, warp-specialised: warp 4 streams key tiles through a
-// kTcScanStages-deep TMA ring, warp 5 issues the UMMAs into two TMEM
-// accumulators, warps 0-3 (one TMEM lane = one key each) write logits and
+// Persistent, warp-specialised: warp 8 streams key tiles through a
+// kTcScanStages-deep TMA ring, warp 9 issues the UMMAs into two TMEM
+// accumulators, warps 0-7 (one TMEM lane = one key each; the two warps of a
+// lane quadrant take half of the group's heads each) write logits and
 // per-32-key (max, sumexp) partials while the next tile is multiplied.
 template <int D>
 struct TcScanCfg {
@@ -118,7 +119,9 @@ struct TcScanCfg {
   static_assert(kSmem >= kTcScanStages * kTileBytes + kBBytes + 1023, "scan smem layout");
   static_assert(kSmem <= 227 * 1024, "scan smem exceeds the per-CTA limit");
 };
-constexpr int kTcScanThreads = 192;
+constexpr int kTcScanEpiWarps = 8;  // two per TMEM lane quadrant
+constexpr int kTcScanProdWarp = kTcScanEpiWarps, kTcScanMmaWarp = kTcScanEpiWarps + 1;
+constexpr int kTcScanThreads = (kTcScanEpiWarps + 2) * 32;
 
 template <int D, int G>
 __global__ void __launch_bounds__(kTcScanThreads, 1)
@@ -145,7 +148,7 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], kTcScanEpiWarps);
     }
     mbar_init(&bbar, 1);
     mbar_init(&mdone, 1);
@@ -169,7 +172,7 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
     return j0 < L;
   };
 
-  if (warp == 4) {
+  if (warp == kTcScanProdWarp) {
     if (lane == 0) {  // ---- TMA producer
       tma_prefetch_desc(&kmap);
       int i = 0;
@@ -190,7 +193,7 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
         ++i;
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kTcScanMmaWarp) {
     if (lane == 0) {  // ---- UMMA issuer
       tma_prefetch_desc(&bmap);
       constexpr uint32_t idesc = make_idesc_bf16(kTcScanKeys, kQhlRows, false, false);
@@ -235,15 +238,18 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
         ++i;
       }
     }
-  } else {  // ---- epilogue: warps 0-3, thread = key row of the tile
-    OnlineLse run[G];
+  } else {  // ---- epilogue: warps 0-7, thread = key row of the tile
+    constexpr int kHpw = (G + 1) / 2;  // heads per warp of a lane quadrant
+    const int quad = warp & 3, h0 = (warp >> 2) * kHpw;
+    OnlineLse run[kHpw];
     int run_seg = -1;
-    const int slot = blockIdx.x * 4 + warp;
+    const int slot = blockIdx.x * 4 + quad;
     auto flush = [&](int sg) {
       const int n = sg / Hkv, g = sg - n * Hkv;
 #pragma unroll
-      for (int h = 0; h < G; ++h)
-        run[h].flush(part1 + (size_t(n) * Hq + g * G + h) * kPartSlots + slot, lane);
+      for (int k = 0; k < kHpw; ++k)
+        if (h0 + k < G)
+          run[k].flush(part1 + (size_t(n) * Hq + g * G + h0 + k) * kPartSlots + slot, lane);
     };
     int i = 0;
     for (int t = t_begin; t < t_end; ++t) {
@@ -261,18 +267,22 @@ __global__ void __launch_bounds__(kTcScanThreads, 1)
       tc_fence_after();
       __syncwarp();
       float v[16];
-      tmem_ld16(tbase + (uint32_t(warp * 32) << 16) + uint32_t(acc * kQhlRows), v);
+      tmem_ld16(tbase + (uint32_t(quad * 32) << 16) + uint32_t(acc * kQhlRows), v);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
       const int n = seg / Hkv, g = seg - n * Hkv;
-      const int j = j0 + warp * 32 + lane;
+      const int j = j0 + quad * 32 + lane;
       if (j < L) {
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float l = v[h] + v[8 + h];
-          logits[(size_t(n) * Hq + g * G + h) * L_pad + j] = l;
-          run[h].add(l);
+        for (int k = 0; k < kHpw; ++k) {
+          if (h0 + k < G) {
+            // the upper warps' heads sit kHpw columns on (compile-time indices)
+            const bool upper = warp >= 4;
+            const float l = (upper ? v[kHpw + k] : v[k]) + (upper ? v[8 + kHpw + k] : v[8 + k]);
+            logits[(size_t(n) * Hq + g * G + h0 + k) * L_pad + j] = l;
+            run[k].add(l);
+          }
         }
       }
       ++i;
