@@ -20,8 +20,8 @@ add up to --min-timed-ms (the median per step is reported).  e2e: the same
 step through the pipeline's public call (one graph per block) with the
 step's inputs copied from pinned host buffers and its outputs read back,
 copies inside the timed region; e2e.direct_calls: the same with the
-library's C-ABI calls issued directly every step (their host cost inside
-the timed region).  `range`: the metric's other workloads (4 x 64K, 128K
+library's C-ABI calls issued directly every step (one herald_block call per
+block for the per-key selection; their host cost inside the timed region).  `range`: the metric's other workloads (4 x 64K, 128K
 with the cache in host memory, the 28-layer stack), each timed the same way
 with its scan and attention rooflines.
 `--impl reference`: the fp64 CPU oracle timed on the host cores.
@@ -939,8 +939,9 @@ def run_e2e(b, args, dist, graph: bool = True):
             "ms_per_step": ms,
             "path": ("BlockPipeline.block(graph=True): C-ABI calls captured once per buffer "
                      "set (during the warm-up), then replayed" if use_graph else
-                     "direct C-ABI calls every step (argument checks, tensor-map lookups and "
-                     "launches inside the timed region)")
+                     "direct C-ABI calls every step: one herald_block call per block for the "
+                     "per-key selection (per-call for the other selections; argument checks, "
+                     "tensor-map lookups and launches inside the timed region)")
                     + "; pinned host buffers, copies on two copy streams into double-buffered "
                     "device inputs/outputs; the cache rotates as in the device-timed run"}
 

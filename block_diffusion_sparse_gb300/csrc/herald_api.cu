@@ -1087,4 +1087,89 @@ herald_status herald_append_kv(herald_dims dims, const uint16_t* block_k, const 
   return HERALD_OK;
 }
 
+// One block of the dual-stream pipeline: the calls a host loop would issue
+// for it, with the stream fork and join, in one call (a block is T + 2
+// library calls and two event operations; issued from here they cost the
+// launches' host time and nothing else).
+herald_status herald_block(herald_dims dims, int C, int K, int sink, int local, int P_max, int T,
+                           int i, const uint16_t* q_steps, const uint16_t* block_k,
+                           const uint16_t* block_v, uint16_t* k_cache, uint16_t* v_cache,
+                           int32_t* ctx_len, const uint16_t* next_k_cache, uint16_t* out,
+                           unsigned flags, int scan_sms, const herald_block_bufs* bufs,
+                           void* stream) {
+  g_err[0] = 0;
+  if (flags & ~HERALD_BLOCK_ADVANCE)
+    return fail(HERALD_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags & ~HERALD_BLOCK_ADVANCE);
+  if (T < 1) return fail(HERALD_ERR_INVALID_ARG, "T=%d must be >= 1", T);
+  if (i < 0) return fail(HERALD_ERR_INVALID_ARG, "i=%d must be >= 0", i);
+  if (scan_sms < 0) return fail(HERALD_ERR_INVALID_ARG, "scan_sms=%d must be >= 0", scan_sms);
+  if (bufs == nullptr) return fail(HERALD_ERR_INVALID_ARG, "bufs is NULL");
+  const bool overlap = bufs->sel_stream != nullptr;
+  if (overlap && (bufs->ev_fork == nullptr || bufs->ev_join == nullptr))
+    return fail(HERALD_ERR_INVALID_ARG, "sel_stream needs ev_fork and ev_join");
+  // everything the calls below check before they launch, checked before
+  // the first of them launches
+  HERALD_RET_IF(check_dims(dims));
+  HERALD_RET_IF(check_c(C));
+  HERALD_RET_IF(check_pmax(dims, P_max));
+  HERALD_RET_IF(check_budget(C, K, sink, local, P_max));
+  HERALD_CHECK_PTR(q_steps);
+  HERALD_CHECK_PTR(block_k);
+  HERALD_CHECK_PTR(block_v);
+  HERALD_CHECK_PTR(k_cache);
+  HERALD_CHECK_PTR(v_cache);
+  HERALD_CHECK_PTR(ctx_len);
+  HERALD_CHECK_PTR(out);
+  if (next_k_cache != nullptr) HERALD_CHECK_PTR(next_k_cache);
+  const int cur = i & 1, nxt = cur ^ 1;
+  HERALD_CHECK_PTR(bufs->cand[0]);
+  HERALD_CHECK_PTR(bufs->cand[1]);
+  HERALD_CHECK_PTR(bufs->n_cand[0]);
+  HERALD_CHECK_PTR(bufs->n_cand[1]);
+  HERALD_CHECK_PTR(bufs->idx);
+  HERALD_CHECK_PTR(bufs->n_sel);
+  HERALD_CHECK_PTR(bufs->pool_k[cur]);
+  HERALD_CHECK_PTR(bufs->pool_v[cur]);
+  WsLayout w;
+  HERALD_RET_IF(check_ws(dims, C, P_max, bufs->ws_den, bufs->ws_bytes, &w));
+  HERALD_RET_IF(check_ws(dims, C, P_max, bufs->ws_sel, bufs->ws_bytes, &w));
+
+  const cudaStream_t den = static_cast<cudaStream_t>(stream);
+  const cudaStream_t sel = overlap ? static_cast<cudaStream_t>(bufs->sel_stream) : den;
+  const cudaEvent_t fork = static_cast<cudaEvent_t>(bufs->ev_fork);
+  const cudaEvent_t join = static_cast<cudaEvent_t>(bufs->ev_join);
+  const size_t q_step = size_t(dims.N) * dims.B * dims.Hq * dims.d;
+  const size_t kv_step = size_t(dims.N) * dims.B * dims.Hkv * dims.d;
+  // stage 1 for block i+1 may start now: block i's queries exist
+  if (overlap) {
+    HERALD_TRY_CUDA(cudaEventRecord(fork, den), "fork event record");
+    HERALD_TRY_CUDA(cudaStreamWaitEvent(sel, fork, 0), "fork event wait");
+  }
+  HERALD_RET_IF(herald_select_stage2_gather(
+      dims, q_steps, k_cache, v_cache, ctx_len, bufs->cand[cur], bufs->n_cand[cur], C, K, sink,
+      local, P_max, bufs->idx, bufs->n_sel, bufs->pool_k[cur], bufs->pool_v[cur], bufs->ws_den,
+      bufs->ws_bytes, den));
+  HERALD_RET_IF(herald_select_stage1(dims, q_steps, next_k_cache ? next_k_cache : k_cache,
+                                     ctx_len, C, bufs->cand[nxt], bufs->n_cand[nxt], bufs->ws_sel,
+                                     bufs->ws_bytes, overlap ? scan_sms : 0, sel));
+  if (overlap) HERALD_TRY_CUDA(cudaEventRecord(join, sel), "join event record");
+  // the SMs the scan leaves the steps, so that each step's clusters fit at once
+  const int n_sm = sm_count();
+  const unsigned sm_flags =
+      (overlap && scan_sms > 0 && scan_sms < n_sm) ? HERALD_ATTN_SMS(n_sm - scan_sms) : 0u;
+  for (int t = 0; t < T; ++t) {
+    unsigned f = (t > 0 ? HERALD_ATTN_SETTLED : 0u) | sm_flags;
+    if (t == T - 1) {
+      // stage 1 reads the cache this step appends to
+      if (overlap) HERALD_TRY_CUDA(cudaStreamWaitEvent(den, join, 0), "join event wait");
+      f |= HERALD_ATTN_APPEND | ((flags & HERALD_BLOCK_ADVANCE) ? HERALD_ATTN_ADVANCE : 0u);
+    }
+    HERALD_RET_IF(denoise_attn(dims, q_steps + t * q_step, bufs->pool_k[cur], bufs->pool_v[cur],
+                               bufs->n_sel, P_max, block_k + t * kv_step, block_v + t * kv_step,
+                               out + t * q_step, 0.f, f, ctx_len, k_cache, v_cache, bufs->ws_den,
+                               bufs->ws_bytes, den));
+  }
+  return HERALD_OK;
+}
+
 }  // extern "C"

@@ -29,6 +29,10 @@ HERALD_ATTN_KERNEL_POOL_CS8, HERALD_ATTN_KERNEL_POOL_CS16, HERALD_ATTN_KERNEL_PO
     6 << 8, 7 << 8, 8 << 8)
 
 
+# flags of herald_block
+HERALD_BLOCK_ADVANCE = 1
+
+
 def HERALD_ATTN_SMS(n: int) -> int:
     """The SM-budget bits of herald_denoise_attn_ex's flags (units of 4 SMs)."""
     return ((int(n) // 4) & 0xFF) << 16
@@ -46,7 +50,7 @@ EXPORTS = ("herald_workspace_size", "herald_status_string", "herald_last_error",
            "herald_select_stage1_blocks", "herald_stage_candidates",
            "herald_select_stage2_staged", "herald_select_stage2_staged_gather",
            "herald_select_stage2_adaptive", "herald_debug_build", "herald_debug_status",
-           "herald_inject_launch_failure")
+           "herald_inject_launch_failure", "herald_block")
 
 
 class HeraldError(RuntimeError):
@@ -62,6 +66,15 @@ class Dims(C.Structure):
     def __repr__(self):
         return (f"Dims(N={self.N}, Hq={self.Hq}, Hkv={self.Hkv}, d={self.d}, B={self.B}, "
                 f"L_max={self.L_max})")
+
+
+class BlockBufs(C.Structure):
+    """herald_block_bufs: the pipeline's buffers, streams and events, kept
+    from block to block (addresses and handles as integers)."""
+    _fields_ = [("cand", C.c_void_p * 2), ("n_cand", C.c_void_p * 2), ("idx", C.c_void_p),
+                ("n_sel", C.c_void_p), ("pool_k", C.c_void_p * 2), ("pool_v", C.c_void_p * 2),
+                ("ws_den", C.c_void_p), ("ws_sel", C.c_void_p), ("ws_bytes", C.c_size_t),
+                ("sel_stream", C.c_void_p), ("ev_fork", C.c_void_p), ("ev_join", C.c_void_p)]
 
 
 def dims(N, Hq, Hkv, d, B, L_max) -> Dims:
@@ -106,6 +119,8 @@ def lib() -> C.CDLL:
         L.herald_denoise_attn_ex.argtypes = [Dims, vp, vp, vp, vp, i32, vp, vp, vp, C.c_float,
                                              C.c_uint, vp, vp, vp, vp, sz, vp]
         L.herald_append_kv.argtypes = [Dims, vp, vp, vp, vp, vp, i32, vp]
+        L.herald_block.argtypes = [Dims, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp,
+                                   vp, vp, vp, C.c_uint, i32, C.POINTER(BlockBufs), vp]
         L.herald_select_stage2_noalloc.argtypes = [Dims, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                    i32, vp, vp, vp]
         L.herald_selftest_wait_timeout.argtypes = [C.c_uint64, vp, vp]
@@ -364,6 +379,15 @@ def herald_append_kv(d, block_k, block_v, ctx_len, k_cache, v_cache, advance=Tru
                      stream=None):
     _check(lib().herald_append_kv(d, _p(block_k), _p(block_v), _p(ctx_len), _p(k_cache),
                                   _p(v_cache), int(bool(advance)), _s(stream)))
+
+
+def herald_block(d, C_, K, S, W, P_max, T, i, q_steps, block_k, block_v, k_cache, v_cache,
+                 ctx_len, next_k_cache, out, flags, scan_sms, bufs, stream=None):
+    """bufs: a BlockBufs (passed by reference)."""
+    _check(lib().herald_block(d, int(C_), int(K), int(S), int(W), int(P_max), int(T), int(i),
+                              _p(q_steps), _p(block_k), _p(block_v), _p(k_cache), _p(v_cache),
+                              _p(ctx_len), _p(next_k_cache), _p(out), int(flags), int(scan_sms),
+                              C.byref(bufs), _s(stream)))
 
 
 class Trace:

@@ -167,6 +167,30 @@ class BlockPipeline:
         self._idx, self._n_sel = P_(self.idx), P_(self.n_sel)
         self._pool_k = [P_(t) for t in self.pool_k]
         self._pool_v = [P_(t) for t in self.pool_v]
+        # herald_block's view of the same buffers: with the selection stream
+        # and the fork/join events (overlap), and without (stage 1 on the
+        # denoising stream); the events exist once recorded
+        self._ev = [torch.cuda.Event() for _ in range(2)]
+        for e in self._ev:
+            e.record(torch.cuda.current_stream())
+
+        def bufs(sel):
+            b = H.BlockBufs()
+            b.cand[0], b.cand[1] = self._cand
+            b.n_cand[0], b.n_cand[1] = self._n_cand
+            b.idx, b.n_sel = self._idx, self._n_sel
+            b.pool_k[0], b.pool_k[1] = self._pool_k
+            b.pool_v[0], b.pool_v[1] = self._pool_v
+            b.ws_den, b.ws_sel, b.ws_bytes = self._ws_den, self._ws_sel, self.ws_bytes
+            if sel is not None:
+                b.sel_stream = H.stream_handle(sel) or None
+                b.ev_fork, b.ev_join = (e.cuda_event for e in self._ev)
+            return b
+        self._bufs = {True: bufs(self.sel), False: bufs(None)}
+        # the default selection (per-key stage 1, fixed K, stage 2 reading the
+        # cache) issues each block as one herald_block call; False: the same
+        # library calls one by one from here
+        self.native = True
         # the exact selection's own workspace (block_exact)
         self.ws_exact = None
         if exact:
@@ -264,7 +288,16 @@ class BlockPipeline:
         nk = k_cache if next_k_cache is None else next_k_cache
         nv = v_cache if next_v_cache is None else next_v_cache
         d, P, L, chk = self.d, self.P, H.lib(), H.check
-        hd, hs = H.stream_handle(den), H.stream_handle(sel)
+        hd = H.stream_handle(den)
+        if self.native and not (self.Bk or self.prefetch or self.budget):
+            H.step_bytes(q_steps), H.step_bytes(block_k), H.step_bytes(out)  # contiguous
+            chk(L.herald_block(d, self.C, self.K, self.S, self.W, P, self.T, i, H.ptr(q_steps),
+                               H.ptr(block_k), H.ptr(block_v), H.ptr(k_cache), H.ptr(v_cache),
+                               H.ptr(ctx), H.ptr(nk), H.ptr(out),
+                               H.HERALD_BLOCK_ADVANCE if advance else 0,
+                               self._scan_sms(nk) if overlap else 0, self._bufs[bool(overlap)],
+                               hd))
+            return
         q0, qstep = H.ptr(q_steps), H.step_bytes(q_steps)
         bk0, bv0, bstep = H.ptr(block_k), H.ptr(block_v), H.step_bytes(block_k)
         o0, ostep = H.ptr(out), H.step_bytes(out)

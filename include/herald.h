@@ -374,6 +374,76 @@ herald_status herald_append_kv(herald_dims dims, const uint16_t *block_k,
                                const uint16_t *block_v, int32_t *ctx_len, uint16_t *k_cache,
                                uint16_t *v_cache, int advance, void *stream);
 
+/* The buffers of the dual-stream block pipeline (herald_block), owned by
+ * the caller and kept from block to block:
+ *   cand[2], n_cand[2]  [N][Hkv][C], [N][Hkv] int32 device: block i's
+ *                       stage 2 reads cand[i%2], its stage 1 for block i+1
+ *                       writes cand[(i+1)%2]
+ *   idx, n_sel          [N][Hkv][P_max], [N][Hkv] int32 device
+ *   pool_k[2], pool_v[2] [N][Hkv][P_max][d] bf16 device: block i's pool is
+ *                       pool[i%2]
+ *   ws_den, ws_sel      two workspaces of ws_bytes >= herald_workspace_size
+ *                       (dims, C, P_max) bytes each: the denoising stream's
+ *                       and the selection stream's
+ *   sel_stream          cudaStream_t for stage 1 beside the denoising steps;
+ *                       NULL: stage 1 runs on the denoising stream (no
+ *                       overlap)
+ *   ev_fork, ev_join    cudaEvent_t created by the caller (timing may be
+ *                       disabled); used only with sel_stream */
+typedef struct {
+  int32_t *cand[2], *n_cand[2];
+  int32_t *idx, *n_sel;
+  uint16_t *pool_k[2], *pool_v[2];
+  void *ws_den, *ws_sel;
+  size_t ws_bytes;
+  void *sel_stream;
+  void *ev_fork, *ev_join;
+} herald_block_bufs;
+
+#define HERALD_BLOCK_ADVANCE 1u /* the last step advances ctx_len by B */
+
+/* One block of one layer through the dual-stream pipeline ([EA]:
+ * selection and denoising run as a dual-stream pipeline over
+ * double-buffered sparse KV pools; [V3]: while the current block is
+ * denoised, stage 1 searches the cache for the next block with the current
+ * block's merged query, and stage 2 refines the candidates with the next
+ * block's real queries), issued by one call.  With den = `stream` and sel =
+ * bufs->sel_stream:
+ *   den: herald_select_stage2_gather(q_steps[0], cand[i%2]) -> idx, n_sel,
+ *        pool[i%2]
+ *   sel: (after everything issued on den before this call)
+ *        herald_select_stage1(q_steps[0], next_k_cache, scan_sms) ->
+ *        cand[(i+1)%2]
+ *   den: T x herald_denoise_attn_ex over pool[i%2] into out[t], steps
+ *        after the first with HERALD_ATTN_SETTLED, each with
+ *        HERALD_ATTN_SMS(SMs - scan_sms) when 0 < scan_sms < SMs; the last
+ *        step waits for sel (stage 1 scans the cache before the block is
+ *        appended) and appends block_k[T-1], block_v[T-1] (HERALD_ATTN_APPEND,
+ *        with HERALD_ATTN_ADVANCE if flags has HERALD_BLOCK_ADVANCE).
+ * The same calls issued one by one give the same results.  Before the
+ * first block, cand[0] must hold stage 1 of block 0 (herald_select_stage1
+ * with its own queries).
+ *   q_steps, out        [T][N][B][Hq][d] bf16 device
+ *   block_k, block_v    [T][N][B][Hkv][d] bf16 device
+ *   k_cache, v_cache    [N][Hkv][L_max][d] bf16, device or mapped pinned host
+ *   ctx_len             [N] int32 device
+ *   next_k_cache        the cache stage 1 scans for block i+1 (NULL: k_cache)
+ *   i                   the block's index (>= 0; its parity picks the buffers)
+ *   scan_sms            SMs stage 1 may hold beside the steps (0: all; the
+ *                       scan is persistent, so a small cache is best left a
+ *                       few dozen SMs and a cache larger than the steps'
+ *                       bytes all of them); ignored without sel_stream
+ * Errors: those of the calls above, T < 1, i < 0, scan_sms < 0, unknown
+ * flags, a null bufs, or sel_stream without both events:
+ * HERALD_ERR_INVALID_ARG.  A call that fails after its first launch leaves
+ * the block partly issued. */
+herald_status herald_block(herald_dims dims, int C, int K, int sink, int local, int P_max, int T,
+                           int i, const uint16_t *q_steps, const uint16_t *block_k,
+                           const uint16_t *block_v, uint16_t *k_cache, uint16_t *v_cache,
+                           int32_t *ctx_len, const uint16_t *next_k_cache, uint16_t *out,
+                           unsigned flags, int scan_sms, const herald_block_bufs *bufs,
+                           void *stream);
+
 /* Exact selection, the accuracy reference for the merged-query stage 1
  * ([MG]: exact attention of the block's queries predicts the important
  * entries; [V3] approximates it with one merged query).  Every cached

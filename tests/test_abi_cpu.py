@@ -120,6 +120,45 @@ def test_attention_and_gather_argument_errors():
     assert e.value.status == 1
 
 
+def test_block_call_argument_errors():
+    """herald_block checks its own arguments and everything its calls would
+    check before the first of them launches."""
+    _built()
+    d = H.dims(1, 4, 1, 64, 16, 2048)
+    ok = 1 << 12
+    ws = H.herald_workspace_size(d, 256, 208)
+
+    def bufs(sel=None, ev=(ok, ok), ws_bytes=ws):
+        b = H.BlockBufs()
+        b.cand[0] = b.cand[1] = b.n_cand[0] = b.n_cand[1] = ok
+        b.idx = b.n_sel = ok
+        b.pool_k[0] = b.pool_k[1] = b.pool_v[0] = b.pool_v[1] = ok
+        b.ws_den = b.ws_sel = ok
+        b.ws_bytes = ws_bytes
+        b.sel_stream = sel
+        b.ev_fork, b.ev_join = ev
+        return b
+
+    def call(b, T=2, i=0, flags=0, scan_sms=0, K=128, q=ok, nk=None):
+        H.herald_block(d, 256, K, 16, 64, 208, T, i, q, ok, ok, ok, ok, ok, nk, ok, flags,
+                       scan_sms, b)
+
+    cases = [(dict(flags=2), bufs(), 1), (dict(T=0), bufs(), 1), (dict(i=-1), bufs(), 1),
+             (dict(scan_sms=-1), bufs(ok), 1), (dict(), bufs(ok, (ok, None)), 1),
+             (dict(), bufs(ok, (None, ok)), 1), (dict(K=300), bufs(), 1),
+             (dict(q=ok + 4), bufs(), 1), (dict(nk=ok + 8), bufs(), 1),
+             (dict(), bufs(ws_bytes=ws - 1), 3)]
+    for kw, b, status in cases:
+        with pytest.raises(H.HeraldError) as e:
+            call(b, **kw)
+        assert e.value.status == status, kw
+        assert H.lib().herald_last_error().decode()
+    with pytest.raises(H.HeraldError) as e:  # no buffers at all
+        H.check(H.lib().herald_block(d, 256, 128, 16, 64, 208, 2, 0, ok, ok, ok, ok, ok, ok,
+                                     None, ok, 0, 0, None, None))
+    assert e.value.status == 1
+
+
 def test_block_stage1_and_staging_argument_errors():
     _built()
     d = H.dims(1, 4, 1, 64, 16, 2048)

@@ -111,6 +111,56 @@ def test_three_blocks_match_oracle_schedule(overlap, graph, T, Bk, host):
                                    kc, vc)
 
 
+@pytest.mark.parametrize("overlap,graph,T", [(True, False, 2), (False, False, 2),
+                                              (True, True, 2), (True, False, 1)])
+def test_block_call_equals_the_calls_one_by_one(overlap, graph, T):
+    """herald_block (one library call per block) against the same library
+    calls issued one by one from Python: bit-identical candidates,
+    selection, pools, outputs, caches and context lengths over three
+    blocks."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    nb = 3
+    w = Workload("pipe", N=2, Hq=8, Hkv=2, d=128, L=3000, B=16, T=T, C=256, K=128, S=16, W=64,
+                 planted="points", n_planted=10, index=33, extra_rows=nb * 16)
+    x0 = synth.make_layer(w)
+    blocks = [synth.make_layer(w.scaled(L=64, extra_rows=0, n_planted=0), layer=i + 1)
+              for i in range(nb)]
+    d = H.dims_of(w)
+    runs = []
+    for native in (True, False):
+        k, v, ctx = dev(x0["k_cache"]), dev(x0["v_cache"]), dev(x0["ctx"])
+        pipe = BlockPipeline(d, w.C, w.K, w.S, w.W, w.P, w.T)
+        pipe.native = native
+        pipe.prime(dev(x0["q_merge"]), k, ctx)
+        fixed = None
+        got = []
+        for i, xb in enumerate(blocks):
+            out = torch.zeros((w.T, w.N, w.B, w.Hq, w.d), dtype=torch.int16, device="cuda")
+            qs, bk, bv = dev(xb["q_steps"]), dev(xb["block_k"]), dev(xb["block_v"])
+            if graph:
+                if fixed is None:
+                    fixed = [torch.empty_like(t) for t in (qs, bk, bv, out)]
+                for dst, src in zip(fixed, (qs, bk, bv, out)):
+                    dst.copy_(src)
+                qs, bk, bv, out = fixed
+            pipe.block(i, qs, bk, bv, k, v, ctx, out, advance=True, overlap=overlap, graph=graph)
+            torch.cuda.synchronize()
+            got.append([t.cpu().numpy().copy() for t in
+                        (pipe.cand[(i + 1) % 2], pipe.n_cand[(i + 1) % 2], pipe.idx, pipe.n_sel,
+                         pipe.pool_k[i % 2], pipe.pool_v[i % 2], out)])
+        assert H.herald_workspace_error(pipe.ws_den) == 0
+        assert H.herald_workspace_error(pipe.ws_sel) == 0
+        runs.append((got, k.cpu().numpy(), v.cpu().numpy(), ctx.cpu().numpy()))
+    (ga, ka, va, ca), (gb, kb, vb, cb) = runs
+    for i in range(nb):
+        for name, a, b in zip(("cand", "n_cand", "idx", "n_sel", "pool_k", "pool_v", "out"),
+                              ga[i], gb[i]):
+            assert np.array_equal(a, b), f"block {i}: {name}"
+    assert np.array_equal(ka, kb) and np.array_equal(va, vb) and np.array_equal(ca, cb)
+    assert ca.tolist() == [w.L + nb * w.B] * w.N
+
+
 @pytest.mark.parametrize("T", [2, 1])
 def test_two_layer_stack_matches_oracle_schedule(T):
     """The stack pipeline runs the per-layer schedule above on every layer,
