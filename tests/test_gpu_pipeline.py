@@ -111,13 +111,14 @@ def test_three_blocks_match_oracle_schedule(overlap, graph, T, Bk, host):
                                    kc, vc)
 
 
-@pytest.mark.parametrize("overlap,graph,T", [(True, False, 2), (False, False, 2),
-                                              (True, True, 2), (True, False, 1)])
-def test_block_call_equals_the_calls_one_by_one(overlap, graph, T):
+@pytest.mark.parametrize("overlap,graph,T,host", [
+    (True, False, 2, False), (False, False, 2, False), (True, True, 2, False),
+    (True, False, 1, False), (True, False, 2, True)])
+def test_block_call_equals_the_calls_one_by_one(overlap, graph, T, host):
     """herald_block (one library call per block) against the same library
     calls issued one by one from Python: bit-identical candidates,
     selection, pools, outputs, caches and context lengths over three
-    blocks."""
+    blocks (host: the cache in pinned host memory)."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     nb = 3
@@ -129,7 +130,12 @@ def test_block_call_equals_the_calls_one_by_one(overlap, graph, T):
     d = H.dims_of(w)
     runs = []
     for native in (True, False):
-        k, v, ctx = dev(x0["k_cache"]), dev(x0["v_cache"]), dev(x0["ctx"])
+        if host:
+            k = torch.from_numpy(x0["k_cache"].view(np.int16).copy()).pin_memory()
+            v = torch.from_numpy(x0["v_cache"].view(np.int16).copy()).pin_memory()
+        else:
+            k, v = dev(x0["k_cache"]), dev(x0["v_cache"])
+        ctx = dev(x0["ctx"])
         pipe = BlockPipeline(d, w.C, w.K, w.S, w.W, w.P, w.T)
         pipe.native = native
         pipe.prime(dev(x0["q_merge"]), k, ctx)
