@@ -126,9 +126,10 @@ EncodeTiledFn encode_fn() {
 
 // bf16 tensor map of 2 or 3 dimensions, 128-byte swizzle.  A map depends
 // only on (base, rank, extents, box): recently encoded ones are reused (per
-// thread, a direct-mapped table of 64 entries), which keeps the per-call
+// thread, a direct-mapped table of 256 entries), which keeps the per-call
 // host cost of the steady state low -- a block step encodes a few maps per
-// attention call.
+// attention call, and a loop over double-buffered inputs and several caches
+// meets ~70 distinct maps.
 static herald_status encode_map(const void* base, int rank, const uint64_t* extent,
                                 const uint32_t* box_in, CUtensorMap* map) {
   struct Entry {
@@ -139,7 +140,7 @@ static herald_status encode_map(const void* base, int rank, const uint64_t* exte
     CUtensorMap map;
   };
   // direct-mapped: one slot per key hash, a lookup is one comparison
-  constexpr int kEntries = 64;
+  constexpr int kEntries = 256;
   thread_local Entry cache[kEntries] = {};
   uint64_t hkey = reinterpret_cast<uintptr_t>(base) >> 4;
   for (int i = 0; i < rank; ++i) hkey = hkey * 1000003u ^ (extent[i] * 31u + box_in[i]);
@@ -198,7 +199,7 @@ herald_status encode_map3(const void* base, const uint64_t* ext, const uint32_t*
 // and device and host allocations occupy disjoint ranges of the unified
 // address space, so recent answers are reused (per thread).
 bool is_device_memory(const void* p) {
-  constexpr int kEntries = 8;
+  constexpr int kEntries = 32;
   thread_local const void* keys[kEntries] = {};
   thread_local bool vals[kEntries] = {};
   thread_local int next = 0;
