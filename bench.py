@@ -30,6 +30,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import gc
 import hashlib
 import json
 import os
@@ -720,7 +721,12 @@ def measure(w, args, dist, world, min_ms: float, serial: bool = True, e2e: bool 
             b.step(0)
         torch.cuda.synchronize()
         launches_per_step = tr.count
-    del tgraphs
+    # the traced graphs and their events (2 x trace_capacity per cache copy:
+    # tens of thousands on the tiny workload) are released before the
+    # end-to-end legs, whose host-side calls they would otherwise slow down
+    del tgraphs, traces
+    gc.collect()
+    torch.cuda.synchronize()
     b.overlap = True
     tot = {k: float(np.sum(v)) / reps for k, v in per.items()}     # ms per step
     avg = {k: float(np.mean(v)) for k, v in per.items()}           # ms per launch
