@@ -15,21 +15,23 @@
 //              columns
 //   warp 8     TMA producer of the query tile and the K tiles (2-stage ring)
 //   warp 9     TMA producer of the V tiles (2-stage ring)
-//   warp 10    tcgen05.mma issuer: S_t = Q K_t^T into one of two TMEM
+//   warp 10    tcgen05.mma issuer: S_t = Q K_t^T into one of three TMEM
 //              buffers, O += P_t V_t into the TMEM accumulator with P_t
 //              read from TMEM (the A operand of the MMA)
-// The MMA warp computes S_{t+1} while the softmax warps work on S_t, and
-// P_t V_t while they work on S_{t+1}; a softmax step waits for nothing but
-// its scores unless its rows' exponent base moves.  The softmax keeps one
+// The MMA warp keeps S two tiles ahead of the softmax warps (three S/P
+// buffers and O fill the 512 TMEM columns), so a softmax step waits for
+// nothing but its scores unless its rows' exponent base moves, and S_{t+1}
+// never waits for P_{t-1} V_{t-1}.  The softmax keeps one
 // exponent base per row for as long as the row max rises by at most 8
 // (log2 units: P <= 256); when it rises by more, O and the row sum are
 // rescaled.  After the last tile each CTA normalises its O rows (fp16,
 // divided by the row sum, staged over the dead K ring) and pushes row slice
 // c to CTA c by bulk copies into receive buffers of their own, with the
 // (max, sum) of the rows, completing on c's mbarrier; each CTA then merges
-// its 128/CS rows, one 8-column chunk per thread, and writes bf16 out.  The optional append of the block to the cache (the
-// last denoising step) is done by the softmax warps of the first row
-// tile's cluster of KV head 0, while the first loads are in flight.
+// its 128/CS rows, one 8-column chunk per thread, and writes bf16 out.
+// The optional append of the block to the cache (the last denoising step)
+// is done by the softmax warps of the first row tile's cluster of KV head
+// 0, while the first loads are in flight.
 #include <cuda_bf16.h>
 
 #include "internal.cuh"
@@ -44,7 +46,10 @@ constexpr int kFlashSoftThreads = kFlashSoftWarps * 32;
 constexpr int kFlashKWarp = 8, kFlashVWarp = 9, kFlashMmaWarp = 10;
 constexpr int kFlashThreads = 11 * 32;
 constexpr float kFlashRebase = 8.f;         // log2 units
-constexpr uint32_t kFlashTmemCols = 512;    // S buffers at 0 and 128, O at 256
+constexpr uint32_t kFlashTmemCols = 512;    // S/P buffers at 0, 128, 256; O at 384
+constexpr int kSBufs = 3;                   // S/P buffers in TMEM
+constexpr uint32_t kOCol = uint32_t(kSBufs * kFT);  // first TMEM column of O
+static_assert(kOCol + 128 <= kFlashTmemCols, "S/P buffers and O fit TMEM");
 constexpr int kFlashMaxB = 64;              // block keys: one tile, the box of the block maps
 
 struct FlashSmem {
@@ -84,8 +89,8 @@ __global__ void __launch_bounds__(kFlashThreads, 1)
   constexpr int RC = kTileM / CS;    // rows merged per CTA
   constexpr uint32_t kStage = uint32_t(H * kFT * 128);
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t barQ, kfull[2], kempty[2], vfull[2], vempty[2], sfull[2];
-  __shared__ uint64_t pfull, pvdone, alldone, barR;
+  __shared__ uint64_t barQ, kfull[2], kempty[2], vfull[2], vempty[2];
+  __shared__ uint64_t sfull[kSBufs], pfull[kSBufs], pvdone[kSBufs], alldone, barR;
   __shared__ uint32_t tmem_base;
   __shared__ float red_m[2][2][kTileM];  // [tile parity][column half][row]
   __shared__ float red_s[2][kTileM];
@@ -112,10 +117,13 @@ __global__ void __launch_bounds__(kFlashThreads, 1)
       mbar_init(&kempty[s], 1);
       mbar_init(&vfull[s], 1);
       mbar_init(&vempty[s], 1);
-      mbar_init(&sfull[s], 1);
     }
-    mbar_init(&pfull, kFlashSoftThreads);
-    mbar_init(&pvdone, 1);
+#pragma unroll
+    for (int b = 0; b < kSBufs; ++b) {
+      mbar_init(&sfull[b], 1);
+      mbar_init(&pfull[b], kFlashSoftThreads);
+      mbar_init(&pvdone[b], 1);
+    }
     mbar_init(&alldone, 1);
     mbar_init(&barR, 1);
     mbar_arrive_expect_tx(&barR, uint32_t(CS) * (kSliceO + kSliceMl));
@@ -229,44 +237,47 @@ __global__ void __launch_bounds__(kFlashThreads, 1)
     if (lane == 0 && nt > 0) {
       if (!mbar_wait(&barQ, 0)) bad |= 0x4u;
       const uint32_t qa = smem_u32(Qs);
-      for (int t = 0; t <= nt; ++t) {
-        if (t < nt) {  // S_t = Q K_t^T into TMEM buffer t % 2
-          const int s = t & 1;
-          if (!mbar_wait(&kfull[s], (t >> 1) & 1)) bad |= 0x8u;
-          // buffer s held P_{t-2}: P_{t-2} V_{t-2} (issued before this, the
-          // last MMA to complete on pvdone so far) must have read it
-          if (t >= 2 && !mbar_wait(&pvdone, t & 1)) bad |= 0x10u;
-          tc_fence_after();
-          const int nk = (tile_keys(t) + 15) & ~15;
-          const uint32_t idesc = make_idesc_bf16(kTileM, nk, false, false);
-          const uint32_t ka = smem_u32(Kr + s * kStage);
+      // S_j = Q K_j^T into TMEM buffer j % 3: issued once K_j has landed and
+      // the buffer's previous P (tile j - 3) has been read by its P V
+      auto issue_s = [&](int j) {
+        const int s = j & 1, b3 = j % kSBufs;
+        if (!mbar_wait(&kfull[s], (j >> 1) & 1)) bad |= 0x8u;
+        if (j >= kSBufs && !mbar_wait(&pvdone[b3], (j / kSBufs - 1) & 1)) bad |= 0x10u;
+        tc_fence_after();
+        const int nk = (tile_keys(j) + 15) & ~15;
+        const uint32_t idesc = make_idesc_bf16(kTileM, nk, false, false);
+        const uint32_t ka = smem_u32(Kr + s * kStage);
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t hv = uint32_t(ks) >> 2, koff = uint32_t(ks & 3) * 32u;
-            const uint64_t a = make_sdesc_sw128(qa + hv * (kTileM * 128) + koff, 16, 1024);
-            const uint64_t b = make_sdesc_sw128(ka + hv * (kFT * 128) + koff, 16, 1024);
-            umma_bf16(tbase + uint32_t(s * 128), a, b, idesc, ks > 0 ? 1u : 0u);
-          }
-          umma_commit(&sfull[s]);
-          umma_commit(&kempty[s]);
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t hv = uint32_t(ks) >> 2, koff = uint32_t(ks & 3) * 32u;
+          const uint64_t a = make_sdesc_sw128(qa + hv * (kTileM * 128) + koff, 16, 1024);
+          const uint64_t b = make_sdesc_sw128(ka + hv * (kFT * 128) + koff, 16, 1024);
+          umma_bf16(tbase + uint32_t(b3) * uint32_t(kFT), a, b, idesc, ks > 0 ? 1u : 0u);
         }
-        if (t >= 1) {  // O += P_u V_u for the previous tile
-          const int u = t - 1, su = u & 1;
-          if (!mbar_wait(&pfull, u & 1)) bad |= 0x20u;
-          if (!mbar_wait(&vfull[su], (u >> 1) & 1)) bad |= 0x40u;
-          tc_fence_after();
-          const int nk = (tile_keys(u) + 15) & ~15;
-          constexpr uint32_t idesc = make_idesc_bf16(kTileM, D, false, true);
-          const uint32_t va = smem_u32(Vr + su * kStage);
-          for (int ks = 0; ks < nk / 16; ++ks) {  // P: 16 keys = 8 packed TMEM columns
-            const uint64_t b =
-                make_sdesc_sw128(va + uint32_t(ks) * 2048u, uint32_t(kFT) * 128u, 1024);
-            umma_bf16_ts(tbase + 256, tbase + uint32_t(su * 128 + ks * 8), b, idesc,
-                         (u > 0 || ks > 0) ? 1u : 0u);
-          }
-          umma_commit(&pvdone);
-          umma_commit(&vempty[su]);
+        umma_commit(&sfull[b3]);
+        umma_commit(&kempty[s]);
+      };
+      // two tiles ahead of the softmax; then per tile u: O += P_u V_u once
+      // P_u is in TMEM, and S_{u+2} into the buffer P_{u-1} V_{u-1} freed
+      issue_s(0);
+      if (nt > 1) issue_s(1);
+      for (int u = 0; u < nt; ++u) {
+        const int su = u & 1, bu = u % kSBufs;
+        if (!mbar_wait(&pfull[bu], (u / kSBufs) & 1)) bad |= 0x20u;
+        if (!mbar_wait(&vfull[su], (u >> 1) & 1)) bad |= 0x40u;
+        tc_fence_after();
+        const int nk = (tile_keys(u) + 15) & ~15;
+        constexpr uint32_t idesc = make_idesc_bf16(kTileM, D, false, true);
+        const uint32_t va = smem_u32(Vr + su * kStage);
+        for (int ks = 0; ks < nk / 16; ++ks) {  // P: 16 keys = 8 packed TMEM columns
+          const uint64_t b =
+              make_sdesc_sw128(va + uint32_t(ks) * 2048u, uint32_t(kFT) * 128u, 1024);
+          umma_bf16_ts(tbase + kOCol, tbase + uint32_t(bu * kFT + ks * 8), b, idesc,
+                       (u > 0 || ks > 0) ? 1u : 0u);
         }
+        umma_commit(&pvdone[bu]);
+        umma_commit(&vempty[su]);
+        if (u + 2 < nt) issue_s(u + 2);
       }
       umma_commit(&alldone);  // (single use: the softmax warps may lag pvdone)
     }
@@ -289,12 +300,12 @@ __global__ void __launch_bounds__(kFlashThreads, 1)
     float m_base = -INFINITY;  // the row's exponent base (log2 units)
     float l = 0.f;             // this thread's share of the row sum
     for (int t = 0; t < nt; ++t) {
-      const int s = t & 1;
+      const int s = t & 1, b3 = t % kSBufs;
       const int nk = tile_keys(t);
       const int nchunks = (nk + 15) >> 4;
       const int half = (nchunks + 1) >> 1;
       const int c_begin = ch == 0 ? 0 : half, cnt = ch == 0 ? half : nchunks - half;
-      if (!mbar_wait(&sfull[s], (t >> 1) & 1)) bad |= 0x80u;
+      if (!mbar_wait(&sfull[b3], (t / kSBufs) & 1)) bad |= 0x80u;
       tc_fence_after();
       constexpr int kMaxChunks = (kFT / 16 + 1) / 2;
       float x[kMaxChunks][16];
@@ -308,7 +319,7 @@ __global__ void __launch_bounds__(kFlashThreads, 1)
               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
                 "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
                 "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-              : "r"(trow + uint32_t(s * 128 + (c_begin + c) * 16)));
+              : "r"(trow + uint32_t(b3 * kFT + (c_begin + c) * 16)));
         }
       }
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -339,17 +350,15 @@ __global__ void __launch_bounds__(kFlashThreads, 1)
       }
       // a new base rescales O, once P_{t-1} V_{t-1} has been added to it
       if (t >= 1 && __any_sync(0xffffffffu, rebase)) {
-        // pvdone is at phase t-1 or just past it: the MMA warp waited for
-        // P_{t-2} V_{t-2} before it computed the S_t read above, and
-        // P_t V_t needs this thread's P_t (a parity wait sees only the
-        // current phase or the one before it)
-        if (!mbar_wait(&pvdone, (t - 1) & 1)) bad |= 0x100u;
+        // P_{t-1} V_{t-1} (in-order after every earlier P V) completes on
+        // pvdone[(t-1) % 3], whose next completion needs this thread's P_{t+2}
+        if (!mbar_wait(&pvdone[(t - 1) % kSBufs], ((t - 1) / kSBufs) & 1)) bad |= 0x100u;
         tc_fence_after();
         {  // this thread's half of its O row
 #pragma unroll
           for (int k = 0; k < D / 32; ++k) {
             float v[16];
-            const uint32_t col = uint32_t(256 + ch * (D / 2) + k * 16);
+            const uint32_t col = kOCol + uint32_t(ch * (D / 2) + k * 16);
             tmem_ld16(trow + col, v);
             uint32_t w[16];
 #pragma unroll
@@ -387,7 +396,7 @@ __global__ void __launch_bounds__(kFlashThreads, 1)
           }
           asm volatile(
               "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::
-                  "r"(trow + uint32_t(s * 128 + (c_begin + c) * 8)),
+                  "r"(trow + uint32_t(b3 * kFT + (c_begin + c) * 8)),
               "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]),
               "r"(pk[6]), "r"(pk[7])
               : "memory");
@@ -397,13 +406,11 @@ __global__ void __launch_bounds__(kFlashThreads, 1)
       f2_unpack(lsum2, lsum, lsum_hi);
       l = l * factor + (lsum + lsum_hi);
       tmem_wait_st();
-      // P_{t-1} V_{t-1} done before P_t is announced: the MMA warp has then
-      // consumed pfull's previous phase, so pfull never runs two phases
-      // ahead of its waiter (with P in TMEM nothing else holds this warp
-      // back for a tile; the wait is normally over long before)
-      if (t >= 1 && !mbar_wait(&pvdone, (t - 1) & 1)) bad |= 0x800u;
+      // pfull[t % 3] cannot run two phases ahead of the MMA warp: its next
+      // arrival (P_{t+3}) needs S_{t+3}, which the MMA warp issues only after
+      // P_t V_t, i.e. after consuming this phase
       tc_fence_before();
-      mbar_arrive(&pfull);
+      mbar_arrive(&pfull[b3]);
     }
     if (nt > 0) {  // every MMA of this CTA is done
       if (!mbar_wait(&alldone, 0)) bad |= 0x200u;
@@ -427,7 +434,7 @@ __global__ void __launch_bounds__(kFlashThreads, 1)
             : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]),
               "=r"(q[6]), "=r"(q[7]), "=r"(q[8]), "=r"(q[9]), "=r"(q[10]), "=r"(q[11]),
               "=r"(q[12]), "=r"(q[13]), "=r"(q[14]), "=r"(q[15])
-            : "r"(trow + uint32_t(256 + ch * (D / 2) + k * 16)));
+            : "r"(trow + kOCol + uint32_t(ch * (D / 2) + k * 16)));
       }
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
@@ -458,6 +465,9 @@ __global__ void __launch_bounds__(kFlashThreads, 1)
   }
   if (!mbar_wait(&barR, 0)) {
     record_error(err, DEV_TIMEOUT_TMA | DEV_K_ATTN_FLASH | (0x400u << 16));
+    // a peer whose own wait ran out pushes late: this CTA must not exit
+    // (its shared memory is the copies' destination) before they land
+    mbar_wait(&barR, 0, 20ull * kWaitLimitNs);
   } else if (app.bk != nullptr && app.advance && mt == 0 && g == 0 && rank == 0 &&
              threadIdx.x == 0) {
     app.ctx[n] = min(min(max(app.ctx[n], 0), L_max) + B, L_max);
@@ -505,12 +515,11 @@ __global__ void __launch_bounds__(kFlashThreads, 1)
                    pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
   }
   if (bad) record_error(err, DEV_TIMEOUT_MMA | DEV_K_ATTN_FLASH | (bad << 16));
-  if (threadIdx.x == 0) bulk_wait_read_all();  // outgoing copies have read the partial
-  // no CTA leaves while a peer may still push into it: a CTA whose wait for
-  // the partials gave up (after a peer's own wait ran out) would otherwise
-  // exit before that peer's copies arrive
-  __cluster_barrier_arrive();
-  __cluster_barrier_wait();
+  // Once barR has completed, every peer's copy into this CTA has landed and
+  // nothing else reaches its shared memory: it leaves as soon as its own
+  // outgoing copies have read the partial, without waiting for its peers
+  // (no cluster barrier at the end of the chain).
+  if (threadIdx.x == 0) bulk_wait_read_all();
   tmem_teardown(tbase, kFlashTmemCols);
 }
 
