@@ -1114,8 +1114,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // keys and values are 3-D TMA boxes (every operand is one bulk transfer,
 // issued by one thread as soon as the predecessor kernel is done).  Each
 // CTA computes S = Q K^T for its keys with one UMMA (N = kpc), P = exp(S -
-// rowmax) in bf16 (written over the Q/K operands, dead once S is in TMEM),
-// O = P V into TMEM.  Rows are finalised 128/CS per CTA: each CTA stages
+// rowmax) in bf16 (packed into TMEM over S, chunk j of 16 keys in columns
+// [8j, 8j + 8), once every S column has been read), O = P V into TMEM with
+// P read from TMEM.  Rows are finalised 128/CS per CTA: each CTA stages
 // its O rows divided by their row sums (fp16) over the dead operands and
 // pushes rows [c*128/CS, (c+1)*128/CS) with their (max, sum) to CTA c by
 // bulk shared::cta -> shared::cluster copies that complete on c's mbarrier;
@@ -1133,7 +1134,7 @@ constexpr int kPoolMaxB = 64;
 constexpr int kPoolMaxCols = 256;
 
 struct PoolSmem {
-  uint32_t q, k, kb, p, pb, v, vb, recv_o, recv_ml, total;
+  uint32_t q, k, kb, v, vb, recv_o, recv_ml, total;
 };
 // Rows each CTA of a cs-CTA cluster finalises (even, so that every slice
 // of (max, sum) pairs is a whole number of 16-byte units).
@@ -1144,15 +1145,13 @@ __host__ __device__ constexpr int pool_rows_per_cta(int cs) {
 __host__ __device__ inline PoolSmem pool_smem(int D, int kpc, int Bp, int cs) {
   const uint32_t H = uint32_t(D / 64);
   PoolSmem L;
-  // region A: Q | K | K_block, later P | P_block
+  // region A: Q | K | K_block, later the staged O rows (fp16, D + 8 apart)
   L.q = 0;
   L.k = H * 128u * 128u;
   L.kb = L.k + H * uint32_t(kpc) * 128u;
   const uint32_t a_end = L.kb + H * uint32_t(Bp) * 128u;
-  L.p = 0;
-  L.pb = uint32_t((kpc + 63) / 64) * 16384u;
-  const uint32_t p_end = L.pb + 16384u;
-  L.v = ((a_end > p_end ? a_end : p_end) + 1023u) & ~1023u;
+  const uint32_t o_end = uint32_t(kTileM) * uint32_t(D + 8) * 2u;
+  L.v = ((a_end > o_end ? a_end : o_end) + 1023u) & ~1023u;
   L.vb = L.v + H * uint32_t(kpc) * 128u;
   L.recv_o = L.vb + H * uint32_t(Bp) * 128u;
   // one slice of pool_rows_per_cta(cs) rows from each of the cs CTAs
@@ -1191,8 +1190,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* Qs = base + S.q;
   uint8_t* Ks = base + S.k;
   uint8_t* Kb = base + S.kb;
-  uint8_t* Ps = base + S.p;
-  uint8_t* Pb = base + S.pb;
   uint8_t* Vs = base + S.v;
   uint8_t* Vb = base + S.vb;
   uint16_t* recv_o = reinterpret_cast<uint16_t*>(base + S.recv_o);
@@ -1391,26 +1388,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         pk[i] = pack_bf16(p0, p1);
       }
       const int j = c_begin + c;
-      uint8_t* blk;
-      int kc;  // key index within the pool slice or within the block
-      if (j < npc) {
-        kc = j * 16;
-        blk = Ps + (kc >> 6) * 16384;
-      } else {
-        kc = (j - npc) * 16;
-        blk = Pb;
-      }
-      const int cc = (kc & 63) >> 3;  // 16-byte chunk (8 keys)
-      *reinterpret_cast<uint4*>(blk + sw128_off(row, cc)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      *reinterpret_cast<uint4*>(blk + sw128_off(row, cc + 1)) =
-          make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      asm volatile(
+          "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+              trow + uint32_t(j * 8)),
+          "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]), "r"(pk[6]),
+          "r"(pk[7])
+          : "memory");
     }
   }
   float lsum, lsum_hi;
   f2_unpack(lsum2, lsum, lsum_hi);
   lsum += lsum_hi;
   red_s[ch][row] = lsum;
-  fence_proxy_async_smem();
+  tmem_wait_st();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1421,22 +1411,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bool acc = false;
     ok = mbar_wait(&barV, 0) && ok;
     tc_fence_after();
-    if (nkp > 0) {  // the chunks the softmax wrote
-      const uint32_t pa = smem_u32(Ps), va = smem_u32(Vs);
+    if (nkp > 0) {  // P of the pool chunks: TMEM columns [0, 8 npc)
+      const uint32_t va = smem_u32(Vs);
       for (int s = 0; s < npc; ++s) {
-        const uint64_t a =
-            make_sdesc_sw128(pa + uint32_t(s >> 2) * 16384u + uint32_t(s & 3) * 32u, 16, 1024);
         const uint64_t b = make_sdesc_sw128(va + uint32_t(s) * 2048u, uint32_t(kpc) * 128u, 1024);
-        umma_bf16(tbase + 256, a, b, idesc, acc ? 1u : 0u);
+        umma_bf16_ts(tbase + 256, tbase + uint32_t(s * 8), b, idesc, acc ? 1u : 0u);
         acc = true;
       }
     }
-    if (has_blk) {
-      const uint32_t pa = smem_u32(Pb), va = smem_u32(Vb);
+    if (has_blk) {  // P of the block chunks: the next 8 nbc columns
+      const uint32_t va = smem_u32(Vb);
       for (int s = 0; s < nbc; ++s) {
-        const uint64_t a = make_sdesc_sw128(pa + uint32_t(s & 3) * 32u, 16, 1024);
         const uint64_t b = make_sdesc_sw128(va + uint32_t(s) * 2048u, uint32_t(Bp) * 128u, 1024);
-        umma_bf16(tbase + 256, a, b, idesc, acc ? 1u : 0u);
+        umma_bf16_ts(tbase + 256, tbase + uint32_t((npc + s) * 8), b, idesc, acc ? 1u : 0u);
         acc = true;
       }
     }
