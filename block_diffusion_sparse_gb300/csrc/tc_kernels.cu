@@ -1436,7 +1436,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncwarp();
   if (!ok) record_error(err, DEV_TIMEOUT_MMA | DEV_K_ATTN_POOL);
 
-  // O partial -> shared memory over the dead operands (P was the last):
+  // O partial -> shared memory over the dead Q/K operands (dead since S):
   // each row divided by its sum and stored as fp16 (|o / l| <= max |v|); the
   // merge re-weights by (max, sum), which stay fp32
   const float lrow = red_s[0][row] + red_s[1][row];
