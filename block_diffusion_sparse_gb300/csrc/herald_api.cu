@@ -308,7 +308,7 @@ herald_status run_stage2(const herald_dims& dm, const uint16_t* q_block, const u
                     "budget launch");
   HERALD_TRY_CUDA(launch_topk_union(dm, ctx_len, cand, n_cand, at<float>(ws, w.s2), n_parts, C, K,
                                     sink, local, P_max, idx, n_sel, st, gather, slot_out,
-                                    budget ? budget->k_sel : nullptr),
+                                    budget ? budget->k_sel : nullptr, true),
                   "topk_union launch");
   return HERALD_OK;
 }

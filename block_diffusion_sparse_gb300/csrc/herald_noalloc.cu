@@ -139,7 +139,8 @@ herald_status herald_select_stage2_noalloc(herald_dims dims, const uint16_t* q_b
                       reinterpret_cast<float*>(base + s2_off), full, err, &qmap, &qmap_all, st);
   if (e == cudaSuccess)
     e = launch_topk_union(dims, ctx_len, cand, n_cand, reinterpret_cast<float*>(base + s2_off),
-                          n_parts, C, K, sink, local, P_max, idx, n_sel, st);
+                          n_parts, C, K, sink, local, P_max, idx, n_sel, st, nullptr, nullptr,
+                          nullptr, true);
   if (e != cudaSuccess)
     return fail(HERALD_ERR_CUDA, "stage-2 launch: %s", cudaGetErrorString(e));
   return HERALD_OK;

@@ -217,12 +217,16 @@ struct PoolGather {
 // gather (optional) also fills the pool; slot_out (optional, [N*Hkv][P_max])
 // receives the candidate slot of every selected row taken from the top-K,
 // -1 for sink, local and padding rows; k_seg (optional, [N*Hkv]) gives each
-// (n, g) a budget of its own, at most K.
+// (n, g) a budget of its own, at most K.  early: ctx, cand and n_cand were
+// written before the kernel launched just before this one began (they are
+// inputs of the stage-2 call, not outputs of its refine), so the kernel reads
+// them before its grid-dependency wait.
 cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const int32_t* cand,
                               const int32_t* n_cand, const float* s2, int n_parts, int C, int K,
                               int S, int W, int P_max, int32_t* idx, int32_t* n_sel,
                               cudaStream_t st, const PoolGather* gather = nullptr,
-                              int32_t* slot_out = nullptr, const int32_t* k_seg = nullptr);
+                              int32_t* slot_out = nullptr, const int32_t* k_seg = nullptr,
+                              bool early = false);
 // The adaptive budget of every (n, g) from the summed stage-2 scores (same
 // partial layout as topk_union): the smallest k whose k largest scores hold
 // tau of their total, clamped to [K_min, K_max]; k_sel [N*Hkv] out.

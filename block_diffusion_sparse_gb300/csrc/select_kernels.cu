@@ -857,7 +857,8 @@ __global__ void __launch_bounds__(kTkThreads)
                       const int32_t* __restrict__ n_cand, const float* __restrict__ s2,
                       int n_parts, int Hkv, int L_max, int C, int K, int S, int W, int P_max,
                       int32_t* __restrict__ idx, int32_t* __restrict__ n_sel, PoolGather pg,
-                      int32_t* __restrict__ slot_out, const int32_t* __restrict__ k_seg) {
+                      int32_t* __restrict__ slot_out, const int32_t* __restrict__ k_seg,
+                      int early) {
   // [C] bit patterns of the threshold-bin members, then (with the gather)
   // [P_max] selected positions
   extern __shared__ uint32_t mem[];
@@ -867,36 +868,46 @@ __global__ void __launch_bounds__(kTkThreads)
   __shared__ uint32_t wt[32], wt2[32];
   __shared__ int s_bin;
   __shared__ uint32_t s_above, s_cnt;
-  griddep_enter();
   // with the gather, pg.copies CTAs per (n, g) select alike (the selection
   // is deterministic) and each gathers one slice of the pool; copy 0 writes
   // idx and n_sel
   const int copies = pg.pk ? pg.copies : 1;
   const int seg = blockIdx.x / copies, copy = blockIdx.x - seg * copies, n = seg / Hkv;
-  const int L = min(max(ctx[n], 0), L_max);
-  debug_flag(threadIdx.x == 0 && (ctx[n] < 0 || ctx[n] > L_max), DEV_BAD_COUNT);
-  const int nc = min(max(n_cand[seg], 0), C);
-  // the budget: K, or this (n, g)'s own (at most K) when k_seg is given
-  const int Ke = min(k_seg ? min(max(k_seg[seg], 0), K) : K, nc);
   // slots per thread from C, not n_cand: the score loads need not wait for it
   const int E = (C + kTkThreads - 1) / kTkThreads;
   const int i0 = threadIdx.x * E;
   const int32_t* cd = cand + size_t(seg) * C;
-  const float* sc = s2 + size_t(seg) * C;
-  const size_t part_stride = size_t(gridDim.x / copies) * C;  // [part][N*Hkv][C]
   // the candidate positions are needed only at the end; with few per thread
-  // their loads are issued here, with the scores', so that no phase waits on
-  // memory twice (with 16 per thread the registers are not there)
+  // their loads are issued with the context length and the candidate count
+  // (with 16 per thread the registers are not there).  early != 0: the
+  // caller's inputs (ctx, cand, n_cand) were written before the stage-2
+  // refine that precedes this kernel began, so they are read before the
+  // grid-dependency wait, which then covers only the refine's scores
   constexpr bool kEarlyPos = kPer <= 4;
   int32_t pk[kPer];
-  if constexpr (kEarlyPos) {
+  int ctx_raw = 0, nc_raw = 0;
+  auto load_inputs = [&]() {
+    ctx_raw = ctx[n];
+    nc_raw = n_cand[seg];
+    if constexpr (kEarlyPos) {
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) pk[k] = (k < E && i0 + k < C) ? __ldg(cd + i0 + k) : -1;
-  }
-  // shared state cleared while the loads are in flight
+      for (int k = 0; k < kPer; ++k) pk[k] = (k < E && i0 + k < C) ? __ldg(cd + i0 + k) : -1;
+    }
+  };
+  if (early) load_inputs();
+  // shared state cleared before the wait
   for (int i = threadIdx.x; i < kHistBins; i += kTkThreads) h[i] = 0u;
   for (int i = threadIdx.x; i < kMaxC / 32; i += kTkThreads) taken[i] = 0u;
   if (threadIdx.x == 0) s_cnt = 0;
+  griddep_enter();
+  if (!early) load_inputs();
+  const int L = min(max(ctx_raw, 0), L_max);
+  debug_flag(threadIdx.x == 0 && (ctx_raw < 0 || ctx_raw > L_max), DEV_BAD_COUNT);
+  const int nc = min(max(nc_raw, 0), C);
+  // the budget: K, or this (n, g)'s own (at most K) when k_seg is given
+  const int Ke = min(k_seg ? min(max(k_seg[seg], 0), K) : K, nc);
+  const float* sc = s2 + size_t(seg) * C;
+  const size_t part_stride = size_t(gridDim.x / copies) * C;  // [part][N*Hkv][C]
   float x[kPer];
 #pragma unroll
   for (int k = 0; k < kPer; ++k) x[k] = 0.f;
@@ -1098,7 +1109,7 @@ cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const i
                               const int32_t* n_cand, const float* s2, int n_parts, int C, int K,
                               int S, int W, int P_max, int32_t* idx, int32_t* n_sel,
                               cudaStream_t st, const PoolGather* gather, int32_t* slot_out,
-                              const int32_t* k_seg) {
+                              const int32_t* k_seg, bool early) {
   static_assert(kMaxC <= 16 * kTkThreads, "16 scores per thread cover every C");
   const PoolGather pg = gather ? *gather : PoolGather{nullptr, nullptr, nullptr, nullptr, 0, 1};
   const size_t smem = size_t(C) * 4 + (pg.pk ? size_t(P_max) * 4 : 0u);
@@ -1109,11 +1120,11 @@ cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const i
   if (C <= 4 * kTkThreads)
     HERALD_CHECK_LAUNCH(launch_k("topk_union_kernel", topk_union_kernel<4>, grid, kTkThreads, smem,
                                  st, ctx, cand, n_cand, s2, n_parts, dm.Hkv, dm.L_max, C, K, S, W,
-                                 P_max, idx, n_sel, pg, slot_out, k_seg));
+                                 P_max, idx, n_sel, pg, slot_out, k_seg, early ? 1 : 0));
   else
     HERALD_CHECK_LAUNCH(launch_k("topk_union_kernel", topk_union_kernel<16>, grid, kTkThreads,
                                  smem, st, ctx, cand, n_cand, s2, n_parts, dm.Hkv, dm.L_max, C, K,
-                                 S, W, P_max, idx, n_sel, pg, slot_out, k_seg));
+                                 S, W, P_max, idx, n_sel, pg, slot_out, k_seg, early ? 1 : 0));
   return cudaGetLastError();
 }
 
