@@ -840,8 +840,11 @@ cudaError_t launch_exact_sum_hist(const herald_dims& dm, float* s, int n_parts, 
 // candidate slots [t*E, (t+1)*E) in registers (E <= kPer; 4 when C <= 4096,
 // 16 up to C = 16384), summed over the refine's row-tile partials with all
 // loads of a partial in flight at once.  The K-th largest score lies in one
-// bin of a 12-bit histogram of the fp32 bit patterns; the members of that bin
-// are ranked exactly (score descending, slot ascending = position ascending,
+// bin of a 14-bit histogram of the fp32 bit patterns (16 sub-bins per
+// octave: on the 32K layer ~100-140 of the 4096 scores share the threshold's
+// bin at 12 bits, a quarter of that at 14, and the ranking below is
+// quadratic in them); the members of that bin are ranked exactly (score
+// descending, slot ascending = position ascending,
 // candidates being ascending), the winners marked in a shared bitmap, and one
 // block scan orders the output: [0, sink_end) ++ kept candidates inside
 // [sink_end, local_begin) ++ [local_begin, L) -- the deduplicated ascending
@@ -849,7 +852,72 @@ cudaError_t launch_exact_sum_hist(const herald_dims& dm, float* s, int n_parts, 
 // came from (-1 for sink, local and padding rows), so that a gather can read
 // candidate rows staged by slot.
 constexpr int kTkThreads = 1024;
+// first radix digit of the top-K: the top 14 bits of the (non-negative)
+// fp32 pattern, 16 sub-bins per octave, in dynamic shared memory
+constexpr int kTkShift = 17;
+constexpr int kTkBins = 1 << (31 - kTkShift);
 constexpr int kTkRankCap = 1024;  // members ranked in one shot
+
+// The bin holding the need-th largest element of a wide histogram h[0..nb)
+// (nb a multiple of 32 * 32; rank order counts from the top bin) and the
+// count strictly above it: every warp sums its nb/32 bins with lane-strided
+// (bank-conflict-free) reads, warp 0 scans the warp totals, and only the
+// warp holding the rank walks its bins in order.
+template <int NT>
+__device__ void find_bin_wide(const uint32_t* h, int nb, uint32_t need, uint32_t* warp_tot,
+                              int* s_warp, uint32_t* s_before, int* out_bin,
+                              uint32_t* out_above) {
+  constexpr int NW = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per_w = nb / NW;  // rank-order bins of a warp
+  uint32_t sum = 0;
+  for (int k = lane; k < per_w; k += 32) sum += h[nb - 1 - (warp * per_w + k)];
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane == 0) warp_tot[warp] = sum;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t t = lane < NW ? warp_tot[lane] : 0u;
+    uint32_t incl = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const uint32_t excl = incl - t;
+    if (lane < NW && excl < need && need <= incl) {
+      *s_warp = lane;
+      *s_before = excl;
+    }
+  }
+  __syncthreads();
+  const int W = *s_warp;
+  if (warp == W) {
+    const int per_l = per_w / 32;  // consecutive rank-order bins of a lane
+    const int rb0 = W * per_w + lane * per_l;
+    uint32_t local = 0;
+    for (int k = 0; k < per_l; ++k) local += h[nb - 1 - (rb0 + k)];
+    uint32_t incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    uint32_t acc = *s_before + incl - local;
+    if (acc < need && need <= acc + local) {
+      for (int k = 0; k < per_l; ++k) {
+        const uint32_t c = h[nb - 1 - (rb0 + k)];
+        if (acc + c >= need) {
+          *out_bin = nb - 1 - (rb0 + k);
+          *out_above = acc;
+          break;
+        }
+        acc += c;
+      }
+    }
+  }
+  __syncthreads();
+}
 
 template <int kPer>
 __global__ void __launch_bounds__(kTkThreads)
@@ -861,13 +929,14 @@ __global__ void __launch_bounds__(kTkThreads)
                       int early) {
   // [C] bit patterns of the threshold-bin members, then (with the gather)
   // [P_max] selected positions
-  extern __shared__ uint32_t mem[];
-  __shared__ uint32_t h[kHistBins];
+  extern __shared__ uint32_t dsm[];
+  uint32_t* h = dsm;              // [kTkBins] histogram, later the finer digits'
+  uint32_t* mem = dsm + kTkBins;  // [C] member patterns, then [P_max] positions
   __shared__ uint32_t taken[kMaxC / 32];      // bitmap over candidate slots
   __shared__ uint2 mpair[kTkRankCap];         // (bit pattern, slot) of the first members
   __shared__ uint32_t wt[32], wt2[32];
-  __shared__ int s_bin;
-  __shared__ uint32_t s_above, s_cnt;
+  __shared__ int s_bin, s_wsel;
+  __shared__ uint32_t s_above, s_cnt, s_wbefore;
   // with the gather, pg.copies CTAs per (n, g) select alike (the selection
   // is deterministic) and each gathers one slice of the pool; copy 0 writes
   // idx and n_sel
@@ -896,7 +965,7 @@ __global__ void __launch_bounds__(kTkThreads)
   };
   if (early) load_inputs();
   // shared state cleared before the wait
-  for (int i = threadIdx.x; i < kHistBins; i += kTkThreads) h[i] = 0u;
+  for (int i = threadIdx.x; i < kTkBins; i += kTkThreads) h[i] = 0u;
   for (int i = threadIdx.x; i < kMaxC / 32; i += kTkThreads) taken[i] = 0u;
   if (threadIdx.x == 0) s_cnt = 0;
   griddep_enter();
@@ -940,16 +1009,17 @@ __global__ void __launch_bounds__(kTkThreads)
     __syncthreads();
 #pragma unroll
     for (int k = 0; k < kPer; ++k)
-      if (k < E && i0 + k < nc) atomicAdd(&h[v[k] >> 19], 1u);
+      if (k < E && i0 + k < nc) atomicAdd(&h[v[k] >> kTkShift], 1u);
     __syncthreads();
-    find_bin_from_top<kTkThreads>(h, kHistBins, uint32_t(Ke), wt, &s_bin, &s_above);
+    find_bin_wide<kTkThreads>(h, kTkBins, uint32_t(Ke), wt, &s_wsel, &s_wbefore, &s_bin,
+                              &s_above);
     b1 = uint32_t(s_bin);
     const uint32_t need = uint32_t(Ke) - s_above;  // winners to take inside bin b1
     // one warp-aggregated allocation for all of a thread's members
     uint32_t my_members = 0;
 #pragma unroll
     for (int k = 0; k < kPer; ++k)
-      my_members += (k < E && i0 + k < nc && (v[k] >> 19) == b1) ? 1u : 0u;
+      my_members += (k < E && i0 + k < nc && (v[k] >> kTkShift) == b1) ? 1u : 0u;
     uint32_t incl = my_members;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -962,7 +1032,7 @@ __global__ void __launch_bounds__(kTkThreads)
     uint32_t slot = wbase + incl - my_members;
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
-      if (k < E && i0 + k < nc && (v[k] >> 19) == b1) {
+      if (k < E && i0 + k < nc && (v[k] >> kTkShift) == b1) {
         mem[slot] = v[k];
         if (slot < uint32_t(kTkRankCap)) mpair[slot] = make_uint2(v[k], uint32_t(i0 + k));
         ++slot;
@@ -991,23 +1061,24 @@ __global__ void __launch_bounds__(kTkThreads)
         if (r0 + r1 + r2 + r3 < need) atomicOr(&taken[me.y >> 5], 1u << (me.y & 31));
       }
     } else {
-      // many members: resolve the remaining 19 bits with two more digits
-      for (int i = threadIdx.x; i < 2048; i += kTkThreads) h[i] = 0u;
+      // many members: resolve the remaining 17 bits with two more digits
+      constexpr uint32_t kMid = (1u << (kTkShift - 8)) - 1u;
+      for (int i = threadIdx.x; i <= int(kMid); i += kTkThreads) h[i] = 0u;
       __syncthreads();
       for (uint32_t i = threadIdx.x; i < cnt; i += kTkThreads)
-        atomicAdd(&h[(mem[i] >> 8) & 2047u], 1u);
+        atomicAdd(&h[(mem[i] >> 8) & kMid], 1u);
       __syncthreads();
       uint32_t nd = need;
-      find_bin_from_top<kTkThreads>(h, 2048, nd, wt, &s_bin, &s_above);
+      find_bin_from_top<kTkThreads>(h, int(kMid) + 1, nd, wt, &s_bin, &s_above);
       const uint32_t b2 = uint32_t(s_bin);
       nd -= s_above;
       for (int i = threadIdx.x; i < 256; i += kTkThreads) h[i] = 0u;
       __syncthreads();
       for (uint32_t i = threadIdx.x; i < cnt; i += kTkThreads)
-        if (((mem[i] >> 8) & 2047u) == b2) atomicAdd(&h[mem[i] & 255u], 1u);
+        if (((mem[i] >> 8) & kMid) == b2) atomicAdd(&h[mem[i] & 255u], 1u);
       __syncthreads();
       find_bin_from_top<kTkThreads>(h, 256, nd, wt, &s_bin, &s_above);
-      const uint32_t tau = (b1 << 19) | (b2 << 8) | uint32_t(s_bin);
+      const uint32_t tau = (b1 << kTkShift) | (b2 << 8) | uint32_t(s_bin);
       const uint32_t need_eq = nd - s_above;
       // members above tau, plus the first need_eq ties in slot order
       uint32_t n_eq = 0;
@@ -1017,7 +1088,7 @@ __global__ void __launch_bounds__(kTkThreads)
       block_excl_scan2<kTkThreads>(n_eq, 0u, wt, wt2, eq_before, d0, d1, d2);
 #pragma unroll
       for (int k = 0; k < kPer; ++k) {
-        if (!(k < E && i0 + k < nc) || (v[k] >> 19) != b1) continue;
+        if (!(k < E && i0 + k < nc) || (v[k] >> kTkShift) != b1) continue;
         bool t = v[k] > tau;
         if (v[k] == tau) t = eq_before++ < need_eq;
         if (t) atomicOr(&taken[(i0 + k) >> 5], 1u << ((i0 + k) & 31));
@@ -1033,8 +1104,8 @@ __global__ void __launch_bounds__(kTkThreads)
   for (int k = 0; k < kPer; ++k) {
     const int slot = i0 + k;
     if (!(k < E && slot < nc) || Ke == 0) continue;
-    if (take_all || (v[k] >> 19) > b1 ||
-        ((v[k] >> 19) == b1 && ((taken[slot >> 5] >> (slot & 31)) & 1u)))
+    if (take_all || (v[k] >> kTkShift) > b1 ||
+        ((v[k] >> kTkShift) == b1 && ((taken[slot >> 5] >> (slot & 31)) & 1u)))
       top_mask |= 1u << k;
   }
   if constexpr (!kEarlyPos) {
@@ -1112,7 +1183,7 @@ cudaError_t launch_topk_union(const herald_dims& dm, const int32_t* ctx, const i
                               const int32_t* k_seg, bool early) {
   static_assert(kMaxC <= 16 * kTkThreads, "16 scores per thread cover every C");
   const PoolGather pg = gather ? *gather : PoolGather{nullptr, nullptr, nullptr, nullptr, 0, 1};
-  const size_t smem = size_t(C) * 4 + (pg.pk ? size_t(P_max) * 4 : 0u);
+  const size_t smem = size_t(kTkBins) * 4 + size_t(C) * 4 + (pg.pk ? size_t(P_max) * 4 : 0u);
   HERALD_CHECK_LAUNCH(C <= 4 * kTkThreads ? ensure_smem(topk_union_kernel<4>, smem)
                                           : ensure_smem(topk_union_kernel<16>, smem));
   const int grid = dm.N * dm.Hkv * (pg.pk ? pg.copies : 1);
