@@ -1132,6 +1132,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 constexpr int kPoolMaxB = 64;
 // S takes TMEM columns [0, kpc + Bp) and O starts at column 256
 constexpr int kPoolMaxCols = 256;
+// 16 warps: four per TMEM lane quadrant share each row's softmax and its
+// O columns (the CTA holds its SM alone either way)
+constexpr int kPoolThreads = 512;
+constexpr int kPoolSplit = kPoolThreads / 128;  // warps per lane quadrant
 
 struct PoolSmem {
   uint32_t q, k, kb, v, vb, recv_o, recv_ml, total;
@@ -1162,7 +1166,7 @@ __host__ __device__ inline PoolSmem pool_smem(int D, int kpc, int Bp, int cs) {
 }
 
 template <int D, int CS>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kPoolThreads, 1)
     attn_pool_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap,
                      const __grid_constant__ CUtensorMap qmap,
@@ -1179,8 +1183,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t barK, barV, bar0, bar1, barR;
   __shared__ uint32_t tmem_base;
-  __shared__ float red_m[2][kTileM];
-  __shared__ float red_s[2][kTileM];
+  __shared__ float red_m[kPoolSplit][kTileM];
+  __shared__ float red_s[kPoolSplit][kTileM];
   __shared__ __align__(16) float2 ml[kTileM];
   constexpr uint32_t kSliceO = uint32_t(kPoolRows * OROW * 2);  // receive slot per sender
   constexpr uint32_t kSliceMl = uint32_t(kPoolRows * 8);
@@ -1279,7 +1283,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     debug_flag(threadIdx.x == 0 && (app.ctx[n] < 0 || app.ctx[n] > L_max), DEV_BAD_COUNT);
     L0 = min(max(app.ctx[n], 0), L_max);
     append_block_rows<1>(app.bk, app.bv, n, B, Hkv, D, L_max, L0, app.kc, app.vc,
-                         int(rank) * kTcThreads + threadIdx.x, kPoolCtas * kTcThreads);
+                         int(rank) * kPoolThreads + threadIdx.x, kPoolCtas * kPoolThreads);
   }
 
   // S = Q [K ; K_block]^T -> TMEM columns [0, kpc) and [kpc, kpc + Bp).
@@ -1322,16 +1326,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   // softmax over this CTA's columns, in log2 units, over the 16-key chunks
   // that hold a valid key (pool chunks, then block chunks), split between
-  // the two warps that share a TMEM lane quadrant
+  // the kPoolSplit warps that share a TMEM lane quadrant
   const int quad = warp & 3, ch = warp >> 2;
   const int row = quad * 32 + lane;
   const uint32_t trow = tbase + (uint32_t(quad * 32) << 16);
   const int npc = (nkp + 15) >> 4;                // pool chunks
   const int nbc = has_blk ? (B + 15) >> 4 : 0;   // block chunks
   const int nchunks = npc + nbc;
-  const int half = (nchunks + 1) >> 1;
-  const int c_begin = ch == 0 ? 0 : half, cnt = ch == 0 ? half : nchunks - half;
-  constexpr int kMaxChunks = kPoolMaxCols / 32;  // 16-column chunks per half
+  const int per = (nchunks + kPoolSplit - 1) / kPoolSplit;
+  const int c_begin = min(ch * per, nchunks), cnt = min(per, nchunks - c_begin);
+  constexpr int kMaxChunks = kPoolMaxCols / (16 * kPoolSplit);  // 16-column chunks per warp
   const float sl2 = scale * 1.4426950408889634f;              // scores -> log2 units
   float x[kMaxChunks][16];
   int nv[kMaxChunks];  // valid keys per chunk (warp-uniform)
@@ -1369,7 +1373,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   red_m[ch][row] = m;
   __syncthreads();
-  m = fmaxf(red_m[0][row], red_m[1][row]) * sl2;  // log2 units; -inf stays -inf
+#pragma unroll
+  for (int k = 0; k < kPoolSplit; ++k) m = fmaxf(m, red_m[k][row]);
+  m *= sl2;                                        // log2 units; -inf stays -inf
   const float mm = m == -INFINITY ? 0.f : m;      // no valid key: every p is 2^-inf = 0
   // p = 2^(x sl2 - m): the scaling and the shift as one paired fma for two
   // keys, the row sum as paired adds
@@ -1439,18 +1445,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // O partial -> shared memory over the dead Q/K operands (dead since S):
   // each row divided by its sum and stored as fp16 (|o / l| <= max |v|); the
   // merge re-weights by (max, sum), which stay fp32
-  const float lrow = red_s[0][row] + red_s[1][row];
+  float lrow = 0.f;
+#pragma unroll
+  for (int k = 0; k < kPoolSplit; ++k) lrow += red_s[k][row];
   uint16_t* Os = reinterpret_cast<uint16_t*>(base);
-  if (any) {
+  if (any) {  // D / kPoolSplit columns of the row per warp
     const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
     uint16_t* orow = Os + row * OROW;
-#pragma unroll
-    for (int k = 0; k < D / 64; ++k) {
-      float v[32];
-      const int col = ch * (D / 2) + k * 32;
+    constexpr int kW = D / kPoolSplit;
+    static_assert(kW == 16 || kW == 32, "16 or 32 O columns per warp");
+    float v[kW];
+    const int col = ch * kW;
+    if constexpr (kW == 32)
       tmem_ld32(trow + 256 + uint32_t(col), v);
+    else
+      tmem_ld16(trow + 256 + uint32_t(col), v);
+    {
 #pragma unroll
-      for (int i = 0; i < 32; i += 8) {
+      for (int i = 0; i < kW; i += 8) {
         uint4 h;
         h.x = pack_half2(v[i] * inv, v[i + 1] * inv);
         h.y = pack_half2(v[i + 2] * inv, v[i + 3] * inv);
@@ -1491,7 +1503,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // merge this CTA's rows from the CS received partials:
   // out = sum_c 2^(m_c - M) l_c (o_c / l_c) / sum_c 2^(m_c - M) l_c
   constexpr int E = D / 32;
-  for (int rr = warp; rr < my_rows; rr += kTcThreads / 32) {
+  for (int rr = warp; rr < my_rows; rr += kPoolThreads / 32) {
     const int lr = int(rank) * kPoolRows + rr;
     if (lr >= rows_t) break;  // warp-uniform: rows past the tile's tokens
     const int grow = b0 * G + lr;
@@ -1645,7 +1657,7 @@ static int pool_resident_clusters(uint32_t smem) {
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(CS, 1, 1);
-  cfg.blockDim = dim3(kTcThreads);
+  cfg.blockDim = dim3(kPoolThreads);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1780,17 +1792,17 @@ static cudaError_t launch_attn_t(const herald_dims& dm, const uint16_t* q, const
       const int early = settled && tiles * segs <= resident ? 1 : 0;
       const AppendArgs none{nullptr, nullptr, nullptr, nullptr, nullptr, 0};
       if (cs == 16)
-        return launch_cluster("attn_pool_kernel", attn_pool_kernel<D, 16>, dim3(16, tiles, segs),
-                              16, smem, st, maps->k, maps->v, maps->q, maps->bk, maps->bv, n_sel,
+        return launch_cluster_threads("attn_pool_kernel", attn_pool_kernel<D, 16>,
+                                      dim3(16, tiles, segs), dim3(kPoolThreads), 16, smem, st, maps->k, maps->v, maps->q, maps->bk, maps->bv, n_sel,
                               P_max, dm.B, dm.Hq, dm.Hkv, maps->bpt, kpc, scale, early, out, err,
                               app ? *app : none, dm.L_max);
       if (cs == 12)
-        return launch_cluster("attn_pool_kernel", attn_pool_kernel<D, 12>, dim3(12, tiles, segs),
-                              12, smem, st, maps->k, maps->v, maps->q, maps->bk, maps->bv, n_sel,
+        return launch_cluster_threads("attn_pool_kernel", attn_pool_kernel<D, 12>,
+                                      dim3(12, tiles, segs), dim3(kPoolThreads), 12, smem, st, maps->k, maps->v, maps->q, maps->bk, maps->bv, n_sel,
                               P_max, dm.B, dm.Hq, dm.Hkv, maps->bpt, kpc, scale, early, out, err,
                               app ? *app : none, dm.L_max);
-      return launch_cluster("attn_pool_kernel", attn_pool_kernel<D, 8>, dim3(8, tiles, segs), 8,
-                            smem, st, maps->k, maps->v, maps->q, maps->bk, maps->bv, n_sel, P_max,
+      return launch_cluster_threads("attn_pool_kernel", attn_pool_kernel<D, 8>,
+                                    dim3(8, tiles, segs), dim3(kPoolThreads), 8, smem, st, maps->k, maps->v, maps->q, maps->bk, maps->bv, n_sel, P_max,
                             dm.B, dm.Hq, dm.Hkv, maps->bpt, kpc, scale, early, out, err,
                             app ? *app : none, dm.L_max);
     }
