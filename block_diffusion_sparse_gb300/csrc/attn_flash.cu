@@ -10,12 +10,12 @@
 // the B block keys as one more tile; kpc is a whole number of tiles, as few
 // as let every CTA hold the same number of tiles (the last one's block tile
 // included).  Warp roles:
-//   warps 0-7  softmax: thread = (query row, half of the tile's 16-key
-//              chunks); S from TMEM, P (bf16) back into the same TMEM
-//              columns
-//   warp 8     TMA producer of the query tile and the K tiles (2-stage ring)
-//   warp 9     TMA producer of the V tiles (2-stage ring)
-//   warp 10    tcgen05.mma issuer: S_t = Q K_t^T into one of three TMEM
+//   warps 0-15 softmax: thread = (query row, a quarter of the tile's
+//              16-key chunks); S from TMEM, P (bf16) back into the same
+//              TMEM columns
+//   warp 16    TMA producer of the query tile and the K tiles (2-stage ring)
+//   warp 17    TMA producer of the V tiles (2-stage ring)
+//   warp 18    tcgen05.mma issuer: S_t = Q K_t^T into one of three TMEM
 //              buffers, O += P_t V_t into the TMEM accumulator with P_t
 //              read from TMEM (the A operand of the MMA)
 // The MMA warp keeps S two tiles ahead of the softmax warps (three S/P
@@ -41,10 +41,11 @@
 namespace herald {
 
 constexpr int kFT = kFlashTileKeys;         // keys per pipelined tile (MMA N, a multiple of 16)
-constexpr int kFlashSoftWarps = 8;          // two per TMEM lane quadrant
+constexpr int kFlashSoftWarps = 16;         // four per TMEM lane quadrant
+constexpr int kFlashSplit = kFlashSoftWarps / 4;  // softmax warps sharing a row
 constexpr int kFlashSoftThreads = kFlashSoftWarps * 32;
-constexpr int kFlashKWarp = 8, kFlashVWarp = 9, kFlashMmaWarp = 10;
-constexpr int kFlashThreads = 11 * 32;
+constexpr int kFlashKWarp = 16, kFlashVWarp = 17, kFlashMmaWarp = 18;
+constexpr int kFlashThreads = 19 * 32;
 constexpr float kFlashRebase = 8.f;         // log2 units
 constexpr uint32_t kFlashTmemCols = 512;    // S/P buffers at 0, 128, 256; O at 384
 constexpr int kSBufs = 3;                   // S/P buffers in TMEM
@@ -92,8 +93,8 @@ __global__ void __launch_bounds__(kFlashThreads, 1)
   __shared__ uint64_t barQ, kfull[2], kempty[2], vfull[2], vempty[2];
   __shared__ uint64_t sfull[kSBufs], pfull[kSBufs], pvdone[kSBufs], alldone, barR;
   __shared__ uint32_t tmem_base;
-  __shared__ float red_m[2][2][kTileM];  // [tile parity][column half][row]
-  __shared__ float red_s[2][kTileM];
+  __shared__ float red_m[2][kFlashSplit][kTileM];  // [tile parity][column share][row]
+  __shared__ float red_s[kFlashSplit][kTileM];
   __shared__ __align__(16) float2 ml[kTileM];
   constexpr uint32_t kSliceO = uint32_t(RC * OROW * 2);
   constexpr uint32_t kSliceMl = uint32_t(RC * 8);
@@ -303,11 +304,11 @@ __global__ void __launch_bounds__(kFlashThreads, 1)
       const int s = t & 1, b3 = t % kSBufs;
       const int nk = tile_keys(t);
       const int nchunks = (nk + 15) >> 4;
-      const int half = (nchunks + 1) >> 1;
-      const int c_begin = ch == 0 ? 0 : half, cnt = ch == 0 ? half : nchunks - half;
+      const int per = (nchunks + kFlashSplit - 1) / kFlashSplit;
+      const int c_begin = min(ch * per, nchunks), cnt = min(per, nchunks - c_begin);
       if (!mbar_wait(&sfull[b3], (t / kSBufs) & 1)) bad |= 0x80u;
       tc_fence_after();
-      constexpr int kMaxChunks = (kFT / 16 + 1) / 2;
+      constexpr int kMaxChunks = (kFT / 16 + kFlashSplit - 1) / kFlashSplit;
       float x[kMaxChunks][16];
 #pragma unroll
       for (int c = 0; c < kMaxChunks; ++c) {
@@ -340,7 +341,9 @@ __global__ void __launch_bounds__(kFlashThreads, 1)
       }
       red_m[s][ch][row] = m;
       softmax_bar();
-      const float mt_ = fmaxf(red_m[s][0][row], red_m[s][1][row]) * sl2;
+#pragma unroll
+      for (int k = 0; k < kFlashSplit; ++k) m = fmaxf(m, red_m[s][k][row]);
+      const float mt_ = m * sl2;
       // a new base only when the max rises by more than kFlashRebase
       const bool rebase = m_base == -INFINITY || mt_ > m_base + kFlashRebase;
       float factor = 1.f;
@@ -354,11 +357,11 @@ __global__ void __launch_bounds__(kFlashThreads, 1)
         // pvdone[(t-1) % 3], whose next completion needs this thread's P_{t+2}
         if (!mbar_wait(&pvdone[(t - 1) % kSBufs], ((t - 1) / kSBufs) & 1)) bad |= 0x100u;
         tc_fence_after();
-        {  // this thread's half of its O row
+        {  // this thread's share of its O row
 #pragma unroll
-          for (int k = 0; k < D / 32; ++k) {
+          for (int k = 0; k < D / (16 * kFlashSplit); ++k) {
             float v[16];
-            const uint32_t col = kOCol + uint32_t(ch * (D / 2) + k * 16);
+            const uint32_t col = kOCol + uint32_t(ch * (D / kFlashSplit) + k * 16);
             tmem_ld16(trow + col, v);
             uint32_t w[16];
 #pragma unroll
@@ -418,15 +421,18 @@ __global__ void __launch_bounds__(kFlashThreads, 1)
     }
     red_s[ch][row] = l;
     softmax_bar();
-    const float lrow = red_s[0][row] + red_s[1][row];
+    float lrow = 0.f;
+#pragma unroll
+    for (int k = 0; k < kFlashSplit; ++k) lrow += red_s[k][row];
     // O / l as fp16 rows over the K ring (dead: every MMA is done): every
     // TMEM load issued, one wait, then the shared-memory stores
-    uint16_t* orow = reinterpret_cast<uint16_t*>(Kr) + row * OROW + ch * (D / 2);
+    constexpr int kW = D / kFlashSplit;  // O columns per thread
+    uint16_t* orow = reinterpret_cast<uint16_t*>(Kr) + row * OROW + ch * kW;
     if (nt > 0) {
       const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
-      uint32_t r[D / 2];
+      uint32_t r[kW];
 #pragma unroll
-      for (int k = 0; k < D / 32; ++k) {
+      for (int k = 0; k < kW / 16; ++k) {
         uint32_t* q = r + k * 16;
         asm volatile(
             "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
@@ -434,11 +440,11 @@ __global__ void __launch_bounds__(kFlashThreads, 1)
             : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]),
               "=r"(q[6]), "=r"(q[7]), "=r"(q[8]), "=r"(q[9]), "=r"(q[10]), "=r"(q[11]),
               "=r"(q[12]), "=r"(q[13]), "=r"(q[14]), "=r"(q[15])
-            : "r"(trow + kOCol + uint32_t(ch * (D / 2) + k * 16)));
+            : "r"(trow + kOCol + uint32_t(ch * kW + k * 16)));
       }
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-      for (int i = 0; i < D / 2; i += 8) {
+      for (int i = 0; i < kW; i += 8) {
         const float* v = reinterpret_cast<const float*>(r + i);
         *reinterpret_cast<uint4*>(orow + i) =
             make_uint4(pack_half2(v[0] * inv, v[1] * inv), pack_half2(v[2] * inv, v[3] * inv),
