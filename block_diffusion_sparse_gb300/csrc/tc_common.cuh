@@ -57,12 +57,12 @@ constexpr int kTcThreads = 256;  // 8 warps: lane quadrant = warp % 4
 // whole rows per step (one 16-byte chunk per lane), so src_of runs once
 // per lane and step, and the unrolled steps keep several rows in flight.
 // Every thread of the (kTcThreads-thread) block must call it.
-template <int D, typename SrcOf>
+template <int D, int NT = kTcThreads, typename SrcOf>
 __device__ __forceinline__ void load_rows_sw128(uint8_t* tile, int rows, int rows_alloc,
                                                 const uint16_t* any_src, SrcOf src_of) {
   constexpr int CPR = D / 8;        // 16-byte chunks per row
   constexpr int RPW = 32 / CPR;     // rows per warp step
-  constexpr int kStep = (kTcThreads / 32) * RPW;
+  constexpr int kStep = (NT / 32) * RPW;  // NT threads in the block
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = lane % CPR, sub = lane / CPR;
   uint8_t* half = tile + (c >> 3) * (rows_alloc * 128);

@@ -8,8 +8,8 @@
 //   refine_pass2  S^T = K_cand . Q_blk^T for 128 candidates x all B*G rows;
 //                 each thread owns one candidate and sums the row-softmax
 //                 probabilities over the rows -> s2 (column sum)
-//   refine_fused  stage 2 in one pass when C <= 4096: a cluster of 12 (or
-//                 8) CTAs per row tile shares the row statistics,
+//   refine_fused  stage 2 in one pass when C <= 4096: a cluster of 16, 12
+//                 or 8 CTAs per row tile shares the row statistics,
 //                 exponentials are kept in TMEM and summed by column
 //   attn_pool     sparse block attention over the pool (HERALD early
 //                 abstract: the selected subset is reused for every
@@ -324,15 +324,19 @@ __global__ void __launch_bounds__(kTcThreads)
 // shared memory; after one cluster barrier each CTA merges them into the row
 // log-sum-exp from its own shared memory, sums exp(S - lse_r) over its 128
 // rows (warp shuffle reductions, rows past B*G excluded) and writes one
-// partial s2 per row tile, which the top-K kernel adds up.  Clusters of 12
-// CTAs (cpc = C/12: three quarters of the UMMA and exponential work per
-// CTA) where every cluster of the launch is resident at once, else 8.
+// partial s2 per row tile, which the top-K kernel adds up.  The cluster
+// has 16, 12 or 8 CTAs: the size with the fewest candidates per CTA (they
+// set the UMMA, exponential and column-sum work of each CTA) among those
+// whose clusters are all resident at once.
 constexpr int kFuseMaxCpc = 512;
+// 16 warps: the four warps of a TMEM lane quadrant take every fourth
+// 32-column chunk of the CTA's candidates
+constexpr int kFuseThreads = 512;
+constexpr int kFuseSplit = kFuseThreads / 128;
 
-// candidates per CTA of a cs-CTA cluster: a multiple of 64 so that each
-// warp's column half is whole 32-column chunks
+// candidates per CTA of a cs-CTA cluster, in whole 32-column chunks
 __host__ __device__ inline int fuse_cpc(int C, int cs = 8) {
-  return ((C + cs - 1) / cs + 63) / 64 * 64;
+  return ((C + cs - 1) / cs + 31) / 32 * 32;
 }
 
 template <int D>
@@ -345,7 +349,7 @@ struct FuseCfg {
 };
 
 template <int D, int kFuseCtas>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kFuseThreads, 1)
     refine_fused_kernel(const __grid_constant__ CUtensorMap qmap,
                         const uint16_t* __restrict__ kc, const int32_t* __restrict__ cand,
                         const int32_t* __restrict__ n_cand, int B, int Hq, int Hkv, int L_max,
@@ -356,9 +360,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ uint64_t bar0, barQ;
   __shared__ uint32_t tmem_base;
   __shared__ int32_t pos[kFuseMaxCpc];
-  __shared__ float2 half_stat[2][kTileM];
+  __shared__ float2 part_stat[kFuseSplit][kTileM];
   __shared__ __align__(16) float2 peer_stat[kFuseCtas][kTileM];  // [sender][row]
-  __shared__ float colsum[2][4][kFuseMaxCpc / 2];
+  __shared__ float colsum[4][kFuseMaxCpc];  // [lane quadrant][candidate]
   uint8_t* Qs = align1024(smem_raw);
   uint8_t* Ks = Qs + Cfg::kQBytes;
   const uint32_t rank = cluster_ctarank();
@@ -392,17 +396,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // below C lies inside the list, and rows past n_cand are masked below
   const int c0 = int(rank) * cpc;
   const int32_t* cd = cand ? cand + size_t(seg) * C : nullptr;  // null: row = slot
-  int pr[kFuseMaxCpc / kTcThreads];
+  int pr[kFuseMaxCpc / kFuseThreads];
 #pragma unroll
-  for (int k = 0; k < kFuseMaxCpc / kTcThreads; ++k) {
-    const int r = threadIdx.x + k * kTcThreads;
+  for (int k = 0; k < kFuseMaxCpc / kFuseThreads; ++k) {
+    const int r = threadIdx.x + k * kFuseThreads;
     pr[k] = (cd && r < cpc && c0 + r < C) ? cd[c0 + r] : -1;
   }
   const int nc = min(max(n_cand[seg], 0), C);
   const int ncv = min(max(nc - c0, 0), cpc);  // valid candidates of this CTA
 #pragma unroll
-  for (int k = 0; k < kFuseMaxCpc / kTcThreads; ++k) {
-    const int r = threadIdx.x + k * kTcThreads;
+  for (int k = 0; k < kFuseMaxCpc / kFuseThreads; ++k) {
+    const int r = threadIdx.x + k * kFuseThreads;
     if (r < cpc) {
       const int p = r < ncv ? (cand ? pr[k] : c0 + r) : -1;
       debug_flag(r < ncv && (p < 0 || p >= L_max), DEV_BAD_INDEX);  // a candidate past the cache
@@ -413,13 +417,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // the tile's rows past its G*bpt query rows are never loaded: zeroed, so
   // that every score row is finite and the column sums below can weight
   // rows with a product (rows past the tile's tokens get weight 0)
-  for (int u = G * bpt * 8 + threadIdx.x; u < kTileM * 8; u += kTcThreads) {
+  for (int u = G * bpt * 8 + threadIdx.x; u < kTileM * 8; u += kFuseThreads) {
 #pragma unroll
     for (int hv = 0; hv < D / 64; ++hv)
       *reinterpret_cast<uint4*>(Qs + hv * kTileM * 128 + u * 16) = make_uint4(0u, 0u, 0u, 0u);
   }
   if (ncv > 0) {
-    load_rows_sw128<D>(Ks, cpc, cpc, kc, [&](int r) -> const uint16_t* {
+    load_rows_sw128<D, kFuseThreads>(Ks, cpc, cpc, kc, [&](int r) -> const uint16_t* {
       const int p = pos[r];
       return p < 0 ? nullptr : kc + (size_t(seg) * L_max + p) * D;
     });
@@ -456,18 +460,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   __syncwarp();
 
-  // row (max, sumexp) over this CTA's candidates, log2 units; the two warps of
-  // a lane quadrant take the two column halves.  The exponentials
-  // p = 2^(s - m_half) are stored back over the scores, so the column sums
-  // below only rescale them by 2^(m_half - lse).
+  // row (max, sumexp) over this CTA's candidates, log2 units; the four warps
+  // of a lane quadrant take every fourth 32-column chunk.  The exponentials
+  // p = 2^(s - m_part) are stored back over the scores, so the column sums
+  // below only rescale them by 2^(m_part - lse).
   const int quad = warp & 3, ch = warp >> 2;
   const int row = quad * 32 + lane;
   const uint32_t trow = tbase + (uint32_t(quad * 32) << 16);
   const float sl2 = scale * 1.4426950408889634f;
-  const int hc0 = ch * (cpc / 2);                        // this warp's columns
-  const int hc1 = min(hc0 + cpc / 2, ncv + 31 & ~31);   // up to the last valid chunk
+  const int nvc = (ncv + 31) >> 5;  // chunks up to the last valid one
   float m = -INFINITY;
-  for (int c = hc0; c < hc1; c += 32) {
+  for (int k = ch; k < nvc; k += kFuseSplit) {
+    const int c = k * 32;
     float v[32];
     tmem_ld32(trow + uint32_t(c), v);
     if (c + 32 > ncv) {  // the one partial chunk
@@ -483,7 +487,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint64_t sl2x2 = f2_pack(sl2, sl2);
   const uint64_t nmx2 = m == -INFINITY ? f2_pack(0.f, 0.f) : f2_pack(-m, -m);
   uint64_t l2 = f2_pack(0.f, 0.f);
-  for (int c = hc0; c < hc1; c += 32) {
+  for (int k = ch; k < nvc; k += kFuseSplit) {
+    const int c = k * 32;
     float v[32];
     tmem_ld32(trow + uint32_t(c), v);
 #pragma unroll
@@ -505,14 +510,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   f2_unpack(l2, l, l_hi);
   l += l_hi;
   tmem_wait_st();
-  half_stat[ch][row] = make_float2(m, l);
+  part_stat[ch][row] = make_float2(m, l);
   __syncthreads();
   __cluster_barrier_wait();  // every CTA of the cluster has started
   if (ch == 0) {
-    const float2 a = half_stat[0][row], b = half_stat[1][row];
-    const float M = fmaxf(a.x, b.x);
-    const float Lr = (a.x == -INFINITY ? 0.f : a.y * fast_exp2(a.x - M)) +
-                     (b.x == -INFINITY ? 0.f : b.y * fast_exp2(b.x - M));
+    float2 a[kFuseSplit];
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kFuseSplit; ++k) {
+      a[k] = part_stat[k][row];
+      M = fmaxf(M, a[k].x);
+    }
+    float Lr = 0.f;
+#pragma unroll
+    for (int k = 0; k < kFuseSplit; ++k)
+      if (a[k].x != -INFINITY) Lr += a[k].y * fast_exp2(a[k].x - M);
 #pragma unroll
     for (int c = 0; c < kFuseCtas; ++c)
       st_peer_f2(peer_addr(&peer_stat[rank][row], uint32_t(c)), make_float2(M, Lr));
@@ -534,7 +546,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     lse = M + __log2f(Lr);
   }
   const bool row_ok = row < rows_t;
-  // 2^(s - lse) = p * 2^(m_half - lse); rows past the tile's tokens contribute nothing
+  // 2^(s - lse) = p * 2^(m_part - lse); rows past the tile's tokens contribute nothing
   const float f = (row_ok && m != -INFINITY) ? fast_exp2(m - lse) : 0.f;
   // column sums over the 128 rows: per 32-column chunk each warp sums its
   // 32 rows by a butterfly of shuffles (after the step of distance sd each
@@ -543,7 +555,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // Rows past the tile's tokens are finite (zeroed or real queries) and
   // weighted 0.
   const uint64_t ff = f2_pack(f, f);
-  for (int c = hc0; c < hc1; c += 32) {
+  for (int k = ch; k < nvc; k += kFuseSplit) {
+    const int c = k * 32;
     float v[32];
     tmem_ld32(trow + uint32_t(c), v);
 #pragma unroll
@@ -557,31 +570,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         v[j] = (upper ? hi : lo) + __shfl_xor_sync(0xffffffffu, upper ? lo : hi, sd);
       }
     }
-    colsum[ch][quad][c - hc0 + lane] = v[0];
+    colsum[quad][c + lane] = v[0];
   }
   __syncthreads();
   float* out = s2p + (size_t(mt) * gridDim.z + seg) * C;
-  const int hw = cpc / 2;
-  for (int j = threadIdx.x; j < cpc; j += kTcThreads) {
-    if (c0 + j >= nc) continue;
-    const int chh = j / hw, jj = j - chh * hw;
-    out[c0 + j] = colsum[chh][0][jj] + colsum[chh][1][jj] + colsum[chh][2][jj] +
-                  colsum[chh][3][jj];
-  }
+  for (int j = threadIdx.x; j < ncv; j += kFuseThreads)
+    out[c0 + j] = colsum[0][j] + colsum[1][j] + colsum[2][j] + colsum[3][j];
   // no peer touches this CTA's shared memory after the cluster barrier
   tmem_teardown(tbase, 512);
 }
 
 bool refine_fused_ok(int C) { return fuse_cpc(C) <= kFuseMaxCpc; }
 
-// Clusters of 12 where every cluster of the launch is resident at once.
-template <int D>
-static int refine_cluster_size(int clusters) {
+// Clusters of CS CTAs of the fused refine that can be resident at once on
+// the current device; cached per (device, CS).
+template <int D, int CS>
+static int refine_resident_clusters() {
   static std::mutex mu;
   static int cache[64];
   static bool init = false;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   int n;
   {
     std::lock_guard<std::mutex> lock(mu);
@@ -593,27 +602,57 @@ static int refine_cluster_size(int clusters) {
   }
   if (n < 0) {
     n = 0;
-    if (ensure_smem(refine_fused_kernel<D, 12>, FuseCfg<D>::kSmem) == cudaSuccess &&
-        ensure_nonportable_cluster(refine_fused_kernel<D, 12>) == cudaSuccess) {
+    if (ensure_smem(refine_fused_kernel<D, CS>, FuseCfg<D>::kSmem) == cudaSuccess &&
+        ensure_nonportable_cluster(refine_fused_kernel<D, CS>) == cudaSuccess) {
       cudaLaunchConfig_t cfg{};
-      cfg.gridDim = dim3(12, 1, 1);
-      cfg.blockDim = dim3(kTcThreads);
+      cfg.gridDim = dim3(CS, 1, 1);
+      cfg.blockDim = dim3(kFuseThreads);
       cfg.dynamicSmemBytes = FuseCfg<D>::kSmem;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = 12;
+      attr[0].val.clusterDim.x = CS;
       attr[0].val.clusterDim.y = 1;
       attr[0].val.clusterDim.z = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&n, refine_fused_kernel<D, 12>, &cfg) != cudaSuccess)
+      if (cudaOccupancyMaxActiveClusters(&n, refine_fused_kernel<D, CS>, &cfg) != cudaSuccess)
         n = 0;
     }
     cudaGetLastError();
     std::lock_guard<std::mutex> lock(mu);
     cache[dev] = n;
   }
-  return clusters <= n ? 12 : 8;
+  return n;
+}
+
+// Among the cluster sizes (16, 12, 8 CTAs) whose clusters are all resident
+// at once, the one with the fewest candidates per CTA (they set every
+// phase of the chain), the smallest such; else 8.
+template <int D>
+static int refine_cluster_size(int clusters, int C) {
+  int best = 8;
+  for (int cs : {12, 16}) {
+    const int n = cs == 16 ? refine_resident_clusters<D, 16>() : refine_resident_clusters<D, 12>();
+    if (clusters <= n && fuse_cpc(C, cs) < fuse_cpc(C, best)) best = cs;
+  }
+  return best;
+}
+
+template <int D, int CS>
+static cudaError_t launch_refine_cs(const herald_dims& dm, const uint16_t* k_cache,
+                                    const int32_t* cand, const int32_t* n_cand, int C, float* s2,
+                                    const WsLayout& w, uint32_t* err, const CUtensorMap& qmap,
+                                    cudaStream_t st) {
+  const int segs = dm.N * dm.Hkv;
+  const int bpt = kTileM / (dm.Hq / dm.Hkv);
+  const float scale = 1.0f / sqrtf(float(dm.d));
+  const int cpc = fuse_cpc(C, CS);
+  HERALD_CHECK_LAUNCH(ensure_smem(refine_fused_kernel<D, CS>, FuseCfg<D>::kSmem));
+  if (CS > 8) HERALD_CHECK_LAUNCH(ensure_nonportable_cluster(refine_fused_kernel<D, CS>));
+  return launch_cluster_threads("refine_fused_kernel", refine_fused_kernel<D, CS>,
+                                dim3(CS, w.MT_tok, segs), dim3(kFuseThreads), CS,
+                                FuseCfg<D>::kSmem, st, qmap, k_cache, cand, n_cand, dm.B, dm.Hq,
+                                dm.Hkv, dm.L_max, C, bpt, cpc, scale, s2, err);
 }
 
 template <int D>
@@ -621,22 +660,14 @@ static cudaError_t launch_refine_fused(const herald_dims& dm, const uint16_t* k_
                                        const int32_t* cand, const int32_t* n_cand, int C,
                                        float* s2, const WsLayout& w, uint32_t* err,
                                        const CUtensorMap& qmap, cudaStream_t st) {
-  const int segs = dm.N * dm.Hkv;
-  const int bpt = kTileM / (dm.Hq / dm.Hkv);
-  const float scale = 1.0f / sqrtf(float(dm.d));
-  if (refine_cluster_size<D>(w.MT_tok * segs) == 12) {
-    const int cpc = fuse_cpc(C, 12);
-    HERALD_CHECK_LAUNCH(ensure_smem(refine_fused_kernel<D, 12>, FuseCfg<D>::kSmem));
-    return launch_cluster("refine_fused_kernel", refine_fused_kernel<D, 12>,
-                          dim3(12, w.MT_tok, segs), 12, FuseCfg<D>::kSmem, st, qmap, k_cache,
-                          cand, n_cand, dm.B, dm.Hq, dm.Hkv, dm.L_max, C, bpt, cpc, scale, s2,
-                          err);
+  switch (refine_cluster_size<D>(w.MT_tok * dm.N * dm.Hkv, C)) {
+    case 16:
+      return launch_refine_cs<D, 16>(dm, k_cache, cand, n_cand, C, s2, w, err, qmap, st);
+    case 12:
+      return launch_refine_cs<D, 12>(dm, k_cache, cand, n_cand, C, s2, w, err, qmap, st);
+    default:
+      return launch_refine_cs<D, 8>(dm, k_cache, cand, n_cand, C, s2, w, err, qmap, st);
   }
-  const int cpc = fuse_cpc(C, 8);
-  HERALD_CHECK_LAUNCH(ensure_smem(refine_fused_kernel<D, 8>, FuseCfg<D>::kSmem));
-  return launch_cluster("refine_fused_kernel", refine_fused_kernel<D, 8>, dim3(8, w.MT_tok, segs),
-                        8, FuseCfg<D>::kSmem, st, qmap, k_cache, cand, n_cand, dm.B, dm.Hq,
-                        dm.Hkv, dm.L_max, C, bpt, cpc, scale, s2, err);
 }
 
 // Pass 1 -> row lse -> pass 2 (C > 4096).
