@@ -1,4 +1,4 @@
-// block_scan.cuh -- block-wide scans and the radix-select bin search shared
+// block_scan.cuh -- block-wide scans and the radix-select bin searches shared
 // by the selection kernels (select_kernels.cu).
 #pragma once
 #include <stdint.h>
@@ -97,6 +97,67 @@ __device__ __forceinline__ void block_excl_scan2(uint32_t a, uint32_t b, uint32_
   eb = (warp ? wb[warp - 1] : 0u) + y - b;
   ta = wa[NW - 1];
   tb = wb[NW - 1];
+  __syncthreads();
+}
+
+// The bin holding the need-th largest element of a wide histogram h[0..nb)
+// (nb a multiple of 32 * 32; rank order counts from the top bin) and the
+// count strictly above it: every warp sums its nb/32 bins with lane-strided
+// (bank-conflict-free) reads, warp 0 scans the warp totals, and only the
+// warp holding the rank walks its bins in order.
+template <int NT>
+__device__ void find_bin_wide(const uint32_t* h, int nb, uint32_t need, uint32_t* warp_tot,
+                              int* s_warp, uint32_t* s_before, int* out_bin,
+                              uint32_t* out_above) {
+  constexpr int NW = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per_w = nb / NW;  // rank-order bins of a warp
+  uint32_t sum = 0;
+  for (int k = lane; k < per_w; k += 32) sum += h[nb - 1 - (warp * per_w + k)];
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane == 0) warp_tot[warp] = sum;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t t = lane < NW ? warp_tot[lane] : 0u;
+    uint32_t incl = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const uint32_t excl = incl - t;
+    if (lane < NW && excl < need && need <= incl) {
+      *s_warp = lane;
+      *s_before = excl;
+    }
+  }
+  __syncthreads();
+  const int W = *s_warp;
+  if (warp == W) {
+    const int per_l = per_w / 32;  // consecutive rank-order bins of a lane
+    const int rb0 = W * per_w + lane * per_l;
+    uint32_t local = 0;
+    for (int k = 0; k < per_l; ++k) local += h[nb - 1 - (rb0 + k)];
+    uint32_t incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    uint32_t acc = *s_before + incl - local;
+    if (acc < need && need <= acc + local) {
+      for (int k = 0; k < per_l; ++k) {
+        const uint32_t c = h[nb - 1 - (rb0 + k)];
+        if (acc + c >= need) {
+          *out_bin = nb - 1 - (rb0 + k);
+          *out_above = acc;
+          break;
+        }
+        acc += c;
+      }
+    }
+  }
   __syncthreads();
 }
 

@@ -603,26 +603,15 @@ cudaError_t launch_s1_hist(const herald_dims& dm, const float* logits, const flo
   return cudaGetLastError();
 }
 
-// Warp-aggregated append: lanes with `take` get consecutive slots from one
-// atomicAdd per warp on *counter.  Every lane of the warp must call it.
-__device__ __forceinline__ uint32_t warp_append_slot(bool take, uint32_t* counter) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t mask = __ballot_sync(0xffffffffu, take);
-  if (!mask) return 0xffffffffu;
-  const int leader = __ffs(mask) - 1;
-  uint32_t base = 0;
-  if (lane == leader) base = atomicAdd(counter, uint32_t(__popc(mask)));
-  base = __shfl_sync(0xffffffffu, base, leader);
-  return take ? base + uint32_t(__popc(mask & ((1u << lane) - 1u))) : 0xffffffffu;
-}
-
 // ============================================================ topc_finish
 // One CTA of 1024 threads per (n, g).  Radix select of the C-th largest s1:
 // the first 12-bit digit comes from the global histogram; the members of
 // that bin are collected into shared memory (bounded; a global two-digit
 // fallback handles overflow) and the remaining 19 bits are resolved there.
 // The ordered compaction then keeps every s1 above the threshold plus the
-// lowest-position ties, with one two-counter block scan.
+// lowest-position ties, with one two-counter block scan per round.  Both
+// passes over s1 load each round while the previous one is processed, and
+// the collection takes one shared-memory atomic per warp and round.
 constexpr int kSelThreads = 1024;
 constexpr int kTieCap = 6144;
 
@@ -655,8 +644,8 @@ __global__ void __launch_bounds__(kSelThreads)
   __shared__ uint32_t h[kHistBins];
   __shared__ uint32_t tie_v[kTieCap];
   __shared__ uint32_t wt[32], wt2[32];
-  __shared__ int s_bin;
-  __shared__ uint32_t s_above, s_cnt;
+  __shared__ int s_bin, s_wsel;
+  __shared__ uint32_t s_above, s_cnt, s_wbefore;
   griddep_enter();
   const int seg = blockIdx.x, n = seg / Hkv;
   const int L = min(max(ctx[n], 0), L_max);
@@ -670,27 +659,50 @@ __global__ void __launch_bounds__(kSelThreads)
     for (int i = threadIdx.x; i < L; i += kSelThreads) out[i] = i;
     return;
   }
-  // digit 1: bits [30:19] from the global histogram
+  // digit 1: bits [30:19] from the global histogram, searched while the
+  // first round of s1 loads
   for (int i = threadIdx.x; i < kHistBins; i += kSelThreads)
     h[i] = hist[size_t(seg) * kHistBins + i];
   if (threadIdx.x == 0) s_cnt = 0;
+  const int lane = threadIdx.x & 31;
+  uint32_t v[kPerThr], vn[kPerThr];
+  load_round(sv, L, 0, v);
   __syncthreads();
   uint32_t need = uint32_t(Ce);
-  find_bin_from_top<kSelThreads>(h, kHistBins, need, wt, &s_bin, &s_above);
+  find_bin_wide<kSelThreads>(h, kHistBins, need, wt, &s_wsel, &s_wbefore, &s_bin, &s_above);
   const uint32_t b1 = uint32_t(s_bin);
   need -= s_above;
-  // collect the low 19 bits of the members of bin b1
+  // collect the low 19 bits of the members of bin b1 (in any order: only
+  // their histograms are used)
   for (int base = 0; base < L; base += kRound) {
-    uint32_t v[kPerThr];
-    load_round(sv, L, base, v);
+    const bool more = base + kRound < L;
+    if (more) load_round(sv, L, base + kRound, vn);
     const int j0 = base + threadIdx.x * kPerThr;
+    uint32_t mine = 0;
 #pragma unroll
-    for (int k = 0; k < kPerThr; ++k) {
-      const bool take = j0 + k < L && (v[k] >> 19) == b1;
-      const uint32_t slot = warp_append_slot(take, &s_cnt);
-      if (take && slot < kTieCap) tie_v[slot] = v[k] & 0x7FFFFu;
+    for (int k = 0; k < kPerThr; ++k) mine += (j0 + k < L && (v[k] >> 19) == b1) ? 1u : 0u;
+    uint32_t incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    uint32_t wbase = 0;
+    if (lane == 31 && incl) wbase = atomicAdd(&s_cnt, incl);
+    uint32_t slot = __shfl_sync(0xffffffffu, wbase, 31) + incl - mine;
+#pragma unroll
+    for (int k = 0; k < kPerThr; ++k)
+      if (j0 + k < L && (v[k] >> 19) == b1) {
+        if (slot < uint32_t(kTieCap)) tie_v[slot] = v[k] & 0x7FFFFu;
+        ++slot;
+      }
+    if (more) {
+#pragma unroll
+      for (int k = 0; k < kPerThr; ++k) v[k] = vn[k];
     }
   }
+  // the compaction's first round loads while digits 2 and 3 are resolved
+  load_round(sv, L, 0, v);
   __syncthreads();
   const uint32_t cnt = s_cnt;
   const bool in_smem = cnt <= uint32_t(kTieCap);
@@ -706,7 +718,7 @@ __global__ void __launch_bounds__(kSelThreads)
     }
   }
   __syncthreads();
-  find_bin_from_top<kSelThreads>(h, 2048, need, wt, &s_bin, &s_above);
+  find_bin_wide<kSelThreads>(h, 2048, need, wt, &s_wsel, &s_wbefore, &s_bin, &s_above);
   const uint32_t b2 = uint32_t(s_bin);
   need -= s_above;
   // digit 3: bits [7:0]
@@ -731,8 +743,8 @@ __global__ void __launch_bounds__(kSelThreads)
   // ordered compaction, one round of kRound positions at a time
   uint32_t gt_run = 0, eq_run = 0;
   for (int base = 0; base < L; base += kRound) {
-    uint32_t v[kPerThr];
-    load_round(sv, L, base, v);
+    const bool more = base + kRound < L;
+    if (more) load_round(sv, L, base + kRound, vn);
     const int j0 = base + threadIdx.x * kPerThr;
     uint32_t n_gt = 0, n_eq = 0;
 #pragma unroll
@@ -760,6 +772,10 @@ __global__ void __launch_bounds__(kSelThreads)
     }
     gt_run += gt_tot;
     eq_run += eq_tot;
+    if (more) {
+#pragma unroll
+      for (int k = 0; k < kPerThr; ++k) v[k] = vn[k];
+    }
   }
 }
 
@@ -857,67 +873,6 @@ constexpr int kTkThreads = 1024;
 constexpr int kTkShift = 17;
 constexpr int kTkBins = 1 << (31 - kTkShift);
 constexpr int kTkRankCap = 1024;  // members ranked in one shot
-
-// The bin holding the need-th largest element of a wide histogram h[0..nb)
-// (nb a multiple of 32 * 32; rank order counts from the top bin) and the
-// count strictly above it: every warp sums its nb/32 bins with lane-strided
-// (bank-conflict-free) reads, warp 0 scans the warp totals, and only the
-// warp holding the rank walks its bins in order.
-template <int NT>
-__device__ void find_bin_wide(const uint32_t* h, int nb, uint32_t need, uint32_t* warp_tot,
-                              int* s_warp, uint32_t* s_before, int* out_bin,
-                              uint32_t* out_above) {
-  constexpr int NW = NT / 32;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int per_w = nb / NW;  // rank-order bins of a warp
-  uint32_t sum = 0;
-  for (int k = lane; k < per_w; k += 32) sum += h[nb - 1 - (warp * per_w + k)];
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  if (lane == 0) warp_tot[warp] = sum;
-  __syncthreads();
-  if (warp == 0) {
-    const uint32_t t = lane < NW ? warp_tot[lane] : 0u;
-    uint32_t incl = t;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const uint32_t excl = incl - t;
-    if (lane < NW && excl < need && need <= incl) {
-      *s_warp = lane;
-      *s_before = excl;
-    }
-  }
-  __syncthreads();
-  const int W = *s_warp;
-  if (warp == W) {
-    const int per_l = per_w / 32;  // consecutive rank-order bins of a lane
-    const int rb0 = W * per_w + lane * per_l;
-    uint32_t local = 0;
-    for (int k = 0; k < per_l; ++k) local += h[nb - 1 - (rb0 + k)];
-    uint32_t incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    uint32_t acc = *s_before + incl - local;
-    if (acc < need && need <= acc + local) {
-      for (int k = 0; k < per_l; ++k) {
-        const uint32_t c = h[nb - 1 - (rb0 + k)];
-        if (acc + c >= need) {
-          *out_bin = nb - 1 - (rb0 + k);
-          *out_above = acc;
-          break;
-        }
-        acc += c;
-      }
-    }
-  }
-  __syncthreads();
-}
 
 template <int kPer>
 __global__ void __launch_bounds__(kTkThreads)
