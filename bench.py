@@ -869,14 +869,20 @@ def run_ours(args, rank, world, dist):
 def run_e2e(b, args, dist, graph: bool = True):
     """Every step: that step's inputs (the T steps' queries and block K/V)
     copied from pinned host memory to the device, the step through the
-    pipeline's public call (BlockPipeline.block with graph=True: the first
-    call per buffer set runs the C-ABI calls and captures them, later calls
-    replay that capture), and its result (the T attention outputs)
-    copied back to pinned host memory -- all inside the timed region.
-    Inputs and outputs travel on two copy streams of their own against two
-    alternating sets of device buffers, so step i+1's inputs arrive and
-    step i-1's outputs leave while step i computes (the double buffering a
-    serving loop would use)."""
+    pipeline's public call (BlockPipeline.block), and its result (the T
+    attention outputs) copied back to pinned host memory -- all inside the
+    timed region.  Inputs and outputs travel on two copy streams of their
+    own against two alternating sets of device buffers, so step i+1's inputs
+    arrive and step i-1's outputs leave while step i computes (the double
+    buffering a serving loop would use).
+
+    graph=True: each step is one CUDA graph, captured once per (cache copy,
+    buffer set) during the warm-up, holding the block's C-ABI calls
+    (BlockPipeline.block) and, on the copy streams forked from it and joined
+    back, the upload of the next step's inputs and the download of the
+    previous step's outputs; the last timed step's outputs are downloaded
+    inside the timed region as well.  graph=False: direct C-ABI calls every
+    step, the copies issued around them on the copy streams."""
     torch = b.torch
     w = b.w
     pin = lambda t: t.cpu().pin_memory()
@@ -896,10 +902,46 @@ def run_e2e(b, args, dist, graph: bool = True):
     for e in h2d_done + comp_done + out_done:
         e.record(comp)
 
-    # the pipeline's graph cache is keyed by buffers: one graph per (cache
-    # copy, input slot); with many rotated cache copies (tiny workloads) the
-    # direct calls are used instead
+    # one graph per (cache copy, input slot); with many rotated cache copies
+    # (tiny workloads) the direct calls are used instead
     use_graph = graph and b.n_rot <= 8
+    graphs = {}
+
+    def upload(x):
+        x["q_s"].copy_(hq_s, non_blocking=True)
+        x["bk"].copy_(hbk, non_blocking=True)
+        x["bv"].copy_(hbv, non_blocking=True)
+
+    def body(i):
+        """Step i on the current stream: the next step's inputs up and the
+        previous step's outputs down on the copy streams, beside the block."""
+        s, cur = i % 2, torch.cuda.current_stream()
+        cp.wait_stream(cur)
+        cpo.wait_stream(cur)
+        with torch.cuda.stream(cp):
+            upload(din[1 - s])
+        with torch.cuda.stream(cpo):
+            o_out.copy_(dout[1 - s], non_blocking=True)
+        x = din[s]
+        b.step(i % b.n_rot, q_steps=x["q_s"], bk=x["bk"], bv=x["bv"], out=dout[s])
+        cur.wait_stream(cp)
+        cur.wait_stream(cpo)
+
+    def one_graph(i):
+        b.before_step(i)
+        key = (i % b.n_rot, i % 2)
+        g = graphs.get(key)
+        if g is not None:
+            g.replay()
+            return
+        body(i)  # the first time: run directly, then capture the same work
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(comp)
+        with torch.cuda.graph(g, stream=cap):
+            body(i)
+        comp.wait_stream(cap)
+        graphs[key] = g
 
     def one(i):
         s = i % 2
@@ -925,15 +967,22 @@ def run_e2e(b, args, dist, graph: bool = True):
     # captured before the timed region
     n_warm = max(args.warmup, 2 * b.n_rot) if use_graph else args.warmup
     n_warm += n_warm % 2
+    step_fn = one_graph if use_graph else one
+    if use_graph:
+        upload(din[0])  # step 0's inputs; each step uploads the next one's
     for i in range(n_warm):
-        one(i)
+        step_fn(i)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(comp)
     for i in range(n_warm, n_warm + args.steps):
-        one(i)
+        step_fn(i)
+    if use_graph:  # the last step's outputs
+        cpo.wait_stream(comp)
+        with torch.cuda.stream(cpo):
+            o_out.copy_(dout[(n_warm + args.steps - 1) % 2], non_blocking=True)
     comp.wait_stream(cp)
     comp.wait_stream(cpo)
     e1.record(comp)
@@ -943,8 +992,10 @@ def run_e2e(b, args, dist, graph: bool = True):
     return {"value": job_value(ms, world, w.N * w.B), "unit": "tokens/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": ms,
-            "path": ("BlockPipeline.block(graph=True): C-ABI calls captured once per buffer "
-                     "set (during the warm-up), then replayed" if use_graph else
+            "path": ("one CUDA graph per step, captured once per (cache copy, buffer set) "
+                     "during the warm-up: BlockPipeline.block's C-ABI calls, with the next "
+                     "step's input upload and the previous step's output download on copy "
+                     "streams forked from it and joined back" if use_graph else
                      "direct C-ABI calls every step: one herald_block call per block for the "
                      "per-key selection (per-call for the other selections; argument checks, "
                      "tensor-map lookups and launches inside the timed region)")
