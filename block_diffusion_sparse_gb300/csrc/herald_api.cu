@@ -263,7 +263,8 @@ herald_status run_stage2(const herald_dims& dm, const uint16_t* q_block, const u
                          int C, int K, int sink, int local, int P_max, int32_t* idx,
                          int32_t* n_sel, void* ws, const WsLayout& w, cudaStream_t st,
                          const PoolGather* gather, const uint16_t* staged_k = nullptr,
-                         int32_t* slot_out = nullptr, const BudgetArgs* budget = nullptr) {
+                         int32_t* slot_out = nullptr, const BudgetArgs* budget = nullptr,
+                         bool cand_settled = false) {
   uint32_t* err = at<uint32_t>(ws, w.err);
   CUtensorMap qmap, qmap_all;
   const int G = dm.Hq / dm.Hkv;
@@ -283,8 +284,11 @@ herald_status run_stage2(const herald_dims& dm, const uint16_t* q_block, const u
                                   &qmap, &qmap_all, st),
                     "refine launch");
   } else if (is_device_memory(k_cache)) {
+    // cand_settled: the candidates and their cache rows were written before
+    // the launch preceding this call began (the refine reads them early)
     HERALD_TRY_CUDA(launch_refine(dm, k_cache, cand, n_cand, C, at<float2>(ws, w.rpart),
-                                  rlse, at<float>(ws, w.s2), w, err, &qmap, &qmap_all, st),
+                                  rlse, at<float>(ws, w.s2), w, err, &qmap, &qmap_all, st,
+                                  cand_settled),
                     "refine launch");
   } else {
     // a host-resident cache: the candidate K rows cross the host link once,
@@ -759,13 +763,13 @@ herald_status herald_select_stage2(herald_dims dims, const uint16_t* q_block,
 constexpr int kFusedGatherMinSegs = 16;
 constexpr int kFusedGatherMaxCopies = 4;
 
-herald_status herald_select_stage2_gather(herald_dims dims, const uint16_t* q_block,
-                                          const uint16_t* k_cache, const uint16_t* v_cache,
-                                          const int32_t* ctx_len, const int32_t* cand,
-                                          const int32_t* n_cand, int C, int K, int sink,
-                                          int local, int P_max, int32_t* idx, int32_t* n_sel,
-                                          uint16_t* pool_k, uint16_t* pool_v, void* ws,
-                                          size_t ws_bytes, void* stream) {
+static herald_status stage2_gather(herald_dims dims, const uint16_t* q_block,
+                                   const uint16_t* k_cache, const uint16_t* v_cache,
+                                   const int32_t* ctx_len, const int32_t* cand,
+                                   const int32_t* n_cand, int C, int K, int sink, int local,
+                                   int P_max, int32_t* idx, int32_t* n_sel, uint16_t* pool_k,
+                                   uint16_t* pool_v, void* ws, size_t ws_bytes, void* stream,
+                                   bool cand_settled) {
   g_err[0] = 0;
   HERALD_RET_IF(check_dims(dims));
   HERALD_RET_IF(check_c(C));
@@ -790,14 +794,26 @@ herald_status herald_select_stage2_gather(herald_dims dims, const uint16_t* q_bl
   if (segs >= kFusedGatherMinSegs && copies >= 2 && on_device) {
     const PoolGather pg{k_cache, v_cache, pool_k, pool_v, dims.d, copies};
     return run_stage2(dims, q_block, k_cache, ctx_len, cand, n_cand, C, K, sink, local, P_max,
-                      idx, n_sel, ws, w, st, &pg);
+                      idx, n_sel, ws, w, st, &pg, nullptr, nullptr, nullptr, cand_settled);
   }
   // a cache in host memory: the wide gather kernel keeps the host link busy
   HERALD_RET_IF(run_stage2(dims, q_block, k_cache, ctx_len, cand, n_cand, C, K, sink, local,
-                           P_max, idx, n_sel, ws, w, st, nullptr));
+                           P_max, idx, n_sel, ws, w, st, nullptr, nullptr, nullptr, nullptr,
+                           cand_settled));
   HERALD_TRY_CUDA(launch_gather(dims, idx, n_sel, P_max, k_cache, v_cache, pool_k, pool_v, st),
                   "gather launch");
   return HERALD_OK;
+}
+
+herald_status herald_select_stage2_gather(herald_dims dims, const uint16_t* q_block,
+                                          const uint16_t* k_cache, const uint16_t* v_cache,
+                                          const int32_t* ctx_len, const int32_t* cand,
+                                          const int32_t* n_cand, int C, int K, int sink,
+                                          int local, int P_max, int32_t* idx, int32_t* n_sel,
+                                          uint16_t* pool_k, uint16_t* pool_v, void* ws,
+                                          size_t ws_bytes, void* stream) {
+  return stage2_gather(dims, q_block, k_cache, v_cache, ctx_len, cand, n_cand, C, K, sink, local,
+                       P_max, idx, n_sel, pool_k, pool_v, ws, ws_bytes, stream, false);
 }
 
 // CTAs of the background candidate copy.  Each one holds an SM that an
@@ -1099,8 +1115,9 @@ herald_status herald_block(herald_dims dims, int C, int K, int sink, int local, 
                            unsigned flags, int scan_sms, const herald_block_bufs* bufs,
                            void* stream) {
   g_err[0] = 0;
-  if (flags & ~HERALD_BLOCK_ADVANCE)
-    return fail(HERALD_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags & ~HERALD_BLOCK_ADVANCE);
+  constexpr unsigned kBlockFlags = HERALD_BLOCK_ADVANCE | HERALD_BLOCK_CAND_SETTLED;
+  if (flags & ~kBlockFlags)
+    return fail(HERALD_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags & ~kBlockFlags);
   if (T < 1) return fail(HERALD_ERR_INVALID_ARG, "T=%d must be >= 1", T);
   if (i < 0) return fail(HERALD_ERR_INVALID_ARG, "i=%d must be >= 0", i);
   if (scan_sms < 0) return fail(HERALD_ERR_INVALID_ARG, "scan_sms=%d must be >= 0", scan_sms);
@@ -1146,10 +1163,10 @@ herald_status herald_block(herald_dims dims, int C, int K, int sink, int local, 
     HERALD_TRY_CUDA(cudaEventRecord(fork, den), "fork event record");
     HERALD_TRY_CUDA(cudaStreamWaitEvent(sel, fork, 0), "fork event wait");
   }
-  HERALD_RET_IF(herald_select_stage2_gather(
-      dims, q_steps, k_cache, v_cache, ctx_len, bufs->cand[cur], bufs->n_cand[cur], C, K, sink,
-      local, P_max, bufs->idx, bufs->n_sel, bufs->pool_k[cur], bufs->pool_v[cur], bufs->ws_den,
-      bufs->ws_bytes, den));
+  HERALD_RET_IF(stage2_gather(dims, q_steps, k_cache, v_cache, ctx_len, bufs->cand[cur],
+                              bufs->n_cand[cur], C, K, sink, local, P_max, bufs->idx, bufs->n_sel,
+                              bufs->pool_k[cur], bufs->pool_v[cur], bufs->ws_den, bufs->ws_bytes,
+                              den, (flags & HERALD_BLOCK_CAND_SETTLED) != 0));
   HERALD_RET_IF(herald_select_stage1(dims, q_steps, next_k_cache ? next_k_cache : k_cache,
                                      ctx_len, C, bufs->cand[nxt], bufs->n_cand[nxt], bufs->ws_sel,
                                      bufs->ws_bytes, overlap ? scan_sms : 0, sel));

@@ -192,11 +192,15 @@ cudaError_t launch_topc(const herald_dims& dm, const float* s1, const uint32_t* 
 // tokens (row tiles of whole tokens, MT_tok of them), qmap_all with a box
 // of all B tokens (the two-pass refine's second pass; may be null when
 // C <= 4096).  rlse: [N*Hkv][MT*128] floats for the two-pass refine.
+// early: the fused refine reads cand, n_cand and the candidate rows of
+// k_cache before its grid-dependency wait; only for inputs written before
+// the launch that precedes it on `st` began (ignored by the two-pass refine).
 bool refine_fused_ok(int C);
 cudaError_t launch_refine(const herald_dims& dm, const uint16_t* k_cache, const int32_t* cand,
                            const int32_t* n_cand, int C, float2* rpart,
                           float* rlse, float* s2, const WsLayout& w, uint32_t* err,
-                          const CUtensorMap* qmap, const CUtensorMap* qmap_all, cudaStream_t st);
+                          const CUtensorMap* qmap, const CUtensorMap* qmap_all, cudaStream_t st,
+                          bool early = false);
 // Host-side tensor map of a [tokens][heads][d] bf16 array, box 64 x
 // box_heads x box_tokens, 128-byte swizzle (cached per thread).
 herald_status encode_heads_map(const void* base, uint64_t tokens, int heads, int d,

@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(kFuseThreads, 1)
                         const uint16_t* __restrict__ kc, const int32_t* __restrict__ cand,
                         const int32_t* __restrict__ n_cand, int B, int Hq, int Hkv, int L_max,
                         int C, int bpt, int cpc, float scale, float* __restrict__ s2p,
-                        uint32_t* err) {
+                        uint32_t* err, int early) {
   using Cfg = FuseCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar0, barQ;
@@ -383,53 +383,66 @@ __global__ void __launch_bounds__(kFuseThreads, 1)
   const uint32_t tbase = tmem_base;
   const int b0 = mt * bpt;                  // first token of the tile
   const int rows_t = min(bpt, B - b0) * G;  // query rows of the tile
+  // The candidate positions, the zeroed query rows past the tile's and the
+  // copies of the candidate rows (cp.async, committed, awaited below).
+  // early != 0: the caller guarantees that cand, n_cand and the candidate
+  // rows of the cache were written before the launch preceding this one
+  // began (the candidates of a block whose stage 1 was joined before the
+  // previous block's last step), so they are read before the
+  // grid-dependency wait, which then covers only the queries.
+  const int c0 = int(rank) * cpc;
+  int ncv = 0;  // valid candidates of this CTA
+  auto stage_rows = [&]() {
+    // the candidate positions are read with n_cand, not after it: every slot
+    // below C lies inside the list, and rows past n_cand are masked below
+    const int32_t* cd = cand ? cand + size_t(seg) * C : nullptr;  // null: row = slot
+    int pr[kFuseMaxCpc / kFuseThreads];
+#pragma unroll
+    for (int k = 0; k < kFuseMaxCpc / kFuseThreads; ++k) {
+      const int r = threadIdx.x + k * kFuseThreads;
+      pr[k] = (cd && r < cpc && c0 + r < C) ? cd[c0 + r] : -1;
+    }
+    const int nc = min(max(n_cand[seg], 0), C);
+    ncv = min(max(nc - c0, 0), cpc);
+#pragma unroll
+    for (int k = 0; k < kFuseMaxCpc / kFuseThreads; ++k) {
+      const int r = threadIdx.x + k * kFuseThreads;
+      if (r < cpc) {
+        const int p = r < ncv ? (cand ? pr[k] : c0 + r) : -1;
+        debug_flag(r < ncv && (p < 0 || p >= L_max), DEV_BAD_INDEX);  // a candidate past the cache
+        pos[r] = (p >= 0 && p < L_max) ? p : -1;
+      }
+    }
+    __syncthreads();
+    // the tile's rows past its G*bpt query rows are never loaded (the query
+    // box fills rows [0, G*bpt)): zeroed, so that every score row is finite
+    // and the column sums below can weight rows with a product (rows past
+    // the tile's tokens get weight 0)
+    for (int u = G * bpt * 8 + threadIdx.x; u < kTileM * 8; u += kFuseThreads) {
+#pragma unroll
+      for (int hv = 0; hv < D / 64; ++hv)
+        *reinterpret_cast<uint4*>(Qs + hv * kTileM * 128 + u * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (ncv > 0) {
+      load_rows_sw128<D, kFuseThreads>(Ks, cpc, cpc, kc, [&](int r) -> const uint16_t* {
+        const int p = pos[r];
+        return p < 0 ? nullptr : kc + (size_t(seg) * L_max + p) * D;
+      });
+      cp_async_commit();
+    }
+  };
+  if (early) stage_rows();
   griddep_enter();
-  // the query tile first (it does not depend on n_cand); every CTA waits for
-  // it before exiting, used or not
+  // the query tile (it does not depend on n_cand); every CTA waits for it
+  // before exiting, used or not
   if (threadIdx.x == 0) {
     mbar_arrive_expect_tx(&barQ, uint32_t((D / 64) * G * bpt * 128));
 #pragma unroll
     for (int hv = 0; hv < D / 64; ++hv)
       tma_load_3d(Qs + hv * kTileM * 128, &qmap, &barQ, hv * 64, g * G, n * B + b0);
   }
-  // the candidate positions are read with n_cand, not after it: every slot
-  // below C lies inside the list, and rows past n_cand are masked below
-  const int c0 = int(rank) * cpc;
-  const int32_t* cd = cand ? cand + size_t(seg) * C : nullptr;  // null: row = slot
-  int pr[kFuseMaxCpc / kFuseThreads];
-#pragma unroll
-  for (int k = 0; k < kFuseMaxCpc / kFuseThreads; ++k) {
-    const int r = threadIdx.x + k * kFuseThreads;
-    pr[k] = (cd && r < cpc && c0 + r < C) ? cd[c0 + r] : -1;
-  }
-  const int nc = min(max(n_cand[seg], 0), C);
-  const int ncv = min(max(nc - c0, 0), cpc);  // valid candidates of this CTA
-#pragma unroll
-  for (int k = 0; k < kFuseMaxCpc / kFuseThreads; ++k) {
-    const int r = threadIdx.x + k * kFuseThreads;
-    if (r < cpc) {
-      const int p = r < ncv ? (cand ? pr[k] : c0 + r) : -1;
-      debug_flag(r < ncv && (p < 0 || p >= L_max), DEV_BAD_INDEX);  // a candidate past the cache
-      pos[r] = (p >= 0 && p < L_max) ? p : -1;
-    }
-  }
-  __syncthreads();
-  // the tile's rows past its G*bpt query rows are never loaded: zeroed, so
-  // that every score row is finite and the column sums below can weight
-  // rows with a product (rows past the tile's tokens get weight 0)
-  for (int u = G * bpt * 8 + threadIdx.x; u < kTileM * 8; u += kFuseThreads) {
-#pragma unroll
-    for (int hv = 0; hv < D / 64; ++hv)
-      *reinterpret_cast<uint4*>(Qs + hv * kTileM * 128 + u * 16) = make_uint4(0u, 0u, 0u, 0u);
-  }
-  if (ncv > 0) {
-    load_rows_sw128<D, kFuseThreads>(Ks, cpc, cpc, kc, [&](int r) -> const uint16_t* {
-      const int p = pos[r];
-      return p < 0 ? nullptr : kc + (size_t(seg) * L_max + p) * D;
-    });
-    cp_async_commit();
-    cp_async_wait_all();
-  }
+  if (!early) stage_rows();
+  if (ncv > 0) cp_async_wait_all();
   fence_proxy_async_smem();  // the zeroed rows and the copied K rows, for the UMMA
   __syncthreads();
   tc_fence_after();
@@ -642,7 +655,7 @@ template <int D, int CS>
 static cudaError_t launch_refine_cs(const herald_dims& dm, const uint16_t* k_cache,
                                     const int32_t* cand, const int32_t* n_cand, int C, float* s2,
                                     const WsLayout& w, uint32_t* err, const CUtensorMap& qmap,
-                                    cudaStream_t st) {
+                                    bool early, cudaStream_t st) {
   const int segs = dm.N * dm.Hkv;
   const int bpt = kTileM / (dm.Hq / dm.Hkv);
   const float scale = 1.0f / sqrtf(float(dm.d));
@@ -652,21 +665,21 @@ static cudaError_t launch_refine_cs(const herald_dims& dm, const uint16_t* k_cac
   return launch_cluster_threads("refine_fused_kernel", refine_fused_kernel<D, CS>,
                                 dim3(CS, w.MT_tok, segs), dim3(kFuseThreads), CS,
                                 FuseCfg<D>::kSmem, st, qmap, k_cache, cand, n_cand, dm.B, dm.Hq,
-                                dm.Hkv, dm.L_max, C, bpt, cpc, scale, s2, err);
+                                dm.Hkv, dm.L_max, C, bpt, cpc, scale, s2, err, early ? 1 : 0);
 }
 
 template <int D>
 static cudaError_t launch_refine_fused(const herald_dims& dm, const uint16_t* k_cache,
                                        const int32_t* cand, const int32_t* n_cand, int C,
                                        float* s2, const WsLayout& w, uint32_t* err,
-                                       const CUtensorMap& qmap, cudaStream_t st) {
+                                       const CUtensorMap& qmap, bool early, cudaStream_t st) {
   switch (refine_cluster_size<D>(w.MT_tok * dm.N * dm.Hkv, C)) {
     case 16:
-      return launch_refine_cs<D, 16>(dm, k_cache, cand, n_cand, C, s2, w, err, qmap, st);
+      return launch_refine_cs<D, 16>(dm, k_cache, cand, n_cand, C, s2, w, err, qmap, early, st);
     case 12:
-      return launch_refine_cs<D, 12>(dm, k_cache, cand, n_cand, C, s2, w, err, qmap, st);
+      return launch_refine_cs<D, 12>(dm, k_cache, cand, n_cand, C, s2, w, err, qmap, early, st);
     default:
-      return launch_refine_cs<D, 8>(dm, k_cache, cand, n_cand, C, s2, w, err, qmap, st);
+      return launch_refine_cs<D, 8>(dm, k_cache, cand, n_cand, C, s2, w, err, qmap, early, st);
   }
 }
 
@@ -697,14 +710,16 @@ static cudaError_t launch_refine_two_pass(const herald_dims& dm, const uint16_t*
 
 cudaError_t launch_refine(const herald_dims& dm, const uint16_t* k_cache, const int32_t* cand,
                           const int32_t* n_cand, int C, float2* rpart, float* rlse, float* s2, const WsLayout& w, uint32_t* err,
-                          const CUtensorMap* qmap, const CUtensorMap* qmap_all, cudaStream_t st) {
+                          const CUtensorMap* qmap, const CUtensorMap* qmap_all, cudaStream_t st,
+                          bool early) {
   const float scale = 1.0f / sqrtf(float(dm.d));
   if (refine_fused_ok(C)) {
     // s2 holds one partial per row tile of whole tokens: [MT_tok][N*Hkv][C]
     if (!qmap) return cudaErrorInvalidValue;
     if (dm.d == 128)
-      return launch_refine_fused<128>(dm, k_cache, cand, n_cand, C, s2, w, err, *qmap, st);
-    return launch_refine_fused<64>(dm, k_cache, cand, n_cand, C, s2, w, err, *qmap, st);
+      return launch_refine_fused<128>(dm, k_cache, cand, n_cand, C, s2, w, err, *qmap, early,
+                                      st);
+    return launch_refine_fused<64>(dm, k_cache, cand, n_cand, C, s2, w, err, *qmap, early, st);
   }
   if (!qmap || !qmap_all) return cudaErrorInvalidValue;
   const int bpt = kTileM / (dm.Hq / dm.Hkv);

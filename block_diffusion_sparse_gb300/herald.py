@@ -31,6 +31,7 @@ HERALD_ATTN_KERNEL_POOL_CS8, HERALD_ATTN_KERNEL_POOL_CS16, HERALD_ATTN_KERNEL_PO
 
 # flags of herald_block
 HERALD_BLOCK_ADVANCE = 1
+HERALD_BLOCK_CAND_SETTLED = 2
 
 
 def HERALD_ATTN_SMS(n: int) -> int:

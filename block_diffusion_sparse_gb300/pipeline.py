@@ -191,6 +191,10 @@ class BlockPipeline:
         # cache) issues each block as one herald_block call; False: the same
         # library calls one by one from here
         self.native = True
+        # True while the last work issued on the streams was a herald_block
+        # call: the next block's candidates come from its stage 1 (joined
+        # before its last step) and may be read early (HERALD_BLOCK_CAND_SETTLED)
+        self._cand_settled = False
         # the exact selection's own workspace (block_exact)
         self.ws_exact = None
         if exact:
@@ -241,6 +245,7 @@ class BlockPipeline:
     def prime(self, q_merge, k_cache, ctx, slot: int = 0, v_cache=None):
         """Stage 1 for the first block (no predecessor: its own queries);
         v_cache is needed with prefetch='kv'."""
+        self._cand_settled = False  # its last kernel writes the candidates
         self._stage1(q_merge, k_cache, ctx, slot, self._den(), v_cache=v_cache)
 
     def block(self, i: int, q_steps, block_k, block_v, k_cache, v_cache, ctx, out,
@@ -291,13 +296,17 @@ class BlockPipeline:
         hd = H.stream_handle(den)
         if self.native and not (self.Bk or self.prefetch or self.budget):
             H.step_bytes(q_steps), H.step_bytes(block_k), H.step_bytes(out)  # contiguous
+            flags = ((H.HERALD_BLOCK_ADVANCE if advance else 0)
+                     | (H.HERALD_BLOCK_CAND_SETTLED if self._cand_settled else 0))
+            self._cand_settled = False
             chk(L.herald_block(d, self.C, self.K, self.S, self.W, P, self.T, i, H.ptr(q_steps),
                                H.ptr(block_k), H.ptr(block_v), H.ptr(k_cache), H.ptr(v_cache),
-                               H.ptr(ctx), H.ptr(nk), H.ptr(out),
-                               H.HERALD_BLOCK_ADVANCE if advance else 0,
+                               H.ptr(ctx), H.ptr(nk), H.ptr(out), flags,
                                self._scan_sms(nk) if overlap else 0, self._bufs[bool(overlap)],
                                hd))
+            self._cand_settled = True
             return
+        self._cand_settled = False
         q0, qstep = H.ptr(q_steps), H.step_bytes(q_steps)
         bk0, bv0, bstep = H.ptr(block_k), H.ptr(block_v), H.step_bytes(block_k)
         o0, ostep = H.ptr(out), H.step_bytes(out)
@@ -353,6 +362,7 @@ class BlockPipeline:
         """Block i with the exact selection (every cached position scored
         with the block's real queries) in place of the two stages: nothing
         of it can run ahead of the block, so the step is one stream."""
+        self._cand_settled = False
         den = self._den()
         cur = i % 2
         d, P, L, chk = self.d, self.P, H.lib(), H.check

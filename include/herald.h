@@ -401,6 +401,16 @@ typedef struct {
 } herald_block_bufs;
 
 #define HERALD_BLOCK_ADVANCE 1u /* the last step advances ctx_len by B */
+/* The caller guarantees that cand[i%2], n_cand[i%2] and their rows of
+ * k_cache are not written by the launch that immediately precedes this call
+ * on `stream` (nor by anything not ordered before it): true when the
+ * previous call on these streams was herald_block for block i-1 (its stage
+ * 1, which wrote cand[i%2], is joined before its last step, and the
+ * candidates lie below the context that step appends to); false right after
+ * herald_select_stage1 wrote them on `stream`.  Stage 2's refine then reads
+ * them before its grid-dependency wait: every launch of the library lets its
+ * successor start only after its own wait, so they are final by then. */
+#define HERALD_BLOCK_CAND_SETTLED 2u
 
 /* One block of one layer through the dual-stream pipeline ([EA]:
  * selection and denoising run as a dual-stream pipeline over
@@ -420,6 +430,7 @@ typedef struct {
  *        step waits for sel (stage 1 scans the cache before the block is
  *        appended) and appends block_k[T-1], block_v[T-1] (HERALD_ATTN_APPEND,
  *        with HERALD_ATTN_ADVANCE if flags has HERALD_BLOCK_ADVANCE).
+ * flags: HERALD_BLOCK_ADVANCE, HERALD_BLOCK_CAND_SETTLED.
  * The same calls issued one by one give the same results.  Before the
  * first block, cand[0] must hold stage 1 of block 0 (herald_select_stage1
  * with its own queries).

@@ -143,7 +143,8 @@ def test_block_call_argument_errors():
         H.herald_block(d, 256, K, 16, 64, 208, T, i, q, ok, ok, ok, ok, ok, nk, ok, flags,
                        scan_sms, b)
 
-    cases = [(dict(flags=2), bufs(), 1), (dict(T=0), bufs(), 1), (dict(i=-1), bufs(), 1),
+    cases = [(dict(flags=4), bufs(), 1), (dict(flags=H.HERALD_BLOCK_CAND_SETTLED | 8), bufs(), 1),
+             (dict(T=0), bufs(), 1), (dict(i=-1), bufs(), 1),
              (dict(scan_sms=-1), bufs(ok), 1), (dict(), bufs(ok, (ok, None)), 1),
              (dict(), bufs(ok, (None, ok)), 1), (dict(K=300), bufs(), 1),
              (dict(q=ok + 4), bufs(), 1), (dict(nk=ok + 8), bufs(), 1),
